@@ -1,0 +1,10 @@
+"""fp64 CPU oracle of the deterministic MoE layer.
+
+TEST INFRASTRUCTURE ONLY: ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` are the only users.  The CUDA path never imports,
+links or calls anything here, and nothing here imports the CUDA package.
+"""
+from .moe_ref import (  # noqa: F401
+    NEAR_TIE, widen, silu, silu_grad, router_logits, route_ref, dispatch_ref,
+    expert_ffn, moe_forward_ref, moe_backward_ref,
+)

@@ -1,0 +1,263 @@
+"""fp64 CPU oracle of the deterministic MoE layer: routing, dispatch, experts,
+combine and the analytic backward.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import this module.  It shares no code with
+the CUDA path and never calls it.
+
+Sources (page title, section):
+  [gtnt]     "MoK揭秘：NVL72上大规模MoE训练工程方案深度解读" (gtnt.cn), §1.1:
+             a gating network (router) picks the best few experts per token.
+  [dothoosh] "Cursor Mixture-of-Kittens cuts MoE training latency by 5.8x"
+             (dothoosh.com), section "MoK technical details":
+             bullet "Hybrid communication": forward = dispatch, expert
+             compute, combine; backward = reverse-combine then reverse-dispatch;
+             bullet "Ring buffer logic": dropless (no token is dropped);
+             bullet "Precision and scheduling": SwiGLU experts, BF16/MXFP8,
+             router-weight gradients taken inside the SwiGLU backward.
+
+Every float computation here runs in float64 on the bf16 inputs widened
+exactly.  The one decision taken in float32 is the top-k selection, because the
+CUDA router takes it on float32 logits (the layer's stated logit precision);
+tokens whose float64 k-th/(k+1)-th logit gap is below 1e-5 are flagged so a
+comparison can leave them out.
+
+Readings where the pages say nothing (all are listed again in the design notes):
+  * routing weights are a softmax over the k chosen logits (equal to the full
+    softmax restricted to the chosen set and renormalised, so they sum to 1);
+  * ties in float32 go to the lower expert index; slots are in descending
+    logit order;
+  * SwiGLU is silu(gate) * up with silu(z) = z*sigmoid(z), gate rows first in
+    the stacked [2I, d] weight;
+  * rows of one expert are ordered by token id (a stable counting sort);
+  * the loss used for the backward is L = sum(y * dy).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+NEAR_TIE = 1e-5
+
+
+# ----------------------------------------------------------------------------
+# storage helpers (own copy: the oracle does not import the CUDA package)
+# ----------------------------------------------------------------------------
+
+def widen(a) -> np.ndarray:
+    """bf16 bit pattern (uint16) or float array -> float64."""
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def _sigmoid(z):
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def silu(z):
+    return z * _sigmoid(z)
+
+
+def silu_grad(z):
+    s = _sigmoid(z)
+    return s * (1.0 + z * (1.0 - s))
+
+
+# ----------------------------------------------------------------------------
+# routing  [gtnt] §1.1; reading: softmax over the chosen k, fixed tie rule
+# ----------------------------------------------------------------------------
+
+def router_logits(x, w_router, bias=None) -> np.ndarray:
+    """l = x W_r^T (+ b), float64 [T, E]."""
+    l = widen(x) @ widen(w_router).T
+    if bias is not None:
+        l = l + np.asarray(bias, dtype=np.float32).astype(np.float64)[None, :]
+    return l
+
+
+def route_ref(x, w_router, bias, k: int):
+    """Top-k routing.
+
+    Returns (topk_idx [T,k] int32, topk_w [T,k] float64, logits [T,E] float64,
+    flagged [T] bool, inner_tie [T] bool).
+
+    Selection: the k largest float32-rounded logits; equal values go to the
+    lower expert index; slots are ordered by descending logit.
+    Weights: p_s = exp(l_s - m) / sum_{j in S} exp(l_j - m), m = max over S.
+    ``flagged``: the float64 gap between the k-th and (k+1)-th largest logit is
+    below 1e-5, so the chosen set itself is not decidable at the kernel's
+    precision.  ``inner_tie``: two adjacent chosen logits are within 1e-5, so
+    only the chosen set (not the slot order) is decidable.
+    """
+    logits = router_logits(x, w_router, bias)
+    T, E = logits.shape
+    l32 = logits.astype(np.float32)
+    # order experts by (-l32, index): lexsort keys are applied last-key-primary
+    cols = np.broadcast_to(np.arange(E), (T, E))
+    order = np.lexsort((cols, -l32), axis=-1)
+    idx = order[:, :k].astype(np.int32)
+    sel = np.take_along_axis(logits, idx.astype(np.int64), axis=1)
+    m = sel.max(axis=1, keepdims=True)
+    ex = np.exp(sel - m)
+    w = ex / ex.sum(axis=1, keepdims=True)
+    ranked = np.take_along_axis(logits, order, axis=1)
+    if k < E:
+        flagged = (ranked[:, k - 1] - ranked[:, k]) < NEAR_TIE
+    else:
+        flagged = np.zeros(T, dtype=bool)
+    if k > 1:
+        inner_tie = (np.abs(np.diff(sel, axis=1)) < NEAR_TIE).any(axis=1)
+    else:
+        inner_tie = np.zeros(T, dtype=bool)
+    return idx, w, logits, flagged, inner_tie
+
+
+# ----------------------------------------------------------------------------
+# dispatch  [dothoosh] "Hybrid communication" + "Ring buffer logic" (dropless)
+# ----------------------------------------------------------------------------
+
+def dispatch_ref(topk_idx, E: int):
+    """Stable counting sort of the T*k (token, slot) pairs by expert.
+
+    counts[e]  = #{(t,s): idx[t,s] = e}
+    offsets    = exclusive prefix sum of counts, length E+1
+    pos[t,s]   = offsets[e] + #{t' < t routed to e}   (ties by token id)
+    token_of_row[pos[t,s]] = t
+    """
+    idx = np.asarray(topk_idx, dtype=np.int64)
+    T, k = idx.shape
+    counts = np.bincount(idx.ravel(), minlength=E).astype(np.int64)
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    np.cumsum(counts, out=offsets[1:])
+    # flat position f = t*k + s is token-major, so a stable sort by expert
+    # keeps token order inside each expert
+    order = np.argsort(idx.ravel(), kind="stable")
+    pos = np.empty(T * k, dtype=np.int64)
+    pos[order] = np.arange(T * k)
+    token_of_row = order // k
+    return (counts.astype(np.int32), offsets.astype(np.int32),
+            pos.reshape(T, k).astype(np.int32), token_of_row.astype(np.int32))
+
+
+# ----------------------------------------------------------------------------
+# forward  ([dothoosh] "Hybrid communication", "Precision and scheduling")
+# ----------------------------------------------------------------------------
+
+def expert_ffn(X, w_gate_up_e, w_down_e):
+    """SwiGLU FFN of one expert on rows X (float64).  Returns (G, U, H, O)."""
+    Wgu = widen(w_gate_up_e)
+    I = Wgu.shape[0] // 2
+    G = X @ Wgu[:I].T
+    U = X @ Wgu[I:].T
+    H = silu(G) * U
+    O = H @ widen(w_down_e).T
+    return G, U, H, O
+
+
+def moe_forward_ref(x, w_router, bias, w_gate_up, w_down, k: int, routing=None,
+                    keep=False):
+    """y_t = sum_s p[t,s] * FFN_{e[t,s]}(x_t), summed in slot order.
+
+    ``routing`` = (topk_idx, topk_w) forces the routing (e.g. to check the
+    later stages on exactly the kernel's selection); otherwise route_ref runs.
+    Returns y [T,d] float64, and with keep=True also a dict of intermediates.
+    """
+    X = widen(x)
+    T, d = X.shape
+    E = np.asarray(w_gate_up).shape[0]
+    if routing is None:
+        idx, p, _, _, _ = route_ref(x, w_router, bias, k)
+    else:
+        idx = np.asarray(routing[0], dtype=np.int32)
+        p = np.asarray(routing[1], dtype=np.float64)
+    counts, offsets, pos, tok = dispatch_ref(idx, E)
+    R = T * k
+    I = np.asarray(w_gate_up).shape[1] // 2
+    O = np.zeros((R, d))
+    G = np.zeros((R, I)); U = np.zeros((R, I)); H = np.zeros((R, I))
+    for e in range(E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if a == b:
+            continue
+        G[a:b], U[a:b], H[a:b], O[a:b] = expert_ffn(X[tok[a:b]], w_gate_up[e], w_down[e])
+    y = np.zeros((T, d))
+    for s in range(k):
+        y += p[:, s:s + 1] * O[pos[:, s]]
+    if not keep:
+        return y
+    return y, dict(idx=idx, p=p, counts=counts, offsets=offsets, pos=pos,
+                   token_of_row=tok, G=G, U=U, H=H, O=O)
+
+
+# ----------------------------------------------------------------------------
+# backward of L = sum(y * dy)
+# ([dothoosh] "Hybrid communication": reverse-combine then reverse-dispatch;
+#  "Precision and scheduling": router-weight gradient from the SwiGLU backward)
+# ----------------------------------------------------------------------------
+
+def moe_backward_ref(x, w_router, bias, w_gate_up, w_down, k: int, dy,
+                     routing=None, fwd=None):
+    """Analytic gradients of L = sum(y*dy).
+
+    Returns dict with dx [T,d], dw_router [E,d], dw_gate_up [E,2I,d],
+    dw_down [E,d,I] (all float64) and dp [T,k] (dL/dp).
+    The routing (the chosen set S_t) is piecewise constant, so only p carries
+    a gradient into the router logits:
+      dp[t,s]   = <dy_t, O[pos[t,s]]>
+      dl[t,j]   = p_j (dp_j - sum_i p_i dp_i) for j in S_t, 0 elsewhere
+      dx       += dl W_r,   dW_r = dl^T x.
+    """
+    X = widen(x)
+    dY = widen(dy)
+    T, d = X.shape
+    E = np.asarray(w_gate_up).shape[0]
+    I = np.asarray(w_gate_up).shape[1] // 2
+    if fwd is None:
+        _, fwd = moe_forward_ref(x, w_router, bias, w_gate_up, w_down, k,
+                                 routing=routing, keep=True)
+    idx, p, offsets, pos, tok = fwd["idx"], fwd["p"], fwd["offsets"], fwd["pos"], fwd["token_of_row"]
+    G, U, H, O = fwd["G"], fwd["U"], fwd["H"], fwd["O"]
+    R = T * k
+
+    # reverse-combine: per routed row, the upstream gradient scaled by p
+    row_t = tok
+    row_p = np.empty(R)
+    for s in range(k):
+        row_p[pos[:, s]] = p[:, s]
+    dO = row_p[:, None] * dY[row_t]
+    dp = np.einsum("tsd,td->ts", O[pos], dY)
+
+    dX_rows = np.zeros((R, d))
+    dw_gate_up = np.zeros((E, 2 * I, d))
+    dw_down = np.zeros((E, d, I))
+    for e in range(E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if a == b:
+            continue
+        Wd = widen(w_down[e])
+        Wgu = widen(w_gate_up[e])
+        dH = dO[a:b] @ Wd                       # [rows, I]
+        dw_down[e] = dO[a:b].T @ H[a:b]         # [d, I]
+        dG = dH * U[a:b] * silu_grad(G[a:b])
+        dU = dH * silu(G[a:b])
+        Xe = X[tok[a:b]]
+        dX_rows[a:b] = dG @ Wgu[:I] + dU @ Wgu[I:]
+        dw_gate_up[e, :I] = dG.T @ Xe
+        dw_gate_up[e, I:] = dU.T @ Xe
+
+    # reverse-dispatch: sum each token's k rows in slot order
+    dx = np.zeros((T, d))
+    for s in range(k):
+        dx += dX_rows[pos[:, s]]
+
+    # router: softmax over the chosen set
+    c = (p * dp).sum(axis=1, keepdims=True)
+    dl_sel = p * (dp - c)
+    dl = np.zeros((T, E))
+    np.put_along_axis(dl, idx.astype(np.int64), dl_sel, axis=1)
+    Wr = widen(w_router)
+    dx += dl @ Wr
+    dw_router = dl.T @ X
+    return dict(dx=dx, dw_router=dw_router, dw_gate_up=dw_gate_up,
+                dw_down=dw_down, dp=dp, dl=dl_sel)
