@@ -1,0 +1,397 @@
+#!/usr/bin/env python
+"""Throughput of one deterministic MoE layer, forward + backward, on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mok|reference]
+
+A step is one forward + backward of the layer (router, dispatch, grouped
+SwiGLU GEMMs, combine, and the mirrored backward) over one batch of the
+fine-grained workload: T=4096 tokens, d=2048, E=64 experts, I=1024, top-8,
+bf16, seeded synthetic inputs.  The weights (0.8 GB) and activations read per
+step are larger than the 129 MB L2, so no flush is needed between steps.
+
+Printed (rank 0, one JSON line): tokens/s over all ranks, per-kernel times
+from CUDA events recorded around each kernel inside the timed region, the
+dominant kernel's roofline, the end-to-end number through the C ABI with
+pinned-host inputs and outputs, the fp64 oracle's CPU throughput on a small
+sample, and the SM clocks sampled during the timed region.
+
+With N > 1 (torchrun) every rank runs its own replica of the layer on its own
+GPU: the layer has no cross-GPU exchange on one node, so scaling is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from routing_dispatch_grouped_router_gb300 import inputs as gen  # noqa: E402
+
+METRIC = "MoE layer fwd+bwd tokens/s on 1 GB300; grouped-GEMM % of tensor-core peak"
+WORKLOAD = "fine"
+
+# Algorithmic work per launch of each kernel (R = T*k routed rows).
+#   GEMMs: 2*M*N*K flops with M summed over the experts' real rows.
+#   Row movers: bytes that must cross HBM once.
+
+
+def gemm_flops(shape: gen.Shape) -> dict:
+    R, d, I, T, E = shape.R, shape.d, shape.I, shape.T, shape.E
+    return {
+        "router_logits": 2.0 * T * d * E,
+        "fwd_gate_up_swiglu": 2.0 * R * d * 2 * I,
+        "fwd_down": 2.0 * R * I * d,
+        "bwd_down_dgrad_swiglu": 2.0 * R * d * I,
+        "bwd_down_wgrad": 2.0 * R * d * I,
+        "bwd_gate_up_dgrad": 2.0 * R * 2 * I * d,
+        "bwd_gate_up_wgrad": 2.0 * R * 2 * I * d,
+    }
+
+
+def mover_bytes(shape: gen.Shape) -> dict:
+    R, d, T, k = shape.R, shape.d, shape.T, shape.k
+    row = 2 * d
+    return {
+        # read each token row once per routed copy, write R rows (+ indices)
+        "gather_rows": R * row + R * row + R * 4,
+        # read k expert rows + weights per token, write the token row
+        "combine": R * row + T * row + R * 8,
+        # read k dX rows and k router rows (router rows come from L2), write dx
+        "reverse_dispatch": R * row + T * row + R * 12,
+    }
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return dict(hbm=j.get("hbm_gbs", 6800.0), bf16=j.get("bf16_tflops", 1900.0),
+                    bf16_sustained=j.get("bf16_tflops_sustained", 1700.0), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------ clocks --
+
+CLOCK_FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, bus_id: str | None):
+        self.bus_id = (bus_id or "").lower()
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + CLOCK_FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append(parts)
+        bus = {r[1].lower() for r in rows}
+        if self.bus_id and any(self.bus_id[-12:] in b for b in bus):
+            rows = [r for r in rows if self.bus_id[-12:] in r[1].lower()]
+        elif len(bus) > 1:
+            rows = [r for r in rows if r[0] == rows[0][0]]
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for i, n in enumerate(names):
+                if r[6 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------- CPU (oracle) side --
+
+def oracle_sample(inp: dict, shape: gen.Shape, tokens: np.ndarray):
+    """fp64 oracle forward + backward on a slice of the workload's tokens
+    (every token is independent in the layer; the expert gradients of the
+    experts the slice touches are complete for that slice)."""
+    import oracle
+    xs = inp["x"][tokens]
+    dys = inp["dy"][tokens]
+    _, fwd = oracle.moe_forward_ref(xs, inp["w_router"], inp["bias"], inp["w_gate_up"],
+                                    inp["w_down"], shape.k, keep=True)
+    experts = np.unique(fwd["idx"])
+    oracle.moe_backward_ref(xs, inp["w_router"], inp["bias"], inp["w_gate_up"], inp["w_down"],
+                            shape.k, dys, fwd=fwd, grad_experts=experts)
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(inp: dict, shape: gen.Shape, budget_s: float = 12.0, tokens_per_sample: int = 32):
+    t0 = time.perf_counter()
+    done = 0
+    n = 0
+    while True:
+        tok = (np.arange(tokens_per_sample) + n * tokens_per_sample) % shape.T
+        oracle_sample(inp, shape, tok)
+        done += tokens_per_sample
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{n} x {tokens_per_sample}-token slices of the {WORKLOAD} workload, fp64 "
+                      f"numpy oracle forward+backward (all routing, dispatch, expert FFNs and "
+                      f"gradients of the touched experts), {dt:.1f} s"}
+
+
+def run_reference(args, shape: gen.Shape, rank: int):
+    if rank != 0:
+        return
+    inp = gen.make_inputs(shape, seed=0)
+    tok_per_step = 1
+    for i in range(args.warmup):
+        oracle_sample(inp, shape, np.array([i % shape.T]))
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_sample(inp, shape, np.array([(args.warmup + i) % shape.T]))
+    dt = time.perf_counter() - t0
+    value = tok_per_step * args.steps / dt
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": workload_config(shape),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"one token of the {WORKLOAD} workload per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(shape: gen.Shape) -> dict:
+    return {"workload": f"{WORKLOAD}: T={shape.T} d={shape.d} E={shape.E} I={shape.I} "
+                        f"top-{shape.k} bf16 forward+backward",
+            "T": shape.T, "d": shape.d, "E": shape.E, "I": shape.I, "k": shape.k,
+            "l2": "inputs larger than L2 (0.8 GB of expert weights read per step), no flush",
+            "parallelism": "replicas (one independent layer per GPU)"}
+
+
+# --------------------------------------------------------------- GPU side --
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="mok", choices=["mok", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    shape = gen.workload_shape(WORKLOAD)
+
+    if args.impl == "reference":
+        run_reference(args, shape, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    from routing_dispatch_grouped_router_gb300 import api, build
+    build.build()
+
+    inp = gen.make_inputs(shape, seed=0)
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+    x, wr, wgu, wd, dy = (dev(inp[n]) for n in ("x", "w_router", "w_gate_up", "w_down", "dy"))
+    layer = api.MoELayer(shape.T, shape.d, shape.E, shape.I, shape.k)
+    y = torch.empty_like(x)
+    dx = torch.empty_like(x)
+    dwr, dwgu, dwd = torch.empty_like(wr), torch.empty_like(wgu), torch.empty_like(wd)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        layer.forward(x, wr, None, wgu, wd, y=y)
+        layer.backward(dy, x, wr, None, wgu, wd, dx=dx, dw_router=dwr, dw_gate_up=dwgu,
+                       dw_down=dwd)
+
+    for _ in range(args.warmup):
+        step()
+    status = layer.status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+    launches_per_step = api.last_launch_count()
+
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(local).pci_bus_id
+    except Exception:
+        bus = None
+    sampler = ClockSampler(str(bus) if bus is not None else None)
+
+    # ---- timed region: K steps, per-kernel events recorded on the stream
+    api.profile_reset()
+    api.profile_enable(True)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    api.profile_enable(False)
+    elapsed_ms = ev0.elapsed_time(ev1)
+    kernels = api.profile_collect()
+    if layer.status() != 0:
+        raise RuntimeError("device status set during the timed region")
+    t_max = elapsed_ms
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_max = float(t.item())
+    value = world * shape.T * args.steps / (t_max / 1e3)
+
+    # ---- per-kernel summary and the dominant kernel's roofline
+    peaks = load_peaks()
+    flops = gemm_flops(shape)
+    movers = mover_bytes(shape)
+    total_k = sum(v[1] for v in kernels.values())
+    ksum = {}
+    for name, (n, ms) in kernels.items():
+        ksum[name] = {"launches": n, "avg_us": 1e3 * ms / n, "share": ms / total_k}
+    dom = max(kernels, key=lambda n: kernels[n][1])
+    n_dom, ms_dom = kernels[dom]
+    avg_s = ms_dom / n_dom / 1e3
+    if dom in flops:
+        ach = flops[dom] / avg_s / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peaks["bf16_sustained"],
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_sustained"], "traffic": None,
+                "peak_source": f"bf16_tflops_sustained of {peaks['source']}",
+                "algorithmic_per_launch": flops[dom]}
+    else:
+        ach = movers.get(dom, 0) / avg_s / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peaks["hbm"],
+                "unit": "GB/s", "frac": ach / peaks["hbm"], "traffic": None,
+                "peak_source": f"hbm_gbs of {peaks['source']}",
+                "algorithmic_per_launch": movers.get(dom, 0)}
+    gemm_ms = sum(kernels[n][1] for n in flops if n in kernels)
+    gemm_fl = sum(flops[n] * kernels[n][0] for n in flops if n in kernels)
+    gg = [n for n in flops if n != "router_logits" and n in kernels]
+    gg_ms = sum(kernels[n][1] for n in gg)
+    gg_fl = sum(flops[n] * kernels[n][0] for n in gg)
+    gg_tflops = gg_fl / (gg_ms / 1e3) / 1e12 if gg_ms else 0.0
+    movers_perf = {}
+    for n, b in movers.items():
+        if n in kernels:
+            gbs = b / (kernels[n][1] / kernels[n][0] / 1e3) / 1e9
+            movers_perf[n] = {"GB/s": gbs, "frac_hbm": gbs / peaks["hbm"]}
+
+    # ---- end to end through the C ABI: pinned host in, pinned host out
+    xh = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    dyh = torch.from_numpy(inp["dy"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    dxh = torch.empty_like(xh).pin_memory()
+    xd, dyd = torch.empty_like(x), torch.empty_like(dy)
+
+    def e2e_step():
+        xd.copy_(xh, non_blocking=True)
+        dyd.copy_(dyh, non_blocking=True)
+        layer.forward(xd, wr, None, wgu, wd, y=y)
+        layer.backward(dyd, xd, wr, None, wgu, wd, dx=dx, dw_router=dwr, dw_gate_up=dwgu,
+                       dw_down=dwd)
+        yh.copy_(y, non_blocking=True)
+        dxh.copy_(dx, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": world * shape.T * args.e2e_steps / (e2e_ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": 2 * xh.numel() * 2, "d2h_bytes_per_step": 2 * yh.numel() * 2,
+           "steps": args.e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp, shape)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": workload_config(shape),
+            "grouped_gemm_tflops": gg_tflops,
+            "grouped_gemm_frac_of_peak": gg_tflops / peaks["bf16_sustained"],
+            "all_gemm_tflops": gemm_fl / (gemm_ms / 1e3) / 1e12 if gemm_ms else 0.0,
+            "roofline": roof, "movers": movers_perf, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps, "launches_per_step": launches_per_step,
+            "clocks": clocks, "kernels": ksum,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,206 @@
+/*
+ * mok.h - C ABI of a deterministic Mixture-of-Experts training layer for one
+ * GB300 GPU (sm_103a): top-k router, dispatch into expert-contiguous order,
+ * grouped SwiGLU expert GEMMs, weighted combine, and the backward mirror
+ * (reverse-combine, grouped dgrad/wgrad GEMMs, reverse-dispatch, router grad).
+ *
+ * Sources (page title, section):
+ *   [gtnt]     "MoK揭秘：NVL72上大规模MoE训练工程方案深度解读" (gtnt.cn)
+ *   [aikraft]  "Cursor MoK: revolution in MoE model training on NVL72"
+ *              (aikraft.ru), sections 01-04
+ *   [dothoosh] "Cursor Mixture-of-Kittens cuts MoE training latency by 5.8x"
+ *              (dothoosh.com), section "MoK technical details" with bullets
+ *              "Hybrid communication", "Overlap granularity",
+ *              "Ring buffer logic", "Precision and scheduling"
+ *
+ * Conventions for every entry point
+ *   - Pointers named as device buffers are device pointers on the current CUDA
+ *     device; the caller allocates and owns every buffer.  The library never
+ *     allocates, frees or copies device->host, and never synchronises the
+ *     stream (mok_get_device_status is the one exception).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *     All work is enqueued on it in order.
+ *   - bf16 tensors are row-major, contiguous, 16-byte aligned.  Every weight
+ *     is stored [out, in] (nn.Linear style), so the reduction dimension is
+ *     the contiguous one.
+ *   - Arguments are validated before anything is enqueued; on an error
+ *     return nothing was enqueued.
+ *   - Results are bitwise identical from call to call for the same inputs,
+ *     descriptor and device (no floating-point atomics anywhere).
+ *
+ * Shape requirements (MOK_ERR_UNSUPPORTED otherwise)
+ *   1 <= k <= min(E, 8);  1 <= E <= 512;  0 <= T;  T*k < 2^31;
+ *   d and I multiples of 128 (the GEMM tile width), d <= 16384, I <= 16384;
+ *   dtype MOK_BF16 (MOK_MXFP8 is declared, not yet served).
+ */
+#ifndef MOK_H_
+#define MOK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mok_status {
+  MOK_OK = 0,
+  MOK_ERR_INVALID_ARG = 1,      /* null pointer, misaligned pointer, bad size */
+  MOK_ERR_UNSUPPORTED = 2,      /* shape/dtype outside the requirements above */
+  MOK_ERR_WORKSPACE = 3,        /* a buffer is smaller than the size query says */
+  MOK_ERR_CUDA = 4,             /* a CUDA runtime call failed */
+  MOK_ERR_NO_DEVICE = 5,        /* the current device is not sm_103 */
+  /* codes written on the device, read back with mok_get_device_status */
+  MOK_ERR_DEVICE_NONFINITE = 16, /* a router logit was NaN; it was treated as -inf */
+  MOK_ERR_DEVICE_INDEX = 17,     /* an expert index outside [0, E) was met and skipped */
+  MOK_ERR_DEVICE_TIMEOUT = 18    /* a bounded wait inside a GEMM gave up; results invalid */
+} mok_status;
+
+typedef enum mok_dtype {
+  MOK_BF16 = 0,  /* bf16 operands, fp32 accumulation, bf16 I/O */
+  MOK_MXFP8 = 1  /* E4M3 operands with 32-element E8M0 block scales (reserved) */
+} mok_dtype;
+
+/* Layer shape.  T tokens of width d, E experts with FFN width I, top-k. */
+typedef struct mok_moe_desc {
+  int64_t T, d, E, I;
+  int32_t k;
+  int32_t dtype;       /* mok_dtype */
+  int32_t mb_tokens;   /* 0 = whole batch at once (micro-batching reserved) */
+  int32_t ring_slots;  /* reserved, 0 */
+  uint32_t flags;      /* reserved, 0 */
+  uint32_t reserved;
+} mok_moe_desc;
+
+/* Byte offsets, inside the `saved` buffer, of the forward results that the
+ * backward consumes.  Row-indexed arrays use the padded row space: expert e
+ * owns rows [padded_offsets[e], padded_offsets[e+1]), each segment a multiple
+ * of 128 rows, its first counts[e] rows real and the rest zero. */
+typedef struct mok_saved_layout {
+  size_t status;          /* int32 device status word */
+  size_t topk_idx;        /* int32 [T,k] expert of each slot, descending logit */
+  size_t topk_w;          /* fp32 [T,k] routing weight of each slot */
+  size_t counts;          /* int32 [E] rows routed to each expert */
+  size_t offsets;         /* int32 [E+1] exclusive prefix sum of counts */
+  size_t pos;             /* int32 [T,k] row of (t,s) in expert order */
+  size_t token_of_row;    /* int32 [T*k] inverse of pos */
+  size_t padded_offsets;  /* int32 [E+1] */
+  size_t padded_pos;      /* int32 [T,k] row of (t,s) in the padded row space */
+  size_t padded_token;    /* int32 [rows_max] token of each padded row, -1 for padding */
+  size_t row_weight;      /* fp32 [rows_max] routing weight of each padded row, 0 for padding */
+  size_t x_perm;          /* bf16 [rows_max, d] dispatched token rows */
+  size_t gate_up;         /* bf16 [rows_max, 2I] pre-activation gate (cols 0..I-1) and up (I..2I-1) */
+  size_t rows_max;        /* number of padded rows the buffers hold: T*k + 127*min(E, T*k), rounded to 128 */
+  size_t total;           /* size of `saved` in bytes */
+} mok_saved_layout;
+
+/* Sizes of the three caller-provided buffers for a layer of shape `desc`.
+ *   fwd_ws_bytes : scratch of mok_moe_forward (free after it returns on the stream)
+ *   saved_bytes  : forward results kept for mok_moe_backward
+ *   bwd_ws_bytes : scratch of mok_moe_backward
+ * Any output pointer may be NULL.  No device work. */
+mok_status mok_moe_workspace_size(const mok_moe_desc* desc, size_t* fwd_ws_bytes,
+                                  size_t* saved_bytes, size_t* bwd_ws_bytes);
+
+/* Offsets of the forward results inside `saved` (see mok_saved_layout). */
+mok_status mok_moe_saved_layout(const mok_moe_desc* desc, mok_saved_layout* out);
+
+/* Forward of the layer ([dothoosh] "Hybrid communication": dispatch, expert
+ * compute, combine; [gtnt] §1.1 router; [dothoosh] "Precision and scheduling":
+ * SwiGLU experts):
+ *   l = x W_r^T (+ b)                      fp32 logits
+ *   S_t = top-k of l_t, larger first, exact ties to the lower expert index
+ *   p_{t,s} = softmax over the k chosen logits (sums to 1)
+ *   rows of expert e = tokens routed to e in ascending token order (dropless)
+ *   [g | u] = X_e W_gu_e^T,  h = silu(g) * u,  O = h W_down_e^T
+ *   y_t = sum_{s=0..k-1} p_{t,s} O[pos[t,s]]   (fp32 sum in slot order)
+ * x [T,d] bf16; w_router [E,d] bf16; router_bias [E] fp32 or NULL;
+ * w_gate_up [E,2I,d] bf16 (gate rows 0..I-1, up rows I..2I-1);
+ * w_down [E,d,I] bf16; y [T,d] bf16 (output).
+ * saved: >= saved_bytes, filled for the backward; its status word is reset.
+ * workspace: >= fwd_ws_bytes.  Buffers must not overlap. */
+mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* w_router,
+                           const float* router_bias, const void* w_gate_up, const void* w_down,
+                           void* y, void* saved, size_t saved_bytes, void* workspace,
+                           size_t ws_bytes, void* stream);
+
+/* Backward of L = sum(y * dy) given the `saved` of the matching forward
+ * ([dothoosh] "Hybrid communication": reverse-combine, then reverse-dispatch;
+ * "Precision and scheduling": router-weight gradient inside the SwiGLU
+ * backward, dp = <dy W_down, h>):
+ *   dx [T,d], dw_router [E,d], dw_gate_up [E,2I,d], dw_down [E,d,I]: bf16
+ *   outputs, overwritten (fp32 accumulation inside, one writer per element,
+ *   fixed summation order).  The routing set is piecewise constant, so the
+ *   router receives gradient only through p.  The bias gets no gradient.
+ * x, w_router, router_bias, w_gate_up, w_down: the forward's inputs.
+ * workspace: >= bwd_ws_bytes. */
+mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void* x,
+                            const void* w_router, const float* router_bias,
+                            const void* w_gate_up, const void* w_down, const void* saved,
+                            size_t saved_bytes, void* dx, void* dw_router, void* dw_gate_up,
+                            void* dw_down, void* workspace, size_t ws_bytes, void* stream);
+
+/* Bytes of scratch that mok_moe_route / mok_moe_dispatch_plan need. */
+mok_status mok_moe_stage_workspace_size(const mok_moe_desc* desc, size_t* bytes);
+
+/* Router alone ([gtnt] §1.1): topk_idx [T,k] int32 and topk_w [T,k] fp32, as
+ * in the forward.  workspace >= the stage size (its first word is the status). */
+mok_status mok_moe_route(const mok_moe_desc* desc, const void* x, const void* w_router,
+                         const float* router_bias, int32_t* topk_idx, float* topk_w,
+                         void* workspace, size_t ws_bytes, void* stream);
+
+/* Dispatch plan alone ([dothoosh] "Hybrid communication", "Ring buffer logic":
+ * dropless): from topk_idx [T,k] int32 (values in [0,E)) computes
+ *   counts [E], offsets [E+1] (exclusive prefix sum), pos [T,k] with
+ *   pos[t,s] = offsets[e] + #{t' < t routed to e}, token_of_row [T*k] = pos^-1.
+ * An index outside [0,E) sets MOK_ERR_DEVICE_INDEX and that slot is skipped
+ * (its pos is -1).  workspace >= the stage size. */
+mok_status mok_moe_dispatch_plan(const mok_moe_desc* desc, const int32_t* topk_idx,
+                                 int32_t* counts, int32_t* offsets, int32_t* pos,
+                                 int32_t* token_of_row, void* workspace, size_t ws_bytes,
+                                 void* stream);
+
+/* Dense GEMM through the layer's tcgen05 engine, C[M,N] = A B in bf16 with
+ * fp32 accumulation and bf16 output (a diagnostic of the grouped engine):
+ *   a_mn_major = 0: A stored [M,K];  1: A stored [K,M]
+ *   b_mn_major = 0: B stored [N,K];  1: B stored [K,N]
+ * (a_mn_major, b_mn_major) = (1, 0) is not served.  M, N, K multiples of 128.
+ * workspace >= 256 bytes (status word). */
+mok_status mok_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int a_mn_major,
+                         const void* B, int b_mn_major, void* C, void* workspace,
+                         size_t ws_bytes, void* stream);
+
+/* Waits for `stream`, then reads the device status word at the start of
+ * `buf` (the `saved` buffer of forward/backward, or the workspace of the
+ * other entry points) into *code (a mok_status; MOK_OK = no device error). */
+mok_status mok_get_device_status(const void* buf, void* stream, int32_t* code);
+
+/* Static description of a status code. */
+const char* mok_status_string(mok_status status);
+
+/* Number of kernels enqueued since the start of the last mok_moe_forward
+ * call (host-side count; after a forward + backward pair it is the number
+ * of kernels of one training step of the layer). */
+int32_t mok_last_launch_count(void);
+
+/* Per-kernel timing.  While enabled, the library brackets each kernel it
+ * enqueues with a pair of CUDA events on the same stream (host-side cost
+ * only; the kernels themselves are unchanged).  mok_profile_collect waits
+ * for the recorded events, then writes up to `max` entries, one per kernel
+ * name, with launch counts and summed durations since the last reset, and
+ * stores the number of entries in *n.  Not thread-safe: enable it around a
+ * single-threaded timing loop. */
+typedef struct mok_kernel_time {
+  char name[48];
+  int32_t launches;
+  double total_ms;
+} mok_kernel_time;
+mok_status mok_profile_enable(int on);
+mok_status mok_profile_reset(void);
+mok_status mok_profile_collect(mok_kernel_time* out, int32_t max, int32_t* n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOK_H_ */

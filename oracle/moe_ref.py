@@ -197,11 +197,13 @@ def moe_forward_ref(x, w_router, bias, w_gate_up, w_down, k: int, routing=None,
 # ----------------------------------------------------------------------------
 
 def moe_backward_ref(x, w_router, bias, w_gate_up, w_down, k: int, dy,
-                     routing=None, fwd=None):
+                     routing=None, fwd=None, grad_experts=None):
     """Analytic gradients of L = sum(y*dy).
 
     Returns dict with dx [T,d], dw_router [E,d], dw_gate_up [E,2I,d],
     dw_down [E,d,I] (all float64) and dp [T,k] (dL/dp).
+    With ``grad_experts`` (an iterable of expert ids), dw_gate_up and dw_down
+    are dicts holding only those experts' gradients (large layers).
     The routing (the chosen set S_t) is piecewise constant, so only p carries
     a gradient into the router logits:
       dp[t,s]   = <dy_t, O[pos[t,s]]>
@@ -229,8 +231,12 @@ def moe_backward_ref(x, w_router, bias, w_gate_up, w_down, k: int, dy,
     dp = np.einsum("tsd,td->ts", O[pos], dY)
 
     dX_rows = np.zeros((R, d))
-    dw_gate_up = np.zeros((E, 2 * I, d))
-    dw_down = np.zeros((E, d, I))
+    if grad_experts is None:
+        dw_gate_up = np.zeros((E, 2 * I, d))
+        dw_down = np.zeros((E, d, I))
+    else:
+        dw_gate_up = {int(e): np.zeros((2 * I, d)) for e in grad_experts}
+        dw_down = {int(e): np.zeros((d, I)) for e in grad_experts}
     for e in range(E):
         a, b = int(offsets[e]), int(offsets[e + 1])
         if a == b:
@@ -238,13 +244,14 @@ def moe_backward_ref(x, w_router, bias, w_gate_up, w_down, k: int, dy,
         Wd = widen(w_down[e])
         Wgu = widen(w_gate_up[e])
         dH = dO[a:b] @ Wd                       # [rows, I]
-        dw_down[e] = dO[a:b].T @ H[a:b]         # [d, I]
         dG = dH * U[a:b] * silu_grad(G[a:b])
         dU = dH * silu(G[a:b])
         Xe = X[tok[a:b]]
         dX_rows[a:b] = dG @ Wgu[:I] + dU @ Wgu[I:]
-        dw_gate_up[e, :I] = dG.T @ Xe
-        dw_gate_up[e, I:] = dU.T @ Xe
+        if grad_experts is None or e in dw_down:
+            dw_down[e][...] = dO[a:b].T @ H[a:b]    # [d, I]
+            dw_gate_up[e][:I] = dG.T @ Xe
+            dw_gate_up[e][I:] = dU.T @ Xe
 
     # reverse-dispatch: sum each token's k rows in slot order
     dx = np.zeros((T, d))

@@ -1,0 +1,170 @@
+"""PyTorch-facing wrappers of the C ABI in include/mok.h.
+
+Tensors only provide device memory and the current stream; every step runs in
+libmok.so.  Shapes and dtypes are checked here, everything else by the library.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+BF16, MXFP8 = 0, 1
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def make_desc(T, d, E, I, k, dtype=BF16) -> _lib.MoeDesc:
+    return _lib.MoeDesc(T=T, d=d, E=E, I=I, k=k, dtype=dtype, mb_tokens=0, ring_slots=0,
+                        flags=0, reserved=0)
+
+
+def workspace_sizes(desc):
+    """(forward scratch, saved, backward scratch) bytes."""
+    lib = _lib.load()
+    f, s, b = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _lib.check(lib.mok_moe_workspace_size(ctypes.byref(desc), ctypes.byref(f), ctypes.byref(s),
+                                          ctypes.byref(b)), "mok_moe_workspace_size")
+    return f.value, s.value, b.value
+
+
+def saved_layout(desc) -> _lib.SavedLayout:
+    lib = _lib.load()
+    L = _lib.SavedLayout()
+    _lib.check(lib.mok_moe_saved_layout(ctypes.byref(desc), ctypes.byref(L)), "mok_moe_saved_layout")
+    return L
+
+
+def stage_workspace_size(desc) -> int:
+    lib = _lib.load()
+    n = ctypes.c_size_t()
+    _lib.check(lib.mok_moe_stage_workspace_size(ctypes.byref(desc), ctypes.byref(n)),
+               "mok_moe_stage_workspace_size")
+    return n.value
+
+
+def forward(desc, x, w_router, bias, w_gate_up, w_down, y, saved, workspace, stream=None):
+    lib = _lib.load()
+    _lib.check(lib.mok_moe_forward(ctypes.byref(desc), _ptr(x), _ptr(w_router), _ptr(bias),
+                                   _ptr(w_gate_up), _ptr(w_down), _ptr(y), _ptr(saved),
+                                   saved.numel(), _ptr(workspace), workspace.numel(),
+                                   _stream(stream)), "mok_moe_forward")
+
+
+def backward(desc, dy, x, w_router, bias, w_gate_up, w_down, saved, dx, dw_router, dw_gate_up,
+             dw_down, workspace, stream=None):
+    lib = _lib.load()
+    _lib.check(lib.mok_moe_backward(ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(w_router),
+                                    _ptr(bias), _ptr(w_gate_up), _ptr(w_down), _ptr(saved),
+                                    saved.numel(), _ptr(dx), _ptr(dw_router), _ptr(dw_gate_up),
+                                    _ptr(dw_down), _ptr(workspace), workspace.numel(),
+                                    _stream(stream)), "mok_moe_backward")
+
+
+def route(desc, x, w_router, bias, topk_idx, topk_w, workspace, stream=None):
+    lib = _lib.load()
+    _lib.check(lib.mok_moe_route(ctypes.byref(desc), _ptr(x), _ptr(w_router), _ptr(bias),
+                                 _ptr(topk_idx), _ptr(topk_w), _ptr(workspace), workspace.numel(),
+                                 _stream(stream)), "mok_moe_route")
+
+
+def dispatch_plan(desc, topk_idx, counts, offsets, pos, token_of_row, workspace, stream=None):
+    lib = _lib.load()
+    _lib.check(lib.mok_moe_dispatch_plan(ctypes.byref(desc), _ptr(topk_idx), _ptr(counts),
+                                         _ptr(offsets), _ptr(pos), _ptr(token_of_row),
+                                         _ptr(workspace), workspace.numel(), _stream(stream)),
+               "mok_moe_dispatch_plan")
+
+
+def gemm_bf16(A, a_mn_major, B, b_mn_major, C, workspace, stream=None):
+    """C = A @ B with A given as [M,K] (a_mn_major=False) or [K,M] (True) and
+    B as [N,K] (b_mn_major=False) or [K,N] (True)."""
+    lib = _lib.load()
+    M, N = C.shape
+    K = A.shape[0] if a_mn_major else A.shape[1]
+    _lib.check(lib.mok_gemm_bf16(M, N, K, _ptr(A), int(a_mn_major), _ptr(B), int(b_mn_major),
+                                 _ptr(C), _ptr(workspace), workspace.numel(), _stream(stream)),
+               "mok_gemm_bf16")
+
+
+def device_status(buf, stream=None) -> int:
+    """Synchronises the stream and returns the device status word of `buf`."""
+    lib = _lib.load()
+    code = ctypes.c_int32()
+    _lib.check(lib.mok_get_device_status(_ptr(buf), _stream(stream), ctypes.byref(code)),
+               "mok_get_device_status")
+    return code.value
+
+
+def last_launch_count() -> int:
+    return int(_lib.load().mok_last_launch_count())
+
+
+def profile_enable(on: bool = True):
+    _lib.check(_lib.load().mok_profile_enable(int(on)), "mok_profile_enable")
+
+
+def profile_reset():
+    _lib.check(_lib.load().mok_profile_reset(), "mok_profile_reset")
+
+
+def profile_collect() -> dict:
+    """{kernel name: (launches, total ms)} since the last reset (waits for the events)."""
+    lib = _lib.load()
+    buf = (_lib.KernelTime * 64)()
+    n = ctypes.c_int32()
+    _lib.check(lib.mok_profile_collect(buf, 64, ctypes.byref(n)), "mok_profile_collect")
+    return {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(n.value)}
+
+
+class MoELayer:
+    """Owns the three buffers of one layer shape and calls forward/backward."""
+
+    def __init__(self, T, d, E, I, k, device="cuda"):
+        self.desc = make_desc(T, d, E, I, k)
+        self.T, self.d, self.E, self.I, self.k = T, d, E, I, k
+        f, s, b = workspace_sizes(self.desc)
+        self.fwd_ws = torch.empty(max(f, 256), dtype=torch.uint8, device=device)
+        self.saved = torch.zeros(max(s, 256), dtype=torch.uint8, device=device)
+        self.bwd_ws = torch.empty(max(b, 256), dtype=torch.uint8, device=device)
+        self.layout = saved_layout(self.desc)
+
+    def saved_tensor(self, field: str, dtype, shape):
+        off = getattr(self.layout, field)
+        n = 1
+        for v in shape:
+            n *= v
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return self.saved[off:off + nbytes].view(dtype).view(*shape)
+
+    def forward(self, x, w_router, bias, w_gate_up, w_down, y=None, stream=None):
+        if y is None:
+            y = torch.empty_like(x)
+        forward(self.desc, x, w_router, bias, w_gate_up, w_down, y, self.saved, self.fwd_ws,
+                stream)
+        return y
+
+    def backward(self, dy, x, w_router, bias, w_gate_up, w_down, dx=None, dw_router=None,
+                 dw_gate_up=None, dw_down=None, stream=None):
+        dx = torch.empty_like(x) if dx is None else dx
+        dw_router = torch.empty_like(w_router) if dw_router is None else dw_router
+        dw_gate_up = torch.empty_like(w_gate_up) if dw_gate_up is None else dw_gate_up
+        dw_down = torch.empty_like(w_down) if dw_down is None else dw_down
+        backward(self.desc, dy, x, w_router, bias, w_gate_up, w_down, self.saved, dx, dw_router,
+                 dw_gate_up, dw_down, self.bwd_ws, stream)
+        return dx, dw_router, dw_gate_up, dw_down
+
+    def status(self, stream=None) -> int:
+        return device_status(self.saved, stream)

@@ -1,0 +1,739 @@
+// Persistent grouped-GEMM engine on tcgen05 (sm_103a) for the experts' SwiGLU
+// FFN: forward gate/up + SwiGLU, forward down, and the backward dgrad/wgrad
+// GEMMs, plus the router logit GEMM.
+//
+// Sources (page title, section):
+//   [gtnt] "MoK揭秘：NVL72上大规模MoE训练工程方案深度解读", §1.3 and §2.2: the
+//     many small per-expert GEMMs are run as one grouped GEMM so the tensor
+//     cores stay busy.
+//   [dothoosh] "Cursor Mixture-of-Kittens cuts MoE training latency by 5.8x",
+//     "MoK technical details", bullet "Overlap granularity": every
+//     expert-grouped GEMM is given at least two full waves of SMs; bullet
+//     "Precision and scheduling": SwiGLU backward fused with the router-weight
+//     gradient.
+//
+// Design (one CTA per SM, 320 threads):
+//   warp 0      TMA producer: 128B-swizzled tiles of A (128 x 64) and B
+//               (BN x 64) into a STAGES-deep shared-memory ring (mbarriers).
+//   warp 1      TMEM owner and MMA issuer: one thread issues
+//               tcgen05.mma.kind::f16 (M=128, N=BN, K=16) x 4 per stage into
+//               one of two fp32 accumulators in TMEM (2*BN columns), and
+//               commits stage release / accumulator-ready to mbarriers.
+//   warps 2..9  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//               lanes 32*(w%4).., columns half (w-2)/4), fused math, stores.
+//               Double-buffered accumulators let tile i's epilogue overlap
+//               tile i+1's MMAs.
+// Tiles are walked in a static round-robin (tile = blockIdx.x + i*gridDim.x),
+// every tile is computed by exactly one CTA with a fixed K order, so results
+// are bitwise reproducible.  Per-expert tile tables come from the dispatch
+// plan (prefix sums of 128-row tiles), read on the device: the host never
+// waits for routing results.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "mok_internal.h"
+#include "ptx.cuh"
+
+namespace mok {
+
+enum Sched : int { SCHED_DENSE = 0, SCHED_MGROUP = 1, SCHED_KGROUP = 2 };
+enum Epi : int { EPI_BF16 = 0, EPI_F32 = 1, EPI_SWIGLU_FWD = 2, EPI_SWIGLU_BWD = 3 };
+
+struct GemmArgs {
+  int E;             // groups (experts); 1 for dense
+  int m_tiles;       // DENSE/KGROUP: 128-row tiles of M
+  int n_tiles;       // N tiles
+  int num_kb;        // DENSE/MGROUP: K / 64
+  int b_group_rows;  // MGROUP: rows of B per expert in its 2-D view
+  int I;             // SwiGLU epilogues: FFN width
+  int m_valid, n_valid;  // DENSE: valid rows / columns of C
+  const int* mtile_prefix;  // MGROUP: [E+1] prefix of 128-row tiles per expert
+  const int* poff;          // MGROUP/KGROUP: [E+1] padded row offsets
+  void* out;                // C (bf16 or fp32)
+  long long ldo;            // C row stride (elements)
+  long long out_group_stride;  // KGROUP: elements between experts' C
+  void* out2;               // SWIGLU_FWD: H [rows,I]; SWIGLU_BWD: HP [rows,I]
+  const void* in_gu;        // SWIGLU_BWD: saved pre-activations [rows,2I]
+  const float* row_w;       // SWIGLU_BWD: routing weight per row
+  float* dp_part;           // SWIGLU_BWD: [rows, np] partial <dA,h>
+  int np;
+  int* status;
+};
+
+template <int BN>
+struct Cfg {
+  static constexpr int BM = 128, BK = 64;
+  static constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+  static constexpr int B_BYTES = BN * BK * 2;  // 32 KB (BN=256) / 16 KB (BN=128)
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int BAR_BYTES = 1024;
+  static constexpr int PREFIX_BYTES = 4 * (kMaxExperts + 1);
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + PREFIX_BYTES;
+};
+static_assert(Cfg<256>::SMEM_BYTES <= 232448, "smem");
+static_assert(Cfg<128>::SMEM_BYTES <= 232448, "smem");
+
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
+
+struct Tile {
+  int e, m_tile, n_tile;
+  int row0;    // MGROUP/DENSE: first row of A and C
+  int k_row0;  // KGROUP: first K row (padded offset of the expert)
+  int num_kb;
+};
+
+template <int SCHED>
+__device__ __forceinline__ int total_tiles(const GemmArgs& a, const int* s_prefix) {
+  if (SCHED == SCHED_MGROUP) return s_prefix[a.E] * a.n_tiles;
+  if (SCHED == SCHED_KGROUP) return a.E * a.m_tiles * a.n_tiles;
+  return a.m_tiles * a.n_tiles;
+}
+
+template <int SCHED>
+__device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const int* s_prefix, int t) {
+  Tile tl;
+  if (SCHED == SCHED_MGROUP) {
+    // largest e with s_prefix[e] * n_tiles <= t
+    int lo = 0, hi = a.E;  // invariant: s_prefix[lo]*nt <= t < s_prefix[hi]*nt
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_prefix[mid] * a.n_tiles <= t) lo = mid; else hi = mid;
+    }
+    const int e = lo;
+    const int mt_e = s_prefix[e + 1] - s_prefix[e];
+    const int local = t - s_prefix[e] * a.n_tiles;
+    tl.e = e;
+    tl.n_tile = local / mt_e;
+    tl.m_tile = local - tl.n_tile * mt_e;
+    tl.row0 = a.poff[e] + tl.m_tile * 128;
+    tl.k_row0 = 0;
+    tl.num_kb = a.num_kb;
+  } else if (SCHED == SCHED_KGROUP) {
+    const int tpe = a.m_tiles * a.n_tiles;
+    const int e = t / tpe;
+    const int local = t - e * tpe;
+    tl.e = e;
+    tl.n_tile = local / a.m_tiles;
+    tl.m_tile = local - tl.n_tile * a.m_tiles;
+    tl.row0 = tl.m_tile * 128;
+    const int k0 = a.poff[e], k1 = a.poff[e + 1];
+    tl.k_row0 = k0;
+    tl.num_kb = (k1 - k0) / 64;
+  } else {
+    tl.e = 0;
+    tl.n_tile = t / a.m_tiles;
+    tl.m_tile = t - tl.n_tile * a.m_tiles;
+    tl.row0 = tl.m_tile * 128;
+    tl.k_row0 = 0;
+    tl.num_kb = a.num_kb;
+  }
+  return tl;
+}
+
+__device__ __forceinline__ float silu_f(float g, float* sig_out) {
+  const float s = 1.0f / (1.0f + __expf(-g));
+  *sig_out = s;
+  return g * s;
+}
+
+// ---------------------------------------------------------------- epilogues --
+
+// Loads 32 consecutive accumulator columns (two x16 loads, one wait).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r0[16], r1[16];
+  tmem_ld16(taddr, r0);
+  tmem_ld16(taddr + 16, r1);
+  tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    v[j] = __uint_as_float(r0[j]);
+    v[16 + j] = __uint_as_float(r1[j]);
+  }
+}
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, const float (&v)[32]) {
+  uint4 w[4];
+  uint32_t* u = reinterpret_cast<uint32_t*>(w);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) u[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+  uint4* q = reinterpret_cast<uint4*>(p);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) q[j] = w[j];
+}
+
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* p, float (&v)[32]) {
+  const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint4 w = q[j];
+    v[8 * j + 0] = bf16lo(w.x); v[8 * j + 1] = bf16hi(w.x);
+    v[8 * j + 2] = bf16lo(w.y); v[8 * j + 3] = bf16hi(w.y);
+    v[8 * j + 4] = bf16lo(w.z); v[8 * j + 5] = bf16hi(w.z);
+    v[8 * j + 6] = bf16lo(w.w); v[8 * j + 7] = bf16hi(w.w);
+  }
+}
+
+template <int BN, int SCHED, int EPI>
+__device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl, uint32_t taddr,
+                                              int row_in_tile, int half) {
+  constexpr int HALF_COLS = BN / 2;
+  const bool zero_k = (tl.num_kb == 0);
+  if (EPI == EPI_BF16 || EPI == EPI_F32) {
+    long long grow;
+    char* base;
+    constexpr int esz = EPI == EPI_F32 ? 4 : 2;
+    if (SCHED == SCHED_KGROUP) {
+      grow = tl.row0 + row_in_tile;
+      base = static_cast<char*>(a.out) + (long long)tl.e * a.out_group_stride * esz;
+    } else {
+      grow = tl.row0 + row_in_tile;
+      base = static_cast<char*>(a.out);
+    }
+    const bool row_ok = (SCHED != SCHED_DENSE) || grow < a.m_valid;
+    const int col0 = tl.n_tile * BN + half * HALF_COLS;
+#pragma unroll 1
+    for (int c = 0; c < HALF_COLS; c += 32) {
+      float v[32];
+      if (!zero_k) {
+        tmem_ld32(taddr + half * HALF_COLS + c, v);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.f;
+      }
+      if (!row_ok) continue;
+      if (EPI == EPI_BF16) {
+        __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(base) + grow * a.ldo + col0 + c;
+        store_bf16x32(p, v);
+      } else {
+        float* p = reinterpret_cast<float*>(base) + grow * a.ldo;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int col = col0 + c + j;
+          if (col < a.n_valid) p[col] = v[j];
+        }
+      }
+    }
+  } else if (EPI == EPI_SWIGLU_FWD) {
+    // BN = 256: accumulator columns [0,128) gate, [128,256) up, for FFN
+    // columns n0 .. n0+127 with n0 = n_tile*128.  This thread: 64 of them.
+    const long long r = tl.row0 + row_in_tile;
+    const int I = a.I;
+    const int n0 = tl.n_tile * 128 + half * 64;
+    __nv_bfloat16* gu = static_cast<__nv_bfloat16*>(a.out) + r * (2LL * I);
+    __nv_bfloat16* h = static_cast<__nv_bfloat16*>(a.out2) + r * (long long)I;
+#pragma unroll 1
+    for (int c = 0; c < 64; c += 32) {
+      float g[32], u[32], hv[32];
+      tmem_ld32(taddr + half * 64 + c, g);
+      tmem_ld32(taddr + 128 + half * 64 + c, u);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        g[j] = bf16_round(g[j]);
+        u[j] = bf16_round(u[j]);
+        float s;
+        hv[j] = silu_f(g[j], &s) * u[j];
+      }
+      store_bf16x32(gu + n0 + c, g);
+      store_bf16x32(gu + I + n0 + c, u);
+      store_bf16x32(h + n0 + c, hv);
+    }
+  } else if (EPI == EPI_SWIGLU_BWD) {
+    // accumulator = dA = dY_perm W_down (rows x BN columns of I, n0 = n_tile*BN)
+    const long long r = tl.row0 + row_in_tile;
+    const int I = a.I;
+    const int n0 = tl.n_tile * BN + half * HALF_COLS;
+    const __nv_bfloat16* gu = static_cast<const __nv_bfloat16*>(a.in_gu) + r * (2LL * I);
+    __nv_bfloat16* dgu = static_cast<__nv_bfloat16*>(a.out) + r * (2LL * I);
+    __nv_bfloat16* hp = static_cast<__nv_bfloat16*>(a.out2) + r * (long long)I;
+    const float p = a.row_w[r];
+    float dp = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < HALF_COLS; c += 32) {
+      float dA[32], g[32], u[32], o1[32], o2[32];
+      tmem_ld32(taddr + half * HALF_COLS + c, dA);
+      load_bf16x32(gu + n0 + c, g);
+      load_bf16x32(gu + I + n0 + c, u);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float s;
+        const float sl = silu_f(g[j], &s);
+        const float hv = bf16_round(sl * u[j]);   // the forward's h
+        dp = fmaf(dA[j], hv, dp);
+        const float dh = p * dA[j];
+        o1[j] = dh * u[j] * (s * (1.0f + g[j] * (1.0f - s)));  // d gate
+        o2[j] = dh * sl;                                       // d up
+        g[j] = p * hv;                                         // p*h for dW_down
+      }
+      store_bf16x32(dgu + n0 + c, o1);
+      store_bf16x32(dgu + I + n0 + c, o2);
+      store_bf16x32(hp + n0 + c, g);
+    }
+    a.dp_part[r * a.np + tl.n_tile * 2 + half] = dp;
+  }
+}
+
+// ------------------------------------------------------------------- kernel --
+
+template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ GemmArgs args) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* tiles = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int* s_prefix = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (threadIdx.x == 32) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (SCHED == SCHED_MGROUP) {
+    for (int i = threadIdx.x; i <= args.E; i += blockDim.x) s_prefix[i] = args.mtile_prefix[i];
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  volatile int* vabort = abort_flag;
+  const int total = total_tiles<SCHED>(args, s_prefix);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------- producer --
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued_par[C::STAGES];
+#pragma unroll
+      for (int s = 0; s < C::STAGES; ++s) issued_par[s] = -1;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile tl = decode_tile<SCHED>(args, s_prefix, t);
+        for (int kb = 0; kb < tl.num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, vabort)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sA = tiles + stage * C::STAGE_BYTES;
+          uint8_t* sB = sA + C::A_BYTES;
+          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+          // A tile: 128 rows (M) x 64 (K)
+          if (!A_MN) {
+            const int kx = (SCHED == SCHED_KGROUP ? tl.k_row0 : 0) + kb * 64;
+            tma_load_2d(sA, &tmA, &full[stage], kx, tl.row0);
+          } else {
+            const int ky = tl.k_row0 + kb * 64;
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+              tma_load_2d(sA + j * 8192, &tmA, &full[stage], tl.row0 + 64 * j, ky);
+          }
+          // B tile: BN rows (N) x 64 (K)
+          if (!B_MN) {
+            if (EPI == EPI_SWIGLU_FWD) {
+              const int r0 = tl.e * args.b_group_rows + tl.n_tile * 128;
+              tma_load_2d(sB, &tmB, &full[stage], kb * 64, r0);
+              tma_load_2d(sB + 16384, &tmB, &full[stage], kb * 64, r0 + args.I);
+            } else {
+              const int r0 = tl.e * args.b_group_rows + tl.n_tile * BN;
+              tma_load_2d(sB, &tmB, &full[stage], kb * 64, r0);
+            }
+          } else {
+            int ky;
+            if (SCHED == SCHED_KGROUP) ky = tl.k_row0 + kb * 64;
+            else ky = tl.e * args.b_group_rows + kb * 64;
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(sB + j * 8192, &tmB, &full[stage], tl.n_tile * BN + 64 * j, ky);
+          }
+          issued_par[stage] = static_cast<int>(phase);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        *vabort = 1;
+        set_status(args.status, MOK_ERR_DEVICE_TIMEOUT);
+        // let the copies already issued land before the CTA can exit
+        const int zero = 0;
+        for (int s = 0; s < C::STAGES; ++s)
+          if (issued_par[s] >= 0) mbar_wait(&full[s], static_cast<uint32_t>(issued_par[s]), &zero);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA --
+      constexpr uint32_t idesc = idesc_bf16_f32(128, BN, A_MN, B_MN);
+      constexpr uint32_t lbo_a = A_MN ? 8192u : 16u;
+      constexpr uint32_t lbo_b = B_MN ? 8192u : 16u;
+      constexpr uint32_t kstep_a = A_MN ? 2048u : 32u;
+      constexpr uint32_t kstep_b = B_MN ? 2048u : 32u;
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+        const Tile tl = decode_tile<SCHED>(args, s_prefix, t);
+        const int acc = it & 1;
+        const uint32_t acc_par = static_cast<uint32_t>((it >> 1) & 1);
+        if (!mbar_wait(&tempty[acc], acc_par ^ 1u, vabort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < tl.num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, vabort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a_base = smem_addr(tiles + stage * C::STAGE_BYTES);
+          const uint32_t b_base = a_base + C::A_BYTES;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t ad = smem_desc_sw128(a_base + j * kstep_a, lbo_a, 1024);
+            const uint64_t bd = smem_desc_sw128(b_base + j * kstep_b, lbo_b, 1024);
+            mma_bf16(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
+          }
+          mma_commit(&empty[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);
+      }
+      if (!ok) {
+        *vabort = 1;
+        set_status(args.status, MOK_ERR_DEVICE_TIMEOUT);
+        const int zero = 0;
+        mma_commit(drain);
+        mbar_wait(drain, 0, &zero);
+      }
+    }
+  } else {
+    // ----------------------------------------------------------- epilogue --
+    const int q = warp & 3;                // TMEM lane quarter this warp may read
+    const int half = (warp - 2) >> 2;      // column half of the tile
+    const int row_in_tile = q * 32 + lane;
+    int it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+      const Tile tl = decode_tile<SCHED>(args, s_prefix, t);
+      const int acc = it & 1;
+      const uint32_t acc_par = static_cast<uint32_t>((it >> 1) & 1);
+      if (!mbar_wait(&tfull[acc], acc_par, vabort)) {
+        *vabort = 1;
+        set_status(args.status, MOK_ERR_DEVICE_TIMEOUT);
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      epilogue_tile<BN, SCHED, EPI>(args, tl, taddr, row_in_tile, half);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// --------------------------------------------------------------------- host --
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 map over a row-major [outer, inner] array with row stride
+// `row_elems`, box {64, box_rows}, 128-byte swizzle, zero fill out of bounds.
+static bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                     uint64_t row_elems, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  if (outer == 0) outer = 1;  // empty operand: the map exists but is never read
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_elems * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI>
+static cudaError_t launch(const char* name, const CUtensorMap& ta, const CUtensorMap& tb,
+                          const GemmArgs& args, int max_tiles, cudaStream_t st) {
+  auto kern = gemm_kernel<BN, A_MN, B_MN, SCHED, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg<BN>::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  if (max_tiles <= 0) return cudaSuccess;
+  int grid = num_sms_current_device();
+  if (max_tiles < grid) grid = max_tiles;
+  ProfScope prof(name, st);
+  kern<<<grid, kThreads, Cfg<BN>::SMEM_BYTES, st>>>(ta, tb, args);
+  count_launch();
+  return cudaGetLastError();
+}
+
+static GemmArgs blank_args(int* status) {
+  GemmArgs a;
+  memset(&a, 0, sizeof(a));
+  a.status = status;
+  return a;
+}
+
+static inline int max_mtiles(const Dims& D) { return static_cast<int>(D.rows_max / 128); }
+
+cudaError_t gemm_fwd_gate_up(const Dims& D, const void* X_perm, const void* w_gate_up,
+                             const int32_t* mtile_prefix, const int32_t* poff, void* GU, void* H,
+                             int* status, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, X_perm, D.d, D.rows_max, D.d, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&tb, w_gate_up, D.d, D.E * 2 * D.I, D.d, 128)) return cudaErrorInvalidValue;
+  GemmArgs a = blank_args(status);
+  a.E = (int)D.E;
+  a.n_tiles = (int)(D.I / 128);
+  a.num_kb = (int)(D.d / 64);
+  a.b_group_rows = (int)(2 * D.I);
+  a.I = (int)D.I;
+  a.mtile_prefix = mtile_prefix;
+  a.poff = poff;
+  a.out = GU;
+  a.out2 = H;
+  return launch<256, false, false, SCHED_MGROUP, EPI_SWIGLU_FWD>("fwd_gate_up_swiglu", ta, tb, a,
+                                                                  max_mtiles(D) * a.n_tiles, st);
+}
+
+cudaError_t gemm_fwd_down(const Dims& D, const void* H, const void* w_down,
+                          const int32_t* mtile_prefix, const int32_t* poff, void* O, int* status,
+                          cudaStream_t st) {
+  const int bn = (D.d % 256 == 0) ? 256 : 128;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, H, D.I, D.rows_max, D.I, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&tb, w_down, D.I, D.E * D.d, D.I, bn)) return cudaErrorInvalidValue;
+  GemmArgs a = blank_args(status);
+  a.E = (int)D.E;
+  a.n_tiles = (int)(D.d / bn);
+  a.num_kb = (int)(D.I / 64);
+  a.b_group_rows = (int)D.d;
+  a.mtile_prefix = mtile_prefix;
+  a.poff = poff;
+  a.out = O;
+  a.ldo = D.d;
+  const int mt = max_mtiles(D) * a.n_tiles;
+  if (bn == 256) return launch<256, false, false, SCHED_MGROUP, EPI_BF16>("fwd_down", ta, tb, a, mt, st);
+  return launch<128, false, false, SCHED_MGROUP, EPI_BF16>("fwd_down", ta, tb, a, mt, st);
+}
+
+cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* w_down,
+                                const int32_t* mtile_prefix, const int32_t* poff, const void* GU,
+                                const float* row_w, void* dGU, void* HP, float* dp_part,
+                                int* status, cudaStream_t st) {
+  const int bn = D.bn_dgrad;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, dY_perm, D.d, D.rows_max, D.d, 128)) return cudaErrorInvalidValue;
+  // W_down_e viewed as [K = d rows, N = I columns]: N-major operand
+  if (!make_map(&tb, w_down, D.I, D.E * D.d, D.I, 64)) return cudaErrorInvalidValue;
+  GemmArgs a = blank_args(status);
+  a.E = (int)D.E;
+  a.n_tiles = (int)(D.I / bn);
+  a.num_kb = (int)(D.d / 64);
+  a.b_group_rows = (int)D.d;
+  a.I = (int)D.I;
+  a.mtile_prefix = mtile_prefix;
+  a.poff = poff;
+  a.out = dGU;
+  a.out2 = HP;
+  a.in_gu = GU;
+  a.row_w = row_w;
+  a.dp_part = dp_part;
+  a.np = D.np;
+  const int mt = max_mtiles(D) * a.n_tiles;
+  if (bn == 256) return launch<256, false, true, SCHED_MGROUP, EPI_SWIGLU_BWD>("bwd_down_dgrad_swiglu", ta, tb, a, mt, st);
+  return launch<128, false, true, SCHED_MGROUP, EPI_SWIGLU_BWD>("bwd_down_dgrad_swiglu", ta, tb, a, mt, st);
+}
+
+cudaError_t gemm_bwd_gate_up_dgrad(const Dims& D, const void* dGU, const void* w_gate_up,
+                                   const int32_t* mtile_prefix, const int32_t* poff,
+                                   void* dX_perm, int* status, cudaStream_t st) {
+  const int bn = (D.d % 256 == 0) ? 256 : 128;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, dGU, 2 * D.I, D.rows_max, 2 * D.I, 128)) return cudaErrorInvalidValue;
+  // W_gu_e viewed as [K = 2I rows, N = d columns]: N-major operand
+  if (!make_map(&tb, w_gate_up, D.d, D.E * 2 * D.I, D.d, 64)) return cudaErrorInvalidValue;
+  GemmArgs a = blank_args(status);
+  a.E = (int)D.E;
+  a.n_tiles = (int)(D.d / bn);
+  a.num_kb = (int)(2 * D.I / 64);
+  a.b_group_rows = (int)(2 * D.I);
+  a.mtile_prefix = mtile_prefix;
+  a.poff = poff;
+  a.out = dX_perm;
+  a.ldo = D.d;
+  const int mt = max_mtiles(D) * a.n_tiles;
+  if (bn == 256) return launch<256, false, true, SCHED_MGROUP, EPI_BF16>("bwd_gate_up_dgrad", ta, tb, a, mt, st);
+  return launch<128, false, true, SCHED_MGROUP, EPI_BF16>("bwd_gate_up_dgrad", ta, tb, a, mt, st);
+}
+
+cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* HP,
+                            const int32_t* poff, void* dw_down, int* status, cudaStream_t st) {
+  // dW_down_e [d, I] = dY_perm_e^T [d x rows] * HP_e [rows x I]
+  const int bn = (D.I % 256 == 0) ? 256 : 128;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, dY_perm, D.d, D.rows_max, D.d, 64)) return cudaErrorInvalidValue;
+  if (!make_map(&tb, HP, D.I, D.rows_max, D.I, 64)) return cudaErrorInvalidValue;
+  GemmArgs a = blank_args(status);
+  a.E = (int)D.E;
+  a.m_tiles = (int)(D.d / 128);
+  a.n_tiles = (int)(D.I / bn);
+  a.poff = poff;
+  a.out = dw_down;
+  a.ldo = D.I;
+  a.out_group_stride = D.d * D.I;
+  const int mt = a.E * a.m_tiles * a.n_tiles;
+  if (bn == 256) return launch<256, true, true, SCHED_KGROUP, EPI_BF16>("bwd_down_wgrad", ta, tb, a, mt, st);
+  return launch<128, true, true, SCHED_KGROUP, EPI_BF16>("bwd_down_wgrad", ta, tb, a, mt, st);
+}
+
+cudaError_t gemm_wgrad_gate_up(const Dims& D, const void* dGU, const void* X_perm,
+                               const int32_t* poff, void* dw_gate_up, int* status,
+                               cudaStream_t st) {
+  // dW_gu_e [2I, d] = dGU_e^T [2I x rows] * X_perm_e [rows x d]
+  const int bn = (D.d % 256 == 0) ? 256 : 128;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, dGU, 2 * D.I, D.rows_max, 2 * D.I, 64)) return cudaErrorInvalidValue;
+  if (!make_map(&tb, X_perm, D.d, D.rows_max, D.d, 64)) return cudaErrorInvalidValue;
+  GemmArgs a = blank_args(status);
+  a.E = (int)D.E;
+  a.m_tiles = (int)(2 * D.I / 128);
+  a.n_tiles = (int)(D.d / bn);
+  a.poff = poff;
+  a.out = dw_gate_up;
+  a.ldo = D.d;
+  a.out_group_stride = 2 * D.I * D.d;
+  const int mt = a.E * a.m_tiles * a.n_tiles;
+  if (bn == 256) return launch<256, true, true, SCHED_KGROUP, EPI_BF16>("bwd_gate_up_wgrad", ta, tb, a, mt, st);
+  return launch<128, true, true, SCHED_KGROUP, EPI_BF16>("bwd_gate_up_wgrad", ta, tb, a, mt, st);
+}
+
+cudaError_t launch_router_logits(const Dims& D, const void* x, const void* w_router,
+                                 float* logits, int* status, cudaStream_t st) {
+  // logits [T, E] fp32 = x [T,d] * W_r[E,d]^T; rows >= T and columns >= E
+  // are zero-filled by the TMA and masked at the store.
+  if (D.T == 0) return cudaSuccess;
+  const int bn = (D.E > 128) ? 256 : 128;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, x, D.d, D.T, D.d, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&tb, w_router, D.d, D.E, D.d, bn)) return cudaErrorInvalidValue;
+  GemmArgs a = blank_args(status);
+  a.E = 1;
+  a.m_tiles = (int)((D.T + 127) / 128);
+  a.n_tiles = (int)((D.E + bn - 1) / bn);
+  a.num_kb = (int)(D.d / 64);
+  a.m_valid = (int)D.T;
+  a.n_valid = (int)D.E;
+  a.out = logits;
+  a.ldo = D.E;
+  const int mt = a.m_tiles * a.n_tiles;
+  if (bn == 256) return launch<256, false, false, SCHED_DENSE, EPI_F32>("router_logits", ta, tb, a, mt, st);
+  return launch<128, false, false, SCHED_DENSE, EPI_F32>("router_logits", ta, tb, a, mt, st);
+}
+
+cudaError_t gemm_dense_bf16(int64_t M, int64_t N, int64_t K, const void* A, bool a_mn,
+                            const void* B, bool b_mn, void* C, int* status, cudaStream_t st) {
+  const int bn = (N % 256 == 0) ? 256 : 128;
+  CUtensorMap ta, tb;
+  if (!a_mn) {
+    if (!make_map(&ta, A, K, M, K, 128)) return cudaErrorInvalidValue;
+  } else {
+    if (!make_map(&ta, A, M, K, M, 64)) return cudaErrorInvalidValue;
+  }
+  if (!b_mn) {
+    if (!make_map(&tb, B, K, N, K, bn)) return cudaErrorInvalidValue;
+  } else {
+    if (!make_map(&tb, B, N, K, N, 64)) return cudaErrorInvalidValue;
+  }
+  GemmArgs a = blank_args(status);
+  a.E = 1;
+  a.m_tiles = (int)(M / 128);
+  a.n_tiles = (int)(N / bn);
+  a.num_kb = (int)(K / 64);
+  a.m_valid = (int)M;
+  a.n_valid = (int)N;
+  a.out = C;
+  a.ldo = N;
+  const int mt = a.m_tiles * a.n_tiles;
+  if (a_mn) {
+    // the MN-major A path walks K from k_row0 = 0
+    if (bn == 256) return launch<256, true, true, SCHED_DENSE, EPI_BF16>("dense_gemm", ta, tb, a, mt, st);
+    return launch<128, true, true, SCHED_DENSE, EPI_BF16>("dense_gemm", ta, tb, a, mt, st);
+  }
+  if (b_mn) {
+    if (bn == 256) return launch<256, false, true, SCHED_DENSE, EPI_BF16>("dense_gemm", ta, tb, a, mt, st);
+    return launch<128, false, true, SCHED_DENSE, EPI_BF16>("dense_gemm", ta, tb, a, mt, st);
+  }
+  if (bn == 256) return launch<256, false, false, SCHED_DENSE, EPI_BF16>("dense_gemm", ta, tb, a, mt, st);
+  return launch<128, false, false, SCHED_DENSE, EPI_BF16>("dense_gemm", ta, tb, a, mt, st);
+}
+
+}  // namespace mok

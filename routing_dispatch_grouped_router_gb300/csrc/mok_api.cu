@@ -1,0 +1,536 @@
+// C ABI of the MoE layer (declared in include/mok.h): argument checks, buffer
+// layouts, and the order of kernels of the forward and the backward.
+//
+// Sources (page title, section):
+//   [dothoosh] "Cursor Mixture-of-Kittens cuts MoE training latency by 5.8x",
+//     "MoK technical details", bullet "Hybrid communication": forward =
+//     dispatch -> expert GEMMs -> combine; backward = reverse-combine ->
+//     grouped dgrad/wgrad -> reverse-dispatch; bullet "Ring buffer logic":
+//     fixed-size buffers, nothing sized by the CPU from routing results.
+//   [aikraft] "Cursor MoK: revolution in MoE model training on NVL72", §03:
+//     no CPU-GPU synchronisation on the critical path.  Every buffer and grid
+//     here is sized from (T, k, E, d, I) bounds; no count is read back.
+#include <cuda_runtime.h>
+#include <string.h>
+
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "mok_internal.h"
+
+namespace mok {
+
+static std::atomic<int32_t> g_launches{0};
+void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+void reset_launch_count() { g_launches.store(0, std::memory_order_relaxed); }
+int32_t launch_count() { return g_launches.load(std::memory_order_relaxed); }
+
+// ---------------------------------------------------------------- profiling --
+struct ProfRec {
+  const char* name;
+  cudaEvent_t a, b;
+};
+static bool g_prof = false;
+static std::vector<ProfRec> g_recs;
+static std::vector<cudaEvent_t> g_pool;
+static size_t g_pool_used = 0;
+
+static cudaEvent_t pool_event() {
+  if (g_pool_used == g_pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    g_pool.push_back(e);
+  }
+  return g_pool[g_pool_used++];
+}
+
+void prof_begin(const char* name, cudaStream_t st) {
+  if (!g_prof) return;
+  ProfRec r{name, pool_event(), pool_event()};
+  if (!r.a || !r.b) return;
+  cudaEventRecord(r.a, st);
+  g_recs.push_back(r);
+}
+
+void prof_end(cudaStream_t st) {
+  if (!g_prof || g_recs.empty()) return;
+  cudaEventRecord(g_recs.back().b, st);
+}
+
+int num_sms_current_device() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 148;
+  }
+  return cache[dev];
+}
+
+static mok_status check_device() {
+  static int ok_cache[64] = {0};  // 0 unknown, 1 ok, 2 bad
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOK_ERR_NO_DEVICE;
+  if (ok_cache[dev] == 0) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    ok_cache[dev] = (major == 10 && minor == 3) ? 1 : 2;
+  }
+  return ok_cache[dev] == 1 ? MOK_OK : MOK_ERR_NO_DEVICE;
+}
+
+static inline size_t al(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+mok_status make_dims(const mok_moe_desc* desc, Dims* out) {
+  if (!desc || !out) return MOK_ERR_INVALID_ARG;
+  const mok_moe_desc& d = *desc;
+  if (d.T < 0 || d.d <= 0 || d.E <= 0 || d.I <= 0 || d.k <= 0) return MOK_ERR_INVALID_ARG;
+  if (d.dtype != MOK_BF16) return MOK_ERR_UNSUPPORTED;
+  if (d.mb_tokens != 0 || d.ring_slots != 0 || d.flags != 0) return MOK_ERR_UNSUPPORTED;
+  if (d.E > kMaxExperts || d.k > kMaxTopK || d.k > d.E) return MOK_ERR_UNSUPPORTED;
+  if (d.d % 128 != 0 || d.I % 128 != 0) return MOK_ERR_UNSUPPORTED;
+  if (d.d > 16384 || d.I > 16384) return MOK_ERR_UNSUPPORTED;
+  if (d.T * d.k >= (1LL << 31) / 2) return MOK_ERR_UNSUPPORTED;
+  Dims D;
+  D.T = d.T;
+  D.d = d.d;
+  D.E = d.E;
+  D.I = d.I;
+  D.k = d.k;
+  D.R = d.T * d.k;
+  const int64_t segs = D.R < D.E ? D.R : D.E;
+  D.rows_max = (D.R + (kRowPad - 1) * segs + kRowPad - 1) / kRowPad * kRowPad;
+  D.nb = (D.T + kPlanBlock - 1) / kPlanBlock;
+  D.bn_dgrad = (D.I % 256 == 0) ? 256 : 128;
+  D.np = static_cast<int>(D.I / D.bn_dgrad) * 2;
+  // every row index and element offset used in 32-bit arithmetic must fit
+  if (D.rows_max * 2 * D.I >= (1LL << 40)) return MOK_ERR_UNSUPPORTED;
+  if (D.rows_max >= (1LL << 31) / 2) return MOK_ERR_UNSUPPORTED;
+  *out = D;
+  return MOK_OK;
+}
+
+void saved_layout(const Dims& D, mok_saved_layout* L, size_t* mtile_prefix_off) {
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += al(bytes);
+    return at;
+  };
+  const size_t Tk = static_cast<size_t>(D.T) * D.k;
+  const size_t E = static_cast<size_t>(D.E);
+  const size_t rows = static_cast<size_t>(D.rows_max);
+  L->status = take(256);
+  L->topk_idx = take(Tk * 4);
+  L->topk_w = take(Tk * 4);
+  L->counts = take(E * 4);
+  L->offsets = take((E + 1) * 4);
+  L->pos = take(Tk * 4);
+  L->token_of_row = take(Tk * 4);
+  L->padded_offsets = take((E + 1) * 4);
+  const size_t mt = take((E + 1) * 4);
+  if (mtile_prefix_off) *mtile_prefix_off = mt;
+  L->padded_pos = take(Tk * 4);
+  L->padded_token = take(rows * 4);
+  L->row_weight = take(rows * 4);
+  L->x_perm = take(rows * D.d * 2);
+  L->gate_up = take(rows * 2 * D.I * 2);
+  L->rows_max = rows;
+  L->total = o;
+}
+
+void fwd_layout(const Dims& D, FwdWs* W) {
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += al(bytes);
+    return at;
+  };
+  const size_t rows = static_cast<size_t>(D.rows_max);
+  W->block_counts = take(static_cast<size_t>(D.nb) * D.E * 4);
+  W->block_base = take(static_cast<size_t>(D.nb) * D.E * 4);
+  W->h = take(rows * D.I * 2);
+  W->o = take(rows * D.d * 2);
+  W->logits = take(static_cast<size_t>(D.T) * D.E * 4);
+  W->total = o;
+}
+
+void bwd_layout(const Dims& D, BwdWs* W) {
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += al(bytes);
+    return at;
+  };
+  const size_t rows = static_cast<size_t>(D.rows_max);
+  W->dy_perm = take(rows * D.d * 2);
+  W->dgu = take(rows * 2 * D.I * 2);
+  W->hp = take(rows * D.I * 2);
+  W->dp_part = take(rows * D.np * 4);
+  W->dx_perm = take(rows * D.d * 2);
+  W->dl_row = take(rows * 4);
+  W->dl_tok = take(static_cast<size_t>(D.T) * D.k * 4);
+  W->total = o;
+}
+
+void stage_layout(const Dims& D, StageWs* W) {
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += al(bytes);
+    return at;
+  };
+  const size_t rows = static_cast<size_t>(D.rows_max);
+  W->status = take(256);
+  W->block_counts = take(static_cast<size_t>(D.nb) * D.E * 4);
+  W->block_base = take(static_cast<size_t>(D.nb) * D.E * 4);
+  W->padded_offsets = take((D.E + 1) * 4);
+  W->mtile_prefix = take((D.E + 1) * 4);
+  W->ppos = take(static_cast<size_t>(D.T) * D.k * 4);
+  W->ptok = take(rows * 4);
+  W->row_w = 0;
+  W->logits = take(static_cast<size_t>(D.T) * D.E * 4);
+  W->total = o;
+}
+
+}  // namespace mok
+
+using namespace mok;
+
+#define MOK_CUDA(call)                          \
+  do {                                          \
+    if ((call) != cudaSuccess) return MOK_ERR_CUDA; \
+  } while (0)
+
+static inline bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+template <typename T>
+static inline T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+template <typename T>
+static inline const T* at(const void* base, size_t off) {
+  return reinterpret_cast<const T*>(static_cast<const char*>(base) + off);
+}
+
+extern "C" {
+
+mok_status mok_moe_workspace_size(const mok_moe_desc* desc, size_t* fwd_ws_bytes,
+                                  size_t* saved_bytes, size_t* bwd_ws_bytes) {
+  Dims D;
+  mok_status s = make_dims(desc, &D);
+  if (s != MOK_OK) return s;
+  mok_saved_layout L;
+  saved_layout(D, &L, nullptr);
+  FwdWs F;
+  fwd_layout(D, &F);
+  BwdWs B;
+  bwd_layout(D, &B);
+  if (fwd_ws_bytes) *fwd_ws_bytes = F.total;
+  if (saved_bytes) *saved_bytes = L.total;
+  if (bwd_ws_bytes) *bwd_ws_bytes = B.total;
+  return MOK_OK;
+}
+
+mok_status mok_moe_saved_layout(const mok_moe_desc* desc, mok_saved_layout* out) {
+  if (!out) return MOK_ERR_INVALID_ARG;
+  Dims D;
+  mok_status s = make_dims(desc, &D);
+  if (s != MOK_OK) return s;
+  saved_layout(D, out, nullptr);
+  return MOK_OK;
+}
+
+mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* w_router,
+                           const float* router_bias, const void* w_gate_up, const void* w_down,
+                           void* y, void* saved, size_t saved_bytes, void* workspace,
+                           size_t ws_bytes, void* stream) {
+  Dims D;
+  mok_status s = make_dims(desc, &D);
+  if (s != MOK_OK) return s;
+  const bool empty = D.T == 0;  // no token rows: x and y may be NULL
+  if ((!x && !empty) || !w_router || !w_gate_up || !w_down || (!y && !empty) || !saved ||
+      !workspace)
+    return MOK_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(w_gate_up) || !aligned16(w_down) ||
+      !aligned16(y) || !aligned16(saved) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(router_bias) & 3u))
+    return MOK_ERR_INVALID_ARG;
+  mok_saved_layout L;
+  size_t mt_off;
+  saved_layout(D, &L, &mt_off);
+  FwdWs F;
+  fwd_layout(D, &F);
+  if (saved_bytes < L.total || ws_bytes < F.total) return MOK_ERR_WORKSPACE;
+  s = check_device();
+  if (s != MOK_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  reset_launch_count();
+
+  int* status = at<int>(saved, L.status);
+  int32_t* topk_idx = at<int32_t>(saved, L.topk_idx);
+  float* topk_w = at<float>(saved, L.topk_w);
+  float* logits = at<float>(workspace, F.logits);
+  MOK_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
+  MOK_CUDA(launch_router_logits(D, x, w_router, logits, status, st));
+  MOK_CUDA(launch_router_topk(D, logits, router_bias, topk_idx, topk_w, status, st));
+
+  PlanOut o;
+  o.counts = at<int32_t>(saved, L.counts);
+  o.offsets = at<int32_t>(saved, L.offsets);
+  o.pos = at<int32_t>(saved, L.pos);
+  o.token_of_row = at<int32_t>(saved, L.token_of_row);
+  o.padded_offsets = at<int32_t>(saved, L.padded_offsets);
+  o.mtile_prefix = at<int32_t>(saved, mt_off);
+  o.ppos = at<int32_t>(saved, L.padded_pos);
+  o.ptok = at<int32_t>(saved, L.padded_token);
+  o.row_w = at<float>(saved, L.row_weight);
+  MOK_CUDA(launch_plan(D, topk_idx, topk_w, at<int32_t>(workspace, F.block_counts),
+                       at<int32_t>(workspace, F.block_base), o, status, st));
+
+  void* x_perm = at<char>(saved, L.x_perm);
+  void* gu = at<char>(saved, L.gate_up);
+  void* h = at<char>(workspace, F.h);
+  void* O = at<char>(workspace, F.o);
+  MOK_CUDA(launch_gather_rows(D, x, o.ptok, o.padded_offsets, x_perm, status, st));
+  MOK_CUDA(gemm_fwd_gate_up(D, x_perm, w_gate_up, o.mtile_prefix, o.padded_offsets, gu, h, status,
+                            st));
+  MOK_CUDA(gemm_fwd_down(D, h, w_down, o.mtile_prefix, o.padded_offsets, O, status, st));
+  MOK_CUDA(launch_combine(D, O, o.ppos, topk_w, y, st));
+  return MOK_OK;
+}
+
+mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void* x,
+                            const void* w_router, const float* router_bias,
+                            const void* w_gate_up, const void* w_down, const void* saved,
+                            size_t saved_bytes, void* dx, void* dw_router, void* dw_gate_up,
+                            void* dw_down, void* workspace, size_t ws_bytes, void* stream) {
+  (void)router_bias;
+  (void)x;
+  Dims D;
+  mok_status s = make_dims(desc, &D);
+  if (s != MOK_OK) return s;
+  const bool empty = D.T == 0;  // no token rows: dy and dx may be NULL
+  if ((!dy && !empty) || !w_router || !w_gate_up || !w_down || !saved || (!dx && !empty) ||
+      !dw_router || !dw_gate_up || !dw_down || !workspace)
+    return MOK_ERR_INVALID_ARG;
+  if (!aligned16(dy) || !aligned16(w_router) || !aligned16(w_gate_up) || !aligned16(w_down) ||
+      !aligned16(saved) || !aligned16(dx) || !aligned16(dw_router) || !aligned16(dw_gate_up) ||
+      !aligned16(dw_down) || !aligned16(workspace))
+    return MOK_ERR_INVALID_ARG;
+  mok_saved_layout L;
+  size_t mt_off;
+  saved_layout(D, &L, &mt_off);
+  BwdWs B;
+  bwd_layout(D, &B);
+  if (saved_bytes < L.total || ws_bytes < B.total) return MOK_ERR_WORKSPACE;
+  s = check_device();
+  if (s != MOK_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  // the status word lives in `saved`; the backward reports into it as well
+  int* status = const_cast<int*>(at<int>(saved, L.status));
+  const int32_t* topk_idx = at<int32_t>(saved, L.topk_idx);
+  const float* topk_w = at<float>(saved, L.topk_w);
+  const int32_t* counts = at<int32_t>(saved, L.counts);
+  const int32_t* poff = at<int32_t>(saved, L.padded_offsets);
+  const int32_t* mtp = at<int32_t>(saved, mt_off);
+  const int32_t* ppos = at<int32_t>(saved, L.padded_pos);
+  const int32_t* ptok = at<int32_t>(saved, L.padded_token);
+  const float* row_w = at<float>(saved, L.row_weight);
+  const void* x_perm = at<char>(saved, L.x_perm);
+  const void* gu = at<char>(saved, L.gate_up);
+
+  void* dy_perm = at<char>(workspace, B.dy_perm);
+  void* dgu = at<char>(workspace, B.dgu);
+  void* hp = at<char>(workspace, B.hp);
+  float* dp_part = at<float>(workspace, B.dp_part);
+  void* dx_perm = at<char>(workspace, B.dx_perm);
+  float* dl_row = at<float>(workspace, B.dl_row);
+  float* dl_tok = at<float>(workspace, B.dl_tok);
+
+  // reverse-combine: pull dy rows into expert order
+  MOK_CUDA(launch_gather_rows(D, dy, ptok, poff, dy_perm, status, st));
+  // down-projection dgrad + SwiGLU backward + router-weight partials
+  MOK_CUDA(gemm_bwd_down_dgrad(D, dy_perm, w_down, mtp, poff, gu, row_w, dgu, hp, dp_part, status,
+                               st));
+  // down-projection wgrad: dW_down_e = dY_e^T (p h)_e
+  MOK_CUDA(gemm_wgrad_down(D, dy_perm, hp, poff, dw_down, status, st));
+  // gate/up dgrad: dX_perm = dGU W_gu
+  MOK_CUDA(gemm_bwd_gate_up_dgrad(D, dgu, w_gate_up, mtp, poff, dx_perm, status, st));
+  // gate/up wgrad: dW_gu_e = dGU_e^T X_e
+  MOK_CUDA(gemm_wgrad_gate_up(D, dgu, x_perm, poff, dw_gate_up, status, st));
+  // reverse-dispatch + router backward
+  MOK_CUDA(launch_reverse_dispatch(D, dx_perm, ppos, topk_idx, topk_w, dp_part, w_router, dx,
+                                   dl_row, dl_tok, st));
+  MOK_CUDA(launch_router_wgrad(D, x_perm, dl_row, poff, counts, dw_router, st));
+  return MOK_OK;
+}
+
+mok_status mok_moe_stage_workspace_size(const mok_moe_desc* desc, size_t* bytes) {
+  if (!bytes) return MOK_ERR_INVALID_ARG;
+  Dims D;
+  mok_status s = make_dims(desc, &D);
+  if (s != MOK_OK) return s;
+  StageWs W;
+  stage_layout(D, &W);
+  *bytes = W.total;
+  return MOK_OK;
+}
+
+mok_status mok_moe_route(const mok_moe_desc* desc, const void* x, const void* w_router,
+                         const float* router_bias, int32_t* topk_idx, float* topk_w,
+                         void* workspace, size_t ws_bytes, void* stream) {
+  Dims D;
+  mok_status s = make_dims(desc, &D);
+  if (s != MOK_OK) return s;
+  if (((!x || !topk_idx || !topk_w) && D.T > 0) || !w_router || !workspace)
+    return MOK_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(workspace)) return MOK_ERR_INVALID_ARG;
+  StageWs W;
+  stage_layout(D, &W);
+  if (ws_bytes < W.total) return MOK_ERR_WORKSPACE;
+  s = check_device();
+  if (s != MOK_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* status = at<int>(workspace, W.status);
+  MOK_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
+  float* logits = at<float>(workspace, W.logits);
+  MOK_CUDA(launch_router_logits(D, x, w_router, logits, status, st));
+  MOK_CUDA(launch_router_topk(D, logits, router_bias, topk_idx, topk_w, status, st));
+  return MOK_OK;
+}
+
+mok_status mok_moe_dispatch_plan(const mok_moe_desc* desc, const int32_t* topk_idx,
+                                 int32_t* counts, int32_t* offsets, int32_t* pos,
+                                 int32_t* token_of_row, void* workspace, size_t ws_bytes,
+                                 void* stream) {
+  Dims D;
+  mok_status s = make_dims(desc, &D);
+  if (s != MOK_OK) return s;
+  if ((!topk_idx && D.T > 0) || !counts || !offsets || (!pos && D.T > 0) ||
+      (!token_of_row && D.T > 0) || !workspace)
+    return MOK_ERR_INVALID_ARG;
+  if (!aligned16(workspace)) return MOK_ERR_INVALID_ARG;
+  StageWs W;
+  stage_layout(D, &W);
+  if (ws_bytes < W.total) return MOK_ERR_WORKSPACE;
+  s = check_device();
+  if (s != MOK_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* status = at<int>(workspace, W.status);
+  MOK_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
+  // slots skipped as invalid keep pos = -1; rows they would have taken stay
+  // unwritten, so pre-set the inverse map to -1
+  if (D.R > 0) MOK_CUDA(cudaMemsetAsync(token_of_row, 0xFF, static_cast<size_t>(D.R) * 4, st));
+  PlanOut o;
+  o.counts = counts;
+  o.offsets = offsets;
+  o.pos = pos;
+  o.token_of_row = token_of_row;
+  o.padded_offsets = at<int32_t>(workspace, W.padded_offsets);
+  o.mtile_prefix = at<int32_t>(workspace, W.mtile_prefix);
+  o.ppos = at<int32_t>(workspace, W.ppos);
+  o.ptok = at<int32_t>(workspace, W.ptok);
+  o.row_w = nullptr;
+  MOK_CUDA(launch_plan(D, topk_idx, nullptr, at<int32_t>(workspace, W.block_counts),
+                       at<int32_t>(workspace, W.block_base), o, status, st));
+  return MOK_OK;
+}
+
+mok_status mok_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int a_mn_major,
+                         const void* B, int b_mn_major, void* C, void* workspace,
+                         size_t ws_bytes, void* stream) {
+  if (M <= 0 || N <= 0 || K <= 0 || !A || !B || !C || !workspace) return MOK_ERR_INVALID_ARG;
+  if (M % 128 || N % 128 || K % 128) return MOK_ERR_UNSUPPORTED;
+  if (M > (1 << 24) || N > (1 << 24) || K > (1 << 24)) return MOK_ERR_UNSUPPORTED;
+  if (a_mn_major && !b_mn_major) return MOK_ERR_UNSUPPORTED;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C) || !aligned16(workspace))
+    return MOK_ERR_INVALID_ARG;
+  if (ws_bytes < 256) return MOK_ERR_WORKSPACE;
+  mok_status s = check_device();
+  if (s != MOK_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* status = static_cast<int*>(workspace);
+  MOK_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
+  MOK_CUDA(gemm_dense_bf16(M, N, K, A, a_mn_major != 0, B, b_mn_major != 0, C, status, st));
+  return MOK_OK;
+}
+
+mok_status mok_get_device_status(const void* buf, void* stream, int32_t* code) {
+  if (!buf || !code) return MOK_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOK_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, buf, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return MOK_ERR_CUDA;
+  *code = v;
+  return MOK_OK;
+}
+
+const char* mok_status_string(mok_status status) {
+  switch (status) {
+    case MOK_OK: return "ok";
+    case MOK_ERR_INVALID_ARG: return "invalid argument";
+    case MOK_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case MOK_ERR_WORKSPACE: return "buffer smaller than the size query";
+    case MOK_ERR_CUDA: return "CUDA runtime error";
+    case MOK_ERR_NO_DEVICE: return "current device is not sm_103";
+    case MOK_ERR_DEVICE_NONFINITE: return "device: NaN router logit (treated as -inf)";
+    case MOK_ERR_DEVICE_INDEX: return "device: expert index out of range or repeated (skipped)";
+    case MOK_ERR_DEVICE_TIMEOUT: return "device: bounded wait timed out (results invalid)";
+  }
+  return "unknown status";
+}
+
+int32_t mok_last_launch_count(void) { return launch_count(); }
+
+mok_status mok_profile_enable(int on) {
+  g_prof = on != 0;
+  return MOK_OK;
+}
+
+mok_status mok_profile_reset(void) {
+  g_recs.clear();
+  g_pool_used = 0;
+  return MOK_OK;
+}
+
+mok_status mok_profile_collect(mok_kernel_time* out, int32_t max, int32_t* n) {
+  if (!n || (max > 0 && !out)) return MOK_ERR_INVALID_ARG;
+  std::map<std::string, std::pair<int32_t, double>> agg;
+  std::vector<std::string> order;
+  for (const ProfRec& r : g_recs) {
+    if (cudaEventSynchronize(r.b) != cudaSuccess) return MOK_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) return MOK_ERR_CUDA;
+    auto it = agg.find(r.name);
+    if (it == agg.end()) {
+      order.push_back(r.name);
+      agg[r.name] = {1, ms};
+    } else {
+      it->second.first += 1;
+      it->second.second += ms;
+    }
+  }
+  int32_t i = 0;
+  for (const std::string& name : order) {
+    if (i >= max) break;
+    memset(out[i].name, 0, sizeof(out[i].name));
+    strncpy(out[i].name, name.c_str(), sizeof(out[i].name) - 1);
+    out[i].launches = agg[name].first;
+    out[i].total_ms = agg[name].second;
+    ++i;
+  }
+  *n = i;
+  return MOK_OK;
+}
+
+}  // extern "C"

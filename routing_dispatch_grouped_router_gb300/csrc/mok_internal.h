@@ -1,0 +1,129 @@
+// Host-side internals shared by the translation units of libmok: buffer
+// layouts, launch helpers of every kernel, and error plumbing.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/mok.h"
+
+namespace mok {
+
+constexpr int kRowPad = 128;     // expert segments are padded to this many rows
+constexpr int kMaxExperts = 512;
+constexpr int kMaxTopK = 8;
+constexpr int kPlanBlock = 256;  // tokens per block of the dispatch plan
+
+// Sizes derived from a descriptor.
+struct Dims {
+  int64_t T, d, E, I;
+  int k;
+  int64_t R;         // T*k routed rows
+  int64_t rows_max;  // bound on padded rows: R + 127*min(E,R), rounded up to 128
+  int64_t nb;        // dispatch-plan blocks: ceil(T / kPlanBlock)
+  int bn_dgrad;      // N tile of the down-projection dgrad (over I)
+  int np;            // dp partials per row = (I / bn_dgrad) * 2
+};
+
+struct FwdWs {
+  size_t block_counts, block_base, h, o, logits, total;
+};
+struct BwdWs {
+  size_t dy_perm, dgu, hp, dp_part, dx_perm, dl_row, dl_tok, total;
+};
+struct StageWs {
+  size_t status, block_counts, block_base, padded_offsets, mtile_prefix, ppos, ptok, row_w,
+      logits, total;
+};
+
+mok_status make_dims(const mok_moe_desc* desc, Dims* out);
+void saved_layout(const Dims& D, mok_saved_layout* L, size_t* mtile_prefix_off);
+void fwd_layout(const Dims& D, FwdWs* W);
+void bwd_layout(const Dims& D, BwdWs* W);
+void stage_layout(const Dims& D, StageWs* W);
+
+int num_sms_current_device();
+
+// ------------------------------------------------------------------ kernels --
+
+// Router: logits through the GEMM engine, then top-k + softmax per token.
+cudaError_t launch_router_logits(const Dims& D, const void* x, const void* w_router, float* logits,
+                                 int* status, cudaStream_t st);
+cudaError_t launch_router_topk(const Dims& D, const float* logits, const float* bias,
+                               int32_t* topk_idx, float* topk_w, int* status, cudaStream_t st);
+
+// Dispatch plan: histogram, scan, stable placement.
+struct PlanOut {
+  int32_t* counts;          // [E]
+  int32_t* offsets;         // [E+1]
+  int32_t* pos;             // [T,k] (may be null)
+  int32_t* token_of_row;    // [R] (may be null)
+  int32_t* padded_offsets;  // [E+1]
+  int32_t* mtile_prefix;    // [E+1]
+  int32_t* ppos;            // [T,k]
+  int32_t* ptok;            // [rows_max]
+  float* row_w;             // [rows_max] (may be null)
+};
+cudaError_t launch_plan(const Dims& D, const int32_t* topk_idx, const float* topk_w,
+                        int32_t* block_counts, int32_t* block_base, const PlanOut& o, int* status,
+                        cudaStream_t st);
+
+// dst[r] = src[ptok[r]] (or zeros where ptok[r] < 0), rows [0, padded_offsets[E]).
+cudaError_t launch_gather_rows(const Dims& D, const void* src, const int32_t* ptok,
+                               const int32_t* padded_offsets, void* dst, int* status,
+                               cudaStream_t st);
+
+// y_t = sum_s p[t,s] O[ppos[t,s]].
+cudaError_t launch_combine(const Dims& D, const void* O, const int32_t* ppos, const float* topk_w,
+                           void* y, cudaStream_t st);
+
+// dl (router logit grad) from dp partials; dx_t = sum_s dX[ppos] + dl W_r[e].
+cudaError_t launch_reverse_dispatch(const Dims& D, const void* dX_perm, const int32_t* ppos,
+                                    const int32_t* topk_idx, const float* topk_w,
+                                    const float* dp_part, const void* w_router, void* dx,
+                                    float* dl_row, float* dl_tok, cudaStream_t st);
+
+// dW_r[e] = sum over rows of e of dl_row[r] * X_perm[r].
+cudaError_t launch_router_wgrad(const Dims& D, const void* X_perm, const float* dl_row,
+                                const int32_t* padded_offsets, const int32_t* counts,
+                                void* dw_router, cudaStream_t st);
+
+// Grouped GEMMs on tcgen05 (see gemm.cu).
+cudaError_t gemm_fwd_gate_up(const Dims& D, const void* X_perm, const void* w_gate_up,
+                             const int32_t* mtile_prefix, const int32_t* poff, void* GU, void* H,
+                             int* status, cudaStream_t st);
+cudaError_t gemm_fwd_down(const Dims& D, const void* H, const void* w_down,
+                          const int32_t* mtile_prefix, const int32_t* poff, void* O, int* status,
+                          cudaStream_t st);
+cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* w_down,
+                                const int32_t* mtile_prefix, const int32_t* poff, const void* GU,
+                                const float* row_w, void* dGU, void* HP, float* dp_part,
+                                int* status, cudaStream_t st);
+cudaError_t gemm_bwd_gate_up_dgrad(const Dims& D, const void* dGU, const void* w_gate_up,
+                                   const int32_t* mtile_prefix, const int32_t* poff,
+                                   void* dX_perm, int* status, cudaStream_t st);
+cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* HP,
+                            const int32_t* poff, void* dw_down, int* status, cudaStream_t st);
+cudaError_t gemm_wgrad_gate_up(const Dims& D, const void* dGU, const void* X_perm,
+                               const int32_t* poff, void* dw_gate_up, int* status,
+                               cudaStream_t st);
+cudaError_t gemm_dense_bf16(int64_t M, int64_t N, int64_t K, const void* A, bool a_mn,
+                            const void* B, bool b_mn, void* C, int* status, cudaStream_t st);
+
+// launches counter (host side)
+void count_launch(int n = 1);
+void reset_launch_count();
+int32_t launch_count();
+
+// Per-kernel CUDA-event timing (enabled through mok_profile_enable): the
+// scope records an event before and after the kernel it encloses.
+void prof_begin(const char* name, cudaStream_t st);
+void prof_end(cudaStream_t st);
+struct ProfScope {
+  cudaStream_t st;
+  ProfScope(const char* name, cudaStream_t s) : st(s) { prof_begin(name, s); }
+  ~ProfScope() { prof_end(st); }
+};
+
+}  // namespace mok

@@ -1,0 +1,566 @@
+// Router top-k, dispatch plan, row gather (dispatch / reverse-combine),
+// combine, reverse-dispatch with the router backward, router weight grad.
+//
+// Sources (page title, section):
+//   [gtnt] "MoK揭秘：NVL72上大规模MoE训练工程方案深度解读", §1.1: a gating
+//     network (router) picks the best few experts for every token.
+//   [dothoosh] "Cursor Mixture-of-Kittens cuts MoE training latency by 5.8x",
+//     "MoK technical details", bullet "Hybrid communication": forward =
+//     dispatch (pulled by the receiver) then combine; backward =
+//     reverse-combine (pulled) then reverse-dispatch; bullet "Ring buffer
+//     logic": no token is dropped and no buffer is sized by the CPU.
+//   [aikraft] "Cursor MoK: revolution in MoE model training on NVL72", §03:
+//     the CPU is kept off the critical path (no host synchronisation).
+//
+// Every kernel here is deterministic: integer atomics only where their order
+// cannot change the result (counts, bit sets), and every floating-point sum
+// runs in a fixed order.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "mok_internal.h"
+#include "ptx.cuh"
+
+namespace mok {
+
+// ------------------------------------------------------------------ router --
+
+// One warp per token: add the bias, pick the k largest logits (exact ties to
+// the lower expert index; NaN counts as -inf and is reported), softmax over
+// the chosen k.  Slots come out in descending logit order.
+__global__ void router_topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
+                                   int T, int E, int k, int32_t* __restrict__ topk_idx,
+                                   float* __restrict__ topk_w, int* status) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= T) return;
+  constexpr int PER = kMaxExperts / 32;  // 16
+  float v[PER];
+  bool nan_seen = false;
+  const float* row = logits + static_cast<long long>(warp) * E;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int e = j * 32 + lane;
+    float x = -INFINITY;
+    if (e < E) {
+      x = row[e];
+      if (bias) x += bias[e];
+      if (x != x) {
+        nan_seen = true;
+        x = -INFINITY;
+      }
+    }
+    v[j] = x;
+  }
+  if (__any_sync(0xffffffffu, nan_seen) && lane == 0) set_status(status, MOK_ERR_DEVICE_NONFINITE);
+  float sel_v[kMaxTopK];
+  int sel_e[kMaxTopK];
+  for (int s = 0; s < k; ++s) {
+    // best of this lane: experts are visited in increasing index order, so a
+    // strict '>' keeps the lower index on equal values
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int e = j * 32 + lane;
+      if (e < E && (v[j] > bv || (v[j] == bv && e < be))) {
+        bv = v[j];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    sel_v[s] = bv;
+    sel_e[s] = be;
+    // remove the winner
+#pragma unroll
+    for (int j = 0; j < PER; ++j)
+      if (j * 32 + lane == be) v[j] = NAN;  // NaN never wins a comparison
+  }
+  if (lane == 0) {
+    const float m = sel_v[0];
+    float den = 0.f;
+    float ex[kMaxTopK];
+    for (int s = 0; s < k; ++s) {
+      ex[s] = (sel_v[s] == -INFINITY) ? (m == -INFINITY ? 1.f : 0.f) : expf(sel_v[s] - m);
+      den += ex[s];
+    }
+    const float inv = 1.0f / den;
+    for (int s = 0; s < k; ++s) {
+      topk_idx[static_cast<long long>(warp) * k + s] = sel_e[s];
+      topk_w[static_cast<long long>(warp) * k + s] = ex[s] * inv;
+    }
+  }
+}
+
+cudaError_t launch_router_topk(const Dims& D, const float* logits, const float* bias,
+                               int32_t* topk_idx, float* topk_w, int* status, cudaStream_t st) {
+  if (D.T == 0) return cudaSuccess;
+  const int threads = 256;
+  const long long blocks = (D.T * 32 + threads - 1) / threads;
+  ProfScope prof("router_topk", st);
+  router_topk_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
+      logits, bias, static_cast<int>(D.T), static_cast<int>(D.E), D.k, topk_idx, topk_w, status);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------- dispatch plan --
+
+// A slot is valid when its expert is in range and not repeated earlier in
+// the same token (a router never repeats; a caller's table might).
+__device__ __forceinline__ bool slot_valid(const int32_t* idx_row, int s, int E) {
+  const int e = idx_row[s];
+  if (e < 0 || e >= E) return false;
+  for (int j = 0; j < s; ++j)
+    if (idx_row[j] == e) return false;
+  return true;
+}
+
+__global__ void plan_hist_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
+                                 int32_t* __restrict__ block_counts, int* status) {
+  __shared__ int cnt[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  const int t = blockIdx.x * kPlanBlock + threadIdx.x;
+  if (t < T) {
+    const int32_t* row = topk_idx + static_cast<long long>(t) * k;
+    bool bad = false;
+    for (int s = 0; s < k; ++s) {
+      if (slot_valid(row, s, E)) atomicAdd(&cnt[row[s]], 1);
+      else bad = true;
+    }
+    if (bad) set_status(status, MOK_ERR_DEVICE_INDEX);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    block_counts[static_cast<long long>(blockIdx.x) * E + e] = cnt[e];
+}
+
+// One CTA: per-expert totals and per-(block, expert) bases, then the
+// exclusive scans (plain and padded to 128 rows), the 128-row tile prefix,
+// and the padding rows of every expert segment (token -1, weight 0).
+__global__ void plan_scan_kernel(const int32_t* __restrict__ block_counts, int nb, int E,
+                                 int32_t* __restrict__ block_base, int32_t* __restrict__ counts,
+                                 int32_t* __restrict__ offsets, int32_t* __restrict__ poff,
+                                 int32_t* __restrict__ mtile_prefix, int32_t* __restrict__ ptok,
+                                 float* __restrict__ row_w) {
+  __shared__ int s_cnt[kMaxExperts];
+  __shared__ int s_off[kMaxExperts + 1];
+  __shared__ int s_poff[kMaxExperts + 1];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int b = 0; b < nb; ++b) {
+      block_base[static_cast<long long>(b) * E + e] = run;
+      run += block_counts[static_cast<long long>(b) * E + e];
+    }
+    s_cnt[e] = run;
+    counts[e] = run;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    // warp scan: lane owns experts [lane*PER, lane*PER+PER)
+    const int lane = threadIdx.x;
+    constexpr int PER = kMaxExperts / 32;
+    int sum = 0, psum = 0;
+    for (int j = 0; j < PER; ++j) {
+      const int e = lane * PER + j;
+      if (e < E) {
+        sum += s_cnt[e];
+        psum += (s_cnt[e] + kRowPad - 1) / kRowPad * kRowPad;
+      }
+    }
+    int incl = sum, pincl = psum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, incl, off);
+      const int b = __shfl_up_sync(0xffffffffu, pincl, off);
+      if (lane >= off) {
+        incl += a;
+        pincl += b;
+      }
+    }
+    int run = incl - sum, prun = pincl - psum;
+    for (int j = 0; j < PER; ++j) {
+      const int e = lane * PER + j;
+      if (e < E) {
+        s_off[e] = run;
+        s_poff[e] = prun;
+        run += s_cnt[e];
+        prun += (s_cnt[e] + kRowPad - 1) / kRowPad * kRowPad;
+      }
+    }
+    if (lane == 31) {
+      s_off[E] = run;
+      s_poff[E] = prun;
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    offsets[e] = s_off[e];
+    poff[e] = s_poff[e];
+    mtile_prefix[e] = s_poff[e] / kRowPad;
+  }
+  // padding rows of each expert segment
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  for (int e = warp; e < E; e += nw) {
+    const int a = s_poff[e] + s_cnt[e], b = s_poff[e + 1];
+    for (int r = a + lane; r < b; r += 32) {
+      ptok[r] = -1;
+      if (row_w) row_w[r] = 0.f;
+    }
+  }
+}
+
+// Stable placement: the rank of token t among the tokens of its block routed
+// to the same expert is the number of set bits below t in that expert's
+// 256-bit membership mask.
+__global__ void plan_place_kernel(const int32_t* __restrict__ topk_idx,
+                                  const float* __restrict__ topk_w, int T, int E, int k,
+                                  const int32_t* __restrict__ block_base,
+                                  const int32_t* __restrict__ offsets,
+                                  const int32_t* __restrict__ poff, int32_t* __restrict__ pos,
+                                  int32_t* __restrict__ token_of_row, int32_t* __restrict__ ppos,
+                                  int32_t* __restrict__ ptok, float* __restrict__ row_w) {
+  constexpr int W = kPlanBlock / 32;  // 8 mask words per expert
+  __shared__ uint32_t mask[kMaxExperts * W];
+  for (int i = threadIdx.x; i < E * W; i += blockDim.x) mask[i] = 0u;
+  __syncthreads();
+  const int t = blockIdx.x * kPlanBlock + threadIdx.x;
+  const int word = threadIdx.x >> 5, bit = threadIdx.x & 31;
+  const int32_t* row = topk_idx + static_cast<long long>(t) * k;
+  if (t < T) {
+    for (int s = 0; s < k; ++s)
+      if (slot_valid(row, s, E)) atomicOr(&mask[row[s] * W + word], 1u << bit);
+  }
+  __syncthreads();
+  if (t >= T) return;
+  for (int s = 0; s < k; ++s) {
+    const long long ts = static_cast<long long>(t) * k + s;
+    if (!slot_valid(row, s, E)) {
+      if (pos) pos[ts] = -1;
+      ppos[ts] = -1;
+      continue;
+    }
+    const int e = row[s];
+    int rank = __popc(mask[e * W + word] & ((1u << bit) - 1u));
+    for (int w = 0; w < word; ++w) rank += __popc(mask[e * W + w]);
+    const int base = block_base[static_cast<long long>(blockIdx.x) * E + e] + rank;
+    const int p = offsets[e] + base;
+    const int pp = poff[e] + base;
+    if (pos) pos[ts] = p;
+    if (token_of_row) token_of_row[p] = t;
+    ppos[ts] = pp;
+    ptok[pp] = t;
+    if (row_w) row_w[pp] = topk_w[ts];
+  }
+}
+
+cudaError_t launch_plan(const Dims& D, const int32_t* topk_idx, const float* topk_w,
+                        int32_t* block_counts, int32_t* block_base, const PlanOut& o, int* status,
+                        cudaStream_t st) {
+  const int nb = static_cast<int>(D.nb);
+  const int E = static_cast<int>(D.E), T = static_cast<int>(D.T);
+  if (nb > 0) {
+    ProfScope prof("plan_hist", st);
+    plan_hist_kernel<<<nb, kPlanBlock, 0, st>>>(topk_idx, T, E, D.k, block_counts, status);
+    count_launch();
+  }
+  {
+    ProfScope prof("plan_scan", st);
+    plan_scan_kernel<<<1, 1024, 0, st>>>(block_counts, nb, E, block_base, o.counts, o.offsets,
+                                         o.padded_offsets, o.mtile_prefix, o.ptok, o.row_w);
+    count_launch();
+  }
+  if (nb > 0) {
+    ProfScope prof("plan_place", st);
+    plan_place_kernel<<<nb, kPlanBlock, 0, st>>>(topk_idx, topk_w, T, E, D.k, block_base,
+                                                 o.offsets, o.padded_offsets, o.pos,
+                                                 o.token_of_row, o.ppos, o.ptok, o.row_w);
+    count_launch();
+  }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------- row gather --
+
+// Destination-driven ("pull") gather staged through TMA: for every padded row
+// r < padded_offsets[E], one thread moves src[ptok[r]] global -> shared with
+// a bulk copy completing on an mbarrier, then shared -> global with a bulk
+// store.  Padding rows are stored from a zeroed slot.  NSLOT copies are in
+// flight per CTA.
+constexpr int kGatherSlots = 4;
+constexpr int kGatherCtasPerSm = 4;
+
+__global__ void __launch_bounds__(32) gather_rows_kernel(const uint8_t* __restrict__ src,
+                                                         const int32_t* __restrict__ ptok,
+                                                         const int32_t* __restrict__ poff_end,
+                                                         int T, uint32_t row_bytes,
+                                                         uint8_t* __restrict__ dst, int* status) {
+  extern __shared__ __align__(128) uint8_t gsm[];
+  __shared__ __align__(8) uint64_t full[kGatherSlots];
+  uint8_t* zero_slot = gsm + kGatherSlots * row_bytes;
+  const int lane = threadIdx.x;
+  const long long P = *poff_end;  // padded rows in use
+  const long long G = gridDim.x;
+  const long long first = blockIdx.x;
+  const long long n_my = (P > first) ? (P - first + G - 1) / G : 0;
+  for (uint32_t i = lane * 16; i < row_bytes; i += 32 * 16)
+    *reinterpret_cast<uint4*>(zero_slot + i) = make_uint4(0, 0, 0, 0);
+  if (lane == 0) {
+    for (int s = 0; s < kGatherSlots; ++s) mbar_init(&full[s], 1);
+    fence_barrier_init();
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane != 0 || n_my == 0) return;
+
+  auto row_of = [&](long long j) { return first + j * G; };
+  auto issue = [&](long long j) {
+    const int s = static_cast<int>(j % kGatherSlots);
+    const int t = ptok[row_of(j)];
+    if (t >= 0 && t < T) {
+      mbar_arrive_expect_tx(&full[s], row_bytes);
+      bulk_load(gsm + s * row_bytes, src + static_cast<long long>(t) * row_bytes, row_bytes,
+                &full[s]);
+    } else {
+      mbar_arrive(&full[s]);
+    }
+  };
+  const long long pro = n_my < kGatherSlots ? n_my : kGatherSlots;
+  for (long long j = 0; j < pro; ++j) issue(j);
+  const int never = 0;
+  for (long long j = 0; j < n_my; ++j) {
+    const int s = static_cast<int>(j % kGatherSlots);
+    const uint32_t par = static_cast<uint32_t>((j / kGatherSlots) & 1);
+    if (!mbar_wait(&full[s], par, &never)) set_status(status, MOK_ERR_DEVICE_TIMEOUT);
+    const long long r = row_of(j);
+    const int t = ptok[r];
+    const uint8_t* from = (t >= 0 && t < T) ? gsm + s * row_bytes : zero_slot;
+    bulk_store(dst + r * row_bytes, from, row_bytes);
+    bulk_commit();
+    if (j + kGatherSlots < n_my) {
+      bulk_wait_read<0>();  // slot s has been read out
+      issue(j + kGatherSlots);
+    }
+  }
+  bulk_wait_all<0>();
+}
+
+cudaError_t launch_gather_rows(const Dims& D, const void* src, const int32_t* ptok,
+                               const int32_t* padded_offsets, void* dst, int* status,
+                               cudaStream_t st) {
+  if (D.T == 0) return cudaSuccess;
+  const uint32_t row_bytes = static_cast<uint32_t>(D.d * 2);
+  const int smem = static_cast<int>((kGatherSlots + 1) * row_bytes);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(gather_rows_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (kGatherSlots + 1) * 16384 * 2);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  long long grid = static_cast<long long>(num_sms_current_device()) * kGatherCtasPerSm;
+  const long long rows_cap = D.rows_max;
+  if (grid > rows_cap) grid = rows_cap;
+  ProfScope prof("gather_rows", st);
+  gather_rows_kernel<<<static_cast<unsigned>(grid), 32, smem, st>>>(
+      static_cast<const uint8_t*>(src), ptok, padded_offsets + D.E, static_cast<int>(D.T),
+      row_bytes, static_cast<uint8_t*>(dst), status);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------- combine --
+
+__device__ __forceinline__ void axpy8(float (&acc)[8], float w, uint4 v) {
+  acc[0] = fmaf(w, bf16lo(v.x), acc[0]); acc[1] = fmaf(w, bf16hi(v.x), acc[1]);
+  acc[2] = fmaf(w, bf16lo(v.y), acc[2]); acc[3] = fmaf(w, bf16hi(v.y), acc[3]);
+  acc[4] = fmaf(w, bf16lo(v.z), acc[4]); acc[5] = fmaf(w, bf16hi(v.z), acc[5]);
+  acc[6] = fmaf(w, bf16lo(v.w), acc[6]); acc[7] = fmaf(w, bf16hi(v.w), acc[7]);
+}
+
+__device__ __forceinline__ void add8(float (&acc)[8], uint4 v) {
+  acc[0] += bf16lo(v.x); acc[1] += bf16hi(v.x); acc[2] += bf16lo(v.y); acc[3] += bf16hi(v.y);
+  acc[4] += bf16lo(v.z); acc[5] += bf16hi(v.z); acc[6] += bf16lo(v.w); acc[7] += bf16hi(v.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&a)[8]) {
+  return make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                    pack_bf16x2(a[6], a[7]));
+}
+
+// One CTA per token: y_t = sum_{s=0..k-1} p[t,s] * O[ppos[t,s]], fp32 in slot order.
+__global__ void combine_kernel(const uint4* __restrict__ O, const int32_t* __restrict__ ppos,
+                               const float* __restrict__ topk_w, int k, int dv,
+                               uint4* __restrict__ y) {
+  __shared__ int s_row[kMaxTopK];
+  __shared__ float s_w[kMaxTopK];
+  const long long t = blockIdx.x;
+  if (threadIdx.x < k) {
+    s_row[threadIdx.x] = ppos[t * k + threadIdx.x];
+    s_w[threadIdx.x] = topk_w[t * k + threadIdx.x];
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < dv; c += blockDim.x) {
+    uint4 v[kMaxTopK];
+#pragma unroll
+    for (int s = 0; s < kMaxTopK; ++s)
+      if (s < k && s_row[s] >= 0) v[s] = ld_global_nc_v4(O + static_cast<long long>(s_row[s]) * dv + c);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int s = 0; s < kMaxTopK; ++s)
+      if (s < k && s_row[s] >= 0) axpy8(acc, s_w[s], v[s]);
+    y[t * dv + c] = pack8(acc);
+  }
+}
+
+static int row_threads(int dv) {
+  int th = dv < 256 ? dv : 256;
+  th = (th + 31) / 32 * 32;
+  return th;
+}
+
+cudaError_t launch_combine(const Dims& D, const void* O, const int32_t* ppos, const float* topk_w,
+                           void* y, cudaStream_t st) {
+  if (D.T == 0) return cudaSuccess;
+  const int dv = static_cast<int>(D.d / 8);
+  ProfScope prof("combine", st);
+  combine_kernel<<<static_cast<unsigned>(D.T), row_threads(dv), 0, st>>>(
+      static_cast<const uint4*>(O), ppos, topk_w, D.k, dv, static_cast<uint4*>(y));
+  count_launch();
+  return cudaGetLastError();
+}
+
+// -------------------------------------------------------- reverse dispatch --
+
+// One CTA per token.  Router backward first:
+//   dp_s = sum_j dp_part[row_s, j]      (fixed j order)
+//   dl_s = p_s (dp_s - sum_i p_i dp_i)  (softmax over the chosen k)
+// then dx_t = sum_s (dX_perm[row_s] + dl_s * W_r[e_s])   in slot order.
+__global__ void reverse_dispatch_kernel(const uint4* __restrict__ dXp,
+                                        const int32_t* __restrict__ ppos,
+                                        const int32_t* __restrict__ topk_idx,
+                                        const float* __restrict__ topk_w,
+                                        const float* __restrict__ dp_part, int np,
+                                        const uint4* __restrict__ Wr, int k, int dv,
+                                        uint4* __restrict__ dx, float* __restrict__ dl_row,
+                                        float* __restrict__ dl_tok) {
+  __shared__ int s_row[kMaxTopK];
+  __shared__ int s_e[kMaxTopK];
+  __shared__ float s_dl[kMaxTopK];
+  const long long t = blockIdx.x;
+  if (threadIdx.x < 32) {
+    const int s = threadIdx.x;
+    int row = -1, e = 0;
+    float p = 0.f, dp = 0.f;
+    if (s < k) {
+      row = ppos[t * k + s];
+      e = topk_idx[t * k + s];
+      p = topk_w[t * k + s];
+      if (row >= 0) {
+        const float* q = dp_part + static_cast<long long>(row) * np;
+        for (int j = 0; j < np; ++j) dp += q[j];
+      }
+    }
+    // c = sum_i p_i dp_i, summed in slot order by every lane
+    float c = 0.f;
+    for (int i = 0; i < kMaxTopK; ++i) {
+      const float pi = __shfl_sync(0xffffffffu, p, i);
+      const float di = __shfl_sync(0xffffffffu, dp, i);
+      if (i < k) c = fmaf(pi, di, c);
+    }
+    if (s < k) {
+      const float dl = (row >= 0) ? p * (dp - c) : 0.f;
+      s_row[s] = row;
+      s_e[s] = e;
+      s_dl[s] = dl;
+      dl_tok[t * k + s] = dl;
+      if (row >= 0) dl_row[row] = dl;
+    }
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < dv; c += blockDim.x) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < k; ++s) {
+      if (s_row[s] < 0) continue;
+      add8(acc, ld_global_nc_v4(dXp + static_cast<long long>(s_row[s]) * dv + c));
+      axpy8(acc, s_dl[s], ld_global_nc_v4(Wr + static_cast<long long>(s_e[s]) * dv + c));
+    }
+    dx[t * dv + c] = pack8(acc);
+  }
+}
+
+cudaError_t launch_reverse_dispatch(const Dims& D, const void* dX_perm, const int32_t* ppos,
+                                    const int32_t* topk_idx, const float* topk_w,
+                                    const float* dp_part, const void* w_router, void* dx,
+                                    float* dl_row, float* dl_tok, cudaStream_t st) {
+  if (D.T == 0) return cudaSuccess;
+  const int dv = static_cast<int>(D.d / 8);
+  int th = row_threads(dv);
+  if (th < 32) th = 32;
+  ProfScope prof("reverse_dispatch", st);
+  reverse_dispatch_kernel<<<static_cast<unsigned>(D.T), th, 0, st>>>(
+      static_cast<const uint4*>(dX_perm), ppos, topk_idx, topk_w, dp_part, D.np,
+      static_cast<const uint4*>(w_router), D.k, dv, static_cast<uint4*>(dx), dl_row, dl_tok);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------ router weight grad --
+
+// dW_r[e, :] = sum over the real rows r of expert e of dl_row[r] * X_perm[r, :].
+// CTA (e, 64-column block): 32 row lanes x 8 column threads (8 columns each);
+// row lane i takes rows i, i+32, ...; the 32 partials are then added in lane
+// order.  Fixed order throughout.
+constexpr int kRwRowLanes = 32;
+__global__ void router_wgrad_kernel(const uint4* __restrict__ Xp, const float* __restrict__ dl_row,
+                                    const int32_t* __restrict__ poff,
+                                    const int32_t* __restrict__ counts, int dv,
+                                    uint4* __restrict__ dw) {
+  __shared__ float part[kRwRowLanes][8][8];
+  const int e = blockIdx.x;
+  const int cv = blockIdx.y * 8 + (threadIdx.x & 7);  // column vector index
+  const int lane_r = threadIdx.x >> 3;
+  const int r0 = poff[e], n = counts[e];
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (cv < dv) {
+    for (int i = lane_r; i < n; i += kRwRowLanes) {
+      const long long r = r0 + i;
+      axpy8(acc, dl_row[r], ld_global_nc_v4(Xp + r * dv + cv));
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) part[lane_r][threadIdx.x & 7][j] = acc[j];
+  __syncthreads();
+  if (threadIdx.x < 8 && cv < dv) {
+    float tot[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int l = 0; l < kRwRowLanes; ++l)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) tot[j] += part[l][threadIdx.x][j];
+    dw[static_cast<long long>(e) * dv + cv] = pack8(tot);
+  }
+}
+
+cudaError_t launch_router_wgrad(const Dims& D, const void* X_perm, const float* dl_row,
+                                const int32_t* padded_offsets, const int32_t* counts,
+                                void* dw_router, cudaStream_t st) {
+  const int dv = static_cast<int>(D.d / 8);
+  dim3 grid(static_cast<unsigned>(D.E), static_cast<unsigned>((dv + 7) / 8));
+  ProfScope prof("router_wgrad", st);
+  router_wgrad_kernel<<<grid, kRwRowLanes * 8, 0, st>>>(static_cast<const uint4*>(X_perm), dl_row,
+                                                        padded_offsets, counts, dv,
+                                                        static_cast<uint4*>(dw_router));
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace mok

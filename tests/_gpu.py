@@ -1,0 +1,149 @@
+"""Helpers of the GPU tests: device copies of the seeded inputs, one layer
+call through the C ABI, and the comparisons against the oracle.
+
+The oracle always computes from the same seeded inputs, never from anything
+the CUDA path produced; where float32 logits make routing undecidable
+(near-ties flagged by the oracle) the affected tokens/experts are left out.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from routing_dispatch_grouped_router_gb300 import api, inputs as gen
+
+BF16_TOL = 2e-2
+
+
+def dev_bf16(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def host64(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def rel_err(got, ref) -> float:
+    ref = np.asarray(ref, dtype=np.float64)
+    got = np.asarray(got, dtype=np.float64)
+    rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
+    if ref.size == 0:
+        return 0.0
+    diff = float(np.max(np.abs(got - ref)))
+    if rms == 0.0:
+        return diff
+    return diff / rms
+
+
+def run_gpu(shape: gen.Shape, inp: dict, layer=None):
+    """Forward + backward of one layer call; returns host copies."""
+    if layer is None:
+        layer = api.MoELayer(shape.T, shape.d, shape.E, shape.I, shape.k)
+    x = dev_bf16(inp["x"])
+    wr = dev_bf16(inp["w_router"])
+    wgu = dev_bf16(inp["w_gate_up"])
+    wd = dev_bf16(inp["w_down"])
+    dy = dev_bf16(inp["dy"])
+    bias = torch.from_numpy(inp["bias"]).cuda() if inp.get("bias") is not None else None
+    y = layer.forward(x, wr, bias, wgu, wd)
+    dx, dwr, dwgu, dwd = layer.backward(dy, x, wr, bias, wgu, wd)
+    status = layer.status()
+    T, k, E = shape.T, shape.k, shape.E
+    L = layer.layout
+    out = dict(
+        status=status,
+        y=y, dx=dx, dw_router=dwr, dw_gate_up=dwgu, dw_down=dwd,
+        topk_idx=layer.saved_tensor("topk_idx", torch.int32, (T, k)).cpu().numpy(),
+        topk_w=layer.saved_tensor("topk_w", torch.float32, (T, k)).cpu().numpy(),
+        counts=layer.saved_tensor("counts", torch.int32, (E,)).cpu().numpy(),
+        offsets=layer.saved_tensor("offsets", torch.int32, (E + 1,)).cpu().numpy(),
+        pos=layer.saved_tensor("pos", torch.int32, (T, k)).cpu().numpy(),
+        token_of_row=layer.saved_tensor("token_of_row", torch.int32, (T * k,)).cpu().numpy(),
+        padded_offsets=layer.saved_tensor("padded_offsets", torch.int32, (E + 1,)).cpu().numpy(),
+        padded_pos=layer.saved_tensor("padded_pos", torch.int32, (T, k)).cpu().numpy(),
+        gate_up=layer.saved_tensor("gate_up", torch.bfloat16, (L.rows_max, 2 * shape.I)),
+        layer=layer,
+    )
+    return out
+
+
+def check_routing(gpu_idx, gpu_w, ref_idx, ref_w, flagged, inner_tie):
+    """Bit-exact routing except where the oracle flags a near-tie.
+    Returns the mask of tokens whose routing is decided (and equal)."""
+    T = ref_idx.shape[0]
+    ok = ~flagged
+    same_order = (gpu_idx == ref_idx).all(axis=1)
+    same_set = (np.sort(gpu_idx, axis=1) == np.sort(ref_idx, axis=1)).all(axis=1)
+    # decided tokens: exact slot order unless two chosen logits are within 1e-5
+    bad = ok & ~np.where(inner_tie, same_set, same_order)
+    assert not bad.any(), f"routing differs on {int(bad.sum())} decided tokens: {np.nonzero(bad)[0][:10]}"
+    w_err = np.abs(np.sort(gpu_w, axis=1) - np.sort(ref_w, axis=1))[ok]
+    assert w_err.size == 0 or w_err.max() < 2e-6, w_err.max()
+    np.testing.assert_allclose(gpu_w.sum(axis=1), 1.0, atol=2e-6)
+    return ok & same_order
+
+
+def check_dispatch_valid(idx, counts, offsets, pos, token_of_row, E):
+    """Properties every correct dispatch of `idx` has (used where the exact
+    result would need the undecided routing)."""
+    T, k = idx.shape
+    assert counts.sum() == T * k
+    assert offsets[0] == 0 and (np.diff(offsets) == counts).all()
+    assert sorted(pos.ravel().tolist()) == list(range(T * k))
+    for e in range(E):
+        seg = token_of_row[offsets[e]:offsets[e + 1]]
+        assert (np.diff(seg) > 0).all()
+    tt = np.repeat(np.arange(T), k)
+    assert (token_of_row[pos.ravel()] == tt).all()
+
+
+def full_parity(shape: gen.Shape, inp: dict, gpu: dict, tol=BF16_TOL):
+    """Element-wise comparison of every output against the full oracle."""
+    assert gpu["status"] == 0, gpu["status"]
+    bias = inp.get("bias")
+    idx, p, logits, flagged, inner = oracle.route_ref(inp["x"], inp["w_router"], bias, shape.k)
+    decided = check_routing(gpu["topk_idx"], gpu["topk_w"], idx, p, flagged, inner)
+    all_same = bool(decided.all())
+    counts, offsets, pos, tok = oracle.dispatch_ref(idx, shape.E)
+    if all_same:
+        assert (gpu["counts"] == counts).all()
+        assert (gpu["offsets"] == offsets).all()
+        assert (gpu["pos"] == pos).all()
+        assert (gpu["token_of_row"] == tok).all()
+    check_dispatch_valid(gpu["topk_idx"], gpu["counts"], gpu["offsets"], gpu["pos"],
+                         gpu["token_of_row"], shape.E)
+
+    y, fwd = oracle.moe_forward_ref(inp["x"], inp["w_router"], bias, inp["w_gate_up"],
+                                    inp["w_down"], shape.k, keep=True)
+    g = oracle.moe_backward_ref(inp["x"], inp["w_router"], bias, inp["w_gate_up"],
+                                inp["w_down"], shape.k, inp["dy"], fwd=fwd)
+    errs = {}
+    tokens = decided
+    errs["y"] = rel_err(host64(gpu["y"])[tokens], y[tokens])
+    errs["dx"] = rel_err(host64(gpu["dx"])[tokens], g["dx"][tokens])
+    # pre-activations kept for the backward, per routed row
+    gu = host64(gpu["gate_up"])
+    rows_gpu = gpu["padded_pos"][tokens].ravel()
+    rows_ref = pos[tokens].ravel()
+    errs["gate"] = rel_err(gu[rows_gpu, :shape.I], fwd["G"][rows_ref])
+    errs["up"] = rel_err(gu[rows_gpu, shape.I:], fwd["U"][rows_ref])
+    # expert gradients: leave out experts touched by an undecided token
+    touched = np.zeros(shape.E, dtype=bool)
+    for t in np.nonzero(~tokens)[0]:
+        touched[idx[t]] = True
+        touched[gpu["topk_idx"][t]] = True
+    keep = ~touched
+    errs["dw_gate_up"] = rel_err(host64(gpu["dw_gate_up"])[keep], g["dw_gate_up"][keep])
+    errs["dw_down"] = rel_err(host64(gpu["dw_down"])[keep], g["dw_down"][keep])
+    if all_same:
+        errs["dw_router"] = rel_err(host64(gpu["dw_router"]), g["dw_router"])
+    for name, v in errs.items():
+        assert v <= tol, (name, v, errs)
+    # experts that received no rows have exactly zero weight gradients
+    empty = counts == 0
+    if all_same and empty.any():
+        assert (host64(gpu["dw_gate_up"])[empty] == 0).all()
+        assert (host64(gpu["dw_down"])[empty] == 0).all()
+        assert (host64(gpu["dw_router"])[empty] == 0).all()
+    return errs

@@ -1,0 +1,175 @@
+"""Parity of the CUDA layer (through the C ABI) against the fp64 oracle, plus
+determinism and edge cases.  Bar: routing, counts, offsets and permutation
+bit-exact (near-ties flagged by the oracle excluded); bf16 outputs and
+gradients within max|diff| <= 2e-2 * rms(oracle) per tensor; repeated calls
+bitwise identical."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from routing_dispatch_grouped_router_gb300 import api, inputs as gen
+
+import _gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from routing_dispatch_grouped_router_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+# ------------------------------------------------------------------ GEMM ---
+
+@pytest.mark.parametrize("a_mn,b_mn", [(False, False), (False, True), (True, True)])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 512, 320 - 64), (384, 384, 640)])
+def test_engine_dense_gemm(a_mn, b_mn, M, N, K):
+    rng = np.random.default_rng(M * 7 + N + K)
+    A = gen.f32_to_bf16_bits(rng.standard_normal((M, K), dtype=np.float32))
+    B = gen.f32_to_bf16_bits(rng.standard_normal((N, K), dtype=np.float32))
+    ref = gen.bf16_bits_to_f32(A).astype(np.float64) @ gen.bf16_bits_to_f32(B).astype(np.float64).T
+    At = _gpu.dev_bf16(np.ascontiguousarray(A.T) if a_mn else A)
+    Bt = _gpu.dev_bf16(np.ascontiguousarray(B.T) if b_mn else B)
+    C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    api.gemm_bf16(At, a_mn, Bt, b_mn, C, ws)
+    assert api.device_status(ws) == 0
+    err = _gpu.rel_err(_gpu.host64(C), ref)
+    assert err < 1e-2, err
+
+
+# ------------------------------------------------------------ full layer ---
+
+SMALL = {
+    "tiny": gen.Shape(T=256, d=128, E=8, I=256, k=2),
+    "ragged": gen.Shape(T=300, d=128, E=5, I=128, k=2),
+    "k1_I384": gen.Shape(T=200, d=256, E=4, I=384, k=1),
+    "k_eq_E": gen.Shape(T=64, d=128, E=4, I=128, k=4),
+    "d384": gen.Shape(T=130, d=384, E=6, I=256, k=3),
+    "one_token": gen.Shape(T=1, d=128, E=8, I=128, k=8),
+    "many_experts": gen.Shape(T=64, d=128, E=128, I=128, k=8),
+    "wide": gen.Shape(T=512, d=512, E=16, I=512, k=4),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_layer_parity_small(name):
+    shape = SMALL[name]
+    inp = gen.make_inputs(shape, seed=0)
+    gpu = _gpu.run_gpu(shape, inp)
+    _gpu.full_parity(shape, inp, gpu)
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3, 4])
+def test_layer_parity_tiny_seeds(seed):
+    shape = gen.workload_shape("tiny")
+    inp = gen.make_inputs(shape, seed=seed)
+    _gpu.full_parity(shape, inp, _gpu.run_gpu(shape, inp))
+
+
+def test_layer_parity_empty_expert():
+    shape = gen.Shape(T=128, d=128, E=8, I=128, k=2)
+    inp = gen.make_inputs(shape, seed=5)
+    inp["bias"] = np.zeros(8, dtype=np.float32)
+    inp["bias"][2] = -1e4
+    gpu = _gpu.run_gpu(shape, inp)
+    assert gpu["counts"][2] == 0
+    _gpu.full_parity(shape, inp, gpu)
+    assert (_gpu.host64(gpu["dw_gate_up"])[2] == 0).all()
+
+
+def test_layer_zero_tokens():
+    shape = gen.Shape(T=0, d=128, E=4, I=128, k=2)
+    layer = api.MoELayer(0, 128, 4, 128, 2)
+    wr = torch.zeros(4, 128, dtype=torch.bfloat16, device="cuda")
+    wgu = torch.ones(4, 256, 128, dtype=torch.bfloat16, device="cuda")
+    wd = torch.ones(4, 128, 128, dtype=torch.bfloat16, device="cuda")
+    x = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
+    y = layer.forward(x, wr, None, wgu, wd)
+    dx, dwr, dwgu, dwd = layer.backward(x, x, wr, None, wgu, wd)
+    assert layer.status() == 0
+    assert y.numel() == 0 and dx.numel() == 0
+    assert (dwgu == 0).all() and (dwd == 0).all() and (dwr == 0).all()
+
+
+def test_layer_parity_fine_full_size():
+    """The fine-grained workload at its full size, every element."""
+    shape = gen.workload_shape("fine")
+    inp = gen.make_inputs(shape, seed=0)
+    gpu = _gpu.run_gpu(shape, inp)
+    errs = _gpu.full_parity(shape, inp, gpu)
+    print("fine errs", errs)
+
+
+@pytest.mark.parametrize("name", ["tiny", "fine"])
+def test_bitwise_deterministic(name):
+    shape = gen.workload_shape(name)
+    inp = gen.make_inputs(shape, seed=0)
+    layer = api.MoELayer(shape.T, shape.d, shape.E, shape.I, shape.k)
+    first = None
+    for _ in range(10):
+        g = _gpu.run_gpu(shape, inp, layer=layer)
+        cur = [g[n].view(torch.int16).cpu().numpy().copy() for n in
+               ("y", "dx", "dw_router", "dw_gate_up", "dw_down")]
+        cur.append(g["topk_idx"].copy())
+        if first is None:
+            first = cur
+        else:
+            for a, b in zip(first, cur):
+                assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------ stage APIs ---
+
+def test_route_stage_matches_oracle():
+    shape = gen.workload_shape("fine")
+    inp = gen.make_inputs(shape, seed=3)
+    desc = api.make_desc(shape.T, shape.d, shape.E, shape.I, shape.k)
+    ws = torch.zeros(api.stage_workspace_size(desc), dtype=torch.uint8, device="cuda")
+    idx = torch.empty(shape.T, shape.k, dtype=torch.int32, device="cuda")
+    w = torch.empty(shape.T, shape.k, dtype=torch.float32, device="cuda")
+    api.route(desc, _gpu.dev_bf16(inp["x"]), _gpu.dev_bf16(inp["w_router"]), None, idx, w, ws)
+    assert api.device_status(ws) == 0
+    ridx, rp, _, flagged, inner = oracle.route_ref(inp["x"], inp["w_router"], None, shape.k)
+    _gpu.check_routing(idx.cpu().numpy(), w.cpu().numpy(), ridx, rp, flagged, inner)
+
+
+@pytest.mark.parametrize("T,E,k", [(1000, 7, 3), (4096, 64, 8), (513, 512, 8), (5, 3, 3)])
+def test_dispatch_plan_stage_bit_exact(T, E, k):
+    rng = np.random.default_rng(T + E + k)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    desc = api.make_desc(T, 128, E, 128, k)
+    ws = torch.zeros(api.stage_workspace_size(desc), dtype=torch.uint8, device="cuda")
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    pos = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    tok = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    api.dispatch_plan(desc, torch.from_numpy(idx).cuda(), counts, offsets, pos, tok, ws)
+    assert api.device_status(ws) == 0
+    c, o, p, t = oracle.dispatch_ref(idx, E)
+    assert np.array_equal(counts.cpu().numpy(), c)
+    assert np.array_equal(offsets.cpu().numpy(), o)
+    assert np.array_equal(pos.cpu().numpy(), p)
+    assert np.array_equal(tok.cpu().numpy(), t)
+
+
+def test_dispatch_plan_flags_bad_indices():
+    T, E, k = 40, 6, 2
+    rng = np.random.default_rng(0)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    idx[3, 1] = 6        # out of range
+    idx[7, 1] = idx[7, 0]  # repeated
+    desc = api.make_desc(T, 128, E, 128, k)
+    ws = torch.zeros(api.stage_workspace_size(desc), dtype=torch.uint8, device="cuda")
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    pos = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    tok = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    api.dispatch_plan(desc, torch.from_numpy(idx).cuda(), counts, offsets, pos, tok, ws)
+    assert api.device_status(ws) == 17
+    p = pos.cpu().numpy()
+    assert p[3, 1] == -1 and p[7, 1] == -1
+    assert counts.cpu().numpy().sum() == T * k - 2
