@@ -245,9 +245,12 @@ def main():
 
     x, wr, wgu, wd, dy = (dev(inp[n]) for n in ("x", "w_router", "w_gate_up", "w_down", "dy"))
     layer = api.MoELayer(shape.T, shape.d, shape.E, shape.I, shape.k)
-    y = torch.empty_like(x)
-    dx = torch.empty_like(x)
-    dwr, dwgu, dwd = torch.empty_like(wr), torch.empty_like(wgu), torch.empty_like(wd)
+    f32 = dict(dtype=torch.float32, device="cuda")
+    y = torch.empty(x.shape, **f32)
+    dx = torch.empty(x.shape, **f32)
+    dwr = torch.empty(wr.shape, **f32)
+    dwgu = torch.empty(wgu.shape, **f32)
+    dwd = torch.empty(wd.shape, **f32)
     stream = torch.cuda.current_stream()
 
     def step():
@@ -337,8 +340,8 @@ def main():
     # ---- end to end through the C ABI: pinned host in, pinned host out
     xh = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
     dyh = torch.from_numpy(inp["dy"].view(np.int16)).view(torch.bfloat16).pin_memory()
-    yh = torch.empty_like(xh).pin_memory()
-    dxh = torch.empty_like(xh).pin_memory()
+    yh = torch.empty(xh.shape, dtype=torch.float32).pin_memory()
+    dxh = torch.empty(xh.shape, dtype=torch.float32).pin_memory()
     xd, dyd = torch.empty_like(x), torch.empty_like(dy)
 
     def e2e_step():
@@ -368,7 +371,7 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
     e2e = {"value": world * shape.T * args.e2e_steps / (e2e_ms / 1e3), "unit": "tokens/s",
-           "h2d_bytes_per_step": 2 * xh.numel() * 2, "d2h_bytes_per_step": 2 * yh.numel() * 2,
+           "h2d_bytes_per_step": 2 * xh.numel() * 2, "d2h_bytes_per_step": 2 * yh.numel() * 4,
            "steps": args.e2e_steps}
 
     cpu = None

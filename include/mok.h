@@ -61,6 +61,13 @@ typedef enum mok_dtype {
   MOK_MXFP8 = 1  /* E4M3 operands with 32-element E8M0 block scales (reserved) */
 } mok_dtype;
 
+/* Output dtypes.  By default y, dx and the three weight gradients are fp32
+ * (the value of the fp32 accumulation, unrounded, as an fp32 master-gradient
+ * would receive it).  These flags select bf16 outputs (round to nearest even
+ * of the same fp32 value). */
+#define MOK_FLAG_BF16_ACT_OUT 0x1u   /* y and dx written as bf16 */
+#define MOK_FLAG_BF16_WGRAD_OUT 0x2u /* dw_router, dw_gate_up, dw_down written as bf16 */
+
 /* Layer shape.  T tokens of width d, E experts with FFN width I, top-k. */
 typedef struct mok_moe_desc {
   int64_t T, d, E, I;
@@ -68,7 +75,7 @@ typedef struct mok_moe_desc {
   int32_t dtype;       /* mok_dtype */
   int32_t mb_tokens;   /* 0 = whole batch at once (micro-batching reserved) */
   int32_t ring_slots;  /* reserved, 0 */
-  uint32_t flags;      /* reserved, 0 */
+  uint32_t flags;      /* MOK_FLAG_* */
   uint32_t reserved;
 } mok_moe_desc;
 
@@ -114,9 +121,11 @@ mok_status mok_moe_saved_layout(const mok_moe_desc* desc, mok_saved_layout* out)
  *   rows of expert e = tokens routed to e in ascending token order (dropless)
  *   [g | u] = X_e W_gu_e^T,  h = silu(g) * u,  O = h W_down_e^T
  *   y_t = sum_{s=0..k-1} p_{t,s} O[pos[t,s]]   (fp32 sum in slot order)
+ * Every GEMM operand is bf16 (g and u are stored as bf16, h = bf16(silu(g) u));
+ * accumulation is fp32; O stays fp32.
  * x [T,d] bf16; w_router [E,d] bf16; router_bias [E] fp32 or NULL;
  * w_gate_up [E,2I,d] bf16 (gate rows 0..I-1, up rows I..2I-1);
- * w_down [E,d,I] bf16; y [T,d] bf16 (output).
+ * w_down [E,d,I] bf16; y [T,d] output, fp32 (bf16 with MOK_FLAG_BF16_ACT_OUT).
  * saved: >= saved_bytes, filled for the backward; its status word is reset.
  * workspace: >= fwd_ws_bytes.  Buffers must not overlap. */
 mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* w_router,
@@ -128,10 +137,13 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
  * ([dothoosh] "Hybrid communication": reverse-combine, then reverse-dispatch;
  * "Precision and scheduling": router-weight gradient inside the SwiGLU
  * backward, dp = <dy W_down, h>):
- *   dx [T,d], dw_router [E,d], dw_gate_up [E,2I,d], dw_down [E,d,I]: bf16
- *   outputs, overwritten (fp32 accumulation inside, one writer per element,
- *   fixed summation order).  The routing set is piecewise constant, so the
- *   router receives gradient only through p.  The bias gets no gradient.
+ *   dO = bf16(p * dy) per routed row, dH = dO W_down, dG and dU in bf16 from
+ *   dH and the stored g, u; dX rows fp32; weight gradients from bf16 operands.
+ *   dx [T,d], dw_router [E,d], dw_gate_up [E,2I,d], dw_down [E,d,I]:
+ *   outputs, overwritten, fp32 (bf16 with the MOK_FLAG_BF16_* flags); fp32
+ *   accumulation inside, one writer per element, fixed summation order.
+ *   The routing set is piecewise constant, so the router receives gradient
+ *   only through p.  The bias gets no gradient.
  * x, w_router, router_bias, w_gate_up, w_down: the forward's inputs.
  * workspace: >= bwd_ws_bytes. */
 mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void* x,

@@ -22,6 +22,19 @@ CUDA router takes it on float32 logits (the layer's stated logit precision);
 tokens whose float64 k-th/(k+1)-th logit gap is below 1e-5 are flagged so a
 comparison can leave them out.
 
+Precision.  ``precision="fp64"`` (default) is the layer's plain definition in
+float64.  ``precision="bf16"`` is the same definition with the operand
+precision the pages fix for the expert GEMMs ([dothoosh] "Precision and
+scheduling": the megakernel runs its GEMMs in BF16): every operand of the six
+expert GEMMs is a bf16 value, each GEMM accumulates exactly (float64), and
+nothing that is not a GEMM operand is rounded.  The rounded operands are
+  G, U            (outputs of the gate/up GEMM, stored as bf16)
+  H = silu(G) U   (operand of the down GEMM and of its weight gradient)
+  dO = p * dy     (operand of the down dgrad and of its weight gradient)
+  dG, dU          (operands of the gate/up dgrad and weight gradient)
+each rounded to the nearest bf16 (ties to even).  The expert output O, y, dp,
+the router gradient, dx and the weight gradients are not rounded.
+
 Readings where the pages say nothing (all are listed again in the design notes):
   * routing weights are a softmax over the k chosen logits (equal to the full
     softmax restricted to the chosen set and renormalised, so they sum to 1);
@@ -49,6 +62,34 @@ def widen(a) -> np.ndarray:
     if a.dtype == np.uint16:
         return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     return a.astype(np.float64)
+
+
+def bf16_round(a) -> np.ndarray:
+    """Nearest bfloat16 value (8 significant bits, ties to even, fp32 exponent
+    range, subnormal quantum 2^-133, overflow to inf) of float64 values."""
+    a = np.asarray(a, dtype=np.float64)
+    m, e = np.frexp(a)                       # a = m * 2**e, 0.5 <= |m| < 1
+    r = np.ldexp(np.round(np.ldexp(m, 8)), e - 8)   # np.round: half to even
+    tiny = np.abs(a) < 2.0 ** -126
+    if tiny.any():
+        q = 2.0 ** -133
+        r = np.where(tiny, np.round(a / q) * q, r)
+    big = np.abs(r) > 3.3895313892515355e38  # largest finite bf16
+    if big.any():
+        r = np.where(big, np.copysign(np.inf, a), r)
+    return r
+
+
+def _identity(a):
+    return a
+
+
+def _rounder(precision: str):
+    if precision == "fp64":
+        return _identity
+    if precision == "bf16":
+        return bf16_round
+    raise ValueError(precision)
 
 
 def _sigmoid(z):
@@ -144,25 +185,28 @@ def dispatch_ref(topk_idx, E: int):
 # forward  ([dothoosh] "Hybrid communication", "Precision and scheduling")
 # ----------------------------------------------------------------------------
 
-def expert_ffn(X, w_gate_up_e, w_down_e):
-    """SwiGLU FFN of one expert on rows X (float64).  Returns (G, U, H, O)."""
+def expert_ffn(X, w_gate_up_e, w_down_e, rnd=_identity):
+    """SwiGLU FFN of one expert on rows X (float64).  Returns (G, U, H, O).
+    ``rnd`` rounds the GEMM operands (identity in float64 mode)."""
     Wgu = widen(w_gate_up_e)
     I = Wgu.shape[0] // 2
-    G = X @ Wgu[:I].T
-    U = X @ Wgu[I:].T
-    H = silu(G) * U
+    G = rnd(X @ Wgu[:I].T)
+    U = rnd(X @ Wgu[I:].T)
+    H = rnd(silu(G) * U)
     O = H @ widen(w_down_e).T
     return G, U, H, O
 
 
 def moe_forward_ref(x, w_router, bias, w_gate_up, w_down, k: int, routing=None,
-                    keep=False):
+                    keep=False, precision="fp64"):
     """y_t = sum_s p[t,s] * FFN_{e[t,s]}(x_t), summed in slot order.
 
     ``routing`` = (topk_idx, topk_w) forces the routing (e.g. to check the
     later stages on exactly the kernel's selection); otherwise route_ref runs.
     Returns y [T,d] float64, and with keep=True also a dict of intermediates.
+    ``precision`` selects the plain float64 definition or the BF16-operand one.
     """
+    rnd = _rounder(precision)
     X = widen(x)
     T, d = X.shape
     E = np.asarray(w_gate_up).shape[0]
@@ -180,14 +224,14 @@ def moe_forward_ref(x, w_router, bias, w_gate_up, w_down, k: int, routing=None,
         a, b = int(offsets[e]), int(offsets[e + 1])
         if a == b:
             continue
-        G[a:b], U[a:b], H[a:b], O[a:b] = expert_ffn(X[tok[a:b]], w_gate_up[e], w_down[e])
+        G[a:b], U[a:b], H[a:b], O[a:b] = expert_ffn(X[tok[a:b]], w_gate_up[e], w_down[e], rnd)
     y = np.zeros((T, d))
     for s in range(k):
         y += p[:, s:s + 1] * O[pos[:, s]]
     if not keep:
         return y
     return y, dict(idx=idx, p=p, counts=counts, offsets=offsets, pos=pos,
-                   token_of_row=tok, G=G, U=U, H=H, O=O)
+                   token_of_row=tok, G=G, U=U, H=H, O=O, precision=precision)
 
 
 # ----------------------------------------------------------------------------
@@ -197,7 +241,7 @@ def moe_forward_ref(x, w_router, bias, w_gate_up, w_down, k: int, routing=None,
 # ----------------------------------------------------------------------------
 
 def moe_backward_ref(x, w_router, bias, w_gate_up, w_down, k: int, dy,
-                     routing=None, fwd=None, grad_experts=None):
+                     routing=None, fwd=None, grad_experts=None, precision=None):
     """Analytic gradients of L = sum(y*dy).
 
     Returns dict with dx [T,d], dw_router [E,d], dw_gate_up [E,2I,d],
@@ -209,7 +253,11 @@ def moe_backward_ref(x, w_router, bias, w_gate_up, w_down, k: int, dy,
       dp[t,s]   = <dy_t, O[pos[t,s]]>
       dl[t,j]   = p_j (dp_j - sum_i p_i dp_i) for j in S_t, 0 elsewhere
       dx       += dl W_r,   dW_r = dl^T x.
+    ``precision`` defaults to the one of ``fwd`` (float64 when fwd is None).
     """
+    if precision is None:
+        precision = fwd.get("precision", "fp64") if fwd is not None else "fp64"
+    rnd = _rounder(precision)
     X = widen(x)
     dY = widen(dy)
     T, d = X.shape
@@ -217,7 +265,7 @@ def moe_backward_ref(x, w_router, bias, w_gate_up, w_down, k: int, dy,
     I = np.asarray(w_gate_up).shape[1] // 2
     if fwd is None:
         _, fwd = moe_forward_ref(x, w_router, bias, w_gate_up, w_down, k,
-                                 routing=routing, keep=True)
+                                 routing=routing, keep=True, precision=precision)
     idx, p, offsets, pos, tok = fwd["idx"], fwd["p"], fwd["offsets"], fwd["pos"], fwd["token_of_row"]
     G, U, H, O = fwd["G"], fwd["U"], fwd["H"], fwd["O"]
     R = T * k
@@ -227,7 +275,7 @@ def moe_backward_ref(x, w_router, bias, w_gate_up, w_down, k: int, dy,
     row_p = np.empty(R)
     for s in range(k):
         row_p[pos[:, s]] = p[:, s]
-    dO = row_p[:, None] * dY[row_t]
+    dO = rnd(row_p[:, None] * dY[row_t])
     dp = np.einsum("tsd,td->ts", O[pos], dY)
 
     dX_rows = np.zeros((R, d))
@@ -244,8 +292,8 @@ def moe_backward_ref(x, w_router, bias, w_gate_up, w_down, k: int, dy,
         Wd = widen(w_down[e])
         Wgu = widen(w_gate_up[e])
         dH = dO[a:b] @ Wd                       # [rows, I]
-        dG = dH * U[a:b] * silu_grad(G[a:b])
-        dU = dH * silu(G[a:b])
+        dG = rnd(dH * U[a:b] * silu_grad(G[a:b]))
+        dU = rnd(dH * silu(G[a:b]))
         Xe = X[tok[a:b]]
         dX_rows[a:b] = dG @ Wgu[:I] + dU @ Wgu[I:]
         if grad_experts is None or e in dw_down:

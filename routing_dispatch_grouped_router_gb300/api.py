@@ -12,6 +12,8 @@ import torch
 from . import _lib
 
 BF16, MXFP8 = 0, 1
+FLAG_BF16_ACT_OUT = 0x1    # y and dx written as bf16 (default fp32)
+FLAG_BF16_WGRAD_OUT = 0x2  # weight gradients written as bf16 (default fp32)
 
 
 def _ptr(t):
@@ -26,9 +28,9 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def make_desc(T, d, E, I, k, dtype=BF16) -> _lib.MoeDesc:
+def make_desc(T, d, E, I, k, dtype=BF16, flags=0) -> _lib.MoeDesc:
     return _lib.MoeDesc(T=T, d=d, E=E, I=I, k=k, dtype=dtype, mb_tokens=0, ring_slots=0,
-                        flags=0, reserved=0)
+                        flags=flags, reserved=0)
 
 
 def workspace_sizes(desc):
@@ -132,9 +134,11 @@ def profile_collect() -> dict:
 class MoELayer:
     """Owns the three buffers of one layer shape and calls forward/backward."""
 
-    def __init__(self, T, d, E, I, k, device="cuda"):
-        self.desc = make_desc(T, d, E, I, k)
+    def __init__(self, T, d, E, I, k, device="cuda", flags=0):
+        self.desc = make_desc(T, d, E, I, k, flags=flags)
         self.T, self.d, self.E, self.I, self.k = T, d, E, I, k
+        self.act_dtype = torch.bfloat16 if flags & FLAG_BF16_ACT_OUT else torch.float32
+        self.wgrad_dtype = torch.bfloat16 if flags & FLAG_BF16_WGRAD_OUT else torch.float32
         f, s, b = workspace_sizes(self.desc)
         self.fwd_ws = torch.empty(max(f, 256), dtype=torch.uint8, device=device)
         self.saved = torch.zeros(max(s, 256), dtype=torch.uint8, device=device)
@@ -151,17 +155,19 @@ class MoELayer:
 
     def forward(self, x, w_router, bias, w_gate_up, w_down, y=None, stream=None):
         if y is None:
-            y = torch.empty_like(x)
+            y = torch.empty(x.shape, dtype=self.act_dtype, device=x.device)
         forward(self.desc, x, w_router, bias, w_gate_up, w_down, y, self.saved, self.fwd_ws,
                 stream)
         return y
 
     def backward(self, dy, x, w_router, bias, w_gate_up, w_down, dx=None, dw_router=None,
                  dw_gate_up=None, dw_down=None, stream=None):
-        dx = torch.empty_like(x) if dx is None else dx
-        dw_router = torch.empty_like(w_router) if dw_router is None else dw_router
-        dw_gate_up = torch.empty_like(w_gate_up) if dw_gate_up is None else dw_gate_up
-        dw_down = torch.empty_like(w_down) if dw_down is None else dw_down
+        def out(like, dt, given):
+            return torch.empty(like.shape, dtype=dt, device=like.device) if given is None else given
+        dx = out(x, self.act_dtype, dx)
+        dw_router = out(w_router, self.wgrad_dtype, dw_router)
+        dw_gate_up = out(w_gate_up, self.wgrad_dtype, dw_gate_up)
+        dw_down = out(w_down, self.wgrad_dtype, dw_down)
         backward(self.desc, dy, x, w_router, bias, w_gate_up, w_down, self.saved, dx, dw_router,
                  dw_gate_up, dw_down, self.bwd_ws, stream)
         return dx, dw_router, dw_gate_up, dw_down

@@ -56,9 +56,8 @@ struct GemmArgs {
   void* out;                // C (bf16 or fp32)
   long long ldo;            // C row stride (elements)
   long long out_group_stride;  // KGROUP: elements between experts' C
-  void* out2;               // SWIGLU_FWD: H [rows,I]; SWIGLU_BWD: HP [rows,I]
+  void* out2;               // SWIGLU_FWD and SWIGLU_BWD: H [rows,I] bf16
   const void* in_gu;        // SWIGLU_BWD: saved pre-activations [rows,2I]
-  const float* row_w;       // SWIGLU_BWD: routing weight per row
   float* dp_part;           // SWIGLU_BWD: [rows, np] partial <dA,h>
   int np;
   int* status;
@@ -186,16 +185,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
   constexpr int HALF_COLS = BN / 2;
   const bool zero_k = (tl.num_kb == 0);
   if (EPI == EPI_BF16 || EPI == EPI_F32) {
-    long long grow;
-    char* base;
     constexpr int esz = EPI == EPI_F32 ? 4 : 2;
-    if (SCHED == SCHED_KGROUP) {
-      grow = tl.row0 + row_in_tile;
-      base = static_cast<char*>(a.out) + (long long)tl.e * a.out_group_stride * esz;
-    } else {
-      grow = tl.row0 + row_in_tile;
-      base = static_cast<char*>(a.out);
-    }
+    const long long grow = tl.row0 + row_in_tile;
+    char* base = static_cast<char*>(a.out);
+    if (SCHED == SCHED_KGROUP) base += (long long)tl.e * a.out_group_stride * esz;
     const bool row_ok = (SCHED != SCHED_DENSE) || grow < a.m_valid;
     const int col0 = tl.n_tile * BN + half * HALF_COLS;
 #pragma unroll 1
@@ -211,13 +204,20 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
       if (EPI == EPI_BF16) {
         __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(base) + grow * a.ldo + col0 + c;
         store_bf16x32(p, v);
-      } else {
+      } else if (SCHED == SCHED_DENSE) {
+        // router logits: the last column tile may extend past N
         float* p = reinterpret_cast<float*>(base) + grow * a.ldo;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int col = col0 + c + j;
           if (col < a.n_valid) p[col] = v[j];
         }
+      } else {
+        float4* p = reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + grow * a.ldo +
+                                              col0 + c);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          p[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
       }
     }
   } else if (EPI == EPI_SWIGLU_FWD) {
@@ -245,35 +245,39 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
       store_bf16x32(h + n0 + c, hv);
     }
   } else if (EPI == EPI_SWIGLU_BWD) {
-    // accumulator = dA = dY_perm W_down (rows x BN columns of I, n0 = n_tile*BN)
+    // accumulator = dH = dO W_down for BN columns of I (n0 = n_tile*BN), with
+    // dO = p * dy already in the A operand.  SwiGLU backward from the stored
+    // bf16 g, u:  dG = dH * u * sigma(g) (1 + g (1 - sigma(g))),
+    //             dU = dH * silu(g);
+    // h = bf16(silu(g) u) is rebuilt bit-identically to the forward's (it is
+    // the B operand of the down-projection weight gradient), and
+    // sum_j dH_j h_j = p <dy, O> is accumulated for the router gradient.
     const long long r = tl.row0 + row_in_tile;
     const int I = a.I;
     const int n0 = tl.n_tile * BN + half * HALF_COLS;
     const __nv_bfloat16* gu = static_cast<const __nv_bfloat16*>(a.in_gu) + r * (2LL * I);
     __nv_bfloat16* dgu = static_cast<__nv_bfloat16*>(a.out) + r * (2LL * I);
-    __nv_bfloat16* hp = static_cast<__nv_bfloat16*>(a.out2) + r * (long long)I;
-    const float p = a.row_w[r];
+    __nv_bfloat16* hout = static_cast<__nv_bfloat16*>(a.out2) + r * (long long)I;
     float dp = 0.f;
 #pragma unroll 1
     for (int c = 0; c < HALF_COLS; c += 32) {
-      float dA[32], g[32], u[32], o1[32], o2[32];
-      tmem_ld32(taddr + half * HALF_COLS + c, dA);
+      float dH[32], g[32], u[32], o1[32];
+      tmem_ld32(taddr + half * HALF_COLS + c, dH);
       load_bf16x32(gu + n0 + c, g);
       load_bf16x32(gu + I + n0 + c, u);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         float s;
         const float sl = silu_f(g[j], &s);
-        const float hv = bf16_round(sl * u[j]);   // the forward's h
-        dp = fmaf(dA[j], hv, dp);
-        const float dh = p * dA[j];
-        o1[j] = dh * u[j] * (s * (1.0f + g[j] * (1.0f - s)));  // d gate
-        o2[j] = dh * sl;                                       // d up
-        g[j] = p * hv;                                         // p*h for dW_down
+        const float hv = bf16_round(sl * u[j]);
+        dp = fmaf(dH[j], hv, dp);
+        o1[j] = dH[j] * u[j] * (s * (1.0f + g[j] * (1.0f - s)));  // d gate
+        u[j] = dH[j] * sl;                                        // d up
+        g[j] = hv;                                                // h
       }
       store_bf16x32(dgu + n0 + c, o1);
-      store_bf16x32(dgu + I + n0 + c, o2);
-      store_bf16x32(hp + n0 + c, g);
+      store_bf16x32(dgu + I + n0 + c, u);
+      store_bf16x32(hout + n0 + c, g);
     }
     a.dp_part[r * a.np + tl.n_tile * 2 + half] = dp;
   }
@@ -578,20 +582,20 @@ cudaError_t gemm_fwd_down(const Dims& D, const void* H, const void* w_down,
   a.b_group_rows = (int)D.d;
   a.mtile_prefix = mtile_prefix;
   a.poff = poff;
-  a.out = O;
+  a.out = O;  // fp32 [rows_max, d]
   a.ldo = D.d;
   const int mt = max_mtiles(D) * a.n_tiles;
-  if (bn == 256) return launch<256, false, false, SCHED_MGROUP, EPI_BF16>("fwd_down", ta, tb, a, mt, st);
-  return launch<128, false, false, SCHED_MGROUP, EPI_BF16>("fwd_down", ta, tb, a, mt, st);
+  if (bn == 256) return launch<256, false, false, SCHED_MGROUP, EPI_F32>("fwd_down", ta, tb, a, mt, st);
+  return launch<128, false, false, SCHED_MGROUP, EPI_F32>("fwd_down", ta, tb, a, mt, st);
 }
 
-cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* w_down,
+cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dO, const void* w_down,
                                 const int32_t* mtile_prefix, const int32_t* poff, const void* GU,
-                                const float* row_w, void* dGU, void* HP, float* dp_part,
-                                int* status, cudaStream_t st) {
+                                void* dGU, void* H, float* dp_part, int* status,
+                                cudaStream_t st) {
   const int bn = D.bn_dgrad;
   CUtensorMap ta, tb;
-  if (!make_map(&ta, dY_perm, D.d, D.rows_max, D.d, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&ta, dO, D.d, D.rows_max, D.d, 128)) return cudaErrorInvalidValue;
   // W_down_e viewed as [K = d rows, N = I columns]: N-major operand
   if (!make_map(&tb, w_down, D.I, D.E * D.d, D.I, 64)) return cudaErrorInvalidValue;
   GemmArgs a = blank_args(status);
@@ -603,9 +607,8 @@ cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* 
   a.mtile_prefix = mtile_prefix;
   a.poff = poff;
   a.out = dGU;
-  a.out2 = HP;
+  a.out2 = H;
   a.in_gu = GU;
-  a.row_w = row_w;
   a.dp_part = dp_part;
   a.np = D.np;
   const int mt = max_mtiles(D) * a.n_tiles;
@@ -628,20 +631,20 @@ cudaError_t gemm_bwd_gate_up_dgrad(const Dims& D, const void* dGU, const void* w
   a.b_group_rows = (int)(2 * D.I);
   a.mtile_prefix = mtile_prefix;
   a.poff = poff;
-  a.out = dX_perm;
+  a.out = dX_perm;  // fp32 [rows_max, d]
   a.ldo = D.d;
   const int mt = max_mtiles(D) * a.n_tiles;
-  if (bn == 256) return launch<256, false, true, SCHED_MGROUP, EPI_BF16>("bwd_gate_up_dgrad", ta, tb, a, mt, st);
-  return launch<128, false, true, SCHED_MGROUP, EPI_BF16>("bwd_gate_up_dgrad", ta, tb, a, mt, st);
+  if (bn == 256) return launch<256, false, true, SCHED_MGROUP, EPI_F32>("bwd_gate_up_dgrad", ta, tb, a, mt, st);
+  return launch<128, false, true, SCHED_MGROUP, EPI_F32>("bwd_gate_up_dgrad", ta, tb, a, mt, st);
 }
 
-cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* HP,
+cudaError_t gemm_wgrad_down(const Dims& D, const void* dO, const void* H,
                             const int32_t* poff, void* dw_down, int* status, cudaStream_t st) {
-  // dW_down_e [d, I] = dY_perm_e^T [d x rows] * HP_e [rows x I]
+  // dW_down_e [d, I] = dO_e^T [d x rows] * H_e [rows x I]
   const int bn = (D.I % 256 == 0) ? 256 : 128;
   CUtensorMap ta, tb;
-  if (!make_map(&ta, dY_perm, D.d, D.rows_max, D.d, 64)) return cudaErrorInvalidValue;
-  if (!make_map(&tb, HP, D.I, D.rows_max, D.I, 64)) return cudaErrorInvalidValue;
+  if (!make_map(&ta, dO, D.d, D.rows_max, D.d, 64)) return cudaErrorInvalidValue;
+  if (!make_map(&tb, H, D.I, D.rows_max, D.I, 64)) return cudaErrorInvalidValue;
   GemmArgs a = blank_args(status);
   a.E = (int)D.E;
   a.m_tiles = (int)(D.d / 128);
@@ -651,8 +654,12 @@ cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* HP,
   a.ldo = D.I;
   a.out_group_stride = D.d * D.I;
   const int mt = a.E * a.m_tiles * a.n_tiles;
-  if (bn == 256) return launch<256, true, true, SCHED_KGROUP, EPI_BF16>("bwd_down_wgrad", ta, tb, a, mt, st);
-  return launch<128, true, true, SCHED_KGROUP, EPI_BF16>("bwd_down_wgrad", ta, tb, a, mt, st);
+  if (D.wgrad_bf16) {
+    if (bn == 256) return launch<256, true, true, SCHED_KGROUP, EPI_BF16>("bwd_down_wgrad", ta, tb, a, mt, st);
+    return launch<128, true, true, SCHED_KGROUP, EPI_BF16>("bwd_down_wgrad", ta, tb, a, mt, st);
+  }
+  if (bn == 256) return launch<256, true, true, SCHED_KGROUP, EPI_F32>("bwd_down_wgrad", ta, tb, a, mt, st);
+  return launch<128, true, true, SCHED_KGROUP, EPI_F32>("bwd_down_wgrad", ta, tb, a, mt, st);
 }
 
 cudaError_t gemm_wgrad_gate_up(const Dims& D, const void* dGU, const void* X_perm,
@@ -672,8 +679,12 @@ cudaError_t gemm_wgrad_gate_up(const Dims& D, const void* dGU, const void* X_per
   a.ldo = D.d;
   a.out_group_stride = 2 * D.I * D.d;
   const int mt = a.E * a.m_tiles * a.n_tiles;
-  if (bn == 256) return launch<256, true, true, SCHED_KGROUP, EPI_BF16>("bwd_gate_up_wgrad", ta, tb, a, mt, st);
-  return launch<128, true, true, SCHED_KGROUP, EPI_BF16>("bwd_gate_up_wgrad", ta, tb, a, mt, st);
+  if (D.wgrad_bf16) {
+    if (bn == 256) return launch<256, true, true, SCHED_KGROUP, EPI_BF16>("bwd_gate_up_wgrad", ta, tb, a, mt, st);
+    return launch<128, true, true, SCHED_KGROUP, EPI_BF16>("bwd_gate_up_wgrad", ta, tb, a, mt, st);
+  }
+  if (bn == 256) return launch<256, true, true, SCHED_KGROUP, EPI_F32>("bwd_gate_up_wgrad", ta, tb, a, mt, st);
+  return launch<128, true, true, SCHED_KGROUP, EPI_F32>("bwd_gate_up_wgrad", ta, tb, a, mt, st);
 }
 
 cudaError_t launch_router_logits(const Dims& D, const void* x, const void* w_router,

@@ -92,7 +92,8 @@ mok_status make_dims(const mok_moe_desc* desc, Dims* out) {
   const mok_moe_desc& d = *desc;
   if (d.T < 0 || d.d <= 0 || d.E <= 0 || d.I <= 0 || d.k <= 0) return MOK_ERR_INVALID_ARG;
   if (d.dtype != MOK_BF16) return MOK_ERR_UNSUPPORTED;
-  if (d.mb_tokens != 0 || d.ring_slots != 0 || d.flags != 0) return MOK_ERR_UNSUPPORTED;
+  if (d.mb_tokens != 0 || d.ring_slots != 0) return MOK_ERR_UNSUPPORTED;
+  if (d.flags & ~(MOK_FLAG_BF16_ACT_OUT | MOK_FLAG_BF16_WGRAD_OUT)) return MOK_ERR_UNSUPPORTED;
   if (d.E > kMaxExperts || d.k > kMaxTopK || d.k > d.E) return MOK_ERR_UNSUPPORTED;
   if (d.d % 128 != 0 || d.I % 128 != 0) return MOK_ERR_UNSUPPORTED;
   if (d.d > 16384 || d.I > 16384) return MOK_ERR_UNSUPPORTED;
@@ -109,6 +110,8 @@ mok_status make_dims(const mok_moe_desc* desc, Dims* out) {
   D.nb = (D.T + kPlanBlock - 1) / kPlanBlock;
   D.bn_dgrad = (D.I % 256 == 0) ? 256 : 128;
   D.np = static_cast<int>(D.I / D.bn_dgrad) * 2;
+  D.act_bf16 = (d.flags & MOK_FLAG_BF16_ACT_OUT) != 0;
+  D.wgrad_bf16 = (d.flags & MOK_FLAG_BF16_WGRAD_OUT) != 0;
   // every row index and element offset used in 32-bit arithmetic must fit
   if (D.rows_max * 2 * D.I >= (1LL << 40)) return MOK_ERR_UNSUPPORTED;
   if (D.rows_max >= (1LL << 31) / 2) return MOK_ERR_UNSUPPORTED;
@@ -156,7 +159,7 @@ void fwd_layout(const Dims& D, FwdWs* W) {
   W->block_counts = take(static_cast<size_t>(D.nb) * D.E * 4);
   W->block_base = take(static_cast<size_t>(D.nb) * D.E * 4);
   W->h = take(rows * D.I * 2);
-  W->o = take(rows * D.d * 2);
+  W->o = take(rows * D.d * 4);  // fp32 expert outputs
   W->logits = take(static_cast<size_t>(D.T) * D.E * 4);
   W->total = o;
 }
@@ -169,11 +172,11 @@ void bwd_layout(const Dims& D, BwdWs* W) {
     return at;
   };
   const size_t rows = static_cast<size_t>(D.rows_max);
-  W->dy_perm = take(rows * D.d * 2);
+  W->d_o = take(rows * D.d * 2);
   W->dgu = take(rows * 2 * D.I * 2);
-  W->hp = take(rows * D.I * 2);
+  W->h = take(rows * D.I * 2);
   W->dp_part = take(rows * D.np * 4);
-  W->dx_perm = take(rows * D.d * 2);
+  W->dx_perm = take(rows * D.d * 4);  // fp32
   W->dl_row = take(rows * 4);
   W->dl_tok = take(static_cast<size_t>(D.T) * D.k * 4);
   W->total = o;
@@ -304,7 +307,7 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
   MOK_CUDA(gemm_fwd_gate_up(D, x_perm, w_gate_up, o.mtile_prefix, o.padded_offsets, gu, h, status,
                             st));
   MOK_CUDA(gemm_fwd_down(D, h, w_down, o.mtile_prefix, o.padded_offsets, O, status, st));
-  MOK_CUDA(launch_combine(D, O, o.ppos, topk_w, y, st));
+  MOK_CUDA(launch_combine(D, static_cast<const float*>(O), o.ppos, topk_w, y, st));
   return MOK_OK;
 }
 
@@ -349,21 +352,20 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
   const void* x_perm = at<char>(saved, L.x_perm);
   const void* gu = at<char>(saved, L.gate_up);
 
-  void* dy_perm = at<char>(workspace, B.dy_perm);
+  void* d_o = at<char>(workspace, B.d_o);
   void* dgu = at<char>(workspace, B.dgu);
-  void* hp = at<char>(workspace, B.hp);
+  void* h = at<char>(workspace, B.h);
   float* dp_part = at<float>(workspace, B.dp_part);
-  void* dx_perm = at<char>(workspace, B.dx_perm);
+  float* dx_perm = at<float>(workspace, B.dx_perm);
   float* dl_row = at<float>(workspace, B.dl_row);
   float* dl_tok = at<float>(workspace, B.dl_tok);
 
-  // reverse-combine: pull dy rows into expert order
-  MOK_CUDA(launch_gather_rows(D, dy, ptok, poff, dy_perm, status, st));
+  // reverse-combine: pull dy rows into expert order, scaled by p (dO = p dy)
+  MOK_CUDA(launch_gather_scale_rows(D, dy, ptok, row_w, poff, d_o, st));
   // down-projection dgrad + SwiGLU backward + router-weight partials
-  MOK_CUDA(gemm_bwd_down_dgrad(D, dy_perm, w_down, mtp, poff, gu, row_w, dgu, hp, dp_part, status,
-                               st));
-  // down-projection wgrad: dW_down_e = dY_e^T (p h)_e
-  MOK_CUDA(gemm_wgrad_down(D, dy_perm, hp, poff, dw_down, status, st));
+  MOK_CUDA(gemm_bwd_down_dgrad(D, d_o, w_down, mtp, poff, gu, dgu, h, dp_part, status, st));
+  // down-projection wgrad: dW_down_e = dO_e^T H_e
+  MOK_CUDA(gemm_wgrad_down(D, d_o, h, poff, dw_down, status, st));
   // gate/up dgrad: dX_perm = dGU W_gu
   MOK_CUDA(gemm_bwd_gate_up_dgrad(D, dgu, w_gate_up, mtp, poff, dx_perm, status, st));
   // gate/up wgrad: dW_gu_e = dGU_e^T X_e

@@ -24,13 +24,15 @@ struct Dims {
   int64_t nb;        // dispatch-plan blocks: ceil(T / kPlanBlock)
   int bn_dgrad;      // N tile of the down-projection dgrad (over I)
   int np;            // dp partials per row = (I / bn_dgrad) * 2
+  bool act_bf16;     // y and dx written as bf16 (else fp32)
+  bool wgrad_bf16;   // dW_* written as bf16 (else fp32)
 };
 
 struct FwdWs {
   size_t block_counts, block_base, h, o, logits, total;
 };
 struct BwdWs {
-  size_t dy_perm, dgu, hp, dp_part, dx_perm, dl_row, dl_tok, total;
+  size_t d_o, dgu, h, dp_part, dx_perm, dl_row, dl_tok, total;
 };
 struct StageWs {
   size_t status, block_counts, block_base, padded_offsets, mtile_prefix, ppos, ptok, row_w,
@@ -74,17 +76,23 @@ cudaError_t launch_gather_rows(const Dims& D, const void* src, const int32_t* pt
                                const int32_t* padded_offsets, void* dst, int* status,
                                cudaStream_t st);
 
-// y_t = sum_s p[t,s] O[ppos[t,s]].
-cudaError_t launch_combine(const Dims& D, const void* O, const int32_t* ppos, const float* topk_w,
+// dO[r] = bf16(row_w[r] * src[ptok[r]]) (zeros where ptok[r] < 0).
+cudaError_t launch_gather_scale_rows(const Dims& D, const void* src, const int32_t* ptok,
+                                     const float* row_w, const int32_t* padded_offsets, void* dst,
+                                     cudaStream_t st);
+
+// y_t = sum_s p[t,s] O[ppos[t,s]] (O fp32; y fp32 or bf16).
+cudaError_t launch_combine(const Dims& D, const float* O, const int32_t* ppos, const float* topk_w,
                            void* y, cudaStream_t st);
 
-// dl (router logit grad) from dp partials; dx_t = sum_s dX[ppos] + dl W_r[e].
-cudaError_t launch_reverse_dispatch(const Dims& D, const void* dX_perm, const int32_t* ppos,
+// dl (router logit grad) from dp partials; dx_t = sum_s dX[ppos] + dl W_r[e]
+// (dX fp32; dx fp32 or bf16).
+cudaError_t launch_reverse_dispatch(const Dims& D, const float* dX_perm, const int32_t* ppos,
                                     const int32_t* topk_idx, const float* topk_w,
                                     const float* dp_part, const void* w_router, void* dx,
                                     float* dl_row, float* dl_tok, cudaStream_t st);
 
-// dW_r[e] = sum over rows of e of dl_row[r] * X_perm[r].
+// dW_r[e] = sum over rows of e of dl_row[r] * X_perm[r] (fp32 or bf16 out).
 cudaError_t launch_router_wgrad(const Dims& D, const void* X_perm, const float* dl_row,
                                 const int32_t* padded_offsets, const int32_t* counts,
                                 void* dw_router, cudaStream_t st);
@@ -96,14 +104,14 @@ cudaError_t gemm_fwd_gate_up(const Dims& D, const void* X_perm, const void* w_ga
 cudaError_t gemm_fwd_down(const Dims& D, const void* H, const void* w_down,
                           const int32_t* mtile_prefix, const int32_t* poff, void* O, int* status,
                           cudaStream_t st);
-cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* w_down,
+cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dO, const void* w_down,
                                 const int32_t* mtile_prefix, const int32_t* poff, const void* GU,
-                                const float* row_w, void* dGU, void* HP, float* dp_part,
-                                int* status, cudaStream_t st);
+                                void* dGU, void* H, float* dp_part, int* status,
+                                cudaStream_t st);
 cudaError_t gemm_bwd_gate_up_dgrad(const Dims& D, const void* dGU, const void* w_gate_up,
                                    const int32_t* mtile_prefix, const int32_t* poff,
                                    void* dX_perm, int* status, cudaStream_t st);
-cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* HP,
+cudaError_t gemm_wgrad_down(const Dims& D, const void* dO, const void* H,
                             const int32_t* poff, void* dw_down, int* status, cudaStream_t st);
 cudaError_t gemm_wgrad_gate_up(const Dims& D, const void* dGU, const void* X_perm,
                                const int32_t* poff, void* dw_gate_up, int* status,

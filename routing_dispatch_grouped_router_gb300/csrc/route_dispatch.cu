@@ -379,29 +379,99 @@ cudaError_t launch_gather_rows(const Dims& D, const void* src, const int32_t* pt
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------- scaled row gather --
+
+// Reverse-combine pull: dO[r] = bf16(p_r * dy[ptok[r]]), the A operand of the
+// down-projection dgrad and of its weight gradient.  One warp per row, 16-byte
+// vectors; padding rows get zeros.
+__global__ void gather_scale_rows_kernel(const uint4* __restrict__ src,
+                                         const int32_t* __restrict__ ptok,
+                                         const float* __restrict__ row_w,
+                                         const int32_t* __restrict__ poff_end, int T, int dv,
+                                         uint4* __restrict__ dst) {
+  const long long P = *poff_end;
+  const int lane = threadIdx.x & 31;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < P; r += warps) {
+    const int t = ptok[r];
+    uint4* out = dst + r * dv;
+    if (t < 0 || t >= T) {
+      for (int c = lane; c < dv; c += 32) out[c] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const float w = row_w[r];
+    const uint4* in = src + static_cast<long long>(t) * dv;
+    for (int c = lane; c < dv; c += 32) {
+      const uint4 v = ld_global_nc_v4(in + c);
+      out[c] = make_uint4(pack_bf16x2(w * bf16lo(v.x), w * bf16hi(v.x)),
+                          pack_bf16x2(w * bf16lo(v.y), w * bf16hi(v.y)),
+                          pack_bf16x2(w * bf16lo(v.z), w * bf16hi(v.z)),
+                          pack_bf16x2(w * bf16lo(v.w), w * bf16hi(v.w)));
+    }
+  }
+}
+
+cudaError_t launch_gather_scale_rows(const Dims& D, const void* src, const int32_t* ptok,
+                                     const float* row_w, const int32_t* padded_offsets, void* dst,
+                                     cudaStream_t st) {
+  if (D.T == 0) return cudaSuccess;
+  const int dv = static_cast<int>(D.d / 8);
+  long long blocks = static_cast<long long>(num_sms_current_device()) * 8;
+  const long long need = (D.rows_max + 7) / 8;
+  if (blocks > need) blocks = need;
+  ProfScope prof("gather_scale_rows", st);
+  gather_scale_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+      static_cast<const uint4*>(src), ptok, row_w, padded_offsets + D.E, static_cast<int>(D.T),
+      dv, static_cast<uint4*>(dst));
+  count_launch();
+  return cudaGetLastError();
+}
+
 // ----------------------------------------------------------------- combine --
 
-__device__ __forceinline__ void axpy8(float (&acc)[8], float w, uint4 v) {
-  acc[0] = fmaf(w, bf16lo(v.x), acc[0]); acc[1] = fmaf(w, bf16hi(v.x), acc[1]);
-  acc[2] = fmaf(w, bf16lo(v.y), acc[2]); acc[3] = fmaf(w, bf16hi(v.y), acc[3]);
-  acc[4] = fmaf(w, bf16lo(v.z), acc[4]); acc[5] = fmaf(w, bf16hi(v.z), acc[5]);
-  acc[6] = fmaf(w, bf16lo(v.w), acc[6]); acc[7] = fmaf(w, bf16hi(v.w), acc[7]);
+__device__ __forceinline__ void axpy4(float (&acc)[4], float w, float4 v) {
+  acc[0] = fmaf(w, v.x, acc[0]);
+  acc[1] = fmaf(w, v.y, acc[1]);
+  acc[2] = fmaf(w, v.z, acc[2]);
+  acc[3] = fmaf(w, v.w, acc[3]);
 }
 
-__device__ __forceinline__ void add8(float (&acc)[8], uint4 v) {
-  acc[0] += bf16lo(v.x); acc[1] += bf16hi(v.x); acc[2] += bf16lo(v.y); acc[3] += bf16hi(v.y);
-  acc[4] += bf16lo(v.z); acc[5] += bf16hi(v.z); acc[6] += bf16lo(v.w); acc[7] += bf16hi(v.w);
+__device__ __forceinline__ void add4(float (&acc)[4], float4 v) {
+  acc[0] += v.x;
+  acc[1] += v.y;
+  acc[2] += v.z;
+  acc[3] += v.w;
 }
 
-__device__ __forceinline__ uint4 pack8(const float (&a)[8]) {
-  return make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
-                    pack_bf16x2(a[6], a[7]));
+__device__ __forceinline__ float4 ld_nc_f4(const float4* p) {
+  float4 v;
+  asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
 }
 
-// One CTA per token: y_t = sum_{s=0..k-1} p[t,s] * O[ppos[t,s]], fp32 in slot order.
-__global__ void combine_kernel(const uint4* __restrict__ O, const int32_t* __restrict__ ppos,
-                               const float* __restrict__ topk_w, int k, int dv,
-                               uint4* __restrict__ y) {
+__device__ __forceinline__ float4 bf16x4_to_f4(uint2 w) {
+  return make_float4(bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y));
+}
+
+// Stores 4 consecutive values of row `row` (fp32 or bf16 output).
+template <bool BF16_OUT>
+__device__ __forceinline__ void store4(void* out, long long row, int dq, int c,
+                                       const float (&a)[4]) {
+  if (BF16_OUT) {
+    reinterpret_cast<uint2*>(out)[row * dq + c] =
+        make_uint2(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]));
+  } else {
+    reinterpret_cast<float4*>(out)[row * dq + c] = make_float4(a[0], a[1], a[2], a[3]);
+  }
+}
+
+// One CTA per token: y_t = sum_{s=0..k-1} p[t,s] * O[ppos[t,s]], fp32 in slot
+// order (O is fp32).
+template <bool BF16_OUT>
+__global__ void combine_kernel(const float4* __restrict__ O, const int32_t* __restrict__ ppos,
+                               const float* __restrict__ topk_w, int k, int dq, void* y) {
   __shared__ int s_row[kMaxTopK];
   __shared__ float s_w[kMaxTopK];
   const long long t = blockIdx.x;
@@ -410,32 +480,36 @@ __global__ void combine_kernel(const uint4* __restrict__ O, const int32_t* __res
     s_w[threadIdx.x] = topk_w[t * k + threadIdx.x];
   }
   __syncthreads();
-  for (int c = threadIdx.x; c < dv; c += blockDim.x) {
-    uint4 v[kMaxTopK];
+  for (int c = threadIdx.x; c < dq; c += blockDim.x) {
+    float4 v[kMaxTopK];
 #pragma unroll
     for (int s = 0; s < kMaxTopK; ++s)
-      if (s < k && s_row[s] >= 0) v[s] = ld_global_nc_v4(O + static_cast<long long>(s_row[s]) * dv + c);
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (s < k && s_row[s] >= 0) v[s] = ld_nc_f4(O + static_cast<long long>(s_row[s]) * dq + c);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int s = 0; s < kMaxTopK; ++s)
-      if (s < k && s_row[s] >= 0) axpy8(acc, s_w[s], v[s]);
-    y[t * dv + c] = pack8(acc);
+      if (s < k && s_row[s] >= 0) axpy4(acc, s_w[s], v[s]);
+    store4<BF16_OUT>(y, t, dq, c, acc);
   }
 }
 
-static int row_threads(int dv) {
-  int th = dv < 256 ? dv : 256;
+static int row_threads(int nvec) {
+  int th = nvec < 256 ? nvec : 256;
   th = (th + 31) / 32 * 32;
-  return th;
+  return th < 32 ? 32 : th;
 }
 
-cudaError_t launch_combine(const Dims& D, const void* O, const int32_t* ppos, const float* topk_w,
+cudaError_t launch_combine(const Dims& D, const float* O, const int32_t* ppos, const float* topk_w,
                            void* y, cudaStream_t st) {
   if (D.T == 0) return cudaSuccess;
-  const int dv = static_cast<int>(D.d / 8);
+  const int dq = static_cast<int>(D.d / 4);
   ProfScope prof("combine", st);
-  combine_kernel<<<static_cast<unsigned>(D.T), row_threads(dv), 0, st>>>(
-      static_cast<const uint4*>(O), ppos, topk_w, D.k, dv, static_cast<uint4*>(y));
+  if (D.act_bf16)
+    combine_kernel<true><<<static_cast<unsigned>(D.T), row_threads(dq), 0, st>>>(
+        reinterpret_cast<const float4*>(O), ppos, topk_w, D.k, dq, y);
+  else
+    combine_kernel<false><<<static_cast<unsigned>(D.T), row_threads(dq), 0, st>>>(
+        reinterpret_cast<const float4*>(O), ppos, topk_w, D.k, dq, y);
   count_launch();
   return cudaGetLastError();
 }
@@ -443,17 +517,18 @@ cudaError_t launch_combine(const Dims& D, const void* O, const int32_t* ppos, co
 // -------------------------------------------------------- reverse dispatch --
 
 // One CTA per token.  Router backward first:
-//   dp_s = sum_j dp_part[row_s, j]      (fixed j order)
-//   dl_s = p_s (dp_s - sum_i p_i dp_i)  (softmax over the chosen k)
+//   dp_s = (sum_j dp_part[row_s, j]) / p_s    (fixed j order; the partials
+//          hold p_s <dy, O_s> because dO = p dy; dp_s is unused when p_s = 0)
+//   dl_s = p_s (dp_s - sum_i p_i dp_i)        (softmax over the chosen k)
 // then dx_t = sum_s (dX_perm[row_s] + dl_s * W_r[e_s])   in slot order.
-__global__ void reverse_dispatch_kernel(const uint4* __restrict__ dXp,
+template <bool BF16_OUT>
+__global__ void reverse_dispatch_kernel(const float4* __restrict__ dXp,
                                         const int32_t* __restrict__ ppos,
                                         const int32_t* __restrict__ topk_idx,
                                         const float* __restrict__ topk_w,
                                         const float* __restrict__ dp_part, int np,
-                                        const uint4* __restrict__ Wr, int k, int dv,
-                                        uint4* __restrict__ dx, float* __restrict__ dl_row,
-                                        float* __restrict__ dl_tok) {
+                                        const uint2* __restrict__ Wr, int k, int dq, void* dx,
+                                        float* __restrict__ dl_row, float* __restrict__ dl_tok) {
   __shared__ int s_row[kMaxTopK];
   __shared__ int s_e[kMaxTopK];
   __shared__ float s_dl[kMaxTopK];
@@ -466,9 +541,11 @@ __global__ void reverse_dispatch_kernel(const uint4* __restrict__ dXp,
       row = ppos[t * k + s];
       e = topk_idx[t * k + s];
       p = topk_w[t * k + s];
-      if (row >= 0) {
+      if (row >= 0 && p > 0.f) {
         const float* q = dp_part + static_cast<long long>(row) * np;
-        for (int j = 0; j < np; ++j) dp += q[j];
+        float acc = 0.f;
+        for (int j = 0; j < np; ++j) acc += q[j];
+        dp = acc / p;
       }
     }
     // c = sum_i p_i dp_i, summed in slot order by every lane
@@ -488,29 +565,37 @@ __global__ void reverse_dispatch_kernel(const uint4* __restrict__ dXp,
     }
   }
   __syncthreads();
-  for (int c = threadIdx.x; c < dv; c += blockDim.x) {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int c = threadIdx.x; c < dq; c += blockDim.x) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int s = 0; s < k; ++s) {
       if (s_row[s] < 0) continue;
-      add8(acc, ld_global_nc_v4(dXp + static_cast<long long>(s_row[s]) * dv + c));
-      axpy8(acc, s_dl[s], ld_global_nc_v4(Wr + static_cast<long long>(s_e[s]) * dv + c));
+      add4(acc, ld_nc_f4(dXp + static_cast<long long>(s_row[s]) * dq + c));
+      uint2 w;
+      asm volatile("ld.global.nc.v2.b32 {%0, %1}, [%2];"
+                   : "=r"(w.x), "=r"(w.y)
+                   : "l"(Wr + static_cast<long long>(s_e[s]) * dq + c));
+      axpy4(acc, s_dl[s], bf16x4_to_f4(w));
     }
-    dx[t * dv + c] = pack8(acc);
+    store4<BF16_OUT>(dx, t, dq, c, acc);
   }
 }
 
-cudaError_t launch_reverse_dispatch(const Dims& D, const void* dX_perm, const int32_t* ppos,
+cudaError_t launch_reverse_dispatch(const Dims& D, const float* dX_perm, const int32_t* ppos,
                                     const int32_t* topk_idx, const float* topk_w,
                                     const float* dp_part, const void* w_router, void* dx,
                                     float* dl_row, float* dl_tok, cudaStream_t st) {
   if (D.T == 0) return cudaSuccess;
-  const int dv = static_cast<int>(D.d / 8);
-  int th = row_threads(dv);
-  if (th < 32) th = 32;
+  const int dq = static_cast<int>(D.d / 4);
+  const int th = row_threads(dq);
   ProfScope prof("reverse_dispatch", st);
-  reverse_dispatch_kernel<<<static_cast<unsigned>(D.T), th, 0, st>>>(
-      static_cast<const uint4*>(dX_perm), ppos, topk_idx, topk_w, dp_part, D.np,
-      static_cast<const uint4*>(w_router), D.k, dv, static_cast<uint4*>(dx), dl_row, dl_tok);
+  if (D.act_bf16)
+    reverse_dispatch_kernel<true><<<static_cast<unsigned>(D.T), th, 0, st>>>(
+        reinterpret_cast<const float4*>(dX_perm), ppos, topk_idx, topk_w, dp_part, D.np,
+        static_cast<const uint2*>(w_router), D.k, dq, dx, dl_row, dl_tok);
+  else
+    reverse_dispatch_kernel<false><<<static_cast<unsigned>(D.T), th, 0, st>>>(
+        reinterpret_cast<const float4*>(dX_perm), ppos, topk_idx, topk_w, dp_part, D.np,
+        static_cast<const uint2*>(w_router), D.k, dq, dx, dl_row, dl_tok);
   count_launch();
   return cudaGetLastError();
 }
@@ -522,10 +607,18 @@ cudaError_t launch_reverse_dispatch(const Dims& D, const void* dX_perm, const in
 // row lane i takes rows i, i+32, ...; the 32 partials are then added in lane
 // order.  Fixed order throughout.
 constexpr int kRwRowLanes = 32;
+
+__device__ __forceinline__ void axpy8(float (&acc)[8], float w, uint4 v) {
+  acc[0] = fmaf(w, bf16lo(v.x), acc[0]); acc[1] = fmaf(w, bf16hi(v.x), acc[1]);
+  acc[2] = fmaf(w, bf16lo(v.y), acc[2]); acc[3] = fmaf(w, bf16hi(v.y), acc[3]);
+  acc[4] = fmaf(w, bf16lo(v.z), acc[4]); acc[5] = fmaf(w, bf16hi(v.z), acc[5]);
+  acc[6] = fmaf(w, bf16lo(v.w), acc[6]); acc[7] = fmaf(w, bf16hi(v.w), acc[7]);
+}
+
+template <bool BF16_OUT>
 __global__ void router_wgrad_kernel(const uint4* __restrict__ Xp, const float* __restrict__ dl_row,
                                     const int32_t* __restrict__ poff,
-                                    const int32_t* __restrict__ counts, int dv,
-                                    uint4* __restrict__ dw) {
+                                    const int32_t* __restrict__ counts, int dv, void* dw) {
   __shared__ float part[kRwRowLanes][8][8];
   const int e = blockIdx.x;
   const int cv = blockIdx.y * 8 + (threadIdx.x & 7);  // column vector index
@@ -546,7 +639,16 @@ __global__ void router_wgrad_kernel(const uint4* __restrict__ Xp, const float* _
     for (int l = 0; l < kRwRowLanes; ++l)
 #pragma unroll
       for (int j = 0; j < 8; ++j) tot[j] += part[l][threadIdx.x][j];
-    dw[static_cast<long long>(e) * dv + cv] = pack8(tot);
+    const long long o = static_cast<long long>(e) * dv + cv;
+    if (BF16_OUT) {
+      reinterpret_cast<uint4*>(dw)[o] =
+          make_uint4(pack_bf16x2(tot[0], tot[1]), pack_bf16x2(tot[2], tot[3]),
+                     pack_bf16x2(tot[4], tot[5]), pack_bf16x2(tot[6], tot[7]));
+    } else {
+      float4* q = reinterpret_cast<float4*>(dw) + 2 * o;
+      q[0] = make_float4(tot[0], tot[1], tot[2], tot[3]);
+      q[1] = make_float4(tot[4], tot[5], tot[6], tot[7]);
+    }
   }
 }
 
@@ -556,9 +658,12 @@ cudaError_t launch_router_wgrad(const Dims& D, const void* X_perm, const float* 
   const int dv = static_cast<int>(D.d / 8);
   dim3 grid(static_cast<unsigned>(D.E), static_cast<unsigned>((dv + 7) / 8));
   ProfScope prof("router_wgrad", st);
-  router_wgrad_kernel<<<grid, kRwRowLanes * 8, 0, st>>>(static_cast<const uint4*>(X_perm), dl_row,
-                                                        padded_offsets, counts, dv,
-                                                        static_cast<uint4*>(dw_router));
+  if (D.wgrad_bf16)
+    router_wgrad_kernel<true><<<grid, kRwRowLanes * 8, 0, st>>>(
+        static_cast<const uint4*>(X_perm), dl_row, padded_offsets, counts, dv, dw_router);
+  else
+    router_wgrad_kernel<false><<<grid, kRwRowLanes * 8, 0, st>>>(
+        static_cast<const uint4*>(X_perm), dl_row, padded_offsets, counts, dv, dw_router);
   count_launch();
   return cudaGetLastError();
 }

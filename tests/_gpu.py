@@ -36,10 +36,10 @@ def rel_err(got, ref) -> float:
     return diff / rms
 
 
-def run_gpu(shape: gen.Shape, inp: dict, layer=None):
+def run_gpu(shape: gen.Shape, inp: dict, layer=None, flags=0):
     """Forward + backward of one layer call; returns host copies."""
     if layer is None:
-        layer = api.MoELayer(shape.T, shape.d, shape.E, shape.I, shape.k)
+        layer = api.MoELayer(shape.T, shape.d, shape.E, shape.I, shape.k, flags=flags)
     x = dev_bf16(inp["x"])
     wr = dev_bf16(inp["w_router"])
     wgu = dev_bf16(inp["w_gate_up"])
@@ -98,8 +98,23 @@ def check_dispatch_valid(idx, counts, offsets, pos, token_of_row, E):
     assert (token_of_row[pos.ravel()] == tt).all()
 
 
+def check_bf16_intermediate(got_bf16: np.ndarray, ref: np.ndarray, name: str):
+    """A stored bf16 GEMM operand against the oracle's bf16 value: equal
+    except where float32 vs float64 accumulation lands on the other side of
+    a rounding boundary (rare), and then by one bf16 ulp."""
+    diff = got_bf16 != ref
+    frac = float(diff.mean()) if diff.size else 0.0
+    assert frac < 2e-3, (name, frac)
+    if diff.any():
+        a = np.abs(ref[diff])
+        ulp = 2.0 ** (np.floor(np.log2(np.maximum(a, 2.0 ** -126))) - 7)
+        assert (np.abs(got_bf16[diff] - ref[diff]) <= ulp * 1.0000001).all(), name
+    return frac
+
+
 def full_parity(shape: gen.Shape, inp: dict, gpu: dict, tol=BF16_TOL):
-    """Element-wise comparison of every output against the full oracle."""
+    """Element-wise comparison of every output against the full oracle (in
+    its BF16-operand mode, the precision the layer's GEMMs are defined in)."""
     assert gpu["status"] == 0, gpu["status"]
     bias = inp.get("bias")
     idx, p, logits, flagged, inner = oracle.route_ref(inp["x"], inp["w_router"], bias, shape.k)
@@ -115,7 +130,7 @@ def full_parity(shape: gen.Shape, inp: dict, gpu: dict, tol=BF16_TOL):
                          gpu["token_of_row"], shape.E)
 
     y, fwd = oracle.moe_forward_ref(inp["x"], inp["w_router"], bias, inp["w_gate_up"],
-                                    inp["w_down"], shape.k, keep=True)
+                                    inp["w_down"], shape.k, keep=True, precision="bf16")
     g = oracle.moe_backward_ref(inp["x"], inp["w_router"], bias, inp["w_gate_up"],
                                 inp["w_down"], shape.k, inp["dy"], fwd=fwd)
     errs = {}
@@ -126,8 +141,8 @@ def full_parity(shape: gen.Shape, inp: dict, gpu: dict, tol=BF16_TOL):
     gu = host64(gpu["gate_up"])
     rows_gpu = gpu["padded_pos"][tokens].ravel()
     rows_ref = pos[tokens].ravel()
-    errs["gate"] = rel_err(gu[rows_gpu, :shape.I], fwd["G"][rows_ref])
-    errs["up"] = rel_err(gu[rows_gpu, shape.I:], fwd["U"][rows_ref])
+    errs["gate_flips"] = check_bf16_intermediate(gu[rows_gpu, :shape.I], fwd["G"][rows_ref], "gate")
+    errs["up_flips"] = check_bf16_intermediate(gu[rows_gpu, shape.I:], fwd["U"][rows_ref], "up")
     # expert gradients: leave out experts touched by an undecided token
     touched = np.zeros(shape.E, dtype=bool)
     for t in np.nonzero(~tokens)[0]:
@@ -139,7 +154,8 @@ def full_parity(shape: gen.Shape, inp: dict, gpu: dict, tol=BF16_TOL):
     if all_same:
         errs["dw_router"] = rel_err(host64(gpu["dw_router"]), g["dw_router"])
     for name, v in errs.items():
-        assert v <= tol, (name, v, errs)
+        if not name.endswith("_flips"):
+            assert v <= tol, (name, v, errs)
     # experts that received no rows have exactly zero weight gradients
     empty = counts == 0
     if all_same and empty.any():

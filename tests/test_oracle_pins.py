@@ -372,7 +372,7 @@ def test_planted_unstable_dispatch_is_caught(monkeypatch):
 def test_planted_gate_up_swap_is_caught(monkeypatch):
     sh, inp = _tiny(seed=3, k=2)
 
-    def wrong(X, wgu, wd):
+    def wrong(X, wgu, wd, rnd=None):
         W = moe_ref.widen(wgu)
         I = W.shape[0] // 2
         U = X @ W[:I].T
@@ -382,3 +382,57 @@ def test_planted_gate_up_swap_is_caught(monkeypatch):
     monkeypatch.setattr(moe_ref, "expert_ffn", wrong)
     y = oracle.moe_forward_ref(inp["x"], inp["w_router"], None, inp["w_gate_up"], inp["w_down"], 2)
     assert np.abs(y - _dense_forward(inp, 2)).max() > 1e-3
+
+
+# ----------------------------------------------------------------------------
+# BF16-operand mode
+# ----------------------------------------------------------------------------
+
+def test_bf16_round_matches_bit_level_rounding():
+    """The oracle's frexp-based rounding against the generator's integer
+    bit-pattern rounding (two independent implementations), including exact
+    ties, subnormals and the largest finite values."""
+    rng = np.random.default_rng(0)
+    vals = [rng.standard_normal(20000).astype(np.float32),
+            (rng.standard_normal(2000) * 1e-39).astype(np.float32),
+            np.array([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -(1.0 + 2 ** -8), 3.3895313892515355e38,
+                      2.0 ** -126, 2.0 ** -133, 0.0, -0.0, 1e-45], dtype=np.float32)]
+    ties = (np.arange(1, 2000, dtype=np.uint32) << 16 | 0x8000).view(np.float32)
+    vals.append(ties)
+    for v in vals:
+        want = gen.bf16_bits_to_f32(gen.f32_to_bf16_bits(v)).astype(np.float64)
+        got = oracle.bf16_round(v.astype(np.float64))
+        assert np.array_equal(got, want)
+
+
+def test_bf16_mode_is_fp64_mode_plus_operand_rounding(monkeypatch):
+    sh, inp = _tiny(seed=1, k=2)
+    args = (inp["x"], inp["w_router"], None, inp["w_gate_up"], inp["w_down"], 2)
+    y64, f64 = oracle.moe_forward_ref(*args, keep=True)
+    g64 = oracle.moe_backward_ref(*args, inp["dy"], fwd=f64)
+    monkeypatch.setattr(moe_ref, "bf16_round", lambda a: a)
+    yb, fb = oracle.moe_forward_ref(*args, keep=True, precision="bf16")
+    gb = oracle.moe_backward_ref(*args, inp["dy"], fwd=fb)
+    assert np.array_equal(y64, yb)
+    for n in ("dx", "dw_router", "dw_gate_up", "dw_down"):
+        assert np.array_equal(g64[n], gb[n])
+
+
+def test_bf16_mode_operands_are_nearest_bf16():
+    sh, inp = _tiny(seed=2, k=2)
+    args = (inp["x"], inp["w_router"], None, inp["w_gate_up"], inp["w_down"], 2)
+    y64, f64 = oracle.moe_forward_ref(*args, keep=True)
+    yb, fb = oracle.moe_forward_ref(*args, keep=True, precision="bf16")
+    G, U, H = fb["G"], fb["U"], fb["H"]
+    for t in (G, U, H):
+        assert np.array_equal(t, oracle.bf16_round(t))
+    # within half an ulp of what the definition gives before rounding
+    def half_ulp(v):
+        e = np.floor(np.log2(np.maximum(np.abs(v), 2.0 ** -126)))
+        return 2.0 ** (e - 8)
+    assert (np.abs(G - f64["G"]) <= half_ulp(f64["G"])).all()
+    hpre = oracle.silu(G) * U
+    assert (np.abs(H - hpre) <= half_ulp(hpre)).all()
+    # bf16 operands change the result by bf16 noise, not more
+    rms = np.sqrt(np.mean(y64 ** 2))
+    assert 0 < np.abs(yb - y64).max() / rms < 0.05
