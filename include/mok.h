@@ -96,7 +96,7 @@ typedef struct mok_saved_layout {
   size_t padded_token;    /* int32 [rows_max] token of each padded row, -1 for padding */
   size_t row_weight;      /* fp32 [rows_max] routing weight of each padded row, 0 for padding */
   size_t x_perm;          /* bf16 [rows_max, d] dispatched token rows */
-  size_t gate_up;         /* bf16 [rows_max, 2I] pre-activation gate (cols 0..I-1) and up (I..2I-1) */
+  size_t gate_up;         /* fp32 [rows_max, 2I] pre-activation gate (cols 0..I-1) and up (I..2I-1) */
   size_t rows_max;        /* number of padded rows the buffers hold: T*k + 127*min(E, T*k), rounded to 128 */
   size_t total;           /* size of `saved` in bytes */
 } mok_saved_layout;
@@ -121,8 +121,8 @@ mok_status mok_moe_saved_layout(const mok_moe_desc* desc, mok_saved_layout* out)
  *   rows of expert e = tokens routed to e in ascending token order (dropless)
  *   [g | u] = X_e W_gu_e^T,  h = silu(g) * u,  O = h W_down_e^T
  *   y_t = sum_{s=0..k-1} p_{t,s} O[pos[t,s]]   (fp32 sum in slot order)
- * Every GEMM operand is bf16 (g and u are stored as bf16, h = bf16(silu(g) u));
- * accumulation is fp32; O stays fp32.
+ * Precision: bf16 inputs and weights; fp32 accumulation; g and u kept in
+ * fp32; h rounded to bf16 (the down GEMM's operand); O stays fp32.
  * x [T,d] bf16; w_router [E,d] bf16; router_bias [E] fp32 or NULL;
  * w_gate_up [E,2I,d] bf16 (gate rows 0..I-1, up rows I..2I-1);
  * w_down [E,d,I] bf16; y [T,d] output, fp32 (bf16 with MOK_FLAG_BF16_ACT_OUT).
@@ -137,8 +137,10 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
  * ([dothoosh] "Hybrid communication": reverse-combine, then reverse-dispatch;
  * "Precision and scheduling": router-weight gradient inside the SwiGLU
  * backward, dp = <dy W_down, h>):
- *   dO = bf16(p * dy) per routed row, dH = dO W_down, dG and dU in bf16 from
- *   dH and the stored g, u; dX rows fp32; weight gradients from bf16 operands.
+ *   dA = dy_r W_down per routed row, dH = p dA (fp32), dp = <dA, h>;
+ *   dG, dU from dH and the stored fp32 g, u; the gate/up dgrad takes them
+ *   rounded to bf16 (dX rows fp32); the two weight-gradient GEMMs take dG, dU
+ *   and p h as bf16 hi + lo pairs (about 16 significant bits).
  *   dx [T,d], dw_router [E,d], dw_gate_up [E,2I,d], dw_down [E,d,I]:
  *   outputs, overwritten, fp32 (bf16 with the MOK_FLAG_BF16_* flags); fp32
  *   accumulation inside, one writer per element, fixed summation order.

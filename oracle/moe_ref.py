@@ -29,11 +29,14 @@ scheduling": the megakernel runs its GEMMs in BF16): every operand of the six
 expert GEMMs is a bf16 value, each GEMM accumulates exactly (float64), and
 nothing that is not a GEMM operand is rounded.  The rounded operands are
   G, U            (outputs of the gate/up GEMM, stored as bf16)
-  H = silu(G) U   (operand of the down GEMM and of its weight gradient)
-  dO = p * dy     (operand of the down dgrad and of its weight gradient)
+  H = silu(G) U   (operand of the down GEMM)
+  P = p * H       (operand of the down-projection weight gradient,
+                   dW_down = sum_r dy_r (p_r h_r)^T)
   dG, dU          (operands of the gate/up dgrad and weight gradient)
-each rounded to the nearest bf16 (ties to even).  The expert output O, y, dp,
-the router gradient, dx and the weight gradients are not rounded.
+each rounded to the nearest bf16 (ties to even).  dy is itself a bf16 input,
+so the down dgrad dH = p * (dy W_down) needs no rounded operand.  The expert
+output O, y, dp, the router gradient, dx and the weight gradients are not
+rounded.
 
 Readings where the pages say nothing (all are listed again in the design notes):
   * routing weights are a softmax over the k chosen logits (equal to the full
@@ -275,7 +278,7 @@ def moe_backward_ref(x, w_router, bias, w_gate_up, w_down, k: int, dy,
     row_p = np.empty(R)
     for s in range(k):
         row_p[pos[:, s]] = p[:, s]
-    dO = rnd(row_p[:, None] * dY[row_t])
+    dO = row_p[:, None] * dY[row_t]
     dp = np.einsum("tsd,td->ts", O[pos], dY)
 
     dX_rows = np.zeros((R, d))
@@ -297,7 +300,8 @@ def moe_backward_ref(x, w_router, bias, w_gate_up, w_down, k: int, dy,
         Xe = X[tok[a:b]]
         dX_rows[a:b] = dG @ Wgu[:I] + dU @ Wgu[I:]
         if grad_experts is None or e in dw_down:
-            dw_down[e][...] = dO[a:b].T @ H[a:b]    # [d, I]
+            # sum_r p_r dy_r h_r^T, with p applied on the h side
+            dw_down[e][...] = dY[row_t[a:b]].T @ rnd(row_p[a:b, None] * H[a:b])
             dw_gate_up[e][:I] = dG.T @ Xe
             dw_gate_up[e][I:] = dU.T @ Xe
 

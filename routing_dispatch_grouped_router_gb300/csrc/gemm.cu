@@ -9,8 +9,8 @@
 //   [dothoosh] "Cursor Mixture-of-Kittens cuts MoE training latency by 5.8x",
 //     "MoK technical details", bullet "Overlap granularity": every
 //     expert-grouped GEMM is given at least two full waves of SMs; bullet
-//     "Precision and scheduling": SwiGLU backward fused with the router-weight
-//     gradient.
+//     "Precision and scheduling": BF16 GEMMs, SwiGLU backward fused with the
+//     router-weight gradient.
 //
 // Design (one CTA per SM, 320 threads):
 //   warp 0      TMA producer: 128B-swizzled tiles of A (128 x 64) and B
@@ -21,8 +21,10 @@
 //               commits stage release / accumulator-ready to mbarriers.
 //   warps 2..9  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
 //               lanes 32*(w%4).., columns half (w-2)/4), fused math, stores.
-//               Double-buffered accumulators let tile i's epilogue overlap
-//               tile i+1's MMAs.
+//               fp32 results leave through a per-warp 4 KB swizzled staging
+//               buffer and a TMA tensor store (32 x 32 box), so HBM sees whole
+//               128-byte lines.  Double-buffered accumulators let tile i's
+//               epilogue overlap tile i+1's MMAs.
 // Tiles are walked in a static round-robin (tile = blockIdx.x + i*gridDim.x),
 // every tile is computed by exactly one CTA with a fixed K order, so results
 // are bitwise reproducible.  Per-expert tile tables come from the dispatch
@@ -42,6 +44,10 @@ namespace mok {
 
 enum Sched : int { SCHED_DENSE = 0, SCHED_MGROUP = 1, SCHED_KGROUP = 2 };
 enum Epi : int { EPI_BF16 = 0, EPI_F32 = 1, EPI_SWIGLU_FWD = 2, EPI_SWIGLU_BWD = 3 };
+// Split operands: a bf16 "hi" tile plus a bf16 "lo" tile (value - hi) whose
+// products are accumulated into the same fp32 accumulator, giving the GEMM
+// an operand with ~16 significant bits.
+enum Split : int { SPLIT_NONE = 0, SPLIT_A = 1, SPLIT_B = 2 };
 
 struct GemmArgs {
   int E;             // groups (experts); 1 for dense
@@ -49,6 +55,7 @@ struct GemmArgs {
   int n_tiles;       // N tiles
   int num_kb;        // DENSE/MGROUP: K / 64
   int b_group_rows;  // MGROUP: rows of B per expert in its 2-D view
+  int m_rows;        // KGROUP: rows of C per group (C viewed as [E*m_rows, N])
   int I;             // SwiGLU epilogues: FFN width
   int m_valid, n_valid;  // DENSE: valid rows / columns of C
   const int* mtile_prefix;  // MGROUP: [E+1] prefix of 128-row tiles per expert
@@ -56,62 +63,74 @@ struct GemmArgs {
   void* out;                // C (bf16 or fp32)
   long long ldo;            // C row stride (elements)
   long long out_group_stride;  // KGROUP: elements between experts' C
-  void* out2;               // SWIGLU_FWD and SWIGLU_BWD: H [rows,I] bf16
-  const void* in_gu;        // SWIGLU_BWD: saved pre-activations [rows,2I]
+  void* out2;               // SWIGLU_FWD: H [rows,I]; SWIGLU_BWD: P_hi = bf16(p*h) [rows,I]
+  void* out3;               // SWIGLU_BWD: dGU_lo [rows,2I]
+  void* out4;               // SWIGLU_BWD: P_lo [rows,I]
+  const void* in_gu;        // SWIGLU_BWD: saved fp32 pre-activations [rows,2I]
+  const float* row_w;       // SWIGLU_BWD: routing weight of each row
   float* dp_part;           // SWIGLU_BWD: [rows, np] partial <dA,h>
   int np;
   int* status;
 };
 
-template <int BN>
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
+constexpr int kStagingBytes = 4096;  // per epilogue warp: 32 rows x 128 bytes
+
+template <int BN, int SPLIT = SPLIT_NONE>
 struct Cfg {
   static constexpr int BM = 128, BK = 64;
   static constexpr int A_BYTES = BM * BK * 2;  // 16 KB
   static constexpr int B_BYTES = BN * BK * 2;  // 32 KB (BN=256) / 16 KB (BN=128)
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int A_TILES = SPLIT == SPLIT_A ? 2 : 1;
+  static constexpr int B_TILES = SPLIT == SPLIT_B ? 2 : 1;
+  static constexpr int B_OFF = A_TILES * A_BYTES;  // B tile(s) follow the A tile(s)
+  static constexpr int STAGE_BYTES = A_TILES * A_BYTES + B_TILES * B_BYTES;
+  static constexpr int STAGES = (196608 / STAGE_BYTES) < 6 ? (196608 / STAGE_BYTES) : 6;
   static constexpr int TMEM_COLS = 2 * BN;
-  static constexpr int BAR_BYTES = 1024;
-  static constexpr int PREFIX_BYTES = 4 * (kMaxExperts + 1);
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + PREFIX_BYTES;
+  static constexpr int STAGING_OFF = STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFF = STAGING_OFF + kEpiWarps * kStagingBytes;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM_BYTES = 1024 + BAR_OFF + BAR_BYTES;
 };
 static_assert(Cfg<256>::SMEM_BYTES <= 232448, "smem");
 static_assert(Cfg<128>::SMEM_BYTES <= 232448, "smem");
-
-constexpr int kThreads = 320;
-constexpr int kEpiWarps = 8;
+static_assert(Cfg<256, SPLIT_A>::SMEM_BYTES <= 232448 && Cfg<256, SPLIT_A>::STAGES >= 3, "smem");
+static_assert(Cfg<128, SPLIT_B>::SMEM_BYTES <= 232448 && Cfg<128, SPLIT_B>::STAGES >= 4, "smem");
 
 struct Tile {
   int e, m_tile, n_tile;
-  int row0;    // MGROUP/DENSE: first row of A and C
+  int row0;    // MGROUP/DENSE: first row of A and C; KGROUP: first row of C_e
   int k_row0;  // KGROUP: first K row (padded offset of the expert)
   int num_kb;
 };
 
 template <int SCHED>
-__device__ __forceinline__ int total_tiles(const GemmArgs& a, const int* s_prefix) {
-  if (SCHED == SCHED_MGROUP) return s_prefix[a.E] * a.n_tiles;
+__device__ __forceinline__ int total_tiles(const GemmArgs& a) {
+  if (SCHED == SCHED_MGROUP) return __ldg(a.mtile_prefix + a.E) * a.n_tiles;
   if (SCHED == SCHED_KGROUP) return a.E * a.m_tiles * a.n_tiles;
   return a.m_tiles * a.n_tiles;
 }
 
 template <int SCHED>
-__device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const int* s_prefix, int t) {
+__device__ __forceinline__ Tile decode_tile(const GemmArgs& a, int t) {
   Tile tl;
   if (SCHED == SCHED_MGROUP) {
-    // largest e with s_prefix[e] * n_tiles <= t
-    int lo = 0, hi = a.E;  // invariant: s_prefix[lo]*nt <= t < s_prefix[hi]*nt
+    // largest e with prefix[e] * n_tiles <= t (empty experts are skipped)
+    const int* pre = a.mtile_prefix;
+    int lo = 0, hi = a.E;  // invariant: pre[lo]*nt <= t < pre[hi]*nt
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (s_prefix[mid] * a.n_tiles <= t) lo = mid; else hi = mid;
+      if (__ldg(pre + mid) * a.n_tiles <= t) lo = mid; else hi = mid;
     }
     const int e = lo;
-    const int mt_e = s_prefix[e + 1] - s_prefix[e];
-    const int local = t - s_prefix[e] * a.n_tiles;
+    const int p0 = __ldg(pre + e);
+    const int mt_e = __ldg(pre + e + 1) - p0;
+    const int local = t - p0 * a.n_tiles;
     tl.e = e;
     tl.n_tile = local / mt_e;
     tl.m_tile = local - tl.n_tile * mt_e;
-    tl.row0 = a.poff[e] + tl.m_tile * 128;
+    tl.row0 = __ldg(a.poff + e) + tl.m_tile * 128;
     tl.k_row0 = 0;
     tl.num_kb = a.num_kb;
   } else if (SCHED == SCHED_KGROUP) {
@@ -122,7 +141,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, const int* s_pref
     tl.n_tile = local / a.m_tiles;
     tl.m_tile = local - tl.n_tile * a.m_tiles;
     tl.row0 = tl.m_tile * 128;
-    const int k0 = a.poff[e], k1 = a.poff[e + 1];
+    const int k0 = __ldg(a.poff + e), k1 = __ldg(a.poff + e + 1);
     tl.k_row0 = k0;
     tl.num_kb = (k1 - k0) / 64;
   } else {
@@ -179,12 +198,69 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* p, float (&v)[
   }
 }
 
+// Stores 16 values as bf16 hi = bf16(v) and lo = bf16(v - hi).
+__device__ __forceinline__ void store_hi_lo16(__nv_bfloat16* hi, __nv_bfloat16* lo,
+                                              const float (&v)[16]) {
+  uint32_t h[8], l[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float a0 = bf16_round(v[2 * j]), a1 = bf16_round(v[2 * j + 1]);
+    h[j] = pack_bf16x2(a0, a1);
+    l[j] = pack_bf16x2(v[2 * j] - a0, v[2 * j + 1] - a1);
+  }
+  uint4* ph = reinterpret_cast<uint4*>(hi);
+  uint4* pl = reinterpret_cast<uint4*>(lo);
+  ph[0] = make_uint4(h[0], h[1], h[2], h[3]);
+  ph[1] = make_uint4(h[4], h[5], h[6], h[7]);
+  pl[0] = make_uint4(l[0], l[1], l[2], l[3]);
+  pl[1] = make_uint4(l[4], l[5], l[6], l[7]);
+}
+
+// One warp writes its 32 rows x 32 fp32 columns to the 4 KB staging buffer in
+// the 128-byte swizzled layout (16-byte chunk j of row r at chunk j ^ (r%8)),
+// then lane 0 stores it with one TMA tensor store at (x, y).
+__device__ __forceinline__ void stage_and_store_f32(uint8_t* buf, const CUtensorMap* tmC,
+                                                    const float (&v)[32], int lane, int x, int y) {
+  if (lane == 0) bulk_wait_read<0>();  // the previous store has read the buffer
+  __syncwarp();
+  uint8_t* row = buf + lane * 128;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int pj = j ^ (lane & 7);
+    *reinterpret_cast<float4*>(row + pj * 16) =
+        make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmC, buf, x, y);
+    bulk_commit();
+  }
+}
+
 template <int BN, int SCHED, int EPI>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl, uint32_t taddr,
-                                              int row_in_tile, int half) {
+                                              int q, int lane, int half, uint8_t* stage_buf,
+                                              const CUtensorMap* tmC) {
   constexpr int HALF_COLS = BN / 2;
+  const int row_in_tile = q * 32 + lane;
   const bool zero_k = (tl.num_kb == 0);
-  if (EPI == EPI_BF16 || EPI == EPI_F32) {
+  if (EPI == EPI_F32 && SCHED != SCHED_DENSE) {
+    // fp32 C through TMA stores; C viewed as 2-D [rows, N]
+    const int y = (SCHED == SCHED_KGROUP ? tl.e * a.m_rows : 0) + tl.row0 + q * 32;
+    const int col0 = tl.n_tile * BN + half * HALF_COLS;
+#pragma unroll 1
+    for (int c = 0; c < HALF_COLS; c += 32) {
+      float v[32];
+      if (!zero_k) {
+        tmem_ld32(taddr + half * HALF_COLS + c, v);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.f;
+      }
+      stage_and_store_f32(stage_buf, tmC, v, lane, col0 + c, y);
+    }
+  } else if (EPI == EPI_BF16 || EPI == EPI_F32) {
     constexpr int esz = EPI == EPI_F32 ? 4 : 2;
     const long long grow = tl.row0 + row_in_tile;
     char* base = static_cast<char*>(a.out);
@@ -204,7 +280,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
       if (EPI == EPI_BF16) {
         __nv_bfloat16* p = reinterpret_cast<__nv_bfloat16*>(base) + grow * a.ldo + col0 + c;
         store_bf16x32(p, v);
-      } else if (SCHED == SCHED_DENSE) {
+      } else {
         // router logits: the last column tile may extend past N
         float* p = reinterpret_cast<float*>(base) + grow * a.ldo;
 #pragma unroll
@@ -212,21 +288,17 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
           const int col = col0 + c + j;
           if (col < a.n_valid) p[col] = v[j];
         }
-      } else {
-        float4* p = reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + grow * a.ldo +
-                                              col0 + c);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          p[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
       }
     }
   } else if (EPI == EPI_SWIGLU_FWD) {
     // BN = 256: accumulator columns [0,128) gate, [128,256) up, for FFN
     // columns n0 .. n0+127 with n0 = n_tile*128.  This thread: 64 of them.
+    // g and u are kept in fp32 (TMA stores into GU [rows, 2I]); h = silu(g) u
+    // is rounded to bf16, the operand of the down projection.
     const long long r = tl.row0 + row_in_tile;
     const int I = a.I;
     const int n0 = tl.n_tile * 128 + half * 64;
-    __nv_bfloat16* gu = static_cast<__nv_bfloat16*>(a.out) + r * (2LL * I);
+    const int y = tl.row0 + q * 32;
     __nv_bfloat16* h = static_cast<__nv_bfloat16*>(a.out2) + r * (long long)I;
 #pragma unroll 1
     for (int c = 0; c < 64; c += 32) {
@@ -235,49 +307,63 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
       tmem_ld32(taddr + 128 + half * 64 + c, u);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        g[j] = bf16_round(g[j]);
-        u[j] = bf16_round(u[j]);
         float s;
         hv[j] = silu_f(g[j], &s) * u[j];
       }
-      store_bf16x32(gu + n0 + c, g);
-      store_bf16x32(gu + I + n0 + c, u);
       store_bf16x32(h + n0 + c, hv);
+      stage_and_store_f32(stage_buf, tmC, g, lane, n0 + c, y);
+      stage_and_store_f32(stage_buf, tmC, u, lane, I + n0 + c, y);
     }
   } else if (EPI == EPI_SWIGLU_BWD) {
-    // accumulator = dH = dO W_down for BN columns of I (n0 = n_tile*BN), with
-    // dO = p * dy already in the A operand.  SwiGLU backward from the stored
-    // bf16 g, u:  dG = dH * u * sigma(g) (1 + g (1 - sigma(g))),
-    //             dU = dH * silu(g);
-    // h = bf16(silu(g) u) is rebuilt bit-identically to the forward's (it is
-    // the B operand of the down-projection weight gradient), and
-    // sum_j dH_j h_j = p <dy, O> is accumulated for the router gradient.
+    // accumulator = dA = dY_perm W_down for BN columns of I (n0 = n_tile*BN).
+    // From the stored fp32 g, u and the row's routing weight p:
+    //   h  = silu(g) u;   dp += dA . h      (router-weight gradient partial)
+    //   dh = p dA;  dG = dh u sigma(g) (1 + g (1 - sigma(g)));  dU = dh silu(g)
+    //   dG, dU -> bf16 hi (operand of the gate/up dgrad) and bf16 lo (value
+    //             minus hi; hi + lo is the gate/up wgrad operand)
+    //   P = p h -> bf16 hi + lo (the down-projection wgrad operand)
     const long long r = tl.row0 + row_in_tile;
     const int I = a.I;
     const int n0 = tl.n_tile * BN + half * HALF_COLS;
-    const __nv_bfloat16* gu = static_cast<const __nv_bfloat16*>(a.in_gu) + r * (2LL * I);
-    __nv_bfloat16* dgu = static_cast<__nv_bfloat16*>(a.out) + r * (2LL * I);
-    __nv_bfloat16* hout = static_cast<__nv_bfloat16*>(a.out2) + r * (long long)I;
+    const float* gu = static_cast<const float*>(a.in_gu) + r * (2LL * I);
+    __nv_bfloat16* dgu_hi = static_cast<__nv_bfloat16*>(a.out) + r * (2LL * I);
+    __nv_bfloat16* dgu_lo = static_cast<__nv_bfloat16*>(a.out3) + r * (2LL * I);
+    __nv_bfloat16* p_hi = static_cast<__nv_bfloat16*>(a.out2) + r * (long long)I;
+    __nv_bfloat16* p_lo = static_cast<__nv_bfloat16*>(a.out4) + r * (long long)I;
+    const float p = a.row_w[r];
     float dp = 0.f;
 #pragma unroll 1
-    for (int c = 0; c < HALF_COLS; c += 32) {
-      float dH[32], g[32], u[32], o1[32];
-      tmem_ld32(taddr + half * HALF_COLS + c, dH);
-      load_bf16x32(gu + n0 + c, g);
-      load_bf16x32(gu + I + n0 + c, u);
+    for (int c = 0; c < HALF_COLS; c += 16) {
+      float dA[16], g[16], u[16], dg[16], du[16], ph[16];
+      {
+        uint32_t rr[16];
+        tmem_ld16(taddr + half * HALF_COLS + c, rr);
+        const float4* gp = reinterpret_cast<const float4*>(gu + n0 + c);
+        const float4* up = reinterpret_cast<const float4*>(gu + I + n0 + c);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < 4; ++j) {
+          const float4 a4 = gp[j], b4 = up[j];
+          g[4 * j] = a4.x; g[4 * j + 1] = a4.y; g[4 * j + 2] = a4.z; g[4 * j + 3] = a4.w;
+          u[4 * j] = b4.x; u[4 * j + 1] = b4.y; u[4 * j + 2] = b4.z; u[4 * j + 3] = b4.w;
+        }
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) dA[j] = __uint_as_float(rr[j]);
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
         float s;
         const float sl = silu_f(g[j], &s);
-        const float hv = bf16_round(sl * u[j]);
-        dp = fmaf(dH[j], hv, dp);
-        o1[j] = dH[j] * u[j] * (s * (1.0f + g[j] * (1.0f - s)));  // d gate
-        u[j] = dH[j] * sl;                                        // d up
-        g[j] = hv;                                                // h
+        const float hv = sl * u[j];
+        dp = fmaf(dA[j], hv, dp);
+        const float dh = p * dA[j];
+        dg[j] = dh * u[j] * (s * (1.0f + g[j] * (1.0f - s)));
+        du[j] = dh * sl;
+        ph[j] = p * hv;
       }
-      store_bf16x32(dgu + n0 + c, o1);
-      store_bf16x32(dgu + I + n0 + c, u);
-      store_bf16x32(hout + n0 + c, g);
+      store_hi_lo16(dgu_hi + n0 + c, dgu_lo + n0 + c, dg);
+      store_hi_lo16(dgu_hi + I + n0 + c, dgu_lo + I + n0 + c, du);
+      store_hi_lo16(p_hi + n0 + c, p_lo + n0 + c, ph);
     }
     a.dp_part[r * a.np + tl.n_tile * 2 + half] = dp;
   }
@@ -285,23 +371,26 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
 
 // ------------------------------------------------------------------- kernel --
 
-template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI>
+template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, int SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmL,
                 const __grid_constant__ GemmArgs args) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, SPLIT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* tiles = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint8_t* staging = smem + C::STAGING_OFF;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  int* s_prefix = reinterpret_cast<int*>(smem + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES);
+  constexpr bool kTmaStore =
+      (EPI == EPI_F32 && SCHED != SCHED_DENSE) || EPI == EPI_SWIGLU_FWD;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -322,9 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 32) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-  }
-  if (SCHED == SCHED_MGROUP) {
-    for (int i = threadIdx.x; i <= args.E; i += blockDim.x) s_prefix[i] = args.mtile_prefix[i];
+    if (kTmaStore) tma_prefetch_desc(&tmC);
+    if (SPLIT != SPLIT_NONE) tma_prefetch_desc(&tmL);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -335,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   volatile int* vabort = abort_flag;
-  const int total = total_tiles<SCHED>(args, s_prefix);
+  const int total = total_tiles<SCHED>(args);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -347,24 +435,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < C::STAGES; ++s) issued_par[s] = -1;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode_tile<SCHED>(args, s_prefix, t);
+        const Tile tl = decode_tile<SCHED>(args, t);
         for (int kb = 0; kb < tl.num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, vabort)) {
             ok = false;
             break;
           }
           uint8_t* sA = tiles + stage * C::STAGE_BYTES;
-          uint8_t* sB = sA + C::A_BYTES;
+          uint8_t* sB = sA + C::B_OFF;
           mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          // A tile: 128 rows (M) x 64 (K)
+          // A tile: 128 rows (M) x 64 (K)  (+ its lo tile with SPLIT_A)
           if (!A_MN) {
-            const int kx = (SCHED == SCHED_KGROUP ? tl.k_row0 : 0) + kb * 64;
-            tma_load_2d(sA, &tmA, &full[stage], kx, tl.row0);
+            tma_load_2d(sA, &tmA, &full[stage], kb * 64, tl.row0);
           } else {
             const int ky = tl.k_row0 + kb * 64;
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
+            for (int j = 0; j < 2; ++j) {
               tma_load_2d(sA + j * 8192, &tmA, &full[stage], tl.row0 + 64 * j, ky);
+              if (SPLIT == SPLIT_A)
+                tma_load_2d(sA + C::A_BYTES + j * 8192, &tmL, &full[stage], tl.row0 + 64 * j, ky);
+            }
           }
           // B tile: BN rows (N) x 64 (K)
           if (!B_MN) {
@@ -381,8 +471,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (SCHED == SCHED_KGROUP) ky = tl.k_row0 + kb * 64;
             else ky = tl.e * args.b_group_rows + kb * 64;
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
+            for (int j = 0; j < BN / 64; ++j) {
               tma_load_2d(sB + j * 8192, &tmB, &full[stage], tl.n_tile * BN + 64 * j, ky);
+              if (SPLIT == SPLIT_B)
+                tma_load_2d(sB + C::B_BYTES + j * 8192, &tmL, &full[stage],
+                            tl.n_tile * BN + 64 * j, ky);
+            }
           }
           issued_par[stage] = static_cast<int>(phase);
           if (++stage == C::STAGES) {
@@ -413,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-        const Tile tl = decode_tile<SCHED>(args, s_prefix, t);
+        const Tile tl = decode_tile<SCHED>(args, t);
         const int acc = it & 1;
         const uint32_t acc_par = static_cast<uint32_t>((it >> 1) & 1);
         if (!mbar_wait(&tempty[acc], acc_par ^ 1u, vabort)) {
@@ -429,12 +523,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after_sync();
           const uint32_t a_base = smem_addr(tiles + stage * C::STAGE_BYTES);
-          const uint32_t b_base = a_base + C::A_BYTES;
+          const uint32_t b_base = a_base + C::B_OFF;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint64_t ad = smem_desc_sw128(a_base + j * kstep_a, lbo_a, 1024);
             const uint64_t bd = smem_desc_sw128(b_base + j * kstep_b, lbo_b, 1024);
             mma_bf16(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
+            if (SPLIT == SPLIT_A) {
+              const uint64_t ad2 = smem_desc_sw128(a_base + C::A_BYTES + j * kstep_a, lbo_a, 1024);
+              mma_bf16(d_tmem, ad2, bd, idesc, 1u);
+            } else if (SPLIT == SPLIT_B) {
+              const uint64_t bd2 = smem_desc_sw128(b_base + C::B_BYTES + j * kstep_b, lbo_b, 1024);
+              mma_bf16(d_tmem, ad, bd2, idesc, 1u);
+            }
           }
           mma_commit(&empty[stage]);
           if (++stage == C::STAGES) {
@@ -457,10 +558,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------------- epilogue --
     const int q = warp & 3;                // TMEM lane quarter this warp may read
     const int half = (warp - 2) >> 2;      // column half of the tile
-    const int row_in_tile = q * 32 + lane;
+    uint8_t* stage_buf = staging + (warp - 2) * kStagingBytes;
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-      const Tile tl = decode_tile<SCHED>(args, s_prefix, t);
+      const Tile tl = decode_tile<SCHED>(args, t);
       const int acc = it & 1;
       const uint32_t acc_par = static_cast<uint32_t>((it >> 1) & 1);
       if (!mbar_wait(&tfull[acc], acc_par, vabort)) {
@@ -471,11 +572,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      epilogue_tile<BN, SCHED, EPI>(args, tl, taddr, row_in_tile, half);
+      epilogue_tile<BN, SCHED, EPI>(args, tl, taddr, q, lane, half, stage_buf, &tmC);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
     }
+    if (kTmaStore && lane == 0) bulk_wait_all<0>();  // stores complete before exit
   }
 
   __syncthreads();
@@ -506,35 +608,49 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 map over a row-major [outer, inner] array with row stride
-// `row_elems`, box {64, box_rows}, 128-byte swizzle, zero fill out of bounds.
-static bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-                     uint64_t row_elems, uint32_t box_rows) {
+// 2-D map over a row-major [outer, inner] array with row stride `row_elems`,
+// box {box_inner, box_rows}, 128-byte swizzle, zero fill out of bounds.
+static bool make_map_t(CUtensorMap* m, CUtensorMapDataType dt, int esz, const void* base,
+                       uint64_t inner, uint64_t outer, uint64_t row_elems, uint32_t box_inner,
+                       uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   if (outer == 0) outer = 1;  // empty operand: the map exists but is never read
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {row_elems * 2};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint64_t strides[1] = {row_elems * esz};
+  cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI>
+// bf16 operand map, box {64, box_rows}
+static bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                     uint64_t row_elems, uint32_t box_rows) {
+  return make_map_t(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, inner, outer, row_elems, 64,
+                    box_rows);
+}
+
+// fp32 output map for the TMA-store epilogue, box {32, 32}
+static bool make_out_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+  return make_map_t(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, cols, rows, cols, 32, 32);
+}
+
+template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, int SPLIT = SPLIT_NONE>
 static cudaError_t launch(const char* name, const CUtensorMap& ta, const CUtensorMap& tb,
-                          const GemmArgs& args, int max_tiles, cudaStream_t st) {
-  auto kern = gemm_kernel<BN, A_MN, B_MN, SCHED, EPI>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Cfg<BN>::SMEM_BYTES);
+                          const CUtensorMap& tc, const GemmArgs& args, int max_tiles,
+                          cudaStream_t st, const CUtensorMap* tl = nullptr) {
+  auto kern = gemm_kernel<BN, A_MN, B_MN, SCHED, EPI, SPLIT>;
+  constexpr int smem = Cfg<BN, SPLIT>::SMEM_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (max_tiles <= 0) return cudaSuccess;
   int grid = num_sms_current_device();
   if (max_tiles < grid) grid = max_tiles;
   ProfScope prof(name, st);
-  kern<<<grid, kThreads, Cfg<BN>::SMEM_BYTES, st>>>(ta, tb, args);
+  kern<<<grid, kThreads, smem, st>>>(ta, tb, tc, tl ? *tl : ta, args);
   count_launch();
   return cudaGetLastError();
 }
@@ -551,9 +667,10 @@ static inline int max_mtiles(const Dims& D) { return static_cast<int>(D.rows_max
 cudaError_t gemm_fwd_gate_up(const Dims& D, const void* X_perm, const void* w_gate_up,
                              const int32_t* mtile_prefix, const int32_t* poff, void* GU, void* H,
                              int* status, cudaStream_t st) {
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   if (!make_map(&ta, X_perm, D.d, D.rows_max, D.d, 128)) return cudaErrorInvalidValue;
   if (!make_map(&tb, w_gate_up, D.d, D.E * 2 * D.I, D.d, 128)) return cudaErrorInvalidValue;
+  if (!make_out_map(&tc, GU, 2 * D.I, D.rows_max)) return cudaErrorInvalidValue;
   GemmArgs a = blank_args(status);
   a.E = (int)D.E;
   a.n_tiles = (int)(D.I / 128);
@@ -564,17 +681,18 @@ cudaError_t gemm_fwd_gate_up(const Dims& D, const void* X_perm, const void* w_ga
   a.poff = poff;
   a.out = GU;
   a.out2 = H;
-  return launch<256, false, false, SCHED_MGROUP, EPI_SWIGLU_FWD>("fwd_gate_up_swiglu", ta, tb, a,
-                                                                  max_mtiles(D) * a.n_tiles, st);
+  return launch<256, false, false, SCHED_MGROUP, EPI_SWIGLU_FWD>(
+      "fwd_gate_up_swiglu", ta, tb, tc, a, max_mtiles(D) * a.n_tiles, st);
 }
 
 cudaError_t gemm_fwd_down(const Dims& D, const void* H, const void* w_down,
                           const int32_t* mtile_prefix, const int32_t* poff, void* O, int* status,
                           cudaStream_t st) {
   const int bn = (D.d % 256 == 0) ? 256 : 128;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   if (!make_map(&ta, H, D.I, D.rows_max, D.I, 128)) return cudaErrorInvalidValue;
   if (!make_map(&tb, w_down, D.I, D.E * D.d, D.I, bn)) return cudaErrorInvalidValue;
+  if (!make_out_map(&tc, O, D.d, D.rows_max)) return cudaErrorInvalidValue;
   GemmArgs a = blank_args(status);
   a.E = (int)D.E;
   a.n_tiles = (int)(D.d / bn);
@@ -585,17 +703,18 @@ cudaError_t gemm_fwd_down(const Dims& D, const void* H, const void* w_down,
   a.out = O;  // fp32 [rows_max, d]
   a.ldo = D.d;
   const int mt = max_mtiles(D) * a.n_tiles;
-  if (bn == 256) return launch<256, false, false, SCHED_MGROUP, EPI_F32>("fwd_down", ta, tb, a, mt, st);
-  return launch<128, false, false, SCHED_MGROUP, EPI_F32>("fwd_down", ta, tb, a, mt, st);
+  if (bn == 256)
+    return launch<256, false, false, SCHED_MGROUP, EPI_F32>("fwd_down", ta, tb, tc, a, mt, st);
+  return launch<128, false, false, SCHED_MGROUP, EPI_F32>("fwd_down", ta, tb, tc, a, mt, st);
 }
 
-cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dO, const void* w_down,
-                                const int32_t* mtile_prefix, const int32_t* poff, const void* GU,
-                                void* dGU, void* H, float* dp_part, int* status,
-                                cudaStream_t st) {
+cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* w_down,
+                                const int32_t* mtile_prefix, const int32_t* poff, const float* GU,
+                                const float* row_w, void* dGU_hi, void* dGU_lo, void* P_hi,
+                                void* P_lo, float* dp_part, int* status, cudaStream_t st) {
   const int bn = D.bn_dgrad;
   CUtensorMap ta, tb;
-  if (!make_map(&ta, dO, D.d, D.rows_max, D.d, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&ta, dY_perm, D.d, D.rows_max, D.d, 128)) return cudaErrorInvalidValue;
   // W_down_e viewed as [K = d rows, N = I columns]: N-major operand
   if (!make_map(&tb, w_down, D.I, D.E * D.d, D.I, 64)) return cudaErrorInvalidValue;
   GemmArgs a = blank_args(status);
@@ -606,24 +725,31 @@ cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dO, const void* w_dow
   a.I = (int)D.I;
   a.mtile_prefix = mtile_prefix;
   a.poff = poff;
-  a.out = dGU;
-  a.out2 = H;
+  a.out = dGU_hi;
+  a.out2 = P_hi;
+  a.out3 = dGU_lo;
+  a.out4 = P_lo;
   a.in_gu = GU;
+  a.row_w = row_w;
   a.dp_part = dp_part;
   a.np = D.np;
   const int mt = max_mtiles(D) * a.n_tiles;
-  if (bn == 256) return launch<256, false, true, SCHED_MGROUP, EPI_SWIGLU_BWD>("bwd_down_dgrad_swiglu", ta, tb, a, mt, st);
-  return launch<128, false, true, SCHED_MGROUP, EPI_SWIGLU_BWD>("bwd_down_dgrad_swiglu", ta, tb, a, mt, st);
+  if (bn == 256)
+    return launch<256, false, true, SCHED_MGROUP, EPI_SWIGLU_BWD>("bwd_down_dgrad_swiglu", ta, tb,
+                                                                   ta, a, mt, st);
+  return launch<128, false, true, SCHED_MGROUP, EPI_SWIGLU_BWD>("bwd_down_dgrad_swiglu", ta, tb,
+                                                                 ta, a, mt, st);
 }
 
 cudaError_t gemm_bwd_gate_up_dgrad(const Dims& D, const void* dGU, const void* w_gate_up,
                                    const int32_t* mtile_prefix, const int32_t* poff,
                                    void* dX_perm, int* status, cudaStream_t st) {
   const int bn = (D.d % 256 == 0) ? 256 : 128;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   if (!make_map(&ta, dGU, 2 * D.I, D.rows_max, 2 * D.I, 128)) return cudaErrorInvalidValue;
   // W_gu_e viewed as [K = 2I rows, N = d columns]: N-major operand
   if (!make_map(&tb, w_gate_up, D.d, D.E * 2 * D.I, D.d, 64)) return cudaErrorInvalidValue;
+  if (!make_out_map(&tc, dX_perm, D.d, D.rows_max)) return cudaErrorInvalidValue;
   GemmArgs a = blank_args(status);
   a.E = (int)D.E;
   a.n_tiles = (int)(D.d / bn);
@@ -634,57 +760,74 @@ cudaError_t gemm_bwd_gate_up_dgrad(const Dims& D, const void* dGU, const void* w
   a.out = dX_perm;  // fp32 [rows_max, d]
   a.ldo = D.d;
   const int mt = max_mtiles(D) * a.n_tiles;
-  if (bn == 256) return launch<256, false, true, SCHED_MGROUP, EPI_F32>("bwd_gate_up_dgrad", ta, tb, a, mt, st);
-  return launch<128, false, true, SCHED_MGROUP, EPI_F32>("bwd_gate_up_dgrad", ta, tb, a, mt, st);
+  if (bn == 256)
+    return launch<256, false, true, SCHED_MGROUP, EPI_F32>("bwd_gate_up_dgrad", ta, tb, tc, a, mt,
+                                                           st);
+  return launch<128, false, true, SCHED_MGROUP, EPI_F32>("bwd_gate_up_dgrad", ta, tb, tc, a, mt,
+                                                         st);
 }
 
-cudaError_t gemm_wgrad_down(const Dims& D, const void* dO, const void* H,
-                            const int32_t* poff, void* dw_down, int* status, cudaStream_t st) {
-  // dW_down_e [d, I] = dO_e^T [d x rows] * H_e [rows x I]
-  const int bn = (D.I % 256 == 0) ? 256 : 128;
-  CUtensorMap ta, tb;
-  if (!make_map(&ta, dO, D.d, D.rows_max, D.d, 64)) return cudaErrorInvalidValue;
-  if (!make_map(&tb, H, D.I, D.rows_max, D.I, 64)) return cudaErrorInvalidValue;
+// K-grouped weight gradient C_e [M, N] = A_e^T B_e over the expert's padded
+// rows, A_e = rows of `A_rows` (inner dim M), B_e = rows of `B_rows` (inner
+// dim N).  One of the two operands comes as a hi/lo pair (`lo_is_a` selects
+// which); fp32 output through TMA stores, or bf16 direct stores.
+static cudaError_t wgrad(const Dims& D, const char* name, const void* A_rows, int64_t M,
+                         const void* B_rows, int64_t N, const void* lo_rows, bool lo_is_a,
+                         const int32_t* poff, void* out, int* status, cudaStream_t st) {
+  // B-split tiles are 128 wide so that four 48 KB stages fit
+  const int bn = (!lo_is_a || N % 256 != 0) ? 128 : 256;
+  CUtensorMap ta, tb, tc, tl;
+  if (!make_map(&ta, A_rows, M, D.rows_max, M, 64)) return cudaErrorInvalidValue;
+  if (!make_map(&tb, B_rows, N, D.rows_max, N, 64)) return cudaErrorInvalidValue;
+  if (lo_is_a) {
+    if (!make_map(&tl, lo_rows, M, D.rows_max, M, 64)) return cudaErrorInvalidValue;
+  } else {
+    if (!make_map(&tl, lo_rows, N, D.rows_max, N, 64)) return cudaErrorInvalidValue;
+  }
   GemmArgs a = blank_args(status);
   a.E = (int)D.E;
-  a.m_tiles = (int)(D.d / 128);
-  a.n_tiles = (int)(D.I / bn);
+  a.m_tiles = (int)(M / 128);
+  a.n_tiles = (int)(N / bn);
+  a.m_rows = (int)M;
   a.poff = poff;
-  a.out = dw_down;
-  a.ldo = D.I;
-  a.out_group_stride = D.d * D.I;
+  a.out = out;
+  a.ldo = N;
+  a.out_group_stride = M * N;
   const int mt = a.E * a.m_tiles * a.n_tiles;
   if (D.wgrad_bf16) {
-    if (bn == 256) return launch<256, true, true, SCHED_KGROUP, EPI_BF16>("bwd_down_wgrad", ta, tb, a, mt, st);
-    return launch<128, true, true, SCHED_KGROUP, EPI_BF16>("bwd_down_wgrad", ta, tb, a, mt, st);
+    if (!lo_is_a)
+      return launch<128, true, true, SCHED_KGROUP, EPI_BF16, SPLIT_B>(name, ta, tb, ta, a, mt, st,
+                                                                      &tl);
+    if (bn == 256)
+      return launch<256, true, true, SCHED_KGROUP, EPI_BF16, SPLIT_A>(name, ta, tb, ta, a, mt, st,
+                                                                      &tl);
+    return launch<128, true, true, SCHED_KGROUP, EPI_BF16, SPLIT_A>(name, ta, tb, ta, a, mt, st,
+                                                                    &tl);
   }
-  if (bn == 256) return launch<256, true, true, SCHED_KGROUP, EPI_F32>("bwd_down_wgrad", ta, tb, a, mt, st);
-  return launch<128, true, true, SCHED_KGROUP, EPI_F32>("bwd_down_wgrad", ta, tb, a, mt, st);
+  if (!make_out_map(&tc, out, N, D.E * M)) return cudaErrorInvalidValue;
+  if (!lo_is_a)
+    return launch<128, true, true, SCHED_KGROUP, EPI_F32, SPLIT_B>(name, ta, tb, tc, a, mt, st,
+                                                                   &tl);
+  if (bn == 256)
+    return launch<256, true, true, SCHED_KGROUP, EPI_F32, SPLIT_A>(name, ta, tb, tc, a, mt, st,
+                                                                   &tl);
+  return launch<128, true, true, SCHED_KGROUP, EPI_F32, SPLIT_A>(name, ta, tb, tc, a, mt, st, &tl);
 }
 
-cudaError_t gemm_wgrad_gate_up(const Dims& D, const void* dGU, const void* X_perm,
-                               const int32_t* poff, void* dw_gate_up, int* status,
-                               cudaStream_t st) {
-  // dW_gu_e [2I, d] = dGU_e^T [2I x rows] * X_perm_e [rows x d]
-  const int bn = (D.d % 256 == 0) ? 256 : 128;
-  CUtensorMap ta, tb;
-  if (!make_map(&ta, dGU, 2 * D.I, D.rows_max, 2 * D.I, 64)) return cudaErrorInvalidValue;
-  if (!make_map(&tb, X_perm, D.d, D.rows_max, D.d, 64)) return cudaErrorInvalidValue;
-  GemmArgs a = blank_args(status);
-  a.E = (int)D.E;
-  a.m_tiles = (int)(2 * D.I / 128);
-  a.n_tiles = (int)(D.d / bn);
-  a.poff = poff;
-  a.out = dw_gate_up;
-  a.ldo = D.d;
-  a.out_group_stride = 2 * D.I * D.d;
-  const int mt = a.E * a.m_tiles * a.n_tiles;
-  if (D.wgrad_bf16) {
-    if (bn == 256) return launch<256, true, true, SCHED_KGROUP, EPI_BF16>("bwd_gate_up_wgrad", ta, tb, a, mt, st);
-    return launch<128, true, true, SCHED_KGROUP, EPI_BF16>("bwd_gate_up_wgrad", ta, tb, a, mt, st);
-  }
-  if (bn == 256) return launch<256, true, true, SCHED_KGROUP, EPI_F32>("bwd_gate_up_wgrad", ta, tb, a, mt, st);
-  return launch<128, true, true, SCHED_KGROUP, EPI_F32>("bwd_gate_up_wgrad", ta, tb, a, mt, st);
+cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* P_hi,
+                            const void* P_lo, const int32_t* poff, void* dw_down, int* status,
+                            cudaStream_t st) {
+  // dW_down_e [d, I] = dY_e^T [d x rows] * (P_hi + P_lo)_e [rows x I],  P = p h
+  return wgrad(D, "bwd_down_wgrad", dY_perm, D.d, P_hi, D.I, P_lo, false, poff, dw_down, status,
+               st);
+}
+
+cudaError_t gemm_wgrad_gate_up(const Dims& D, const void* dGU_hi, const void* dGU_lo,
+                               const void* X_perm, const int32_t* poff, void* dw_gate_up,
+                               int* status, cudaStream_t st) {
+  // dW_gu_e [2I, d] = (dGU_hi + dGU_lo)_e^T [2I x rows] * X_e [rows x d]
+  return wgrad(D, "bwd_gate_up_wgrad", dGU_hi, 2 * D.I, X_perm, D.d, dGU_lo, true, poff,
+               dw_gate_up, status, st);
 }
 
 cudaError_t launch_router_logits(const Dims& D, const void* x, const void* w_router,
@@ -706,8 +849,9 @@ cudaError_t launch_router_logits(const Dims& D, const void* x, const void* w_rou
   a.out = logits;
   a.ldo = D.E;
   const int mt = a.m_tiles * a.n_tiles;
-  if (bn == 256) return launch<256, false, false, SCHED_DENSE, EPI_F32>("router_logits", ta, tb, a, mt, st);
-  return launch<128, false, false, SCHED_DENSE, EPI_F32>("router_logits", ta, tb, a, mt, st);
+  if (bn == 256)
+    return launch<256, false, false, SCHED_DENSE, EPI_F32>("router_logits", ta, tb, ta, a, mt, st);
+  return launch<128, false, false, SCHED_DENSE, EPI_F32>("router_logits", ta, tb, ta, a, mt, st);
 }
 
 cudaError_t gemm_dense_bf16(int64_t M, int64_t N, int64_t K, const void* A, bool a_mn,
@@ -735,16 +879,18 @@ cudaError_t gemm_dense_bf16(int64_t M, int64_t N, int64_t K, const void* A, bool
   a.ldo = N;
   const int mt = a.m_tiles * a.n_tiles;
   if (a_mn) {
-    // the MN-major A path walks K from k_row0 = 0
-    if (bn == 256) return launch<256, true, true, SCHED_DENSE, EPI_BF16>("dense_gemm", ta, tb, a, mt, st);
-    return launch<128, true, true, SCHED_DENSE, EPI_BF16>("dense_gemm", ta, tb, a, mt, st);
+    if (bn == 256)
+      return launch<256, true, true, SCHED_DENSE, EPI_BF16>("dense_gemm", ta, tb, ta, a, mt, st);
+    return launch<128, true, true, SCHED_DENSE, EPI_BF16>("dense_gemm", ta, tb, ta, a, mt, st);
   }
   if (b_mn) {
-    if (bn == 256) return launch<256, false, true, SCHED_DENSE, EPI_BF16>("dense_gemm", ta, tb, a, mt, st);
-    return launch<128, false, true, SCHED_DENSE, EPI_BF16>("dense_gemm", ta, tb, a, mt, st);
+    if (bn == 256)
+      return launch<256, false, true, SCHED_DENSE, EPI_BF16>("dense_gemm", ta, tb, ta, a, mt, st);
+    return launch<128, false, true, SCHED_DENSE, EPI_BF16>("dense_gemm", ta, tb, ta, a, mt, st);
   }
-  if (bn == 256) return launch<256, false, false, SCHED_DENSE, EPI_BF16>("dense_gemm", ta, tb, a, mt, st);
-  return launch<128, false, false, SCHED_DENSE, EPI_BF16>("dense_gemm", ta, tb, a, mt, st);
+  if (bn == 256)
+    return launch<256, false, false, SCHED_DENSE, EPI_BF16>("dense_gemm", ta, tb, ta, a, mt, st);
+  return launch<128, false, false, SCHED_DENSE, EPI_BF16>("dense_gemm", ta, tb, ta, a, mt, st);
 }
 
 }  // namespace mok

@@ -143,7 +143,7 @@ void saved_layout(const Dims& D, mok_saved_layout* L, size_t* mtile_prefix_off) 
   L->padded_token = take(rows * 4);
   L->row_weight = take(rows * 4);
   L->x_perm = take(rows * D.d * 2);
-  L->gate_up = take(rows * 2 * D.I * 2);
+  L->gate_up = take(rows * 2 * D.I * 4);  // fp32
   L->rows_max = rows;
   L->total = o;
 }
@@ -172,9 +172,11 @@ void bwd_layout(const Dims& D, BwdWs* W) {
     return at;
   };
   const size_t rows = static_cast<size_t>(D.rows_max);
-  W->d_o = take(rows * D.d * 2);
-  W->dgu = take(rows * 2 * D.I * 2);
-  W->h = take(rows * D.I * 2);
+  W->dy_perm = take(rows * D.d * 2);
+  W->dgu_hi = take(rows * 2 * D.I * 2);
+  W->dgu_lo = take(rows * 2 * D.I * 2);
+  W->p_hi = take(rows * D.I * 2);
+  W->p_lo = take(rows * D.I * 2);
   W->dp_part = take(rows * D.np * 4);
   W->dx_perm = take(rows * D.d * 4);  // fp32
   W->dl_row = take(rows * 4);
@@ -352,24 +354,28 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
   const void* x_perm = at<char>(saved, L.x_perm);
   const void* gu = at<char>(saved, L.gate_up);
 
-  void* d_o = at<char>(workspace, B.d_o);
-  void* dgu = at<char>(workspace, B.dgu);
-  void* h = at<char>(workspace, B.h);
+  void* dy_perm = at<char>(workspace, B.dy_perm);
+  void* dgu_hi = at<char>(workspace, B.dgu_hi);
+  void* dgu_lo = at<char>(workspace, B.dgu_lo);
+  void* p_hi = at<char>(workspace, B.p_hi);
+  void* p_lo = at<char>(workspace, B.p_lo);
   float* dp_part = at<float>(workspace, B.dp_part);
   float* dx_perm = at<float>(workspace, B.dx_perm);
   float* dl_row = at<float>(workspace, B.dl_row);
   float* dl_tok = at<float>(workspace, B.dl_tok);
 
-  // reverse-combine: pull dy rows into expert order, scaled by p (dO = p dy)
-  MOK_CUDA(launch_gather_scale_rows(D, dy, ptok, row_w, poff, d_o, st));
-  // down-projection dgrad + SwiGLU backward + router-weight partials
-  MOK_CUDA(gemm_bwd_down_dgrad(D, d_o, w_down, mtp, poff, gu, dgu, h, dp_part, status, st));
-  // down-projection wgrad: dW_down_e = dO_e^T H_e
-  MOK_CUDA(gemm_wgrad_down(D, d_o, h, poff, dw_down, status, st));
-  // gate/up dgrad: dX_perm = dGU W_gu
-  MOK_CUDA(gemm_bwd_gate_up_dgrad(D, dgu, w_gate_up, mtp, poff, dx_perm, status, st));
-  // gate/up wgrad: dW_gu_e = dGU_e^T X_e
-  MOK_CUDA(gemm_wgrad_gate_up(D, dgu, x_perm, poff, dw_gate_up, status, st));
+  // reverse-combine: pull dy rows into expert order
+  MOK_CUDA(launch_gather_rows(D, dy, ptok, poff, dy_perm, status, st));
+  // down-projection dgrad + SwiGLU backward + router-weight partials;
+  // dG, dU and P = p h leave as bf16 hi/lo pairs
+  MOK_CUDA(gemm_bwd_down_dgrad(D, dy_perm, w_down, mtp, poff, static_cast<const float*>(gu),
+                               row_w, dgu_hi, dgu_lo, p_hi, p_lo, dp_part, status, st));
+  // down-projection wgrad: dW_down_e = dY_e^T (P_hi + P_lo)_e
+  MOK_CUDA(gemm_wgrad_down(D, dy_perm, p_hi, p_lo, poff, dw_down, status, st));
+  // gate/up dgrad: dX_perm = dGU_hi W_gu (fp32 rows)
+  MOK_CUDA(gemm_bwd_gate_up_dgrad(D, dgu_hi, w_gate_up, mtp, poff, dx_perm, status, st));
+  // gate/up wgrad: dW_gu_e = (dGU_hi + dGU_lo)_e^T X_e
+  MOK_CUDA(gemm_wgrad_gate_up(D, dgu_hi, dgu_lo, x_perm, poff, dw_gate_up, status, st));
   // reverse-dispatch + router backward
   MOK_CUDA(launch_reverse_dispatch(D, dx_perm, ppos, topk_idx, topk_w, dp_part, w_router, dx,
                                    dl_row, dl_tok, st));

@@ -32,7 +32,7 @@ struct FwdWs {
   size_t block_counts, block_base, h, o, logits, total;
 };
 struct BwdWs {
-  size_t d_o, dgu, h, dp_part, dx_perm, dl_row, dl_tok, total;
+  size_t dy_perm, dgu_hi, dgu_lo, p_hi, p_lo, dp_part, dx_perm, dl_row, dl_tok, total;
 };
 struct StageWs {
   size_t status, block_counts, block_base, padded_offsets, mtile_prefix, ppos, ptok, row_w,
@@ -76,11 +76,6 @@ cudaError_t launch_gather_rows(const Dims& D, const void* src, const int32_t* pt
                                const int32_t* padded_offsets, void* dst, int* status,
                                cudaStream_t st);
 
-// dO[r] = bf16(row_w[r] * src[ptok[r]]) (zeros where ptok[r] < 0).
-cudaError_t launch_gather_scale_rows(const Dims& D, const void* src, const int32_t* ptok,
-                                     const float* row_w, const int32_t* padded_offsets, void* dst,
-                                     cudaStream_t st);
-
 // y_t = sum_s p[t,s] O[ppos[t,s]] (O fp32; y fp32 or bf16).
 cudaError_t launch_combine(const Dims& D, const float* O, const int32_t* ppos, const float* topk_w,
                            void* y, cudaStream_t st);
@@ -104,18 +99,19 @@ cudaError_t gemm_fwd_gate_up(const Dims& D, const void* X_perm, const void* w_ga
 cudaError_t gemm_fwd_down(const Dims& D, const void* H, const void* w_down,
                           const int32_t* mtile_prefix, const int32_t* poff, void* O, int* status,
                           cudaStream_t st);
-cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dO, const void* w_down,
-                                const int32_t* mtile_prefix, const int32_t* poff, const void* GU,
-                                void* dGU, void* H, float* dp_part, int* status,
-                                cudaStream_t st);
+cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* w_down,
+                                const int32_t* mtile_prefix, const int32_t* poff, const float* GU,
+                                const float* row_w, void* dGU_hi, void* dGU_lo, void* P_hi,
+                                void* P_lo, float* dp_part, int* status, cudaStream_t st);
 cudaError_t gemm_bwd_gate_up_dgrad(const Dims& D, const void* dGU, const void* w_gate_up,
                                    const int32_t* mtile_prefix, const int32_t* poff,
                                    void* dX_perm, int* status, cudaStream_t st);
-cudaError_t gemm_wgrad_down(const Dims& D, const void* dO, const void* H,
-                            const int32_t* poff, void* dw_down, int* status, cudaStream_t st);
-cudaError_t gemm_wgrad_gate_up(const Dims& D, const void* dGU, const void* X_perm,
-                               const int32_t* poff, void* dw_gate_up, int* status,
-                               cudaStream_t st);
+cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* P_hi,
+                            const void* P_lo, const int32_t* poff, void* dw_down, int* status,
+                            cudaStream_t st);
+cudaError_t gemm_wgrad_gate_up(const Dims& D, const void* dGU_hi, const void* dGU_lo,
+                               const void* X_perm, const int32_t* poff, void* dw_gate_up,
+                               int* status, cudaStream_t st);
 cudaError_t gemm_dense_bf16(int64_t M, int64_t N, int64_t K, const void* A, bool a_mn,
                             const void* B, bool b_mn, void* C, int* status, cudaStream_t st);
 

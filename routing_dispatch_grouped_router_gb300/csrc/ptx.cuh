@@ -98,6 +98,16 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* t
       : "memory");
 }
 
+// Tiled 2-D store shared -> global, tracked by bulk groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, const void* src, int32_t c0,
+                                             int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(tm)),
+      "r"(smem_addr(src)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
                                           uint64_t* bar) {

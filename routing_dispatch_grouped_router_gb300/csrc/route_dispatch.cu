@@ -379,54 +379,6 @@ cudaError_t launch_gather_rows(const Dims& D, const void* src, const int32_t* pt
   return cudaGetLastError();
 }
 
-// ------------------------------------------------------- scaled row gather --
-
-// Reverse-combine pull: dO[r] = bf16(p_r * dy[ptok[r]]), the A operand of the
-// down-projection dgrad and of its weight gradient.  One warp per row, 16-byte
-// vectors; padding rows get zeros.
-__global__ void gather_scale_rows_kernel(const uint4* __restrict__ src,
-                                         const int32_t* __restrict__ ptok,
-                                         const float* __restrict__ row_w,
-                                         const int32_t* __restrict__ poff_end, int T, int dv,
-                                         uint4* __restrict__ dst) {
-  const long long P = *poff_end;
-  const int lane = threadIdx.x & 31;
-  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  for (long long r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < P; r += warps) {
-    const int t = ptok[r];
-    uint4* out = dst + r * dv;
-    if (t < 0 || t >= T) {
-      for (int c = lane; c < dv; c += 32) out[c] = make_uint4(0, 0, 0, 0);
-      continue;
-    }
-    const float w = row_w[r];
-    const uint4* in = src + static_cast<long long>(t) * dv;
-    for (int c = lane; c < dv; c += 32) {
-      const uint4 v = ld_global_nc_v4(in + c);
-      out[c] = make_uint4(pack_bf16x2(w * bf16lo(v.x), w * bf16hi(v.x)),
-                          pack_bf16x2(w * bf16lo(v.y), w * bf16hi(v.y)),
-                          pack_bf16x2(w * bf16lo(v.z), w * bf16hi(v.z)),
-                          pack_bf16x2(w * bf16lo(v.w), w * bf16hi(v.w)));
-    }
-  }
-}
-
-cudaError_t launch_gather_scale_rows(const Dims& D, const void* src, const int32_t* ptok,
-                                     const float* row_w, const int32_t* padded_offsets, void* dst,
-                                     cudaStream_t st) {
-  if (D.T == 0) return cudaSuccess;
-  const int dv = static_cast<int>(D.d / 8);
-  long long blocks = static_cast<long long>(num_sms_current_device()) * 8;
-  const long long need = (D.rows_max + 7) / 8;
-  if (blocks > need) blocks = need;
-  ProfScope prof("gather_scale_rows", st);
-  gather_scale_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-      static_cast<const uint4*>(src), ptok, row_w, padded_offsets + D.E, static_cast<int>(D.T),
-      dv, static_cast<uint4*>(dst));
-  count_launch();
-  return cudaGetLastError();
-}
-
 // ----------------------------------------------------------------- combine --
 
 __device__ __forceinline__ void axpy4(float (&acc)[4], float w, float4 v) {
@@ -517,8 +469,7 @@ cudaError_t launch_combine(const Dims& D, const float* O, const int32_t* ppos, c
 // -------------------------------------------------------- reverse dispatch --
 
 // One CTA per token.  Router backward first:
-//   dp_s = (sum_j dp_part[row_s, j]) / p_s    (fixed j order; the partials
-//          hold p_s <dy, O_s> because dO = p dy; dp_s is unused when p_s = 0)
+//   dp_s = sum_j dp_part[row_s, j]            (fixed j order; = <dy, O_s>)
 //   dl_s = p_s (dp_s - sum_i p_i dp_i)        (softmax over the chosen k)
 // then dx_t = sum_s (dX_perm[row_s] + dl_s * W_r[e_s])   in slot order.
 template <bool BF16_OUT>
@@ -541,11 +492,9 @@ __global__ void reverse_dispatch_kernel(const float4* __restrict__ dXp,
       row = ppos[t * k + s];
       e = topk_idx[t * k + s];
       p = topk_w[t * k + s];
-      if (row >= 0 && p > 0.f) {
+      if (row >= 0) {
         const float* q = dp_part + static_cast<long long>(row) * np;
-        float acc = 0.f;
-        for (int j = 0; j < np; ++j) acc += q[j];
-        dp = acc / p;
+        for (int j = 0; j < np; ++j) dp += q[j];
       }
     }
     // c = sum_i p_i dp_i, summed in slot order by every lane

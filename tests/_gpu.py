@@ -62,7 +62,7 @@ def run_gpu(shape: gen.Shape, inp: dict, layer=None, flags=0):
         token_of_row=layer.saved_tensor("token_of_row", torch.int32, (T * k,)).cpu().numpy(),
         padded_offsets=layer.saved_tensor("padded_offsets", torch.int32, (E + 1,)).cpu().numpy(),
         padded_pos=layer.saved_tensor("padded_pos", torch.int32, (T, k)).cpu().numpy(),
-        gate_up=layer.saved_tensor("gate_up", torch.bfloat16, (L.rows_max, 2 * shape.I)),
+        gate_up=layer.saved_tensor("gate_up", torch.float32, (L.rows_max, 2 * shape.I)),
         layer=layer,
     )
     return out
@@ -99,22 +99,31 @@ def check_dispatch_valid(idx, counts, offsets, pos, token_of_row, E):
 
 
 def check_bf16_intermediate(got_bf16: np.ndarray, ref: np.ndarray, name: str):
-    """A stored bf16 GEMM operand against the oracle's bf16 value: equal
-    except where float32 vs float64 accumulation lands on the other side of
-    a rounding boundary (rare), and then by one bf16 ulp."""
+    """A stored bf16 value against the oracle's bf16 value of the same
+    quantity.  They agree except where the kernel's float32 accumulation and
+    the oracle's exact one fall on the two sides of a bf16 rounding boundary:
+    then they differ by one bf16 ulp, plus at most the float32 accumulation
+    error (which matters only for results near zero, where a bf16 ulp is
+    smaller than it).  Returns the fraction of elements that differ."""
+    got_bf16 = np.asarray(got_bf16, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if ref.size == 0:
+        return 0.0
     diff = got_bf16 != ref
-    frac = float(diff.mean()) if diff.size else 0.0
-    assert frac < 2e-3, (name, frac)
+    frac = float(diff.mean())
+    rms = float(np.sqrt(np.mean(ref * ref)))
     if diff.any():
         a = np.abs(ref[diff])
         ulp = 2.0 ** (np.floor(np.log2(np.maximum(a, 2.0 ** -126))) - 7)
-        assert (np.abs(got_bf16[diff] - ref[diff]) <= ulp * 1.0000001).all(), name
+        excess = np.abs(got_bf16[diff] - ref[diff]) - ulp
+        worst = float(excess.max()) / rms if rms else float(excess.max())
+        assert worst <= 1e-5, (name, "beyond one ulp by", worst, "x rms; differing fraction", frac)
+    assert frac < 1e-2, (name, "differing fraction", frac)
     return frac
 
 
 def full_parity(shape: gen.Shape, inp: dict, gpu: dict, tol=BF16_TOL):
-    """Element-wise comparison of every output against the full oracle (in
-    its BF16-operand mode, the precision the layer's GEMMs are defined in)."""
+    """Element-wise comparison of every output against the full fp64 oracle."""
     assert gpu["status"] == 0, gpu["status"]
     bias = inp.get("bias")
     idx, p, logits, flagged, inner = oracle.route_ref(inp["x"], inp["w_router"], bias, shape.k)
@@ -130,7 +139,7 @@ def full_parity(shape: gen.Shape, inp: dict, gpu: dict, tol=BF16_TOL):
                          gpu["token_of_row"], shape.E)
 
     y, fwd = oracle.moe_forward_ref(inp["x"], inp["w_router"], bias, inp["w_gate_up"],
-                                    inp["w_down"], shape.k, keep=True, precision="bf16")
+                                    inp["w_down"], shape.k, keep=True)
     g = oracle.moe_backward_ref(inp["x"], inp["w_router"], bias, inp["w_gate_up"],
                                 inp["w_down"], shape.k, inp["dy"], fwd=fwd)
     errs = {}
@@ -141,8 +150,10 @@ def full_parity(shape: gen.Shape, inp: dict, gpu: dict, tol=BF16_TOL):
     gu = host64(gpu["gate_up"])
     rows_gpu = gpu["padded_pos"][tokens].ravel()
     rows_ref = pos[tokens].ravel()
-    errs["gate_flips"] = check_bf16_intermediate(gu[rows_gpu, :shape.I], fwd["G"][rows_ref], "gate")
-    errs["up_flips"] = check_bf16_intermediate(gu[rows_gpu, shape.I:], fwd["U"][rows_ref], "up")
+    # fp32 pre-activations saved for the backward: fp32 accumulation error only
+    errs["gate"] = rel_err(gu[rows_gpu, :shape.I], fwd["G"][rows_ref])
+    errs["up"] = rel_err(gu[rows_gpu, shape.I:], fwd["U"][rows_ref])
+    assert errs["gate"] < 1e-4 and errs["up"] < 1e-4, errs
     # expert gradients: leave out experts touched by an undecided token
     touched = np.zeros(shape.E, dtype=bool)
     for t in np.nonzero(~tokens)[0]:
@@ -154,8 +165,7 @@ def full_parity(shape: gen.Shape, inp: dict, gpu: dict, tol=BF16_TOL):
     if all_same:
         errs["dw_router"] = rel_err(host64(gpu["dw_router"]), g["dw_router"])
     for name, v in errs.items():
-        if not name.endswith("_flips"):
-            assert v <= tol, (name, v, errs)
+        assert v <= tol, (name, v, errs)
     # experts that received no rows have exactly zero weight gradients
     empty = counts == 0
     if all_same and empty.any():

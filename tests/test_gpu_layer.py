@@ -1,9 +1,8 @@
-"""Parity of the CUDA layer (through the C ABI) against the oracle, plus
+"""Parity of the CUDA layer (through the C ABI) against the fp64 oracle, plus
 determinism and edge cases.  Bar: routing, counts, offsets and permutation
 bit-exact (near-ties flagged by the oracle excluded); outputs and gradients
-within max|diff| <= 2e-2 * rms(oracle) per tensor against the oracle's
-BF16-operand definition; stored bf16 operands equal to the oracle's up to rare
-one-ulp flips; repeated calls bitwise identical."""
+within max|diff| <= 2e-2 * rms(oracle) per tensor; repeated calls bitwise
+identical."""
 import numpy as np
 import pytest
 import torch
