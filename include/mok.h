@@ -50,6 +50,7 @@ typedef enum mok_status {
   MOK_ERR_WORKSPACE = 3,        /* a buffer is smaller than the size query says */
   MOK_ERR_CUDA = 4,             /* a CUDA runtime call failed */
   MOK_ERR_NO_DEVICE = 5,        /* the current device is not sm_103 */
+  MOK_ERR_SCRATCH_LIMIT = 6,    /* larger than the fixed scratch of mok_moe_dispatch_plan_noalloc */
   /* codes written on the device, read back with mok_get_device_status */
   MOK_ERR_DEVICE_NONFINITE = 16, /* a router logit was NaN; it was treated as -inf */
   MOK_ERR_DEVICE_INDEX = 17,     /* an expert index outside [0, E) was met and skipped */
@@ -173,6 +174,33 @@ mok_status mok_moe_dispatch_plan(const mok_moe_desc* desc, const int32_t* topk_i
                                  int32_t* counts, int32_t* offsets, int32_t* pos,
                                  int32_t* token_of_row, void* workspace, size_t ws_bytes,
                                  void* stream);
+
+/* Dispatch plan without scratch memory from the caller.  No counterpart on
+ * the pages: an addition of this library.
+ *
+ * Same inputs, outputs and results as mok_moe_dispatch_plan, for callers
+ * that cannot allocate device memory at the point of the call and so have no
+ * workspace to hand over: for instance code running inside another
+ * library's allocator or memory-pool callback, or a process whose device
+ * memory is entirely reserved up front by its framework.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ * The scratch is one 4 MiB array in device memory defined inside libmok
+ * (held by every device that loads the library until the process exits).
+ * Problems whose plan needs more than that -- roughly T*k*4 + 4*(T*k +
+ * 127*E) + 8*E*ceil(T/256) bytes -- are rejected with
+ * MOK_ERR_SCRATCH_LIMIT before anything is enqueued.
+ *   status: device int32 that receives the device-side error code (reset to
+ *           MOK_OK by this call), or NULL to keep it inside the scratch.
+ * The first call on a device resolves the array's device address there
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls share the one array, whose contents
+ * are whatever the last call left: each call rewrites what it reads, and two
+ * calls whose work overlaps on the GPU (different streams, or different host
+ * threads on one device) race on it. */
+mok_status mok_moe_dispatch_plan_noalloc(const mok_moe_desc* desc, const int32_t* topk_idx,
+                                         int32_t* counts, int32_t* offsets, int32_t* pos,
+                                         int32_t* token_of_row, int32_t* status, void* stream);
 
 /* Dense GEMM through the layer's tcgen05 engine, C[M,N] = A B in bf16 with
  * fp32 accumulation and bf16 output (a diagnostic of the grouped engine):

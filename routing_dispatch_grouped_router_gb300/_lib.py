@@ -46,6 +46,8 @@ _SIGS = {
                                 c_void_p, c_void_p, c_size_t, c_void_p]),
     "mok_moe_dispatch_plan": (c_int32, [ctypes.POINTER(MoeDesc), c_void_p, c_void_p, c_void_p,
                                         c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "mok_moe_dispatch_plan_noalloc": (c_int32, [ctypes.POINTER(MoeDesc), c_void_p, c_void_p,
+                                                c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "mok_gemm_bf16": (c_int32, [c_int64, c_int64, c_int64, c_void_p, c_int32, c_void_p, c_int32,
                                 c_void_p, c_void_p, c_size_t, c_void_p]),
     "mok_get_device_status": (c_int32, [c_void_p, c_void_p, ctypes.POINTER(c_int32)]),

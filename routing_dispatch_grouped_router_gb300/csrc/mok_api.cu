@@ -72,7 +72,7 @@ int num_sms_current_device() {
   return cache[dev];
 }
 
-static mok_status check_device() {
+mok_status mok_check_device() {
   static int ok_cache[64] = {0};  // 0 unknown, 1 ok, 2 bad
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOK_ERR_NO_DEVICE;
@@ -275,7 +275,7 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
   FwdWs F;
   fwd_layout(D, &F);
   if (saved_bytes < L.total || ws_bytes < F.total) return MOK_ERR_WORKSPACE;
-  s = check_device();
+  s = mok_check_device();
   if (s != MOK_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   reset_launch_count();
@@ -337,7 +337,7 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
   BwdWs B;
   bwd_layout(D, &B);
   if (saved_bytes < L.total || ws_bytes < B.total) return MOK_ERR_WORKSPACE;
-  s = check_device();
+  s = mok_check_device();
   if (s != MOK_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
@@ -406,7 +406,7 @@ mok_status mok_moe_route(const mok_moe_desc* desc, const void* x, const void* w_
   StageWs W;
   stage_layout(D, &W);
   if (ws_bytes < W.total) return MOK_ERR_WORKSPACE;
-  s = check_device();
+  s = mok_check_device();
   if (s != MOK_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* status = at<int>(workspace, W.status);
@@ -431,7 +431,7 @@ mok_status mok_moe_dispatch_plan(const mok_moe_desc* desc, const int32_t* topk_i
   StageWs W;
   stage_layout(D, &W);
   if (ws_bytes < W.total) return MOK_ERR_WORKSPACE;
-  s = check_device();
+  s = mok_check_device();
   if (s != MOK_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* status = at<int>(workspace, W.status);
@@ -464,7 +464,7 @@ mok_status mok_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int a_m
   if (!aligned16(A) || !aligned16(B) || !aligned16(C) || !aligned16(workspace))
     return MOK_ERR_INVALID_ARG;
   if (ws_bytes < 256) return MOK_ERR_WORKSPACE;
-  mok_status s = check_device();
+  mok_status s = mok_check_device();
   if (s != MOK_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* status = static_cast<int*>(workspace);
@@ -491,6 +491,7 @@ const char* mok_status_string(mok_status status) {
     case MOK_ERR_WORKSPACE: return "buffer smaller than the size query";
     case MOK_ERR_CUDA: return "CUDA runtime error";
     case MOK_ERR_NO_DEVICE: return "current device is not sm_103";
+    case MOK_ERR_SCRATCH_LIMIT: return "problem needs more than the fixed device scratch of the no-allocation entry point";
     case MOK_ERR_DEVICE_NONFINITE: return "device: NaN router logit (treated as -inf)";
     case MOK_ERR_DEVICE_INDEX: return "device: expert index out of range or repeated (skipped)";
     case MOK_ERR_DEVICE_TIMEOUT: return "device: bounded wait timed out (results invalid)";

@@ -46,6 +46,7 @@ void bwd_layout(const Dims& D, BwdWs* W);
 void stage_layout(const Dims& D, StageWs* W);
 
 int num_sms_current_device();
+mok_status mok_check_device();  // MOK_OK when the current device is sm_103
 
 // ------------------------------------------------------------------ kernels --
 
