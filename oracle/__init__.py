@@ -8,3 +8,4 @@ from .moe_ref import (  # noqa: F401
     NEAR_TIE, widen, bf16_round, silu, silu_grad, router_logits, route_ref, dispatch_ref,
     expert_ffn, moe_forward_ref, moe_backward_ref,
 )
+from .mx_ref import e4m3_round, mx_quantize, mx_fake  # noqa: F401

@@ -33,7 +33,15 @@ nothing that is not a GEMM operand is rounded.  The rounded operands are
   P = p * H       (operand of the down-projection weight gradient,
                    dW_down = sum_r dy_r (p_r h_r)^T)
   dG, dU          (operands of the gate/up dgrad and weight gradient)
-each rounded to the nearest bf16 (ties to even).  dy is itself a bf16 input,
+each rounded to the nearest bf16 (ties to even).  ``precision="mxfp8"`` is the
+MXFP8 definition (E4M3 elements, one E8M0 scale per 32 values along each
+GEMM's reduction dimension, see mx_ref.py): every operand of the forward
+GEMMs and of the two dgrads is fake-quantised (x rows, W_gate/W_up along d,
+h and W_down along I, dy rows along d, W_down along d, [dG dU] along 2I,
+W_gate_up along 2I); in the two weight-gradient GEMMs the layer inputs x and
+dy are quantised along the token dimension (each expert's rows zero-padded to
+a multiple of 32) while the derived operands p*h and [dG dU] are not.
+dy is itself a bf16 input,
 so the down dgrad dH = p * (dy W_down) needs no rounded operand.  The expert
 output O, y, dp, the router gradient, dx and the weight gradients are not
 rounded.
@@ -51,6 +59,8 @@ Readings where the pages say nothing (all are listed again in the design notes):
 from __future__ import annotations
 
 import numpy as np
+
+from .mx_ref import mx_fake
 
 NEAR_TIE = 1e-5
 
@@ -88,7 +98,7 @@ def _identity(a):
 
 
 def _rounder(precision: str):
-    if precision == "fp64":
+    if precision in ("fp64", "mxfp8"):
         return _identity
     if precision == "bf16":
         return bf16_round
@@ -188,16 +198,34 @@ def dispatch_ref(topk_idx, E: int):
 # forward  ([dothoosh] "Hybrid communication", "Precision and scheduling")
 # ----------------------------------------------------------------------------
 
-def expert_ffn(X, w_gate_up_e, w_down_e, rnd=_identity):
+def expert_ffn(X, w_gate_up_e, w_down_e, rnd=_identity, mx=False):
     """SwiGLU FFN of one expert on rows X (float64).  Returns (G, U, H, O).
-    ``rnd`` rounds the GEMM operands (identity in float64 mode)."""
+    ``rnd`` rounds the GEMM operands (identity in float64 mode); ``mx``
+    fake-quantises them to MXFP8 along their reduction dimension."""
     Wgu = widen(w_gate_up_e)
+    Wd = widen(w_down_e)
     I = Wgu.shape[0] // 2
+    if mx:
+        Xq, Wq = mx_fake(X, -1), mx_fake(Wgu, -1)
+        G = Xq @ Wq[:I].T
+        U = Xq @ Wq[I:].T
+        H = silu(G) * U
+        return G, U, H, mx_fake(H, -1) @ mx_fake(Wd, -1).T
     G = rnd(X @ Wgu[:I].T)
     U = rnd(X @ Wgu[I:].T)
     H = rnd(silu(G) * U)
-    O = H @ widen(w_down_e).T
+    O = H @ Wd.T
     return G, U, H, O
+
+
+def _mx_rows(a):
+    """MXFP8 along the token dimension (axis 0), the rows zero-padded to a
+    multiple of 32 as the blocks start at the expert's first row."""
+    n = a.shape[0]
+    pad = (-n) % 32
+    if pad:
+        a = np.concatenate([a, np.zeros((pad,) + a.shape[1:])], axis=0)
+    return mx_fake(a, 0)[:n]
 
 
 def moe_forward_ref(x, w_router, bias, w_gate_up, w_down, k: int, routing=None,
@@ -227,7 +255,8 @@ def moe_forward_ref(x, w_router, bias, w_gate_up, w_down, k: int, routing=None,
         a, b = int(offsets[e]), int(offsets[e + 1])
         if a == b:
             continue
-        G[a:b], U[a:b], H[a:b], O[a:b] = expert_ffn(X[tok[a:b]], w_gate_up[e], w_down[e], rnd)
+        G[a:b], U[a:b], H[a:b], O[a:b] = expert_ffn(X[tok[a:b]], w_gate_up[e], w_down[e], rnd,
+                                                     mx=(precision == "mxfp8"))
     y = np.zeros((T, d))
     for s in range(k):
         y += p[:, s:s + 1] * O[pos[:, s]]
@@ -294,14 +323,25 @@ def moe_backward_ref(x, w_router, bias, w_gate_up, w_down, k: int, dy,
             continue
         Wd = widen(w_down[e])
         Wgu = widen(w_gate_up[e])
+        Xe = X[tok[a:b]]
+        dYe = dY[row_t[a:b]]
+        if precision == "mxfp8":
+            dH = row_p[a:b, None] * (mx_fake(dYe, -1) @ mx_fake(Wd, 0))
+            dG = dH * U[a:b] * silu_grad(G[a:b])
+            dU = dH * silu(G[a:b])
+            dGU = np.concatenate([dG, dU], axis=1)
+            dX_rows[a:b] = mx_fake(dGU, -1) @ mx_fake(Wgu, 0)
+            if grad_experts is None or e in dw_down:
+                dw_down[e][...] = _mx_rows(dYe).T @ (row_p[a:b, None] * H[a:b])
+                dw_gate_up[e][...] = dGU.T @ _mx_rows(Xe)
+            continue
         dH = dO[a:b] @ Wd                       # [rows, I]
         dG = rnd(dH * U[a:b] * silu_grad(G[a:b]))
         dU = rnd(dH * silu(G[a:b]))
-        Xe = X[tok[a:b]]
         dX_rows[a:b] = dG @ Wgu[:I] + dU @ Wgu[I:]
         if grad_experts is None or e in dw_down:
             # sum_r p_r dy_r h_r^T, with p applied on the h side
-            dw_down[e][...] = dY[row_t[a:b]].T @ rnd(row_p[a:b, None] * H[a:b])
+            dw_down[e][...] = dYe.T @ rnd(row_p[a:b, None] * H[a:b])
             dw_gate_up[e][:I] = dG.T @ Xe
             dw_gate_up[e][I:] = dU.T @ Xe
 

@@ -33,10 +33,10 @@ WORKLOADS = {
     "mxfp8":      dict(T=16384, d=4096, E=128, I=1536, k=8, mb_tokens=2048, ring_slots=2),
 }
 
-# Scale of the Zipf offsets for the imbalanced workload (seed 0).  It was found
-# by bisection so that the hottest expert receives about 8x the mean number of
-# rows; tests/golden/make_zipf_beta.py re-derives it with the oracle's router.
-ZIPF_BETA = {"imbalanced": 1.0}
+# Scale of the Zipf offsets for the imbalanced workload (seed 0), found by
+# bisection so that the hottest expert receives 8x the mean number of rows
+# (tests/golden/zipf_beta.json, written by tests/golden/make_zipf_beta.py).
+ZIPF_BETA = {"imbalanced": 0.391659}
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -143,6 +143,95 @@ def make_inputs(shape: Shape, seed: int, zipf_s: float | None = None,
         dy=_normal_bf16(kids[2 + 3 * E], (shape.T, d), 1.0),
         bias=bias,
     )
+
+
+def _expert_worker(args):
+    """Pool worker: draws experts [e0, e1) into the shared-memory weights."""
+    from multiprocessing import shared_memory
+    name_gu, name_dn, shape_t, seed, e0, e1 = args
+    shape = Shape(*shape_t)
+    E, I, d = shape.E, shape.I, shape.d
+    sgu = shared_memory.SharedMemory(name=name_gu)
+    sdn = shared_memory.SharedMemory(name=name_dn)
+    try:
+        w_gu = np.ndarray((E, 2 * I, d), dtype=np.uint16, buffer=sgu.buf)
+        w_dn = np.ndarray((E, d, I), dtype=np.uint16, buffer=sdn.buf)
+        kids = _streams(seed, E)
+        for e in range(e0, e1):
+            wg, wu, wd = make_expert(shape, seed, e, kids)
+            w_gu[e, :I] = wg
+            w_gu[e, I:] = wu
+            w_dn[e] = wd
+        del w_gu, w_dn
+    finally:
+        sgu.close()
+        sdn.close()
+    return e1 - e0
+
+
+class _SharedArrays:
+    """Keeps shared-memory segments mapped while their arrays are alive."""
+
+    def __init__(self, segs):
+        self.segs = segs
+
+    def __del__(self):
+        for s in self.segs:
+            try:
+                s.close()
+            except Exception:
+                pass
+
+
+def make_inputs_parallel(shape: Shape, seed: int, zipf_s: float | None = None,
+                         zipf_beta: float | None = None, workers: int | None = None) -> dict:
+    """make_inputs with the experts drawn by a pool of processes (spawned, so
+    it is safe after CUDA initialisation).  Same values as make_inputs."""
+    import multiprocessing as mp
+    import os
+    from multiprocessing import shared_memory
+    E, I, d = shape.E, shape.I, shape.d
+    n_gu = E * 2 * I * d * 2
+    n_dn = E * d * I * 2
+    sgu = shared_memory.SharedMemory(create=True, size=max(n_gu, 1))
+    sdn = shared_memory.SharedMemory(create=True, size=max(n_dn, 1))
+    try:
+        workers = workers or min(E, len(os.sched_getaffinity(0)), 32)
+        bounds = np.linspace(0, E, workers + 1).astype(int)
+        jobs = [(sgu.name, sdn.name, (shape.T, shape.d, shape.E, shape.I, shape.k), seed,
+                 int(bounds[i]), int(bounds[i + 1])) for i in range(workers) if bounds[i] < bounds[i + 1]]
+        with mp.get_context("spawn").Pool(len(jobs)) as pool:
+            assert sum(pool.map(_expert_worker, jobs)) == E
+    finally:
+        sgu.unlink()
+        sdn.unlink()
+    keep = _SharedArrays([sgu, sdn])
+    w_gu = np.ndarray((E, 2 * I, d), dtype=np.uint16, buffer=sgu.buf)
+    w_dn = np.ndarray((E, d, I), dtype=np.uint16, buffer=sdn.buf)
+    kids = _streams(seed, E)
+    bias = None
+    if zipf_s is not None:
+        bias = make_zipf_bias(shape, seed, zipf_s, zipf_beta if zipf_beta is not None else 1.0)
+    return dict(
+        x=_normal_bf16(kids[0], (shape.T, d), 1.0),
+        w_router=_normal_bf16(kids[1], (E, d), d ** -0.5),
+        w_gate_up=w_gu,
+        w_down=w_dn,
+        dy=_normal_bf16(kids[2 + 3 * E], (shape.T, d), 1.0),
+        bias=bias,
+        _shared=keep,
+    )
+
+
+def workload_inputs(name: str, seed: int = 0, parallel: bool = False) -> dict:
+    """Inputs of a named workload (with its Zipf offsets where it has them)."""
+    shape = workload_shape(name)
+    w = WORKLOADS[name]
+    zs = w.get("zipf_s")
+    zb = ZIPF_BETA.get(name) if zs is not None else None
+    if parallel:
+        return make_inputs_parallel(shape, seed, zs, zb)
+    return make_inputs(shape, seed, zs, zb)
 
 
 def workload_shape(name: str) -> Shape:

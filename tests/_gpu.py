@@ -78,8 +78,10 @@ def check_routing(gpu_idx, gpu_w, ref_idx, ref_w, flagged, inner_tie):
     # decided tokens: exact slot order unless two chosen logits are within 1e-5
     bad = ok & ~np.where(inner_tie, same_set, same_order)
     assert not bad.any(), f"routing differs on {int(bad.sum())} decided tokens: {np.nonzero(bad)[0][:10]}"
+    # routing weights: softmax of fp32 logits whose accumulation over d terms
+    # is off by ~1e-6 of |l| (|l| < ~10 here); 1e-4 bounds |dp| with margin
     w_err = np.abs(np.sort(gpu_w, axis=1) - np.sort(ref_w, axis=1))[ok]
-    assert w_err.size == 0 or w_err.max() < 2e-6, w_err.max()
+    assert w_err.size == 0 or w_err.max() < 1e-4, w_err.max()
     np.testing.assert_allclose(gpu_w.sum(axis=1), 1.0, atol=2e-6)
     return ok & same_order
 

@@ -372,7 +372,7 @@ def test_planted_unstable_dispatch_is_caught(monkeypatch):
 def test_planted_gate_up_swap_is_caught(monkeypatch):
     sh, inp = _tiny(seed=3, k=2)
 
-    def wrong(X, wgu, wd, rnd=None):
+    def wrong(X, wgu, wd, rnd=None, mx=False):
         W = moe_ref.widen(wgu)
         I = W.shape[0] // 2
         U = X @ W[:I].T
