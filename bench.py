@@ -207,6 +207,22 @@ def workload_config(shape: gen.Shape) -> dict:
             "parallelism": "replicas (one independent layer per GPU)"}
 
 
+# ------------------------------------------------------------- multi-rank --
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest `value` of all ranks (the slowest rank's time)."""
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, tokens_per_rank: int, steps: int, t_max_ms: float) -> float:
+    """Tokens/s of the whole job: every rank runs its own replica on its own
+    tokens, and the job takes as long as its slowest rank."""
+    return world * tokens_per_rank * steps / (t_max_ms / 1e3)
+
+
 # --------------------------------------------------------------- GPU side --
 
 def main():
@@ -295,12 +311,8 @@ def main():
     kernels = api.profile_collect()
     if layer.status() != 0:
         raise RuntimeError("device status set during the timed region")
-    t_max = elapsed_ms
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_max = float(t.item())
-    value = world * shape.T * args.steps / (t_max / 1e3)
+    t_max = max_over_ranks(elapsed_ms, dist, "cuda") if world > 1 else elapsed_ms
+    value = job_throughput(world, shape.T, args.steps, t_max)
 
     # ---- per-kernel summary and the dominant kernel's roofline
     peaks = load_peaks()
@@ -367,10 +379,8 @@ def main():
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": world * shape.T * args.e2e_steps / (e2e_ms / 1e3), "unit": "tokens/s",
+        e2e_ms = max_over_ranks(e2e_ms, dist, "cuda")
+    e2e = {"value": job_throughput(world, shape.T, args.e2e_steps, e2e_ms), "unit": "tokens/s",
            "h2d_bytes_per_step": 2 * xh.numel() * 2, "d2h_bytes_per_step": 2 * yh.numel() * 4,
            "steps": args.e2e_steps}
 

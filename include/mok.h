@@ -31,7 +31,8 @@
  * Shape requirements (MOK_ERR_UNSUPPORTED otherwise)
  *   1 <= k <= min(E, 8);  1 <= E <= 512;  0 <= T;  T*k < 2^31;
  *   d and I multiples of 128 (the GEMM tile width), d <= 16384, I <= 16384;
- *   dtype MOK_BF16 (MOK_MXFP8 is declared, not yet served).
+ *   micro-batching: T a multiple of mb_tokens, 0 <= ring_slots <= T/mb_tokens,
+ *   fp32 weight-gradient outputs (they accumulate over micro-batches).
  */
 #ifndef MOK_H_
 #define MOK_H_
@@ -59,7 +60,8 @@ typedef enum mok_status {
 
 typedef enum mok_dtype {
   MOK_BF16 = 0,  /* bf16 operands, fp32 accumulation, bf16 I/O */
-  MOK_MXFP8 = 1  /* E4M3 operands with 32-element E8M0 block scales (reserved) */
+  MOK_MXFP8 = 1  /* expert GEMMs on MXFP8 operands: E4M3 with one E8M0 scale per 32
+                    values along K, fp32 accumulation (see mok_moe_forward) */
 } mok_dtype;
 
 /* Output dtypes.  By default y, dx and the three weight gradients are fp32
@@ -68,14 +70,27 @@ typedef enum mok_dtype {
  * of the same fp32 value). */
 #define MOK_FLAG_BF16_ACT_OUT 0x1u   /* y and dx written as bf16 */
 #define MOK_FLAG_BF16_WGRAD_OUT 0x2u /* dw_router, dw_gate_up, dw_down written as bf16 */
+#define MOK_FLAG_ACCUMULATE_WGRAD 0x4u /* backward adds into the fp32 dw_* instead of
+                                          overwriting them (gradient accumulation) */
+/* Activation recompute: the forward keeps no pre-activations g, u; the
+ * backward recomputes them from the dispatched rows with the same kernel and
+ * schedule (results bitwise identical to the default).  Saves rows_max*2I*4
+ * bytes of `saved` per micro-batch for one more gate/up GEMM in the backward.
+ * (h is never kept: the backward always derives it from g, u.) */
+#define MOK_FLAG_RECOMPUTE_GATE_UP 0x8u
+
+/* Offset value of a mok_saved_layout field the flags leave out of `saved`. */
+#define MOK_NOT_KEPT ((size_t)-1)
 
 /* Layer shape.  T tokens of width d, E experts with FFN width I, top-k. */
 typedef struct mok_moe_desc {
   int64_t T, d, E, I;
   int32_t k;
   int32_t dtype;       /* mok_dtype */
-  int32_t mb_tokens;   /* 0 = whole batch at once (micro-batching reserved) */
-  int32_t ring_slots;  /* reserved, 0 */
+  int32_t mb_tokens;   /* 0: one pass over all T tokens; else tokens per
+                          micro-batch (T a multiple of it) */
+  int32_t ring_slots;  /* micro-batching: slots of the dispatched-row ring
+                          (0 = one per micro-batch) */
   uint32_t flags;      /* MOK_FLAG_* */
   uint32_t reserved;
 } mok_moe_desc;
@@ -83,7 +98,11 @@ typedef struct mok_moe_desc {
 /* Byte offsets, inside the `saved` buffer, of the forward results that the
  * backward consumes.  Row-indexed arrays use the padded row space: expert e
  * owns rows [padded_offsets[e], padded_offsets[e+1]), each segment a multiple
- * of 128 rows, its first counts[e] rows real and the rest zero. */
+ * of 128 rows, its first counts[e] rows real and the rest zero.
+ * With micro-batching the per-token fields describe micro-batch 0 (T =
+ * mb_tokens) and micro-batch i's are at + i * mb_stride; x_perm is ring slot
+ * 0 and slot j is at + j * ring_slot_bytes (micro-batch i was dispatched to
+ * slot i % ring_slots). */
 typedef struct mok_saved_layout {
   size_t status;          /* int32 device status word */
   size_t topk_idx;        /* int32 [T,k] expert of each slot, descending logit */
@@ -97,8 +116,13 @@ typedef struct mok_saved_layout {
   size_t padded_token;    /* int32 [rows_max] token of each padded row, -1 for padding */
   size_t row_weight;      /* fp32 [rows_max] routing weight of each padded row, 0 for padding */
   size_t x_perm;          /* bf16 [rows_max, d] dispatched token rows */
-  size_t gate_up;         /* fp32 [rows_max, 2I] pre-activation gate (cols 0..I-1) and up (I..2I-1) */
+  size_t gate_up;         /* fp32 [rows_max, 2I] pre-activation gate (cols 0..I-1) and up (I..2I-1);
+                             MOK_NOT_KEPT with MOK_FLAG_RECOMPUTE_GATE_UP */
   size_t rows_max;        /* number of padded rows the buffers hold: T*k + 127*min(E, T*k), rounded to 128 */
+  size_t mb_count;        /* micro-batches (1 without micro-batching) */
+  size_t mb_stride;       /* bytes between consecutive micro-batches' fields */
+  size_t ring_slots;      /* slots of dispatched rows (1 without micro-batching) */
+  size_t ring_slot_bytes; /* bytes between ring slots */
   size_t total;           /* size of `saved` in bytes */
 } mok_saved_layout;
 
@@ -202,6 +226,21 @@ mok_status mok_moe_dispatch_plan_noalloc(const mok_moe_desc* desc, const int32_t
                                          int32_t* counts, int32_t* offsets, int32_t* pos,
                                          int32_t* token_of_row, int32_t* status, void* stream);
 
+/* MXFP8 quantisation ([dothoosh] "Precision and scheduling": MXFP8; the
+ * scaling rule is the OCP Microscaling v1.0 one): E4M3 elements with one E8M0
+ * power-of-two scale per block of 32 values,
+ *   shared = floor(log2 max|v|) - 8 (clamped to [-127,127], -127 for an
+ *            all-zero block),  q = RNE_E4M3(v / 2^shared) saturating at 448.
+ * in: bf16 [rows, cols] row-major.  along_rows = 0: blocks of 32 consecutive
+ * values of a row (cols % 32 == 0); along_rows = 1: blocks of 32 consecutive
+ * rows of a column (rows % 32 == 0).
+ * out: bf16 [rows, cols], the dequantised values q * 2^shared (exact in
+ * bf16); may equal `in`.  codes: NULL or uint8 [rows, cols] E4M3 codes.
+ * scales: NULL or uint8 E8M0 bytes (shared + 127), [rows, cols/32]
+ * (along_rows = 0) or [rows/32, cols] (along_rows = 1). */
+mok_status mok_mx_quantize(const void* in, int64_t rows, int64_t cols, int along_rows, void* out,
+                           uint8_t* codes, uint8_t* scales, void* stream);
+
 /* Dense GEMM through the layer's tcgen05 engine, C[M,N] = A B in bf16 with
  * fp32 accumulation and bf16 output (a diagnostic of the grouped engine):
  *   a_mn_major = 0: A stored [M,K];  1: A stored [K,M]
@@ -211,6 +250,14 @@ mok_status mok_moe_dispatch_plan_noalloc(const mok_moe_desc* desc, const int32_t
 mok_status mok_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int a_mn_major,
                          const void* B, int b_mn_major, void* C, void* workspace,
                          size_t ws_bytes, void* stream);
+
+/* Failure-path self-test: enqueues one CTA that waits on an mbarrier phase
+ * nothing completes.  The wait is the bounded one every GEMM uses: it gives
+ * up after its limit (0.2 s) and the kernel writes MOK_ERR_DEVICE_TIMEOUT to
+ * the status word at the start of `workspace` (>= 256 bytes, reset first)
+ * and returns, leaving the context usable.  Read it with
+ * mok_get_device_status. */
+mok_status mok_selftest_bounded_wait(void* workspace, size_t ws_bytes, void* stream);
 
 /* Waits for `stream`, then reads the device status word at the start of
  * `buf` (the `saved` buffer of forward/backward, or the workspace of the

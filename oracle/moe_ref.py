@@ -40,7 +40,11 @@ GEMMs and of the two dgrads is fake-quantised (x rows, W_gate/W_up along d,
 h and W_down along I, dy rows along d, W_down along d, [dG dU] along 2I,
 W_gate_up along 2I); in the two weight-gradient GEMMs the layer inputs x and
 dy are quantised along the token dimension (each expert's rows zero-padded to
-a multiple of 32) while the derived operands p*h and [dG dU] are not.
+a multiple of 32) while the derived operands p*h and [dG dU] are not.  With
+quantised GEMMs the identity <dy, O> = <dy W_down, h> no longer holds exactly;
+the router-weight gradient is taken the way the pages fuse it into the SwiGLU
+backward ([dothoosh] "Precision and scheduling"): dp = <dA, h> with dA the
+(quantised) down-projection dgrad of the row and h unquantised.
 dy is itself a bf16 input,
 so the down dgrad dH = p * (dy W_down) needs no rounded operand.  The expert
 output O, y, dp, the router gradient, dx and the weight gradients are not
@@ -308,7 +312,10 @@ def moe_backward_ref(x, w_router, bias, w_gate_up, w_down, k: int, dy,
     for s in range(k):
         row_p[pos[:, s]] = p[:, s]
     dO = row_p[:, None] * dY[row_t]
-    dp = np.einsum("tsd,td->ts", O[pos], dY)
+    if precision == "mxfp8":
+        dp_rows = np.zeros(R)
+    else:
+        dp = np.einsum("tsd,td->ts", O[pos], dY)
 
     dX_rows = np.zeros((R, d))
     if grad_experts is None:
@@ -326,7 +333,9 @@ def moe_backward_ref(x, w_router, bias, w_gate_up, w_down, k: int, dy,
         Xe = X[tok[a:b]]
         dYe = dY[row_t[a:b]]
         if precision == "mxfp8":
-            dH = row_p[a:b, None] * (mx_fake(dYe, -1) @ mx_fake(Wd, 0))
+            dA = mx_fake(dYe, -1) @ mx_fake(Wd, 0)
+            dp_rows[a:b] = (dA * H[a:b]).sum(axis=1)
+            dH = row_p[a:b, None] * dA
             dG = dH * U[a:b] * silu_grad(G[a:b])
             dU = dH * silu(G[a:b])
             dGU = np.concatenate([dG, dU], axis=1)
@@ -344,6 +353,9 @@ def moe_backward_ref(x, w_router, bias, w_gate_up, w_down, k: int, dy,
             dw_down[e][...] = dYe.T @ rnd(row_p[a:b, None] * H[a:b])
             dw_gate_up[e][:I] = dG.T @ Xe
             dw_gate_up[e][I:] = dU.T @ Xe
+
+    if precision == "mxfp8":
+        dp = dp_rows[pos]
 
     # reverse-dispatch: sum each token's k rows in slot order
     dx = np.zeros((T, d))

@@ -23,7 +23,7 @@ class SavedLayout(ctypes.Structure):
     _fields_ = [(n, c_size_t) for n in (
         "status", "topk_idx", "topk_w", "counts", "offsets", "pos", "token_of_row",
         "padded_offsets", "padded_pos", "padded_token", "row_weight", "x_perm", "gate_up",
-        "rows_max", "total")]
+        "rows_max", "mb_count", "mb_stride", "ring_slots", "ring_slot_bytes", "total")]
 
 
 class KernelTime(ctypes.Structure):
@@ -48,8 +48,11 @@ _SIGS = {
                                         c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "mok_moe_dispatch_plan_noalloc": (c_int32, [ctypes.POINTER(MoeDesc), c_void_p, c_void_p,
                                                 c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "mok_mx_quantize": (c_int32, [c_void_p, c_int64, c_int64, c_int32, c_void_p, c_void_p,
+                                  c_void_p, c_void_p]),
     "mok_gemm_bf16": (c_int32, [c_int64, c_int64, c_int64, c_void_p, c_int32, c_void_p, c_int32,
                                 c_void_p, c_void_p, c_size_t, c_void_p]),
+    "mok_selftest_bounded_wait": (c_int32, [c_void_p, c_size_t, c_void_p]),
     "mok_get_device_status": (c_int32, [c_void_p, c_void_p, ctypes.POINTER(c_int32)]),
     "mok_status_string": (ctypes.c_char_p, [c_int32]),
     "mok_last_launch_count": (c_int32, []),

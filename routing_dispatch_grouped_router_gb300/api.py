@@ -14,6 +14,9 @@ from . import _lib
 BF16, MXFP8 = 0, 1
 FLAG_BF16_ACT_OUT = 0x1    # y and dx written as bf16 (default fp32)
 FLAG_BF16_WGRAD_OUT = 0x2  # weight gradients written as bf16 (default fp32)
+FLAG_ACCUMULATE_WGRAD = 0x4  # backward adds into the fp32 weight gradients
+FLAG_RECOMPUTE_GATE_UP = 0x8  # g, u not kept by the forward; the backward recomputes them
+NOT_KEPT = (1 << 64) - 1  # saved-layout offset of a field the flags leave out
 
 
 def _ptr(t):
@@ -28,9 +31,9 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def make_desc(T, d, E, I, k, dtype=BF16, flags=0) -> _lib.MoeDesc:
-    return _lib.MoeDesc(T=T, d=d, E=E, I=I, k=k, dtype=dtype, mb_tokens=0, ring_slots=0,
-                        flags=flags, reserved=0)
+def make_desc(T, d, E, I, k, dtype=BF16, flags=0, mb_tokens=0, ring_slots=0) -> _lib.MoeDesc:
+    return _lib.MoeDesc(T=T, d=d, E=E, I=I, k=k, dtype=dtype, mb_tokens=mb_tokens,
+                        ring_slots=ring_slots, flags=flags, reserved=0)
 
 
 def workspace_sizes(desc):
@@ -101,6 +104,16 @@ def gemm_bf16(A, a_mn_major, B, b_mn_major, C, workspace, stream=None):
                "mok_gemm_bf16")
 
 
+def mx_quantize(x, along_rows: bool, out=None, codes=None, scales=None, stream=None):
+    """MXFP8 fake quantisation of a 2-D bf16 tensor (see mok_mx_quantize)."""
+    lib = _lib.load()
+    out = torch.empty_like(x) if out is None else out
+    rows, cols = x.shape
+    _lib.check(lib.mok_mx_quantize(_ptr(x), rows, cols, int(along_rows), _ptr(out), _ptr(codes),
+                                   _ptr(scales), _stream(stream)), "mok_mx_quantize")
+    return out
+
+
 def device_status(buf, stream=None) -> int:
     """Synchronises the stream and returns the device status word of `buf`."""
     lib = _lib.load()
@@ -134,8 +147,10 @@ def profile_collect() -> dict:
 class MoELayer:
     """Owns the three buffers of one layer shape and calls forward/backward."""
 
-    def __init__(self, T, d, E, I, k, device="cuda", flags=0):
-        self.desc = make_desc(T, d, E, I, k, flags=flags)
+    def __init__(self, T, d, E, I, k, device="cuda", flags=0, dtype=BF16, mb_tokens=0,
+                 ring_slots=0):
+        self.desc = make_desc(T, d, E, I, k, dtype=dtype, flags=flags, mb_tokens=mb_tokens,
+                              ring_slots=ring_slots)
         self.T, self.d, self.E, self.I, self.k = T, d, E, I, k
         self.act_dtype = torch.bfloat16 if flags & FLAG_BF16_ACT_OUT else torch.float32
         self.wgrad_dtype = torch.bfloat16 if flags & FLAG_BF16_WGRAD_OUT else torch.float32
@@ -145,8 +160,11 @@ class MoELayer:
         self.bwd_ws = torch.empty(max(b, 256), dtype=torch.uint8, device=device)
         self.layout = saved_layout(self.desc)
 
-    def saved_tensor(self, field: str, dtype, shape):
+    def saved_tensor(self, field: str, dtype, shape, micro_batch: int = 0):
         off = getattr(self.layout, field)
+        if off == NOT_KEPT:
+            raise KeyError(f"{field} is not kept in saved with these flags")
+        off += micro_batch * self.layout.mb_stride
         n = 1
         for v in shape:
             n *= v

@@ -38,12 +38,19 @@
 #include <mutex>
 
 #include "mok_internal.h"
+#include "mx.cuh"
 #include "ptx.cuh"
 
 namespace mok {
 
 enum Sched : int { SCHED_DENSE = 0, SCHED_MGROUP = 1, SCHED_KGROUP = 2 };
-enum Epi : int { EPI_BF16 = 0, EPI_F32 = 1, EPI_SWIGLU_FWD = 2, EPI_SWIGLU_BWD = 3 };
+enum Epi : int {
+  EPI_BF16 = 0,
+  EPI_F32 = 1,
+  EPI_SWIGLU_FWD = 2,
+  EPI_SWIGLU_BWD = 3,
+  EPI_F32_T = 4,  // KGROUP: fp32 C^T through TMA (the tile is stored transposed)
+};
 // Split operands: a bf16 "hi" tile plus a bf16 "lo" tile (value - hi) whose
 // products are accumulated into the same fp32 accumulator, giving the GEMM
 // an operand with ~16 significant bits.
@@ -63,9 +70,13 @@ struct GemmArgs {
   void* out;                // C (bf16 or fp32)
   long long ldo;            // C row stride (elements)
   long long out_group_stride;  // KGROUP: elements between experts' C
-  void* out2;               // SWIGLU_FWD: H [rows,I]; SWIGLU_BWD: P_hi = bf16(p*h) [rows,I]
+  void* out2;               // SWIGLU_FWD: H [rows,I] (NULL: not stored); SWIGLU_BWD: P_hi = bf16(p*h) [rows,I]
   void* out3;               // SWIGLU_BWD: dGU_lo [rows,2I]
   void* out4;               // SWIGLU_BWD: P_lo [rows,I]
+  void* out5;               // SWIGLU_BWD with mx: MXFP8 dGU [rows,2I] (dgrad operand)
+  int mx;                   // SwiGLU epilogues: quantise the derived GEMM operands to MXFP8
+  int accumulate;           // fp32 TMA-store epilogue: add into C instead of overwriting
+  int store_c;              // SWIGLU_FWD: write g, u through the C map
   const void* in_gu;        // SWIGLU_BWD: saved fp32 pre-activations [rows,2I]
   const float* row_w;       // SWIGLU_BWD: routing weight of each row
   float* dp_part;           // SWIGLU_BWD: [rows, np] partial <dA,h>
@@ -155,8 +166,10 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, int t) {
   return tl;
 }
 
+// silu(g) = g * sigmoid(g); the sigmoid through the hardware exponential and a
+// correctly rounded reciprocal.
 __device__ __forceinline__ float silu_f(float g, float* sig_out) {
-  const float s = 1.0f / (1.0f + __expf(-g));
+  const float s = __frcp_rn(1.0f + __expf(-g));
   *sig_out = s;
   return g * s;
 }
@@ -198,29 +211,32 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* p, float (&v)[
   }
 }
 
-// Stores 16 values as bf16 hi = bf16(v) and lo = bf16(v - hi).
-__device__ __forceinline__ void store_hi_lo16(__nv_bfloat16* hi, __nv_bfloat16* lo,
-                                              const float (&v)[16]) {
-  uint32_t h[8], l[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float a0 = bf16_round(v[2 * j]), a1 = bf16_round(v[2 * j + 1]);
-    h[j] = pack_bf16x2(a0, a1);
-    l[j] = pack_bf16x2(v[2 * j] - a0, v[2 * j + 1] - a1);
-  }
+// Stores 32 values as bf16 hi = bf16(v) and lo = bf16(v - hi).
+__device__ __forceinline__ void store_hi_lo32(__nv_bfloat16* hi, __nv_bfloat16* lo,
+                                              const float (&v)[32]) {
   uint4* ph = reinterpret_cast<uint4*>(hi);
   uint4* pl = reinterpret_cast<uint4*>(lo);
-  ph[0] = make_uint4(h[0], h[1], h[2], h[3]);
-  ph[1] = make_uint4(h[4], h[5], h[6], h[7]);
-  pl[0] = make_uint4(l[0], l[1], l[2], l[3]);
-  pl[1] = make_uint4(l[4], l[5], l[6], l[7]);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float v0 = v[8 * q + 2 * j], v1 = v[8 * q + 2 * j + 1];
+      const float a0 = bf16_round(v0), a1 = bf16_round(v1);
+      h[j] = pack_bf16x2(a0, a1);
+      l[j] = pack_bf16x2(v0 - a0, v1 - a1);
+    }
+    ph[q] = make_uint4(h[0], h[1], h[2], h[3]);
+    pl[q] = make_uint4(l[0], l[1], l[2], l[3]);
+  }
 }
 
 // One warp writes its 32 rows x 32 fp32 columns to the 4 KB staging buffer in
 // the 128-byte swizzled layout (16-byte chunk j of row r at chunk j ^ (r%8)),
 // then lane 0 stores it with one TMA tensor store at (x, y).
 __device__ __forceinline__ void stage_and_store_f32(uint8_t* buf, const CUtensorMap* tmC,
-                                                    const float (&v)[32], int lane, int x, int y) {
+                                                    const float (&v)[32], int lane, int x, int y,
+                                                    bool add = false) {
   if (lane == 0) bulk_wait_read<0>();  // the previous store has read the buffer
   __syncwarp();
   uint8_t* row = buf + lane * 128;
@@ -233,7 +249,30 @@ __device__ __forceinline__ void stage_and_store_f32(uint8_t* buf, const CUtensor
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
-    tma_store_2d(tmC, buf, x, y);
+    if (add) tma_reduce_add_2d(tmC, buf, x, y);
+    else tma_store_2d(tmC, buf, x, y);
+    bulk_commit();
+  }
+}
+
+// As stage_and_store_f32, but the warp's 32 x 32 block is stored transposed:
+// lane i holds row i of the accumulator block (v[j] = column j), and the
+// staging buffer receives column j of the block as its row j, so the TMA store
+// at (x, y) writes element (i, j) to output row y + j, column x + i.
+__device__ __forceinline__ void stage_and_store_f32_t(uint8_t* buf, const CUtensorMap* tmC,
+                                                      const float (&v)[32], int lane, int x,
+                                                      int y, bool add) {
+  if (lane == 0) bulk_wait_read<0>();
+  __syncwarp();
+  const int chunk = lane >> 2, word = (lane & 3) * 4;
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    *reinterpret_cast<float*>(buf + j * 128 + ((chunk ^ (j & 7)) << 4) + word) = v[j];
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    if (add) tma_reduce_add_2d(tmC, buf, x, y);
+    else tma_store_2d(tmC, buf, x, y);
     bulk_commit();
   }
 }
@@ -258,7 +297,24 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = 0.f;
       }
-      stage_and_store_f32(stage_buf, tmC, v, lane, col0 + c, y);
+      stage_and_store_f32(stage_buf, tmC, v, lane, col0 + c, y, a.accumulate != 0);
+    }
+  } else if (EPI == EPI_F32_T) {
+    // C^T through TMA: accumulator rows are output columns; C viewed as
+    // [E * N, M] with group e's block at rows e*N
+    const int x = tl.row0 + q * 32;
+    const int col0 = tl.n_tile * BN + half * HALF_COLS;
+#pragma unroll 1
+    for (int c = 0; c < HALF_COLS; c += 32) {
+      float v[32];
+      if (!zero_k) {
+        tmem_ld32(taddr + half * HALF_COLS + c, v);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.f;
+      }
+      stage_and_store_f32_t(stage_buf, tmC, v, lane, x, tl.e * a.ldo + col0 + c,
+                            a.accumulate != 0);
     }
   } else if (EPI == EPI_BF16 || EPI == EPI_F32) {
     constexpr int esz = EPI == EPI_F32 ? 4 : 2;
@@ -302,17 +358,23 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
     __nv_bfloat16* h = static_cast<__nv_bfloat16*>(a.out2) + r * (long long)I;
 #pragma unroll 1
     for (int c = 0; c < 64; c += 32) {
-      float g[32], u[32], hv[32];
+      float g[32], u[32];
       tmem_ld32(taddr + half * 64 + c, g);
       tmem_ld32(taddr + 128 + half * 64 + c, u);
+      if (a.out2) {
+        float hv[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float s;
-        hv[j] = silu_f(g[j], &s) * u[j];
+        for (int j = 0; j < 32; ++j) {
+          float s;
+          hv[j] = silu_f(g[j], &s) * u[j];
+        }
+        if (a.mx) mx_fake32(hv);  // one MX block: 32 consecutive columns of a row
+        store_bf16x32(h + n0 + c, hv);
       }
-      store_bf16x32(h + n0 + c, hv);
-      stage_and_store_f32(stage_buf, tmC, g, lane, n0 + c, y);
-      stage_and_store_f32(stage_buf, tmC, u, lane, I + n0 + c, y);
+      if (a.store_c) {
+        stage_and_store_f32(stage_buf, tmC, g, lane, n0 + c, y);
+        stage_and_store_f32(stage_buf, tmC, u, lane, I + n0 + c, y);
+      }
     }
   } else if (EPI == EPI_SWIGLU_BWD) {
     // accumulator = dA = dY_perm W_down for BN columns of I (n0 = n_tile*BN).
@@ -331,39 +393,51 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
     __nv_bfloat16* p_hi = static_cast<__nv_bfloat16*>(a.out2) + r * (long long)I;
     __nv_bfloat16* p_lo = static_cast<__nv_bfloat16*>(a.out4) + r * (long long)I;
     const float p = a.row_w[r];
+    __nv_bfloat16* dgu_mx = static_cast<__nv_bfloat16*>(a.out5) + r * (2LL * I);
     float dp = 0.f;
 #pragma unroll 1
-    for (int c = 0; c < HALF_COLS; c += 16) {
-      float dA[16], g[16], u[16], dg[16], du[16], ph[16];
+    for (int c = 0; c < HALF_COLS; c += 32) {
+      float dA[32], g[32], u[32], t[32];
       {
-        uint32_t rr[16];
-        tmem_ld16(taddr + half * HALF_COLS + c, rr);
+        uint32_t r0[16], r1[16];
+        tmem_ld16(taddr + half * HALF_COLS + c, r0);
+        tmem_ld16(taddr + half * HALF_COLS + c + 16, r1);
         const float4* gp = reinterpret_cast<const float4*>(gu + n0 + c);
         const float4* up = reinterpret_cast<const float4*>(gu + I + n0 + c);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 8; ++j) {
           const float4 a4 = gp[j], b4 = up[j];
           g[4 * j] = a4.x; g[4 * j + 1] = a4.y; g[4 * j + 2] = a4.z; g[4 * j + 3] = a4.w;
           u[4 * j] = b4.x; u[4 * j + 1] = b4.y; u[4 * j + 2] = b4.z; u[4 * j + 3] = b4.w;
         }
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) dA[j] = __uint_as_float(rr[j]);
+        for (int j = 0; j < 16; ++j) {
+          dA[j] = __uint_as_float(r0[j]);
+          dA[16 + j] = __uint_as_float(r1[j]);
+        }
       }
+      // one pass: d gate -> t, d up -> dA, p h -> u (g is free afterwards)
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        float s;
-        const float sl = silu_f(g[j], &s);
-        const float hv = sl * u[j];
-        dp = fmaf(dA[j], hv, dp);
+      for (int j = 0; j < 32; ++j) {
+        float sg;
+        const float sl = silu_f(g[j], &sg);
+        const float uu = u[j];
         const float dh = p * dA[j];
-        dg[j] = dh * u[j] * (s * (1.0f + g[j] * (1.0f - s)));
-        du[j] = dh * sl;
-        ph[j] = p * hv;
+        dp = fmaf(dA[j], sl * uu, dp);
+        t[j] = dh * uu * (sg * (1.0f + g[j] * (1.0f - sg)));
+        dA[j] = dh * sl;
+        u[j] = p * sl * uu;
       }
-      store_hi_lo16(dgu_hi + n0 + c, dgu_lo + n0 + c, dg);
-      store_hi_lo16(dgu_hi + I + n0 + c, dgu_lo + I + n0 + c, du);
-      store_hi_lo16(p_hi + n0 + c, p_lo + n0 + c, ph);
+      store_hi_lo32(dgu_hi + n0 + c, dgu_lo + n0 + c, t);
+      store_hi_lo32(dgu_hi + I + n0 + c, dgu_lo + I + n0 + c, dA);
+      if (a.mx) {
+        mx_fake32(t);
+        store_bf16x32(dgu_mx + n0 + c, t);
+        mx_fake32(dA);
+        store_bf16x32(dgu_mx + I + n0 + c, dA);
+      }
+      store_hi_lo32(p_hi + n0 + c, p_lo + n0 + c, u);
     }
     a.dp_part[r * a.np + tl.n_tile * 2 + half] = dp;
   }
@@ -390,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   constexpr bool kTmaStore =
-      (EPI == EPI_F32 && SCHED != SCHED_DENSE) || EPI == EPI_SWIGLU_FWD;
+      (EPI == EPI_F32 && SCHED != SCHED_DENSE) || EPI == EPI_SWIGLU_FWD || EPI == EPI_F32_T;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -570,6 +644,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after_sync();
+      if (EPI == EPI_SWIGLU_BWD) {
+        // the fp32 g, u rows of this thread's next tile (and, the first time,
+        // of this one) go to L2 while this tile's epilogue runs
+        for (int tp = (it == 0 ? t : t + (int)gridDim.x); tp <= t + (int)gridDim.x && tp < total;
+             tp += (int)gridDim.x) {
+          const Tile tn = decode_tile<SCHED>(args, tp);
+          const float* row = static_cast<const float*>(args.in_gu) +
+                             (long long)(tn.row0 + q * 32 + lane) * (2LL * args.I) +
+                             tn.n_tile * BN + half * (BN / 2);
+          prefetch_l2_bulk(row, BN / 2 * 4);
+          prefetch_l2_bulk(row + args.I, BN / 2 * 4);
+        }
+      }
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
       epilogue_tile<BN, SCHED, EPI>(args, tl, taddr, q, lane, half, stage_buf, &tmC);
@@ -670,8 +757,13 @@ cudaError_t gemm_fwd_gate_up(const Dims& D, const void* X_perm, const void* w_ga
   CUtensorMap ta, tb, tc;
   if (!make_map(&ta, X_perm, D.d, D.rows_max, D.d, 128)) return cudaErrorInvalidValue;
   if (!make_map(&tb, w_gate_up, D.d, D.E * 2 * D.I, D.d, 128)) return cudaErrorInvalidValue;
-  if (!make_out_map(&tc, GU, 2 * D.I, D.rows_max)) return cudaErrorInvalidValue;
+  // without GU the C map is never used; it then describes the A operand so
+  // that the kernel's descriptor prefetch still sees a valid map
+  if (GU ? !make_out_map(&tc, GU, 2 * D.I, D.rows_max) : !make_map(&tc, X_perm, D.d, D.rows_max, D.d, 128))
+    return cudaErrorInvalidValue;
+  if (!GU && !H) return cudaErrorInvalidValue;
   GemmArgs a = blank_args(status);
+  a.store_c = GU ? 1 : 0;
   a.E = (int)D.E;
   a.n_tiles = (int)(D.I / 128);
   a.num_kb = (int)(D.d / 64);
@@ -681,6 +773,7 @@ cudaError_t gemm_fwd_gate_up(const Dims& D, const void* X_perm, const void* w_ga
   a.poff = poff;
   a.out = GU;
   a.out2 = H;
+  a.mx = D.mx ? 1 : 0;
   return launch<256, false, false, SCHED_MGROUP, EPI_SWIGLU_FWD>(
       "fwd_gate_up_swiglu", ta, tb, tc, a, max_mtiles(D) * a.n_tiles, st);
 }
@@ -711,7 +804,8 @@ cudaError_t gemm_fwd_down(const Dims& D, const void* H, const void* w_down,
 cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* w_down,
                                 const int32_t* mtile_prefix, const int32_t* poff, const float* GU,
                                 const float* row_w, void* dGU_hi, void* dGU_lo, void* P_hi,
-                                void* P_lo, float* dp_part, int* status, cudaStream_t st) {
+                                void* P_lo, void* dGU_mx, float* dp_part, int* status,
+                                cudaStream_t st) {
   const int bn = D.bn_dgrad;
   CUtensorMap ta, tb;
   if (!make_map(&ta, dY_perm, D.d, D.rows_max, D.d, 128)) return cudaErrorInvalidValue;
@@ -729,6 +823,8 @@ cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* 
   a.out2 = P_hi;
   a.out3 = dGU_lo;
   a.out4 = P_lo;
+  a.out5 = dGU_mx;
+  a.mx = D.mx ? 1 : 0;
   a.in_gu = GU;
   a.row_w = row_w;
   a.dp_part = dp_part;
@@ -773,7 +869,8 @@ cudaError_t gemm_bwd_gate_up_dgrad(const Dims& D, const void* dGU, const void* w
 // which); fp32 output through TMA stores, or bf16 direct stores.
 static cudaError_t wgrad(const Dims& D, const char* name, const void* A_rows, int64_t M,
                          const void* B_rows, int64_t N, const void* lo_rows, bool lo_is_a,
-                         const int32_t* poff, void* out, int* status, cudaStream_t st) {
+                         const int32_t* poff, void* out, bool accumulate, int* status,
+                         cudaStream_t st) {
   // B-split tiles are 128 wide so that four 48 KB stages fit
   const int bn = (!lo_is_a || N % 256 != 0) ? 128 : 256;
   CUtensorMap ta, tb, tc, tl;
@@ -793,8 +890,10 @@ static cudaError_t wgrad(const Dims& D, const char* name, const void* A_rows, in
   a.out = out;
   a.ldo = N;
   a.out_group_stride = M * N;
+  a.accumulate = accumulate ? 1 : 0;
   const int mt = a.E * a.m_tiles * a.n_tiles;
   if (D.wgrad_bf16) {
+    if (accumulate) return cudaErrorInvalidValue;  // accumulation is fp32 only
     if (!lo_is_a)
       return launch<128, true, true, SCHED_KGROUP, EPI_BF16, SPLIT_B>(name, ta, tb, ta, a, mt, st,
                                                                       &tl);
@@ -815,19 +914,39 @@ static cudaError_t wgrad(const Dims& D, const char* name, const void* A_rows, in
 }
 
 cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* P_hi,
-                            const void* P_lo, const int32_t* poff, void* dw_down, int* status,
-                            cudaStream_t st) {
-  // dW_down_e [d, I] = dY_e^T [d x rows] * (P_hi + P_lo)_e [rows x I],  P = p h
-  return wgrad(D, "bwd_down_wgrad", dY_perm, D.d, P_hi, D.I, P_lo, false, poff, dw_down, status,
-               st);
+                            const void* P_lo, const int32_t* poff, void* dw_down,
+                            bool accumulate, int* status, cudaStream_t st) {
+  // dW_down_e [d, I] (+)= dY_e^T [d x rows] * (P_hi + P_lo)_e [rows x I],  P = p h
+  if (D.wgrad_bf16 || D.d % 256 != 0)
+    return wgrad(D, "bwd_down_wgrad", dY_perm, D.d, P_hi, D.I, P_lo, false, poff, dw_down,
+                 accumulate, status, st);
+  // computed as its transpose, (P_hi + P_lo)_e^T [I x rows] * dY_e [rows x d],
+  // so that the hi/lo pair is the A operand and the tile is 128 x 256 like
+  // the gate/up wgrad's; the epilogue stores each block transposed
+  CUtensorMap ta, tb, tc, tl;
+  if (!make_map(&ta, P_hi, D.I, D.rows_max, D.I, 64)) return cudaErrorInvalidValue;
+  if (!make_map(&tl, P_lo, D.I, D.rows_max, D.I, 64)) return cudaErrorInvalidValue;
+  if (!make_map(&tb, dY_perm, D.d, D.rows_max, D.d, 64)) return cudaErrorInvalidValue;
+  if (!make_out_map(&tc, dw_down, D.I, D.E * D.d)) return cudaErrorInvalidValue;
+  GemmArgs a = blank_args(status);
+  a.E = (int)D.E;
+  a.m_tiles = (int)(D.I / 128);
+  a.n_tiles = (int)(D.d / 256);
+  a.m_rows = (int)D.I;
+  a.poff = poff;
+  a.out = dw_down;
+  a.ldo = D.d;  // rows of one expert's block in the [E*d, I] view
+  a.accumulate = accumulate ? 1 : 0;
+  return launch<256, true, true, SCHED_KGROUP, EPI_F32_T, SPLIT_A>(
+      "bwd_down_wgrad", ta, tb, tc, a, a.E * a.m_tiles * a.n_tiles, st, &tl);
 }
 
 cudaError_t gemm_wgrad_gate_up(const Dims& D, const void* dGU_hi, const void* dGU_lo,
                                const void* X_perm, const int32_t* poff, void* dw_gate_up,
-                               int* status, cudaStream_t st) {
-  // dW_gu_e [2I, d] = (dGU_hi + dGU_lo)_e^T [2I x rows] * X_e [rows x d]
+                               bool accumulate, int* status, cudaStream_t st) {
+  // dW_gu_e [2I, d] (+)= (dGU_hi + dGU_lo)_e^T [2I x rows] * X_e [rows x d]
   return wgrad(D, "bwd_gate_up_wgrad", dGU_hi, 2 * D.I, X_perm, D.d, dGU_lo, true, poff,
-               dw_gate_up, status, st);
+               dw_gate_up, accumulate, status, st);
 }
 
 cudaError_t launch_router_logits(const Dims& D, const void* x, const void* w_router,

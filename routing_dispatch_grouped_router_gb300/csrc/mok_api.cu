@@ -91,20 +91,38 @@ mok_status make_dims(const mok_moe_desc* desc, Dims* out) {
   if (!desc || !out) return MOK_ERR_INVALID_ARG;
   const mok_moe_desc& d = *desc;
   if (d.T < 0 || d.d <= 0 || d.E <= 0 || d.I <= 0 || d.k <= 0) return MOK_ERR_INVALID_ARG;
-  if (d.dtype != MOK_BF16) return MOK_ERR_UNSUPPORTED;
-  if (d.mb_tokens != 0 || d.ring_slots != 0) return MOK_ERR_UNSUPPORTED;
-  if (d.flags & ~(MOK_FLAG_BF16_ACT_OUT | MOK_FLAG_BF16_WGRAD_OUT)) return MOK_ERR_UNSUPPORTED;
+  if (d.dtype != MOK_BF16 && d.dtype != MOK_MXFP8) return MOK_ERR_UNSUPPORTED;
+  if (d.mb_tokens < 0 || d.ring_slots < 0) return MOK_ERR_INVALID_ARG;
+  if (d.flags & ~(MOK_FLAG_BF16_ACT_OUT | MOK_FLAG_BF16_WGRAD_OUT | MOK_FLAG_ACCUMULATE_WGRAD |
+                  MOK_FLAG_RECOMPUTE_GATE_UP))
+    return MOK_ERR_UNSUPPORTED;
+  if ((d.flags & MOK_FLAG_ACCUMULATE_WGRAD) && (d.flags & MOK_FLAG_BF16_WGRAD_OUT))
+    return MOK_ERR_UNSUPPORTED;  // accumulation is fp32 only
   if (d.E > kMaxExperts || d.k > kMaxTopK || d.k > d.E) return MOK_ERR_UNSUPPORTED;
   if (d.d % 128 != 0 || d.I % 128 != 0) return MOK_ERR_UNSUPPORTED;
   if (d.d > 16384 || d.I > 16384) return MOK_ERR_UNSUPPORTED;
   if (d.T * d.k >= (1LL << 31) / 2) return MOK_ERR_UNSUPPORTED;
   Dims D;
-  D.T = d.T;
+  D.T_total = d.T;
+  D.nmb = 1;
+  D.ring = 1;
+  int64_t mb = d.T;
+  if (d.mb_tokens > 0 && d.T > 0) {
+    if (d.T % d.mb_tokens != 0) return MOK_ERR_UNSUPPORTED;
+    if (d.flags & MOK_FLAG_BF16_WGRAD_OUT) return MOK_ERR_UNSUPPORTED;  // fp32 accumulation
+    mb = d.mb_tokens;
+    D.nmb = static_cast<int>(d.T / d.mb_tokens);
+    if (d.ring_slots > D.nmb) return MOK_ERR_UNSUPPORTED;
+    D.ring = d.ring_slots > 0 ? d.ring_slots : D.nmb;
+  } else if (d.ring_slots > 1) {
+    return MOK_ERR_UNSUPPORTED;
+  }
+  D.T = mb;
   D.d = d.d;
   D.E = d.E;
   D.I = d.I;
   D.k = d.k;
-  D.R = d.T * d.k;
+  D.R = D.T * d.k;
   const int64_t segs = D.R < D.E ? D.R : D.E;
   D.rows_max = (D.R + (kRowPad - 1) * segs + kRowPad - 1) / kRowPad * kRowPad;
   D.nb = (D.T + kPlanBlock - 1) / kPlanBlock;
@@ -112,6 +130,9 @@ mok_status make_dims(const mok_moe_desc* desc, Dims* out) {
   D.np = static_cast<int>(D.I / D.bn_dgrad) * 2;
   D.act_bf16 = (d.flags & MOK_FLAG_BF16_ACT_OUT) != 0;
   D.wgrad_bf16 = (d.flags & MOK_FLAG_BF16_WGRAD_OUT) != 0;
+  D.mx = d.dtype == MOK_MXFP8;
+  D.accumulate = (d.flags & MOK_FLAG_ACCUMULATE_WGRAD) != 0;
+  D.recompute_gu = (d.flags & MOK_FLAG_RECOMPUTE_GATE_UP) != 0;
   // every row index and element offset used in 32-bit arithmetic must fit
   if (D.rows_max * 2 * D.I >= (1LL << 40)) return MOK_ERR_UNSUPPORTED;
   if (D.rows_max >= (1LL << 31) / 2) return MOK_ERR_UNSUPPORTED;
@@ -119,69 +140,108 @@ mok_status make_dims(const mok_moe_desc* desc, Dims* out) {
   return MOK_OK;
 }
 
-void saved_layout(const Dims& D, mok_saved_layout* L, size_t* mtile_prefix_off) {
+namespace {
+struct Bump {
   size_t o = 0;
-  auto take = [&](size_t bytes) {
+  size_t take(size_t bytes) {
     const size_t at = o;
-    o += al(bytes);
+    o += (bytes + 255) & ~static_cast<size_t>(255);
     return at;
-  };
+  }
+};
+}  // namespace
+
+void block_layout(const Dims& D, BlockL* B) {
+  Bump b;
   const size_t Tk = static_cast<size_t>(D.T) * D.k;
   const size_t E = static_cast<size_t>(D.E);
   const size_t rows = static_cast<size_t>(D.rows_max);
-  L->status = take(256);
-  L->topk_idx = take(Tk * 4);
-  L->topk_w = take(Tk * 4);
-  L->counts = take(E * 4);
-  L->offsets = take((E + 1) * 4);
-  L->pos = take(Tk * 4);
-  L->token_of_row = take(Tk * 4);
-  L->padded_offsets = take((E + 1) * 4);
-  const size_t mt = take((E + 1) * 4);
-  if (mtile_prefix_off) *mtile_prefix_off = mt;
-  L->padded_pos = take(Tk * 4);
-  L->padded_token = take(rows * 4);
-  L->row_weight = take(rows * 4);
-  L->x_perm = take(rows * D.d * 2);
-  L->gate_up = take(rows * 2 * D.I * 4);  // fp32
-  L->rows_max = rows;
-  L->total = o;
+  B->topk_idx = b.take(Tk * 4);
+  B->topk_w = b.take(Tk * 4);
+  B->counts = b.take(E * 4);
+  B->offsets = b.take((E + 1) * 4);
+  B->pos = b.take(Tk * 4);
+  B->token_of_row = b.take(Tk * 4);
+  B->padded_offsets = b.take((E + 1) * 4);
+  B->mtile_prefix = b.take((E + 1) * 4);
+  B->padded_pos = b.take(Tk * 4);
+  B->padded_token = b.take(rows * 4);
+  B->row_weight = b.take(rows * 4);
+  B->gate_up = D.recompute_gu ? 0 : b.take(rows * 2 * D.I * 4);  // fp32
+  B->total = b.o;
+}
+
+// saved = status | nmb micro-batch blocks | ring slots of dispatched rows
+void saved_layout(const Dims& D, mok_saved_layout* L, size_t* mtile_prefix_off) {
+  BlockL B;
+  block_layout(D, &B);
+  const size_t base = 256;
+  const size_t slot = static_cast<size_t>(D.rows_max) * D.d * 2;
+  const size_t slot_al = (slot + 255) & ~static_cast<size_t>(255);
+  const size_t ring0 = base + B.total * D.nmb;
+  L->status = 0;
+  L->topk_idx = base + B.topk_idx;
+  L->topk_w = base + B.topk_w;
+  L->counts = base + B.counts;
+  L->offsets = base + B.offsets;
+  L->pos = base + B.pos;
+  L->token_of_row = base + B.token_of_row;
+  L->padded_offsets = base + B.padded_offsets;
+  if (mtile_prefix_off) *mtile_prefix_off = base + B.mtile_prefix;
+  L->padded_pos = base + B.padded_pos;
+  L->padded_token = base + B.padded_token;
+  L->row_weight = base + B.row_weight;
+  L->gate_up = D.recompute_gu ? MOK_NOT_KEPT : base + B.gate_up;
+  L->x_perm = ring0;
+  L->rows_max = static_cast<size_t>(D.rows_max);
+  L->mb_count = static_cast<size_t>(D.nmb);
+  L->mb_stride = B.total;
+  L->ring_slots = static_cast<size_t>(D.ring);
+  L->ring_slot_bytes = slot_al;
+  L->total = ring0 + slot_al * D.ring;
 }
 
 void fwd_layout(const Dims& D, FwdWs* W) {
-  size_t o = 0;
-  auto take = [&](size_t bytes) {
-    const size_t at = o;
-    o += al(bytes);
-    return at;
-  };
+  Bump b;
   const size_t rows = static_cast<size_t>(D.rows_max);
-  W->block_counts = take(static_cast<size_t>(D.nb) * D.E * 4);
-  W->block_base = take(static_cast<size_t>(D.nb) * D.E * 4);
-  W->h = take(rows * D.I * 2);
-  W->o = take(rows * D.d * 4);  // fp32 expert outputs
-  W->logits = take(static_cast<size_t>(D.T) * D.E * 4);
-  W->total = o;
+  W->block_counts = b.take(static_cast<size_t>(D.nb) * D.E * 4);
+  W->block_base = b.take(static_cast<size_t>(D.nb) * D.E * 4);
+  W->h = b.take(rows * D.I * 2);
+  W->o = b.take(rows * D.d * 4);  // fp32 expert outputs
+  W->logits = b.take(static_cast<size_t>(D.T) * D.E * 4);
+  const size_t wgu = static_cast<size_t>(D.E) * 2 * D.I * D.d * 2;
+  const size_t wd = static_cast<size_t>(D.E) * D.d * D.I * 2;
+  W->xq_row = D.mx ? b.take(rows * D.d * 2) : 0;  // MXFP8 copies
+  W->wgu_row = D.mx ? b.take(wgu) : 0;
+  W->wd_row = D.mx ? b.take(wd) : 0;
+  W->total = b.o;
 }
 
 void bwd_layout(const Dims& D, BwdWs* W) {
-  size_t o = 0;
-  auto take = [&](size_t bytes) {
-    const size_t at = o;
-    o += al(bytes);
-    return at;
-  };
+  Bump b;
   const size_t rows = static_cast<size_t>(D.rows_max);
-  W->dy_perm = take(rows * D.d * 2);
-  W->dgu_hi = take(rows * 2 * D.I * 2);
-  W->dgu_lo = take(rows * 2 * D.I * 2);
-  W->p_hi = take(rows * D.I * 2);
-  W->p_lo = take(rows * D.I * 2);
-  W->dp_part = take(rows * D.np * 4);
-  W->dx_perm = take(rows * D.d * 4);  // fp32
-  W->dl_row = take(rows * 4);
-  W->dl_tok = take(static_cast<size_t>(D.T) * D.k * 4);
-  W->total = o;
+  W->dy_perm = b.take(rows * D.d * 2);
+  W->dgu_hi = b.take(rows * 2 * D.I * 2);
+  W->dgu_lo = b.take(rows * 2 * D.I * 2);
+  W->p_hi = b.take(rows * D.I * 2);
+  W->p_lo = b.take(rows * D.I * 2);
+  W->dp_part = b.take(rows * D.np * 4);
+  W->dx_perm = b.take(rows * D.d * 4);  // fp32
+  W->dl_row = b.take(rows * 4);
+  W->dl_tok = b.take(static_cast<size_t>(D.T) * D.k * 4);
+  const size_t wgu = static_cast<size_t>(D.E) * 2 * D.I * D.d * 2;
+  const size_t wd = static_cast<size_t>(D.E) * D.d * D.I * 2;
+  W->dyq_row = D.mx ? b.take(rows * D.d * 2) : 0;  // MXFP8 copies
+  W->dyq_col = D.mx ? b.take(rows * D.d * 2) : 0;
+  W->xq_col = D.mx ? b.take(rows * D.d * 2) : 0;
+  W->dgu_mx = D.mx ? b.take(rows * 2 * D.I * 2) : 0;
+  W->wd_col = D.mx ? b.take(wd) : 0;
+  W->wgu_col = D.mx ? b.take(wgu) : 0;
+  // recompute of g, u: their fp32 rows, and the forward's MXFP8 operands
+  W->gu = D.recompute_gu ? b.take(rows * 2 * D.I * 4) : 0;
+  W->xq_row = (D.recompute_gu && D.mx) ? b.take(rows * D.d * 2) : 0;
+  W->wgu_row = (D.recompute_gu && D.mx) ? b.take(wgu) : 0;
+  W->total = b.o;
 }
 
 void stage_layout(const Dims& D, StageWs* W) {
@@ -281,35 +341,57 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
   reset_launch_count();
 
   int* status = at<int>(saved, L.status);
-  int32_t* topk_idx = at<int32_t>(saved, L.topk_idx);
-  float* topk_w = at<float>(saved, L.topk_w);
-  float* logits = at<float>(workspace, F.logits);
   MOK_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
-  MOK_CUDA(launch_router_logits(D, x, w_router, logits, status, st));
-  MOK_CUDA(launch_router_topk(D, logits, router_bias, topk_idx, topk_w, status, st));
-
-  PlanOut o;
-  o.counts = at<int32_t>(saved, L.counts);
-  o.offsets = at<int32_t>(saved, L.offsets);
-  o.pos = at<int32_t>(saved, L.pos);
-  o.token_of_row = at<int32_t>(saved, L.token_of_row);
-  o.padded_offsets = at<int32_t>(saved, L.padded_offsets);
-  o.mtile_prefix = at<int32_t>(saved, mt_off);
-  o.ppos = at<int32_t>(saved, L.padded_pos);
-  o.ptok = at<int32_t>(saved, L.padded_token);
-  o.row_w = at<float>(saved, L.row_weight);
-  MOK_CUDA(launch_plan(D, topk_idx, topk_w, at<int32_t>(workspace, F.block_counts),
-                       at<int32_t>(workspace, F.block_base), o, status, st));
-
-  void* x_perm = at<char>(saved, L.x_perm);
-  void* gu = at<char>(saved, L.gate_up);
+  const void* wgu_op = w_gate_up;
+  const void* wd_op = w_down;
+  if (D.mx) {
+    // weights quantised once per call, along d (gate/up) and along I (down)
+    void* wgu_q = at<char>(workspace, F.wgu_row);
+    void* wd_q = at<char>(workspace, F.wd_row);
+    MOK_CUDA(launch_mx_rows(w_gate_up, wgu_q, D.E * 2 * D.I, D.d, nullptr, nullptr, st));
+    MOK_CUDA(launch_mx_rows(w_down, wd_q, D.E * D.d, D.I, nullptr, nullptr, st));
+    wgu_op = wgu_q;
+    wd_op = wd_q;
+  }
+  const size_t y_esz = D.act_bf16 ? 2 : 4;
+  float* logits = at<float>(workspace, F.logits);
   void* h = at<char>(workspace, F.h);
   void* O = at<char>(workspace, F.o);
-  MOK_CUDA(launch_gather_rows(D, x, o.ptok, o.padded_offsets, x_perm, status, st));
-  MOK_CUDA(gemm_fwd_gate_up(D, x_perm, w_gate_up, o.mtile_prefix, o.padded_offsets, gu, h, status,
-                            st));
-  MOK_CUDA(gemm_fwd_down(D, h, w_down, o.mtile_prefix, o.padded_offsets, O, status, st));
-  MOK_CUDA(launch_combine(D, static_cast<const float*>(O), o.ppos, topk_w, y, st));
+  for (int i = 0; i < D.nmb; ++i) {
+    // micro-batch i: tokens [i*T, (i+1)*T), dispatched into ring slot i % ring
+    const char* xi = static_cast<const char*>(x) + static_cast<size_t>(i) * D.T * D.d * 2;
+    char* yi = static_cast<char*>(y) + static_cast<size_t>(i) * D.T * D.d * y_esz;
+    const size_t blk = static_cast<size_t>(i) * L.mb_stride;
+    int32_t* topk_idx = at<int32_t>(saved, L.topk_idx + blk);
+    float* topk_w = at<float>(saved, L.topk_w + blk);
+    MOK_CUDA(launch_router_logits(D, xi, w_router, logits, status, st));
+    MOK_CUDA(launch_router_topk(D, logits, router_bias, topk_idx, topk_w, status, st));
+    PlanOut o;
+    o.counts = at<int32_t>(saved, L.counts + blk);
+    o.offsets = at<int32_t>(saved, L.offsets + blk);
+    o.pos = at<int32_t>(saved, L.pos + blk);
+    o.token_of_row = at<int32_t>(saved, L.token_of_row + blk);
+    o.padded_offsets = at<int32_t>(saved, L.padded_offsets + blk);
+    o.mtile_prefix = at<int32_t>(saved, mt_off + blk);
+    o.ppos = at<int32_t>(saved, L.padded_pos + blk);
+    o.ptok = at<int32_t>(saved, L.padded_token + blk);
+    o.row_w = at<float>(saved, L.row_weight + blk);
+    MOK_CUDA(launch_plan(D, topk_idx, topk_w, at<int32_t>(workspace, F.block_counts),
+                         at<int32_t>(workspace, F.block_base), o, status, st));
+    void* x_perm = at<char>(saved, L.x_perm + (i % D.ring) * L.ring_slot_bytes);
+    void* gu = D.recompute_gu ? nullptr : at<char>(saved, L.gate_up + blk);
+    MOK_CUDA(launch_gather_rows(D, xi, o.ptok, o.padded_offsets, x_perm, status, st));
+    const void* x_op = x_perm;
+    if (D.mx) {
+      void* xq = at<char>(workspace, F.xq_row);
+      MOK_CUDA(launch_mx_rows(x_perm, xq, D.rows_max, D.d, nullptr, nullptr, st));
+      x_op = xq;
+    }
+    MOK_CUDA(gemm_fwd_gate_up(D, x_op, wgu_op, o.mtile_prefix, o.padded_offsets, gu, h, status,
+                              st));
+    MOK_CUDA(gemm_fwd_down(D, h, wd_op, o.mtile_prefix, o.padded_offsets, O, status, st));
+    MOK_CUDA(launch_combine(D, static_cast<const float*>(O), o.ppos, topk_w, yi, st));
+  }
   return MOK_OK;
 }
 
@@ -319,17 +401,17 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
                             size_t saved_bytes, void* dx, void* dw_router, void* dw_gate_up,
                             void* dw_down, void* workspace, size_t ws_bytes, void* stream) {
   (void)router_bias;
-  (void)x;
   Dims D;
   mok_status s = make_dims(desc, &D);
   if (s != MOK_OK) return s;
-  const bool empty = D.T == 0;  // no token rows: dy and dx may be NULL
-  if ((!dy && !empty) || !w_router || !w_gate_up || !w_down || !saved || (!dx && !empty) ||
-      !dw_router || !dw_gate_up || !dw_down || !workspace)
+  const bool empty = D.T == 0;  // no token rows: dy, x and dx may be NULL
+  if ((!dy && !empty) || (!x && !empty && D.ring < D.nmb) || !w_router || !w_gate_up ||
+      !w_down || !saved || (!dx && !empty) || !dw_router || !dw_gate_up || !dw_down ||
+      !workspace)
     return MOK_ERR_INVALID_ARG;
-  if (!aligned16(dy) || !aligned16(w_router) || !aligned16(w_gate_up) || !aligned16(w_down) ||
-      !aligned16(saved) || !aligned16(dx) || !aligned16(dw_router) || !aligned16(dw_gate_up) ||
-      !aligned16(dw_down) || !aligned16(workspace))
+  if (!aligned16(dy) || !aligned16(x) || !aligned16(w_router) || !aligned16(w_gate_up) ||
+      !aligned16(w_down) || !aligned16(saved) || !aligned16(dx) || !aligned16(dw_router) ||
+      !aligned16(dw_gate_up) || !aligned16(dw_down) || !aligned16(workspace))
     return MOK_ERR_INVALID_ARG;
   mok_saved_layout L;
   size_t mt_off;
@@ -343,17 +425,6 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
 
   // the status word lives in `saved`; the backward reports into it as well
   int* status = const_cast<int*>(at<int>(saved, L.status));
-  const int32_t* topk_idx = at<int32_t>(saved, L.topk_idx);
-  const float* topk_w = at<float>(saved, L.topk_w);
-  const int32_t* counts = at<int32_t>(saved, L.counts);
-  const int32_t* poff = at<int32_t>(saved, L.padded_offsets);
-  const int32_t* mtp = at<int32_t>(saved, mt_off);
-  const int32_t* ppos = at<int32_t>(saved, L.padded_pos);
-  const int32_t* ptok = at<int32_t>(saved, L.padded_token);
-  const float* row_w = at<float>(saved, L.row_weight);
-  const void* x_perm = at<char>(saved, L.x_perm);
-  const void* gu = at<char>(saved, L.gate_up);
-
   void* dy_perm = at<char>(workspace, B.dy_perm);
   void* dgu_hi = at<char>(workspace, B.dgu_hi);
   void* dgu_lo = at<char>(workspace, B.dgu_lo);
@@ -363,23 +434,92 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
   float* dx_perm = at<float>(workspace, B.dx_perm);
   float* dl_row = at<float>(workspace, B.dl_row);
   float* dl_tok = at<float>(workspace, B.dl_tok);
-
-  // reverse-combine: pull dy rows into expert order
-  MOK_CUDA(launch_gather_rows(D, dy, ptok, poff, dy_perm, status, st));
-  // down-projection dgrad + SwiGLU backward + router-weight partials;
-  // dG, dU and P = p h leave as bf16 hi/lo pairs
-  MOK_CUDA(gemm_bwd_down_dgrad(D, dy_perm, w_down, mtp, poff, static_cast<const float*>(gu),
-                               row_w, dgu_hi, dgu_lo, p_hi, p_lo, dp_part, status, st));
-  // down-projection wgrad: dW_down_e = dY_e^T (P_hi + P_lo)_e
-  MOK_CUDA(gemm_wgrad_down(D, dy_perm, p_hi, p_lo, poff, dw_down, status, st));
-  // gate/up dgrad: dX_perm = dGU_hi W_gu (fp32 rows)
-  MOK_CUDA(gemm_bwd_gate_up_dgrad(D, dgu_hi, w_gate_up, mtp, poff, dx_perm, status, st));
-  // gate/up wgrad: dW_gu_e = (dGU_hi + dGU_lo)_e^T X_e
-  MOK_CUDA(gemm_wgrad_gate_up(D, dgu_hi, dgu_lo, x_perm, poff, dw_gate_up, status, st));
-  // reverse-dispatch + router backward
-  MOK_CUDA(launch_reverse_dispatch(D, dx_perm, ppos, topk_idx, topk_w, dp_part, w_router, dx,
-                                   dl_row, dl_tok, st));
-  MOK_CUDA(launch_router_wgrad(D, x_perm, dl_row, poff, counts, dw_router, st));
+  void* dgu_mx = D.mx ? at<char>(workspace, B.dgu_mx) : nullptr;
+  const void* wd_op = w_down;
+  const void* wgu_op = w_gate_up;
+  const void* wgu_fwd_op = w_gate_up;  // operand of the recomputed gate/up GEMM
+  if (D.mx && D.recompute_gu) {
+    void* q = at<char>(workspace, B.wgu_row);
+    MOK_CUDA(launch_mx_rows(w_gate_up, q, D.E * 2 * D.I, D.d, nullptr, nullptr, st));
+    wgu_fwd_op = q;
+  }
+  if (D.mx) {
+    // weights quantised once per call along the dgrads' reduction dims:
+    // W_down along d, W_gate_up along 2I (blocks of 32 rows)
+    void* wd_q = at<char>(workspace, B.wd_col);
+    void* wgu_q = at<char>(workspace, B.wgu_col);
+    MOK_CUDA(launch_mx_cols(w_down, wd_q, D.E * D.d, D.I, nullptr, nullptr, st));
+    MOK_CUDA(launch_mx_cols(w_gate_up, wgu_q, D.E * 2 * D.I, D.d, nullptr, nullptr, st));
+    wd_op = wd_q;
+    wgu_op = wgu_q;
+  }
+  const size_t dx_esz = D.act_bf16 ? 2 : 4;
+  // micro-batches in reverse, so the last ring slots are still resident;
+  // weight gradients accumulate in fp32 in this fixed order
+  for (int i = D.nmb - 1; i >= 0; --i) {
+    const bool first = (i == D.nmb - 1) && !D.accumulate;
+    const size_t blk = static_cast<size_t>(i) * L.mb_stride;
+    const char* dyi = static_cast<const char*>(dy) + static_cast<size_t>(i) * D.T * D.d * 2;
+    const char* xi = static_cast<const char*>(x) + static_cast<size_t>(i) * D.T * D.d * 2;
+    char* dxi = static_cast<char*>(dx) + static_cast<size_t>(i) * D.T * D.d * dx_esz;
+    const int32_t* topk_idx = at<int32_t>(saved, L.topk_idx + blk);
+    const float* topk_w = at<float>(saved, L.topk_w + blk);
+    const int32_t* counts = at<int32_t>(saved, L.counts + blk);
+    const int32_t* poff = at<int32_t>(saved, L.padded_offsets + blk);
+    const int32_t* mtp = at<int32_t>(saved, mt_off + blk);
+    const int32_t* ppos = at<int32_t>(saved, L.padded_pos + blk);
+    const int32_t* ptok = at<int32_t>(saved, L.padded_token + blk);
+    const float* row_w = at<float>(saved, L.row_weight + blk);
+    const void* gu = D.recompute_gu ? at<char>(workspace, B.gu) : at<char>(saved, L.gate_up + blk);
+    void* x_perm = const_cast<char*>(at<char>(saved, L.x_perm + (i % D.ring) * L.ring_slot_bytes));
+    if (i < D.nmb - D.ring) {
+      // the slot now holds a later micro-batch: dispatch this one again
+      MOK_CUDA(launch_gather_rows(D, xi, ptok, poff, x_perm, status, st));
+    }
+    if (D.recompute_gu) {
+      // the forward's gate/up GEMM again, g and u only (no h)
+      const void* x_op = x_perm;
+      if (D.mx) {
+        void* xq = at<char>(workspace, B.xq_row);
+        MOK_CUDA(launch_mx_rows(x_perm, xq, D.rows_max, D.d, nullptr, nullptr, st));
+        x_op = xq;
+      }
+      MOK_CUDA(gemm_fwd_gate_up(D, x_op, wgu_fwd_op, mtp, poff, const_cast<void*>(gu), nullptr,
+                                status, st));
+    }
+    // reverse-combine: pull dy rows into expert order
+    MOK_CUDA(launch_gather_rows(D, dyi, ptok, poff, dy_perm, status, st));
+    const void* dy_row_op = dy_perm;
+    const void* dy_col_op = dy_perm;
+    const void* x_col_op = x_perm;
+    if (D.mx) {
+      void* q1 = at<char>(workspace, B.dyq_row);
+      void* q2 = at<char>(workspace, B.dyq_col);
+      void* q3 = at<char>(workspace, B.xq_col);
+      MOK_CUDA(launch_mx_rows(dy_perm, q1, D.rows_max, D.d, nullptr, nullptr, st));
+      MOK_CUDA(launch_mx_cols(dy_perm, q2, D.rows_max, D.d, nullptr, nullptr, st));
+      MOK_CUDA(launch_mx_cols(x_perm, q3, D.rows_max, D.d, nullptr, nullptr, st));
+      dy_row_op = q1;
+      dy_col_op = q2;
+      x_col_op = q3;
+    }
+    // down-projection dgrad + SwiGLU backward + router-weight partials;
+    // dG, dU and P = p h leave as bf16 hi/lo pairs (and dG, dU as MXFP8)
+    MOK_CUDA(gemm_bwd_down_dgrad(D, dy_row_op, wd_op, mtp, poff, static_cast<const float*>(gu),
+                                 row_w, dgu_hi, dgu_lo, p_hi, p_lo, dgu_mx, dp_part, status, st));
+    // down-projection wgrad: dW_down_e (+)= dY_e^T (P_hi + P_lo)_e
+    MOK_CUDA(gemm_wgrad_down(D, dy_col_op, p_hi, p_lo, poff, dw_down, !first, status, st));
+    // gate/up dgrad: dX_perm = dGU W_gu (fp32 rows)
+    MOK_CUDA(gemm_bwd_gate_up_dgrad(D, D.mx ? dgu_mx : dgu_hi, wgu_op, mtp, poff, dx_perm, status,
+                                    st));
+    // gate/up wgrad: dW_gu_e (+)= (dGU_hi + dGU_lo)_e^T X_e
+    MOK_CUDA(gemm_wgrad_gate_up(D, dgu_hi, dgu_lo, x_col_op, poff, dw_gate_up, !first, status,
+                                st));
+    // reverse-dispatch + router backward
+    MOK_CUDA(launch_reverse_dispatch(D, dx_perm, ppos, topk_idx, topk_w, dp_part, w_router, dxi,
+                                     dl_row, dl_tok, st));
+    MOK_CUDA(launch_router_wgrad(D, x_perm, dl_row, poff, counts, dw_router, !first, st));
+  }
   return MOK_OK;
 }
 
@@ -400,6 +540,7 @@ mok_status mok_moe_route(const mok_moe_desc* desc, const void* x, const void* w_
   Dims D;
   mok_status s = make_dims(desc, &D);
   if (s != MOK_OK) return s;
+  if (D.nmb != 1) return MOK_ERR_UNSUPPORTED;
   if (((!x || !topk_idx || !topk_w) && D.T > 0) || !w_router || !workspace)
     return MOK_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_router) || !aligned16(workspace)) return MOK_ERR_INVALID_ARG;
@@ -424,6 +565,7 @@ mok_status mok_moe_dispatch_plan(const mok_moe_desc* desc, const int32_t* topk_i
   Dims D;
   mok_status s = make_dims(desc, &D);
   if (s != MOK_OK) return s;
+  if (D.nmb != 1) return MOK_ERR_UNSUPPORTED;
   if ((!topk_idx && D.T > 0) || !counts || !offsets || (!pos && D.T > 0) ||
       (!token_of_row && D.T > 0) || !workspace)
     return MOK_ERR_INVALID_ARG;
@@ -470,6 +612,18 @@ mok_status mok_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int a_m
   int* status = static_cast<int*>(workspace);
   MOK_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
   MOK_CUDA(gemm_dense_bf16(M, N, K, A, a_mn_major != 0, B, b_mn_major != 0, C, status, st));
+  return MOK_OK;
+}
+
+mok_status mok_selftest_bounded_wait(void* workspace, size_t ws_bytes, void* stream) {
+  if (!workspace || !aligned16(workspace)) return MOK_ERR_INVALID_ARG;
+  if (ws_bytes < 256) return MOK_ERR_WORKSPACE;
+  mok_status s = mok_check_device();
+  if (s != MOK_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* status = static_cast<int*>(workspace);
+  MOK_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
+  MOK_CUDA(launch_bounded_wait_selftest(status, st));
   return MOK_OK;
 }
 

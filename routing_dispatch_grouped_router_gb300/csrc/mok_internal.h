@@ -15,8 +15,13 @@ constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 8;
 constexpr int kPlanBlock = 256;  // tokens per block of the dispatch plan
 
-// Sizes derived from a descriptor.
+// Sizes derived from a descriptor.  T is the tokens of one micro-batch (the
+// whole batch when the descriptor asks for no micro-batching); every kernel
+// sees one micro-batch at a time.
 struct Dims {
+  int64_t T_total;   // tokens of the whole call
+  int nmb;           // micro-batches (T_total / T)
+  int ring;          // ring slots holding dispatched token rows
   int64_t T, d, E, I;
   int k;
   int64_t R;         // T*k routed rows
@@ -26,13 +31,22 @@ struct Dims {
   int np;            // dp partials per row = (I / bn_dgrad) * 2
   bool act_bf16;     // y and dx written as bf16 (else fp32)
   bool wgrad_bf16;   // dW_* written as bf16 (else fp32)
+  bool mx;           // MXFP8 expert GEMM operands
+  bool accumulate;   // backward adds into the weight gradients
+  bool recompute_gu; // g, u not kept: the backward recomputes them
 };
 
+// Offsets inside one micro-batch's block of `saved` (relative to the block).
+struct BlockL {
+  size_t topk_idx, topk_w, counts, offsets, pos, token_of_row, padded_offsets, mtile_prefix,
+      padded_pos, padded_token, row_weight, gate_up, total;
+};
 struct FwdWs {
-  size_t block_counts, block_base, h, o, logits, total;
+  size_t block_counts, block_base, h, o, logits, xq_row, wgu_row, wd_row, total;
 };
 struct BwdWs {
-  size_t dy_perm, dgu_hi, dgu_lo, p_hi, p_lo, dp_part, dx_perm, dl_row, dl_tok, total;
+  size_t dy_perm, dgu_hi, dgu_lo, p_hi, p_lo, dp_part, dx_perm, dl_row, dl_tok, dyq_row, dyq_col,
+      xq_col, dgu_mx, wd_col, wgu_col, gu, xq_row, wgu_row, total;
 };
 struct StageWs {
   size_t status, block_counts, block_base, padded_offsets, mtile_prefix, ppos, ptok, row_w,
@@ -40,6 +54,7 @@ struct StageWs {
 };
 
 mok_status make_dims(const mok_moe_desc* desc, Dims* out);
+void block_layout(const Dims& D, BlockL* B);
 void saved_layout(const Dims& D, mok_saved_layout* L, size_t* mtile_prefix_off);
 void fwd_layout(const Dims& D, FwdWs* W);
 void bwd_layout(const Dims& D, BwdWs* W);
@@ -88,10 +103,11 @@ cudaError_t launch_reverse_dispatch(const Dims& D, const float* dX_perm, const i
                                     const float* dp_part, const void* w_router, void* dx,
                                     float* dl_row, float* dl_tok, cudaStream_t st);
 
-// dW_r[e] = sum over rows of e of dl_row[r] * X_perm[r] (fp32 or bf16 out).
+// dW_r[e] (+)= sum over rows of e of dl_row[r] * X_perm[r] (fp32 or bf16 out;
+// accumulation fp32 only).
 cudaError_t launch_router_wgrad(const Dims& D, const void* X_perm, const float* dl_row,
                                 const int32_t* padded_offsets, const int32_t* counts,
-                                void* dw_router, cudaStream_t st);
+                                void* dw_router, bool accumulate, cudaStream_t st);
 
 // Grouped GEMMs on tcgen05 (see gemm.cu).
 cudaError_t gemm_fwd_gate_up(const Dims& D, const void* X_perm, const void* w_gate_up,
@@ -103,18 +119,29 @@ cudaError_t gemm_fwd_down(const Dims& D, const void* H, const void* w_down,
 cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* w_down,
                                 const int32_t* mtile_prefix, const int32_t* poff, const float* GU,
                                 const float* row_w, void* dGU_hi, void* dGU_lo, void* P_hi,
-                                void* P_lo, float* dp_part, int* status, cudaStream_t st);
+                                void* P_lo, void* dGU_mx, float* dp_part, int* status,
+                                cudaStream_t st);
 cudaError_t gemm_bwd_gate_up_dgrad(const Dims& D, const void* dGU, const void* w_gate_up,
                                    const int32_t* mtile_prefix, const int32_t* poff,
                                    void* dX_perm, int* status, cudaStream_t st);
 cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* P_hi,
-                            const void* P_lo, const int32_t* poff, void* dw_down, int* status,
-                            cudaStream_t st);
+                            const void* P_lo, const int32_t* poff, void* dw_down,
+                            bool accumulate, int* status, cudaStream_t st);
 cudaError_t gemm_wgrad_gate_up(const Dims& D, const void* dGU_hi, const void* dGU_lo,
                                const void* X_perm, const int32_t* poff, void* dw_gate_up,
-                               int* status, cudaStream_t st);
+                               bool accumulate, int* status, cudaStream_t st);
 cudaError_t gemm_dense_bf16(int64_t M, int64_t N, int64_t K, const void* A, bool a_mn,
                             const void* B, bool b_mn, void* C, int* status, cudaStream_t st);
+
+// MXFP8 fake quantisation (mx.cu): rows = blocks along each row, cols =
+// blocks of 32 rows; codes/scales may be null.
+cudaError_t launch_mx_rows(const void* in, void* out, long long rows, long long cols,
+                           uint8_t* codes, uint8_t* scales, cudaStream_t st);
+cudaError_t launch_mx_cols(const void* in, void* out, long long rows, long long cols,
+                           uint8_t* codes, uint8_t* scales, cudaStream_t st);
+
+// One CTA whose mbarrier wait can never complete: exercises the bounded wait.
+cudaError_t launch_bounded_wait_selftest(int* status, cudaStream_t st);
 
 // launches counter (host side)
 void count_launch(int n = 1);

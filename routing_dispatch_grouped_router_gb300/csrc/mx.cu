@@ -1,0 +1,136 @@
+// MXFP8 quantisation kernels (E4M3 elements, one E8M0 scale per 32 values),
+// row-wise (blocks of 32 consecutive values of a row) and column-wise (blocks
+// of 32 consecutive rows of a column).  They write the dequantised bf16 values
+// (exact: 4 significant bits times a power of two), and optionally the E4M3
+// codes and E8M0 scale bytes.
+// Source: [dothoosh] "Cursor Mixture-of-Kittens cuts MoE training latency by
+// 5.8x", "MoK technical details", bullet "Precision and scheduling"; the
+// rule itself is the OCP Microscaling v1.0 one (see mx.cuh).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "mok_internal.h"
+#include "mx.cuh"
+#include "ptx.cuh"
+
+namespace mok {
+
+// E4M3 code and E8M0 scale byte of one dequantised value v' = q * 2^shared.
+__device__ __forceinline__ uint8_t e4m3_code_of(float vq, int shared) {
+  const uint16_t q = cvt_e4m3x2(ldexpf(vq, -shared), 0.f);
+  return static_cast<uint8_t>(q >> 8);
+}
+
+__device__ __forceinline__ int mx_shared_exp(const float (&v)[32]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  if (!(amax > 0.f)) return -127;
+  int e;
+  frexpf(amax, &e);
+  const int s = e - 1 - 8;
+  return s < -127 ? -127 : (s > 127 ? 127 : s);
+}
+
+// One thread per block of 32 consecutive values of a row.
+__global__ void mx_rows_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
+                               uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                               long long nblocks) {
+  for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < nblocks;
+       b += (long long)gridDim.x * blockDim.x) {
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 w = ld_global_nc_v4(in + b * 4 + j);
+      v[8 * j + 0] = bf16lo(w.x); v[8 * j + 1] = bf16hi(w.x);
+      v[8 * j + 2] = bf16lo(w.y); v[8 * j + 3] = bf16hi(w.y);
+      v[8 * j + 4] = bf16lo(w.z); v[8 * j + 5] = bf16hi(w.z);
+      v[8 * j + 6] = bf16lo(w.w); v[8 * j + 7] = bf16hi(w.w);
+    }
+    const int shared = mx_shared_exp(v);
+    mx_fake32(v);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      out[b * 4 + j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]),
+                                  pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                                  pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                                  pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+    if (codes) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) codes[b * 32 + j] = e4m3_code_of(v[j], shared);
+    }
+    if (scales) scales[b] = static_cast<uint8_t>(shared + 127);
+  }
+}
+
+// One thread per (32-row block, column).
+__global__ void mx_cols_kernel(const __nv_bfloat16* __restrict__ in,
+                               __nv_bfloat16* __restrict__ out, uint8_t* __restrict__ codes,
+                               uint8_t* __restrict__ scales, long long row_blocks, long long cols) {
+  const long long n = row_blocks * cols;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long rb = i / cols, c = i - rb * cols;
+    const long long base = rb * 32 * cols + c;
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __bfloat162float(in[base + j * cols]);
+    const int shared = mx_shared_exp(v);
+    mx_fake32(v);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) out[base + j * cols] = __float2bfloat16_rn(v[j]);
+    if (codes) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) codes[base + j * cols] = e4m3_code_of(v[j], shared);
+    }
+    if (scales) scales[rb * cols + c] = static_cast<uint8_t>(shared + 127);
+  }
+}
+
+static unsigned grid_for(long long n, int threads) {
+  long long g = (n + threads - 1) / threads;
+  const long long cap = static_cast<long long>(num_sms_current_device()) * 16;
+  if (g > cap) g = cap;
+  return static_cast<unsigned>(g < 1 ? 1 : g);
+}
+
+cudaError_t launch_mx_rows(const void* in, void* out, long long rows, long long cols,
+                           uint8_t* codes, uint8_t* scales, cudaStream_t st) {
+  const long long nb = rows * (cols / 32);
+  if (nb == 0) return cudaSuccess;
+  ProfScope prof("mx_quant_rows", st);
+  mx_rows_kernel<<<grid_for(nb, 256), 256, 0, st>>>(static_cast<const uint4*>(in),
+                                                    static_cast<uint4*>(out), codes, scales, nb);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_cols(const void* in, void* out, long long rows, long long cols,
+                           uint8_t* codes, uint8_t* scales, cudaStream_t st) {
+  const long long n = (rows / 32) * cols;
+  if (n == 0) return cudaSuccess;
+  ProfScope prof("mx_quant_cols", st);
+  mx_cols_kernel<<<grid_for(n, 256), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(in),
+                                                   static_cast<__nv_bfloat16*>(out), codes,
+                                                   scales, rows / 32, cols);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace mok
+
+using namespace mok;
+
+extern "C" mok_status mok_mx_quantize(const void* in, int64_t rows, int64_t cols, int along_rows,
+                                      void* out, uint8_t* codes, uint8_t* scales, void* stream) {
+  if (rows < 0 || cols < 0 || (rows * cols > 0 && (!in || !out))) return MOK_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 15u)
+    return MOK_ERR_INVALID_ARG;
+  if (along_rows ? (rows % 32) : (cols % 32)) return MOK_ERR_UNSUPPORTED;
+  const mok_status s = mok_check_device();
+  if (s != MOK_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = along_rows ? launch_mx_cols(in, out, rows, cols, codes, scales, st)
+                                   : launch_mx_rows(in, out, rows, cols, codes, scales, st);
+  return e == cudaSuccess ? MOK_OK : MOK_ERR_CUDA;
+}

@@ -1,0 +1,56 @@
+// MXFP8 fake-quantisation of 32 values held by one thread: E4M3 elements with
+// one E8M0 (power-of-two) scale per block of 32, as in the OCP Microscaling
+// v1.0 rule:
+//   shared = floor(log2 max|v|) - 8   (clamped to [-127, 127]; -127 when all
+//            values are zero), 8 being the exponent of the largest E4M3 normal
+//   q      = v * 2^-shared rounded to nearest even on the E4M3 grid,
+//            saturating at +-448
+//   v'     = q * 2^shared            (exact in fp32 and in bf16)
+// Source: [dothoosh] "Cursor Mixture-of-Kittens cuts MoE training latency by
+// 5.8x", "MoK technical details", bullet "Precision and scheduling" (MXFP8).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace mok {
+
+// Two fp32 -> packed E4M3x2 (round to nearest even, saturate to finite).
+// The first operand lands in the upper byte.
+__device__ __forceinline__ uint16_t cvt_e4m3x2(float hi, float lo) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Packed E4M3x2 -> two fp32 (exact; upper byte to `hi`).
+__device__ __forceinline__ void e4m3x2_to_f32(uint16_t q, float* hi, float* lo) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(q));
+  *lo = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+  *hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
+}
+
+// In-place MXFP8 fake quantisation of one 32-value block.
+__device__ __forceinline__ void mx_fake32(float (&v)[32]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  int shared = -127;
+  if (amax > 0.f) {
+    int e;
+    frexpf(amax, &e);  // amax = m * 2^e with 0.5 <= m < 1
+    shared = e - 1 - 8;
+    shared = shared < -127 ? -127 : (shared > 127 ? 127 : shared);
+  }
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    const uint16_t q = cvt_e4m3x2(ldexpf(v[j + 1], -shared), ldexpf(v[j], -shared));
+    float hi, lo;
+    e4m3x2_to_f32(q, &hi, &lo);
+    v[j] = ldexpf(lo, shared);
+    v[j + 1] = ldexpf(hi, shared);
+  }
+}
+
+}  // namespace mok

@@ -50,6 +50,7 @@ extern "C" mok_status mok_moe_dispatch_plan_noalloc(const mok_moe_desc* desc,
   Dims D;
   mok_status s = make_dims(desc, &D);
   if (s != MOK_OK) return s;
+  if (D.nmb != 1) return MOK_ERR_UNSUPPORTED;
   if ((!topk_idx && D.T > 0) || !counts || !offsets || (!pos && D.T > 0) ||
       (!token_of_row && D.T > 0))
     return MOK_ERR_INVALID_ARG;

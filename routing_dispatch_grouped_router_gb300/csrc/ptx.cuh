@@ -108,6 +108,16 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, const void* 
       : "memory");
 }
 
+// Tiled 2-D element-wise add shared -> global (fp32), tracked by bulk groups.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* tm, const void* src,
+                                                  int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3}], [%1];" ::"l"(reinterpret_cast<uint64_t>(tm)),
+      "r"(smem_addr(src)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
                                           uint64_t* bar) {
@@ -139,6 +149,12 @@ __device__ __forceinline__ void bulk_wait_read() {
 template <int N>
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Asks L2 to fetch `bytes` (a multiple of 16) at a 16-byte aligned global
+// address; no data reaches the SM and nothing waits for it.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -567,7 +567,8 @@ __device__ __forceinline__ void axpy8(float (&acc)[8], float w, uint4 v) {
 template <bool BF16_OUT>
 __global__ void router_wgrad_kernel(const uint4* __restrict__ Xp, const float* __restrict__ dl_row,
                                     const int32_t* __restrict__ poff,
-                                    const int32_t* __restrict__ counts, int dv, void* dw) {
+                                    const int32_t* __restrict__ counts, int dv, void* dw,
+                                    int accumulate) {
   __shared__ float part[kRwRowLanes][8][8];
   const int e = blockIdx.x;
   const int cv = blockIdx.y * 8 + (threadIdx.x & 7);  // column vector index
@@ -595,6 +596,11 @@ __global__ void router_wgrad_kernel(const uint4* __restrict__ Xp, const float* _
                      pack_bf16x2(tot[4], tot[5]), pack_bf16x2(tot[6], tot[7]));
     } else {
       float4* q = reinterpret_cast<float4*>(dw) + 2 * o;
+      if (accumulate) {
+        const float4 a0 = q[0], a1 = q[1];
+        tot[0] += a0.x; tot[1] += a0.y; tot[2] += a0.z; tot[3] += a0.w;
+        tot[4] += a1.x; tot[5] += a1.y; tot[6] += a1.z; tot[7] += a1.w;
+      }
       q[0] = make_float4(tot[0], tot[1], tot[2], tot[3]);
       q[1] = make_float4(tot[4], tot[5], tot[6], tot[7]);
     }
@@ -603,16 +609,39 @@ __global__ void router_wgrad_kernel(const uint4* __restrict__ Xp, const float* _
 
 cudaError_t launch_router_wgrad(const Dims& D, const void* X_perm, const float* dl_row,
                                 const int32_t* padded_offsets, const int32_t* counts,
-                                void* dw_router, cudaStream_t st) {
+                                void* dw_router, bool accumulate, cudaStream_t st) {
+  if (accumulate && D.wgrad_bf16) return cudaErrorInvalidValue;
   const int dv = static_cast<int>(D.d / 8);
   dim3 grid(static_cast<unsigned>(D.E), static_cast<unsigned>((dv + 7) / 8));
   ProfScope prof("router_wgrad", st);
   if (D.wgrad_bf16)
     router_wgrad_kernel<true><<<grid, kRwRowLanes * 8, 0, st>>>(
-        static_cast<const uint4*>(X_perm), dl_row, padded_offsets, counts, dv, dw_router);
+        static_cast<const uint4*>(X_perm), dl_row, padded_offsets, counts, dv, dw_router, 0);
   else
     router_wgrad_kernel<false><<<grid, kRwRowLanes * 8, 0, st>>>(
-        static_cast<const uint4*>(X_perm), dl_row, padded_offsets, counts, dv, dw_router);
+        static_cast<const uint4*>(X_perm), dl_row, padded_offsets, counts, dv, dw_router,
+        accumulate ? 1 : 0);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// --------------------------------------------------------- bounded waits --
+
+// Waits on an mbarrier phase that nothing completes: the bounded wait gives up
+// after its limit and records MOK_ERR_DEVICE_TIMEOUT, as a GEMM would.
+__global__ void bounded_wait_selftest_kernel(int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_barrier_init();
+  const int never = 0;
+  if (!mbar_wait(&bar, 0, &never)) set_status(status, MOK_ERR_DEVICE_TIMEOUT);
+  // complete the phase so the barrier is left consistent
+  mbar_arrive(&bar);
+}
+
+cudaError_t launch_bounded_wait_selftest(int* status, cudaStream_t st) {
+  bounded_wait_selftest_kernel<<<1, 32, 0, st>>>(status);
   count_launch();
   return cudaGetLastError();
 }

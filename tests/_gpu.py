@@ -13,7 +13,8 @@ import torch
 import oracle
 from routing_dispatch_grouped_router_gb300 import api, inputs as gen
 
-BF16_TOL = 2e-2
+BF16_TOL = 2e-2   # max|diff| <= tol * rms(oracle) for BF16 layers
+MX_TOL = 6e-2     # and for MXFP8 layers
 
 
 def dev_bf16(bits: np.ndarray) -> torch.Tensor:
@@ -36,10 +37,12 @@ def rel_err(got, ref) -> float:
     return diff / rms
 
 
-def run_gpu(shape: gen.Shape, inp: dict, layer=None, flags=0):
-    """Forward + backward of one layer call; returns host copies."""
+def run_gpu(shape: gen.Shape, inp: dict, layer=None, flags=0, dtype=0, mb_tokens=0, ring_slots=0):
+    """Forward + backward of one layer call; returns host copies of the plan of
+    every micro-batch and device tensors of the outputs."""
     if layer is None:
-        layer = api.MoELayer(shape.T, shape.d, shape.E, shape.I, shape.k, flags=flags)
+        layer = api.MoELayer(shape.T, shape.d, shape.E, shape.I, shape.k, flags=flags,
+                             dtype=dtype, mb_tokens=mb_tokens, ring_slots=ring_slots)
     x = dev_bf16(inp["x"])
     wr = dev_bf16(inp["w_router"])
     wgu = dev_bf16(inp["w_gate_up"])
@@ -49,22 +52,29 @@ def run_gpu(shape: gen.Shape, inp: dict, layer=None, flags=0):
     y = layer.forward(x, wr, bias, wgu, wd)
     dx, dwr, dwgu, dwd = layer.backward(dy, x, wr, bias, wgu, wd)
     status = layer.status()
-    T, k, E = shape.T, shape.k, shape.E
+    k, E = shape.k, shape.E
     L = layer.layout
+    nmb = int(L.mb_count)
+    T = shape.T // nmb if shape.T else 0
+
+    def plan(field, dtype, shp):
+        return [layer.saved_tensor(field, dtype, shp, i).cpu().numpy() for i in range(nmb)]
     out = dict(
         status=status,
         y=y, dx=dx, dw_router=dwr, dw_gate_up=dwgu, dw_down=dwd,
-        topk_idx=layer.saved_tensor("topk_idx", torch.int32, (T, k)).cpu().numpy(),
-        topk_w=layer.saved_tensor("topk_w", torch.float32, (T, k)).cpu().numpy(),
-        counts=layer.saved_tensor("counts", torch.int32, (E,)).cpu().numpy(),
-        offsets=layer.saved_tensor("offsets", torch.int32, (E + 1,)).cpu().numpy(),
-        pos=layer.saved_tensor("pos", torch.int32, (T, k)).cpu().numpy(),
-        token_of_row=layer.saved_tensor("token_of_row", torch.int32, (T * k,)).cpu().numpy(),
-        padded_offsets=layer.saved_tensor("padded_offsets", torch.int32, (E + 1,)).cpu().numpy(),
+        topk_idx=np.concatenate(plan("topk_idx", torch.int32, (T, k))),
+        topk_w=np.concatenate(plan("topk_w", torch.float32, (T, k))),
+        mb_counts=plan("counts", torch.int32, (E,)),
+        mb_offsets=plan("offsets", torch.int32, (E + 1,)),
+        mb_pos=plan("pos", torch.int32, (T, k)),
+        mb_token_of_row=plan("token_of_row", torch.int32, (T * k,)),
         padded_pos=layer.saved_tensor("padded_pos", torch.int32, (T, k)).cpu().numpy(),
-        gate_up=layer.saved_tensor("gate_up", torch.float32, (L.rows_max, 2 * shape.I)),
-        layer=layer,
+        gate_up=(None if L.gate_up == api.NOT_KEPT else
+                 layer.saved_tensor("gate_up", torch.float32, (L.rows_max, 2 * shape.I))),
+        layer=layer, nmb=nmb, mb=T,
     )
+    out["counts"], out["offsets"] = out["mb_counts"][0], out["mb_offsets"][0]
+    out["pos"], out["token_of_row"] = out["mb_pos"][0], out["mb_token_of_row"][0]
     return out
 
 
@@ -124,38 +134,59 @@ def check_bf16_intermediate(got_bf16: np.ndarray, ref: np.ndarray, name: str):
     return frac
 
 
-def full_parity(shape: gen.Shape, inp: dict, gpu: dict, tol=BF16_TOL):
-    """Element-wise comparison of every output against the full fp64 oracle."""
+def full_parity(shape: gen.Shape, inp: dict, gpu: dict, tol=BF16_TOL, precision="fp64"):
+    """Element-wise comparison of every output against the full oracle (fp64,
+    or its mxfp8 definition).  With micro-batches each one is dispatched on
+    its own, so the plan is compared per micro-batch and the weight gradients
+    against the sum of the oracle's per-micro-batch gradients (MXFP8 blocks
+    along the token dimension are formed inside each micro-batch's expert
+    segments)."""
     assert gpu["status"] == 0, gpu["status"]
     bias = inp.get("bias")
+    nmb, mb = gpu["nmb"], gpu["mb"]
     idx, p, logits, flagged, inner = oracle.route_ref(inp["x"], inp["w_router"], bias, shape.k)
     decided = check_routing(gpu["topk_idx"], gpu["topk_w"], idx, p, flagged, inner)
-    all_same = bool(decided.all())
-    counts, offsets, pos, tok = oracle.dispatch_ref(idx, shape.E)
-    if all_same:
-        assert (gpu["counts"] == counts).all()
-        assert (gpu["offsets"] == offsets).all()
-        assert (gpu["pos"] == pos).all()
-        assert (gpu["token_of_row"] == tok).all()
-    check_dispatch_valid(gpu["topk_idx"], gpu["counts"], gpu["offsets"], gpu["pos"],
-                         gpu["token_of_row"], shape.E)
+    for i in range(nmb):
+        sl = slice(i * mb, (i + 1) * mb)
+        counts, offsets, pos, tok = oracle.dispatch_ref(idx[sl], shape.E)
+        if decided[sl].all():
+            assert (gpu["mb_counts"][i] == counts).all()
+            assert (gpu["mb_offsets"][i] == offsets).all()
+            assert (gpu["mb_pos"][i] == pos).all()
+            assert (gpu["mb_token_of_row"][i] == tok).all()
+        check_dispatch_valid(gpu["topk_idx"][sl], gpu["mb_counts"][i], gpu["mb_offsets"][i],
+                             gpu["mb_pos"][i], gpu["mb_token_of_row"][i], shape.E)
 
-    y, fwd = oracle.moe_forward_ref(inp["x"], inp["w_router"], bias, inp["w_gate_up"],
-                                    inp["w_down"], shape.k, keep=True)
-    g = oracle.moe_backward_ref(inp["x"], inp["w_router"], bias, inp["w_gate_up"],
-                                inp["w_down"], shape.k, inp["dy"], fwd=fwd)
+    args = (inp["w_router"], bias, inp["w_gate_up"], inp["w_down"], shape.k)
+    y, fwd = oracle.moe_forward_ref(inp["x"], *args, keep=True, precision=precision)
+    g = oracle.moe_backward_ref(inp["x"], *args, inp["dy"], fwd=fwd)
+    if nmb > 1:
+        parts = []
+        for i in range(nmb):
+            sl = slice(i * mb, (i + 1) * mb)
+            _, fi = oracle.moe_forward_ref(inp["x"][sl], *args, keep=True, precision=precision)
+            parts.append(oracle.moe_backward_ref(inp["x"][sl], *args, inp["dy"][sl], fwd=fi))
+        for n in ("dw_router", "dw_gate_up", "dw_down"):
+            g[n] = sum(q[n] for q in parts)
     errs = {}
     tokens = decided
     errs["y"] = rel_err(host64(gpu["y"])[tokens], y[tokens])
     errs["dx"] = rel_err(host64(gpu["dx"])[tokens], g["dx"][tokens])
-    # pre-activations kept for the backward, per routed row
-    gu = host64(gpu["gate_up"])
-    rows_gpu = gpu["padded_pos"][tokens].ravel()
-    rows_ref = pos[tokens].ravel()
-    # fp32 pre-activations saved for the backward: fp32 accumulation error only
-    errs["gate"] = rel_err(gu[rows_gpu, :shape.I], fwd["G"][rows_ref])
-    errs["up"] = rel_err(gu[rows_gpu, shape.I:], fwd["U"][rows_ref])
-    assert errs["gate"] < 1e-4 and errs["up"] < 1e-4, errs
+    # fp32 pre-activations saved for the backward (micro-batch 0): fp32
+    # accumulation error only
+    if gpu["gate_up"] is not None:
+        pos0 = oracle.dispatch_ref(idx[:mb], shape.E)[2]
+        gu = host64(gpu["gate_up"])
+        t0 = tokens[:mb]
+        rows_gpu = gpu["padded_pos"][t0].ravel()
+        rows_ref = pos0[t0].ravel()
+        if nmb > 1:
+            _, f0 = oracle.moe_forward_ref(inp["x"][:mb], *args, keep=True, precision=precision)
+        else:
+            f0 = fwd
+        errs["gate"] = rel_err(gu[rows_gpu, :shape.I], f0["G"][rows_ref])
+        errs["up"] = rel_err(gu[rows_gpu, shape.I:], f0["U"][rows_ref])
+        assert errs["gate"] < 1e-4 and errs["up"] < 1e-4, errs
     # expert gradients: leave out experts touched by an undecided token
     touched = np.zeros(shape.E, dtype=bool)
     for t in np.nonzero(~tokens)[0]:
@@ -164,13 +195,14 @@ def full_parity(shape: gen.Shape, inp: dict, gpu: dict, tol=BF16_TOL):
     keep = ~touched
     errs["dw_gate_up"] = rel_err(host64(gpu["dw_gate_up"])[keep], g["dw_gate_up"][keep])
     errs["dw_down"] = rel_err(host64(gpu["dw_down"])[keep], g["dw_down"][keep])
-    if all_same:
+    if bool(decided.all()):
         errs["dw_router"] = rel_err(host64(gpu["dw_router"]), g["dw_router"])
     for name, v in errs.items():
         assert v <= tol, (name, v, errs)
     # experts that received no rows have exactly zero weight gradients
+    counts = np.bincount(idx.ravel(), minlength=shape.E)
     empty = counts == 0
-    if all_same and empty.any():
+    if bool(decided.all()) and empty.any():
         assert (host64(gpu["dw_gate_up"])[empty] == 0).all()
         assert (host64(gpu["dw_down"])[empty] == 0).all()
         assert (host64(gpu["dw_router"])[empty] == 0).all()

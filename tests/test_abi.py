@@ -36,7 +36,8 @@ def _desc(**kw):
     base = dict(T=256, d=128, E=8, I=256, k=2)
     base.update(kw)
     return _lib.MoeDesc(T=base["T"], d=base["d"], E=base["E"], I=base["I"], k=base["k"],
-                        dtype=base.get("dtype", 0), mb_tokens=0, ring_slots=0, flags=0, reserved=0)
+                        dtype=base.get("dtype", 0), mb_tokens=base.get("mb", 0),
+                        ring_slots=base.get("ring", 0), flags=base.get("flags", 0), reserved=0)
 
 
 def _sizes(lib, desc):
@@ -46,24 +47,73 @@ def _sizes(lib, desc):
     return code, f.value, s.value, b.value
 
 
+def _regions(L, T, k, E, I, d, mb=None):
+    """(offset, bytes) of every field of one micro-batch, plus ring slot 0."""
+    Tk = (mb or T) * k
+    rows = L.rows_max
+    return [(L.status, 4), (L.topk_idx, Tk * 4), (L.topk_w, Tk * 4), (L.counts, E * 4),
+            (L.offsets, (E + 1) * 4), (L.pos, Tk * 4), (L.token_of_row, Tk * 4),
+            (L.padded_offsets, (E + 1) * 4), (L.padded_pos, Tk * 4), (L.padded_token, rows * 4),
+            (L.row_weight, rows * 4), (L.gate_up, rows * 2 * I * 4), (L.x_perm, rows * d * 2)]
+
+
+def _no_overlap(regions, total):
+    regions = sorted(regions)
+    for (o1, n1), (o2, _) in zip(regions, regions[1:]):
+        assert o1 + n1 <= o2
+    assert regions[-1][0] + regions[-1][1] <= total
+    assert all(o % 256 == 0 for o, _ in regions)
+
+
 def test_workspace_sizes_cover_the_layout(lib):
     d = _desc()
     code, f, s, b = _sizes(lib, d)
     assert code == 0 and f > 0 and s > 0 and b > 0
     L = _lib.SavedLayout()
     assert lib.mok_moe_saved_layout(ctypes.byref(d), ctypes.byref(L)) == 0
-    assert L.total == s
+    assert L.total == s and L.mb_count == 1 and L.ring_slots == 1
     R = 256 * 2
     assert L.rows_max == (R + 127 * 8 + 127) // 128 * 128
-    offs = [L.status, L.topk_idx, L.topk_w, L.counts, L.offsets, L.pos, L.token_of_row,
-            L.padded_offsets, L.padded_pos, L.padded_token, L.row_weight, L.x_perm, L.gate_up]
-    assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
-    assert L.gate_up + L.rows_max * 2 * 256 * 2 <= L.total
+    _no_overlap(_regions(L, 256, 2, 8, 256, 128), L.total)
+
+
+def test_micro_batch_layout(lib):
+    d = _desc(T=1024, mb=256, ring=2)
+    L = _lib.SavedLayout()
+    assert lib.mok_moe_saved_layout(ctypes.byref(d), ctypes.byref(L)) == 0
+    assert L.mb_count == 4 and L.ring_slots == 2
+    assert L.rows_max == (512 + 127 * 8 + 127) // 128 * 128  # per micro-batch
+    regs = []
+    for i in range(4):
+        for o, n in _regions(L, 1024, 2, 8, 256, 128, mb=256)[:-1]:
+            regs.append((o + i * L.mb_stride if o else o, n) if o else (o, n))
+    regs = [r for r in regs if r[0] != 0] + [(0, 4)]
+    for j in range(2):
+        regs.append((L.x_perm + j * L.ring_slot_bytes, L.rows_max * 128 * 2))
+    _no_overlap(list(set(regs)), L.total)
+    # micro-batching needs a divisor of T, a ring no larger than the batches,
+    # and fp32 weight gradients
+    assert _sizes(lib, _desc(T=1000, mb=256))[0] == 2
+    assert _sizes(lib, _desc(T=1024, mb=256, ring=5))[0] == 2
+    assert _sizes(lib, _desc(T=1024, mb=256, flags=2))[0] == 2
+
+
+def test_recompute_flag_drops_gate_up_from_saved(lib):
+    base, rec = _desc(T=1024, mb=256, ring=2), _desc(T=1024, mb=256, ring=2, flags=8)
+    Lb, Lr = _lib.SavedLayout(), _lib.SavedLayout()
+    assert lib.mok_moe_saved_layout(ctypes.byref(base), ctypes.byref(Lb)) == 0
+    assert lib.mok_moe_saved_layout(ctypes.byref(rec), ctypes.byref(Lr)) == 0
+    assert Lr.gate_up == (1 << 64) - 1
+    per_mb = Lb.rows_max * 2 * 256 * 4
+    assert Lb.total - Lr.total == 4 * per_mb
+    _, _, sb, bb = _sizes(lib, base)
+    _, _, sr, br = _sizes(lib, rec)
+    assert sr == Lr.total and br - bb == per_mb  # one micro-batch of g, u in the scratch
 
 
 @pytest.mark.parametrize("kw,expect", [
     (dict(k=9, E=16), 2), (dict(k=3, E=2), 2), (dict(E=513), 2), (dict(d=96), 2),
-    (dict(I=200), 2), (dict(dtype=1), 2), (dict(T=-1), 1), (dict(k=0), 1), (dict(d=0), 1),
+    (dict(I=200), 2), (dict(dtype=2), 2), (dict(T=-1), 1), (dict(k=0), 1), (dict(d=0), 1),
 ])
 def test_invalid_shapes_are_rejected(lib, kw, expect):
     code, *_ = _sizes(lib, _desc(**kw))

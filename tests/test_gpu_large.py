@@ -111,3 +111,57 @@ def test_full_size_sampled_parity(name):
     print(name, errs)
     for n, v in errs.items():
         assert v <= _gpu.BF16_TOL, (n, v, errs)
+
+
+def test_mxfp8_workload_sampled_parity():
+    """MXFP8 expert GEMMs, T=16384 in 8 micro-batches of 2048 through a ring
+    of 2 slots (micro-batches 0..5 are dispatched again in the backward);
+    BF16 activation outputs, fp32 weight gradients.  Bar 6e-2 * rms."""
+    from routing_dispatch_grouped_router_gb300 import api
+    name = "mxfp8"
+    w = gen.WORKLOADS[name]
+    shape = gen.workload_shape(name)
+    inp = gen.workload_inputs(name, seed=0, parallel=True)
+    gpu = _gpu.run_gpu(shape, inp, dtype=api.MXFP8, flags=api.FLAG_BF16_ACT_OUT,
+                       mb_tokens=w["mb_tokens"], ring_slots=w["ring_slots"])
+    assert gpu["status"] == 0 and gpu["nmb"] == 8
+    k, E, mb = shape.k, shape.E, gpu["mb"]
+    idx, p, _, flagged, inner = oracle.route_ref(inp["x"], inp["w_router"], None, k)
+    decided = _gpu.check_routing(gpu["topk_idx"], gpu["topk_w"], idx, p, flagged, inner)
+    rng = np.random.default_rng(99)
+    errs = {}
+    args = (inp["w_router"], None, inp["w_gate_up"], inp["w_down"])
+    toks = np.sort(rng.choice(np.nonzero(decided)[0], size=6, replace=False))
+    y_ref, fwd = oracle.moe_forward_ref(inp["x"][toks], *args, k, keep=True, precision="mxfp8")
+    g = oracle.moe_backward_ref(inp["x"][toks], *args, k, inp["dy"][toks], fwd=fwd,
+                                grad_experts=[])
+    errs["y"] = _gpu.rel_err(_gpu.host64(gpu["y"][toks]), y_ref)
+    errs["dx"] = _gpu.rel_err(_gpu.host64(gpu["dx"][toks]), g["dx"])
+    touched = np.zeros(E, dtype=bool)
+    for t in np.nonzero(~decided)[0]:
+        touched[idx[t]] = True
+        touched[gpu["topk_idx"][t]] = True
+    counts = np.bincount(idx.ravel(), minlength=E)
+    ok = (counts > 0) & ~touched
+    for e in rng.choice(np.nonzero(ok)[0], size=2, replace=False):
+        dwgu = 0.0
+        dwd = 0.0
+        for i in range(gpu["nmb"]):
+            sl = np.arange(i * mb, (i + 1) * mb)
+            rows = sl[(idx[sl] == e).any(axis=1)]
+            if len(rows) == 0:
+                continue
+            slot = np.argmax(idx[rows] == e, axis=1)
+            pe = p[rows, slot][:, None]
+            ie = np.full((len(rows), 1), e, dtype=np.int32)
+            _, fe = oracle.moe_forward_ref(inp["x"][rows], *args, 1, routing=(ie, pe), keep=True,
+                                           precision="mxfp8")
+            ge = oracle.moe_backward_ref(inp["x"][rows], *args, 1, inp["dy"][rows], fwd=fe,
+                                         grad_experts=[e])
+            dwgu = dwgu + ge["dw_gate_up"][e]
+            dwd = dwd + ge["dw_down"][e]
+        errs[f"dw_gate_up[{e}]"] = _gpu.rel_err(_gpu.host64(gpu["dw_gate_up"][e]), dwgu)
+        errs[f"dw_down[{e}]"] = _gpu.rel_err(_gpu.host64(gpu["dw_down"][e]), dwd)
+    print(name, errs)
+    for n, v in errs.items():
+        assert v <= _gpu.MX_TOL, (n, v, errs)

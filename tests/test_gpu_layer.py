@@ -136,6 +136,64 @@ def test_bf16_output_flags_round_the_fp32_outputs():
         assert torch.equal(a[n].to(torch.bfloat16).view(torch.int16), b[n].view(torch.int16)), n
 
 
+@pytest.mark.parametrize("dtype,mb,ring", [(0, 0, 0), (0, 256, 1), (1, 256, 2)])
+def test_recompute_gate_up_is_bitwise_identical(dtype, mb, ring):
+    """The backward's recomputed g, u equal the ones the forward would have
+    kept, so every output is bitwise the same as without the flag."""
+    shape = gen.Shape(T=1024, d=256, E=8, I=256, k=2)
+    inp = gen.make_inputs(shape, seed=5)
+    outs = []
+    for flags in (0, api.FLAG_RECOMPUTE_GATE_UP):
+        g = _gpu.run_gpu(shape, inp, flags=flags, dtype=dtype, mb_tokens=mb, ring_slots=ring)
+        assert g["status"] == 0
+        assert (g["gate_up"] is None) == bool(flags)
+        outs.append([g[n].view(torch.int32).cpu().numpy() for n in
+                     ("y", "dx", "dw_router", "dw_gate_up", "dw_down")])
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b)
+
+
+def test_recompute_gate_up_parity():
+    shape = SMALL["wide"]
+    inp = gen.make_inputs(shape, seed=1)
+    gpu = _gpu.run_gpu(shape, inp, flags=api.FLAG_RECOMPUTE_GATE_UP)
+    _gpu.full_parity(shape, inp, gpu)
+
+
+def test_accumulate_wgrad_flag_adds_into_the_gradients():
+    shape = SMALL["wide"]
+    inp = gen.make_inputs(shape, seed=2)
+    a = _gpu.run_gpu(shape, inp)
+    layer = api.MoELayer(shape.T, shape.d, shape.E, shape.I, shape.k,
+                         flags=api.FLAG_ACCUMULATE_WGRAD)
+    x, wr, wgu, wd, dy = (_gpu.dev_bf16(inp[n]) for n in ("x", "w_router", "w_gate_up", "w_down",
+                                                          "dy"))
+    dws = [torch.zeros(t.shape, dtype=torch.float32, device="cuda") for t in (wr, wgu, wd)]
+    for _ in range(2):
+        layer.forward(x, wr, None, wgu, wd)
+        layer.backward(dy, x, wr, None, wgu, wd, dw_router=dws[0], dw_gate_up=dws[1],
+                       dw_down=dws[2])
+    assert layer.status() == 0
+    for got, one in zip(dws, (a["dw_router"], a["dw_gate_up"], a["dw_down"])):
+        assert torch.equal(got, 2 * one)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A wait that nothing completes ends with MOK_ERR_DEVICE_TIMEOUT in the
+    status word (no hang, no trap), and the next call runs normally."""
+    from routing_dispatch_grouped_router_gb300 import _lib
+    import ctypes
+    lib = _lib.load()
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    code = lib.mok_selftest_bounded_wait(ctypes.c_void_p(ws.data_ptr()), 256,
+                                         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert code == 0
+    assert api.device_status(ws) == 18  # MOK_ERR_DEVICE_TIMEOUT
+    shape = SMALL["tiny"]
+    inp = gen.make_inputs(shape, seed=0)
+    _gpu.full_parity(shape, inp, _gpu.run_gpu(shape, inp))
+
+
 # ------------------------------------------------------------ stage APIs ---
 
 def test_route_stage_matches_oracle():
@@ -187,3 +245,80 @@ def test_dispatch_plan_flags_bad_indices():
     p = pos.cpu().numpy()
     assert p[3, 1] == -1 and p[7, 1] == -1
     assert counts.cpu().numpy().sum() == T * k - 2
+
+
+# --------------------------------------------------- micro-batches, MXFP8 ---
+
+@pytest.mark.parametrize("ring", [0, 1, 2])
+def test_layer_micro_batched_bf16(ring):
+    """Four micro-batches of 256 tokens through a ring of `ring` slots
+    (0 = one per micro-batch; 1 and 2 re-dispatch evicted slots in backward)."""
+    shape = gen.Shape(T=1024, d=256, E=8, I=256, k=2)
+    inp = gen.make_inputs(shape, seed=2)
+    gpu = _gpu.run_gpu(shape, inp, mb_tokens=256, ring_slots=ring)
+    assert gpu["nmb"] == 4
+    _gpu.full_parity(shape, inp, gpu)
+
+
+@pytest.mark.parametrize("name", ["tiny", "wide", "k1_I384"])
+def test_layer_parity_mxfp8(name):
+    shape = SMALL[name]
+    inp = gen.make_inputs(shape, seed=0)
+    gpu = _gpu.run_gpu(shape, inp, dtype=api.MXFP8, flags=api.FLAG_BF16_ACT_OUT)
+    errs = _gpu.full_parity(shape, inp, gpu, tol=_gpu.MX_TOL, precision="mxfp8")
+    print(name, errs)
+
+
+def test_layer_micro_batched_mxfp8():
+    shape = gen.Shape(T=1024, d=512, E=16, I=512, k=4)
+    inp = gen.make_inputs(shape, seed=3)
+    gpu = _gpu.run_gpu(shape, inp, dtype=api.MXFP8, flags=api.FLAG_BF16_ACT_OUT, mb_tokens=256,
+                       ring_slots=2)
+    errs = _gpu.full_parity(shape, inp, gpu, tol=_gpu.MX_TOL, precision="mxfp8")
+    print(errs)
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_micro_batched_deterministic(dtype):
+    shape = gen.Shape(T=1024, d=256, E=8, I=256, k=2)
+    inp = gen.make_inputs(shape, seed=4)
+    layer = api.MoELayer(shape.T, shape.d, shape.E, shape.I, shape.k, dtype=dtype,
+                         mb_tokens=256, ring_slots=2)
+    outs = []
+    for _ in range(3):
+        g = _gpu.run_gpu(shape, inp, layer=layer)
+        outs.append([g[n].view(torch.int32).cpu().numpy().copy() for n in
+                     ("y", "dx", "dw_router", "dw_gate_up", "dw_down")])
+    for a, b in zip(outs[0], outs[1]):
+        assert np.array_equal(a, b)
+    for a, b in zip(outs[0], outs[2]):
+        assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------------ MXFP8 ---
+
+@pytest.mark.parametrize("along_rows", [False, True])
+def test_mx_quantize_bit_exact(along_rows):
+    rng = np.random.default_rng(7)
+    a = rng.standard_normal((96, 160)).astype(np.float32) * np.exp(
+        rng.uniform(-30, 30, (96, 1)).astype(np.float32))
+    a[5, :32] = 0.0
+    a[:32, 7] = 0.0
+    bits = gen.f32_to_bf16_bits(a)
+    x = _gpu.dev_bf16(bits)
+    codes = torch.empty(a.shape, dtype=torch.uint8, device="cuda")
+    nsc = (96 // 32, 160) if along_rows else (96, 160 // 32)
+    scales = torch.empty(nsc, dtype=torch.uint8, device="cuda")
+    out = api.mx_quantize(x, along_rows, codes=codes, scales=scales)
+    ref, shared = oracle.mx_quantize(gen.bf16_bits_to_f32(bits).astype(np.float64),
+                                     axis=0 if along_rows else 1)
+    assert np.array_equal(_gpu.host64(out), ref)
+    # the oracle lists the blocks of a column along its last axis
+    shared = shared.T if along_rows else shared
+    assert np.array_equal(scales.cpu().numpy().astype(np.int64), shared + 127)
+    # codes decode (sign, exponent bias 7, 3 mantissa bits) to ref / 2^shared
+    c = codes.cpu().numpy().astype(np.int64)
+    s, e, m = c >> 7, (c >> 3) & 15, c & 7
+    mag = np.where(e > 0, 2.0 ** (e - 7) * (1 + m / 8), 2.0 ** -6 * (m / 8))
+    sh = np.repeat(shared, 32, axis=0) if along_rows else np.repeat(shared, 32, axis=1)
+    np.testing.assert_array_equal(np.where(s == 1, -mag, mag) * 2.0 ** sh, ref)
