@@ -57,15 +57,19 @@ def gemm_flops(shape: gen.Shape) -> dict:
 
 
 def mover_bytes(shape: gen.Shape) -> dict:
-    R, d, T, k = shape.R, shape.d, shape.T, shape.k
-    row = 2 * d
+    """Bytes each data-movement kernel must move in the layer's layout: bf16
+    token rows, fp32 expert-output and dX rows, fp32 y and dx (the default)."""
+    R, d, T, E, I = shape.R, shape.d, shape.T, shape.E, shape.I
+    np_ = 2 * I // (256 if I % 256 == 0 else 128)
     return {
-        # read each token row once per routed copy, write R rows (+ indices)
-        "gather_rows": R * row + R * row + R * 4,
-        # read k expert rows + weights per token, write the token row
-        "combine": R * row + T * row + R * 8,
-        # read k dX rows and k router rows (router rows come from L2), write dx
-        "reverse_dispatch": R * row + T * row + R * 12,
+        # read each token row once per routed copy, write R bf16 rows (+ indices)
+        "gather_rows": R * 2 * d * 2 + R * 4,
+        # read k fp32 expert rows + weights per token, write the fp32 token row
+        "combine": R * 4 * d + T * 4 * d + R * 8,
+        # read k fp32 dX rows and the dp partials, write fp32 dx (router rows from L2)
+        "reverse_dispatch": R * 4 * d + T * 4 * d + R * (12 + 4 * np_),
+        # read the dispatched bf16 rows once, write dW_r
+        "router_wgrad": R * 2 * d + E * d * 4,
     }
 
 
@@ -225,6 +229,66 @@ def job_throughput(world: int, tokens_per_rank: int, steps: int, t_max_ms: float
 
 # --------------------------------------------------------------- GPU side --
 
+def e2e_pipelined(layer, inp, x, dy, wr, wgu, wd, dwr, dwgu, dwd, stream, steps, world, dist):
+    """Milliseconds for `steps` layer steps through the public API, each with
+    its inputs uploaded from and its outputs read back to pinned host memory
+    inside the timed region (copies on a side stream, two buffer sets)."""
+    import torch
+    xh = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    dyh = torch.from_numpy(inp["dy"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    yh = [torch.empty(xh.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    dxh = [torch.empty(xh.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    xd = [torch.empty_like(x) for _ in range(2)]
+    dyd = [torch.empty_like(dy) for _ in range(2)]
+    yd = [torch.empty(x.shape, dtype=torch.float32, device=x.device) for _ in range(2)]
+    dxd = [torch.empty(x.shape, dtype=torch.float32, device=x.device) for _ in range(2)]
+    copy = torch.cuda.Stream()
+    inputs_in = [torch.cuda.Event() for _ in range(2)]      # upload into set b done
+    inputs_free = [torch.cuda.Event() for _ in range(2)]    # the step that read set b finished
+    outputs_out = [torch.cuda.Event() for _ in range(2)]    # read-back of set b done
+    outputs_ready = [torch.cuda.Event() for _ in range(2)]  # the step that wrote set b finished
+
+    def run(n):
+        with torch.cuda.stream(copy):
+            xd[0].copy_(xh, non_blocking=True)
+            dyd[0].copy_(dyh, non_blocking=True)
+            inputs_in[0].record(copy)
+        for i in range(n):
+            b = i % 2
+            if i + 1 < n:  # upload the next step's inputs into the other set
+                with torch.cuda.stream(copy):
+                    if i >= 1:
+                        copy.wait_event(inputs_free[1 - b])
+                    xd[1 - b].copy_(xh, non_blocking=True)
+                    dyd[1 - b].copy_(dyh, non_blocking=True)
+                    inputs_in[1 - b].record(copy)
+            stream.wait_event(inputs_in[b])
+            if i >= 2:
+                stream.wait_event(outputs_out[b])  # y, dx of step i-2 read back
+            layer.forward(xd[b], wr, None, wgu, wd, y=yd[b])
+            layer.backward(dyd[b], xd[b], wr, None, wgu, wd, dx=dxd[b], dw_router=dwr,
+                           dw_gate_up=dwgu, dw_down=dwd)
+            inputs_free[b].record(stream)
+            outputs_ready[b].record(stream)
+            with torch.cuda.stream(copy):
+                copy.wait_event(outputs_ready[b])
+                yh[b].copy_(yd[b], non_blocking=True)
+                dxh[b].copy_(dxd[b], non_blocking=True)
+                outputs_out[b].record(copy)
+        stream.wait_stream(copy)
+
+    run(3)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run(steps)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -349,39 +413,18 @@ def main():
             gbs = b / (kernels[n][1] / kernels[n][0] / 1e3) / 1e9
             movers_perf[n] = {"GB/s": gbs, "frac_hbm": gbs / peaks["hbm"]}
 
-    # ---- end to end through the C ABI: pinned host in, pinned host out
-    xh = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
-    dyh = torch.from_numpy(inp["dy"].view(np.int16)).view(torch.bfloat16).pin_memory()
-    yh = torch.empty(xh.shape, dtype=torch.float32).pin_memory()
-    dxh = torch.empty(xh.shape, dtype=torch.float32).pin_memory()
-    xd, dyd = torch.empty_like(x), torch.empty_like(dy)
-
-    def e2e_step():
-        xd.copy_(xh, non_blocking=True)
-        dyd.copy_(dyh, non_blocking=True)
-        layer.forward(xd, wr, None, wgu, wd, y=y)
-        layer.backward(dyd, xd, wr, None, wgu, wd, dx=dx, dw_router=dwr, dw_gate_up=dwgu,
-                       dw_down=dwd)
-        yh.copy_(y, non_blocking=True)
-        dxh.copy_(dx, non_blocking=True)
-
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    # ---- end to end through the C ABI: every step's x, dy uploaded from
+    # pinned host memory and its y, dx read back to pinned host memory.  The
+    # copies run on a second stream, double-buffered, so that step i+1's
+    # upload and step i's read-back overlap the layer's kernels; events order
+    # every reuse of a buffer.
+    e2e_ms = e2e_pipelined(layer, inp, x, dy, wr, wgu, wd, dwr, dwgu, dwd, stream,
+                           args.e2e_steps, world, dist)
+    xh_bytes = x.numel() * 2
     if world > 1:
         e2e_ms = max_over_ranks(e2e_ms, dist, "cuda")
     e2e = {"value": job_throughput(world, shape.T, args.e2e_steps, e2e_ms), "unit": "tokens/s",
-           "h2d_bytes_per_step": 2 * xh.numel() * 2, "d2h_bytes_per_step": 2 * yh.numel() * 4,
+           "h2d_bytes_per_step": 2 * xh_bytes, "d2h_bytes_per_step": 2 * x.numel() * 4,
            "steps": args.e2e_steps}
 
     cpu = None

@@ -78,6 +78,12 @@ typedef enum mok_dtype {
  * bytes of `saved` per micro-batch for one more gate/up GEMM in the backward.
  * (h is never kept: the backward always derives it from g, u.) */
 #define MOK_FLAG_RECOMPUTE_GATE_UP 0x8u
+/* Engine choice.  By default the grouped GEMMs with 256-wide tiles run on
+ * clusters of two CTAs (256-row tiles, tcgen05.mma.cta_group::2, each SM
+ * staging half of the weight tile).  This flag runs every GEMM on single-CTA
+ * 128-row tiles instead.  Both engines accumulate every output element over
+ * the same K sequence, so the results are bitwise the same. */
+#define MOK_FLAG_SINGLE_CTA_GEMM 0x10u
 
 /* Offset value of a mok_saved_layout field the flags leave out of `saved`. */
 #define MOK_NOT_KEPT ((size_t)-1)

@@ -65,7 +65,8 @@ struct GemmArgs {
   int m_rows;        // KGROUP: rows of C per group (C viewed as [E*m_rows, N])
   int I;             // SwiGLU epilogues: FFN width
   int m_valid, n_valid;  // DENSE: valid rows / columns of C
-  const int* mtile_prefix;  // MGROUP: [E+1] prefix of 128-row tiles per expert
+  const int* mtile_prefix;  // MGROUP: [E+1] prefix of 128-row tiles per expert, then
+                            // [E+1] prefix of tile pairs (an odd count rounded up)
   const int* poff;          // MGROUP/KGROUP: [E+1] padded row offsets
   void* out;                // C (bf16 or fp32)
   long long ldo;            // C row stride (elements)
@@ -88,26 +89,51 @@ constexpr int kThreads = 320;
 constexpr int kEpiWarps = 8;
 constexpr int kStagingBytes = 4096;  // per epilogue warp: 32 rows x 128 bytes
 
-template <int BN, int SPLIT = SPLIT_NONE>
+// PAIR: the tile is 256 x BN, computed by a cluster of two CTAs with
+// tcgen05.mma.cta_group::2; each CTA stages its own 128 rows of A and BN/2
+// rows of B, and holds its 128 x BN accumulator in its own TMEM.
+// Staging bytes per epilogue warp: 4 KB (TMA-store blocks); the SwiGLU
+// backward double-buffers its fp32 g, u operands (2 x 4 KB).
+template <int EPI>
+constexpr int staging_bytes() {
+  return EPI == EPI_SWIGLU_BWD ? 8192 : kStagingBytes;
+}
+
+template <int BN, int SPLIT = SPLIT_NONE, bool PAIR = false, int STG = kStagingBytes>
 struct Cfg {
   static constexpr int BM = 128, BK = 64;
-  static constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-  static constexpr int B_BYTES = BN * BK * 2;  // 32 KB (BN=256) / 16 KB (BN=128)
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // rows of B staged by one CTA
+  static constexpr int A_BYTES = BM * BK * 2;        // 16 KB
+  static constexpr int B_BYTES = B_ROWS * BK * 2;    // 32 KB (BN=256) / 16 KB (BN=128 or PAIR)
   static constexpr int A_TILES = SPLIT == SPLIT_A ? 2 : 1;
   static constexpr int B_TILES = SPLIT == SPLIT_B ? 2 : 1;
   static constexpr int B_OFF = A_TILES * A_BYTES;  // B tile(s) follow the A tile(s)
   static constexpr int STAGE_BYTES = A_TILES * A_BYTES + B_TILES * B_BYTES;
-  static constexpr int STAGES = (196608 / STAGE_BYTES) < 6 ? (196608 / STAGE_BYTES) : 6;
+  static constexpr int BAR_BYTES = 512;
+  static constexpr int STAGE_ROOM = 232448 - 1024 - BAR_BYTES - kEpiWarps * STG;
+  static constexpr int STAGES = (STAGE_ROOM / STAGE_BYTES) < 6 ? (STAGE_ROOM / STAGE_BYTES) : 6;
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int STAGING_OFF = STAGES * STAGE_BYTES;
-  static constexpr int BAR_OFF = STAGING_OFF + kEpiWarps * kStagingBytes;
-  static constexpr int BAR_BYTES = 256;
+  static constexpr int STAGING_PER_WARP = STG;
+  static constexpr int BAR_OFF = STAGING_OFF + kEpiWarps * STG;
   static constexpr int SMEM_BYTES = 1024 + BAR_OFF + BAR_BYTES;
 };
 static_assert(Cfg<256>::SMEM_BYTES <= 232448, "smem");
 static_assert(Cfg<128>::SMEM_BYTES <= 232448, "smem");
 static_assert(Cfg<256, SPLIT_A>::SMEM_BYTES <= 232448 && Cfg<256, SPLIT_A>::STAGES >= 3, "smem");
 static_assert(Cfg<128, SPLIT_B>::SMEM_BYTES <= 232448 && Cfg<128, SPLIT_B>::STAGES >= 4, "smem");
+static_assert(Cfg<256, SPLIT_NONE, true>::SMEM_BYTES <= 232448 &&
+                  Cfg<256, SPLIT_NONE, true>::STAGES == 6, "smem");
+static_assert(Cfg<256, SPLIT_A, true>::SMEM_BYTES <= 232448 &&
+                  Cfg<256, SPLIT_A, true>::STAGES >= 4, "smem");
+static_assert(Cfg<256, SPLIT_NONE, true, 8192>::SMEM_BYTES <= 232448 &&
+                  Cfg<256, SPLIT_NONE, true, 8192>::STAGES == 5, "smem");
+static_assert(Cfg<256, SPLIT_NONE, false, 8192>::STAGES >= 3, "smem");
+// stage counts of the other configurations are unchanged by the 512-byte barrier block
+static_assert(Cfg<256>::STAGES == 4 && Cfg<128>::STAGES == 6 && Cfg<256, SPLIT_A>::STAGES == 3 &&
+                  Cfg<128, SPLIT_B>::STAGES == 4 && Cfg<256, SPLIT_NONE, true>::STAGES == 6 &&
+                  Cfg<256, SPLIT_A, true>::STAGES == 4,
+              "stages");
 
 struct Tile {
   int e, m_tile, n_tile;
@@ -121,6 +147,58 @@ __device__ __forceinline__ int total_tiles(const GemmArgs& a) {
   if (SCHED == SCHED_MGROUP) return __ldg(a.mtile_prefix + a.E) * a.n_tiles;
   if (SCHED == SCHED_KGROUP) return a.E * a.m_tiles * a.n_tiles;
   return a.m_tiles * a.n_tiles;
+}
+
+// Tiles of 256 rows for CTA pairs: MGROUP pairs the 128-row tiles of one
+// expert (2j, 2j+1); when an expert has an odd number, the odd CTA of its
+// last pair stages the even CTA's rows again and stores nothing (*valid =
+// false).  KGROUP pairs the 128-row tiles of C (their number is even).
+template <int SCHED>
+__device__ __forceinline__ int total_pairs(const GemmArgs& a) {
+  if (SCHED == SCHED_MGROUP) return __ldg(a.mtile_prefix + 2 * a.E + 1) * a.n_tiles;
+  return a.E * (a.m_tiles / 2) * a.n_tiles;
+}
+
+template <int SCHED>
+__device__ __forceinline__ Tile decode_pair(const GemmArgs& a, int t, int rank, bool* valid) {
+  Tile tl;
+  if (SCHED == SCHED_MGROUP) {
+    const int* pre = a.mtile_prefix + a.E + 1;
+    int lo = 0, hi = a.E;  // invariant: pre[lo]*nt <= t < pre[hi]*nt
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(pre + mid) * a.n_tiles <= t) lo = mid; else hi = mid;
+    }
+    const int e = lo;
+    const int q0 = __ldg(pre + e);
+    const int np_e = __ldg(pre + e + 1) - q0;
+    const int local = t - q0 * a.n_tiles;
+    const int mt_e = __ldg(a.mtile_prefix + e + 1) - __ldg(a.mtile_prefix + e);
+    tl.e = e;
+    tl.n_tile = local / np_e;
+    const int pair = local - tl.n_tile * np_e;
+    int m = 2 * pair + rank;
+    *valid = m < mt_e;
+    if (!*valid) m = 2 * pair;
+    tl.m_tile = m;
+    tl.row0 = __ldg(a.poff + e) + m * 128;
+    tl.k_row0 = 0;
+    tl.num_kb = a.num_kb;
+  } else {
+    const int mp = a.m_tiles / 2;
+    const int tpe = mp * a.n_tiles;
+    const int e = t / tpe;
+    const int local = t - e * tpe;
+    tl.e = e;
+    tl.n_tile = local / mp;
+    tl.m_tile = 2 * (local - tl.n_tile * mp) + rank;
+    tl.row0 = tl.m_tile * 128;
+    const int k0 = __ldg(a.poff + e), k1 = __ldg(a.poff + e + 1);
+    tl.k_row0 = k0;
+    tl.num_kb = (k1 - k0) / 64;
+    *valid = true;
+  }
+  return tl;
 }
 
 template <int SCHED>
@@ -208,6 +286,26 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* p, float (&v)[
     v[8 * j + 2] = bf16lo(w.y); v[8 * j + 3] = bf16hi(w.y);
     v[8 * j + 4] = bf16lo(w.z); v[8 * j + 5] = bf16hi(w.z);
     v[8 * j + 6] = bf16lo(w.w); v[8 * j + 7] = bf16hi(w.w);
+  }
+}
+
+// Stores 16 values as bf16 hi = bf16(v) and lo = bf16(v - hi).
+__device__ __forceinline__ void store_hi_lo16(__nv_bfloat16* hi, __nv_bfloat16* lo,
+                                              const float (&v)[16]) {
+  uint4* ph = reinterpret_cast<uint4*>(hi);
+  uint4* pl = reinterpret_cast<uint4*>(lo);
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float v0 = v[8 * q + 2 * j], v1 = v[8 * q + 2 * j + 1];
+      const float a0 = bf16_round(v0), a1 = bf16_round(v1);
+      h[j] = pack_bf16x2(a0, a1);
+      l[j] = pack_bf16x2(v0 - a0, v1 - a1);
+    }
+    ph[q] = make_uint4(h[0], h[1], h[2], h[3]);
+    pl[q] = make_uint4(l[0], l[1], l[2], l[3]);
   }
 }
 
@@ -443,14 +541,103 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
   }
 }
 
+// ------------------------------------------ SwiGLU backward, TMA operands --
+// g, u of one chunk: 32 rows (this warp's lane quarter) x 16 fp32 columns of
+// each, TMA-loaded into a 4 KB staging buffer (g at +0, u at +2048, 64-byte
+// swizzle: 16-byte chunk j of row r at chunk j ^ ((r >> 1) & 3)).  The
+// warp's chunks are numbered from the kernel start; chunk n uses buffer n & 1
+// and completes phase n >> 1 of that buffer's barrier.
+template <int BN>
+__device__ __forceinline__ void gu_issue(const GemmArgs& a, const Tile& tl, int q, int lane,
+                                         int half, int c, uint8_t* stage_buf, uint64_t* wbar,
+                                         uint32_t count, const CUtensorMap* tmG) {
+  // every lane's earlier reads of the buffer come before the copy rewrites it
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane != 0) return;
+  const int b = count & 1;
+  uint8_t* buf = stage_buf + b * 4096;
+  const int x = tl.n_tile * BN + half * (BN / 2) + c;
+  const int y = tl.row0 + q * 32;
+  mbar_arrive_expect_tx(&wbar[b], 4096);
+  tma_load_2d(buf, tmG, &wbar[b], x, y);
+  tma_load_2d(buf + 2048, tmG, &wbar[b], a.I + x, y);
+}
+
+// The SwiGLU backward epilogue of one tile (BF16 operands) with g, u staged
+// by TMA, chunk 0 already requested; the next chunk's copies are in flight
+// while this one is computed.  Returns the updated chunk count.
+template <int BN>
+__device__ __forceinline__ uint32_t swiglu_bwd_tma(const GemmArgs& a, const Tile& tl,
+                                                   uint32_t taddr, int q, int lane, int half,
+                                                   uint8_t* stage_buf, uint64_t* wbar,
+                                                   uint32_t count, const CUtensorMap* tmG,
+                                                   volatile int* vabort) {
+  constexpr int HALF_COLS = BN / 2;
+  const long long r = tl.row0 + q * 32 + lane;
+  const int I = a.I;
+  const int n0 = tl.n_tile * BN + half * HALF_COLS;
+  __nv_bfloat16* dgu_hi = static_cast<__nv_bfloat16*>(a.out) + r * (2LL * I);
+  __nv_bfloat16* dgu_lo = static_cast<__nv_bfloat16*>(a.out3) + r * (2LL * I);
+  __nv_bfloat16* p_hi = static_cast<__nv_bfloat16*>(a.out2) + r * (long long)I;
+  __nv_bfloat16* p_lo = static_cast<__nv_bfloat16*>(a.out4) + r * (long long)I;
+  const float p = a.row_w[r];
+  float dp = 0.f;
+  const int sw = (lane >> 1) & 3;
+#pragma unroll 1
+  for (int c = 0; c < HALF_COLS; c += 16, ++count) {
+    if (c + 16 < HALF_COLS)
+      gu_issue<BN>(a, tl, q, lane, half, c + 16, stage_buf, wbar, count + 1, tmG);
+    const int b = count & 1;
+    if (!mbar_wait(&wbar[b], (count >> 1) & 1u, vabort)) {
+      *vabort = 1;
+      set_status(a.status, MOK_ERR_DEVICE_TIMEOUT);
+    }
+    const uint8_t* buf = stage_buf + b * 4096 + lane * 64;
+    float g[16], u[16], dA[16], t[16];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 a4 = *reinterpret_cast<const float4*>(buf + ((j ^ sw) << 4));
+      const float4 b4 = *reinterpret_cast<const float4*>(buf + 2048 + ((j ^ sw) << 4));
+      g[4 * j] = a4.x; g[4 * j + 1] = a4.y; g[4 * j + 2] = a4.z; g[4 * j + 3] = a4.w;
+      u[4 * j] = b4.x; u[4 * j + 1] = b4.y; u[4 * j + 2] = b4.z; u[4 * j + 3] = b4.w;
+    }
+    {
+      uint32_t r0[16];
+      tmem_ld16(taddr + half * HALF_COLS + c, r0);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) dA[j] = __uint_as_float(r0[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float sg;
+      const float sl = silu_f(g[j], &sg);
+      const float uu = u[j];
+      const float dh = p * dA[j];
+      dp = fmaf(dA[j], sl * uu, dp);
+      t[j] = dh * uu * (sg * (1.0f + g[j] * (1.0f - sg)));
+      dA[j] = dh * sl;
+      u[j] = p * sl * uu;
+    }
+    store_hi_lo16(dgu_hi + n0 + c, dgu_lo + n0 + c, t);
+    store_hi_lo16(dgu_hi + I + n0 + c, dgu_lo + I + n0 + c, dA);
+    store_hi_lo16(p_hi + n0 + c, p_lo + n0 + c, u);
+  }
+  __syncwarp();
+  a.dp_part[r * a.np + tl.n_tile * 2 + half] = dp;
+  return count;
+}
+
 // ------------------------------------------------------------------- kernel --
 
-template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, int SPLIT>
+template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, int SPLIT, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmL,
                 const __grid_constant__ GemmArgs args) {
-  using C = Cfg<BN, SPLIT>;
+  using C = Cfg<BN, SPLIT, PAIR, staging_bytes<EPI>()>;
+  static_assert(!PAIR || (SCHED != SCHED_DENSE && SPLIT != SPLIT_B && BN == 256), "pair");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -463,11 +650,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  // SwiGLU backward: two g/u staging buffers per epilogue warp, one barrier each
+  uint64_t* gu_bar = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF + 256);
   constexpr bool kTmaStore =
       (EPI == EPI_F32 && SCHED != SCHED_DENSE) || EPI == EPI_SWIGLU_FWD || EPI == EPI_F32_T;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // work units: tiles (one CTA) or tile pairs (one cluster of two CTAs)
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  const bool leader = rank == 0;
+  const int first = PAIR ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int step = PAIR ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -476,80 +670,111 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], kEpiWarps);
+      // PAIR: the leader's MMA waits for the epilogues of both CTAs
+      mbar_init(&tempty[i], PAIR ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(drain, 1);
+    if (EPI == EPI_SWIGLU_BWD)
+      for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(&gu_bar[i], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (threadIdx.x == 32) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (kTmaStore) tma_prefetch_desc(&tmC);
+    if (kTmaStore || EPI == EPI_SWIGLU_BWD) tma_prefetch_desc(&tmC);
     if (SPLIT != SPLIT_NONE) tma_prefetch_desc(&tmL);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, C::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before_sync();
-  __syncthreads();
+  if (PAIR) cluster_sync(); else __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   volatile int* vabort = abort_flag;
-  const int total = total_tiles<SCHED>(args);
+  const int total = PAIR ? total_pairs<SCHED>(args) : total_tiles<SCHED>(args);
+  auto tile_at = [&](int t, bool* valid) -> Tile {
+    if (PAIR) return decode_pair<SCHED>(args, t, rank, valid);
+    *valid = true;
+    return decode_tile<SCHED>(args, t);
+  };
+  // bounded waits; barriers that the other CTA of a pair completes are
+  // acquired at cluster scope
+  auto wait = [&](uint64_t* bar, uint32_t par) -> bool {
+    return PAIR ? mbar_wait_cluster(bar, par, vabort) : mbar_wait(bar, par, vabort);
+  };
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------- producer --
+      // PAIR: both CTAs load their halves; the copies complete on the
+      // leader's `full` barrier, which the leader arms for both
+      const uint32_t full_leader = PAIR ? mapa_shared(smem_addr(full), 0) : 0u;
       int stage = 0;
       uint32_t phase = 0;
       int issued_par[C::STAGES];
 #pragma unroll
       for (int s = 0; s < C::STAGES; ++s) issued_par[s] = -1;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode_tile<SCHED>(args, t);
+      for (int t = first; t < total && ok; t += step) {
+        bool valid;
+        const Tile tl = tile_at(t, &valid);
         for (int kb = 0; kb < tl.num_kb; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, vabort)) {
+          if (!wait(&empty[stage], phase ^ 1u)) {
             ok = false;
             break;
           }
           uint8_t* sA = tiles + stage * C::STAGE_BYTES;
           uint8_t* sB = sA + C::B_OFF;
-          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+          const uint32_t bar_c = full_leader + 8u * stage;
+          auto load = [&](void* dst, const CUtensorMap* tm, int x, int y) {
+            if (PAIR) tma_load_2d_pair(dst, tm, bar_c, x, y);
+            else tma_load_2d(dst, tm, &full[stage], x, y);
+          };
+          if (!PAIR) mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+          else if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
           // A tile: 128 rows (M) x 64 (K)  (+ its lo tile with SPLIT_A)
           if (!A_MN) {
-            tma_load_2d(sA, &tmA, &full[stage], kb * 64, tl.row0);
+            load(sA, &tmA, kb * 64, tl.row0);
           } else {
             const int ky = tl.k_row0 + kb * 64;
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-              tma_load_2d(sA + j * 8192, &tmA, &full[stage], tl.row0 + 64 * j, ky);
-              if (SPLIT == SPLIT_A)
-                tma_load_2d(sA + C::A_BYTES + j * 8192, &tmL, &full[stage], tl.row0 + 64 * j, ky);
+              load(sA + j * 8192, &tmA, tl.row0 + 64 * j, ky);
+              if (SPLIT == SPLIT_A) load(sA + C::A_BYTES + j * 8192, &tmL, tl.row0 + 64 * j, ky);
             }
           }
-          // B tile: BN rows (N) x 64 (K)
+          // B tile: B_ROWS rows (N) x 64 (K); PAIR: this CTA's half of N
           if (!B_MN) {
             if (EPI == EPI_SWIGLU_FWD) {
+              // gate rows n0..n0+127, then the matching up rows (+I)
               const int r0 = tl.e * args.b_group_rows + tl.n_tile * 128;
-              tma_load_2d(sB, &tmB, &full[stage], kb * 64, r0);
-              tma_load_2d(sB + 16384, &tmB, &full[stage], kb * 64, r0 + args.I);
+              if (PAIR) {
+                load(sB, &tmB, kb * 64, r0 + rank * args.I);
+              } else {
+                load(sB, &tmB, kb * 64, r0);
+                load(sB + 16384, &tmB, kb * 64, r0 + args.I);
+              }
             } else {
-              const int r0 = tl.e * args.b_group_rows + tl.n_tile * BN;
-              tma_load_2d(sB, &tmB, &full[stage], kb * 64, r0);
+              const int r0 = tl.e * args.b_group_rows + tl.n_tile * BN + rank * C::B_ROWS;
+              load(sB, &tmB, kb * 64, r0);
             }
           } else {
             int ky;
             if (SCHED == SCHED_KGROUP) ky = tl.k_row0 + kb * 64;
             else ky = tl.e * args.b_group_rows + kb * 64;
+            const int x0 = tl.n_tile * BN + rank * C::B_ROWS;
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) {
-              tma_load_2d(sB + j * 8192, &tmB, &full[stage], tl.n_tile * BN + 64 * j, ky);
-              if (SPLIT == SPLIT_B)
-                tma_load_2d(sB + C::B_BYTES + j * 8192, &tmL, &full[stage],
-                            tl.n_tile * BN + 64 * j, ky);
+            for (int j = 0; j < C::B_ROWS / 64; ++j) {
+              load(sB + j * 8192, &tmB, x0 + 64 * j, ky);
+              if (SPLIT == SPLIT_B) load(sB + C::B_BYTES + j * 8192, &tmL, x0 + 64 * j, ky);
             }
           }
           issued_par[stage] = static_cast<int>(phase);
@@ -562,36 +787,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         *vabort = 1;
         set_status(args.status, MOK_ERR_DEVICE_TIMEOUT);
-        // let the copies already issued land before the CTA can exit
+        // let the copies already issued land before the CTA can exit: their
+        // barriers where this CTA holds them, else a fixed millisecond
         const int zero = 0;
-        for (int s = 0; s < C::STAGES; ++s)
-          if (issued_par[s] >= 0) mbar_wait(&full[s], static_cast<uint32_t>(issued_par[s]), &zero);
+        if (!PAIR || leader) {
+          for (int s = 0; s < C::STAGES; ++s)
+            if (issued_par[s] >= 0)
+              mbar_wait(&full[s], static_cast<uint32_t>(issued_par[s]), &zero);
+        } else {
+          spin_ns(1000000ull);
+        }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       // ------------------------------------------------------------ MMA --
-      constexpr uint32_t idesc = idesc_bf16_f32(128, BN, A_MN, B_MN);
+      constexpr uint32_t idesc = idesc_bf16_f32(PAIR ? 256 : 128, BN, A_MN, B_MN);
       constexpr uint32_t lbo_a = A_MN ? 8192u : 16u;
       constexpr uint32_t lbo_b = B_MN ? 8192u : 16u;
       constexpr uint32_t kstep_a = A_MN ? 2048u : 32u;
       constexpr uint32_t kstep_b = B_MN ? 2048u : 32u;
+      auto mma = [&](uint32_t d, uint64_t ad, uint64_t bd, uint32_t acc_in) {
+        if (PAIR) mma_bf16_pair(d, ad, bd, idesc, acc_in);
+        else mma_bf16(d, ad, bd, idesc, acc_in);
+      };
+      auto commit = [&](uint64_t* bar) {
+        if (PAIR) mma_commit_pair(bar);
+        else mma_commit(bar);
+      };
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-        const Tile tl = decode_tile<SCHED>(args, t);
+      for (int t = first; t < total && ok; t += step, ++it) {
+        bool valid;
+        const Tile tl = tile_at(t, &valid);
         const int acc = it & 1;
         const uint32_t acc_par = static_cast<uint32_t>((it >> 1) & 1);
-        if (!mbar_wait(&tempty[acc], acc_par ^ 1u, vabort)) {
+        if (!wait(&tempty[acc], acc_par ^ 1u)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < tl.num_kb; ++kb) {
-          if (!mbar_wait(&full[stage], phase, vabort)) {
+          if (!wait(&full[stage], phase)) {
             ok = false;
             break;
           }
@@ -602,29 +842,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 4; ++j) {
             const uint64_t ad = smem_desc_sw128(a_base + j * kstep_a, lbo_a, 1024);
             const uint64_t bd = smem_desc_sw128(b_base + j * kstep_b, lbo_b, 1024);
-            mma_bf16(d_tmem, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
+            mma(d_tmem, ad, bd, (kb | j) != 0 ? 1u : 0u);
             if (SPLIT == SPLIT_A) {
               const uint64_t ad2 = smem_desc_sw128(a_base + C::A_BYTES + j * kstep_a, lbo_a, 1024);
-              mma_bf16(d_tmem, ad2, bd, idesc, 1u);
+              mma(d_tmem, ad2, bd, 1u);
             } else if (SPLIT == SPLIT_B) {
               const uint64_t bd2 = smem_desc_sw128(b_base + C::B_BYTES + j * kstep_b, lbo_b, 1024);
-              mma_bf16(d_tmem, ad, bd2, idesc, 1u);
+              mma(d_tmem, ad, bd2, 1u);
             }
           }
-          mma_commit(&empty[stage]);
+          commit(&empty[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit(&tfull[acc]);
+        commit(&tfull[acc]);
       }
       if (!ok) {
         *vabort = 1;
         set_status(args.status, MOK_ERR_DEVICE_TIMEOUT);
         const int zero = 0;
-        mma_commit(drain);
+        commit(drain);
         mbar_wait(drain, 0, &zero);
       }
     }
@@ -632,45 +872,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------------- epilogue --
     const int q = warp & 3;                // TMEM lane quarter this warp may read
     const int half = (warp - 2) >> 2;      // column half of the tile
-    uint8_t* stage_buf = staging + (warp - 2) * kStagingBytes;
+    uint8_t* stage_buf = staging + (warp - 2) * C::STAGING_PER_WARP;
+    const uint32_t tempty_leader = PAIR ? mapa_shared(smem_addr(tempty), 0) : 0u;
+    // SwiGLU backward with BF16 operands: g, u come by TMA (tmC maps them);
+    // `gu_chunks` counts the chunks this warp has requested
+    constexpr bool kGuTma = EPI == EPI_SWIGLU_BWD;
+    const bool gu_tma = kGuTma && !args.mx;
+    uint64_t* wbar = gu_bar + 2 * (warp - 2);
+    uint32_t gu_chunks = 0;
     int it = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-      const Tile tl = decode_tile<SCHED>(args, t);
+    for (int t = first; t < total; t += step, ++it) {
+      bool valid;
+      const Tile tl = tile_at(t, &valid);
       const int acc = it & 1;
       const uint32_t acc_par = static_cast<uint32_t>((it >> 1) & 1);
-      if (!mbar_wait(&tfull[acc], acc_par, vabort)) {
+      // the tile's first g, u chunk does not depend on the accumulator
+      if (gu_tma && valid)
+        gu_issue<BN>(args, tl, q, lane, half, 0, stage_buf, wbar, gu_chunks, &tmC);
+      if (!wait(&tfull[acc], acc_par)) {
         *vabort = 1;
         set_status(args.status, MOK_ERR_DEVICE_TIMEOUT);
         break;
       }
       tc_fence_after_sync();
-      if (EPI == EPI_SWIGLU_BWD) {
-        // the fp32 g, u rows of this thread's next tile (and, the first time,
-        // of this one) go to L2 while this tile's epilogue runs
-        for (int tp = (it == 0 ? t : t + (int)gridDim.x); tp <= t + (int)gridDim.x && tp < total;
-             tp += (int)gridDim.x) {
-          const Tile tn = decode_tile<SCHED>(args, tp);
-          const float* row = static_cast<const float*>(args.in_gu) +
-                             (long long)(tn.row0 + q * 32 + lane) * (2LL * args.I) +
-                             tn.n_tile * BN + half * (BN / 2);
-          prefetch_l2_bulk(row, BN / 2 * 4);
-          prefetch_l2_bulk(row + args.I, BN / 2 * 4);
-        }
-      }
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      epilogue_tile<BN, SCHED, EPI>(args, tl, taddr, q, lane, half, stage_buf, &tmC);
+      if (gu_tma) {
+        if (valid)
+          gu_chunks = swiglu_bwd_tma<BN>(args, tl, taddr, q, lane, half, stage_buf, wbar,
+                                         gu_chunks, &tmC, vabort);
+      } else if (valid) {
+        epilogue_tile<BN, SCHED, EPI>(args, tl, taddr, q, lane, half, stage_buf, &tmC);
+      }
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (lane == 0) {
+        if (PAIR) mbar_arrive_cluster(tempty_leader + 8u * acc);
+        else mbar_arrive(&tempty[acc]);
+      }
     }
     if (kTmaStore && lane == 0) bulk_wait_all<0>();  // stores complete before exit
+    // after a failed wait, g/u copies may still be landing in staging
+    if (kGuTma && *vabort) spin_ns(1000000ull);
   }
 
-  __syncthreads();
+  // the leader's MMAs read the other CTA's shared memory: neither CTA of a
+  // pair leaves (or frees TMEM) before both are done
+  tc_fence_before_sync();
+  if (PAIR) cluster_sync(); else __syncthreads();
   if (warp == 1) {
+    __syncwarp();
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if (PAIR) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
@@ -699,7 +953,8 @@ static EncodeTiledFn encode_fn() {
 // box {box_inner, box_rows}, 128-byte swizzle, zero fill out of bounds.
 static bool make_map_t(CUtensorMap* m, CUtensorMapDataType dt, int esz, const void* base,
                        uint64_t inner, uint64_t outer, uint64_t row_elems, uint32_t box_inner,
-                       uint32_t box_rows) {
+                       uint32_t box_rows,
+                       CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   if (outer == 0) outer = 1;  // empty operand: the map exists but is never read
@@ -708,7 +963,7 @@ static bool make_map_t(CUtensorMap* m, CUtensorMapDataType dt, int esz, const vo
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -725,20 +980,53 @@ static bool make_out_map(CUtensorMap* m, const void* base, uint64_t cols, uint64
   return make_map_t(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, cols, rows, cols, 32, 32);
 }
 
-template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, int SPLIT = SPLIT_NONE>
+// max_units: an upper bound on the tiles (PAIR: tile pairs) of the launch;
+// the kernel reads the exact count on the device.
+template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, int SPLIT = SPLIT_NONE,
+          bool PAIR = false>
 static cudaError_t launch(const char* name, const CUtensorMap& ta, const CUtensorMap& tb,
-                          const CUtensorMap& tc, const GemmArgs& args, int max_tiles,
+                          const CUtensorMap& tc, const GemmArgs& args, int max_units,
                           cudaStream_t st, const CUtensorMap* tl = nullptr) {
-  auto kern = gemm_kernel<BN, A_MN, B_MN, SCHED, EPI, SPLIT>;
-  constexpr int smem = Cfg<BN, SPLIT>::SMEM_BYTES;
+  auto kern = gemm_kernel<BN, A_MN, B_MN, SCHED, EPI, SPLIT, PAIR>;
+  constexpr int smem = Cfg<BN, SPLIT, PAIR, staging_bytes<EPI>()>::SMEM_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  if (max_tiles <= 0) return cudaSuccess;
-  int grid = num_sms_current_device();
-  if (max_tiles < grid) grid = max_tiles;
+  if (max_units <= 0) return cudaSuccess;
+  if (!PAIR) {
+    int grid = num_sms_current_device();
+    if (max_units < grid) grid = max_units;
+    ProfScope prof(name, st);
+    kern<<<grid, kThreads, smem, st>>>(ta, tb, tc, tl ? *tl : ta, args);
+    count_launch();
+    return cudaGetLastError();
+  }
+  // clusters of two CTAs, as many as can be resident at once (one per SM pair)
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(num_sms_current_device() / 2 * 2), 1, 1);
+  static int max_clusters = -1;  // per kernel instantiation and process (one device type)
+  if (max_clusters < 0) {
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    max_clusters = n;
+  }
+  if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+  int clusters = max_clusters < max_units ? max_clusters : max_units;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
   ProfScope prof(name, st);
-  kern<<<grid, kThreads, smem, st>>>(ta, tb, tc, tl ? *tl : ta, args);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tl ? *tl : ta, args);
   count_launch();
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -750,6 +1038,11 @@ static GemmArgs blank_args(int* status) {
 }
 
 static inline int max_mtiles(const Dims& D) { return static_cast<int>(D.rows_max / 128); }
+// bound on the tile pairs: sum over experts of ceil(tiles_e / 2)
+static inline int max_mpairs(const Dims& D) {
+  const int64_t segs = D.R < D.E ? D.R : D.E;
+  return static_cast<int>((D.rows_max / 128 + segs + 1) / 2);
+}
 
 cudaError_t gemm_fwd_gate_up(const Dims& D, const void* X_perm, const void* w_gate_up,
                              const int32_t* mtile_prefix, const int32_t* poff, void* GU, void* H,
@@ -774,6 +1067,9 @@ cudaError_t gemm_fwd_gate_up(const Dims& D, const void* X_perm, const void* w_ga
   a.out = GU;
   a.out2 = H;
   a.mx = D.mx ? 1 : 0;
+  if (D.pair)
+    return launch<256, false, false, SCHED_MGROUP, EPI_SWIGLU_FWD, SPLIT_NONE, true>(
+        "fwd_gate_up_swiglu", ta, tb, tc, a, max_mpairs(D) * a.n_tiles, st);
   return launch<256, false, false, SCHED_MGROUP, EPI_SWIGLU_FWD>(
       "fwd_gate_up_swiglu", ta, tb, tc, a, max_mtiles(D) * a.n_tiles, st);
 }
@@ -782,9 +1078,11 @@ cudaError_t gemm_fwd_down(const Dims& D, const void* H, const void* w_down,
                           const int32_t* mtile_prefix, const int32_t* poff, void* O, int* status,
                           cudaStream_t st) {
   const int bn = (D.d % 256 == 0) ? 256 : 128;
+  const bool pair = D.pair && bn == 256;
   CUtensorMap ta, tb, tc;
   if (!make_map(&ta, H, D.I, D.rows_max, D.I, 128)) return cudaErrorInvalidValue;
-  if (!make_map(&tb, w_down, D.I, D.E * D.d, D.I, bn)) return cudaErrorInvalidValue;
+  if (!make_map(&tb, w_down, D.I, D.E * D.d, D.I, pair ? bn / 2 : bn))
+    return cudaErrorInvalidValue;
   if (!make_out_map(&tc, O, D.d, D.rows_max)) return cudaErrorInvalidValue;
   GemmArgs a = blank_args(status);
   a.E = (int)D.E;
@@ -796,6 +1094,9 @@ cudaError_t gemm_fwd_down(const Dims& D, const void* H, const void* w_down,
   a.out = O;  // fp32 [rows_max, d]
   a.ldo = D.d;
   const int mt = max_mtiles(D) * a.n_tiles;
+  if (pair)
+    return launch<256, false, false, SCHED_MGROUP, EPI_F32, SPLIT_NONE, true>(
+        "fwd_down", ta, tb, tc, a, max_mpairs(D) * a.n_tiles, st);
   if (bn == 256)
     return launch<256, false, false, SCHED_MGROUP, EPI_F32>("fwd_down", ta, tb, tc, a, mt, st);
   return launch<128, false, false, SCHED_MGROUP, EPI_F32>("fwd_down", ta, tb, tc, a, mt, st);
@@ -807,8 +1108,12 @@ cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* 
                                 void* P_lo, void* dGU_mx, float* dp_part, int* status,
                                 cudaStream_t st) {
   const int bn = D.bn_dgrad;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tg;
   if (!make_map(&ta, dY_perm, D.d, D.rows_max, D.d, 128)) return cudaErrorInvalidValue;
+  // fp32 g, u rows for the epilogue: boxes of 32 rows x 16 columns, 64-byte swizzle
+  if (!make_map_t(&tg, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, GU, 2 * D.I, D.rows_max, 2 * D.I, 16,
+                  32, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
   // W_down_e viewed as [K = d rows, N = I columns]: N-major operand
   if (!make_map(&tb, w_down, D.I, D.E * D.d, D.I, 64)) return cudaErrorInvalidValue;
   GemmArgs a = blank_args(status);
@@ -830,11 +1135,14 @@ cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* 
   a.dp_part = dp_part;
   a.np = D.np;
   const int mt = max_mtiles(D) * a.n_tiles;
+  if (bn == 256 && D.pair)
+    return launch<256, false, true, SCHED_MGROUP, EPI_SWIGLU_BWD, SPLIT_NONE, true>(
+        "bwd_down_dgrad_swiglu", ta, tb, tg, a, max_mpairs(D) * a.n_tiles, st);
   if (bn == 256)
     return launch<256, false, true, SCHED_MGROUP, EPI_SWIGLU_BWD>("bwd_down_dgrad_swiglu", ta, tb,
-                                                                   ta, a, mt, st);
+                                                                   tg, a, mt, st);
   return launch<128, false, true, SCHED_MGROUP, EPI_SWIGLU_BWD>("bwd_down_dgrad_swiglu", ta, tb,
-                                                                 ta, a, mt, st);
+                                                                 tg, a, mt, st);
 }
 
 cudaError_t gemm_bwd_gate_up_dgrad(const Dims& D, const void* dGU, const void* w_gate_up,
@@ -856,6 +1164,9 @@ cudaError_t gemm_bwd_gate_up_dgrad(const Dims& D, const void* dGU, const void* w
   a.out = dX_perm;  // fp32 [rows_max, d]
   a.ldo = D.d;
   const int mt = max_mtiles(D) * a.n_tiles;
+  if (bn == 256 && D.pair)
+    return launch<256, false, true, SCHED_MGROUP, EPI_F32, SPLIT_NONE, true>(
+        "bwd_gate_up_dgrad", ta, tb, tc, a, max_mpairs(D) * a.n_tiles, st);
   if (bn == 256)
     return launch<256, false, true, SCHED_MGROUP, EPI_F32>("bwd_gate_up_dgrad", ta, tb, tc, a, mt,
                                                            st);
@@ -907,6 +1218,9 @@ static cudaError_t wgrad(const Dims& D, const char* name, const void* A_rows, in
   if (!lo_is_a)
     return launch<128, true, true, SCHED_KGROUP, EPI_F32, SPLIT_B>(name, ta, tb, tc, a, mt, st,
                                                                    &tl);
+  if (bn == 256 && D.pair && a.m_tiles % 2 == 0)
+    return launch<256, true, true, SCHED_KGROUP, EPI_F32, SPLIT_A, true>(name, ta, tb, tc, a,
+                                                                         mt / 2, st, &tl);
   if (bn == 256)
     return launch<256, true, true, SCHED_KGROUP, EPI_F32, SPLIT_A>(name, ta, tb, tc, a, mt, st,
                                                                    &tl);
@@ -937,8 +1251,12 @@ cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* P_hi
   a.out = dw_down;
   a.ldo = D.d;  // rows of one expert's block in the [E*d, I] view
   a.accumulate = accumulate ? 1 : 0;
-  return launch<256, true, true, SCHED_KGROUP, EPI_F32_T, SPLIT_A>(
-      "bwd_down_wgrad", ta, tb, tc, a, a.E * a.m_tiles * a.n_tiles, st, &tl);
+  const int mt = a.E * a.m_tiles * a.n_tiles;
+  if (D.pair && a.m_tiles % 2 == 0)
+    return launch<256, true, true, SCHED_KGROUP, EPI_F32_T, SPLIT_A, true>(
+        "bwd_down_wgrad", ta, tb, tc, a, mt / 2, st, &tl);
+  return launch<256, true, true, SCHED_KGROUP, EPI_F32_T, SPLIT_A>("bwd_down_wgrad", ta, tb, tc,
+                                                                   a, mt, st, &tl);
 }
 
 cudaError_t gemm_wgrad_gate_up(const Dims& D, const void* dGU_hi, const void* dGU_lo,

@@ -94,7 +94,7 @@ mok_status make_dims(const mok_moe_desc* desc, Dims* out) {
   if (d.dtype != MOK_BF16 && d.dtype != MOK_MXFP8) return MOK_ERR_UNSUPPORTED;
   if (d.mb_tokens < 0 || d.ring_slots < 0) return MOK_ERR_INVALID_ARG;
   if (d.flags & ~(MOK_FLAG_BF16_ACT_OUT | MOK_FLAG_BF16_WGRAD_OUT | MOK_FLAG_ACCUMULATE_WGRAD |
-                  MOK_FLAG_RECOMPUTE_GATE_UP))
+                  MOK_FLAG_RECOMPUTE_GATE_UP | MOK_FLAG_SINGLE_CTA_GEMM))
     return MOK_ERR_UNSUPPORTED;
   if ((d.flags & MOK_FLAG_ACCUMULATE_WGRAD) && (d.flags & MOK_FLAG_BF16_WGRAD_OUT))
     return MOK_ERR_UNSUPPORTED;  // accumulation is fp32 only
@@ -133,6 +133,7 @@ mok_status make_dims(const mok_moe_desc* desc, Dims* out) {
   D.mx = d.dtype == MOK_MXFP8;
   D.accumulate = (d.flags & MOK_FLAG_ACCUMULATE_WGRAD) != 0;
   D.recompute_gu = (d.flags & MOK_FLAG_RECOMPUTE_GATE_UP) != 0;
+  D.pair = (d.flags & MOK_FLAG_SINGLE_CTA_GEMM) == 0;
   // every row index and element offset used in 32-bit arithmetic must fit
   if (D.rows_max * 2 * D.I >= (1LL << 40)) return MOK_ERR_UNSUPPORTED;
   if (D.rows_max >= (1LL << 31) / 2) return MOK_ERR_UNSUPPORTED;
@@ -163,7 +164,7 @@ void block_layout(const Dims& D, BlockL* B) {
   B->pos = b.take(Tk * 4);
   B->token_of_row = b.take(Tk * 4);
   B->padded_offsets = b.take((E + 1) * 4);
-  B->mtile_prefix = b.take((E + 1) * 4);
+  B->mtile_prefix = b.take((E + 1) * 8);  // tiles, then tile pairs
   B->padded_pos = b.take(Tk * 4);
   B->padded_token = b.take(rows * 4);
   B->row_weight = b.take(rows * 4);
@@ -256,7 +257,7 @@ void stage_layout(const Dims& D, StageWs* W) {
   W->block_counts = take(static_cast<size_t>(D.nb) * D.E * 4);
   W->block_base = take(static_cast<size_t>(D.nb) * D.E * 4);
   W->padded_offsets = take((D.E + 1) * 4);
-  W->mtile_prefix = take((D.E + 1) * 4);
+  W->mtile_prefix = take((D.E + 1) * 8);
   W->ppos = take(static_cast<size_t>(D.T) * D.k * 4);
   W->ptok = take(rows * 4);
   W->row_w = 0;

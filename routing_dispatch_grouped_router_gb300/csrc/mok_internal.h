@@ -34,6 +34,7 @@ struct Dims {
   bool mx;           // MXFP8 expert GEMM operands
   bool accumulate;   // backward adds into the weight gradients
   bool recompute_gu; // g, u not kept: the backward recomputes them
+  bool pair;         // grouped GEMMs with 256-row tiles on CTA pairs (2-SM MMA)
 };
 
 // Offsets inside one micro-batch's block of `saved` (relative to the block).
@@ -78,7 +79,7 @@ struct PlanOut {
   int32_t* pos;             // [T,k] (may be null)
   int32_t* token_of_row;    // [R] (may be null)
   int32_t* padded_offsets;  // [E+1]
-  int32_t* mtile_prefix;    // [E+1]
+  int32_t* mtile_prefix;    // [2(E+1)]: prefix of 128-row tiles, then of tile pairs
   int32_t* ppos;            // [T,k]
   int32_t* ptok;            // [rows_max]
   float* row_w;             // [rows_max] (may be null)

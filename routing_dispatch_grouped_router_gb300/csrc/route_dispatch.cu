@@ -155,6 +155,7 @@ __global__ void plan_scan_kernel(const int32_t* __restrict__ block_counts, int n
   __shared__ int s_cnt[kMaxExperts];
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_poff[kMaxExperts + 1];
+  __shared__ int s_pair[kMaxExperts + 1];
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = 0;
     for (int b = 0; b < nb; ++b) {
@@ -169,37 +170,45 @@ __global__ void plan_scan_kernel(const int32_t* __restrict__ block_counts, int n
     // warp scan: lane owns experts [lane*PER, lane*PER+PER)
     const int lane = threadIdx.x;
     constexpr int PER = kMaxExperts / 32;
-    int sum = 0, psum = 0;
+    // row tiles of an expert, and pairs of row tiles (an odd count rounds up)
+    auto tiles = [](int c) { return (c + kRowPad - 1) / kRowPad; };
+    int sum = 0, psum = 0, qsum = 0;
     for (int j = 0; j < PER; ++j) {
       const int e = lane * PER + j;
       if (e < E) {
         sum += s_cnt[e];
-        psum += (s_cnt[e] + kRowPad - 1) / kRowPad * kRowPad;
+        psum += tiles(s_cnt[e]) * kRowPad;
+        qsum += (tiles(s_cnt[e]) + 1) / 2;
       }
     }
-    int incl = sum, pincl = psum;
+    int incl = sum, pincl = psum, qincl = qsum;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int a = __shfl_up_sync(0xffffffffu, incl, off);
       const int b = __shfl_up_sync(0xffffffffu, pincl, off);
+      const int c = __shfl_up_sync(0xffffffffu, qincl, off);
       if (lane >= off) {
         incl += a;
         pincl += b;
+        qincl += c;
       }
     }
-    int run = incl - sum, prun = pincl - psum;
+    int run = incl - sum, prun = pincl - psum, qrun = qincl - qsum;
     for (int j = 0; j < PER; ++j) {
       const int e = lane * PER + j;
       if (e < E) {
         s_off[e] = run;
         s_poff[e] = prun;
+        s_pair[e] = qrun;
         run += s_cnt[e];
-        prun += (s_cnt[e] + kRowPad - 1) / kRowPad * kRowPad;
+        prun += tiles(s_cnt[e]) * kRowPad;
+        qrun += (tiles(s_cnt[e]) + 1) / 2;
       }
     }
     if (lane == 31) {
       s_off[E] = run;
       s_poff[E] = prun;
+      s_pair[E] = qrun;
     }
   }
   __syncthreads();
@@ -207,6 +216,7 @@ __global__ void plan_scan_kernel(const int32_t* __restrict__ block_counts, int n
     offsets[e] = s_off[e];
     poff[e] = s_poff[e];
     mtile_prefix[e] = s_poff[e] / kRowPad;
+    mtile_prefix[E + 1 + e] = s_pair[e];  // prefix of tile pairs
   }
   // padding rows of each expert segment
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;

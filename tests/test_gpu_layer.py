@@ -136,6 +136,28 @@ def test_bf16_output_flags_round_the_fp32_outputs():
         assert torch.equal(a[n].to(torch.bfloat16).view(torch.int16), b[n].view(torch.int16)), n
 
 
+@pytest.mark.parametrize("shape,dtype,mb", [
+    # one 128-row tile per expert: every pair's odd CTA stages rows it never stores
+    (gen.Shape(T=256, d=256, E=4, I=256, k=2), 0, 0),
+    # 2-3 tiles per expert (odd and even counts), wider N and K
+    (gen.Shape(T=1024, d=512, E=16, I=512, k=4), 0, 0),
+    (gen.Shape(T=1024, d=512, E=16, I=512, k=4), 1, 256),
+])
+def test_pair_and_single_cta_engines_agree_bitwise(shape, dtype, mb):
+    """256-row tiles on CTA pairs (tcgen05.mma.cta_group::2) and 128-row
+    tiles on single CTAs accumulate every element over the same K sequence."""
+    inp = gen.make_inputs(shape, seed=6)
+    outs = []
+    for flags in (0, api.FLAG_SINGLE_CTA_GEMM):
+        g = _gpu.run_gpu(shape, inp, flags=flags, dtype=dtype, mb_tokens=mb,
+                         ring_slots=2 if mb else 0)
+        assert g["status"] == 0
+        outs.append([g[n].view(torch.int32).cpu().numpy() for n in
+                     ("y", "dx", "dw_router", "dw_gate_up", "dw_down")])
+    for n, a, b in zip(("y", "dx", "dw_router", "dw_gate_up", "dw_down"), *outs):
+        assert np.array_equal(a, b), n
+
+
 @pytest.mark.parametrize("dtype,mb,ring", [(0, 0, 0), (0, 256, 1), (1, 256, 2)])
 def test_recompute_gate_up_is_bitwise_identical(dtype, mb, ring):
     """The backward's recomputed g, u equal the ones the forward would have
