@@ -56,6 +56,19 @@ def gemm_flops(shape: gen.Shape) -> dict:
     }
 
 
+# Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# grouped GEMMs on the fine workload, from the ncu capture summarised in
+# profiles/grouped_gemms_fine.txt (kernels as of the commit named there).
+NCU_TRAFFIC_FINE = {
+    "fwd_gate_up_swiglu": 707.647232e6 + 335.297e6,
+    "fwd_down": 343.551744e6 + 255.242e6,
+    "bwd_down_dgrad_swiglu": 805.615616e6 + 398.565e6,
+    "bwd_down_wgrad": 300.024832e6 + 478.920e6,
+    "bwd_gate_up_dgrad": 694.450432e6 + 271.880e6,
+    "bwd_gate_up_wgrad": 450.134016e6 + 1014.016e6,
+}
+
+
 def mover_bytes(shape: gen.Shape) -> dict:
     """Bytes each data-movement kernel must move in the layer's layout: bf16
     token rows, fp32 expert-output and dX rows, fp32 y and dx (the default)."""
@@ -392,7 +405,9 @@ def main():
     if dom in flops:
         ach = flops[dom] / avg_s / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peaks["bf16_sustained"],
-                "unit": "TFLOP/s", "frac": ach / peaks["bf16_sustained"], "traffic": None,
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_sustained"],
+                "traffic": NCU_TRAFFIC_FINE.get(dom) if WORKLOAD == "fine" else None,
+                "traffic_source": "profiles/grouped_gemms_fine.txt",
                 "peak_source": f"bf16_tflops_sustained of {peaks['source']}",
                 "algorithmic_per_launch": flops[dom]}
     else:
