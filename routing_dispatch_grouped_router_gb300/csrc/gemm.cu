@@ -78,11 +78,19 @@ struct GemmArgs {
   int mx;                   // SwiGLU epilogues: quantise the derived GEMM operands to MXFP8
   int accumulate;           // fp32 TMA-store epilogue: add into C instead of overwriting
   int store_c;              // SWIGLU_FWD: write g, u through the C map
+  int evict_first;          // TMA-store epilogues: C is not read again soon (L2 evict-first)
+  int k_splits;             // DENSE: K split into this many partial products (0 or 1: none)
   const void* in_gu;        // SWIGLU_BWD: saved fp32 pre-activations [rows,2I]
   const float* row_w;       // SWIGLU_BWD: routing weight of each row
   float* dp_part;           // SWIGLU_BWD: [rows, np] partial <dA,h>
   int np;
   int* status;
+};
+
+// Extra output maps: the SwiGLU backward stores dG/dU (hi, lo) and p*h (hi,
+// lo) through TMA, boxes of 32 rows x 16 bf16 columns.
+struct OutMaps {
+  CUtensorMap dgu_hi, dgu_lo, p_hi, p_lo;
 };
 
 constexpr int kThreads = 320;
@@ -93,10 +101,13 @@ constexpr int kStagingBytes = 4096;  // per epilogue warp: 32 rows x 128 bytes
 // tcgen05.mma.cta_group::2; each CTA stages its own 128 rows of A and BN/2
 // rows of B, and holds its 128 x BN accumulator in its own TMEM.
 // Staging bytes per epilogue warp: 4 KB (TMA-store blocks); the SwiGLU
-// backward double-buffers its fp32 g, u operands (2 x 4 KB).
+// backward double-buffers its fp32 g, u operands (2 x 4 KB) and stages the
+// six bf16 output blocks of a chunk (6 x 1 KB).
+constexpr int kGuStageBytes = 8192;
+constexpr int kSwigluBwdStaging = kGuStageBytes + 6 * 1024;
 template <int EPI>
 constexpr int staging_bytes() {
-  return EPI == EPI_SWIGLU_BWD ? 8192 : kStagingBytes;
+  return EPI == EPI_SWIGLU_BWD ? kSwigluBwdStaging : kStagingBytes;
 }
 
 template <int BN, int SPLIT = SPLIT_NONE, bool PAIR = false, int STG = kStagingBytes>
@@ -126,9 +137,10 @@ static_assert(Cfg<256, SPLIT_NONE, true>::SMEM_BYTES <= 232448 &&
                   Cfg<256, SPLIT_NONE, true>::STAGES == 6, "smem");
 static_assert(Cfg<256, SPLIT_A, true>::SMEM_BYTES <= 232448 &&
                   Cfg<256, SPLIT_A, true>::STAGES >= 4, "smem");
-static_assert(Cfg<256, SPLIT_NONE, true, 8192>::SMEM_BYTES <= 232448 &&
-                  Cfg<256, SPLIT_NONE, true, 8192>::STAGES == 5, "smem");
-static_assert(Cfg<256, SPLIT_NONE, false, 8192>::STAGES >= 3, "smem");
+static_assert(Cfg<256, SPLIT_NONE, true, kSwigluBwdStaging>::SMEM_BYTES <= 232448 &&
+                  Cfg<256, SPLIT_NONE, true, kSwigluBwdStaging>::STAGES == 3, "smem");
+static_assert(Cfg<256, SPLIT_NONE, false, kSwigluBwdStaging>::STAGES >= 2 &&
+                  Cfg<128, SPLIT_NONE, false, kSwigluBwdStaging>::STAGES >= 3, "smem");
 // stage counts of the other configurations are unchanged by the 512-byte barrier block
 static_assert(Cfg<256>::STAGES == 4 && Cfg<128>::STAGES == 6 && Cfg<256, SPLIT_A>::STAGES == 3 &&
                   Cfg<128, SPLIT_B>::STAGES == 4 && Cfg<256, SPLIT_NONE, true>::STAGES == 6 &&
@@ -140,13 +152,14 @@ struct Tile {
   int row0;    // MGROUP/DENSE: first row of A and C; KGROUP: first row of C_e
   int k_row0;  // KGROUP: first K row (padded offset of the expert)
   int num_kb;
+  int kb0;     // DENSE with split K: first K block of this split (e = the split)
 };
 
 template <int SCHED>
 __device__ __forceinline__ int total_tiles(const GemmArgs& a) {
   if (SCHED == SCHED_MGROUP) return __ldg(a.mtile_prefix + a.E) * a.n_tiles;
   if (SCHED == SCHED_KGROUP) return a.E * a.m_tiles * a.n_tiles;
-  return a.m_tiles * a.n_tiles;
+  return a.m_tiles * a.n_tiles * (a.k_splits > 1 ? a.k_splits : 1);
 }
 
 // Tiles of 256 rows for CTA pairs: MGROUP pairs the 128-row tiles of one
@@ -184,6 +197,7 @@ __device__ __forceinline__ Tile decode_pair(const GemmArgs& a, int t, int rank, 
     tl.row0 = __ldg(a.poff + e) + m * 128;
     tl.k_row0 = 0;
     tl.num_kb = a.num_kb;
+    tl.kb0 = 0;
   } else {
     const int mp = a.m_tiles / 2;
     const int tpe = mp * a.n_tiles;
@@ -196,6 +210,7 @@ __device__ __forceinline__ Tile decode_pair(const GemmArgs& a, int t, int rank, 
     const int k0 = __ldg(a.poff + e), k1 = __ldg(a.poff + e + 1);
     tl.k_row0 = k0;
     tl.num_kb = (k1 - k0) / 64;
+    tl.kb0 = 0;
     *valid = true;
   }
   return tl;
@@ -222,6 +237,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, int t) {
     tl.row0 = __ldg(a.poff + e) + tl.m_tile * 128;
     tl.k_row0 = 0;
     tl.num_kb = a.num_kb;
+    tl.kb0 = 0;
   } else if (SCHED == SCHED_KGROUP) {
     const int tpe = a.m_tiles * a.n_tiles;
     const int e = t / tpe;
@@ -233,13 +249,19 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, int t) {
     const int k0 = __ldg(a.poff + e), k1 = __ldg(a.poff + e + 1);
     tl.k_row0 = k0;
     tl.num_kb = (k1 - k0) / 64;
+    tl.kb0 = 0;
   } else {
-    tl.e = 0;
-    tl.n_tile = t / a.m_tiles;
-    tl.m_tile = t - tl.n_tile * a.m_tiles;
+    // DENSE: split-K partial products go to separate C blocks (e = split)
+    const int mn = a.m_tiles * a.n_tiles;
+    const int split = t / mn;
+    const int tt = t - split * mn;
+    tl.e = split;
+    tl.n_tile = tt / a.m_tiles;
+    tl.m_tile = tt - tl.n_tile * a.m_tiles;
     tl.row0 = tl.m_tile * 128;
     tl.k_row0 = 0;
     tl.num_kb = a.num_kb;
+    tl.kb0 = split * a.num_kb;
   }
   return tl;
 }
@@ -332,9 +354,24 @@ __device__ __forceinline__ void store_hi_lo32(__nv_bfloat16* hi, __nv_bfloat16* 
 // One warp writes its 32 rows x 32 fp32 columns to the 4 KB staging buffer in
 // the 128-byte swizzled layout (16-byte chunk j of row r at chunk j ^ (r%8)),
 // then lane 0 stores it with one TMA tensor store at (x, y).
+// Lane 0: the TMA store (or reduce-add) of one staged block, with an
+// evict-first L2 policy for output that is not read again soon.
+__device__ __forceinline__ void tma_out_2d(const CUtensorMap* tmC, const void* buf, int x, int y,
+                                           bool add, bool evict_first) {
+  if (evict_first) {
+    const uint64_t pol = l2_policy_evict_first();
+    if (add) tma_reduce_add_2d_hint(tmC, buf, x, y, pol);
+    else tma_store_2d_hint(tmC, buf, x, y, pol);
+  } else {
+    if (add) tma_reduce_add_2d(tmC, buf, x, y);
+    else tma_store_2d(tmC, buf, x, y);
+  }
+  bulk_commit();
+}
+
 __device__ __forceinline__ void stage_and_store_f32(uint8_t* buf, const CUtensorMap* tmC,
                                                     const float (&v)[32], int lane, int x, int y,
-                                                    bool add = false) {
+                                                    bool add = false, bool evict_first = false) {
   if (lane == 0) bulk_wait_read<0>();  // the previous store has read the buffer
   __syncwarp();
   uint8_t* row = buf + lane * 128;
@@ -346,11 +383,7 @@ __device__ __forceinline__ void stage_and_store_f32(uint8_t* buf, const CUtensor
   }
   fence_proxy_async_smem();
   __syncwarp();
-  if (lane == 0) {
-    if (add) tma_reduce_add_2d(tmC, buf, x, y);
-    else tma_store_2d(tmC, buf, x, y);
-    bulk_commit();
-  }
+  if (lane == 0) tma_out_2d(tmC, buf, x, y, add, evict_first);
 }
 
 // As stage_and_store_f32, but the warp's 32 x 32 block is stored transposed:
@@ -359,7 +392,7 @@ __device__ __forceinline__ void stage_and_store_f32(uint8_t* buf, const CUtensor
 // at (x, y) writes element (i, j) to output row y + j, column x + i.
 __device__ __forceinline__ void stage_and_store_f32_t(uint8_t* buf, const CUtensorMap* tmC,
                                                       const float (&v)[32], int lane, int x,
-                                                      int y, bool add) {
+                                                      int y, bool add, bool evict_first) {
   if (lane == 0) bulk_wait_read<0>();
   __syncwarp();
   const int chunk = lane >> 2, word = (lane & 3) * 4;
@@ -368,11 +401,7 @@ __device__ __forceinline__ void stage_and_store_f32_t(uint8_t* buf, const CUtens
     *reinterpret_cast<float*>(buf + j * 128 + ((chunk ^ (j & 7)) << 4) + word) = v[j];
   fence_proxy_async_smem();
   __syncwarp();
-  if (lane == 0) {
-    if (add) tma_reduce_add_2d(tmC, buf, x, y);
-    else tma_store_2d(tmC, buf, x, y);
-    bulk_commit();
-  }
+  if (lane == 0) tma_out_2d(tmC, buf, x, y, add, evict_first);
 }
 
 template <int BN, int SCHED, int EPI>
@@ -395,7 +424,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = 0.f;
       }
-      stage_and_store_f32(stage_buf, tmC, v, lane, col0 + c, y, a.accumulate != 0);
+      stage_and_store_f32(stage_buf, tmC, v, lane, col0 + c, y, a.accumulate != 0,
+                          a.evict_first != 0);
     }
   } else if (EPI == EPI_F32_T) {
     // C^T through TMA: accumulator rows are output columns; C viewed as
@@ -412,13 +442,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
         for (int j = 0; j < 32; ++j) v[j] = 0.f;
       }
       stage_and_store_f32_t(stage_buf, tmC, v, lane, x, tl.e * a.ldo + col0 + c,
-                            a.accumulate != 0);
+                            a.accumulate != 0, a.evict_first != 0);
     }
   } else if (EPI == EPI_BF16 || EPI == EPI_F32) {
     constexpr int esz = EPI == EPI_F32 ? 4 : 2;
     const long long grow = tl.row0 + row_in_tile;
     char* base = static_cast<char*>(a.out);
-    if (SCHED == SCHED_KGROUP) base += (long long)tl.e * a.out_group_stride * esz;
+    if (SCHED != SCHED_MGROUP) base += (long long)tl.e * a.out_group_stride * esz;
     const bool row_ok = (SCHED != SCHED_DENSE) || grow < a.m_valid;
     const int col0 = tl.n_tile * BN + half * HALF_COLS;
 #pragma unroll 1
@@ -470,8 +500,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
         store_bf16x32(h + n0 + c, hv);
       }
       if (a.store_c) {
-        stage_and_store_f32(stage_buf, tmC, g, lane, n0 + c, y);
-        stage_and_store_f32(stage_buf, tmC, u, lane, I + n0 + c, y);
+        stage_and_store_f32(stage_buf, tmC, g, lane, n0 + c, y, false, a.evict_first != 0);
+        stage_and_store_f32(stage_buf, tmC, u, lane, I + n0 + c, y, false, a.evict_first != 0);
       }
     }
   } else if (EPI == EPI_SWIGLU_BWD) {
@@ -572,15 +602,15 @@ __device__ __forceinline__ uint32_t swiglu_bwd_tma(const GemmArgs& a, const Tile
                                                    uint32_t taddr, int q, int lane, int half,
                                                    uint8_t* stage_buf, uint64_t* wbar,
                                                    uint32_t count, const CUtensorMap* tmG,
-                                                   volatile int* vabort) {
+                                                   const OutMaps* om, volatile int* vabort) {
   constexpr int HALF_COLS = BN / 2;
   const long long r = tl.row0 + q * 32 + lane;
   const int I = a.I;
   const int n0 = tl.n_tile * BN + half * HALF_COLS;
-  __nv_bfloat16* dgu_hi = static_cast<__nv_bfloat16*>(a.out) + r * (2LL * I);
-  __nv_bfloat16* dgu_lo = static_cast<__nv_bfloat16*>(a.out3) + r * (2LL * I);
-  __nv_bfloat16* p_hi = static_cast<__nv_bfloat16*>(a.out2) + r * (long long)I;
-  __nv_bfloat16* p_lo = static_cast<__nv_bfloat16*>(a.out4) + r * (long long)I;
+  const int y = tl.row0 + q * 32;
+  // output blocks of a chunk, 32 rows x 32 bytes each: dG hi, dG lo, dU hi,
+  // dU lo, P hi, P lo
+  uint8_t* ostage = stage_buf + kGuStageBytes;
   const float p = a.row_w[r];
   float dp = 0.f;
   const int sw = (lane >> 1) & 3;
@@ -620,9 +650,26 @@ __device__ __forceinline__ uint32_t swiglu_bwd_tma(const GemmArgs& a, const Tile
       dA[j] = dh * sl;
       u[j] = p * sl * uu;
     }
-    store_hi_lo16(dgu_hi + n0 + c, dgu_lo + n0 + c, t);
-    store_hi_lo16(dgu_hi + I + n0 + c, dgu_lo + I + n0 + c, dA);
-    store_hi_lo16(p_hi + n0 + c, p_lo + n0 + c, u);
+    if (lane == 0) bulk_wait_read<0>();  // the previous chunk's stores have read staging
+    __syncwarp();
+    uint8_t* row = ostage + lane * 32;
+    store_hi_lo16(reinterpret_cast<__nv_bfloat16*>(row), reinterpret_cast<__nv_bfloat16*>(row + 1024),
+                  t);
+    store_hi_lo16(reinterpret_cast<__nv_bfloat16*>(row + 2048),
+                  reinterpret_cast<__nv_bfloat16*>(row + 3072), dA);
+    store_hi_lo16(reinterpret_cast<__nv_bfloat16*>(row + 4096),
+                  reinterpret_cast<__nv_bfloat16*>(row + 5120), u);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(&om->dgu_hi, ostage, n0 + c, y);
+      tma_store_2d(&om->dgu_lo, ostage + 1024, n0 + c, y);
+      tma_store_2d(&om->dgu_hi, ostage + 2048, I + n0 + c, y);
+      tma_store_2d(&om->dgu_lo, ostage + 3072, I + n0 + c, y);
+      tma_store_2d(&om->p_hi, ostage + 4096, n0 + c, y);
+      tma_store_2d(&om->p_lo, ostage + 5120, n0 + c, y);
+      bulk_commit();
+    }
   }
   __syncwarp();
   a.dp_part[r * a.np + tl.n_tile * 2 + half] = dp;
@@ -635,7 +682,7 @@ template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, int SPLIT, bool PAIR
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmL,
-                const __grid_constant__ GemmArgs args) {
+                const __grid_constant__ GemmArgs args, const __grid_constant__ OutMaps om) {
   using C = Cfg<BN, SPLIT, PAIR, staging_bytes<EPI>()>;
   static_assert(!PAIR || (SCHED != SCHED_DENSE && SPLIT != SPLIT_B && BN == 256), "pair");
   extern __shared__ uint8_t smem_raw[];
@@ -652,8 +699,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   // SwiGLU backward: two g/u staging buffers per epilogue warp, one barrier each
   uint64_t* gu_bar = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF + 256);
-  constexpr bool kTmaStore =
-      (EPI == EPI_F32 && SCHED != SCHED_DENSE) || EPI == EPI_SWIGLU_FWD || EPI == EPI_F32_T;
+  constexpr bool kTmaStore = (EPI == EPI_F32 && SCHED != SCHED_DENSE) || EPI == EPI_SWIGLU_FWD ||
+                             EPI == EPI_F32_T || EPI == EPI_SWIGLU_BWD;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -682,7 +729,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 32) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (kTmaStore || EPI == EPI_SWIGLU_BWD) tma_prefetch_desc(&tmC);
+    if (kTmaStore) tma_prefetch_desc(&tmC);
+    if (EPI == EPI_SWIGLU_BWD && !args.mx) {
+      tma_prefetch_desc(&om.dgu_hi);
+      tma_prefetch_desc(&om.dgu_lo);
+      tma_prefetch_desc(&om.p_hi);
+      tma_prefetch_desc(&om.p_lo);
+    }
     if (SPLIT != SPLIT_NONE) tma_prefetch_desc(&tmL);
   }
   if (warp == 1) {
@@ -742,9 +795,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           else if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
           // A tile: 128 rows (M) x 64 (K)  (+ its lo tile with SPLIT_A)
           if (!A_MN) {
-            load(sA, &tmA, kb * 64, tl.row0);
+            load(sA, &tmA, (tl.kb0 + kb) * 64, tl.row0);
           } else {
-            const int ky = tl.k_row0 + kb * 64;
+            const int ky = tl.k_row0 + (tl.kb0 + kb) * 64;
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
               load(sA + j * 8192, &tmA, tl.row0 + 64 * j, ky);
@@ -763,12 +816,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 load(sB + 16384, &tmB, kb * 64, r0 + args.I);
               }
             } else {
-              const int r0 = tl.e * args.b_group_rows + tl.n_tile * BN + rank * C::B_ROWS;
-              load(sB, &tmB, kb * 64, r0);
+              const int r0 = (SCHED == SCHED_DENSE ? 0 : tl.e * args.b_group_rows) +
+                             tl.n_tile * BN + rank * C::B_ROWS;
+              load(sB, &tmB, (tl.kb0 + kb) * 64, r0);
             }
           } else {
             int ky;
             if (SCHED == SCHED_KGROUP) ky = tl.k_row0 + kb * 64;
+            else if (SCHED == SCHED_DENSE) ky = (tl.kb0 + kb) * 64;
             else ky = tl.e * args.b_group_rows + kb * 64;
             const int x0 = tl.n_tile * BN + rank * C::B_ROWS;
 #pragma unroll
@@ -900,7 +955,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (gu_tma) {
         if (valid)
           gu_chunks = swiglu_bwd_tma<BN>(args, tl, taddr, q, lane, half, stage_buf, wbar,
-                                         gu_chunks, &tmC, vabort);
+                                         gu_chunks, &tmC, &om, vabort);
       } else if (valid) {
         epilogue_tile<BN, SCHED, EPI>(args, tl, taddr, q, lane, half, stage_buf, &tmC);
       }
@@ -986,7 +1041,11 @@ template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, int SPLIT = SPLIT_NO
           bool PAIR = false>
 static cudaError_t launch(const char* name, const CUtensorMap& ta, const CUtensorMap& tb,
                           const CUtensorMap& tc, const GemmArgs& args, int max_units,
-                          cudaStream_t st, const CUtensorMap* tl = nullptr) {
+                          cudaStream_t st, const CUtensorMap* tl = nullptr,
+                          const OutMaps* om = nullptr) {
+  OutMaps om_v;
+  if (om) om_v = *om;
+  else memset(&om_v, 0, sizeof(om_v));
   auto kern = gemm_kernel<BN, A_MN, B_MN, SCHED, EPI, SPLIT, PAIR>;
   constexpr int smem = Cfg<BN, SPLIT, PAIR, staging_bytes<EPI>()>::SMEM_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -996,7 +1055,7 @@ static cudaError_t launch(const char* name, const CUtensorMap& ta, const CUtenso
     int grid = num_sms_current_device();
     if (max_units < grid) grid = max_units;
     ProfScope prof(name, st);
-    kern<<<grid, kThreads, smem, st>>>(ta, tb, tc, tl ? *tl : ta, args);
+    kern<<<grid, kThreads, smem, st>>>(ta, tb, tc, tl ? *tl : ta, args, om_v);
     count_launch();
     return cudaGetLastError();
   }
@@ -1024,7 +1083,7 @@ static cudaError_t launch(const char* name, const CUtensorMap& ta, const CUtenso
   int clusters = max_clusters < max_units ? max_clusters : max_units;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
   ProfScope prof(name, st);
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tl ? *tl : ta, args);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tl ? *tl : ta, args, om_v);
   count_launch();
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -1057,6 +1116,7 @@ cudaError_t gemm_fwd_gate_up(const Dims& D, const void* X_perm, const void* w_ga
   if (!GU && !H) return cudaErrorInvalidValue;
   GemmArgs a = blank_args(status);
   a.store_c = GU ? 1 : 0;
+  a.evict_first = 1;  // g, u are read again only by the backward
   a.E = (int)D.E;
   a.n_tiles = (int)(D.I / 128);
   a.num_kb = (int)(D.d / 64);
@@ -1114,6 +1174,15 @@ cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* 
   if (!make_map_t(&tg, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, GU, 2 * D.I, D.rows_max, 2 * D.I, 16,
                   32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
+  // bf16 outputs: boxes of 32 rows x 16 columns, unswizzled
+  OutMaps om;
+  const auto bf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto none = CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (!make_map_t(&om.dgu_hi, bf16, 2, dGU_hi, 2 * D.I, D.rows_max, 2 * D.I, 16, 32, none) ||
+      !make_map_t(&om.dgu_lo, bf16, 2, dGU_lo, 2 * D.I, D.rows_max, 2 * D.I, 16, 32, none) ||
+      !make_map_t(&om.p_hi, bf16, 2, P_hi, D.I, D.rows_max, D.I, 16, 32, none) ||
+      !make_map_t(&om.p_lo, bf16, 2, P_lo, D.I, D.rows_max, D.I, 16, 32, none))
+    return cudaErrorInvalidValue;
   // W_down_e viewed as [K = d rows, N = I columns]: N-major operand
   if (!make_map(&tb, w_down, D.I, D.E * D.d, D.I, 64)) return cudaErrorInvalidValue;
   GemmArgs a = blank_args(status);
@@ -1137,12 +1206,12 @@ cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* 
   const int mt = max_mtiles(D) * a.n_tiles;
   if (bn == 256 && D.pair)
     return launch<256, false, true, SCHED_MGROUP, EPI_SWIGLU_BWD, SPLIT_NONE, true>(
-        "bwd_down_dgrad_swiglu", ta, tb, tg, a, max_mpairs(D) * a.n_tiles, st);
+        "bwd_down_dgrad_swiglu", ta, tb, tg, a, max_mpairs(D) * a.n_tiles, st, nullptr, &om);
   if (bn == 256)
     return launch<256, false, true, SCHED_MGROUP, EPI_SWIGLU_BWD>("bwd_down_dgrad_swiglu", ta, tb,
-                                                                   tg, a, mt, st);
+                                                                   tg, a, mt, st, nullptr, &om);
   return launch<128, false, true, SCHED_MGROUP, EPI_SWIGLU_BWD>("bwd_down_dgrad_swiglu", ta, tb,
-                                                                 tg, a, mt, st);
+                                                                 tg, a, mt, st, nullptr, &om);
 }
 
 cudaError_t gemm_bwd_gate_up_dgrad(const Dims& D, const void* dGU, const void* w_gate_up,
@@ -1202,6 +1271,7 @@ static cudaError_t wgrad(const Dims& D, const char* name, const void* A_rows, in
   a.ldo = N;
   a.out_group_stride = M * N;
   a.accumulate = accumulate ? 1 : 0;
+  a.evict_first = 1;  // weight gradients: the layer's output
   const int mt = a.E * a.m_tiles * a.n_tiles;
   if (D.wgrad_bf16) {
     if (accumulate) return cudaErrorInvalidValue;  // accumulation is fp32 only
@@ -1251,6 +1321,7 @@ cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* P_hi
   a.out = dw_down;
   a.ldo = D.d;  // rows of one expert's block in the [E*d, I] view
   a.accumulate = accumulate ? 1 : 0;
+  a.evict_first = 1;  // weight gradients: the layer's output
   const int mt = a.E * a.m_tiles * a.n_tiles;
   if (D.pair && a.m_tiles % 2 == 0)
     return launch<256, true, true, SCHED_KGROUP, EPI_F32_T, SPLIT_A, true>(
@@ -1285,7 +1356,12 @@ cudaError_t launch_router_logits(const Dims& D, const void* x, const void* w_rou
   a.n_valid = (int)D.E;
   a.out = logits;
   a.ldo = D.E;
-  const int mt = a.m_tiles * a.n_tiles;
+  // split K so that about 128 CTAs share the work; split s writes its
+  // partial logits to logits + s*T*E and the top-k sums them in order
+  a.k_splits = router_k_splits(D);
+  a.num_kb /= a.k_splits;
+  a.out_group_stride = D.T * D.E;
+  const int mt = a.m_tiles * a.n_tiles * a.k_splits;
   if (bn == 256)
     return launch<256, false, false, SCHED_DENSE, EPI_F32>("router_logits", ta, tb, ta, a, mt, st);
   return launch<128, false, false, SCHED_DENSE, EPI_F32>("router_logits", ta, tb, ta, a, mt, st);

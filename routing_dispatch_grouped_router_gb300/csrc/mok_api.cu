@@ -209,7 +209,7 @@ void fwd_layout(const Dims& D, FwdWs* W) {
   W->block_base = b.take(static_cast<size_t>(D.nb) * D.E * 4);
   W->h = b.take(rows * D.I * 2);
   W->o = b.take(rows * D.d * 4);  // fp32 expert outputs
-  W->logits = b.take(static_cast<size_t>(D.T) * D.E * 4);
+  W->logits = b.take(static_cast<size_t>(D.T) * D.E * 4 * router_k_splits(D));
   const size_t wgu = static_cast<size_t>(D.E) * 2 * D.I * D.d * 2;
   const size_t wd = static_cast<size_t>(D.E) * D.d * D.I * 2;
   W->xq_row = D.mx ? b.take(rows * D.d * 2) : 0;  // MXFP8 copies
@@ -261,7 +261,7 @@ void stage_layout(const Dims& D, StageWs* W) {
   W->ppos = take(static_cast<size_t>(D.T) * D.k * 4);
   W->ptok = take(rows * 4);
   W->row_w = 0;
-  W->logits = take(static_cast<size_t>(D.T) * D.E * 4);
+  W->logits = take(static_cast<size_t>(D.T) * D.E * 4 * router_k_splits(D));
   W->total = o;
 }
 

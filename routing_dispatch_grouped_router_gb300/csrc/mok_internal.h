@@ -37,6 +37,18 @@ struct Dims {
   bool pair;         // grouped GEMMs with 256-row tiles on CTA pairs (2-SM MMA)
 };
 
+// Split-K factor of the router logit GEMM: the largest power of two (up to
+// 8, dividing d/64) that keeps its tiles within 128 CTAs.  A function of the
+// shape only, so the logits are the same on every call.
+inline int router_k_splits(const Dims& D) {
+  const int64_t bn = D.E > 128 ? 256 : 128;
+  const int64_t tiles = ((D.T + 127) / 128) * ((D.E + bn - 1) / bn);
+  const int64_t nkb = D.d / 64;
+  int s = 1;
+  while (s < 8 && tiles * s * 2 <= 128 && nkb % (s * 2) == 0) s *= 2;
+  return s;
+}
+
 // Offsets inside one micro-batch's block of `saved` (relative to the block).
 struct BlockL {
   size_t topk_idx, topk_w, counts, offsets, pos, token_of_row, padded_offsets, mtile_prefix,

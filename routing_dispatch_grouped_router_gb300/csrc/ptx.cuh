@@ -108,6 +108,16 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, const void* 
       : "memory");
 }
 
+// The same store with an L2 eviction-priority policy (createpolicy).
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* tm, const void* src,
+                                                  int32_t c0, int32_t c1, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+      " [%0, {%2, %3}], [%1], %4;" ::"l"(reinterpret_cast<uint64_t>(tm)),
+      "r"(smem_addr(src)), "r"(c0), "r"(c1), "l"(policy)
+      : "memory");
+}
+
 // Tiled 2-D element-wise add shared -> global (fp32), tracked by bulk groups.
 __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* tm, const void* src,
                                                   int32_t c0, int32_t c1) {
@@ -153,6 +163,15 @@ __device__ __forceinline__ void bulk_wait_all() {
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_reduce_add_2d_hint(const CUtensorMap* tm, const void* src,
+                                                       int32_t c0, int32_t c1, uint64_t policy) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group.L2::cache_hint"
+      " [%0, {%2, %3}], [%1], %4;" ::"l"(reinterpret_cast<uint64_t>(tm)),
+      "r"(smem_addr(src)), "r"(c0), "r"(c1), "l"(policy)
+      : "memory");
 }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {

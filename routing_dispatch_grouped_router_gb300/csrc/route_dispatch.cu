@@ -29,8 +29,9 @@ namespace mok {
 // the lower expert index; NaN counts as -inf and is reported), softmax over
 // the chosen k.  Slots come out in descending logit order.
 __global__ void router_topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
-                                   int T, int E, int k, int32_t* __restrict__ topk_idx,
-                                   float* __restrict__ topk_w, int* status) {
+                                   int T, int E, int k, int nsplit,
+                                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                                   int* status) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= T) return;
@@ -43,7 +44,9 @@ __global__ void router_topk_kernel(const float* __restrict__ logits, const float
     const int e = j * 32 + lane;
     float x = -INFINITY;
     if (e < E) {
+      // the split-K partial logits, summed in split order
       x = row[e];
+      for (int sp = 1; sp < nsplit; ++sp) x += row[static_cast<long long>(sp) * T * E + e];
       if (bias) x += bias[e];
       if (x != x) {
         nan_seen = true;
@@ -107,21 +110,30 @@ cudaError_t launch_router_topk(const Dims& D, const float* logits, const float* 
   const long long blocks = (D.T * 32 + threads - 1) / threads;
   ProfScope prof("router_topk", st);
   router_topk_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
-      logits, bias, static_cast<int>(D.T), static_cast<int>(D.E), D.k, topk_idx, topk_w, status);
+      logits, bias, static_cast<int>(D.T), static_cast<int>(D.E), D.k, router_k_splits(D), topk_idx,
+      topk_w, status);
   count_launch();
   return cudaGetLastError();
 }
 
 // ----------------------------------------------------------- dispatch plan --
 
-// A slot is valid when its expert is in range and not repeated earlier in
-// the same token (a router never repeats; a caller's table might).
-__device__ __forceinline__ bool slot_valid(const int32_t* idx_row, int s, int E) {
-  const int e = idx_row[s];
-  if (e < 0 || e >= E) return false;
-  for (int j = 0; j < s; ++j)
-    if (idx_row[j] == e) return false;
-  return true;
+// A token's k experts, loaded once into registers, and the mask of its valid
+// slots: bit s is set when slot s names an expert in range that no earlier
+// slot of the token names (a router never repeats; a caller's table might).
+__device__ __forceinline__ uint32_t load_row(const int32_t* row, int k, int E,
+                                             int (&ids)[kMaxTopK]) {
+#pragma unroll
+  for (int s = 0; s < kMaxTopK; ++s) ids[s] = s < k ? row[s] : -1;
+  uint32_t valid = 0;
+#pragma unroll
+  for (int s = 0; s < kMaxTopK; ++s) {
+    bool ok = s < k && ids[s] >= 0 && ids[s] < E;
+#pragma unroll
+    for (int j = 0; j < s; ++j) ok = ok && ids[j] != ids[s];
+    valid |= ok ? (1u << s) : 0u;
+  }
+  return valid;
 }
 
 __global__ void plan_hist_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
@@ -131,13 +143,12 @@ __global__ void plan_hist_kernel(const int32_t* __restrict__ topk_idx, int T, in
   __syncthreads();
   const int t = blockIdx.x * kPlanBlock + threadIdx.x;
   if (t < T) {
-    const int32_t* row = topk_idx + static_cast<long long>(t) * k;
-    bool bad = false;
-    for (int s = 0; s < k; ++s) {
-      if (slot_valid(row, s, E)) atomicAdd(&cnt[row[s]], 1);
-      else bad = true;
-    }
-    if (bad) set_status(status, MOK_ERR_DEVICE_INDEX);
+    int ids[kMaxTopK];
+    const uint32_t valid = load_row(topk_idx + static_cast<long long>(t) * k, k, E, ids);
+#pragma unroll
+    for (int s = 0; s < kMaxTopK; ++s)
+      if (valid & (1u << s)) atomicAdd(&cnt[ids[s]], 1);
+    if (valid != (1u << k) - 1u) set_status(status, MOK_ERR_DEVICE_INDEX);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x)
@@ -241,30 +252,41 @@ __global__ void plan_place_kernel(const int32_t* __restrict__ topk_idx,
                                   int32_t* __restrict__ ptok, float* __restrict__ row_w) {
   constexpr int W = kPlanBlock / 32;  // 8 mask words per expert
   __shared__ uint32_t mask[kMaxExperts * W];
+  // per expert: first row of this block's tokens, plain and padded
+  __shared__ int s_row[kMaxExperts], s_prow[kMaxExperts];
   for (int i = threadIdx.x; i < E * W; i += blockDim.x) mask[i] = 0u;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int b = block_base[static_cast<long long>(blockIdx.x) * E + e];
+    s_row[e] = offsets[e] + b;
+    s_prow[e] = poff[e] + b;
+  }
   __syncthreads();
   const int t = blockIdx.x * kPlanBlock + threadIdx.x;
   const int word = threadIdx.x >> 5, bit = threadIdx.x & 31;
-  const int32_t* row = topk_idx + static_cast<long long>(t) * k;
+  int ids[kMaxTopK];
+  uint32_t valid = 0;
   if (t < T) {
-    for (int s = 0; s < k; ++s)
-      if (slot_valid(row, s, E)) atomicOr(&mask[row[s] * W + word], 1u << bit);
+    valid = load_row(topk_idx + static_cast<long long>(t) * k, k, E, ids);
+#pragma unroll
+    for (int s = 0; s < kMaxTopK; ++s)
+      if (valid & (1u << s)) atomicOr(&mask[ids[s] * W + word], 1u << bit);
   }
   __syncthreads();
   if (t >= T) return;
-  for (int s = 0; s < k; ++s) {
+#pragma unroll
+  for (int s = 0; s < kMaxTopK; ++s) {
+    if (s >= k) break;
     const long long ts = static_cast<long long>(t) * k + s;
-    if (!slot_valid(row, s, E)) {
+    if (!(valid & (1u << s))) {
       if (pos) pos[ts] = -1;
       ppos[ts] = -1;
       continue;
     }
-    const int e = row[s];
+    const int e = ids[s];
     int rank = __popc(mask[e * W + word] & ((1u << bit) - 1u));
     for (int w = 0; w < word; ++w) rank += __popc(mask[e * W + w]);
-    const int base = block_base[static_cast<long long>(blockIdx.x) * E + e] + rank;
-    const int p = offsets[e] + base;
-    const int pp = poff[e] + base;
+    const int p = s_row[e] + rank;
+    const int pp = s_prow[e] + rank;
     if (pos) pos[ts] = p;
     if (token_of_row) token_of_row[p] = t;
     ppos[ts] = pp;
