@@ -193,7 +193,7 @@ def cpu_baseline(inp: dict, shape: gen.Shape, budget_s: float = 12.0, tokens_per
 def run_reference(args, shape: gen.Shape, rank: int):
     if rank != 0:
         return
-    inp = gen.make_inputs(shape, seed=0)
+    inp = gen.workload_inputs(WORKLOAD, seed=0, parallel=True)
     tok_per_step = 1
     for i in range(args.warmup):
         oracle_sample(inp, shape, np.array([i % shape.T]))
@@ -217,11 +217,29 @@ def run_reference(args, shape: gen.Shape, rank: int):
 
 
 def workload_config(shape: gen.Shape) -> dict:
-    return {"workload": f"{WORKLOAD}: T={shape.T} d={shape.d} E={shape.E} I={shape.I} "
-                        f"top-{shape.k} bf16 forward+backward",
-            "T": shape.T, "d": shape.d, "E": shape.E, "I": shape.I, "k": shape.k,
-            "l2": "inputs larger than L2 (0.8 GB of expert weights read per step), no flush",
-            "parallelism": "replicas (one independent layer per GPU)"}
+    w = gen.WORKLOADS[WORKLOAD]
+    prec = "bf16"
+    if WORKLOAD == "mxfp8":
+        prec = (f"MXFP8 operands, {shape.T // w['mb_tokens']} micro-batches of {w['mb_tokens']} "
+                f"tokens through a {w['ring_slots']}-slot ring")
+    if w.get("zipf_s"):
+        prec += f", Zipf({w['zipf_s']}) router bias"
+    wbytes = shape.E * 3 * shape.I * shape.d * 2
+    cfg = {"workload": f"{WORKLOAD}: T={shape.T} d={shape.d} E={shape.E} I={shape.I} "
+                       f"top-{shape.k} {prec} forward+backward",
+           "T": shape.T, "d": shape.d, "E": shape.E, "I": shape.I, "k": shape.k,
+           "l2": f"inputs larger than L2 ({wbytes / 1e9:.1f} GB of expert weights read per step), "
+                 "no flush",
+           "parallelism": "replicas (one independent layer per GPU)"}
+    return cfg
+
+
+def layer_options(api) -> dict:
+    """MoELayer keyword arguments of the selected workload."""
+    w = gen.WORKLOADS[WORKLOAD]
+    if WORKLOAD == "mxfp8":
+        return dict(dtype=api.MXFP8, mb_tokens=w["mb_tokens"], ring_slots=w["ring_slots"])
+    return {}
 
 
 # ------------------------------------------------------------- multi-rank --
@@ -242,7 +260,8 @@ def job_throughput(world: int, tokens_per_rank: int, steps: int, t_max_ms: float
 
 # --------------------------------------------------------------- GPU side --
 
-def e2e_pipelined(layer, inp, x, dy, wr, wgu, wd, dwr, dwgu, dwd, stream, steps, world, dist):
+def e2e_pipelined(layer, inp, x, dy, wr, bias, wgu, wd, dwr, dwgu, dwd, stream, steps, world,
+                  dist):
     """Milliseconds for `steps` layer steps through the public API, each with
     its inputs uploaded from and its outputs read back to pinned host memory
     inside the timed region (copies on a side stream, two buffer sets)."""
@@ -278,8 +297,8 @@ def e2e_pipelined(layer, inp, x, dy, wr, wgu, wd, dwr, dwgu, dwd, stream, steps,
             stream.wait_event(inputs_in[b])
             if i >= 2:
                 stream.wait_event(outputs_out[b])  # y, dx of step i-2 read back
-            layer.forward(xd[b], wr, None, wgu, wd, y=yd[b])
-            layer.backward(dyd[b], xd[b], wr, None, wgu, wd, dx=dxd[b], dw_router=dwr,
+            layer.forward(xd[b], wr, bias, wgu, wd, y=yd[b])
+            layer.backward(dyd[b], xd[b], wr, bias, wgu, wd, dx=dxd[b], dw_router=dwr,
                            dw_gate_up=dwgu, dw_down=dwd)
             inputs_free[b].record(stream)
             outputs_ready[b].record(stream)
@@ -310,8 +329,12 @@ def main():
     ap.add_argument("--impl", default="mok", choices=["mok", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="fine", choices=sorted(gen.WORKLOADS),
+                    help="fine (default, the measured configuration) or another configuration")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    global WORKLOAD
+    WORKLOAD = args.workload
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -331,13 +354,14 @@ def main():
     from routing_dispatch_grouped_router_gb300 import api, build
     build.build()
 
-    inp = gen.make_inputs(shape, seed=0)
+    inp = gen.workload_inputs(WORKLOAD, seed=0, parallel=True)
 
     def dev(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
 
     x, wr, wgu, wd, dy = (dev(inp[n]) for n in ("x", "w_router", "w_gate_up", "w_down", "dy"))
-    layer = api.MoELayer(shape.T, shape.d, shape.E, shape.I, shape.k)
+    bias = torch.from_numpy(inp["bias"]).cuda() if inp.get("bias") is not None else None
+    layer = api.MoELayer(shape.T, shape.d, shape.E, shape.I, shape.k, **layer_options(api))
     f32 = dict(dtype=torch.float32, device="cuda")
     y = torch.empty(x.shape, **f32)
     dx = torch.empty(x.shape, **f32)
@@ -347,8 +371,8 @@ def main():
     stream = torch.cuda.current_stream()
 
     def step():
-        layer.forward(x, wr, None, wgu, wd, y=y)
-        layer.backward(dy, x, wr, None, wgu, wd, dx=dx, dw_router=dwr, dw_gate_up=dwgu,
+        layer.forward(x, wr, bias, wgu, wd, y=y)
+        layer.backward(dy, x, wr, bias, wgu, wd, dx=dx, dw_router=dwr, dw_gate_up=dwgu,
                        dw_down=dwd)
 
     for _ in range(args.warmup):
@@ -433,7 +457,7 @@ def main():
     # copies run on a second stream, double-buffered, so that step i+1's
     # upload and step i's read-back overlap the layer's kernels; events order
     # every reuse of a buffer.
-    e2e_ms = e2e_pipelined(layer, inp, x, dy, wr, wgu, wd, dwr, dwgu, dwd, stream,
+    e2e_ms = e2e_pipelined(layer, inp, x, dy, wr, bias, wgu, wd, dwr, dwgu, dwd, stream,
                            args.e2e_steps, world, dist)
     xh_bytes = x.numel() * 2
     if world > 1:
@@ -450,7 +474,8 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if WORKLOAD != "mxfp8" else "bf16 MMAs on MXFP8-quantised operands",
             "data": "synthetic", "config": workload_config(shape),
             "grouped_gemm_tflops": gg_tflops,
             "grouped_gemm_frac_of_peak": gg_tflops / peaks["bf16_sustained"],

@@ -105,9 +105,19 @@ constexpr int kStagingBytes = 4096;  // per epilogue warp: 32 rows x 128 bytes
 // six bf16 output blocks of a chunk (6 x 1 KB).
 constexpr int kGuStageBytes = 8192;
 constexpr int kSwigluBwdStaging = kGuStageBytes + 6 * 1024;
-template <int EPI>
+// Double-buffered store staging (a block is written while the previous
+// block's store still reads shared memory) is implemented but off: it costs
+// the 256-wide pair kernels their sixth operand stage, and measured slower
+// (fwd_gate_up 245 -> 260 us, fwd_down 132 -> 151 us on the fine workload).
+template <int EPI, int SPLIT, int SCHED>
+constexpr bool dbuf_store() {
+  return false;
+}
+template <int EPI, int SPLIT, int SCHED>
 constexpr int staging_bytes() {
-  return EPI == EPI_SWIGLU_BWD ? kSwigluBwdStaging : kStagingBytes;
+  return EPI == EPI_SWIGLU_BWD ? kSwigluBwdStaging
+                               : (dbuf_store<EPI, SPLIT, SCHED>() ? 2 * kStagingBytes
+                                                                  : kStagingBytes);
 }
 
 template <int BN, int SPLIT = SPLIT_NONE, bool PAIR = false, int STG = kStagingBytes>
@@ -141,6 +151,10 @@ static_assert(Cfg<256, SPLIT_NONE, true, kSwigluBwdStaging>::SMEM_BYTES <= 23244
                   Cfg<256, SPLIT_NONE, true, kSwigluBwdStaging>::STAGES == 3, "smem");
 static_assert(Cfg<256, SPLIT_NONE, false, kSwigluBwdStaging>::STAGES >= 2 &&
                   Cfg<128, SPLIT_NONE, false, kSwigluBwdStaging>::STAGES >= 3, "smem");
+static_assert(Cfg<256, SPLIT_NONE, true, 2 * kStagingBytes>::STAGES == 5 &&
+                  Cfg<256, SPLIT_NONE, false, 2 * kStagingBytes>::STAGES == 3 &&
+                  Cfg<128, SPLIT_NONE, false, 2 * kStagingBytes>::STAGES == 5,
+              "stages with double-buffered store staging");
 // stage counts of the other configurations are unchanged by the 512-byte barrier block
 static_assert(Cfg<256>::STAGES == 4 && Cfg<128>::STAGES == 6 && Cfg<256, SPLIT_A>::STAGES == 3 &&
                   Cfg<128, SPLIT_B>::STAGES == 4 && Cfg<256, SPLIT_NONE, true>::STAGES == 6 &&
@@ -369,10 +383,19 @@ __device__ __forceinline__ void tma_out_2d(const CUtensorMap* tmC, const void* b
   bulk_commit();
 }
 
-__device__ __forceinline__ void stage_and_store_f32(uint8_t* buf, const CUtensorMap* tmC,
+// DBUF: `base` holds two buffers used alternately (n counts this warp's
+// stores); a buffer is rewritten once the store two back has read it.
+template <bool DBUF = false>
+__device__ __forceinline__ void stage_and_store_f32(uint8_t* base, uint32_t& n,
+                                                    const CUtensorMap* tmC,
                                                     const float (&v)[32], int lane, int x, int y,
                                                     bool add = false, bool evict_first = false) {
-  if (lane == 0) bulk_wait_read<0>();  // the previous store has read the buffer
+  uint8_t* buf = DBUF ? base + (n & 1u) * kStagingBytes : base;
+  ++n;
+  if (lane == 0) {  // the store that last used this buffer has read it
+    if (DBUF) bulk_wait_read<1>();
+    else bulk_wait_read<0>();
+  }
   __syncwarp();
   uint8_t* row = buf + lane * 128;
 #pragma unroll
@@ -404,10 +427,10 @@ __device__ __forceinline__ void stage_and_store_f32_t(uint8_t* buf, const CUtens
   if (lane == 0) tma_out_2d(tmC, buf, x, y, add, evict_first);
 }
 
-template <int BN, int SCHED, int EPI>
+template <int BN, int SCHED, int EPI, bool DBUF>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl, uint32_t taddr,
                                               int q, int lane, int half, uint8_t* stage_buf,
-                                              const CUtensorMap* tmC) {
+                                              uint32_t& nst, const CUtensorMap* tmC) {
   constexpr int HALF_COLS = BN / 2;
   const int row_in_tile = q * 32 + lane;
   const bool zero_k = (tl.num_kb == 0);
@@ -424,8 +447,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = 0.f;
       }
-      stage_and_store_f32(stage_buf, tmC, v, lane, col0 + c, y, a.accumulate != 0,
-                          a.evict_first != 0);
+      stage_and_store_f32<DBUF>(stage_buf, nst, tmC, v, lane, col0 + c, y, a.accumulate != 0,
+                                a.evict_first != 0);
     }
   } else if (EPI == EPI_F32_T) {
     // C^T through TMA: accumulator rows are output columns; C viewed as
@@ -500,8 +523,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
         store_bf16x32(h + n0 + c, hv);
       }
       if (a.store_c) {
-        stage_and_store_f32(stage_buf, tmC, g, lane, n0 + c, y, false, a.evict_first != 0);
-        stage_and_store_f32(stage_buf, tmC, u, lane, I + n0 + c, y, false, a.evict_first != 0);
+        stage_and_store_f32<DBUF>(stage_buf, nst, tmC, g, lane, n0 + c, y, false,
+                                  a.evict_first != 0);
+        stage_and_store_f32<DBUF>(stage_buf, nst, tmC, u, lane, I + n0 + c, y, false,
+                                  a.evict_first != 0);
       }
     }
   } else if (EPI == EPI_SWIGLU_BWD) {
@@ -683,7 +708,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmL,
                 const __grid_constant__ GemmArgs args, const __grid_constant__ OutMaps om) {
-  using C = Cfg<BN, SPLIT, PAIR, staging_bytes<EPI>()>;
+  using C = Cfg<BN, SPLIT, PAIR, staging_bytes<EPI, SPLIT, SCHED>()>;
+  constexpr bool kDbuf = dbuf_store<EPI, SPLIT, SCHED>();
   static_assert(!PAIR || (SCHED != SCHED_DENSE && SPLIT != SPLIT_B && BN == 256), "pair");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -935,6 +961,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool gu_tma = kGuTma && !args.mx;
     uint64_t* wbar = gu_bar + 2 * (warp - 2);
     uint32_t gu_chunks = 0;
+    uint32_t nst = 0;  // TMA-store blocks issued by this warp
     int it = 0;
     for (int t = first; t < total; t += step, ++it) {
       bool valid;
@@ -957,7 +984,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           gu_chunks = swiglu_bwd_tma<BN>(args, tl, taddr, q, lane, half, stage_buf, wbar,
                                          gu_chunks, &tmC, &om, vabort);
       } else if (valid) {
-        epilogue_tile<BN, SCHED, EPI>(args, tl, taddr, q, lane, half, stage_buf, &tmC);
+        epilogue_tile<BN, SCHED, EPI, kDbuf>(args, tl, taddr, q, lane, half, stage_buf, nst,
+                                             &tmC);
       }
       tc_fence_before_sync();
       __syncwarp();
@@ -1047,7 +1075,7 @@ static cudaError_t launch(const char* name, const CUtensorMap& ta, const CUtenso
   if (om) om_v = *om;
   else memset(&om_v, 0, sizeof(om_v));
   auto kern = gemm_kernel<BN, A_MN, B_MN, SCHED, EPI, SPLIT, PAIR>;
-  constexpr int smem = Cfg<BN, SPLIT, PAIR, staging_bytes<EPI>()>::SMEM_BYTES;
+  constexpr int smem = Cfg<BN, SPLIT, PAIR, staging_bytes<EPI, SPLIT, SCHED>()>::SMEM_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (max_units <= 0) return cudaSuccess;

@@ -28,6 +28,8 @@ namespace mok {
 // One warp per token: add the bias, pick the k largest logits (exact ties to
 // the lower expert index; NaN counts as -inf and is reported), softmax over
 // the chosen k.  Slots come out in descending logit order.
+// PER = logits per lane: ceil(E / 32) rounded up to a power of two.
+template <int PER>
 __global__ void router_topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
                                    int T, int E, int k, int nsplit,
                                    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
@@ -35,7 +37,6 @@ __global__ void router_topk_kernel(const float* __restrict__ logits, const float
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= T) return;
-  constexpr int PER = kMaxExperts / 32;  // 16
   float v[PER];
   bool nan_seen = false;
   const float* row = logits + static_cast<long long>(warp) * E;
@@ -109,9 +110,19 @@ cudaError_t launch_router_topk(const Dims& D, const float* logits, const float* 
   const int threads = 256;
   const long long blocks = (D.T * 32 + threads - 1) / threads;
   ProfScope prof("router_topk", st);
-  router_topk_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
-      logits, bias, static_cast<int>(D.T), static_cast<int>(D.E), D.k, router_k_splits(D), topk_idx,
-      topk_w, status);
+  const int T = static_cast<int>(D.T), E = static_cast<int>(D.E), ns = router_k_splits(D);
+  const unsigned g = static_cast<unsigned>(blocks);
+  if (E <= 32)
+    router_topk_kernel<1><<<g, threads, 0, st>>>(logits, bias, T, E, D.k, ns, topk_idx, topk_w, status);
+  else if (E <= 64)
+    router_topk_kernel<2><<<g, threads, 0, st>>>(logits, bias, T, E, D.k, ns, topk_idx, topk_w, status);
+  else if (E <= 128)
+    router_topk_kernel<4><<<g, threads, 0, st>>>(logits, bias, T, E, D.k, ns, topk_idx, topk_w, status);
+  else if (E <= 256)
+    router_topk_kernel<8><<<g, threads, 0, st>>>(logits, bias, T, E, D.k, ns, topk_idx, topk_w, status);
+  else
+    router_topk_kernel<16><<<g, threads, 0, st>>>(logits, bias, T, E, D.k, ns, topk_idx, topk_w,
+                                                  status);
   count_launch();
   return cudaGetLastError();
 }
@@ -608,7 +619,21 @@ __global__ void router_wgrad_kernel(const uint4* __restrict__ Xp, const float* _
   const int r0 = poff[e], n = counts[e];
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (cv < dv) {
-    for (int i = lane_r; i < n; i += kRwRowLanes) {
+    // four rows' loads in flight at a time; the sum still runs row by row
+    int i = lane_r;
+    for (; i + 3 * kRwRowLanes < n; i += 4 * kRwRowLanes) {
+      uint4 v[4];
+      float w[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const long long r = r0 + i + u * kRwRowLanes;
+        v[u] = ld_global_nc_v4(Xp + r * dv + cv);
+        w[u] = dl_row[r];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) axpy8(acc, w[u], v[u]);
+    }
+    for (; i < n; i += kRwRowLanes) {
       const long long r = r0 + i;
       axpy8(acc, dl_row[r], ld_global_nc_v4(Xp + r * dv + cv));
     }
