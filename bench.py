@@ -43,8 +43,11 @@ WORKLOAD = "fine"
 #   Row movers: bytes that must cross HBM once.
 
 
-def gemm_flops(shape: gen.Shape) -> dict:
-    R, d, I, T, E = shape.R, shape.d, shape.I, shape.T, shape.E
+def gemm_flops(shape: gen.Shape, micro_batches: int = 1) -> dict:
+    """Algorithmic FLOP of one launch of each GEMM; with micro-batching every
+    launch covers T / micro_batches tokens."""
+    R, d, I, T, E = (shape.R // micro_batches, shape.d, shape.I, shape.T // micro_batches,
+                     shape.E)
     return {
         "router_logits": 2.0 * T * d * E,
         "fwd_gate_up_swiglu": 2.0 * R * d * 2 * I,
@@ -69,10 +72,12 @@ NCU_TRAFFIC_FINE = {
 }
 
 
-def mover_bytes(shape: gen.Shape) -> dict:
-    """Bytes each data-movement kernel must move in the layer's layout: bf16
-    token rows, fp32 expert-output and dX rows, fp32 y and dx (the default)."""
-    R, d, T, E, I = shape.R, shape.d, shape.T, shape.E, shape.I
+def mover_bytes(shape: gen.Shape, micro_batches: int = 1) -> dict:
+    """Bytes one launch of each data-movement kernel must move in the layer's
+    layout: bf16 token rows, fp32 expert-output and dX rows, fp32 y and dx
+    (the default); with micro-batching a launch covers T / micro_batches tokens."""
+    R, d, T, E, I = (shape.R // micro_batches, shape.d, shape.T // micro_batches, shape.E,
+                     shape.I)
     np_ = 2 * I // (256 if I % 256 == 0 else 128)
     return {
         # read each token row once per routed copy, write R bf16 rows (+ indices)
@@ -417,8 +422,8 @@ def main():
 
     # ---- per-kernel summary and the dominant kernel's roofline
     peaks = load_peaks()
-    flops = gemm_flops(shape)
-    movers = mover_bytes(shape)
+    flops = gemm_flops(shape, int(layer.layout.mb_count))
+    movers = mover_bytes(shape, int(layer.layout.mb_count))
     total_k = sum(v[1] for v in kernels.values())
     ksum = {}
     for name, (n, ms) in kernels.items():

@@ -257,6 +257,18 @@ mok_status mok_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int a_m
                          const void* B, int b_mn_major, void* C, void* workspace,
                          size_t ws_bytes, void* stream);
 
+/* Dense MXFP8 GEMM on the block-scaled tensor cores ([dothoosh] "MoK
+ * technical details", "Precision and scheduling": MXFP8 expert GEMMs):
+ *   C[m,n] = sum_k A[m,k] 2^(sa[m,k/32]-127) * B[n,k] 2^(sb[n,k/32]-127)
+ * A: uint8 [M,K] E4M3 codes, sa: uint8 [M,K/32] E8M0 scale bytes; B, sb the
+ * same for [N,K]; C: fp32 [M,N] (fp32 accumulation).  This is the layout
+ * mok_mx_quantize writes with along_rows = 0.  M, N, K multiples of 128;
+ * A, B, C 16-byte aligned, sa, sb 4-byte aligned.  workspace >= 256 bytes
+ * (status word). */
+mok_status mok_gemm_mxfp8(int64_t M, int64_t N, int64_t K, const uint8_t* A, const uint8_t* sa,
+                          const uint8_t* B, const uint8_t* sb, float* C, void* workspace,
+                          size_t ws_bytes, void* stream);
+
 /* Failure-path self-test: enqueues one CTA that waits on an mbarrier phase
  * nothing completes.  The wait is the bounded one every GEMM uses: it gives
  * up after its limit (0.2 s) and the kernel writes MOK_ERR_DEVICE_TIMEOUT to

@@ -1051,6 +1051,12 @@ static bool make_map_t(CUtensorMap* m, CUtensorMapDataType dt, int esz, const vo
   return r == CUDA_SUCCESS;
 }
 
+bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, int esz, const void* base,
+                        uint64_t inner, uint64_t outer, uint64_t row_elems, uint32_t box_inner,
+                        uint32_t box_rows, CUtensorMapSwizzle swz) {
+  return make_map_t(m, dt, esz, base, inner, outer, row_elems, box_inner, box_rows, swz);
+}
+
 // bf16 operand map, box {64, box_rows}
 static bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                      uint64_t row_elems, uint32_t box_rows) {

@@ -2,6 +2,7 @@
 // layouts, launch helpers of every kernel, and error plumbing.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -143,6 +144,16 @@ cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* P_hi
 cudaError_t gemm_wgrad_gate_up(const Dims& D, const void* dGU_hi, const void* dGU_lo,
                                const void* X_perm, const int32_t* poff, void* dw_gate_up,
                                bool accumulate, int* status, cudaStream_t st);
+// 2-D TMA map over a row-major [outer, inner] array (row stride row_elems),
+// box {box_inner, box_rows}, zero fill out of bounds.
+bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, int esz, const void* base,
+                        uint64_t inner, uint64_t outer, uint64_t row_elems, uint32_t box_inner,
+                        uint32_t box_rows, CUtensorMapSwizzle swz);
+// C[M,N] fp32 = dequant(A)[M,K] dequant(B)[N,K]^T, MXFP8 operands (E4M3 codes,
+// one E8M0 scale byte per 32 consecutive K values) on block-scaled tcgen05.
+cudaError_t gemm_dense_mxfp8(int64_t M, int64_t N, int64_t K, const uint8_t* A,
+                             const uint8_t* A_scales, const uint8_t* B, const uint8_t* B_scales,
+                             float* C, int* status, cudaStream_t st);
 cudaError_t gemm_dense_bf16(int64_t M, int64_t N, int64_t K, const void* A, bool a_mn,
                             const void* B, bool b_mn, void* C, int* status, cudaStream_t st);
 
