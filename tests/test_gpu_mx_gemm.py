@@ -50,7 +50,10 @@ def test_mxfp8_gemm_scale_placement(pattern):
     cb = np.full((N, K), E4M3_ONE, np.uint8)
     got = _run(ca, sa, cb, sb)
     ref = 32.0 * (2.0 ** (sa.astype(np.float64) - 127)) @ (2.0 ** (sb.astype(np.float64) - 127)).T
-    np.testing.assert_allclose(got, ref, rtol=1e-6, atol=0)
+    # every term is positive, so fp32 accumulation of the K/32 block sums is
+    # within (K/32) * 2^-24 * ref (plus rounding slack); a scale byte read from
+    # the wrong row, column or K block changes a term by a factor of 2 or more
+    np.testing.assert_allclose(got, ref, rtol=2e-5, atol=0)
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 384, 1024), (512, 256, 2048)])
