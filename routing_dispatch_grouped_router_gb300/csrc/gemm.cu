@@ -54,7 +54,10 @@ enum Epi : int {
 // Split operands: a bf16 "hi" tile plus a bf16 "lo" tile (value - hi) whose
 // products are accumulated into the same fp32 accumulator, giving the GEMM
 // an operand with ~16 significant bits.
-enum Split : int { SPLIT_NONE = 0, SPLIT_A = 1, SPLIT_B = 2 };
+// SPLIT_MX: not a split but the MXFP8 operand mode: A and B are E4M3 codes
+// (K-major, 128 K values per stage) with one E8M0 scale byte per 32 K values,
+// multiplied by tcgen05.mma.kind::mxf8f6f4.block_scale (single CTA, BN=128).
+enum Split : int { SPLIT_NONE = 0, SPLIT_A = 1, SPLIT_B = 2, SPLIT_MX = 3 };
 
 struct GemmArgs {
   int E;             // groups (experts); 1 for dense
@@ -76,6 +79,11 @@ struct GemmArgs {
   void* out4;               // SWIGLU_BWD: P_lo [rows,I]
   void* out5;               // SWIGLU_BWD with mx: MXFP8 dGU [rows,2I] (dgrad operand)
   int mx;                   // SwiGLU epilogues: quantise the derived GEMM operands to MXFP8
+  const uint8_t* sa;        // SPLIT_MX: A scale bytes, row-major [rows of A, K/32]
+  const uint8_t* sb;        // SPLIT_MX: B scale bytes, row-major [rows of B, K/32]
+  int ks;                   // SPLIT_MX: K / 32 (scale bytes per row)
+  uint8_t* h_codes;         // SWIGLU_FWD with SPLIT_MX: h as E4M3 codes [rows, I] (NULL: none)
+  uint8_t* h_scales;        // ... and its E8M0 bytes [rows, I/32]
   int accumulate;           // fp32 TMA-store epilogue: add into C instead of overwriting
   int store_c;              // SWIGLU_FWD: write g, u through the C map
   int evict_first;          // TMA-store epilogues: C is not read again soon (L2 evict-first)
@@ -129,11 +137,16 @@ struct Cfg {
   static constexpr int A_TILES = SPLIT == SPLIT_A ? 2 : 1;
   static constexpr int B_TILES = SPLIT == SPLIT_B ? 2 : 1;
   static constexpr int B_OFF = A_TILES * A_BYTES;  // B tile(s) follow the A tile(s)
-  static constexpr int STAGE_BYTES = A_TILES * A_BYTES + B_TILES * B_BYTES;
+  // SPLIT_MX: 128-row x 128-byte code tiles (the bf16 tile sizes) and the two
+  // 512-byte scale blocks of the stage (A's 128 rows, B's 128 rows)
+  static constexpr int SF_OFF = A_TILES * A_BYTES + B_TILES * B_BYTES;
+  static constexpr int SF_BYTES = SPLIT == SPLIT_MX ? 1024 : 0;
+  static constexpr int STAGE_BYTES = SF_OFF + SF_BYTES;
   static constexpr int BAR_BYTES = 512;
   static constexpr int STAGE_ROOM = 232448 - 1024 - BAR_BYTES - kEpiWarps * STG;
   static constexpr int STAGES = (STAGE_ROOM / STAGE_BYTES) < 6 ? (STAGE_ROOM / STAGE_BYTES) : 6;
-  static constexpr int TMEM_COLS = 2 * BN;
+  // SPLIT_MX: after the accumulators, 8 columns of scales per stage
+  static constexpr int TMEM_COLS = SPLIT == SPLIT_MX ? 512 : 2 * BN;
   static constexpr int STAGING_OFF = STAGES * STAGE_BYTES;
   static constexpr int STAGING_PER_WARP = STG;
   static constexpr int BAR_OFF = STAGING_OFF + kEpiWarps * STG;
@@ -151,6 +164,9 @@ static_assert(Cfg<256, SPLIT_NONE, true, kSwigluBwdStaging>::SMEM_BYTES <= 23244
                   Cfg<256, SPLIT_NONE, true, kSwigluBwdStaging>::STAGES == 3, "smem");
 static_assert(Cfg<256, SPLIT_NONE, false, kSwigluBwdStaging>::STAGES >= 2 &&
                   Cfg<128, SPLIT_NONE, false, kSwigluBwdStaging>::STAGES >= 3, "smem");
+static_assert(Cfg<128, SPLIT_MX>::STAGES == 5 && Cfg<128, SPLIT_MX>::STAGE_BYTES % 1024 == 0 &&
+                  2 * 128 + 8 * Cfg<128, SPLIT_MX>::STAGES <= 512,
+              "MXFP8 stages");
 static_assert(Cfg<256, SPLIT_NONE, true, 2 * kStagingBytes>::STAGES == 5 &&
                   Cfg<256, SPLIT_NONE, false, 2 * kStagingBytes>::STAGES == 3 &&
                   Cfg<128, SPLIT_NONE, false, 2 * kStagingBytes>::STAGES == 5,
@@ -427,7 +443,7 @@ __device__ __forceinline__ void stage_and_store_f32_t(uint8_t* buf, const CUtens
   if (lane == 0) tma_out_2d(tmC, buf, x, y, add, evict_first);
 }
 
-template <int BN, int SCHED, int EPI, bool DBUF>
+template <int BN, int SCHED, int EPI, bool DBUF, int SPLIT>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl, uint32_t taddr,
                                               int q, int lane, int half, uint8_t* stage_buf,
                                               uint32_t& nst, const CUtensorMap* tmC) {
@@ -496,6 +512,36 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
           if (col < a.n_valid) p[col] = v[j];
         }
       }
+    }
+  } else if (EPI == EPI_SWIGLU_FWD && SPLIT == SPLIT_MX) {
+    // BN = 128: accumulator columns [0,64) gate, [64,128) up, for FFN columns
+    // n0 .. n0+63 (n0 = n_tile*64); this warp: 32 of them, one MX block of h
+    const long long r = tl.row0 + row_in_tile;
+    const int I = a.I;
+    const int c0 = half * 32;
+    const int n0 = tl.n_tile * 64 + c0;
+    const int y = tl.row0 + q * 32;
+    float g[32], u[32];
+    tmem_ld32(taddr + c0, g);
+    tmem_ld32(taddr + 64 + c0, u);
+    if (a.h_codes) {
+      float hv[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float s;
+        hv[j] = silu_f(g[j], &s) * u[j];
+      }
+      uint32_t w[8];
+      const uint32_t sbyte = mx_encode32(hv, w);
+      uint4* cp = reinterpret_cast<uint4*>(a.h_codes + r * I + n0);
+      cp[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      cp[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      a.h_scales[r * (I / 32) + n0 / 32] = static_cast<uint8_t>(sbyte);
+    }
+    if (a.store_c) {
+      stage_and_store_f32<DBUF>(stage_buf, nst, tmC, g, lane, n0, y, false, a.evict_first != 0);
+      stage_and_store_f32<DBUF>(stage_buf, nst, tmC, u, lane, I + n0, y, false,
+                                a.evict_first != 0);
     }
   } else if (EPI == EPI_SWIGLU_FWD) {
     // BN = 256: accumulator columns [0,128) gate, [128,256) up, for FFN
@@ -710,7 +756,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ GemmArgs args, const __grid_constant__ OutMaps om) {
   using C = Cfg<BN, SPLIT, PAIR, staging_bytes<EPI, SPLIT, SCHED>()>;
   constexpr bool kDbuf = dbuf_store<EPI, SPLIT, SCHED>();
-  static_assert(!PAIR || (SCHED != SCHED_DENSE && SPLIT != SPLIT_B && BN == 256), "pair");
+  static_assert(!PAIR || (SCHED != SCHED_DENSE && SPLIT != SPLIT_B && SPLIT != SPLIT_MX &&
+                          BN == 256), "pair");
+  static_assert(SPLIT != SPLIT_MX || (!A_MN && !B_MN && BN == 128 && SCHED == SCHED_MGROUP),
+                "MXFP8 operands: K-major, single CTA, 128-wide tiles");
+  constexpr int KX = SPLIT == SPLIT_MX ? 128 : 64;  // K values per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -791,7 +841,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (warp == 0) {
-    if (lane == 0) {
+    // SPLIT_MX: every lane gathers scale bytes; lane 0 alone issues the TMA
+    if (lane == 0 || SPLIT == SPLIT_MX) {
       // ------------------------------------------------------- producer --
       // PAIR: both CTAs load their halves; the copies complete on the
       // leader's `full` barrier, which the leader arms for both
@@ -813,15 +864,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sA = tiles + stage * C::STAGE_BYTES;
           uint8_t* sB = sA + C::B_OFF;
           const uint32_t bar_c = full_leader + 8u * stage;
+          if (SPLIT == SPLIT_MX) {
+            // the stage's scale blocks: A rows row0.., then the B tile's rows
+            // (SWIGLU_FWD: 64 gate rows, then the matching 64 up rows)
+            gather_sf(sA + C::SF_OFF, args.sa, args.ks, tl.row0, (long long)(tl.kb0 + kb) * 4,
+                      lane);
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int t = lane + 32 * j;  // row of the B tile
+              long long grow;
+              if (EPI == EPI_SWIGLU_FWD)
+                grow = (long long)tl.e * args.b_group_rows + tl.n_tile * (BN / 2) +
+                       (t < BN / 2 ? t : args.I + t - BN / 2);
+              else
+                grow = (long long)tl.e * args.b_group_rows + tl.n_tile * BN + t;
+              w[j] = *reinterpret_cast<const uint32_t*>(args.sb + grow * args.ks +
+                                                        (long long)(tl.kb0 + kb) * 4);
+            }
+            *reinterpret_cast<uint4*>(sA + C::SF_OFF + 512 + lane * 16) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+            fence_proxy_async_smem();  // read by tcgen05.cp through the async proxy
+            __syncwarp();
+          }
           auto load = [&](void* dst, const CUtensorMap* tm, int x, int y) {
+            if (SPLIT == SPLIT_MX && lane != 0) return;
             if (PAIR) tma_load_2d_pair(dst, tm, bar_c, x, y);
             else tma_load_2d(dst, tm, &full[stage], x, y);
           };
-          if (!PAIR) mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          else if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+          if (!PAIR) {
+            if (lane == 0) mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES - C::SF_BYTES);
+          } else if (leader) {
+            mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+          }
           // A tile: 128 rows (M) x 64 (K)  (+ its lo tile with SPLIT_A)
           if (!A_MN) {
-            load(sA, &tmA, (tl.kb0 + kb) * 64, tl.row0);
+            load(sA, &tmA, (tl.kb0 + kb) * KX, tl.row0);
           } else {
             const int ky = tl.k_row0 + (tl.kb0 + kb) * 64;
 #pragma unroll
@@ -833,18 +911,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           // B tile: B_ROWS rows (N) x 64 (K); PAIR: this CTA's half of N
           if (!B_MN) {
             if (EPI == EPI_SWIGLU_FWD) {
-              // gate rows n0..n0+127, then the matching up rows (+I)
-              const int r0 = tl.e * args.b_group_rows + tl.n_tile * 128;
+              // gate rows n0..n0+BN/2-1, then the matching up rows (+I)
+              const int r0 = tl.e * args.b_group_rows + tl.n_tile * (BN / 2);
               if (PAIR) {
-                load(sB, &tmB, kb * 64, r0 + rank * args.I);
+                load(sB, &tmB, kb * KX, r0 + rank * args.I);
               } else {
-                load(sB, &tmB, kb * 64, r0);
-                load(sB + 16384, &tmB, kb * 64, r0 + args.I);
+                load(sB, &tmB, kb * KX, r0);
+                load(sB + (BN / 2) * 128, &tmB, kb * KX, r0 + args.I);
               }
             } else {
               const int r0 = (SCHED == SCHED_DENSE ? 0 : tl.e * args.b_group_rows) +
                              tl.n_tile * BN + rank * C::B_ROWS;
-              load(sB, &tmB, (tl.kb0 + kb) * 64, r0);
+              load(sB, &tmB, (tl.kb0 + kb) * KX, r0);
             }
           } else {
             int ky;
@@ -919,6 +997,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after_sync();
           const uint32_t a_base = smem_addr(tiles + stage * C::STAGE_BYTES);
           const uint32_t b_base = a_base + C::B_OFF;
+          if (SPLIT == SPLIT_MX) {
+            // scales to TMEM (8 columns per stage after the accumulators),
+            // then four K=32 block-scaled MMAs, scale byte j each
+            const uint32_t sfa = tmem_base + 2u * BN + 8u * stage;
+            tmem_cp_sf(sfa, smem_desc_sf(a_base + C::SF_OFF));
+            tmem_cp_sf(sfa + 4u, smem_desc_sf(a_base + C::SF_OFF + 512));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint64_t ad = smem_desc_sw128(a_base + j * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(b_base + j * 32, 16, 1024);
+              mma_mxf8(d_tmem, ad, bd, idesc_mxf8(128, BN, static_cast<uint32_t>(j)), sfa,
+                       sfa + 4u, (kb | j) != 0 ? 1u : 0u);
+            }
+            commit(&empty[stage]);
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint64_t ad = smem_desc_sw128(a_base + j * kstep_a, lbo_a, 1024);
@@ -984,8 +1082,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           gu_chunks = swiglu_bwd_tma<BN>(args, tl, taddr, q, lane, half, stage_buf, wbar,
                                          gu_chunks, &tmC, &om, vabort);
       } else if (valid) {
-        epilogue_tile<BN, SCHED, EPI, kDbuf>(args, tl, taddr, q, lane, half, stage_buf, nst,
-                                             &tmC);
+        epilogue_tile<BN, SCHED, EPI, kDbuf, SPLIT>(args, tl, taddr, q, lane, half, stage_buf,
+                                                    nst, &tmC);
       }
       tc_fence_before_sync();
       __syncwarp();
@@ -1166,6 +1264,70 @@ cudaError_t gemm_fwd_gate_up(const Dims& D, const void* X_perm, const void* w_ga
         "fwd_gate_up_swiglu", ta, tb, tc, a, max_mpairs(D) * a.n_tiles, st);
   return launch<256, false, false, SCHED_MGROUP, EPI_SWIGLU_FWD>(
       "fwd_gate_up_swiglu", ta, tb, tc, a, max_mtiles(D) * a.n_tiles, st);
+}
+
+// MXFP8 operands (E4M3 codes, E8M0 scale bytes per 32 K values, K-major):
+// the gate/up GEMM with g, u to GU (NULL: not stored) and h as MXFP8 codes
+// and scales (NULL: not stored), single-CTA 128-wide tiles of 64 FFN columns.
+cudaError_t gemm_fwd_gate_up_mx(const Dims& D, const uint8_t* x_codes, const uint8_t* x_scales,
+                                const uint8_t* wgu_codes, const uint8_t* wgu_scales,
+                                const int32_t* mtile_prefix, const int32_t* poff, void* GU,
+                                uint8_t* h_codes, uint8_t* h_scales, int* status,
+                                cudaStream_t st) {
+  const auto u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  CUtensorMap ta, tb, tc;
+  if (!make_map_t(&ta, u8, 1, x_codes, D.d, D.rows_max, D.d, 128, 128, sw) ||
+      !make_map_t(&tb, u8, 1, wgu_codes, D.d, D.E * 2 * D.I, D.d, 128, 64, sw))
+    return cudaErrorInvalidValue;
+  if (GU ? !make_out_map(&tc, GU, 2 * D.I, D.rows_max) : false) return cudaErrorInvalidValue;
+  if (!GU) tc = ta;  // never used without GU; a valid map for the prefetch
+  if (!GU && !h_codes) return cudaErrorInvalidValue;
+  GemmArgs a = blank_args(status);
+  a.store_c = GU ? 1 : 0;
+  a.evict_first = 1;
+  a.E = (int)D.E;
+  a.n_tiles = (int)(D.I / 64);
+  a.num_kb = (int)(D.d / 128);
+  a.b_group_rows = (int)(2 * D.I);
+  a.I = (int)D.I;
+  a.mtile_prefix = mtile_prefix;
+  a.poff = poff;
+  a.out = GU;
+  a.sa = x_scales;
+  a.sb = wgu_scales;
+  a.ks = (int)(D.d / 32);
+  a.h_codes = h_codes;
+  a.h_scales = h_scales;
+  return launch<128, false, false, SCHED_MGROUP, EPI_SWIGLU_FWD, SPLIT_MX>(
+      "fwd_gate_up_swiglu", ta, tb, tc, a, max_mtiles(D) * a.n_tiles, st);
+}
+
+cudaError_t gemm_fwd_down_mx(const Dims& D, const uint8_t* h_codes, const uint8_t* h_scales,
+                             const uint8_t* wd_codes, const uint8_t* wd_scales,
+                             const int32_t* mtile_prefix, const int32_t* poff, void* O,
+                             int* status, cudaStream_t st) {
+  const auto u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  CUtensorMap ta, tb, tc;
+  if (!make_map_t(&ta, u8, 1, h_codes, D.I, D.rows_max, D.I, 128, 128, sw) ||
+      !make_map_t(&tb, u8, 1, wd_codes, D.I, D.E * D.d, D.I, 128, 128, sw) ||
+      !make_out_map(&tc, O, D.d, D.rows_max))
+    return cudaErrorInvalidValue;
+  GemmArgs a = blank_args(status);
+  a.E = (int)D.E;
+  a.n_tiles = (int)(D.d / 128);
+  a.num_kb = (int)(D.I / 128);
+  a.b_group_rows = (int)D.d;
+  a.mtile_prefix = mtile_prefix;
+  a.poff = poff;
+  a.out = O;  // fp32 [rows_max, d]
+  a.ldo = D.d;
+  a.sa = h_scales;
+  a.sb = wd_scales;
+  a.ks = (int)(D.I / 32);
+  return launch<128, false, false, SCHED_MGROUP, EPI_F32, SPLIT_MX>(
+      "fwd_down", ta, tb, tc, a, max_mtiles(D) * a.n_tiles, st);
 }
 
 cudaError_t gemm_fwd_down(const Dims& D, const void* H, const void* w_down,

@@ -207,14 +207,19 @@ void fwd_layout(const Dims& D, FwdWs* W) {
   const size_t rows = static_cast<size_t>(D.rows_max);
   W->block_counts = b.take(static_cast<size_t>(D.nb) * D.E * 4);
   W->block_base = b.take(static_cast<size_t>(D.nb) * D.E * 4);
-  W->h = b.take(rows * D.I * 2);
+  W->h = D.mx ? 0 : b.take(rows * D.I * 2);  // bf16 h (MXFP8: codes below)
   W->o = b.take(rows * D.d * 4);  // fp32 expert outputs
   W->logits = b.take(static_cast<size_t>(D.T) * D.E * 4 * router_k_splits(D));
-  const size_t wgu = static_cast<size_t>(D.E) * 2 * D.I * D.d * 2;
-  const size_t wd = static_cast<size_t>(D.E) * D.d * D.I * 2;
-  W->xq_row = D.mx ? b.take(rows * D.d * 2) : 0;  // MXFP8 copies
-  W->wgu_row = D.mx ? b.take(wgu) : 0;
-  W->wd_row = D.mx ? b.take(wd) : 0;
+  const size_t wgu = static_cast<size_t>(D.E) * 2 * D.I * D.d;  // elements
+  const size_t wd = static_cast<size_t>(D.E) * D.d * D.I;
+  auto mx = [&](size_t elems, size_t* codes, size_t* scales) {
+    *codes = D.mx ? b.take(elems) : 0;
+    *scales = D.mx ? b.take(elems / 32) : 0;
+  };
+  mx(rows * D.d, &W->xq_codes, &W->xq_scales);
+  mx(rows * D.I, &W->h_codes, &W->h_scales);
+  mx(wgu, &W->wgu_codes, &W->wgu_scales);
+  mx(wd, &W->wd_codes, &W->wd_scales);
   W->total = b.o;
 }
 
@@ -240,8 +245,11 @@ void bwd_layout(const Dims& D, BwdWs* W) {
   W->wgu_col = D.mx ? b.take(wgu) : 0;
   // recompute of g, u: their fp32 rows, and the forward's MXFP8 operands
   W->gu = D.recompute_gu ? b.take(rows * 2 * D.I * 4) : 0;
-  W->xq_row = (D.recompute_gu && D.mx) ? b.take(rows * D.d * 2) : 0;
-  W->wgu_row = (D.recompute_gu && D.mx) ? b.take(wgu) : 0;
+  const bool rmx = D.recompute_gu && D.mx;  // MXFP8 operands of the recomputed gate/up GEMM
+  W->xq_codes = rmx ? b.take(rows * D.d) : 0;
+  W->xq_scales = rmx ? b.take(rows * D.d / 32) : 0;
+  W->wgu_codes = rmx ? b.take(wgu / 2) : 0;
+  W->wgu_scales = rmx ? b.take(wgu / 64) : 0;
   W->total = b.o;
 }
 
@@ -343,20 +351,23 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
 
   int* status = at<int>(saved, L.status);
   MOK_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
-  const void* wgu_op = w_gate_up;
-  const void* wd_op = w_down;
+  // MXFP8: E4M3 codes and E8M0 scales (blocks of 32 along K) of the weights,
+  // once per call: W_gate_up along d, W_down along I
+  uint8_t* wgu_c = at<uint8_t>(workspace, F.wgu_codes);
+  uint8_t* wgu_s = at<uint8_t>(workspace, F.wgu_scales);
+  uint8_t* wd_c = at<uint8_t>(workspace, F.wd_codes);
+  uint8_t* wd_s = at<uint8_t>(workspace, F.wd_scales);
+  uint8_t* xq_c = at<uint8_t>(workspace, F.xq_codes);
+  uint8_t* xq_s = at<uint8_t>(workspace, F.xq_scales);
+  uint8_t* h_c = at<uint8_t>(workspace, F.h_codes);
+  uint8_t* h_s = at<uint8_t>(workspace, F.h_scales);
   if (D.mx) {
-    // weights quantised once per call, along d (gate/up) and along I (down)
-    void* wgu_q = at<char>(workspace, F.wgu_row);
-    void* wd_q = at<char>(workspace, F.wd_row);
-    MOK_CUDA(launch_mx_rows(w_gate_up, wgu_q, D.E * 2 * D.I, D.d, nullptr, nullptr, st));
-    MOK_CUDA(launch_mx_rows(w_down, wd_q, D.E * D.d, D.I, nullptr, nullptr, st));
-    wgu_op = wgu_q;
-    wd_op = wd_q;
+    MOK_CUDA(launch_mx_rows(w_gate_up, nullptr, D.E * 2 * D.I, D.d, wgu_c, wgu_s, st));
+    MOK_CUDA(launch_mx_rows(w_down, nullptr, D.E * D.d, D.I, wd_c, wd_s, st));
   }
   const size_t y_esz = D.act_bf16 ? 2 : 4;
   float* logits = at<float>(workspace, F.logits);
-  void* h = at<char>(workspace, F.h);
+  void* h = D.mx ? nullptr : at<char>(workspace, F.h);
   void* O = at<char>(workspace, F.o);
   for (int i = 0; i < D.nmb; ++i) {
     // micro-batch i: tokens [i*T, (i+1)*T), dispatched into ring slot i % ring
@@ -382,15 +393,19 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
     void* x_perm = at<char>(saved, L.x_perm + (i % D.ring) * L.ring_slot_bytes);
     void* gu = D.recompute_gu ? nullptr : at<char>(saved, L.gate_up + blk);
     MOK_CUDA(launch_gather_rows(D, xi, o.ptok, o.padded_offsets, x_perm, status, st));
-    const void* x_op = x_perm;
     if (D.mx) {
-      void* xq = at<char>(workspace, F.xq_row);
-      MOK_CUDA(launch_mx_rows(x_perm, xq, D.rows_max, D.d, nullptr, nullptr, st));
-      x_op = xq;
+      // expert GEMMs on the block-scaled tensor cores: x rows to MXFP8, the
+      // gate/up GEMM writes h as MXFP8 for the down projection
+      MOK_CUDA(launch_mx_rows(x_perm, nullptr, D.rows_max, D.d, xq_c, xq_s, st));
+      MOK_CUDA(gemm_fwd_gate_up_mx(D, xq_c, xq_s, wgu_c, wgu_s, o.mtile_prefix, o.padded_offsets,
+                                   gu, h_c, h_s, status, st));
+      MOK_CUDA(gemm_fwd_down_mx(D, h_c, h_s, wd_c, wd_s, o.mtile_prefix, o.padded_offsets, O,
+                                status, st));
+    } else {
+      MOK_CUDA(gemm_fwd_gate_up(D, x_perm, w_gate_up, o.mtile_prefix, o.padded_offsets, gu, h,
+                                status, st));
+      MOK_CUDA(gemm_fwd_down(D, h, w_down, o.mtile_prefix, o.padded_offsets, O, status, st));
     }
-    MOK_CUDA(gemm_fwd_gate_up(D, x_op, wgu_op, o.mtile_prefix, o.padded_offsets, gu, h, status,
-                              st));
-    MOK_CUDA(gemm_fwd_down(D, h, wd_op, o.mtile_prefix, o.padded_offsets, O, status, st));
     MOK_CUDA(launch_combine(D, static_cast<const float*>(O), o.ppos, topk_w, yi, st));
   }
   return MOK_OK;
@@ -438,12 +453,13 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
   void* dgu_mx = D.mx ? at<char>(workspace, B.dgu_mx) : nullptr;
   const void* wd_op = w_down;
   const void* wgu_op = w_gate_up;
-  const void* wgu_fwd_op = w_gate_up;  // operand of the recomputed gate/up GEMM
-  if (D.mx && D.recompute_gu) {
-    void* q = at<char>(workspace, B.wgu_row);
-    MOK_CUDA(launch_mx_rows(w_gate_up, q, D.E * 2 * D.I, D.d, nullptr, nullptr, st));
-    wgu_fwd_op = q;
-  }
+  // MXFP8 operands of the recomputed gate/up GEMM (the forward's kernel)
+  uint8_t* rwgu_c = at<uint8_t>(workspace, B.wgu_codes);
+  uint8_t* rwgu_s = at<uint8_t>(workspace, B.wgu_scales);
+  uint8_t* rxq_c = at<uint8_t>(workspace, B.xq_codes);
+  uint8_t* rxq_s = at<uint8_t>(workspace, B.xq_scales);
+  if (D.mx && D.recompute_gu)
+    MOK_CUDA(launch_mx_rows(w_gate_up, nullptr, D.E * 2 * D.I, D.d, rwgu_c, rwgu_s, st));
   if (D.mx) {
     // weights quantised once per call along the dgrads' reduction dims:
     // W_down along d, W_gate_up along 2I (blocks of 32 rows)
@@ -479,14 +495,14 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
     }
     if (D.recompute_gu) {
       // the forward's gate/up GEMM again, g and u only (no h)
-      const void* x_op = x_perm;
       if (D.mx) {
-        void* xq = at<char>(workspace, B.xq_row);
-        MOK_CUDA(launch_mx_rows(x_perm, xq, D.rows_max, D.d, nullptr, nullptr, st));
-        x_op = xq;
+        MOK_CUDA(launch_mx_rows(x_perm, nullptr, D.rows_max, D.d, rxq_c, rxq_s, st));
+        MOK_CUDA(gemm_fwd_gate_up_mx(D, rxq_c, rxq_s, rwgu_c, rwgu_s, mtp, poff,
+                                     const_cast<void*>(gu), nullptr, nullptr, status, st));
+      } else {
+        MOK_CUDA(gemm_fwd_gate_up(D, x_perm, w_gate_up, mtp, poff, const_cast<void*>(gu),
+                                  nullptr, status, st));
       }
-      MOK_CUDA(gemm_fwd_gate_up(D, x_op, wgu_fwd_op, mtp, poff, const_cast<void*>(gu), nullptr,
-                                status, st));
     }
     // reverse-combine: pull dy rows into expert order
     MOK_CUDA(launch_gather_rows(D, dyi, ptok, poff, dy_perm, status, st));

@@ -56,11 +56,14 @@ struct BlockL {
       padded_pos, padded_token, row_weight, gate_up, total;
 };
 struct FwdWs {
-  size_t block_counts, block_base, h, o, logits, xq_row, wgu_row, wd_row, total;
+  size_t block_counts, block_base, h, o, logits;
+  // MXFP8: E4M3 codes and E8M0 scale bytes of x rows, h, W_gate_up, W_down
+  size_t xq_codes, xq_scales, h_codes, h_scales, wgu_codes, wgu_scales, wd_codes, wd_scales;
+  size_t total;
 };
 struct BwdWs {
   size_t dy_perm, dgu_hi, dgu_lo, p_hi, p_lo, dp_part, dx_perm, dl_row, dl_tok, dyq_row, dyq_col,
-      xq_col, dgu_mx, wd_col, wgu_col, gu, xq_row, wgu_row, total;
+      xq_col, dgu_mx, wd_col, wgu_col, gu, xq_codes, xq_scales, wgu_codes, wgu_scales, total;
 };
 struct StageWs {
   size_t status, block_counts, block_base, padded_offsets, mtile_prefix, ppos, ptok, row_w,
@@ -126,6 +129,15 @@ cudaError_t launch_router_wgrad(const Dims& D, const void* X_perm, const float* 
 // Grouped GEMMs on tcgen05 (see gemm.cu).
 cudaError_t gemm_fwd_gate_up(const Dims& D, const void* X_perm, const void* w_gate_up,
                              const int32_t* mtile_prefix, const int32_t* poff, void* GU, void* H,
+                             int* status, cudaStream_t st);
+cudaError_t gemm_fwd_gate_up_mx(const Dims& D, const uint8_t* x_codes, const uint8_t* x_scales,
+                                const uint8_t* wgu_codes, const uint8_t* wgu_scales,
+                                const int32_t* mtile_prefix, const int32_t* poff, void* GU,
+                                uint8_t* h_codes, uint8_t* h_scales, int* status,
+                                cudaStream_t st);
+cudaError_t gemm_fwd_down_mx(const Dims& D, const uint8_t* h_codes, const uint8_t* h_scales,
+                             const uint8_t* wd_codes, const uint8_t* wd_scales,
+                             const int32_t* mtile_prefix, const int32_t* poff, void* O,
                              int* status, cudaStream_t st);
 cudaError_t gemm_fwd_down(const Dims& D, const void* H, const void* w_down,
                           const int32_t* mtile_prefix, const int32_t* poff, void* O, int* status,

@@ -47,19 +47,25 @@ __global__ void mx_rows_kernel(const uint4* __restrict__ in, uint4* __restrict__
       v[8 * j + 4] = bf16lo(w.z); v[8 * j + 5] = bf16hi(w.z);
       v[8 * j + 6] = bf16lo(w.w); v[8 * j + 7] = bf16hi(w.w);
     }
-    const int shared = mx_shared_exp(v);
-    mx_fake32(v);
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      out[b * 4 + j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]),
-                                  pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
-                                  pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
-                                  pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
-    if (codes) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) codes[b * 32 + j] = e4m3_code_of(v[j], shared);
+    if (codes || scales) {
+      uint32_t w[8];
+      const uint32_t sbyte = mx_encode32(v, w);
+      if (codes) {
+        uint4* c = reinterpret_cast<uint4*>(codes + b * 32);
+        c[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        c[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+      if (scales) scales[b] = static_cast<uint8_t>(sbyte);
     }
-    if (scales) scales[b] = static_cast<uint8_t>(shared + 127);
+    if (out) {  // NULL: codes and scales only
+      mx_fake32(v);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        out[b * 4 + j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]),
+                                    pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                                    pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                                    pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+    }
   }
 }
 

@@ -53,4 +53,29 @@ __device__ __forceinline__ void mx_fake32(float (&v)[32]) {
   }
 }
 
+// MXFP8 encoding of one 32-value block held by one thread: the E4M3 codes
+// (same rule as mx_fake32: v' = code * 2^shared) into four 32-bit words,
+// codes of v[4i..4i+3] in word i, lowest byte first; returns the E8M0 byte.
+__device__ __forceinline__ uint32_t mx_encode32(const float (&v)[32], uint32_t (&w)[8]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  int shared = -127;
+  if (amax > 0.f) {
+    int e;
+    frexpf(amax, &e);
+    shared = e - 1 - 8;
+    shared = shared < -127 ? -127 : (shared > 127 ? 127 : shared);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    // cvt packs its first operand into the upper byte
+    const uint16_t p01 = cvt_e4m3x2(ldexpf(v[4 * i + 1], -shared), ldexpf(v[4 * i], -shared));
+    const uint16_t p23 =
+        cvt_e4m3x2(ldexpf(v[4 * i + 3], -shared), ldexpf(v[4 * i + 2], -shared));
+    w[i] = static_cast<uint32_t>(p01) | (static_cast<uint32_t>(p23) << 16);
+  }
+  return static_cast<uint32_t>(shared + 127);
+}
+
 }  // namespace mok

@@ -423,4 +423,58 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
       : "memory");
 }
 
+
+// ------------------------------------------------- MXFP8 block-scaled MMA --
+// Instruction descriptor of kind::mxf8f6f4 with block scaling: E4M3 A and B,
+// K-major, UE8M0 scales; sf_id picks the scale byte (K block) of this MMA.
+__device__ __forceinline__ uint32_t idesc_mxf8(int M, int N, uint32_t sf_id) {
+  return (sf_id << 4)                                // B scale id
+         | (0u << 7)                                 // A format: E4M3
+         | (0u << 10)                                // B format: E4M3
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (1u << 23)                                // scale type: UE8M0
+         | (static_cast<uint32_t>(M >> 4) << 24)     // M / 16
+         | (sf_id << 29);                            // A scale id
+}
+
+// Descriptor of a scale block in shared memory: 32 rows of 16 bytes, no
+// swizzle (8-row core matrices 128 bytes apart).
+__device__ __forceinline__ uint64_t smem_desc_sf(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128u >> 4) << 16;  // LBO
+  d |= static_cast<uint64_t>(128u >> 4) << 32;  // SBO
+  d |= static_cast<uint64_t>(1) << 46;          // descriptor version of tcgen05
+  return d;                                     // swizzle mode 0: none
+}
+
+__device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Lane i of the producer warp writes row i of a scale block: the four K-block
+// bytes of rows i, i+32, i+64, i+96 of the tile (scales row-major, ks bytes
+// per row; the tile's first row r0, the stage's first scale column c0).
+__device__ __forceinline__ void gather_sf(uint8_t* dst, const uint8_t* scales, long long ks,
+                                          long long r0, long long c0, int lane) {
+  uint32_t w[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    w[j] = *reinterpret_cast<const uint32_t*>(scales + (r0 + lane + 32 * j) * ks + c0);
+  *reinterpret_cast<uint4*>(dst + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+
 }  // namespace mok
