@@ -92,6 +92,13 @@ struct GemmArgs {
   const float* row_w;       // SWIGLU_BWD: routing weight of each row
   float* dp_part;           // SWIGLU_BWD: [rows, np] partial <dA,h>
   int np;
+  // KGROUP over several row spaces (deferred weight gradients of a micro-
+  // batched backward): segment s of expert e is rows [poff_s[e], poff_s[e+1])
+  // of row space s, poff_s = poff + s*poff_stride, at operand row s*seg_rows.
+  // The K loop runs through the segments in order.  nseg <= 1: one row space.
+  int nseg;
+  int poff_stride;
+  int seg_rows;
   int* status;
 };
 
@@ -192,6 +199,42 @@ __device__ __forceinline__ int total_tiles(const GemmArgs& a) {
   return a.m_tiles * a.n_tiles * (a.k_splits > 1 ? a.k_splits : 1);
 }
 
+// K blocks of expert e over all row spaces of a KGROUP launch.
+__device__ __forceinline__ int kgroup_kb(const GemmArgs& a, int e) {
+  const int ns = a.nseg > 1 ? a.nseg : 1;
+  int n = 0;
+  for (int s = 0; s < ns; ++s) {
+    const int* p = a.poff + static_cast<long long>(s) * a.poff_stride;
+    n += (__ldg(p + e + 1) - __ldg(p + e)) / 64;
+  }
+  return n;
+}
+
+// Walks a KGROUP K loop through its segments: the operand row of K block kb.
+struct SegWalk {
+  int seg, first_kb, nkb, row;
+  __device__ __forceinline__ void load(const GemmArgs& a, int e) {
+    const int* p = a.poff + static_cast<long long>(seg) * a.poff_stride;
+    const int k0 = __ldg(p + e), k1 = __ldg(p + e + 1);
+    nkb = (k1 - k0) / 64;
+    row = seg * a.seg_rows + k0;
+  }
+  __device__ __forceinline__ void init(const GemmArgs& a, int e) {
+    seg = 0;
+    first_kb = 0;
+    load(a, e);
+  }
+  // kb below the expert's total: the loop ends within its segments
+  __device__ __forceinline__ int row_of(const GemmArgs& a, int e, int kb) {
+    while (kb >= first_kb + nkb) {
+      first_kb += nkb;
+      ++seg;
+      load(a, e);
+    }
+    return row + (kb - first_kb) * 64;
+  }
+};
+
 // Tiles of 256 rows for CTA pairs: MGROUP pairs the 128-row tiles of one
 // expert (2j, 2j+1); when an expert has an odd number, the odd CTA of its
 // last pair stages the even CTA's rows again and stores nothing (*valid =
@@ -237,9 +280,8 @@ __device__ __forceinline__ Tile decode_pair(const GemmArgs& a, int t, int rank, 
     tl.n_tile = local / mp;
     tl.m_tile = 2 * (local - tl.n_tile * mp) + rank;
     tl.row0 = tl.m_tile * 128;
-    const int k0 = __ldg(a.poff + e), k1 = __ldg(a.poff + e + 1);
-    tl.k_row0 = k0;
-    tl.num_kb = (k1 - k0) / 64;
+    tl.k_row0 = __ldg(a.poff + e);
+    tl.num_kb = kgroup_kb(a, e);
     tl.kb0 = 0;
     *valid = true;
   }
@@ -276,9 +318,8 @@ __device__ __forceinline__ Tile decode_tile(const GemmArgs& a, int t) {
     tl.n_tile = local / a.m_tiles;
     tl.m_tile = local - tl.n_tile * a.m_tiles;
     tl.row0 = tl.m_tile * 128;
-    const int k0 = __ldg(a.poff + e), k1 = __ldg(a.poff + e + 1);
-    tl.k_row0 = k0;
-    tl.num_kb = (k1 - k0) / 64;
+    tl.k_row0 = __ldg(a.poff + e);
+    tl.num_kb = kgroup_kb(a, e);
     tl.kb0 = 0;
   } else {
     // DENSE: split-K partial products go to separate C blocks (e = split)
@@ -856,7 +897,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = first; t < total && ok; t += step) {
         bool valid;
         const Tile tl = tile_at(t, &valid);
+        SegWalk walk;
+        if (SCHED == SCHED_KGROUP) walk.init(args, tl.e);
         for (int kb = 0; kb < tl.num_kb; ++kb) {
+          // K-grouped: this K block's operand row, through the row spaces
+          const int kgy = SCHED == SCHED_KGROUP ? walk.row_of(args, tl.e, kb) : 0;
           if (!wait(&empty[stage], phase ^ 1u)) {
             ok = false;
             break;
@@ -901,7 +946,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!A_MN) {
             load(sA, &tmA, (tl.kb0 + kb) * KX, tl.row0);
           } else {
-            const int ky = tl.k_row0 + (tl.kb0 + kb) * 64;
+            const int ky = SCHED == SCHED_KGROUP ? kgy : tl.k_row0 + (tl.kb0 + kb) * 64;
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
               load(sA + j * 8192, &tmA, tl.row0 + 64 * j, ky);
@@ -926,7 +971,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else {
             int ky;
-            if (SCHED == SCHED_KGROUP) ky = tl.k_row0 + kb * 64;
+            if (SCHED == SCHED_KGROUP) ky = kgy;
             else if (SCHED == SCHED_DENSE) ky = (tl.kb0 + kb) * 64;
             else ky = tl.e * args.b_group_rows + kb * 64;
             const int x0 = tl.n_tile * BN + rank * C::B_ROWS;
@@ -1446,18 +1491,22 @@ cudaError_t gemm_bwd_gate_up_dgrad(const Dims& D, const void* dGU, const void* w
 static cudaError_t wgrad(const Dims& D, const char* name, const void* A_rows, int64_t M,
                          const void* B_rows, int64_t N, const void* lo_rows, bool lo_is_a,
                          const int32_t* poff, void* out, bool accumulate, int* status,
-                         cudaStream_t st) {
+                         cudaStream_t st, const WgradSegs& sg) {
   // B-split tiles are 128 wide so that four 48 KB stages fit
   const int bn = (!lo_is_a || N % 256 != 0) ? 128 : 256;
+  const int64_t rows = D.rows_max * sg.nseg;  // operand rows of all row spaces
   CUtensorMap ta, tb, tc, tl;
-  if (!make_map(&ta, A_rows, M, D.rows_max, M, 64)) return cudaErrorInvalidValue;
-  if (!make_map(&tb, B_rows, N, D.rows_max, N, 64)) return cudaErrorInvalidValue;
+  if (!make_map(&ta, A_rows, M, rows, M, 64)) return cudaErrorInvalidValue;
+  if (!make_map(&tb, B_rows, N, rows, N, 64)) return cudaErrorInvalidValue;
   if (lo_is_a) {
-    if (!make_map(&tl, lo_rows, M, D.rows_max, M, 64)) return cudaErrorInvalidValue;
+    if (!make_map(&tl, lo_rows, M, rows, M, 64)) return cudaErrorInvalidValue;
   } else {
-    if (!make_map(&tl, lo_rows, N, D.rows_max, N, 64)) return cudaErrorInvalidValue;
+    if (!make_map(&tl, lo_rows, N, rows, N, 64)) return cudaErrorInvalidValue;
   }
   GemmArgs a = blank_args(status);
+  a.nseg = sg.nseg;
+  a.poff_stride = sg.poff_stride;
+  a.seg_rows = (int)D.rows_max;
   a.E = (int)D.E;
   a.m_tiles = (int)(M / 128);
   a.n_tiles = (int)(N / bn);
@@ -1495,20 +1544,24 @@ static cudaError_t wgrad(const Dims& D, const char* name, const void* A_rows, in
 
 cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* P_hi,
                             const void* P_lo, const int32_t* poff, void* dw_down,
-                            bool accumulate, int* status, cudaStream_t st) {
+                            bool accumulate, int* status, cudaStream_t st, const WgradSegs& sg) {
   // dW_down_e [d, I] (+)= dY_e^T [d x rows] * (P_hi + P_lo)_e [rows x I],  P = p h
   if (D.wgrad_bf16 || D.d % 256 != 0)
     return wgrad(D, "bwd_down_wgrad", dY_perm, D.d, P_hi, D.I, P_lo, false, poff, dw_down,
-                 accumulate, status, st);
+                 accumulate, status, st, sg);
   // computed as its transpose, (P_hi + P_lo)_e^T [I x rows] * dY_e [rows x d],
   // so that the hi/lo pair is the A operand and the tile is 128 x 256 like
   // the gate/up wgrad's; the epilogue stores each block transposed
+  const int64_t rows = D.rows_max * sg.nseg;
   CUtensorMap ta, tb, tc, tl;
-  if (!make_map(&ta, P_hi, D.I, D.rows_max, D.I, 64)) return cudaErrorInvalidValue;
-  if (!make_map(&tl, P_lo, D.I, D.rows_max, D.I, 64)) return cudaErrorInvalidValue;
-  if (!make_map(&tb, dY_perm, D.d, D.rows_max, D.d, 64)) return cudaErrorInvalidValue;
+  if (!make_map(&ta, P_hi, D.I, rows, D.I, 64)) return cudaErrorInvalidValue;
+  if (!make_map(&tl, P_lo, D.I, rows, D.I, 64)) return cudaErrorInvalidValue;
+  if (!make_map(&tb, dY_perm, D.d, rows, D.d, 64)) return cudaErrorInvalidValue;
   if (!make_out_map(&tc, dw_down, D.I, D.E * D.d)) return cudaErrorInvalidValue;
   GemmArgs a = blank_args(status);
+  a.nseg = sg.nseg;
+  a.poff_stride = sg.poff_stride;
+  a.seg_rows = (int)D.rows_max;
   a.E = (int)D.E;
   a.m_tiles = (int)(D.I / 128);
   a.n_tiles = (int)(D.d / 256);
@@ -1528,10 +1581,11 @@ cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* P_hi
 
 cudaError_t gemm_wgrad_gate_up(const Dims& D, const void* dGU_hi, const void* dGU_lo,
                                const void* X_perm, const int32_t* poff, void* dw_gate_up,
-                               bool accumulate, int* status, cudaStream_t st) {
+                               bool accumulate, int* status, cudaStream_t st,
+                               const WgradSegs& sg) {
   // dW_gu_e [2I, d] (+)= (dGU_hi + dGU_lo)_e^T [2I x rows] * X_e [rows x d]
   return wgrad(D, "bwd_gate_up_wgrad", dGU_hi, 2 * D.I, X_perm, D.d, dGU_lo, true, poff,
-               dw_gate_up, accumulate, status, st);
+               dw_gate_up, accumulate, status, st, sg);
 }
 
 cudaError_t launch_router_logits(const Dims& D, const void* x, const void* w_router,

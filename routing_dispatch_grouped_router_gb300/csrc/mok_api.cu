@@ -223,14 +223,18 @@ void fwd_layout(const Dims& D, FwdWs* W) {
   W->total = b.o;
 }
 
+// With micro-batches the weight-gradient GEMMs run once after the loop over
+// every micro-batch's rows, so their operands keep one slot per micro-batch
+// (ns slots): dG/dU and p*h hi/lo, and the dY and x operands along the rows.
 void bwd_layout(const Dims& D, BwdWs* W) {
   Bump b;
   const size_t rows = static_cast<size_t>(D.rows_max);
-  W->dy_perm = b.take(rows * D.d * 2);
-  W->dgu_hi = b.take(rows * 2 * D.I * 2);
-  W->dgu_lo = b.take(rows * 2 * D.I * 2);
-  W->p_hi = b.take(rows * D.I * 2);
-  W->p_lo = b.take(rows * D.I * 2);
+  const size_t ns = D.nmb > 1 ? static_cast<size_t>(D.nmb) : 1;
+  W->dy_perm = b.take(rows * D.d * 2 * (D.mx ? 1 : ns));
+  W->dgu_hi = b.take(ns * rows * 2 * D.I * 2);
+  W->dgu_lo = b.take(ns * rows * 2 * D.I * 2);
+  W->p_hi = b.take(ns * rows * D.I * 2);
+  W->p_lo = b.take(ns * rows * D.I * 2);
   W->dp_part = b.take(rows * D.np * 4);
   W->dx_perm = b.take(rows * D.d * 4);  // fp32
   W->dl_row = b.take(rows * 4);
@@ -238,8 +242,10 @@ void bwd_layout(const Dims& D, BwdWs* W) {
   const size_t wgu = static_cast<size_t>(D.E) * 2 * D.I * D.d * 2;
   const size_t wd = static_cast<size_t>(D.E) * D.d * D.I * 2;
   W->dyq_row = D.mx ? b.take(rows * D.d * 2) : 0;  // MXFP8 copies
-  W->dyq_col = D.mx ? b.take(rows * D.d * 2) : 0;
-  W->xq_col = D.mx ? b.take(rows * D.d * 2) : 0;
+  W->dyq_col = D.mx ? b.take(ns * rows * D.d * 2) : 0;
+  W->xq_col = D.mx ? b.take(ns * rows * D.d * 2) : 0;
+  // BF16 with micro-batches: each micro-batch's dispatched x rows
+  W->x_def = (!D.mx && ns > 1) ? b.take(ns * rows * D.d * 2) : 0;
   W->dgu_mx = D.mx ? b.take(rows * 2 * D.I * 2) : 0;
   W->wd_col = D.mx ? b.take(wd) : 0;
   W->wgu_col = D.mx ? b.take(wgu) : 0;
@@ -471,11 +477,25 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
     wgu_op = wgu_q;
   }
   const size_t dx_esz = D.act_bf16 ? 2 : 4;
-  // micro-batches in reverse, so the last ring slots are still resident;
-  // weight gradients accumulate in fp32 in this fixed order
+  // micro-batches in reverse, so the last ring slots are still resident.
+  // With several micro-batches the expert weight gradients are deferred: each
+  // micro-batch leaves its operands in its own slot and one launch per weight
+  // runs K through every micro-batch's rows after the loop (dW written once);
+  // the router gradient still accumulates micro-batch by micro-batch.
+  const bool defer = D.nmb > 1;
+  const size_t rows = static_cast<size_t>(D.rows_max);
+  auto slot = [&](void* base, int i, size_t bytes) {
+    return static_cast<void*>(static_cast<char*>(base) + (defer ? static_cast<size_t>(i) : 0) *
+                                                             bytes);
+  };
   for (int i = D.nmb - 1; i >= 0; --i) {
     const bool first = (i == D.nmb - 1) && !D.accumulate;
     const size_t blk = static_cast<size_t>(i) * L.mb_stride;
+    void* dgu_hi_i = slot(dgu_hi, i, rows * 2 * D.I * 2);
+    void* dgu_lo_i = slot(dgu_lo, i, rows * 2 * D.I * 2);
+    void* p_hi_i = slot(p_hi, i, rows * D.I * 2);
+    void* p_lo_i = slot(p_lo, i, rows * D.I * 2);
+    void* dy_perm_i = D.mx ? dy_perm : slot(dy_perm, i, rows * D.d * 2);
     const char* dyi = static_cast<const char*>(dy) + static_cast<size_t>(i) * D.T * D.d * 2;
     const char* xi = static_cast<const char*>(x) + static_cast<size_t>(i) * D.T * D.d * 2;
     char* dxi = static_cast<char*>(dx) + static_cast<size_t>(i) * D.T * D.d * dx_esz;
@@ -489,7 +509,11 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
     const float* row_w = at<float>(saved, L.row_weight + blk);
     const void* gu = D.recompute_gu ? at<char>(workspace, B.gu) : at<char>(saved, L.gate_up + blk);
     void* x_perm = const_cast<char*>(at<char>(saved, L.x_perm + (i % D.ring) * L.ring_slot_bytes));
-    if (i < D.nmb - D.ring) {
+    if (defer && !D.mx) {
+      // this micro-batch's rows go to its own slot (the deferred wgrad reads them)
+      x_perm = at<char>(workspace, B.x_def) + static_cast<size_t>(i) * rows * D.d * 2;
+      MOK_CUDA(launch_gather_rows(D, xi, ptok, poff, x_perm, status, st));
+    } else if (i < D.nmb - D.ring) {
       // the slot now holds a later micro-batch: dispatch this one again
       MOK_CUDA(launch_gather_rows(D, xi, ptok, poff, x_perm, status, st));
     }
@@ -505,16 +529,16 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
       }
     }
     // reverse-combine: pull dy rows into expert order
-    MOK_CUDA(launch_gather_rows(D, dyi, ptok, poff, dy_perm, status, st));
-    const void* dy_row_op = dy_perm;
-    const void* dy_col_op = dy_perm;
+    MOK_CUDA(launch_gather_rows(D, dyi, ptok, poff, dy_perm_i, status, st));
+    const void* dy_row_op = dy_perm_i;
+    const void* dy_col_op = dy_perm_i;
     const void* x_col_op = x_perm;
     if (D.mx) {
       void* q1 = at<char>(workspace, B.dyq_row);
-      void* q2 = at<char>(workspace, B.dyq_col);
-      void* q3 = at<char>(workspace, B.xq_col);
-      MOK_CUDA(launch_mx_rows(dy_perm, q1, D.rows_max, D.d, nullptr, nullptr, st));
-      MOK_CUDA(launch_mx_cols(dy_perm, q2, D.rows_max, D.d, nullptr, nullptr, st));
+      void* q2 = slot(at<char>(workspace, B.dyq_col), i, rows * D.d * 2);
+      void* q3 = slot(at<char>(workspace, B.xq_col), i, rows * D.d * 2);
+      MOK_CUDA(launch_mx_rows(dy_perm_i, q1, D.rows_max, D.d, nullptr, nullptr, st));
+      MOK_CUDA(launch_mx_cols(dy_perm_i, q2, D.rows_max, D.d, nullptr, nullptr, st));
       MOK_CUDA(launch_mx_cols(x_perm, q3, D.rows_max, D.d, nullptr, nullptr, st));
       dy_row_op = q1;
       dy_col_op = q2;
@@ -523,19 +547,36 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
     // down-projection dgrad + SwiGLU backward + router-weight partials;
     // dG, dU and P = p h leave as bf16 hi/lo pairs (and dG, dU as MXFP8)
     MOK_CUDA(gemm_bwd_down_dgrad(D, dy_row_op, wd_op, mtp, poff, static_cast<const float*>(gu),
-                                 row_w, dgu_hi, dgu_lo, p_hi, p_lo, dgu_mx, dp_part, status, st));
+                                 row_w, dgu_hi_i, dgu_lo_i, p_hi_i, p_lo_i, dgu_mx, dp_part,
+                                 status, st));
     // down-projection wgrad: dW_down_e (+)= dY_e^T (P_hi + P_lo)_e
-    MOK_CUDA(gemm_wgrad_down(D, dy_col_op, p_hi, p_lo, poff, dw_down, !first, status, st));
+    if (!defer)
+      MOK_CUDA(gemm_wgrad_down(D, dy_col_op, p_hi_i, p_lo_i, poff, dw_down, !first, status, st));
     // gate/up dgrad: dX_perm = dGU W_gu (fp32 rows)
-    MOK_CUDA(gemm_bwd_gate_up_dgrad(D, D.mx ? dgu_mx : dgu_hi, wgu_op, mtp, poff, dx_perm, status,
-                                    st));
+    MOK_CUDA(gemm_bwd_gate_up_dgrad(D, D.mx ? dgu_mx : dgu_hi_i, wgu_op, mtp, poff, dx_perm,
+                                    status, st));
     // gate/up wgrad: dW_gu_e (+)= (dGU_hi + dGU_lo)_e^T X_e
-    MOK_CUDA(gemm_wgrad_gate_up(D, dgu_hi, dgu_lo, x_col_op, poff, dw_gate_up, !first, status,
-                                st));
+    if (!defer)
+      MOK_CUDA(gemm_wgrad_gate_up(D, dgu_hi_i, dgu_lo_i, x_col_op, poff, dw_gate_up, !first,
+                                  status, st));
     // reverse-dispatch + router backward
     MOK_CUDA(launch_reverse_dispatch(D, dx_perm, ppos, topk_idx, topk_w, dp_part, w_router, dxi,
                                      dl_row, dl_tok, st));
     MOK_CUDA(launch_router_wgrad(D, x_perm, dl_row, poff, counts, dw_router, !first, st));
+  }
+  if (defer) {
+    // the expert weight gradients over all micro-batches: K runs through
+    // micro-batch 0, 1, ... rows of each expert (offsets one block apart)
+    WgradSegs sg;
+    sg.nseg = D.nmb;
+    sg.poff_stride = static_cast<int>(L.mb_stride / 4);
+    const int32_t* poff0 = at<int32_t>(saved, L.padded_offsets);
+    const void* dy_col = D.mx ? at<char>(workspace, B.dyq_col) : dy_perm;
+    const void* x_col = D.mx ? at<char>(workspace, B.xq_col) : at<char>(workspace, B.x_def);
+    MOK_CUDA(gemm_wgrad_down(D, dy_col, p_hi, p_lo, poff0, dw_down, D.accumulate, status, st,
+                             sg));
+    MOK_CUDA(gemm_wgrad_gate_up(D, dgu_hi, dgu_lo, x_col, poff0, dw_gate_up, D.accumulate, status,
+                                st, sg));
   }
   return MOK_OK;
 }

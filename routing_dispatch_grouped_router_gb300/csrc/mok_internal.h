@@ -63,7 +63,8 @@ struct FwdWs {
 };
 struct BwdWs {
   size_t dy_perm, dgu_hi, dgu_lo, p_hi, p_lo, dp_part, dx_perm, dl_row, dl_tok, dyq_row, dyq_col,
-      xq_col, dgu_mx, wd_col, wgu_col, gu, xq_codes, xq_scales, wgu_codes, wgu_scales, total;
+      xq_col, dgu_mx, wd_col, wgu_col, gu, xq_codes, xq_scales, wgu_codes, wgu_scales, x_def,
+      total;
 };
 struct StageWs {
   size_t status, block_counts, block_base, padded_offsets, mtile_prefix, ppos, ptok, row_w,
@@ -150,12 +151,22 @@ cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* 
 cudaError_t gemm_bwd_gate_up_dgrad(const Dims& D, const void* dGU, const void* w_gate_up,
                                    const int32_t* mtile_prefix, const int32_t* poff,
                                    void* dX_perm, int* status, cudaStream_t st);
+// Weight-gradient GEMMs over nseg row spaces (the micro-batches of a call):
+// operands are [nseg * rows_max, cols] with row space s at rows s*rows_max;
+// row space s has its padded offsets at poff + s*poff_stride.  K runs through
+// the row spaces in order.
+struct WgradSegs {
+  int nseg = 1;
+  int poff_stride = 0;  // int32 elements between successive offset arrays
+};
 cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* P_hi,
                             const void* P_lo, const int32_t* poff, void* dw_down,
-                            bool accumulate, int* status, cudaStream_t st);
+                            bool accumulate, int* status, cudaStream_t st,
+                            const WgradSegs& sg = WgradSegs());
 cudaError_t gemm_wgrad_gate_up(const Dims& D, const void* dGU_hi, const void* dGU_lo,
                                const void* X_perm, const int32_t* poff, void* dw_gate_up,
-                               bool accumulate, int* status, cudaStream_t st);
+                               bool accumulate, int* status, cudaStream_t st,
+                               const WgradSegs& sg = WgradSegs());
 // 2-D TMA map over a row-major [outer, inner] array (row stride row_elems),
 // box {box_inner, box_rows}, zero fill out of bounds.
 bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, int esz, const void* base,
