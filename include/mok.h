@@ -239,7 +239,7 @@ mok_status mok_moe_dispatch_plan_noalloc(const mok_moe_desc* desc, const int32_t
  *            all-zero block),  q = RNE_E4M3(v / 2^shared) saturating at 448.
  * in: bf16 [rows, cols] row-major.  along_rows = 0: blocks of 32 consecutive
  * values of a row (cols % 32 == 0); along_rows = 1: blocks of 32 consecutive
- * rows of a column (rows % 32 == 0).
+ * rows of a column (rows % 32 == 0, cols even).
  * out: bf16 [rows, cols], the dequantised values q * 2^shared (exact in
  * bf16); may equal `in`.  codes: NULL or uint8 [rows, cols] E4M3 codes.
  * scales: NULL or uint8 E8M0 bytes (shared + 127), [rows, cols/32]

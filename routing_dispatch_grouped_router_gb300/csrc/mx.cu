@@ -69,27 +69,43 @@ __global__ void mx_rows_kernel(const uint4* __restrict__ in, uint4* __restrict__
   }
 }
 
-// One thread per (32-row block, column).
-__global__ void mx_cols_kernel(const __nv_bfloat16* __restrict__ in,
-                               __nv_bfloat16* __restrict__ out, uint8_t* __restrict__ codes,
+// One thread per (32-row block, pair of adjacent columns): the two columns'
+// blocks are quantised independently; loads and stores move bf16 pairs.
+__global__ void mx_cols_kernel(const __nv_bfloat162* __restrict__ in,
+                               __nv_bfloat162* __restrict__ out, uint8_t* __restrict__ codes,
                                uint8_t* __restrict__ scales, long long row_blocks, long long cols) {
-  const long long n = row_blocks * cols;
+  const long long cp = cols / 2;  // column pairs
+  const long long n = row_blocks * cp;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
-    const long long rb = i / cols, c = i - rb * cols;
-    const long long base = rb * 32 * cols + c;
-    float v[32];
+    const long long rb = i / cp, c2 = i - rb * cp;
+    const long long base = rb * 32 * cp + c2;
+    float v0[32], v1[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = __bfloat162float(in[base + j * cols]);
-    const int shared = mx_shared_exp(v);
-    mx_fake32(v);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) out[base + j * cols] = __float2bfloat16_rn(v[j]);
-    if (codes) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) codes[base + j * cols] = e4m3_code_of(v[j], shared);
+    for (int j = 0; j < 32; ++j) {
+      const float2 f = __bfloat1622float2(in[base + j * cp]);
+      v0[j] = f.x;
+      v1[j] = f.y;
     }
-    if (scales) scales[rb * cols + c] = static_cast<uint8_t>(shared + 127);
+    const int s0 = mx_shared_exp(v0), s1 = mx_shared_exp(v1);
+    mx_fake32(v0);
+    mx_fake32(v1);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) out[base + j * cp] = __floats2bfloat162_rn(v0[j], v1[j]);
+    const long long c = 2 * c2;
+    if (codes) {
+      const long long cb = rb * 32 * cols + c;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const uint16_t pair = static_cast<uint16_t>(e4m3_code_of(v0[j], s0)) |
+                              (static_cast<uint16_t>(e4m3_code_of(v1[j], s1)) << 8);
+        *reinterpret_cast<uint16_t*>(codes + cb + j * cols) = pair;
+      }
+    }
+    if (scales) {
+      scales[rb * cols + c] = static_cast<uint8_t>(s0 + 127);
+      scales[rb * cols + c + 1] = static_cast<uint8_t>(s1 + 127);
+    }
   }
 }
 
@@ -113,11 +129,11 @@ cudaError_t launch_mx_rows(const void* in, void* out, long long rows, long long 
 
 cudaError_t launch_mx_cols(const void* in, void* out, long long rows, long long cols,
                            uint8_t* codes, uint8_t* scales, cudaStream_t st) {
-  const long long n = (rows / 32) * cols;
+  const long long n = (rows / 32) * (cols / 2);
   if (n == 0) return cudaSuccess;
   ProfScope prof("mx_quant_cols", st);
-  mx_cols_kernel<<<grid_for(n, 256), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(in),
-                                                   static_cast<__nv_bfloat16*>(out), codes,
+  mx_cols_kernel<<<grid_for(n, 256), 256, 0, st>>>(static_cast<const __nv_bfloat162*>(in),
+                                                   static_cast<__nv_bfloat162*>(out), codes,
                                                    scales, rows / 32, cols);
   count_launch();
   return cudaGetLastError();
@@ -132,7 +148,7 @@ extern "C" mok_status mok_mx_quantize(const void* in, int64_t rows, int64_t cols
   if (rows < 0 || cols < 0 || (rows * cols > 0 && (!in || !out))) return MOK_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 15u)
     return MOK_ERR_INVALID_ARG;
-  if (along_rows ? (rows % 32) : (cols % 32)) return MOK_ERR_UNSUPPORTED;
+  if (along_rows ? (rows % 32 || cols % 2) : (cols % 32)) return MOK_ERR_UNSUPPORTED;
   const mok_status s = mok_check_device();
   if (s != MOK_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
