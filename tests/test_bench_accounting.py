@@ -1,0 +1,50 @@
+"""bench.py's per-launch accounting: the algorithmic FLOP of each grouped GEMM
+and the bytes of each data-movement kernel, with and without micro-batches."""
+import pytest
+
+import bench
+from routing_dispatch_grouped_router_gb300 import inputs as gen
+
+
+def test_gemm_flops_fine():
+    s = gen.workload_shape("fine")
+    f = bench.gemm_flops(s)
+    R, d, I = s.T * s.k, s.d, s.I
+    assert f["fwd_gate_up_swiglu"] == 2 * R * d * 2 * I == pytest.approx(274.9e9, rel=1e-3)
+    assert f["fwd_down"] == f["bwd_down_dgrad_swiglu"] == f["bwd_down_wgrad"] == 2 * R * d * I
+    assert f["bwd_gate_up_dgrad"] == f["bwd_gate_up_wgrad"] == 2 * R * d * 2 * I
+    # the step's expert GEMMs: 18 R d I
+    total = sum(v for n, v in f.items() if n != "router_logits")
+    assert total == 18 * R * d * I
+
+
+def test_micro_batches_divide_the_work_of_a_launch():
+    s = gen.workload_shape("mxfp8")
+    nmb = s.T // gen.WORKLOADS["mxfp8"]["mb_tokens"]
+    whole, part = bench.gemm_flops(s), bench.gemm_flops(s, nmb)
+    for n in whole:
+        assert part[n] * nmb == pytest.approx(whole[n])
+    mw, mp = bench.mover_bytes(s), bench.mover_bytes(s, nmb)
+    for n in ("gather_rows", "combine"):
+        assert mp[n] * nmb == pytest.approx(mw[n], rel=1e-9)
+
+
+def test_mover_bytes_follow_the_fp32_row_layout():
+    s = gen.workload_shape("fine")
+    m = bench.mover_bytes(s)
+    R, T, d = s.T * s.k, s.T, s.d
+    assert m["combine"] == R * d * 4 + T * d * 4 + R * 8
+    assert m["gather_rows"] == 2 * R * d * 2 + R * 4
+
+
+def test_workload_options():
+    class FakeApi:
+        MXFP8 = 1
+    bench.WORKLOAD = "mxfp8"
+    try:
+        opts = bench.layer_options(FakeApi)
+        assert opts == dict(dtype=1, mb_tokens=2048, ring_slots=2)
+        assert "MXFP8" in bench.workload_config(gen.workload_shape("mxfp8"))["workload"]
+    finally:
+        bench.WORKLOAD = "fine"
+    assert bench.layer_options(FakeApi) == {}
