@@ -263,11 +263,13 @@ mok_status mok_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int a_m
  * A: uint8 [M,K] E4M3 codes, sa: uint8 [M,K/32] E8M0 scale bytes; B, sb the
  * same for [N,K]; C: fp32 [M,N] (fp32 accumulation).  This is the layout
  * mok_mx_quantize writes with along_rows = 0.  M, N, K multiples of 128;
- * A, B, C 16-byte aligned, sa, sb 4-byte aligned.  workspace >= 256 bytes
- * (status word). */
+ * A, B, C 16-byte aligned, sa, sb 4-byte aligned.  cta_pair = 0: 128 x 128
+ * tiles on single CTAs; 1: 256 x 256 tiles on clusters of two CTAs
+ * (tcgen05.mma.cta_group::2; M, N multiples of 256).  Both accumulate every
+ * element over the same K sequence.  workspace >= 256 bytes (status word). */
 mok_status mok_gemm_mxfp8(int64_t M, int64_t N, int64_t K, const uint8_t* A, const uint8_t* sa,
-                          const uint8_t* B, const uint8_t* sb, float* C, void* workspace,
-                          size_t ws_bytes, void* stream);
+                          const uint8_t* B, const uint8_t* sb, float* C, int cta_pair,
+                          void* workspace, size_t ws_bytes, void* stream);
 
 /* Failure-path self-test: enqueues one CTA that waits on an mbarrier phase
  * nothing completes.  The wait is the bounded one every GEMM uses: it gives

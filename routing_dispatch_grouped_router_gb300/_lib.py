@@ -53,7 +53,7 @@ _SIGS = {
     "mok_gemm_bf16": (c_int32, [c_int64, c_int64, c_int64, c_void_p, c_int32, c_void_p, c_int32,
                                 c_void_p, c_void_p, c_size_t, c_void_p]),
     "mok_gemm_mxfp8": (c_int32, [c_int64, c_int64, c_int64, c_void_p, c_void_p, c_void_p,
-                                 c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+                                 c_void_p, c_void_p, c_int32, c_void_p, c_size_t, c_void_p]),
     "mok_selftest_bounded_wait": (c_int32, [c_void_p, c_size_t, c_void_p]),
     "mok_get_device_status": (c_int32, [c_void_p, c_void_p, ctypes.POINTER(c_int32)]),
     "mok_status_string": (ctypes.c_char_p, [c_int32]),

@@ -105,14 +105,15 @@ def gemm_bf16(A, a_mn_major, B, b_mn_major, C, workspace, stream=None):
                "mok_gemm_bf16")
 
 
-def gemm_mxfp8(A, sa, B, sb, C, workspace, stream=None):
+def gemm_mxfp8(A, sa, B, sb, C, workspace, cta_pair=False, stream=None):
     """C[M,N] fp32 = dequant(A) dequant(B)^T for E4M3 codes A [M,K], B [N,K]
     and E8M0 scale bytes sa [M,K/32], sb [N,K/32] (see mok_gemm_mxfp8)."""
     lib = _lib.load()
     M, N = C.shape
     K = A.shape[1]
     _lib.check(lib.mok_gemm_mxfp8(M, N, K, _ptr(A), _ptr(sa), _ptr(B), _ptr(sb), _ptr(C),
-                                  _ptr(workspace), workspace.numel(), _stream(stream)),
+                                  int(cta_pair), _ptr(workspace), workspace.numel(),
+                                  _stream(stream)),
                "mok_gemm_mxfp8")
 
 

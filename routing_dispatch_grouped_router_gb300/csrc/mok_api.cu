@@ -674,11 +674,12 @@ mok_status mok_gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int a_m
 }
 
 mok_status mok_gemm_mxfp8(int64_t M, int64_t N, int64_t K, const uint8_t* A, const uint8_t* sa,
-                          const uint8_t* B, const uint8_t* sb, float* C, void* workspace,
-                          size_t ws_bytes, void* stream) {
+                          const uint8_t* B, const uint8_t* sb, float* C, int cta_pair,
+                          void* workspace, size_t ws_bytes, void* stream) {
   if (M <= 0 || N <= 0 || K <= 0 || !A || !sa || !B || !sb || !C || !workspace)
     return MOK_ERR_INVALID_ARG;
   if (M % 128 || N % 128 || K % 128) return MOK_ERR_UNSUPPORTED;
+  if (cta_pair && (M % 256 || N % 256)) return MOK_ERR_UNSUPPORTED;
   if (M > (1 << 24) || N > (1 << 24) || K > (1 << 24)) return MOK_ERR_UNSUPPORTED;
   if (!aligned16(A) || !aligned16(B) || !aligned16(C) || !aligned16(workspace) ||
       (reinterpret_cast<uintptr_t>(sa) & 3u) || (reinterpret_cast<uintptr_t>(sb) & 3u))
@@ -689,7 +690,7 @@ mok_status mok_gemm_mxfp8(int64_t M, int64_t N, int64_t K, const uint8_t* A, con
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* status = static_cast<int*>(workspace);
   MOK_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
-  MOK_CUDA(gemm_dense_mxfp8(M, N, K, A, sa, B, sb, C, status, st));
+  MOK_CUDA(gemm_dense_mxfp8(M, N, K, A, sa, B, sb, C, cta_pair != 0, status, st));
   return MOK_OK;
 }
 

@@ -176,7 +176,7 @@ bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, int esz, const v
 // one E8M0 scale byte per 32 consecutive K values) on block-scaled tcgen05.
 cudaError_t gemm_dense_mxfp8(int64_t M, int64_t N, int64_t K, const uint8_t* A,
                              const uint8_t* A_scales, const uint8_t* B, const uint8_t* B_scales,
-                             float* C, int* status, cudaStream_t st);
+                             float* C, bool cta_pair, int* status, cudaStream_t st);
 cudaError_t gemm_dense_bf16(int64_t M, int64_t N, int64_t K, const void* A, bool a_mn,
                             const void* B, bool b_mn, void* C, int* status, cudaStream_t st);
 

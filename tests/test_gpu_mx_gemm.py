@@ -18,19 +18,20 @@ pytestmark = pytest.mark.gpu
 E4M3_ONE = 0x38  # sign 0, exponent 7 (bias 7), mantissa 0
 
 
-def _run(codes_a, sc_a, codes_b, sc_b):
+def _run(codes_a, sc_a, codes_b, sc_b, pair=False):
     M, K = codes_a.shape
     N = codes_b.shape[0]
     dev = [torch.from_numpy(np.ascontiguousarray(a)).cuda() for a in (codes_a, sc_a, codes_b, sc_b)]
     C = torch.empty(M, N, dtype=torch.float32, device="cuda")
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
-    api.gemm_mxfp8(*dev, C, ws)
+    api.gemm_mxfp8(*dev, C, ws, cta_pair=pair)
     assert api.device_status(ws) == 0
     return C.cpu().numpy().astype(np.float64)
 
 
+@pytest.mark.parametrize("pair", [False, True])
 @pytest.mark.parametrize("pattern", ["rows", "cols", "kblocks", "mixed"])
-def test_mxfp8_gemm_scale_placement(pattern):
+def test_mxfp8_gemm_scale_placement(pattern, pair):
     M, N, K = 256, 256, 512
     kb = K // 32
     rng = np.random.default_rng(11)
@@ -48,7 +49,7 @@ def test_mxfp8_gemm_scale_placement(pattern):
         sb = rng.integers(115, 135, (N, kb)).astype(np.uint8)
     ca = np.full((M, K), E4M3_ONE, np.uint8)
     cb = np.full((N, K), E4M3_ONE, np.uint8)
-    got = _run(ca, sa, cb, sb)
+    got = _run(ca, sa, cb, sb, pair)
     ref = 32.0 * (2.0 ** (sa.astype(np.float64) - 127)) @ (2.0 ** (sb.astype(np.float64) - 127)).T
     # every term is positive, so fp32 accumulation of the K/32 block sums is
     # within (K/32) * 2^-24 * ref (plus rounding slack); a scale byte read from
@@ -56,8 +57,10 @@ def test_mxfp8_gemm_scale_placement(pattern):
     np.testing.assert_allclose(got, ref, rtol=2e-5, atol=0)
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 384, 1024), (512, 256, 2048)])
-def test_mxfp8_gemm_matches_dequantised_product(M, N, K):
+@pytest.mark.parametrize("M,N,K,pair", [(128, 128, 128, False), (256, 384, 1024, False),
+                                        (512, 256, 2048, False), (256, 256, 128, True),
+                                        (512, 768, 1024, True)])
+def test_mxfp8_gemm_matches_dequantised_product(M, N, K, pair):
     rng = np.random.default_rng(M + N + K)
     a = rng.standard_normal((M, K)).astype(np.float32) * np.exp(rng.uniform(-3, 3, (M, 1)))
     b = rng.standard_normal((N, K)).astype(np.float32) * np.exp(rng.uniform(-3, 3, (N, 1)))
@@ -70,7 +73,7 @@ def test_mxfp8_gemm_matches_dequantised_product(M, N, K):
         api.mx_quantize(x, False, codes=codes, scales=scales)
         deq, _ = oracle.mx_quantize(gen.bf16_bits_to_f32(bits).astype(np.float64), axis=1)
         out[name] = (codes.cpu().numpy(), scales.cpu().numpy(), deq)
-    got = _run(out["a"][0], out["a"][1], out["b"][0], out["b"][1])
+    got = _run(out["a"][0], out["a"][1], out["b"][0], out["b"][1], pair)
     ref = out["a"][2] @ out["b"][2].T
     scale = np.abs(out["a"][2]) @ np.abs(out["b"][2]).T
     # fp32 accumulation: each entry within a few ulps of its absolute sum
