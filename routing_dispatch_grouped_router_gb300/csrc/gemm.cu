@@ -147,8 +147,14 @@ struct Cfg {
   // SPLIT_MX: 128-row x 128-byte code tiles (the bf16 tile sizes) and the two
   // 512-byte scale blocks of the stage (A's 128 rows, B's 128 rows)
   static constexpr int SF_OFF = A_TILES * A_BYTES + B_TILES * B_BYTES;
-  static constexpr int SF_BYTES = SPLIT == SPLIT_MX ? 1024 : 0;
-  static constexpr int STAGE_BYTES = SF_OFF + SF_BYTES;
+  // (CTA pairs: the CTA's 128 A rows, and all 256 B rows of the pair's tile)
+  static constexpr int SF_BYTES = SPLIT != SPLIT_MX ? 0 : (PAIR ? 1536 : 1024);
+  static constexpr int STAGE_BYTES =
+      SPLIT == SPLIT_MX ? (SF_OFF + SF_BYTES + 1023) / 1024 * 1024 : SF_OFF;
+  // accumulators; MXFP8 pairs keep one (256 columns) so that the stages'
+  // scale columns fit beside it (12 per stage: 4 for A, 8 for B)
+  static constexpr int NACC = (SPLIT == SPLIT_MX && PAIR) ? 1 : 2;
+  static constexpr int SF_COLS = SPLIT != SPLIT_MX ? 0 : (PAIR ? 12 : 8);
   static constexpr int BAR_BYTES = 512;
   static constexpr int STAGE_ROOM = 232448 - 1024 - BAR_BYTES - kEpiWarps * STG;
   static constexpr int STAGES = (STAGE_ROOM / STAGE_BYTES) < 6 ? (STAGE_ROOM / STAGE_BYTES) : 6;
@@ -174,6 +180,10 @@ static_assert(Cfg<256, SPLIT_NONE, false, kSwigluBwdStaging>::STAGES >= 2 &&
 static_assert(Cfg<128, SPLIT_MX>::STAGES == 5 && Cfg<128, SPLIT_MX>::STAGE_BYTES % 1024 == 0 &&
                   2 * 128 + 8 * Cfg<128, SPLIT_MX>::STAGES <= 512,
               "MXFP8 stages");
+static_assert(Cfg<256, SPLIT_MX, true>::STAGES == 5 &&
+                  Cfg<256, SPLIT_MX, true>::STAGE_BYTES % 1024 == 0 &&
+                  256 + 12 * Cfg<256, SPLIT_MX, true>::STAGES <= 512,
+              "MXFP8 pair stages");
 static_assert(Cfg<256, SPLIT_NONE, true, 2 * kStagingBytes>::STAGES == 5 &&
                   Cfg<256, SPLIT_NONE, false, 2 * kStagingBytes>::STAGES == 3 &&
                   Cfg<128, SPLIT_NONE, false, 2 * kStagingBytes>::STAGES == 5,
@@ -554,7 +564,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
         }
       }
     }
-  } else if (EPI == EPI_SWIGLU_FWD && SPLIT == SPLIT_MX) {
+  } else if (EPI == EPI_SWIGLU_FWD && SPLIT == SPLIT_MX && BN == 128) {
     // BN = 128: accumulator columns [0,64) gate, [64,128) up, for FFN columns
     // n0 .. n0+63 (n0 = n_tile*64); this warp: 32 of them, one MX block of h
     const long long r = tl.row0 + row_in_tile;
@@ -599,15 +609,25 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
       float g[32], u[32];
       tmem_ld32(taddr + half * 64 + c, g);
       tmem_ld32(taddr + 128 + half * 64 + c, u);
-      if (a.out2) {
+      if (SPLIT == SPLIT_MX ? a.h_codes != nullptr : a.out2 != nullptr) {
         float hv[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           float s;
           hv[j] = silu_f(g[j], &s) * u[j];
         }
-        if (a.mx) mx_fake32(hv);  // one MX block: 32 consecutive columns of a row
-        store_bf16x32(h + n0 + c, hv);
+        if (SPLIT == SPLIT_MX) {
+          // MXFP8 operand of the down projection: one block of 32 columns
+          uint32_t w[8];
+          const uint32_t sbyte = mx_encode32(hv, w);
+          uint4* cp = reinterpret_cast<uint4*>(a.h_codes + r * I + n0 + c);
+          cp[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          cp[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          a.h_scales[r * (I / 32) + (n0 + c) / 32] = static_cast<uint8_t>(sbyte);
+        } else {
+          if (a.mx) mx_fake32(hv);  // one MX block: 32 consecutive columns of a row
+          store_bf16x32(h + n0 + c, hv);
+        }
       }
       if (a.store_c) {
         stage_and_store_f32<DBUF>(stage_buf, nst, tmC, g, lane, n0 + c, y, false,
@@ -797,10 +817,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ GemmArgs args, const __grid_constant__ OutMaps om) {
   using C = Cfg<BN, SPLIT, PAIR, staging_bytes<EPI, SPLIT, SCHED>()>;
   constexpr bool kDbuf = dbuf_store<EPI, SPLIT, SCHED>();
-  static_assert(!PAIR || (SCHED != SCHED_DENSE && SPLIT != SPLIT_B && SPLIT != SPLIT_MX &&
-                          BN == 256), "pair");
-  static_assert(SPLIT != SPLIT_MX || (!A_MN && !B_MN && BN == 128 && SCHED == SCHED_MGROUP),
-                "MXFP8 operands: K-major, single CTA, 128-wide tiles");
+  static_assert(!PAIR || (SCHED != SCHED_DENSE && SPLIT != SPLIT_B && BN == 256), "pair");
+  static_assert(SPLIT != SPLIT_MX ||
+                    (!A_MN && !B_MN && BN == (PAIR ? 256 : 128) && SCHED == SCHED_MGROUP),
+                "MXFP8 operands: K-major, 128-wide tiles (256 on CTA pairs)");
   constexpr int KX = SPLIT == SPLIT_MX ? 128 : 64;  // K values per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -829,7 +849,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      // MXFP8 pairs: the leader's armed arrival and the peer's scales-ready one
+      mbar_init(&full[s], (PAIR && SPLIT == SPLIT_MX) ? 2 : 1);
       mbar_init(&empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -914,21 +935,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (SWIGLU_FWD: 64 gate rows, then the matching 64 up rows)
             gather_sf(sA + C::SF_OFF, args.sa, args.ks, tl.row0, (long long)(tl.kb0 + kb) * 4,
                       lane);
-            uint32_t w[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int t = lane + 32 * j;  // row of the B tile
-              long long grow;
-              if (EPI == EPI_SWIGLU_FWD)
-                grow = (long long)tl.e * args.b_group_rows + tl.n_tile * (BN / 2) +
-                       (t < BN / 2 ? t : args.I + t - BN / 2);
-              else
-                grow = (long long)tl.e * args.b_group_rows + tl.n_tile * BN + t;
-              w[j] = *reinterpret_cast<const uint32_t*>(args.sb + grow * args.ks +
-                                                        (long long)(tl.kb0 + kb) * 4);
+            for (int blk = 0; blk < BN / 128; ++blk) {  // all BN rows of the tile's B
+              uint32_t w[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int t = blk * 128 + lane + 32 * j;  // row of the B tile
+                long long grow;
+                if (EPI == EPI_SWIGLU_FWD)
+                  grow = (long long)tl.e * args.b_group_rows + tl.n_tile * (BN / 2) +
+                         (t < BN / 2 ? t : args.I + t - BN / 2);
+                else
+                  grow = (long long)tl.e * args.b_group_rows + tl.n_tile * BN + t;
+                w[j] = *reinterpret_cast<const uint32_t*>(args.sb + grow * args.ks +
+                                                          (long long)(tl.kb0 + kb) * 4);
+              }
+              *reinterpret_cast<uint4*>(sA + C::SF_OFF + 512 + blk * 512 + lane * 16) =
+                  make_uint4(w[0], w[1], w[2], w[3]);
             }
-            *reinterpret_cast<uint4*>(sA + C::SF_OFF + 512 + lane * 16) =
-                make_uint4(w[0], w[1], w[2], w[3]);
             fence_proxy_async_smem();  // read by tcgen05.cp through the async proxy
             __syncwarp();
           }
@@ -937,10 +961,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (PAIR) tma_load_2d_pair(dst, tm, bar_c, x, y);
             else tma_load_2d(dst, tm, &full[stage], x, y);
           };
+          // the stage's TMA bytes (the code or bf16 tiles: SF_OFF)
           if (!PAIR) {
-            if (lane == 0) mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES - C::SF_BYTES);
+            if (lane == 0) mbar_arrive_expect_tx(&full[stage], C::SF_OFF);
           } else if (leader) {
-            mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+            if (lane == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::SF_OFF);
           }
           // A tile: 128 rows (M) x 64 (K)  (+ its lo tile with SPLIT_A)
           if (!A_MN) {
@@ -981,6 +1006,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (SPLIT == SPLIT_B) load(sB + C::B_BYTES + j * 8192, &tmL, x0 + 64 * j, ky);
             }
           }
+          // MXFP8 pair: this CTA's scale blocks are written (the leader's
+          // tcgen05.cp reads them from here)
+          if (PAIR && SPLIT == SPLIT_MX && !leader && lane == 0) mbar_arrive_cluster(bar_c);
           issued_par[stage] = static_cast<int>(phase);
           if (++stage == C::STAGES) {
             stage = 0;
@@ -1026,8 +1054,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = first; t < total && ok; t += step, ++it) {
         bool valid;
         const Tile tl = tile_at(t, &valid);
-        const int acc = it & 1;
-        const uint32_t acc_par = static_cast<uint32_t>((it >> 1) & 1);
+        const int acc = C::NACC == 2 ? (it & 1) : 0;
+        const uint32_t acc_par = static_cast<uint32_t>(C::NACC == 2 ? ((it >> 1) & 1) : (it & 1));
         if (!wait(&tempty[acc], acc_par ^ 1u)) {
           ok = false;
           break;
@@ -1043,17 +1071,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a_base = smem_addr(tiles + stage * C::STAGE_BYTES);
           const uint32_t b_base = a_base + C::B_OFF;
           if (SPLIT == SPLIT_MX) {
-            // scales to TMEM (8 columns per stage after the accumulators),
-            // then four K=32 block-scaled MMAs, scale byte j each
-            const uint32_t sfa = tmem_base + 2u * BN + 8u * stage;
-            tmem_cp_sf(sfa, smem_desc_sf(a_base + C::SF_OFF));
-            tmem_cp_sf(sfa + 4u, smem_desc_sf(a_base + C::SF_OFF + 512));
+            // scales to TMEM (SF_COLS columns per stage after the
+            // accumulators), then four K=32 block-scaled MMAs, scale byte j
+            // each; CTA pairs copy each CTA's blocks to its own TMEM
+            const uint32_t sfa = tmem_base + C::NACC * BN + C::SF_COLS * stage;
+            if (PAIR) {
+              tmem_cp_sf_pair(sfa, smem_desc_sf(a_base + C::SF_OFF));
+              tmem_cp_sf_pair(sfa + 4u, smem_desc_sf(a_base + C::SF_OFF + 512));
+              tmem_cp_sf_pair(sfa + 8u, smem_desc_sf(a_base + C::SF_OFF + 1024));
+            } else {
+              tmem_cp_sf(sfa, smem_desc_sf(a_base + C::SF_OFF));
+              tmem_cp_sf(sfa + 4u, smem_desc_sf(a_base + C::SF_OFF + 512));
+            }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const uint64_t ad = smem_desc_sw128(a_base + j * 32, 16, 1024);
               const uint64_t bd = smem_desc_sw128(b_base + j * 32, 16, 1024);
-              mma_mxf8(d_tmem, ad, bd, idesc_mxf8(128, BN, static_cast<uint32_t>(j)), sfa,
-                       sfa + 4u, (kb | j) != 0 ? 1u : 0u);
+              const uint32_t id = idesc_mxf8(PAIR ? 256 : 128, BN, static_cast<uint32_t>(j));
+              if (PAIR)
+                mma_mxf8_pair(d_tmem, ad, bd, id, sfa, sfa + 4u, (kb | j) != 0 ? 1u : 0u);
+              else
+                mma_mxf8(d_tmem, ad, bd, id, sfa, sfa + 4u, (kb | j) != 0 ? 1u : 0u);
             }
             commit(&empty[stage]);
             if (++stage == C::STAGES) {
@@ -1109,8 +1147,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = first; t < total; t += step, ++it) {
       bool valid;
       const Tile tl = tile_at(t, &valid);
-      const int acc = it & 1;
-      const uint32_t acc_par = static_cast<uint32_t>((it >> 1) & 1);
+      const int acc = C::NACC == 2 ? (it & 1) : 0;
+      const uint32_t acc_par = static_cast<uint32_t>(C::NACC == 2 ? ((it >> 1) & 1) : (it & 1));
       // the tile's first g, u chunk does not depend on the accumulator
       if (gu_tma && valid)
         gu_issue<BN>(args, tl, q, lane, half, 0, stage_buf, wbar, gu_chunks, &tmC);
@@ -1321,9 +1359,10 @@ cudaError_t gemm_fwd_gate_up_mx(const Dims& D, const uint8_t* x_codes, const uin
                                 cudaStream_t st) {
   const auto u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  const bool pair = D.pair;  // 256-wide tiles (128 FFN columns) on CTA pairs
   CUtensorMap ta, tb, tc;
   if (!make_map_t(&ta, u8, 1, x_codes, D.d, D.rows_max, D.d, 128, 128, sw) ||
-      !make_map_t(&tb, u8, 1, wgu_codes, D.d, D.E * 2 * D.I, D.d, 128, 64, sw))
+      !make_map_t(&tb, u8, 1, wgu_codes, D.d, D.E * 2 * D.I, D.d, 128, pair ? 128 : 64, sw))
     return cudaErrorInvalidValue;
   if (GU ? !make_out_map(&tc, GU, 2 * D.I, D.rows_max) : false) return cudaErrorInvalidValue;
   if (!GU) tc = ta;  // never used without GU; a valid map for the prefetch
@@ -1344,6 +1383,11 @@ cudaError_t gemm_fwd_gate_up_mx(const Dims& D, const uint8_t* x_codes, const uin
   a.ks = (int)(D.d / 32);
   a.h_codes = h_codes;
   a.h_scales = h_scales;
+  if (pair) {
+    a.n_tiles = (int)(D.I / 128);
+    return launch<256, false, false, SCHED_MGROUP, EPI_SWIGLU_FWD, SPLIT_MX, true>(
+        "fwd_gate_up_swiglu", ta, tb, tc, a, max_mpairs(D) * a.n_tiles, st);
+  }
   return launch<128, false, false, SCHED_MGROUP, EPI_SWIGLU_FWD, SPLIT_MX>(
       "fwd_gate_up_swiglu", ta, tb, tc, a, max_mtiles(D) * a.n_tiles, st);
 }
@@ -1371,6 +1415,11 @@ cudaError_t gemm_fwd_down_mx(const Dims& D, const uint8_t* h_codes, const uint8_
   a.sa = h_scales;
   a.sb = wd_scales;
   a.ks = (int)(D.I / 32);
+  if (D.pair && D.d % 256 == 0) {
+    a.n_tiles = (int)(D.d / 256);
+    return launch<256, false, false, SCHED_MGROUP, EPI_F32, SPLIT_MX, true>(
+        "fwd_down", ta, tb, tc, a, max_mpairs(D) * a.n_tiles, st);
+  }
   return launch<128, false, false, SCHED_MGROUP, EPI_F32, SPLIT_MX>(
       "fwd_down", ta, tb, tc, a, max_mtiles(D) * a.n_tiles, st);
 }
