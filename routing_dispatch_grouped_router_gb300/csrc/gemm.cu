@@ -79,11 +79,11 @@ struct GemmArgs {
   void* out4;               // SWIGLU_BWD: P_lo [rows,I]
   void* out5;               // SWIGLU_BWD with mx: MXFP8 dGU [rows,2I] (dgrad operand)
   int mx;                   // SwiGLU epilogues: quantise the derived GEMM operands to MXFP8
-  const uint8_t* sa;        // SPLIT_MX: A scale bytes, row-major [rows of A, K/32]
-  const uint8_t* sb;        // SPLIT_MX: B scale bytes, row-major [rows of B, K/32]
+  const uint8_t* sa;        // SPLIT_MX: A scale bytes, tiled layout (mx_tiled_off)
+  const uint8_t* sb;        // SPLIT_MX: B scale bytes, tiled layout
   int ks;                   // SPLIT_MX: K / 32 (scale bytes per row)
   uint8_t* h_codes;         // SWIGLU_FWD with SPLIT_MX: h as E4M3 codes [rows, I] (NULL: none)
-  uint8_t* h_scales;        // ... and its E8M0 bytes [rows, I/32]
+  uint8_t* h_scales;        // ... and its E8M0 bytes (tiled layout, mx_tiled_off)
   int accumulate;           // fp32 TMA-store epilogue: add into C instead of overwriting
   int store_c;              // SWIGLU_FWD: write g, u through the C map
   int evict_first;          // TMA-store epilogues: C is not read again soon (L2 evict-first)
@@ -104,8 +104,11 @@ struct GemmArgs {
 
 // Extra output maps: the SwiGLU backward stores dG/dU (hi, lo) and p*h (hi,
 // lo) through TMA, boxes of 32 rows x 16 bf16 columns.
+// MXFP8 on CTA pairs: the A and B scales (tiled layout) viewed as rows of 256
+// bytes, one 512-byte block = 2 rows.
 struct OutMaps {
   CUtensorMap dgu_hi, dgu_lo, p_hi, p_lo;
+  CUtensorMap sfa, sfb;
 };
 
 constexpr int kThreads = 320;
@@ -587,7 +590,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
       uint4* cp = reinterpret_cast<uint4*>(a.h_codes + r * I + n0);
       cp[0] = make_uint4(w[0], w[1], w[2], w[3]);
       cp[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      a.h_scales[r * (I / 32) + n0 / 32] = static_cast<uint8_t>(sbyte);
+      a.h_scales[mx_tiled_off(r, n0 / 32, I / 128)] = static_cast<uint8_t>(sbyte);
     }
     if (a.store_c) {
       stage_and_store_f32<DBUF>(stage_buf, nst, tmC, g, lane, n0, y, false, a.evict_first != 0);
@@ -623,7 +626,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
           uint4* cp = reinterpret_cast<uint4*>(a.h_codes + r * I + n0 + c);
           cp[0] = make_uint4(w[0], w[1], w[2], w[3]);
           cp[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          a.h_scales[r * (I / 32) + (n0 + c) / 32] = static_cast<uint8_t>(sbyte);
+          a.h_scales[mx_tiled_off(r, (n0 + c) / 32, I / 128)] = static_cast<uint8_t>(sbyte);
         } else {
           if (a.mx) mx_fake32(hv);  // one MX block: 32 consecutive columns of a row
           store_bf16x32(h + n0 + c, hv);
@@ -849,8 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      // MXFP8 pairs: the leader's armed arrival and the peer's scales-ready one
-      mbar_init(&full[s], (PAIR && SPLIT == SPLIT_MX) ? 2 : 1);
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -868,6 +870,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (kTmaStore) tma_prefetch_desc(&tmC);
+    if (SPLIT == SPLIT_MX && PAIR) {
+      tma_prefetch_desc(&om.sfa);
+      tma_prefetch_desc(&om.sfb);
+    }
     if (EPI == EPI_SWIGLU_BWD && !args.mx) {
       tma_prefetch_desc(&om.dgu_hi);
       tma_prefetch_desc(&om.dgu_lo);
@@ -903,8 +909,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (warp == 0) {
-    // SPLIT_MX: every lane gathers scale bytes; lane 0 alone issues the TMA
-    if (lane == 0 || SPLIT == SPLIT_MX) {
+    // single-CTA SPLIT_MX: every lane gathers scale bytes; lane 0 alone
+    // issues the TMA (CTA pairs load the scale blocks by TMA as well)
+    if (lane == 0 || (SPLIT == SPLIT_MX && !PAIR)) {
       // ------------------------------------------------------- producer --
       // PAIR: both CTAs load their halves; the copies complete on the
       // leader's `full` barrier, which the leader arms for both
@@ -930,29 +937,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sA = tiles + stage * C::STAGE_BYTES;
           uint8_t* sB = sA + C::B_OFF;
           const uint32_t bar_c = full_leader + 8u * stage;
-          if (SPLIT == SPLIT_MX) {
-            // the stage's scale blocks: A rows row0.., then the B tile's rows
-            // (SWIGLU_FWD: 64 gate rows, then the matching 64 up rows)
-            gather_sf(sA + C::SF_OFF, args.sa, args.ks, tl.row0, (long long)(tl.kb0 + kb) * 4,
-                      lane);
+          if (SPLIT == SPLIT_MX && !PAIR) {
+            // the stage's scale blocks from the tiled layout (each row's four
+            // K-block bytes are one word there): A rows row0.., then the B
+            // tile's rows (SWIGLU_FWD: 64 gate rows, then the 64 up rows)
+            const long long nkg = args.ks / 4, j0 = (long long)(tl.kb0 + kb) * 4;
+            uint32_t w[4];
 #pragma unroll
-            for (int blk = 0; blk < BN / 128; ++blk) {  // all BN rows of the tile's B
-              uint32_t w[4];
+            for (int j = 0; j < 4; ++j)
+              w[j] = *reinterpret_cast<const uint32_t*>(
+                  args.sa + mx_tiled_off(tl.row0 + lane + 32 * j, j0, nkg));
+            *reinterpret_cast<uint4*>(sA + C::SF_OFF + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int t = blk * 128 + lane + 32 * j;  // row of the B tile
-                long long grow;
-                if (EPI == EPI_SWIGLU_FWD)
-                  grow = (long long)tl.e * args.b_group_rows + tl.n_tile * (BN / 2) +
-                         (t < BN / 2 ? t : args.I + t - BN / 2);
-                else
-                  grow = (long long)tl.e * args.b_group_rows + tl.n_tile * BN + t;
-                w[j] = *reinterpret_cast<const uint32_t*>(args.sb + grow * args.ks +
-                                                          (long long)(tl.kb0 + kb) * 4);
-              }
-              *reinterpret_cast<uint4*>(sA + C::SF_OFF + 512 + blk * 512 + lane * 16) =
-                  make_uint4(w[0], w[1], w[2], w[3]);
+            for (int j = 0; j < 4; ++j) {
+              const int t = lane + 32 * j;  // row of the B tile
+              long long grow;
+              if (EPI == EPI_SWIGLU_FWD)
+                grow = (long long)tl.e * args.b_group_rows + tl.n_tile * (BN / 2) +
+                       (t < BN / 2 ? t : args.I + t - BN / 2);
+              else
+                grow = (long long)tl.e * args.b_group_rows + tl.n_tile * BN + t;
+              w[j] = *reinterpret_cast<const uint32_t*>(args.sb + mx_tiled_off(grow, j0, nkg));
             }
+            *reinterpret_cast<uint4*>(sA + C::SF_OFF + 512 + lane * 16) =
+                make_uint4(w[0], w[1], w[2], w[3]);
             fence_proxy_async_smem();  // read by tcgen05.cp through the async proxy
             __syncwarp();
           }
@@ -961,11 +969,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (PAIR) tma_load_2d_pair(dst, tm, bar_c, x, y);
             else tma_load_2d(dst, tm, &full[stage], x, y);
           };
-          // the stage's TMA bytes (the code or bf16 tiles: SF_OFF)
+          // the stage's TMA bytes: the code or bf16 tiles (SF_OFF), and on
+          // MXFP8 pairs the scale blocks as well
           if (!PAIR) {
             if (lane == 0) mbar_arrive_expect_tx(&full[stage], C::SF_OFF);
           } else if (leader) {
-            if (lane == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::SF_OFF);
+            if (lane == 0)
+              mbar_arrive_expect_tx(&full[stage],
+                                    2 * (C::SF_OFF + (SPLIT == SPLIT_MX ? C::SF_BYTES : 0)));
+          }
+          if (PAIR && SPLIT == SPLIT_MX) {
+            // scale blocks by TMA: this CTA's A rows, and all BN rows of B
+            const int nkg = args.ks / 4, kg = tl.kb0 + kb;
+            load(sA + C::SF_OFF, &om.sfa, 0, 2 * ((tl.row0 >> 7) * nkg + kg));
+#pragma unroll
+            for (int blk = 0; blk < BN / 128; ++blk) {
+              const int g0 = EPI == EPI_SWIGLU_FWD
+                                 ? tl.e * args.b_group_rows + tl.n_tile * 128 + (blk ? args.I : 0)
+                                 : tl.e * args.b_group_rows + tl.n_tile * BN + blk * 128;
+              load(sA + C::SF_OFF + 512 + blk * 512, &om.sfb, 0, 2 * ((g0 >> 7) * nkg + kg));
+            }
           }
           // A tile: 128 rows (M) x 64 (K)  (+ its lo tile with SPLIT_A)
           if (!A_MN) {
@@ -1006,9 +1029,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (SPLIT == SPLIT_B) load(sB + C::B_BYTES + j * 8192, &tmL, x0 + 64 * j, ky);
             }
           }
-          // MXFP8 pair: this CTA's scale blocks are written (the leader's
-          // tcgen05.cp reads them from here)
-          if (PAIR && SPLIT == SPLIT_MX && !leader && lane == 0) mbar_arrive_cluster(bar_c);
           issued_par[stage] = static_cast<int>(phase);
           if (++stage == C::STAGES) {
             stage = 0;
@@ -1349,6 +1369,14 @@ cudaError_t gemm_fwd_gate_up(const Dims& D, const void* X_perm, const void* w_ga
       "fwd_gate_up_swiglu", ta, tb, tc, a, max_mtiles(D) * a.n_tiles, st);
 }
 
+// The tiled scales of a [rows, K] MXFP8 operand as a TMA map: 512-byte blocks
+// viewed as pairs of 256-byte rows (box: one block).
+static bool make_sf_map(CUtensorMap* m, const uint8_t* scales, int64_t rows, int64_t K) {
+  const uint64_t blocks = static_cast<uint64_t>(rows / 128) * static_cast<uint64_t>(K / 128);
+  return make_map_t(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, scales, 256, 2 * blocks, 256, 256, 2,
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 // MXFP8 operands (E4M3 codes, E8M0 scale bytes per 32 K values, K-major):
 // the gate/up GEMM with g, u to GU (NULL: not stored) and h as MXFP8 codes
 // and scales (NULL: not stored), single-CTA 128-wide tiles of 64 FFN columns.
@@ -1385,8 +1413,13 @@ cudaError_t gemm_fwd_gate_up_mx(const Dims& D, const uint8_t* x_codes, const uin
   a.h_scales = h_scales;
   if (pair) {
     a.n_tiles = (int)(D.I / 128);
+    OutMaps om;
+    memset(&om, 0, sizeof(om));
+    if (!make_sf_map(&om.sfa, x_scales, D.rows_max, D.d) ||
+        !make_sf_map(&om.sfb, wgu_scales, D.E * 2 * D.I, D.d))
+      return cudaErrorInvalidValue;
     return launch<256, false, false, SCHED_MGROUP, EPI_SWIGLU_FWD, SPLIT_MX, true>(
-        "fwd_gate_up_swiglu", ta, tb, tc, a, max_mpairs(D) * a.n_tiles, st);
+        "fwd_gate_up_swiglu", ta, tb, tc, a, max_mpairs(D) * a.n_tiles, st, nullptr, &om);
   }
   return launch<128, false, false, SCHED_MGROUP, EPI_SWIGLU_FWD, SPLIT_MX>(
       "fwd_gate_up_swiglu", ta, tb, tc, a, max_mtiles(D) * a.n_tiles, st);
@@ -1417,8 +1450,13 @@ cudaError_t gemm_fwd_down_mx(const Dims& D, const uint8_t* h_codes, const uint8_
   a.ks = (int)(D.I / 32);
   if (D.pair && D.d % 256 == 0) {
     a.n_tiles = (int)(D.d / 256);
+    OutMaps om;
+    memset(&om, 0, sizeof(om));
+    if (!make_sf_map(&om.sfa, h_scales, D.rows_max, D.I) ||
+        !make_sf_map(&om.sfb, wd_scales, D.E * D.d, D.I))
+      return cudaErrorInvalidValue;
     return launch<256, false, false, SCHED_MGROUP, EPI_F32, SPLIT_MX, true>(
-        "fwd_down", ta, tb, tc, a, max_mpairs(D) * a.n_tiles, st);
+        "fwd_down", ta, tb, tc, a, max_mpairs(D) * a.n_tiles, st, nullptr, &om);
   }
   return launch<128, false, false, SCHED_MGROUP, EPI_F32, SPLIT_MX>(
       "fwd_down", ta, tb, tc, a, max_mtiles(D) * a.n_tiles, st);

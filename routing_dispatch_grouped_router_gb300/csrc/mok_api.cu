@@ -368,8 +368,8 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
   uint8_t* h_c = at<uint8_t>(workspace, F.h_codes);
   uint8_t* h_s = at<uint8_t>(workspace, F.h_scales);
   if (D.mx) {
-    MOK_CUDA(launch_mx_rows(w_gate_up, nullptr, D.E * 2 * D.I, D.d, wgu_c, wgu_s, st));
-    MOK_CUDA(launch_mx_rows(w_down, nullptr, D.E * D.d, D.I, wd_c, wd_s, st));
+    MOK_CUDA(launch_mx_rows(w_gate_up, nullptr, D.E * 2 * D.I, D.d, wgu_c, wgu_s, st, true));
+    MOK_CUDA(launch_mx_rows(w_down, nullptr, D.E * D.d, D.I, wd_c, wd_s, st, true));
   }
   const size_t y_esz = D.act_bf16 ? 2 : 4;
   float* logits = at<float>(workspace, F.logits);
@@ -402,7 +402,7 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
     if (D.mx) {
       // expert GEMMs on the block-scaled tensor cores: x rows to MXFP8, the
       // gate/up GEMM writes h as MXFP8 for the down projection
-      MOK_CUDA(launch_mx_rows(x_perm, nullptr, D.rows_max, D.d, xq_c, xq_s, st));
+      MOK_CUDA(launch_mx_rows(x_perm, nullptr, D.rows_max, D.d, xq_c, xq_s, st, true));
       MOK_CUDA(gemm_fwd_gate_up_mx(D, xq_c, xq_s, wgu_c, wgu_s, o.mtile_prefix, o.padded_offsets,
                                    gu, h_c, h_s, status, st));
       MOK_CUDA(gemm_fwd_down_mx(D, h_c, h_s, wd_c, wd_s, o.mtile_prefix, o.padded_offsets, O,
@@ -465,7 +465,7 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
   uint8_t* rxq_c = at<uint8_t>(workspace, B.xq_codes);
   uint8_t* rxq_s = at<uint8_t>(workspace, B.xq_scales);
   if (D.mx && D.recompute_gu)
-    MOK_CUDA(launch_mx_rows(w_gate_up, nullptr, D.E * 2 * D.I, D.d, rwgu_c, rwgu_s, st));
+    MOK_CUDA(launch_mx_rows(w_gate_up, nullptr, D.E * 2 * D.I, D.d, rwgu_c, rwgu_s, st, true));
   if (D.mx) {
     // weights quantised once per call along the dgrads' reduction dims:
     // W_down along d, W_gate_up along 2I (blocks of 32 rows)
@@ -520,7 +520,7 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
     if (D.recompute_gu) {
       // the forward's gate/up GEMM again, g and u only (no h)
       if (D.mx) {
-        MOK_CUDA(launch_mx_rows(x_perm, nullptr, D.rows_max, D.d, rxq_c, rxq_s, st));
+        MOK_CUDA(launch_mx_rows(x_perm, nullptr, D.rows_max, D.d, rxq_c, rxq_s, st, true));
         MOK_CUDA(gemm_fwd_gate_up_mx(D, rxq_c, rxq_s, rwgu_c, rwgu_s, mtp, poff,
                                      const_cast<void*>(gu), nullptr, nullptr, status, st));
       } else {

@@ -182,8 +182,10 @@ cudaError_t gemm_dense_bf16(int64_t M, int64_t N, int64_t K, const void* A, bool
 
 // MXFP8 fake quantisation (mx.cu): rows = blocks along each row, cols =
 // blocks of 32 rows; codes/scales may be null.
+// tiled: scales in the tiled layout of mx_tiled_off (rows, cols multiples of
+// 128), the layout of the expert GEMMs' MXFP8 operands; else row-major.
 cudaError_t launch_mx_rows(const void* in, void* out, long long rows, long long cols,
-                           uint8_t* codes, uint8_t* scales, cudaStream_t st);
+                           uint8_t* codes, uint8_t* scales, cudaStream_t st, bool tiled = false);
 cudaError_t launch_mx_cols(const void* in, void* out, long long rows, long long cols,
                            uint8_t* codes, uint8_t* scales, cudaStream_t st);
 

@@ -33,9 +33,11 @@ __device__ __forceinline__ int mx_shared_exp(const float (&v)[32]) {
 }
 
 // One thread per block of 32 consecutive values of a row.
+// tiled_nkg > 0: scales in the tiled layout of a matrix with tiled_nkg*128
+// columns (mx_tiled_off); 0: row-major [rows, cols/32].
 __global__ void mx_rows_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
                                uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                               long long nblocks) {
+                               long long nblocks, long long tiled_nkg) {
   for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < nblocks;
        b += (long long)gridDim.x * blockDim.x) {
     float v[32];
@@ -55,7 +57,11 @@ __global__ void mx_rows_kernel(const uint4* __restrict__ in, uint4* __restrict__
         c[0] = make_uint4(w[0], w[1], w[2], w[3]);
         c[1] = make_uint4(w[4], w[5], w[6], w[7]);
       }
-      if (scales) scales[b] = static_cast<uint8_t>(sbyte);
+      if (scales) {
+        const long long off =
+            tiled_nkg > 0 ? mx_tiled_off(b / (tiled_nkg * 4), b % (tiled_nkg * 4), tiled_nkg) : b;
+        scales[off] = static_cast<uint8_t>(sbyte);
+      }
     }
     if (out) {  // NULL: codes and scales only
       mx_fake32(v);
@@ -117,12 +123,14 @@ static unsigned grid_for(long long n, int threads) {
 }
 
 cudaError_t launch_mx_rows(const void* in, void* out, long long rows, long long cols,
-                           uint8_t* codes, uint8_t* scales, cudaStream_t st) {
+                           uint8_t* codes, uint8_t* scales, cudaStream_t st, bool tiled) {
+  if (tiled && (rows % 128 || cols % 128)) return cudaErrorInvalidValue;
   const long long nb = rows * (cols / 32);
   if (nb == 0) return cudaSuccess;
   ProfScope prof("mx_quant_rows", st);
   mx_rows_kernel<<<grid_for(nb, 256), 256, 0, st>>>(static_cast<const uint4*>(in),
-                                                    static_cast<uint4*>(out), codes, scales, nb);
+                                                    static_cast<uint4*>(out), codes, scales, nb,
+                                                    tiled ? cols / 128 : 0);
   count_launch();
   return cudaGetLastError();
 }

@@ -53,6 +53,16 @@ __device__ __forceinline__ void mx_fake32(float (&v)[32]) {
   }
 }
 
+// Tiled layout of the E8M0 scales of a [rows, K] MXFP8 operand (rows and K
+// multiples of 128), the layout the block-scaled MMA's scale copy takes: the
+// scales of rows 128a..128a+127 and K blocks 4b..4b+3 (32 values each) form
+// one contiguous 512-byte block (index a * (K/128) + b), in which the scale of
+// row r, K block j sits at byte 16*(r%32) + 4*((r/32)%4) + j%4.
+__host__ __device__ __forceinline__ long long mx_tiled_off(long long r, long long j,
+                                                           long long n_kg) {
+  return ((r >> 7) * n_kg + (j >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3);
+}
+
 // MXFP8 encoding of one 32-value block held by one thread: the E4M3 codes
 // (same rule as mx_fake32: v' = code * 2^shared) into four 32-bit words,
 // codes of v[4i..4i+3] in word i, lowest byte first; returns the E8M0 byte.
