@@ -76,6 +76,25 @@ NCU_TRAFFIC_FINE = {
 }
 
 
+def mx_quant_bytes(shape: gen.Shape, nmb: int, rows_max: int, kernels: dict, steps: int) -> dict:
+    """Average bytes per launch of the MXFP8 quantisers in one step: once per
+    call the weights (rows: E4M3 codes + scales for the forward; columns: bf16
+    values along the dgrads' K for the backward), per micro-batch the
+    dispatched x rows (codes) and dy rows (rows and columns, bf16 values) and
+    the x rows along the columns for the weight gradients."""
+    E, d, I = shape.E, shape.d, shape.I
+    w = E * 2 * I * d + E * d * I              # weight elements
+    act = rows_max * d                         # one micro-batch's dispatched rows
+    rows_bytes = w * (2 + 1 + 1 / 32) + nmb * act * (2 + 1 + 1 / 32) + nmb * act * 4
+    cols_bytes = w * 4 + nmb * 2 * act * 4
+    out = {}
+    for name, total in (("mx_quant_rows", rows_bytes), ("mx_quant_cols", cols_bytes)):
+        if name in kernels:
+            n, _ = kernels[name]
+            out[name] = total / (n / steps)
+    return out
+
+
 def mover_bytes(shape: gen.Shape, micro_batches: int = 1) -> dict:
     """Bytes one launch of each data-movement kernel must move in the layer's
     layout: bf16 token rows, fp32 expert-output and dX rows, fp32 y and dx
@@ -428,11 +447,15 @@ def main():
     peaks = load_peaks()
     flops = gemm_flops(shape, int(layer.layout.mb_count))
     movers = mover_bytes(shape, int(layer.layout.mb_count))
+    if WORKLOAD == "mxfp8":
+        movers.update(mx_quant_bytes(shape, int(layer.layout.mb_count), int(layer.layout.rows_max),
+                                     kernels, args.steps))
     total_k = sum(v[1] for v in kernels.values())
     ksum = {}
     for name, (n, ms) in kernels.items():
         ksum[name] = {"launches": n, "avg_us": 1e3 * ms / n, "share": ms / total_k}
-    dom = max(kernels, key=lambda n: kernels[n][1])
+    # the dominant kernel among those whose work per launch is known
+    dom = max((n for n in kernels if n in flops or n in movers), key=lambda n: kernels[n][1])
     n_dom, ms_dom = kernels[dom]
     avg_s = ms_dom / n_dom / 1e3
     if dom in flops:

@@ -48,3 +48,12 @@ def test_workload_options():
     finally:
         bench.WORKLOAD = "fine"
     assert bench.layer_options(FakeApi) == {}
+
+
+def test_mx_quantiser_bytes_average_over_launches():
+    s = gen.workload_shape("mxfp8")
+    nmb, rows_max = 8, 32640
+    kernels = {"mx_quant_cols": (18 * 20, 1.0), "mx_quant_rows": (18 * 20, 1.0)}
+    got = bench.mx_quant_bytes(s, nmb, rows_max, kernels, steps=20)
+    w = s.E * 3 * s.I * s.d
+    assert got["mx_quant_cols"] * 18 == pytest.approx(4 * w + nmb * 2 * rows_max * s.d * 4)
