@@ -17,7 +17,7 @@ namespace mok {
 
 // E4M3 code and E8M0 scale byte of one dequantised value v' = q * 2^shared.
 __device__ __forceinline__ uint8_t e4m3_code_of(float vq, int shared) {
-  const uint16_t q = cvt_e4m3x2(ldexpf(vq, -shared), 0.f);
+  const uint16_t q = cvt_e4m3x2(vq * exp2i(-shared), 0.f);
   return static_cast<uint8_t>(q >> 8);
 }
 

@@ -31,7 +31,16 @@ __device__ __forceinline__ void e4m3x2_to_f32(uint16_t q, float* hi, float* lo) 
   *hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
 }
 
-// In-place MXFP8 fake quantisation of one 32-value block.
+// 2^n as an fp32 value, for n in [-149, 127] (below -126: subnormal).  A
+// product with it is exact when representable and otherwise rounds like any
+// fp32 multiplication, so x * exp2i(n) equals x scaled by 2^n with one rounding.
+__device__ __forceinline__ float exp2i(int n) {
+  return n >= -126 ? __int_as_float((n + 127) << 23) : __int_as_float(1 << (n + 149));
+}
+
+// In-place MXFP8 fake quantisation of one 32-value block.  shared lies in
+// [-127, 119] for finite input (floor(log2 of the largest finite fp32) - 8 =
+// 119), so both scale factors are fp32 powers of two.
 __device__ __forceinline__ void mx_fake32(float (&v)[32]) {
   float amax = 0.f;
 #pragma unroll
@@ -43,13 +52,14 @@ __device__ __forceinline__ void mx_fake32(float (&v)[32]) {
     shared = e - 1 - 8;
     shared = shared < -127 ? -127 : (shared > 127 ? 127 : shared);
   }
+  const float down = exp2i(-shared), up = exp2i(shared);
 #pragma unroll
   for (int j = 0; j < 32; j += 2) {
-    const uint16_t q = cvt_e4m3x2(ldexpf(v[j + 1], -shared), ldexpf(v[j], -shared));
+    const uint16_t q = cvt_e4m3x2(v[j + 1] * down, v[j] * down);
     float hi, lo;
     e4m3x2_to_f32(q, &hi, &lo);
-    v[j] = ldexpf(lo, shared);
-    v[j + 1] = ldexpf(hi, shared);
+    v[j] = lo * up;
+    v[j + 1] = hi * up;
   }
 }
 
@@ -77,12 +87,12 @@ __device__ __forceinline__ uint32_t mx_encode32(const float (&v)[32], uint32_t (
     shared = e - 1 - 8;
     shared = shared < -127 ? -127 : (shared > 127 ? 127 : shared);
   }
+  const float down = exp2i(-shared);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     // cvt packs its first operand into the upper byte
-    const uint16_t p01 = cvt_e4m3x2(ldexpf(v[4 * i + 1], -shared), ldexpf(v[4 * i], -shared));
-    const uint16_t p23 =
-        cvt_e4m3x2(ldexpf(v[4 * i + 3], -shared), ldexpf(v[4 * i + 2], -shared));
+    const uint16_t p01 = cvt_e4m3x2(v[4 * i + 1] * down, v[4 * i] * down);
+    const uint16_t p23 = cvt_e4m3x2(v[4 * i + 3] * down, v[4 * i + 2] * down);
     w[i] = static_cast<uint32_t>(p01) | (static_cast<uint32_t>(p23) << 16);
   }
   return static_cast<uint32_t>(shared + 127);
