@@ -1090,7 +1090,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after_sync();
           const uint32_t a_base = smem_addr(tiles + stage * C::STAGE_BYTES);
           const uint32_t b_base = a_base + C::B_OFF;
-          if (SPLIT == SPLIT_MX) {
+          if constexpr (SPLIT == SPLIT_MX) {
             // scales to TMEM (SF_COLS columns per stage after the
             // accumulators), then four K=32 block-scaled MMAs, scale byte j
             // each; CTA pairs copy each CTA's blocks to its own TMEM
@@ -1113,24 +1113,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               else
                 mma_mxf8(d_tmem, ad, bd, id, sfa, sfa + 4u, (kb | j) != 0 ? 1u : 0u);
             }
-            commit(&empty[stage]);
-            if (++stage == C::STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
-            continue;
-          }
+          } else {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint64_t ad = smem_desc_sw128(a_base + j * kstep_a, lbo_a, 1024);
-            const uint64_t bd = smem_desc_sw128(b_base + j * kstep_b, lbo_b, 1024);
-            mma(d_tmem, ad, bd, (kb | j) != 0 ? 1u : 0u);
-            if (SPLIT == SPLIT_A) {
-              const uint64_t ad2 = smem_desc_sw128(a_base + C::A_BYTES + j * kstep_a, lbo_a, 1024);
-              mma(d_tmem, ad2, bd, 1u);
-            } else if (SPLIT == SPLIT_B) {
-              const uint64_t bd2 = smem_desc_sw128(b_base + C::B_BYTES + j * kstep_b, lbo_b, 1024);
-              mma(d_tmem, ad, bd2, 1u);
+            for (int j = 0; j < 4; ++j) {
+              const uint64_t ad = smem_desc_sw128(a_base + j * kstep_a, lbo_a, 1024);
+              const uint64_t bd = smem_desc_sw128(b_base + j * kstep_b, lbo_b, 1024);
+              mma(d_tmem, ad, bd, (kb | j) != 0 ? 1u : 0u);
+              if (SPLIT == SPLIT_A) {
+                const uint64_t ad2 =
+                    smem_desc_sw128(a_base + C::A_BYTES + j * kstep_a, lbo_a, 1024);
+                mma(d_tmem, ad2, bd, 1u);
+              } else if (SPLIT == SPLIT_B) {
+                const uint64_t bd2 =
+                    smem_desc_sw128(b_base + C::B_BYTES + j * kstep_b, lbo_b, 1024);
+                mma(d_tmem, ad, bd2, 1u);
+              }
             }
           }
           commit(&empty[stage]);
