@@ -67,12 +67,12 @@ def gemm_flops(shape: gen.Shape, micro_batches: int = 1) -> dict:
 # grouped GEMMs on the fine workload, from the ncu capture summarised in
 # profiles/grouped_gemms_fine.txt (kernels as of the commit named there).
 NCU_TRAFFIC_FINE = {
-    "fwd_gate_up_swiglu": 688.125952e6 + 331.846e6,
-    "fwd_down": 343.462144e6 + 255.012e6,
-    "bwd_down_dgrad_swiglu": 771.265792e6 + 402.168e6,
-    "bwd_down_wgrad": 300.166656e6 + 475.782e6,
-    "bwd_gate_up_dgrad": 690.546688e6 + 272.063e6,
-    "bwd_gate_up_wgrad": 449.908736e6 + 1011.848e6,
+    "fwd_gate_up_swiglu": 689.573376e6 + 331.275e6,
+    "fwd_down": 343.459072e6 + 254.775e6,
+    "bwd_down_dgrad_swiglu": 770.239744e6 + 401.826e6,
+    "bwd_down_wgrad": 300.351488e6 + 476.125e6,
+    "bwd_gate_up_dgrad": 689.331968e6 + 271.781e6,
+    "bwd_gate_up_wgrad": 449.907200e6 + 1012.112e6,
 }
 
 
