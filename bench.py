@@ -292,7 +292,8 @@ def e2e_pipelined(layer, inp, x, dy, wr, bias, wgu, wd, dwr, dwgu, dwd, stream, 
                   dist):
     """Milliseconds for `steps` layer steps through the public API, each with
     its inputs uploaded from and its outputs read back to pinned host memory
-    inside the timed region (copies on a side stream, two buffer sets)."""
+    inside the timed region (uploads and read-backs on two side streams, so
+    both directions of the host link run at once; two buffer sets)."""
     import torch
     xh = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
     dyh = torch.from_numpy(inp["dy"].view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -302,7 +303,8 @@ def e2e_pipelined(layer, inp, x, dy, wr, bias, wgu, wd, dwr, dwgu, dwd, stream, 
     dyd = [torch.empty_like(dy) for _ in range(2)]
     yd = [torch.empty(x.shape, dtype=torch.float32, device=x.device) for _ in range(2)]
     dxd = [torch.empty(x.shape, dtype=torch.float32, device=x.device) for _ in range(2)]
-    copy = torch.cuda.Stream()
+    copy = torch.cuda.Stream()  # uploads
+    back = torch.cuda.Stream()  # read-backs
     inputs_in = [torch.cuda.Event() for _ in range(2)]      # upload into set b done
     inputs_free = [torch.cuda.Event() for _ in range(2)]    # the step that read set b finished
     outputs_out = [torch.cuda.Event() for _ in range(2)]    # read-back of set b done
@@ -330,12 +332,13 @@ def e2e_pipelined(layer, inp, x, dy, wr, bias, wgu, wd, dwr, dwgu, dwd, stream, 
                            dw_gate_up=dwgu, dw_down=dwd)
             inputs_free[b].record(stream)
             outputs_ready[b].record(stream)
-            with torch.cuda.stream(copy):
-                copy.wait_event(outputs_ready[b])
+            with torch.cuda.stream(back):
+                back.wait_event(outputs_ready[b])
                 yh[b].copy_(yd[b], non_blocking=True)
                 dxh[b].copy_(dxd[b], non_blocking=True)
-                outputs_out[b].record(copy)
+                outputs_out[b].record(back)
         stream.wait_stream(copy)
+        stream.wait_stream(back)
 
     run(3)
     torch.cuda.synchronize()
