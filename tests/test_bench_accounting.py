@@ -57,3 +57,21 @@ def test_mx_quantiser_bytes_average_over_launches():
     got = bench.mx_quant_bytes(s, nmb, rows_max, kernels, steps=20)
     w = s.E * 3 * s.I * s.d
     assert got["mx_quant_cols"] * 18 == pytest.approx(4 * w + nmb * 2 * rows_max * s.d * 4)
+
+
+def test_reference_arm_prints_one_json_line():
+    """`bench.py --impl reference` times the fp64 oracle on the host and prints
+    the contract's line (tiny workload here to keep it quick)."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                          "--steps", "3", "--warmup", "3", "--workload", "tiny"],
+                         capture_output=True, text=True, timeout=300, cwd=root)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "tokens/s"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["config"]["workload"].startswith("tiny")
