@@ -527,28 +527,6 @@ __global__ void reverse_dispatch_kernel(const float4* __restrict__ dXp,
   __shared__ int s_e[kMaxTopK];
   __shared__ float s_dl[kMaxTopK];
   const long long t = blockIdx.x;
-  // every thread reads the token's rows and experts itself (a broadcast) and
-  // puts its first column's dX and router-weight loads in flight before it
-  // waits for warp 0's dl; the sums below keep their order
-  int rows[kMaxTopK], exps[kMaxTopK];
-#pragma unroll
-  for (int s = 0; s < kMaxTopK; ++s) {
-    rows[s] = s < k ? ppos[t * k + s] : -1;
-    exps[s] = s < k ? topk_idx[t * k + s] : 0;
-  }
-  const int c_first = threadIdx.x;
-  float4 xr[kMaxTopK];
-  uint2 wr[kMaxTopK];
-  if (c_first < dq) {
-#pragma unroll
-    for (int s = 0; s < kMaxTopK; ++s) {
-      if (rows[s] < 0) continue;
-      xr[s] = ld_nc_f4(dXp + static_cast<long long>(rows[s]) * dq + c_first);
-      asm volatile("ld.global.nc.v2.b32 {%0, %1}, [%2];"
-                   : "=r"(wr[s].x), "=r"(wr[s].y)
-                   : "l"(Wr + static_cast<long long>(exps[s]) * dq + c_first));
-    }
-  }
   if (threadIdx.x < 32) {
     const int s = threadIdx.x;
     int row = -1, e = 0;
@@ -579,17 +557,7 @@ __global__ void reverse_dispatch_kernel(const float4* __restrict__ dXp,
     }
   }
   __syncthreads();
-  if (c_first < dq) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int s = 0; s < kMaxTopK; ++s) {
-      if (rows[s] < 0) continue;
-      add4(acc, xr[s]);
-      axpy4(acc, s_dl[s], bf16x4_to_f4(wr[s]));
-    }
-    store4<BF16_OUT>(dx, t, dq, c_first, acc);
-  }
-  for (int c = c_first + blockDim.x; c < dq; c += blockDim.x) {
+  for (int c = threadIdx.x; c < dq; c += blockDim.x) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int s = 0; s < k; ++s) {
       if (s_row[s] < 0) continue;
