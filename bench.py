@@ -44,15 +44,21 @@ WORKLOAD = "fine"
 
 
 # GEMMs that run on the block-scaled FP8 tensor cores in the MXFP8 workload
-MX_GEMMS = ("fwd_gate_up_swiglu", "fwd_down")
+MX_GEMMS = ("fwd_gate_up_swiglu", "fwd_down", "bwd_gate_up_dgrad")
+
+
+# Weight-gradient GEMMs: with micro-batches the layer defers them and launches
+# each once per step over every micro-batch's rows
+DEFERRED_WGRADS = ("bwd_down_wgrad", "bwd_gate_up_wgrad")
 
 
 def gemm_flops(shape: gen.Shape, micro_batches: int = 1) -> dict:
-    """Algorithmic FLOP of one launch of each GEMM; with micro-batching every
-    launch covers T / micro_batches tokens."""
+    """Algorithmic FLOP of one launch of each GEMM; with micro-batching a
+    launch covers T / micro_batches tokens, except the deferred weight
+    gradients, whose one launch per step covers all T."""
     R, d, I, T, E = (shape.R // micro_batches, shape.d, shape.I, shape.T // micro_batches,
                      shape.E)
-    return {
+    f = {
         "router_logits": 2.0 * T * d * E,
         "fwd_gate_up_swiglu": 2.0 * R * d * 2 * I,
         "fwd_down": 2.0 * R * I * d,
@@ -61,6 +67,9 @@ def gemm_flops(shape: gen.Shape, micro_batches: int = 1) -> dict:
         "bwd_gate_up_dgrad": 2.0 * R * 2 * I * d,
         "bwd_gate_up_wgrad": 2.0 * R * 2 * I * d,
     }
+    for n in DEFERRED_WGRADS:
+        f[n] *= micro_batches
+    return f
 
 
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the
@@ -78,15 +87,19 @@ NCU_TRAFFIC_FINE = {
 
 def mx_quant_bytes(shape: gen.Shape, nmb: int, rows_max: int, kernels: dict, steps: int) -> dict:
     """Average bytes per launch of the MXFP8 quantisers in one step: once per
-    call the weights (rows: E4M3 codes + scales for the forward; columns: bf16
-    values along the dgrads' K for the backward), per micro-batch the
-    dispatched x rows (codes) and dy rows (rows and columns, bf16 values) and
-    the x rows along the columns for the weight gradients."""
+    call the weights (rows: E4M3 codes + scales for the forward; columns along
+    the dgrads' K for the backward: W_down as bf16 values, W_gate_up as
+    transposed E4M3 codes + scales), per micro-batch the dispatched x rows
+    (codes), dy (one column-kernel launch reads it once and writes bf16 values
+    in both block directions) and the x rows along the columns for the weight
+    gradients."""
     E, d, I = shape.E, shape.d, shape.I
-    w = E * 2 * I * d + E * d * I              # weight elements
+    w_gu, w_d = E * 2 * I * d, E * d * I       # weight elements
+    w = w_gu + w_d
     act = rows_max * d                         # one micro-batch's dispatched rows
-    rows_bytes = w * (2 + 1 + 1 / 32) + nmb * act * (2 + 1 + 1 / 32) + nmb * act * 4
-    cols_bytes = w * 4 + nmb * 2 * act * 4
+    q8 = 2 + 1 + 1 / 32                        # bf16 in, E4M3 code + 1/32 scale out
+    rows_bytes = w * q8 + nmb * act * q8
+    cols_bytes = w_d * 4 + w_gu * q8 + nmb * act * (2 + 2 + 2) + nmb * act * 4
     out = {}
     for name, total in (("mx_quant_rows", rows_bytes), ("mx_quant_cols", cols_bytes)):
         if name in kernels:
@@ -463,7 +476,7 @@ def main():
     avg_s = ms_dom / n_dom / 1e3
     if dom in flops:
         ach = flops[dom] / avg_s / 1e12
-        # the MXFP8 workload's forward GEMMs run on the FP8 tensor rate: their
+        # the MXFP8 workload's block-scaled GEMMs run on the FP8 tensor rate: their
         # peak is the measured bf16 one times the nominal fp8/bf16 ratio (2)
         fp8 = WORKLOAD == "mxfp8" and dom in MX_GEMMS
         peak = peaks["bf16_sustained"] * (2.0 if fp8 else 1.0)
@@ -515,7 +528,11 @@ def main():
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if WORKLOAD != "mxfp8" else "bf16 MMAs on MXFP8-quantised operands",
+            "dtype": "bf16" if WORKLOAD != "mxfp8" else "mxfp8",
+            "dtype_detail": None if WORKLOAD != "mxfp8" else (
+                "E4M3 + E8M0 per 32: block-scaled FP8 MMAs for the forward GEMMs and the "
+                "gate/up dgrad; bf16 MMAs on MX-valued operands for the down dgrad; "
+                "weight gradients on bf16 hi/lo operands"),
             "data": "synthetic", "config": workload_config(shape),
             "grouped_gemm_tflops": gg_tflops,
             "grouped_gemm_frac_of_peak": gg_tflops / peaks["bf16_sustained"],

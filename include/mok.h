@@ -239,9 +239,10 @@ mok_status mok_moe_dispatch_plan_noalloc(const mok_moe_desc* desc, const int32_t
  *            all-zero block),  q = RNE_E4M3(v / 2^shared) saturating at 448.
  * in: bf16 [rows, cols] row-major.  along_rows = 0: blocks of 32 consecutive
  * values of a row (cols % 32 == 0); along_rows = 1: blocks of 32 consecutive
- * rows of a column (rows % 32 == 0, cols even).
+ * rows of a column (rows % 32 == 0, cols % 8 == 0).
  * out: bf16 [rows, cols], the dequantised values q * 2^shared (exact in
  * bf16); may equal `in`.  codes: NULL or uint8 [rows, cols] E4M3 codes.
+ * in, out and codes 16-byte aligned (else MOK_ERR_INVALID_ARG).
  * scales: NULL or uint8 E8M0 bytes (shared + 127), [rows, cols/32]
  * (along_rows = 0) or [rows/32, cols] (along_rows = 1). */
 mok_status mok_mx_quantize(const void* in, int64_t rows, int64_t cols, int along_rows, void* out,

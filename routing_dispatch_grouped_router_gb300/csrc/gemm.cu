@@ -77,7 +77,8 @@ struct GemmArgs {
   void* out2;               // SWIGLU_FWD: H [rows,I] (NULL: not stored); SWIGLU_BWD: P_hi = bf16(p*h) [rows,I]
   void* out3;               // SWIGLU_BWD: dGU_lo [rows,2I]
   void* out4;               // SWIGLU_BWD: P_lo [rows,I]
-  void* out5;               // SWIGLU_BWD with mx: MXFP8 dGU [rows,2I] (dgrad operand)
+  uint8_t* dgu_codes;       // SWIGLU_BWD with mx: dG, dU as E4M3 codes [rows,2I] (dgrad operand)
+  uint8_t* dgu_scales;      // ... and its E8M0 bytes (tiled layout, mx_tiled_off)
   int mx;                   // SwiGLU epilogues: quantise the derived GEMM operands to MXFP8
   const uint8_t* sa;        // SPLIT_MX: A scale bytes, tiled layout (mx_tiled_off)
   const uint8_t* sb;        // SPLIT_MX: B scale bytes, tiled layout
@@ -639,70 +640,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
                                   a.evict_first != 0);
       }
     }
-  } else if (EPI == EPI_SWIGLU_BWD) {
-    // accumulator = dA = dY_perm W_down for BN columns of I (n0 = n_tile*BN).
-    // From the stored fp32 g, u and the row's routing weight p:
-    //   h  = silu(g) u;   dp += dA . h      (router-weight gradient partial)
-    //   dh = p dA;  dG = dh u sigma(g) (1 + g (1 - sigma(g)));  dU = dh silu(g)
-    //   dG, dU -> bf16 hi (operand of the gate/up dgrad) and bf16 lo (value
-    //             minus hi; hi + lo is the gate/up wgrad operand)
-    //   P = p h -> bf16 hi + lo (the down-projection wgrad operand)
-    const long long r = tl.row0 + row_in_tile;
-    const int I = a.I;
-    const int n0 = tl.n_tile * BN + half * HALF_COLS;
-    const float* gu = static_cast<const float*>(a.in_gu) + r * (2LL * I);
-    __nv_bfloat16* dgu_hi = static_cast<__nv_bfloat16*>(a.out) + r * (2LL * I);
-    __nv_bfloat16* dgu_lo = static_cast<__nv_bfloat16*>(a.out3) + r * (2LL * I);
-    __nv_bfloat16* p_hi = static_cast<__nv_bfloat16*>(a.out2) + r * (long long)I;
-    __nv_bfloat16* p_lo = static_cast<__nv_bfloat16*>(a.out4) + r * (long long)I;
-    const float p = a.row_w[r];
-    __nv_bfloat16* dgu_mx = static_cast<__nv_bfloat16*>(a.out5) + r * (2LL * I);
-    float dp = 0.f;
-#pragma unroll 1
-    for (int c = 0; c < HALF_COLS; c += 32) {
-      float dA[32], g[32], u[32], t[32];
-      {
-        uint32_t r0[16], r1[16];
-        tmem_ld16(taddr + half * HALF_COLS + c, r0);
-        tmem_ld16(taddr + half * HALF_COLS + c + 16, r1);
-        const float4* gp = reinterpret_cast<const float4*>(gu + n0 + c);
-        const float4* up = reinterpret_cast<const float4*>(gu + I + n0 + c);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 a4 = gp[j], b4 = up[j];
-          g[4 * j] = a4.x; g[4 * j + 1] = a4.y; g[4 * j + 2] = a4.z; g[4 * j + 3] = a4.w;
-          u[4 * j] = b4.x; u[4 * j + 1] = b4.y; u[4 * j + 2] = b4.z; u[4 * j + 3] = b4.w;
-        }
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          dA[j] = __uint_as_float(r0[j]);
-          dA[16 + j] = __uint_as_float(r1[j]);
-        }
-      }
-      // one pass: d gate -> t, d up -> dA, p h -> u (g is free afterwards)
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float sg;
-        const float sl = silu_f(g[j], &sg);
-        const float uu = u[j];
-        const float dh = p * dA[j];
-        dp = fmaf(dA[j], sl * uu, dp);
-        t[j] = dh * uu * (sg * (1.0f + g[j] * (1.0f - sg)));
-        dA[j] = dh * sl;
-        u[j] = p * sl * uu;
-      }
-      store_hi_lo32(dgu_hi + n0 + c, dgu_lo + n0 + c, t);
-      store_hi_lo32(dgu_hi + I + n0 + c, dgu_lo + I + n0 + c, dA);
-      if (a.mx) {
-        mx_fake32(t);
-        store_bf16x32(dgu_mx + n0 + c, t);
-        mx_fake32(dA);
-        store_bf16x32(dgu_mx + I + n0 + c, dA);
-      }
-      store_hi_lo32(p_hi + n0 + c, p_lo + n0 + c, u);
-    }
-    a.dp_part[r * a.np + tl.n_tile * 2 + half] = dp;
   }
 }
 
@@ -729,9 +666,12 @@ __device__ __forceinline__ void gu_issue(const GemmArgs& a, const Tile& tl, int 
   tma_load_2d(buf + 2048, tmG, &wbar[b], a.I + x, y);
 }
 
-// The SwiGLU backward epilogue of one tile (BF16 operands) with g, u staged
-// by TMA, chunk 0 already requested; the next chunk's copies are in flight
-// while this one is computed.  Returns the updated chunk count.
+// The SwiGLU backward epilogue of one tile with g, u staged by TMA, chunk 0
+// already requested; the next chunk's copies are in flight while this one is
+// computed.  Returns the updated chunk count.  With a.mx, dG and dU are also
+// quantised to MXFP8 (the gate/up dgrad's A operand): a block is 32
+// consecutive columns of a row, so each odd chunk encodes itself together
+// with the even chunk before it (n0 is a multiple of 32).
 template <int BN>
 __device__ __forceinline__ uint32_t swiglu_bwd_tma(const GemmArgs& a, const Tile& tl,
                                                    uint32_t taddr, int q, int lane, int half,
@@ -749,6 +689,7 @@ __device__ __forceinline__ uint32_t swiglu_bwd_tma(const GemmArgs& a, const Tile
   const float p = a.row_w[r];
   float dp = 0.f;
   const int sw = (lane >> 1) & 3;
+  float t_prev[16], dA_prev[16];  // mx: the even chunk's dG, dU
 #pragma unroll 1
   for (int c = 0; c < HALF_COLS; c += 16, ++count) {
     if (c + 16 < HALF_COLS)
@@ -784,6 +725,40 @@ __device__ __forceinline__ uint32_t swiglu_bwd_tma(const GemmArgs& a, const Tile
       t[j] = dh * uu * (sg * (1.0f + g[j] * (1.0f - sg)));
       dA[j] = dh * sl;
       u[j] = p * sl * uu;
+    }
+    if (a.mx) {
+      if ((c & 16) == 0) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          t_prev[j] = t[j];
+          dA_prev[j] = dA[j];
+        }
+      } else {
+        const int col = n0 + c - 16;  // first column of the block
+        const long long base = r * (2LL * I);
+        float blk[32];
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          blk[j] = t_prev[j];
+          blk[16 + j] = t[j];
+        }
+        uint32_t sbyte = mx_encode32(blk, w);
+        uint4* cp = reinterpret_cast<uint4*>(a.dgu_codes + base + col);
+        cp[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        cp[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        a.dgu_scales[mx_tiled_off(r, col / 32, 2 * I / 128)] = static_cast<uint8_t>(sbyte);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          blk[j] = dA_prev[j];
+          blk[16 + j] = dA[j];
+        }
+        sbyte = mx_encode32(blk, w);
+        cp = reinterpret_cast<uint4*>(a.dgu_codes + base + I + col);
+        cp[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        cp[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        a.dgu_scales[mx_tiled_off(r, (I + col) / 32, 2 * I / 128)] = static_cast<uint8_t>(sbyte);
+      }
     }
     if (lane == 0) bulk_wait_read<0>();  // the previous chunk's stores have read staging
     __syncwarp();
@@ -874,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&om.sfa);
       tma_prefetch_desc(&om.sfb);
     }
-    if (EPI == EPI_SWIGLU_BWD && !args.mx) {
+    if (EPI == EPI_SWIGLU_BWD) {
       tma_prefetch_desc(&om.dgu_hi);
       tma_prefetch_desc(&om.dgu_lo);
       tma_prefetch_desc(&om.p_hi);
@@ -1153,10 +1128,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - 2) >> 2;      // column half of the tile
     uint8_t* stage_buf = staging + (warp - 2) * C::STAGING_PER_WARP;
     const uint32_t tempty_leader = PAIR ? mapa_shared(smem_addr(tempty), 0) : 0u;
-    // SwiGLU backward with BF16 operands: g, u come by TMA (tmC maps them);
-    // `gu_chunks` counts the chunks this warp has requested
+    // SwiGLU backward: g, u come by TMA (tmC maps them); `gu_chunks` counts
+    // the chunks this warp has requested
     constexpr bool kGuTma = EPI == EPI_SWIGLU_BWD;
-    const bool gu_tma = kGuTma && !args.mx;
     uint64_t* wbar = gu_bar + 2 * (warp - 2);
     uint32_t gu_chunks = 0;
     uint32_t nst = 0;  // TMA-store blocks issued by this warp
@@ -1167,7 +1141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int acc = C::NACC == 2 ? (it & 1) : 0;
       const uint32_t acc_par = static_cast<uint32_t>(C::NACC == 2 ? ((it >> 1) & 1) : (it & 1));
       // the tile's first g, u chunk does not depend on the accumulator
-      if (gu_tma && valid)
+      if (kGuTma && valid)
         gu_issue<BN>(args, tl, q, lane, half, 0, stage_buf, wbar, gu_chunks, &tmC);
       if (!wait(&tfull[acc], acc_par)) {
         *vabort = 1;
@@ -1177,7 +1151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      if (gu_tma) {
+      if constexpr (kGuTma) {
         if (valid)
           gu_chunks = swiglu_bwd_tma<BN>(args, tl, taddr, q, lane, half, stage_buf, wbar,
                                          gu_chunks, &tmC, &om, vabort);
@@ -1422,41 +1396,63 @@ cudaError_t gemm_fwd_gate_up_mx(const Dims& D, const uint8_t* x_codes, const uin
       "fwd_gate_up_swiglu", ta, tb, tc, a, max_mtiles(D) * a.n_tiles, st);
 }
 
-cudaError_t gemm_fwd_down_mx(const Dims& D, const uint8_t* h_codes, const uint8_t* h_scales,
-                             const uint8_t* wd_codes, const uint8_t* wd_scales,
-                             const int32_t* mtile_prefix, const int32_t* poff, void* O,
-                             int* status, cudaStream_t st) {
+// An M-grouped GEMM on MXFP8 operands with fp32 rows out: O[rows_max, d] =
+// A[rows_max, K] B_e[d, K]^T per expert segment, A and B as E4M3 codes,
+// K-major, with tiled scales.  The down projection (K = I) and the gate/up
+// dgrad (K = 2I, B = W_gate_up transposed) are this GEMM.
+static cudaError_t grouped_mx_f32(const char* name, const Dims& D, int64_t K,
+                                  const uint8_t* a_codes, const uint8_t* a_scales,
+                                  const uint8_t* b_codes, const uint8_t* b_scales,
+                                  const int32_t* mtile_prefix, const int32_t* poff, void* O,
+                                  int* status, cudaStream_t st) {
   const auto u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
   CUtensorMap ta, tb, tc;
-  if (!make_map_t(&ta, u8, 1, h_codes, D.I, D.rows_max, D.I, 128, 128, sw) ||
-      !make_map_t(&tb, u8, 1, wd_codes, D.I, D.E * D.d, D.I, 128, 128, sw) ||
+  if (!make_map_t(&ta, u8, 1, a_codes, K, D.rows_max, K, 128, 128, sw) ||
+      !make_map_t(&tb, u8, 1, b_codes, K, D.E * D.d, K, 128, 128, sw) ||
       !make_out_map(&tc, O, D.d, D.rows_max))
     return cudaErrorInvalidValue;
   GemmArgs a = blank_args(status);
   a.E = (int)D.E;
   a.n_tiles = (int)(D.d / 128);
-  a.num_kb = (int)(D.I / 128);
+  a.num_kb = (int)(K / 128);
   a.b_group_rows = (int)D.d;
   a.mtile_prefix = mtile_prefix;
   a.poff = poff;
   a.out = O;  // fp32 [rows_max, d]
   a.ldo = D.d;
-  a.sa = h_scales;
-  a.sb = wd_scales;
-  a.ks = (int)(D.I / 32);
+  a.sa = a_scales;
+  a.sb = b_scales;
+  a.ks = (int)(K / 32);
   if (D.pair && D.d % 256 == 0) {
     a.n_tiles = (int)(D.d / 256);
     OutMaps om;
     memset(&om, 0, sizeof(om));
-    if (!make_sf_map(&om.sfa, h_scales, D.rows_max, D.I) ||
-        !make_sf_map(&om.sfb, wd_scales, D.E * D.d, D.I))
+    if (!make_sf_map(&om.sfa, a_scales, D.rows_max, K) ||
+        !make_sf_map(&om.sfb, b_scales, D.E * D.d, K))
       return cudaErrorInvalidValue;
     return launch<256, false, false, SCHED_MGROUP, EPI_F32, SPLIT_MX, true>(
-        "fwd_down", ta, tb, tc, a, max_mpairs(D) * a.n_tiles, st, nullptr, &om);
+        name, ta, tb, tc, a, max_mpairs(D) * a.n_tiles, st, nullptr, &om);
   }
   return launch<128, false, false, SCHED_MGROUP, EPI_F32, SPLIT_MX>(
-      "fwd_down", ta, tb, tc, a, max_mtiles(D) * a.n_tiles, st);
+      name, ta, tb, tc, a, max_mtiles(D) * a.n_tiles, st);
+}
+
+cudaError_t gemm_fwd_down_mx(const Dims& D, const uint8_t* h_codes, const uint8_t* h_scales,
+                             const uint8_t* wd_codes, const uint8_t* wd_scales,
+                             const int32_t* mtile_prefix, const int32_t* poff, void* O,
+                             int* status, cudaStream_t st) {
+  return grouped_mx_f32("fwd_down", D, D.I, h_codes, h_scales, wd_codes, wd_scales, mtile_prefix,
+                        poff, O, status, st);
+}
+
+cudaError_t gemm_bwd_gate_up_dgrad_mx(const Dims& D, const uint8_t* dgu_codes,
+                                      const uint8_t* dgu_scales, const uint8_t* wgu_t_codes,
+                                      const uint8_t* wgu_t_scales, const int32_t* mtile_prefix,
+                                      const int32_t* poff, void* dX_perm, int* status,
+                                      cudaStream_t st) {
+  return grouped_mx_f32("bwd_gate_up_dgrad", D, 2 * D.I, dgu_codes, dgu_scales, wgu_t_codes,
+                        wgu_t_scales, mtile_prefix, poff, dX_perm, status, st);
 }
 
 cudaError_t gemm_fwd_down(const Dims& D, const void* H, const void* w_down,
@@ -1490,7 +1486,8 @@ cudaError_t gemm_fwd_down(const Dims& D, const void* H, const void* w_down,
 cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* w_down,
                                 const int32_t* mtile_prefix, const int32_t* poff, const float* GU,
                                 const float* row_w, void* dGU_hi, void* dGU_lo, void* P_hi,
-                                void* P_lo, void* dGU_mx, float* dp_part, int* status,
+                                void* P_lo, uint8_t* dgu_codes, uint8_t* dgu_scales,
+                                float* dp_part, int* status,
                                 cudaStream_t st) {
   const int bn = D.bn_dgrad;
   CUtensorMap ta, tb, tg;
@@ -1522,8 +1519,10 @@ cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* 
   a.out2 = P_hi;
   a.out3 = dGU_lo;
   a.out4 = P_lo;
-  a.out5 = dGU_mx;
+  a.dgu_codes = dgu_codes;
+  a.dgu_scales = dgu_scales;
   a.mx = D.mx ? 1 : 0;
+  if (D.mx && (!dgu_codes || !dgu_scales)) return cudaErrorInvalidValue;
   a.in_gu = GU;
   a.row_w = row_w;
   a.dp_part = dp_part;

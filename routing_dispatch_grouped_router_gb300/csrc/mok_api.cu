@@ -246,9 +246,13 @@ void bwd_layout(const Dims& D, BwdWs* W) {
   W->xq_col = D.mx ? b.take(ns * rows * D.d * 2) : 0;
   // BF16 with micro-batches: each micro-batch's dispatched x rows
   W->x_def = (!D.mx && ns > 1) ? b.take(ns * rows * D.d * 2) : 0;
-  W->dgu_mx = D.mx ? b.take(rows * 2 * D.I * 2) : 0;
+  // MXFP8 operands of the gate/up dgrad: dG, dU codes and W_gate_up
+  // transposed ([E*d, 2I] codes), both with tiled scales
+  W->dgu_codes = D.mx ? b.take(rows * 2 * D.I) : 0;
+  W->dgu_scales = D.mx ? b.take(rows * 2 * D.I / 32) : 0;
   W->wd_col = D.mx ? b.take(wd) : 0;
-  W->wgu_col = D.mx ? b.take(wgu) : 0;
+  W->wgu_t_codes = D.mx ? b.take(wgu / 2) : 0;
+  W->wgu_t_scales = D.mx ? b.take(wgu / 64) : 0;
   // recompute of g, u: their fp32 rows, and the forward's MXFP8 operands
   W->gu = D.recompute_gu ? b.take(rows * 2 * D.I * 4) : 0;
   const bool rmx = D.recompute_gu && D.mx;  // MXFP8 operands of the recomputed gate/up GEMM
@@ -456,9 +460,11 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
   float* dx_perm = at<float>(workspace, B.dx_perm);
   float* dl_row = at<float>(workspace, B.dl_row);
   float* dl_tok = at<float>(workspace, B.dl_tok);
-  void* dgu_mx = D.mx ? at<char>(workspace, B.dgu_mx) : nullptr;
+  uint8_t* dgu_c = D.mx ? at<uint8_t>(workspace, B.dgu_codes) : nullptr;
+  uint8_t* dgu_s = D.mx ? at<uint8_t>(workspace, B.dgu_scales) : nullptr;
+  uint8_t* wgu_t_c = D.mx ? at<uint8_t>(workspace, B.wgu_t_codes) : nullptr;
+  uint8_t* wgu_t_s = D.mx ? at<uint8_t>(workspace, B.wgu_t_scales) : nullptr;
   const void* wd_op = w_down;
-  const void* wgu_op = w_gate_up;
   // MXFP8 operands of the recomputed gate/up GEMM (the forward's kernel)
   uint8_t* rwgu_c = at<uint8_t>(workspace, B.wgu_codes);
   uint8_t* rwgu_s = at<uint8_t>(workspace, B.wgu_scales);
@@ -468,13 +474,12 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
     MOK_CUDA(launch_mx_rows(w_gate_up, nullptr, D.E * 2 * D.I, D.d, rwgu_c, rwgu_s, st, true));
   if (D.mx) {
     // weights quantised once per call along the dgrads' reduction dims:
-    // W_down along d, W_gate_up along 2I (blocks of 32 rows)
+    // W_down along d (bf16 values, blocks of 32 rows), W_gate_up along 2I
+    // (E4M3 codes written K-major for the block-scaled gate/up dgrad)
     void* wd_q = at<char>(workspace, B.wd_col);
-    void* wgu_q = at<char>(workspace, B.wgu_col);
     MOK_CUDA(launch_mx_cols(w_down, wd_q, D.E * D.d, D.I, nullptr, nullptr, st));
-    MOK_CUDA(launch_mx_cols(w_gate_up, wgu_q, D.E * 2 * D.I, D.d, nullptr, nullptr, st));
+    MOK_CUDA(launch_mx_cols_t(w_gate_up, D.E * 2 * D.I, D.d, 2 * D.I, wgu_t_c, wgu_t_s, st));
     wd_op = wd_q;
-    wgu_op = wgu_q;
   }
   const size_t dx_esz = D.act_bf16 ? 2 : 4;
   // micro-batches in reverse, so the last ring slots are still resident.
@@ -537,8 +542,8 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
       void* q1 = at<char>(workspace, B.dyq_row);
       void* q2 = slot(at<char>(workspace, B.dyq_col), i, rows * D.d * 2);
       void* q3 = slot(at<char>(workspace, B.xq_col), i, rows * D.d * 2);
-      MOK_CUDA(launch_mx_rows(dy_perm_i, q1, D.rows_max, D.d, nullptr, nullptr, st));
-      MOK_CUDA(launch_mx_cols(dy_perm_i, q2, D.rows_max, D.d, nullptr, nullptr, st));
+      // dy in both block directions from one read
+      MOK_CUDA(launch_mx_cols(dy_perm_i, q2, D.rows_max, D.d, nullptr, nullptr, st, q1));
       MOK_CUDA(launch_mx_cols(x_perm, q3, D.rows_max, D.d, nullptr, nullptr, st));
       dy_row_op = q1;
       dy_col_op = q2;
@@ -547,14 +552,17 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
     // down-projection dgrad + SwiGLU backward + router-weight partials;
     // dG, dU and P = p h leave as bf16 hi/lo pairs (and dG, dU as MXFP8)
     MOK_CUDA(gemm_bwd_down_dgrad(D, dy_row_op, wd_op, mtp, poff, static_cast<const float*>(gu),
-                                 row_w, dgu_hi_i, dgu_lo_i, p_hi_i, p_lo_i, dgu_mx, dp_part,
+                                 row_w, dgu_hi_i, dgu_lo_i, p_hi_i, p_lo_i, dgu_c, dgu_s, dp_part,
                                  status, st));
     // down-projection wgrad: dW_down_e (+)= dY_e^T (P_hi + P_lo)_e
     if (!defer)
       MOK_CUDA(gemm_wgrad_down(D, dy_col_op, p_hi_i, p_lo_i, poff, dw_down, !first, status, st));
     // gate/up dgrad: dX_perm = dGU W_gu (fp32 rows)
-    MOK_CUDA(gemm_bwd_gate_up_dgrad(D, D.mx ? dgu_mx : dgu_hi_i, wgu_op, mtp, poff, dx_perm,
-                                    status, st));
+    if (D.mx)
+      MOK_CUDA(gemm_bwd_gate_up_dgrad_mx(D, dgu_c, dgu_s, wgu_t_c, wgu_t_s, mtp, poff, dx_perm,
+                                         status, st));
+    else
+      MOK_CUDA(gemm_bwd_gate_up_dgrad(D, dgu_hi_i, w_gate_up, mtp, poff, dx_perm, status, st));
     // gate/up wgrad: dW_gu_e (+)= (dGU_hi + dGU_lo)_e^T X_e
     if (!defer)
       MOK_CUDA(gemm_wgrad_gate_up(D, dgu_hi_i, dgu_lo_i, x_col_op, poff, dw_gate_up, !first,

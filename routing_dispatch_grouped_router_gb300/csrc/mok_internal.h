@@ -63,8 +63,8 @@ struct FwdWs {
 };
 struct BwdWs {
   size_t dy_perm, dgu_hi, dgu_lo, p_hi, p_lo, dp_part, dx_perm, dl_row, dl_tok, dyq_row, dyq_col,
-      xq_col, dgu_mx, wd_col, wgu_col, gu, xq_codes, xq_scales, wgu_codes, wgu_scales, x_def,
-      total;
+      xq_col, dgu_codes, dgu_scales, wd_col, wgu_t_codes, wgu_t_scales, gu, xq_codes, xq_scales,
+      wgu_codes, wgu_scales, x_def, total;
 };
 struct StageWs {
   size_t status, block_counts, block_base, padded_offsets, mtile_prefix, ppos, ptok, row_w,
@@ -146,8 +146,15 @@ cudaError_t gemm_fwd_down(const Dims& D, const void* H, const void* w_down,
 cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* w_down,
                                 const int32_t* mtile_prefix, const int32_t* poff, const float* GU,
                                 const float* row_w, void* dGU_hi, void* dGU_lo, void* P_hi,
-                                void* P_lo, void* dGU_mx, float* dp_part, int* status,
-                                cudaStream_t st);
+                                void* P_lo, uint8_t* dgu_codes, uint8_t* dgu_scales,
+                                float* dp_part, int* status, cudaStream_t st);
+// MXFP8: dX_perm = dGU W_gate_up per expert on the block-scaled tensor cores,
+// dGU as the codes B2 writes, W_gate_up as launch_mx_cols_t writes it.
+cudaError_t gemm_bwd_gate_up_dgrad_mx(const Dims& D, const uint8_t* dgu_codes,
+                                      const uint8_t* dgu_scales, const uint8_t* wgu_t_codes,
+                                      const uint8_t* wgu_t_scales, const int32_t* mtile_prefix,
+                                      const int32_t* poff, void* dX_perm, int* status,
+                                      cudaStream_t st);
 cudaError_t gemm_bwd_gate_up_dgrad(const Dims& D, const void* dGU, const void* w_gate_up,
                                    const int32_t* mtile_prefix, const int32_t* poff,
                                    void* dX_perm, int* status, cudaStream_t st);
@@ -186,8 +193,16 @@ cudaError_t gemm_dense_bf16(int64_t M, int64_t N, int64_t K, const void* A, bool
 // 128), the layout of the expert GEMMs' MXFP8 operands; else row-major.
 cudaError_t launch_mx_rows(const void* in, void* out, long long rows, long long cols,
                            uint8_t* codes, uint8_t* scales, cudaStream_t st, bool tiled = false);
+// Column blocks of a weight [rows = E*group_rows, cols] written as the K-major
+// operand [E*cols, group_rows]: E4M3 codes and tiled scales (group_rows % 128,
+// cols % 128).
+cudaError_t launch_mx_cols_t(const void* in, long long rows, long long cols, long long group_rows,
+                             uint8_t* codes, uint8_t* scales, cudaStream_t st);
+// Column blocks (rows % 32 == 0, cols % 8 == 0); rows_out != NULL also writes
+// the row-block dequantised values of the same input (cols % 32 == 0).
 cudaError_t launch_mx_cols(const void* in, void* out, long long rows, long long cols,
-                           uint8_t* codes, uint8_t* scales, cudaStream_t st);
+                           uint8_t* codes, uint8_t* scales, cudaStream_t st,
+                           void* rows_out = nullptr);
 
 // One CTA whose mbarrier wait can never complete: exercises the bounded wait.
 cudaError_t launch_bounded_wait_selftest(int* status, cudaStream_t st);

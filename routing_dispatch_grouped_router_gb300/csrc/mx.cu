@@ -15,134 +15,338 @@
 
 namespace mok {
 
-// E4M3 code and E8M0 scale byte of one dequantised value v' = q * 2^shared.
-__device__ __forceinline__ uint8_t e4m3_code_of(float vq, int shared) {
-  const uint16_t q = cvt_e4m3x2(vq * exp2i(-shared), 0.f);
-  return static_cast<uint8_t>(q >> 8);
-}
-
-__device__ __forceinline__ int mx_shared_exp(const float (&v)[32]) {
-  float amax = 0.f;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+// Shared exponent of a block from its largest magnitude (the rule above).
+__device__ __forceinline__ int mx_shared_of(float amax) {
   if (!(amax > 0.f)) return -127;
   int e;
-  frexpf(amax, &e);
+  frexpf(amax, &e);  // amax = m * 2^e with 0.5 <= m < 1
   const int s = e - 1 - 8;
   return s < -127 ? -127 : (s > 127 ? 127 : s);
 }
 
-// One thread per block of 32 consecutive values of a row.
+__device__ __forceinline__ void unpack8(const uint4& w, float (&v)[8]) {
+  v[0] = bf16lo(w.x); v[1] = bf16hi(w.x); v[2] = bf16lo(w.y); v[3] = bf16hi(w.y);
+  v[4] = bf16lo(w.z); v[5] = bf16hi(w.z); v[6] = bf16lo(w.w); v[7] = bf16hi(w.w);
+}
+
+__device__ __forceinline__ float amax8(const float (&v)[8]) {
+  float m = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
+  return m;
+}
+
+// Quantises 8 values, value j with the factors down[j] = 2^-shared_j and
+// up[j] = 2^shared_j: CODES gives the E4M3 codes (value j in byte j), DEQ the
+// dequantised values q * 2^shared rounded to bf16 (exact), packed as 8 bf16.
+template <bool CODES, bool DEQ>
+__device__ __forceinline__ void mx_quant8(const float (&v)[8], const float (&down)[8],
+                                          const float (&up)[8], uint2* codes, uint4* deq) {
+  uint32_t c[4], d[4];
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    // cvt packs its first operand into the upper byte
+    const uint16_t q = cvt_e4m3x2(v[j + 1] * down[j + 1], v[j] * down[j]);
+    c[j / 2] = q;
+    if (DEQ) {
+      float hi, lo;
+      e4m3x2_to_f32(q, &hi, &lo);
+      d[j / 2] = pack_bf16x2(lo * up[j], hi * up[j + 1]);
+    }
+  }
+  if (CODES) *codes = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+  if (DEQ) *deq = make_uint4(d[0], d[1], d[2], d[3]);
+}
+
+// The factors of one shared exponent for all 8 values.
+__device__ __forceinline__ void uniform_factors(int s, float (&down)[8], float (&up)[8]) {
+  const float dn = exp2i(-s), u = exp2i(s);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    down[j] = dn;
+    up[j] = u;
+  }
+}
+
+// Row blocks.  Four consecutive lanes hold one block of 32 values (8 each, one
+// 16-byte load), so a warp reads 512 contiguous bytes; the block maximum is
+// two shuffles.  Each lane keeps kRowUnroll independent chunks in flight.
+// The loop runs per warp (every lane takes the same trips) and nchunks is a
+// multiple of 4, so a block's four lanes are all in range or all out.
 // tiled_nkg > 0: scales in the tiled layout of a matrix with tiled_nkg*128
 // columns (mx_tiled_off); 0: row-major [rows, cols/32].
-__global__ void mx_rows_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
-                               uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                               long long nblocks, long long tiled_nkg) {
-  for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < nblocks;
-       b += (long long)gridDim.x * blockDim.x) {
-    float v[32];
+constexpr int kRowUnroll = 4;
+template <bool CODES, bool OUT>
+__global__ void __launch_bounds__(256) mx_rows_kernel(const uint4* __restrict__ in,
+                                                      uint4* __restrict__ out,
+                                                      uint8_t* __restrict__ codes,
+                                                      uint8_t* __restrict__ scales,
+                                                      long long nchunks, long long tiled_nkg) {
+  const int lane = threadIdx.x & 31;
+  const long long G = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i0 = static_cast<long long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+       i0 < nchunks; i0 += kRowUnroll * G) {
+    uint4 w[kRowUnroll];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint4 w = ld_global_nc_v4(in + b * 4 + j);
-      v[8 * j + 0] = bf16lo(w.x); v[8 * j + 1] = bf16hi(w.x);
-      v[8 * j + 2] = bf16lo(w.y); v[8 * j + 3] = bf16hi(w.y);
-      v[8 * j + 4] = bf16lo(w.z); v[8 * j + 5] = bf16hi(w.z);
-      v[8 * j + 6] = bf16lo(w.w); v[8 * j + 7] = bf16hi(w.w);
+    for (int u = 0; u < kRowUnroll; ++u) {
+      const long long c = i0 + lane + u * G;
+      w[u] = c < nchunks ? ld_global_nc_v4(in + c) : make_uint4(0, 0, 0, 0);
     }
-    if (codes || scales) {
-      uint32_t w[8];
-      const uint32_t sbyte = mx_encode32(v, w);
-      if (codes) {
-        uint4* c = reinterpret_cast<uint4*>(codes + b * 32);
-        c[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        c[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      }
-      if (scales) {
-        const long long off =
-            tiled_nkg > 0 ? mx_tiled_off(b / (tiled_nkg * 4), b % (tiled_nkg * 4), tiled_nkg) : b;
-        scales[off] = static_cast<uint8_t>(sbyte);
-      }
-    }
-    if (out) {  // NULL: codes and scales only
-      mx_fake32(v);
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        out[b * 4 + j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]),
-                                    pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
-                                    pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
-                                    pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+    for (int u = 0; u < kRowUnroll; ++u) {
+      const long long c = i0 + lane + u * G;
+      float v[8];
+      unpack8(w[u], v);
+      float m = amax8(v);
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      if (c >= nchunks) continue;
+      const int s = mx_shared_of(m);
+      float down[8], up[8];
+      uniform_factors(s, down, up);
+      uint2 q;
+      uint4 deq;
+      mx_quant8<CODES, OUT>(v, down, up, &q, &deq);
+      if (CODES) reinterpret_cast<uint2*>(codes)[c] = q;
+      if (OUT) out[c] = deq;
+      if (scales && (lane & 3) == 0) {
+        // block index below 2^32 (checked by the launcher): 32-bit division
+        const uint32_t b = static_cast<uint32_t>(c >> 2);
+        const uint32_t bpr = static_cast<uint32_t>(tiled_nkg) * 4;  // blocks per row
+        const long long off = tiled_nkg > 0 ? mx_tiled_off(b / bpr, b % bpr, tiled_nkg) : b;
+        scales[off] = static_cast<uint8_t>(s + 127);
+      }
     }
   }
 }
 
-// One thread per (32-row block, pair of adjacent columns): the two columns'
-// blocks are quantised independently; loads and stores move bf16 pairs.
-__global__ void mx_cols_kernel(const __nv_bfloat162* __restrict__ in,
-                               __nv_bfloat162* __restrict__ out, uint8_t* __restrict__ codes,
-                               uint8_t* __restrict__ scales, long long row_blocks, long long cols) {
-  const long long cp = cols / 2;  // column pairs
-  const long long n = row_blocks * cp;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
-       i += (long long)gridDim.x * blockDim.x) {
-    const long long rb = i / cp, c2 = i - rb * cp;
-    const long long base = rb * 32 * cp + c2;
-    float v0[32], v1[32];
+// Column blocks, one 32-row x 256-column tile per CTA trip (256 threads).
+// Warp w loads rows w, w+8, w+16, w+24 of the tile and lane l columns
+// 8l..8l+7 (16-byte loads, 512 contiguous bytes per warp and row).  The 32-row
+// column maxima meet in shared memory; each thread then quantises its own 32
+// values with its 8 columns' exponents.  ROWS_OUT (cols % 32 == 0): the same
+// tile is also quantised in row blocks (four lanes per block, as in
+// mx_rows_kernel) into rows_out, so both layouts cost one read.
+template <bool CODES, bool OUT, bool ROWS_OUT>
+__global__ void __launch_bounds__(256, ROWS_OUT ? 3 : 4) mx_cols_kernel(const uint4* __restrict__ in,
+                                                         uint4* __restrict__ out,
+                                                         uint8_t* __restrict__ codes,
+                                                         uint8_t* __restrict__ scales,
+                                                         uint4* __restrict__ rows_out,
+                                                         long long row_blocks, long long cols) {
+  __shared__ __align__(16) float s_part[8][256];
+  __shared__ __align__(16) int s_exp[256];
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const long long c8 = cols / 8;  // 16-byte chunks per row
+  // tile counts below 2^31 (checked by the launcher): 32-bit division
+  const uint32_t tiles_c = static_cast<uint32_t>((cols + 255) / 256);
+  const uint32_t ntiles = static_cast<uint32_t>(row_blocks) * tiles_c;
+  for (uint32_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const long long rb = t / tiles_c, tc = t - static_cast<uint32_t>(rb) * tiles_c;
+    const long long ch = tc * 32 + l;  // this lane's chunk of each row
+    const bool ok = ch < c8;
+    uint4 x[4];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float2 f = __bfloat1622float2(in[base + j * cp]);
-      v0[j] = f.x;
-      v1[j] = f.y;
+    for (int r = 0; r < 4; ++r)
+      x[r] = ok ? ld_global_nc_v4(in + (rb * 32 + w + 8 * r) * c8 + ch) : make_uint4(0, 0, 0, 0);
+    float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      float v[8];
+      unpack8(x[r], v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) part[j] = fmaxf(part[j], fabsf(v[j]));
     }
-    const int s0 = mx_shared_exp(v0), s1 = mx_shared_exp(v1);
-    mx_fake32(v0);
-    mx_fake32(v1);
+    reinterpret_cast<float4*>(&s_part[w][8 * l])[0] = make_float4(part[0], part[1], part[2], part[3]);
+    reinterpret_cast<float4*>(&s_part[w][8 * l])[1] = make_float4(part[4], part[5], part[6], part[7]);
+    __syncthreads();
+    {
+      float m = 0.f;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) out[base + j * cp] = __floats2bfloat162_rn(v0[j], v1[j]);
-    const long long c = 2 * c2;
-    if (codes) {
-      const long long cb = rb * 32 * cols + c;
+      for (int k = 0; k < 8; ++k) m = fmaxf(m, s_part[k][threadIdx.x]);
+      const int s = mx_shared_of(m);
+      s_exp[threadIdx.x] = s;
+      const long long col = tc * 256 + threadIdx.x;
+      if (scales && col < cols) scales[rb * cols + col] = static_cast<uint8_t>(s + 127);
+    }
+    __syncthreads();
+    if (ok && (CODES || OUT)) {
+      const int4 e0 = reinterpret_cast<const int4*>(&s_exp[8 * l])[0];
+      const int4 e1 = reinterpret_cast<const int4*>(&s_exp[8 * l])[1];
+      const int sh[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+      float down[8], up[8];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const uint16_t pair = static_cast<uint16_t>(e4m3_code_of(v0[j], s0)) |
-                              (static_cast<uint16_t>(e4m3_code_of(v1[j], s1)) << 8);
-        *reinterpret_cast<uint16_t*>(codes + cb + j * cols) = pair;
+      for (int j = 0; j < 8; ++j) {
+        down[j] = exp2i(-sh[j]);
+        up[j] = exp2i(sh[j]);
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const long long idx = (rb * 32 + w + 8 * r) * c8 + ch;
+        float v[8];
+        unpack8(x[r], v);
+        uint2 q;
+        uint4 deq;
+        mx_quant8<CODES, OUT>(v, down, up, &q, &deq);
+        if (CODES) reinterpret_cast<uint2*>(codes)[idx] = q;
+        if (OUT) out[idx] = deq;
       }
     }
-    if (scales) {
-      scales[rb * cols + c] = static_cast<uint8_t>(s0 + 127);
-      scales[rb * cols + c + 1] = static_cast<uint8_t>(s1 + 127);
+    if (ROWS_OUT) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        float v[8];
+        unpack8(x[r], v);
+        float m = amax8(v);
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        if (!ok) continue;
+        float down[8], up[8];
+        uniform_factors(mx_shared_of(m), down, up);
+        uint2 q;
+        uint4 deq;
+        mx_quant8<false, true>(v, down, up, &q, &deq);
+        rows_out[(rb * 32 + w + 8 * r) * c8 + ch] = deq;
+      }
     }
+  }
+}
+
+// Column blocks written transposed, for a weight stored [E*G rows, C cols]
+// (G rows per expert) that an MMA needs K-major along G: the E4M3 codes go to
+// [E*C rows, G cols] (row e*C + c holds expert e's column c) with the scales
+// in the tiled layout of that matrix (mx_tiled_off, G/128 K groups).  One warp
+// per 32-row block and 64 columns: lane l holds columns 2l, 2l+1 of the 32
+// rows (bf16 pairs, 128 contiguous bytes per warp and row), so each lane has
+// two whole blocks and writes each block's 32 codes as one 32-byte run.
+__global__ void __launch_bounds__(256) mx_cols_t_kernel(const uint32_t* __restrict__ in,
+                                                        uint8_t* __restrict__ codes,
+                                                        uint8_t* __restrict__ scales,
+                                                        uint32_t row_blocks, uint32_t cols,
+                                                        uint32_t group_rows) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t cp = cols / 2;          // bf16 pairs per row
+  const uint32_t groups_c = cols / 64;   // 64-column groups per row
+  const uint32_t kb = group_rows / 32;   // 32-row blocks per expert
+  const uint32_t n_kg = group_rows / 128;
+  const uint32_t nwork = row_blocks * groups_c;
+  const uint32_t nwarps = gridDim.x * (blockDim.x / 32);
+  for (uint32_t wi = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; wi < nwork;
+       wi += nwarps) {
+    const uint32_t rb = wi / groups_c, cg = wi - rb * groups_c;
+    const uint32_t e = rb / kb, j = rb - e * kb;
+    const uint32_t c2 = cg * 32 + lane;
+    uint32_t x[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      const uint32_t* p = in + (static_cast<long long>(rb) * 32 + r) * cp + c2;
+      asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(x[r]) : "l"(p));
+    }
+    float m0 = 0.f, m1 = 0.f;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      m0 = fmaxf(m0, fabsf(bf16lo(x[r])));
+      m1 = fmaxf(m1, fabsf(bf16hi(x[r])));
+    }
+    const int s0 = mx_shared_of(m0), s1 = mx_shared_of(m1);
+    const float d0 = exp2i(-s0), d1 = exp2i(-s1);
+    uint32_t w0[8], w1[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      // cvt packs its first operand into the upper byte: rows 4i..4i+3 in order
+      const uint32_t a01 = cvt_e4m3x2(bf16lo(x[4 * i + 1]) * d0, bf16lo(x[4 * i]) * d0);
+      const uint32_t a23 = cvt_e4m3x2(bf16lo(x[4 * i + 3]) * d0, bf16lo(x[4 * i + 2]) * d0);
+      const uint32_t b01 = cvt_e4m3x2(bf16hi(x[4 * i + 1]) * d1, bf16hi(x[4 * i]) * d1);
+      const uint32_t b23 = cvt_e4m3x2(bf16hi(x[4 * i + 3]) * d1, bf16hi(x[4 * i + 2]) * d1);
+      w0[i] = a01 | (a23 << 16);
+      w1[i] = b01 | (b23 << 16);
+    }
+    const long long orow = static_cast<long long>(e) * cols + 2 * c2;  // column 2*c2's row
+    uint4* o0 = reinterpret_cast<uint4*>(codes + orow * group_rows + j * 32);
+    uint4* o1 = reinterpret_cast<uint4*>(codes + (orow + 1) * group_rows + j * 32);
+    o0[0] = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+    o0[1] = make_uint4(w0[4], w0[5], w0[6], w0[7]);
+    o1[0] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+    o1[1] = make_uint4(w1[4], w1[5], w1[6], w1[7]);
+    scales[mx_tiled_off(orow, j, n_kg)] = static_cast<uint8_t>(s0 + 127);
+    scales[mx_tiled_off(orow + 1, j, n_kg)] = static_cast<uint8_t>(s1 + 127);
   }
 }
 
 static unsigned grid_for(long long n, int threads) {
   long long g = (n + threads - 1) / threads;
-  const long long cap = static_cast<long long>(num_sms_current_device()) * 16;
+  const long long cap = static_cast<long long>(num_sms_current_device()) * 8;
   if (g > cap) g = cap;
   return static_cast<unsigned>(g < 1 ? 1 : g);
 }
 
 cudaError_t launch_mx_rows(const void* in, void* out, long long rows, long long cols,
                            uint8_t* codes, uint8_t* scales, cudaStream_t st, bool tiled) {
+  if (cols % 32) return cudaErrorInvalidValue;
   if (tiled && (rows % 128 || cols % 128)) return cudaErrorInvalidValue;
-  const long long nb = rows * (cols / 32);
-  if (nb == 0) return cudaSuccess;
+  const long long nchunks = rows * (cols / 8);
+  if (nchunks == 0) return cudaSuccess;
+  if (nchunks / 4 >= (1LL << 32)) return cudaErrorInvalidValue;  // 32-bit block index
   ProfScope prof("mx_quant_rows", st);
-  mx_rows_kernel<<<grid_for(nb, 256), 256, 0, st>>>(static_cast<const uint4*>(in),
-                                                    static_cast<uint4*>(out), codes, scales, nb,
-                                                    tiled ? cols / 128 : 0);
+  const unsigned grid = grid_for((nchunks + kRowUnroll - 1) / kRowUnroll, 256);
+  const uint4* i4 = static_cast<const uint4*>(in);
+  uint4* o4 = static_cast<uint4*>(out);
+  const long long nkg = tiled ? cols / 128 : 0;
+  if (codes && out)
+    mx_rows_kernel<true, true><<<grid, 256, 0, st>>>(i4, o4, codes, scales, nchunks, nkg);
+  else if (codes)
+    mx_rows_kernel<true, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, nchunks, nkg);
+  else if (out)
+    mx_rows_kernel<false, true><<<grid, 256, 0, st>>>(i4, o4, codes, scales, nchunks, nkg);
+  else
+    mx_rows_kernel<false, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, nchunks, nkg);
   count_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_mx_cols(const void* in, void* out, long long rows, long long cols,
-                           uint8_t* codes, uint8_t* scales, cudaStream_t st) {
-  const long long n = (rows / 32) * (cols / 2);
-  if (n == 0) return cudaSuccess;
+                           uint8_t* codes, uint8_t* scales, cudaStream_t st, void* rows_out) {
+  if (rows % 32 || cols % 8 || (rows_out && (cols % 32 || !out || codes)))
+    return cudaErrorInvalidValue;
+  const long long ntiles = (rows / 32) * ((cols + 255) / 256);
+  if (ntiles == 0) return cudaSuccess;
+  if (ntiles >= (1LL << 31)) return cudaErrorInvalidValue;
   ProfScope prof("mx_quant_cols", st);
-  mx_cols_kernel<<<grid_for(n, 256), 256, 0, st>>>(static_cast<const __nv_bfloat162*>(in),
-                                                   static_cast<__nv_bfloat162*>(out), codes,
-                                                   scales, rows / 32, cols);
+  const long long cap = static_cast<long long>(num_sms_current_device()) * 8;
+  const unsigned grid = static_cast<unsigned>(ntiles < cap ? ntiles : cap);
+  const uint4* i4 = static_cast<const uint4*>(in);
+  uint4* o4 = static_cast<uint4*>(out);
+  uint4* r4 = static_cast<uint4*>(rows_out);
+  const long long rb = rows / 32;
+  if (rows_out)  // the layer's dy: bf16 values in both directions
+    mx_cols_kernel<false, true, true><<<grid, 256, 0, st>>>(i4, o4, codes, scales, r4, rb, cols);
+  else if (codes && out)
+    mx_cols_kernel<true, true, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, r4, rb, cols);
+  else if (codes)
+    mx_cols_kernel<true, false, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, r4, rb, cols);
+  else if (out)
+    mx_cols_kernel<false, true, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, r4, rb, cols);
+  else
+    mx_cols_kernel<false, false, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, r4, rb, cols);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_cols_t(const void* in, long long rows, long long cols, long long group_rows,
+                             uint8_t* codes, uint8_t* scales, cudaStream_t st) {
+  if (group_rows <= 0 || group_rows % 128 || rows % group_rows || cols % 128 || !codes ||
+      !scales)
+    return cudaErrorInvalidValue;
+  const long long nwork = (rows / 32) * (cols / 64);
+  if (nwork == 0) return cudaSuccess;
+  if (nwork >= (1LL << 31) || cols >= (1LL << 31) || group_rows >= (1LL << 31))
+    return cudaErrorInvalidValue;
+  ProfScope prof("mx_quant_cols", st);
+  const long long blocks = (nwork + 7) / 8;  // 8 warps per CTA
+  const long long cap = static_cast<long long>(num_sms_current_device()) * 8;
+  mx_cols_t_kernel<<<static_cast<unsigned>(blocks < cap ? blocks : cap), 256, 0, st>>>(
+      static_cast<const uint32_t*>(in), codes, scales, static_cast<uint32_t>(rows / 32),
+      static_cast<uint32_t>(cols), static_cast<uint32_t>(group_rows));
   count_launch();
   return cudaGetLastError();
 }
@@ -154,9 +358,10 @@ using namespace mok;
 extern "C" mok_status mok_mx_quantize(const void* in, int64_t rows, int64_t cols, int along_rows,
                                       void* out, uint8_t* codes, uint8_t* scales, void* stream) {
   if (rows < 0 || cols < 0 || (rows * cols > 0 && (!in || !out))) return MOK_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) & 15u)
+  if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out) |
+       reinterpret_cast<uintptr_t>(codes)) & 15u)
     return MOK_ERR_INVALID_ARG;
-  if (along_rows ? (rows % 32 || cols % 2) : (cols % 32)) return MOK_ERR_UNSUPPORTED;
+  if (along_rows ? (rows % 32 || cols % 8) : (cols % 32)) return MOK_ERR_UNSUPPORTED;
   const mok_status s = mok_check_device();
   if (s != MOK_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

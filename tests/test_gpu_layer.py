@@ -320,16 +320,20 @@ def test_micro_batched_deterministic(dtype):
 # ------------------------------------------------------------------ MXFP8 ---
 
 @pytest.mark.parametrize("along_rows", [False, True])
-def test_mx_quantize_bit_exact(along_rows):
+@pytest.mark.parametrize("shape", [(96, 160), (352, 1056)])
+def test_mx_quantize_bit_exact(along_rows, shape):
+    """(352, 1056): the column quantiser's 32 x 256 tiles, eleven row blocks by
+    five column tiles, the last 32 columns wide."""
+    rows, cols = shape
     rng = np.random.default_rng(7)
-    a = rng.standard_normal((96, 160)).astype(np.float32) * np.exp(
-        rng.uniform(-30, 30, (96, 1)).astype(np.float32))
+    a = rng.standard_normal((rows, cols)).astype(np.float32) * np.exp(
+        rng.uniform(-30, 30, (rows, 1)).astype(np.float32))
     a[5, :32] = 0.0
     a[:32, 7] = 0.0
     bits = gen.f32_to_bf16_bits(a)
     x = _gpu.dev_bf16(bits)
     codes = torch.empty(a.shape, dtype=torch.uint8, device="cuda")
-    nsc = (96 // 32, 160) if along_rows else (96, 160 // 32)
+    nsc = (rows // 32, cols) if along_rows else (rows, cols // 32)
     scales = torch.empty(nsc, dtype=torch.uint8, device="cuda")
     out = api.mx_quantize(x, along_rows, codes=codes, scales=scales)
     ref, shared = oracle.mx_quantize(gen.bf16_bits_to_f32(bits).astype(np.float64),
