@@ -116,8 +116,9 @@ def mover_bytes(shape: gen.Shape, micro_batches: int = 1) -> dict:
                      shape.I)
     np_ = 2 * I // (256 if I % 256 == 0 else 128)
     return {
-        # read each token row once per routed copy, write R bf16 rows (+ indices)
-        "gather_rows": R * 2 * d * 2 + R * 4,
+        # read each token row once (its other k-1 copies come from L2), write R
+        # bf16 rows, read the row indices
+        "gather_rows": T * d * 2 + R * d * 2 + R * 4,
         # read k fp32 expert rows + weights per token, write the fp32 token row
         "combine": R * 4 * d + T * 4 * d + R * 8,
         # read k fp32 dX rows and the dp partials, write fp32 dx (router rows from L2)
@@ -125,6 +126,39 @@ def mover_bytes(shape: gen.Shape, micro_batches: int = 1) -> dict:
         # read the dispatched bf16 rows once, write dW_r
         "router_wgrad": R * 2 * d + E * d * 4,
     }
+
+
+def mover_write_bytes(shape: gen.Shape, micro_batches: int = 1) -> dict:
+    """Bytes each data-movement launch writes (part of mover_bytes)."""
+    R, d, T, E = shape.R // micro_batches, shape.d, shape.T // micro_batches, shape.E
+    return {"gather_rows": R * d * 2, "combine": T * d * 4, "reverse_dispatch": T * d * 4,
+            "router_wgrad": E * d * 4}
+
+
+def mover_roofline_us(total_bytes: float, write_bytes: float, copy_gbs: float,
+                      write_gbs: float) -> float:
+    """Shortest time for a launch that moves total_bytes, write_bytes of them
+    written: HBM moves at most copy_gbs in both directions together and
+    write_gbs of writes alone."""
+    return max(total_bytes / copy_gbs, write_bytes / write_gbs) / 1e3
+
+
+def measure_write_gbs(torch) -> float:
+    """HBM write bandwidth on this GPU: a 1 GiB zero fill (library kernel),
+    best of 5 CUDA-event timings, after one warm-up."""
+    buf = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    buf.zero_()
+    best = None
+    for _ in range(5):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        buf.zero_()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+        best = ms if best is None else min(best, ms)
+    del buf
+    return (1 << 30) / (best / 1e3) / 1e9
 
 
 def load_peaks():
@@ -500,10 +534,19 @@ def main():
     gg_fl = sum(flops[n] * kernels[n][0] for n in gg)
     gg_tflops = gg_fl / (gg_ms / 1e3) / 1e12 if gg_ms else 0.0
     movers_perf = {}
+    write_gbs = measure_write_gbs(torch)
+    wbytes = mover_write_bytes(shape, int(layer.layout.mb_count))
     for n, b in movers.items():
         if n in kernels:
-            gbs = b / (kernels[n][1] / kernels[n][0] / 1e3) / 1e9
+            avg_us = kernels[n][1] / kernels[n][0] * 1e3
+            gbs = b / (avg_us / 1e6) / 1e9
             movers_perf[n] = {"GB/s": gbs, "frac_hbm": gbs / peaks["hbm"]}
+            if n in wbytes:
+                # against the copy bandwidth and the measured write bandwidth
+                # together: write-heavy movers (the gather) are bound by the latter
+                roof_us = mover_roofline_us(b, wbytes[n], peaks["hbm"], write_gbs)
+                movers_perf[n]["frac_roofline"] = roof_us / avg_us
+    movers_perf["write_bw_gbs"] = write_gbs
 
     # ---- end to end through the C ABI: every step's x, dy uploaded from
     # pinned host memory and its y, dx read back to pinned host memory.  The

@@ -138,11 +138,30 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// The same copy with an L2 eviction-priority policy (createpolicy).
+__device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint32_t bytes,
+                                               uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 // 1-D bulk copy shared -> global, tracked by bulk groups.
 __device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
                    reinterpret_cast<uint64_t>(dst)),
                "r"(smem_addr(src)), "r"(bytes)
+               : "memory");
+}
+
+// The same store with an L2 eviction-priority policy.
+__device__ __forceinline__ void bulk_store_hint(void* dst, const void* src, uint32_t bytes,
+                                                uint64_t policy) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::
+                   "l"(reinterpret_cast<uint64_t>(dst)),
+               "r"(smem_addr(src)), "r"(bytes), "l"(policy)
                : "memory");
 }
 

@@ -334,67 +334,95 @@ cudaError_t launch_plan(const Dims& D, const int32_t* topk_idx, const float* top
 
 // ------------------------------------------------------------- row gather --
 
-// Destination-driven ("pull") gather staged through TMA: for every padded row
-// r < padded_offsets[E], one thread moves src[ptok[r]] global -> shared with
-// a bulk copy completing on an mbarrier, then shared -> global with a bulk
-// store.  Padding rows are stored from a zeroed slot.  NSLOT copies are in
-// flight per CTA.
-constexpr int kGatherSlots = 4;
-constexpr int kGatherCtasPerSm = 4;
+// Destination-driven ("pull") gather staged through TMA: padded row r <
+// padded_offsets[E] receives src[ptok[r]], or zeros for a padding row.  CTA b
+// (one warp) moves rows b, b + G, b + 2G, ... (G CTAs), so at any moment the
+// grid writes one compact window of consecutive rows.  Rows pass through a
+// ring of `nslot` row-sized shared-memory slots: a bulk copy global -> shared
+// completing on the slot's mbarrier, then a bulk store shared -> global.  A
+// slot is refilled kGatherLag rows after its store was issued, so up to
+// kGatherLag + 1 stores and nslot - kGatherLag - 1 loads are in flight.  The
+// row indices come through a 128-entry shared ring that the warp refills 32
+// at a time, each refill's loads issued 16 rows before they are written, so
+// the issuing lane never waits on an index load.  A padding row's slot is
+// zeroed by the warp and stored like any other, so every row commits exactly
+// one bulk group and the lag counts rows.  Token rows are read with an L2
+// evict-last policy (each is read k times) and the output rows are stored
+// evict-first (a stream larger than L2 that should not displace them).
+constexpr int kGatherLag = 2;
+constexpr int kGatherMaxSlots = 32;
+constexpr int kGatherIdx = 128;
 
 __global__ void __launch_bounds__(32) gather_rows_kernel(const uint8_t* __restrict__ src,
                                                          const int32_t* __restrict__ ptok,
                                                          const int32_t* __restrict__ poff_end,
-                                                         int T, uint32_t row_bytes,
+                                                         int T, uint32_t row_bytes, int nslot,
                                                          uint8_t* __restrict__ dst, int* status) {
   extern __shared__ __align__(128) uint8_t gsm[];
-  __shared__ __align__(8) uint64_t full[kGatherSlots];
-  uint8_t* zero_slot = gsm + kGatherSlots * row_bytes;
+  __shared__ __align__(8) uint64_t full[kGatherMaxSlots];
+  __shared__ int s_tok[kGatherIdx];
   const int lane = threadIdx.x;
   const long long P = *poff_end;  // padded rows in use
   const long long G = gridDim.x;
   const long long first = blockIdx.x;
-  const long long n_my = (P > first) ? (P - first + G - 1) / G : 0;
-  for (uint32_t i = lane * 16; i < row_bytes; i += 32 * 16)
-    *reinterpret_cast<uint4*>(zero_slot + i) = make_uint4(0, 0, 0, 0);
+  const long long n = (P > first) ? (P - first + G - 1) / G : 0;  // rows of this CTA
+  if (n <= 0) return;  // the whole warp
   if (lane == 0) {
-    for (int s = 0; s < kGatherSlots; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < nslot; ++s) mbar_init(&full[s], 1);
     fence_barrier_init();
   }
-  fence_proxy_async_smem();
+  // indices of this CTA's rows 0..95; rows 96..127 come with the first refill
+  for (int i = lane; i < kGatherIdx - 32; i += 32) s_tok[i] = i < n ? ptok[first + i * G] : -1;
   __syncwarp();
-  if (lane != 0 || n_my == 0) return;
-
-  auto row_of = [&](long long j) { return first + j * G; };
-  auto issue = [&](long long j) {
-    const int s = static_cast<int>(j % kGatherSlots);
-    const int t = ptok[row_of(j)];
+  const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
+  auto issue = [&](long long j) {  // lane 0: this CTA's row j into its slot
+    const int s = static_cast<int>(j % nslot);
+    const int t = s_tok[j % kGatherIdx];
     if (t >= 0 && t < T) {
       mbar_arrive_expect_tx(&full[s], row_bytes);
-      bulk_load(gsm + s * row_bytes, src + static_cast<long long>(t) * row_bytes, row_bytes,
-                &full[s]);
+      bulk_load_hint(gsm + static_cast<size_t>(s) * row_bytes,
+                     src + static_cast<long long>(t) * row_bytes, row_bytes, &full[s], keep);
     } else {
-      mbar_arrive(&full[s]);
+      mbar_arrive(&full[s]);  // padding: the warp zeroes the slot at store time
     }
   };
-  const long long pro = n_my < kGatherSlots ? n_my : kGatherSlots;
-  for (long long j = 0; j < pro; ++j) issue(j);
+  if (lane == 0) {
+    const long long pro = n < nslot ? n : nslot;
+    for (long long j = 0; j < pro; ++j) issue(j);
+  }
   const int never = 0;
-  for (long long j = 0; j < n_my; ++j) {
-    const int s = static_cast<int>(j % kGatherSlots);
-    const uint32_t par = static_cast<uint32_t>((j / kGatherSlots) & 1);
-    if (!mbar_wait(&full[s], par, &never)) set_status(status, MOK_ERR_DEVICE_TIMEOUT);
-    const long long r = row_of(j);
-    const int t = ptok[r];
-    const uint8_t* from = (t >= 0 && t < T) ? gsm + s * row_bytes : zero_slot;
-    bulk_store(dst + r * row_bytes, from, row_bytes);
-    bulk_commit();
-    if (j + kGatherSlots < n_my) {
-      bulk_wait_read<0>();  // slot s has been read out
-      issue(j + kGatherSlots);
+  int pend = -1;  // the index refill in flight
+  for (long long j = 0; j < n; ++j) {
+    __syncwarp();
+    if ((j & 31) == 0) {
+      const long long jj = j + (kGatherIdx - 32) + lane;
+      pend = jj < n ? ptok[first + jj * G] : -1;
+    } else if ((j & 31) == 16) {
+      s_tok[(j - 16 + (kGatherIdx - 32) + lane) % kGatherIdx] = pend;
+    }
+    const int s = static_cast<int>(j % nslot);
+    uint8_t* slot = gsm + static_cast<size_t>(s) * row_bytes;
+    const int t = s_tok[j % kGatherIdx];
+    if (!(t >= 0 && t < T)) {
+      for (uint32_t i = lane * 16; i < row_bytes; i += 32 * 16)
+        *reinterpret_cast<uint4*>(slot + i) = make_uint4(0, 0, 0, 0);
+      fence_proxy_async_smem();
+    }
+    __syncwarp();
+    if (lane == 0) {
+      const uint32_t par = static_cast<uint32_t>((j / nslot) & 1);
+      if (!mbar_wait(&full[s], par, &never)) set_status(status, MOK_ERR_DEVICE_TIMEOUT);
+      bulk_store_hint(dst + (first + j * G) * row_bytes, slot, row_bytes, stream);
+      bulk_commit();
+      // the store of row j - lag has read its slot: refill it with row j - lag + nslot
+      const long long r = j - kGatherLag + nslot;
+      if (j >= kGatherLag && r < n) {
+        bulk_wait_read<kGatherLag>();
+        issue(r);
+      }
     }
   }
-  bulk_wait_all<0>();
+  if (lane == 0) bulk_wait_all<0>();
 }
 
 cudaError_t launch_gather_rows(const Dims& D, const void* src, const int32_t* ptok,
@@ -402,22 +430,29 @@ cudaError_t launch_gather_rows(const Dims& D, const void* src, const int32_t* pt
                                cudaStream_t st) {
   if (D.T == 0) return cudaSuccess;
   const uint32_t row_bytes = static_cast<uint32_t>(D.d * 2);
-  const int smem = static_cast<int>((kGatherSlots + 1) * row_bytes);
-  static bool attr = false;
-  if (!attr) {
+  // about 200 KB of slots per SM, split over up to four CTAs of at least six
+  // slots each (d <= 16384: one CTA of six 32 KB slots at the largest)
+  constexpr int kSmemPerSm = 200 * 1024;
+  int per_sm = static_cast<int>(kSmemPerSm / (6 * row_bytes));
+  per_sm = per_sm > 4 ? 4 : (per_sm < 1 ? 1 : per_sm);
+  int nslot = static_cast<int>((kSmemPerSm / per_sm) / row_bytes);
+  nslot = nslot > kGatherMaxSlots ? kGatherMaxSlots : nslot;
+  if (nslot < kGatherLag + 2) return cudaErrorInvalidValue;
+  const int smem = nslot * static_cast<int>(row_bytes);
+  static int attr = 0;
+  if (smem > attr) {
     cudaError_t e = cudaFuncSetAttribute(gather_rows_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (kGatherSlots + 1) * 16384 * 2);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attr = true;
+    attr = smem;
   }
-  long long grid = static_cast<long long>(num_sms_current_device()) * kGatherCtasPerSm;
+  long long grid = static_cast<long long>(num_sms_current_device()) * per_sm;
   const long long rows_cap = D.rows_max;
   if (grid > rows_cap) grid = rows_cap;
   ProfScope prof("gather_rows", st);
   gather_rows_kernel<<<static_cast<unsigned>(grid), 32, smem, st>>>(
       static_cast<const uint8_t*>(src), ptok, padded_offsets + D.E, static_cast<int>(D.T),
-      row_bytes, static_cast<uint8_t*>(dst), status);
+      row_bytes, nslot, static_cast<uint8_t*>(dst), status);
   count_launch();
   return cudaGetLastError();
 }

@@ -37,7 +37,8 @@ def test_mover_bytes_follow_the_fp32_row_layout():
     m = bench.mover_bytes(s)
     R, T, d = s.T * s.k, s.T, s.d
     assert m["combine"] == R * d * 4 + T * d * 4 + R * 8
-    assert m["gather_rows"] == 2 * R * d * 2 + R * 4
+    # unique bytes: x read once, R rows written
+    assert m["gather_rows"] == T * d * 2 + R * d * 2 + R * 4
 
 
 def test_workload_options():
@@ -83,3 +84,14 @@ def test_reference_arm_prints_one_json_line():
     assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "tokens/s"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["config"]["workload"].startswith("tiny")
+
+
+def test_mover_roofline_takes_the_tighter_bound():
+    # 1 GB moved, 0.9 GB of it written: at 6.7 TB/s copy and 4 TB/s writes
+    # the writes bind (225 us > 149 us)
+    assert bench.mover_roofline_us(1e9, 0.9e9, 6700.0, 4000.0) == pytest.approx(225.0)
+    assert bench.mover_roofline_us(2e9, 0.2e9, 6700.0, 4000.0) == pytest.approx(2e9 / 6700.0 / 1e3)
+    s = gen.workload_shape("fine")
+    w, m = bench.mover_write_bytes(s), bench.mover_bytes(s)
+    for n in w:
+        assert 0 < w[n] < m[n]
