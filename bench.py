@@ -72,16 +72,54 @@ def gemm_flops(shape: gen.Shape, micro_batches: int = 1) -> dict:
     return f
 
 
+def gemm_bytes(shape: gen.Shape, micro_batches: int = 1, mx: bool = False,
+               wgrad_elem_bytes: int = 4) -> dict:
+    """Algorithmic HBM bytes of one launch of each grouped GEMM in the layer's
+    layout, as (total, written): every operand read once, every output written
+    once.  Forward: bf16 rows, weights, fp32 g/u and O, bf16 h.  Backward:
+    the SwiGLU backward reads fp32 g/u and writes dG/dU and p*h as bf16 hi/lo
+    pairs; the dgrads write fp32 rows; the weight gradients read their hi/lo
+    operand and write dW (fp32 by default).  MXFP8: E4M3 codes (+1/32 scale
+    byte) for the block-scaled GEMMs' operands.  A deferred weight gradient
+    reads every micro-batch's operands and writes dW once."""
+    R, d, I, E = shape.R // micro_batches, shape.d, shape.I, shape.E
+    wgu, wd = E * 2 * I * d, E * d * I
+    q8 = 1 + 1 / 32
+    a_gu, w_gu = (R * d * q8, wgu * q8) if mx else (R * d * 2, wgu * 2)
+    h_out = R * I * q8 if mx else R * I * 2
+    f = {
+        "fwd_gate_up_swiglu": (a_gu + w_gu + R * 2 * I * 4 + h_out, R * 2 * I * 4 + h_out),
+        "fwd_down": ((R * I * q8 + wd * q8) if mx else (R * I * 2 + wd * 2)) + R * d * 4,
+        "bwd_down_dgrad_swiglu": R * d * 2 + wd * 2 + R * 2 * I * 4 + R * 2 * I * 4 + R * I * 4
+                                 + (R * 2 * I * q8 if mx else 0),
+        "bwd_gate_up_dgrad": ((R * 2 * I * q8 + wgu * q8) if mx else (R * 2 * I * 2 + wgu * 2))
+                             + R * d * 4,
+    }
+    w = {
+        "fwd_gate_up_swiglu": f["fwd_gate_up_swiglu"][1],
+        "fwd_down": R * d * 4,
+        "bwd_down_dgrad_swiglu": R * 2 * I * 4 + R * I * 4 + (R * 2 * I * q8 if mx else 0),
+        "bwd_gate_up_dgrad": R * d * 4,
+    }
+    out = {n: (v[0] if isinstance(v, tuple) else v, w[n]) for n, v in f.items()}
+    mb = micro_batches
+    out["bwd_down_wgrad"] = (mb * (R * d * 2 + R * I * 4) + wd * wgrad_elem_bytes,
+                             wd * wgrad_elem_bytes)
+    out["bwd_gate_up_wgrad"] = (mb * (R * 2 * I * 4 + R * d * 2) + wgu * wgrad_elem_bytes,
+                                wgu * wgrad_elem_bytes)
+    return out
+
+
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # grouped GEMMs on the fine workload, from the ncu capture summarised in
 # profiles/grouped_gemms_fine.txt (kernels as of the commit named there).
 NCU_TRAFFIC_FINE = {
-    "fwd_gate_up_swiglu": 689.573376e6 + 331.275e6,
-    "fwd_down": 343.459072e6 + 254.775e6,
-    "bwd_down_dgrad_swiglu": 770.239744e6 + 401.826e6,
-    "bwd_down_wgrad": 300.351488e6 + 476.125e6,
-    "bwd_gate_up_dgrad": 689.331968e6 + 271.781e6,
-    "bwd_gate_up_wgrad": 449.907200e6 + 1012.112e6,
+    "fwd_gate_up_swiglu": 688.293376e6 + 331.700e6,
+    "fwd_down": 343.460352e6 + 254.705e6,
+    "bwd_down_dgrad_swiglu": 769.596416e6 + 401.101e6,
+    "bwd_down_wgrad": 300.184064e6 + 475.803e6,
+    "bwd_gate_up_dgrad": 689.076992e6 + 272.009e6,
+    "bwd_gate_up_wgrad": 449.944064e6 + 1011.943e6,
 }
 
 
@@ -309,12 +347,15 @@ def workload_config(shape: gen.Shape) -> dict:
     return cfg
 
 
-def layer_options(api) -> dict:
-    """MoELayer keyword arguments of the selected workload."""
+def layer_options(api, bf16_wgrad: bool = False) -> dict:
+    """MoELayer keyword arguments of the selected workload (bf16_wgrad: weight
+    gradients returned in bf16, rounded once from the fp32 accumulation)."""
     w = gen.WORKLOADS[WORKLOAD]
     if WORKLOAD == "mxfp8":
+        if bf16_wgrad:
+            raise SystemExit("--bf16-wgrad: the micro-batched workload accumulates dW in fp32")
         return dict(dtype=api.MXFP8, mb_tokens=w["mb_tokens"], ring_slots=w["ring_slots"])
-    return {}
+    return dict(flags=api.FLAG_BF16_WGRAD_OUT) if bf16_wgrad else {}
 
 
 # ------------------------------------------------------------- multi-rank --
@@ -407,6 +448,8 @@ def main():
     ap.add_argument("--impl", default="mok", choices=["mok", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bf16-wgrad", action="store_true",
+                    help="return the weight gradients in bf16 (default fp32)")
     ap.add_argument("--workload", default="fine", choices=sorted(gen.WORKLOADS),
                     help="fine (default, the measured configuration) or another configuration")
     args = ap.parse_args()
@@ -439,13 +482,15 @@ def main():
 
     x, wr, wgu, wd, dy = (dev(inp[n]) for n in ("x", "w_router", "w_gate_up", "w_down", "dy"))
     bias = torch.from_numpy(inp["bias"]).cuda() if inp.get("bias") is not None else None
-    layer = api.MoELayer(shape.T, shape.d, shape.E, shape.I, shape.k, **layer_options(api))
+    layer = api.MoELayer(shape.T, shape.d, shape.E, shape.I, shape.k,
+                         **layer_options(api, args.bf16_wgrad))
     f32 = dict(dtype=torch.float32, device="cuda")
     y = torch.empty(x.shape, **f32)
     dx = torch.empty(x.shape, **f32)
-    dwr = torch.empty(wr.shape, **f32)
-    dwgu = torch.empty(wgu.shape, **f32)
-    dwd = torch.empty(wd.shape, **f32)
+    wg = dict(dtype=layer.wgrad_dtype, device="cuda")
+    dwr = torch.empty(wr.shape, **wg)
+    dwgu = torch.empty(wgu.shape, **wg)
+    dwd = torch.empty(wd.shape, **wg)
     stream = torch.cuda.current_stream()
 
     def step():
@@ -495,7 +540,20 @@ def main():
 
     # ---- per-kernel summary and the dominant kernel's roofline
     peaks = load_peaks()
+    write_gbs = measure_write_gbs(torch)
     flops = gemm_flops(shape, int(layer.layout.mb_count))
+    gbytes = gemm_bytes(shape, int(layer.layout.mb_count), mx=WORKLOAD == "mxfp8",
+                        wgrad_elem_bytes=2 if args.bf16_wgrad else 4)
+
+    def gemm_roofline_us(n):
+        """(bound, shortest time in us) of GEMM n: tensor time at the measured
+        (FP8: x2) peak against HBM time at the copy and write bandwidths."""
+        fp8 = WORKLOAD == "mxfp8" and n in MX_GEMMS
+        t_tc = flops[n] / (peaks["bf16_sustained"] * (2.0 if fp8 else 1.0) * 1e12) * 1e6
+        if n not in gbytes:
+            return "tensor", t_tc
+        t_mem = mover_roofline_us(gbytes[n][0], gbytes[n][1], peaks["hbm"], write_gbs)
+        return ("hbm", t_mem) if t_mem > t_tc else ("tensor", t_tc)
     movers = mover_bytes(shape, int(layer.layout.mb_count))
     if WORKLOAD == "mxfp8":
         movers.update(mx_quant_bytes(shape, int(layer.layout.mb_count), int(layer.layout.rows_max),
@@ -504,11 +562,31 @@ def main():
     ksum = {}
     for name, (n, ms) in kernels.items():
         ksum[name] = {"launches": n, "avg_us": 1e3 * ms / n, "share": ms / total_k}
+        if name in flops:
+            b, t_us = gemm_roofline_us(name)
+            ksum[name].update({"bound": b, "roofline_us": t_us,
+                               "frac_roofline": t_us / ksum[name]["avg_us"]})
     # the dominant kernel among those whose work per launch is known
     dom = max((n for n in kernels if n in flops or n in movers), key=lambda n: kernels[n][1])
     n_dom, ms_dom = kernels[dom]
     avg_s = ms_dom / n_dom / 1e3
-    if dom in flops:
+    if dom in flops and gemm_roofline_us(dom)[0] == "hbm":
+        # bound by HBM: its fp32 outputs (dW, g/u, rows) outweigh its tensor time
+        tb, tw = gbytes[dom]
+        ach = tb / avg_s / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peaks["hbm"],
+                "unit": "GB/s", "frac": ach / peaks["hbm"],
+                "frac_roofline": gemm_roofline_us(dom)[1] / (avg_s * 1e6),
+                "written_per_launch": tw, "write_bw_gbs": write_gbs,
+                "traffic": NCU_TRAFFIC_FINE.get(dom) if WORKLOAD == "fine" else None,
+                "traffic_source": "profiles/grouped_gemms_fine.txt",
+                "peak_source": f"hbm_gbs of {peaks['source']}; write bandwidth measured here "
+                               "(1 GiB zero fill)",
+                "algorithmic_per_launch": tb,
+                "tensor": {"achieved_tflops": flops[dom] / avg_s / 1e12,
+                           "peak_tflops": peaks["bf16_sustained"],
+                           "frac": flops[dom] / avg_s / 1e12 / peaks["bf16_sustained"]}}
+    elif dom in flops:
         ach = flops[dom] / avg_s / 1e12
         # the MXFP8 workload's block-scaled GEMMs run on the FP8 tensor rate: their
         # peak is the measured bf16 one times the nominal fp8/bf16 ratio (2)
@@ -534,7 +612,6 @@ def main():
     gg_fl = sum(flops[n] * kernels[n][0] for n in gg)
     gg_tflops = gg_fl / (gg_ms / 1e3) / 1e12 if gg_ms else 0.0
     movers_perf = {}
-    write_gbs = measure_write_gbs(torch)
     wbytes = mover_write_bytes(shape, int(layer.layout.mb_count))
     for n, b in movers.items():
         if n in kernels:
@@ -576,7 +653,9 @@ def main():
                 "E4M3 + E8M0 per 32: block-scaled FP8 MMAs for the forward GEMMs and the "
                 "gate/up dgrad; bf16 MMAs on MX-valued operands for the down dgrad; "
                 "weight gradients on bf16 hi/lo operands"),
-            "data": "synthetic", "config": workload_config(shape),
+            "data": "synthetic",
+            "config": dict(workload_config(shape),
+                           weight_grad_out="bf16" if args.bf16_wgrad else "fp32"),
             "grouped_gemm_tflops": gg_tflops,
             "grouped_gemm_frac_of_peak": gg_tflops / peaks["bf16_sustained"],
             "all_gemm_tflops": gemm_fl / (gemm_ms / 1e3) / 1e12 if gemm_ms else 0.0,

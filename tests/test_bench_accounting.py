@@ -95,3 +95,25 @@ def test_mover_roofline_takes_the_tighter_bound():
     w, m = bench.mover_write_bytes(s), bench.mover_bytes(s)
     for n in w:
         assert 0 < w[n] < m[n]
+
+
+def test_gemm_bytes_fine_weight_gradients_are_write_bound():
+    """On the fine workload the gate/up weight gradient writes 1.07 GB of fp32
+    dW: at ~4 TB/s of writes that takes longer than its 275 GFLOP on the
+    tensor cores, so its roofline is the HBM one."""
+    s = gen.workload_shape("fine")
+    b = bench.gemm_bytes(s)
+    tot, wr = b["bwd_gate_up_wgrad"]
+    assert wr == s.E * 2 * s.I * s.d * 4
+    assert tot == 32768 * 2 * s.I * 4 + 32768 * s.d * 2 + wr
+    t_mem = bench.mover_roofline_us(tot, wr, 6688.8, 3990.0)
+    t_tc = bench.gemm_flops(s)["bwd_gate_up_wgrad"] / 1748.6e12 * 1e6
+    assert t_mem > t_tc
+    # bf16 dW halves the write; the deferred form reads every micro-batch
+    assert bench.gemm_bytes(s, wgrad_elem_bytes=2)["bwd_gate_up_wgrad"][1] == wr // 2
+    m = gen.workload_shape("mxfp8")
+    one, eight = bench.gemm_bytes(m, 1), bench.gemm_bytes(m, 8)
+    assert eight["bwd_gate_up_wgrad"][1] == one["bwd_gate_up_wgrad"][1]
+    assert eight["bwd_gate_up_wgrad"][0] == pytest.approx(one["bwd_gate_up_wgrad"][0])
+    for n, (t, w) in b.items():
+        assert 0 < w < t, n
