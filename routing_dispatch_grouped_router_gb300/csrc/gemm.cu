@@ -50,6 +50,8 @@ enum Epi : int {
   EPI_SWIGLU_FWD = 2,
   EPI_SWIGLU_BWD = 3,
   EPI_F32_T = 4,  // KGROUP: fp32 C^T through TMA (the tile is stored transposed)
+  EPI_BF16_TMA = 5,  // KGROUP: C rounded to bf16, through TMA
+  EPI_BF16_T = 6,    // KGROUP: C^T rounded to bf16, through TMA
 };
 // Split operands: a bf16 "hi" tile plus a bf16 "lo" tile (value - hi) whose
 // products are accumulated into the same fp32 accumulator, giving the GEMM
@@ -498,6 +500,45 @@ __device__ __forceinline__ void stage_and_store_f32_t(uint8_t* buf, const CUtens
   if (lane == 0) tma_out_2d(tmC, buf, x, y, add, evict_first);
 }
 
+// As stage_and_store_f32, but a 32 x 64 block (columns x .. x+63: v0 then
+// v1) is rounded to bf16 (nearest even) and stored as 128-byte rows, in the
+// same 128B-swizzled layout (16-byte chunk j of row r at chunk j ^ (r % 8)).
+__device__ __forceinline__ void stage_and_store_bf16(uint8_t* buf, const CUtensorMap* tmC,
+                                                     const float (&v0)[32], const float (&v1)[32],
+                                                     int lane, int x, int y, bool evict_first) {
+  if (lane == 0) bulk_wait_read<0>();
+  __syncwarp();
+  uint8_t* row = buf + lane * 128;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float* v = j < 4 ? v0 + 8 * j : v1 + 8 * (j - 4);
+    *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) =
+        make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                   pack_bf16x2(v[6], v[7]));
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) tma_out_2d(tmC, buf, x, y, false, evict_first);
+}
+
+// The transposed form (see stage_and_store_f32_t) in bf16: staging row j is
+// column j of the block, lane i's element at 16-byte chunk (i / 8) ^ ((j >> 1)
+// & 3), byte 2 * (i % 8).
+__device__ __forceinline__ void stage_and_store_bf16_t(uint8_t* buf, const CUtensorMap* tmC,
+                                                       const float (&v)[32], int lane, int x,
+                                                       int y, bool evict_first) {
+  if (lane == 0) bulk_wait_read<0>();
+  __syncwarp();
+  const int chunk = lane >> 3, off = (lane & 7) * 2;
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    *reinterpret_cast<__nv_bfloat16*>(buf + j * 64 + ((chunk ^ ((j >> 1) & 3)) << 4) + off) =
+        __float2bfloat16_rn(v[j]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) tma_out_2d(tmC, buf, x, y, false, evict_first);
+}
+
 template <int BN, int SCHED, int EPI, bool DBUF, int SPLIT>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl, uint32_t taddr,
                                               int q, int lane, int half, uint8_t* stage_buf,
@@ -505,23 +546,39 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
   constexpr int HALF_COLS = BN / 2;
   const int row_in_tile = q * 32 + lane;
   const bool zero_k = (tl.num_kb == 0);
-  if (EPI == EPI_F32 && SCHED != SCHED_DENSE) {
-    // fp32 C through TMA stores; C viewed as 2-D [rows, N]
+  if ((EPI == EPI_F32 || EPI == EPI_BF16_TMA) && SCHED != SCHED_DENSE) {
+    // fp32 (or bf16) C through TMA stores; C viewed as 2-D [rows, N]
     const int y = (SCHED == SCHED_KGROUP ? tl.e * a.m_rows : 0) + tl.row0 + q * 32;
     const int col0 = tl.n_tile * BN + half * HALF_COLS;
+    if constexpr (EPI == EPI_BF16_TMA) {
+      // 64 columns per store: 128-byte rows
 #pragma unroll 1
-    for (int c = 0; c < HALF_COLS; c += 32) {
-      float v[32];
-      if (!zero_k) {
-        tmem_ld32(taddr + half * HALF_COLS + c, v);
-      } else {
+      for (int c = 0; c < HALF_COLS; c += 64) {
+        float v0[32], v1[32];
+        if (!zero_k) {
+          tmem_ld32(taddr + half * HALF_COLS + c, v0);
+          tmem_ld32(taddr + half * HALF_COLS + c + 32, v1);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = 0.f;
+          for (int j = 0; j < 32; ++j) v0[j] = v1[j] = 0.f;
+        }
+        stage_and_store_bf16(stage_buf, tmC, v0, v1, lane, col0 + c, y, a.evict_first != 0);
       }
-      stage_and_store_f32<DBUF>(stage_buf, nst, tmC, v, lane, col0 + c, y, a.accumulate != 0,
-                                a.evict_first != 0);
+    } else {
+#pragma unroll 1
+      for (int c = 0; c < HALF_COLS; c += 32) {
+        float v[32];
+        if (!zero_k) {
+          tmem_ld32(taddr + half * HALF_COLS + c, v);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0.f;
+        }
+        stage_and_store_f32<DBUF>(stage_buf, nst, tmC, v, lane, col0 + c, y, a.accumulate != 0,
+                                  a.evict_first != 0);
+      }
     }
-  } else if (EPI == EPI_F32_T) {
+  } else if (EPI == EPI_F32_T || EPI == EPI_BF16_T) {
     // C^T through TMA: accumulator rows are output columns; C viewed as
     // [E * N, M] with group e's block at rows e*N
     const int x = tl.row0 + q * 32;
@@ -535,8 +592,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = 0.f;
       }
-      stage_and_store_f32_t(stage_buf, tmC, v, lane, x, tl.e * a.ldo + col0 + c,
-                            a.accumulate != 0, a.evict_first != 0);
+      if (EPI == EPI_BF16_T)
+        stage_and_store_bf16_t(stage_buf, tmC, v, lane, x, tl.e * a.ldo + col0 + c,
+                               a.evict_first != 0);
+      else
+        stage_and_store_f32_t(stage_buf, tmC, v, lane, x, tl.e * a.ldo + col0 + c,
+                              a.accumulate != 0, a.evict_first != 0);
     }
   } else if (EPI == EPI_BF16 || EPI == EPI_F32) {
     constexpr int esz = EPI == EPI_F32 ? 4 : 2;
@@ -815,7 +876,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // SwiGLU backward: two g/u staging buffers per epilogue warp, one barrier each
   uint64_t* gu_bar = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF + 256);
   constexpr bool kTmaStore = (EPI == EPI_F32 && SCHED != SCHED_DENSE) || EPI == EPI_SWIGLU_FWD ||
-                             EPI == EPI_F32_T || EPI == EPI_SWIGLU_BWD;
+                             EPI == EPI_F32_T || EPI == EPI_SWIGLU_BWD || EPI == EPI_BF16_TMA ||
+                             EPI == EPI_BF16_T;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -1240,6 +1302,15 @@ static bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t 
 static bool make_out_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
   return make_map_t(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, cols, rows, cols, 32, 32);
 }
+// bf16 C: 32-row x 64-column blocks (128-byte rows, 128-byte swizzle)
+static bool make_out_map_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+  return make_map_t(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, cols, rows, cols, 64, 32);
+}
+// bf16 C^T: 32 x 32 blocks (64-byte rows, 64-byte swizzle)
+static bool make_out_map_bf16_t(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+  return make_map_t(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, cols, rows, cols, 32, 32,
+                    CU_TENSOR_MAP_SWIZZLE_64B);
+}
 
 // max_units: an upper bound on the tiles (PAIR: tile pairs) of the launch;
 // the kernel reads the exact count on the device.
@@ -1602,15 +1673,20 @@ static cudaError_t wgrad(const Dims& D, const char* name, const void* A_rows, in
   a.evict_first = 1;  // weight gradients: the layer's output
   const int mt = a.E * a.m_tiles * a.n_tiles;
   if (D.wgrad_bf16) {
+    // bf16 dW: the fp32 accumulation rounded once, stored through TMA
     if (accumulate) return cudaErrorInvalidValue;  // accumulation is fp32 only
+    if (!make_out_map_bf16(&tc, out, N, D.E * M)) return cudaErrorInvalidValue;
     if (!lo_is_a)
-      return launch<128, true, true, SCHED_KGROUP, EPI_BF16, SPLIT_B>(name, ta, tb, ta, a, mt, st,
-                                                                      &tl);
+      return launch<128, true, true, SCHED_KGROUP, EPI_BF16_TMA, SPLIT_B>(name, ta, tb, tc, a, mt,
+                                                                          st, &tl);
+    if (bn == 256 && D.pair && a.m_tiles % 2 == 0)
+      return launch<256, true, true, SCHED_KGROUP, EPI_BF16_TMA, SPLIT_A, true>(
+          name, ta, tb, tc, a, mt / 2, st, &tl);
     if (bn == 256)
-      return launch<256, true, true, SCHED_KGROUP, EPI_BF16, SPLIT_A>(name, ta, tb, ta, a, mt, st,
-                                                                      &tl);
-    return launch<128, true, true, SCHED_KGROUP, EPI_BF16, SPLIT_A>(name, ta, tb, ta, a, mt, st,
-                                                                    &tl);
+      return launch<256, true, true, SCHED_KGROUP, EPI_BF16_TMA, SPLIT_A>(name, ta, tb, tc, a, mt,
+                                                                          st, &tl);
+    return launch<128, true, true, SCHED_KGROUP, EPI_BF16_TMA, SPLIT_A>(name, ta, tb, tc, a, mt,
+                                                                        st, &tl);
   }
   if (!make_out_map(&tc, out, N, D.E * M)) return cudaErrorInvalidValue;
   if (!lo_is_a)
@@ -1629,7 +1705,7 @@ cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* P_hi
                             const void* P_lo, const int32_t* poff, void* dw_down,
                             bool accumulate, int* status, cudaStream_t st, const WgradSegs& sg) {
   // dW_down_e [d, I] (+)= dY_e^T [d x rows] * (P_hi + P_lo)_e [rows x I],  P = p h
-  if (D.wgrad_bf16 || D.d % 256 != 0)
+  if (D.d % 256 != 0)
     return wgrad(D, "bwd_down_wgrad", dY_perm, D.d, P_hi, D.I, P_lo, false, poff, dw_down,
                  accumulate, status, st, sg);
   // computed as its transpose, (P_hi + P_lo)_e^T [I x rows] * dY_e [rows x d],
@@ -1640,7 +1716,10 @@ cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* P_hi
   if (!make_map(&ta, P_hi, D.I, rows, D.I, 64)) return cudaErrorInvalidValue;
   if (!make_map(&tl, P_lo, D.I, rows, D.I, 64)) return cudaErrorInvalidValue;
   if (!make_map(&tb, dY_perm, D.d, rows, D.d, 64)) return cudaErrorInvalidValue;
-  if (!make_out_map(&tc, dw_down, D.I, D.E * D.d)) return cudaErrorInvalidValue;
+  if (D.wgrad_bf16 && accumulate) return cudaErrorInvalidValue;  // accumulation is fp32 only
+  if (!(D.wgrad_bf16 ? make_out_map_bf16_t(&tc, dw_down, D.I, D.E * D.d)
+                     : make_out_map(&tc, dw_down, D.I, D.E * D.d)))
+    return cudaErrorInvalidValue;
   GemmArgs a = blank_args(status);
   a.nseg = sg.nseg;
   a.poff_stride = sg.poff_stride;
@@ -1655,6 +1734,13 @@ cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* P_hi
   a.accumulate = accumulate ? 1 : 0;
   a.evict_first = 1;  // weight gradients: the layer's output
   const int mt = a.E * a.m_tiles * a.n_tiles;
+  if (D.wgrad_bf16) {
+    if (D.pair && a.m_tiles % 2 == 0)
+      return launch<256, true, true, SCHED_KGROUP, EPI_BF16_T, SPLIT_A, true>(
+          "bwd_down_wgrad", ta, tb, tc, a, mt / 2, st, &tl);
+    return launch<256, true, true, SCHED_KGROUP, EPI_BF16_T, SPLIT_A>("bwd_down_wgrad", ta, tb,
+                                                                      tc, a, mt, st, &tl);
+  }
   if (D.pair && a.m_tiles % 2 == 0)
     return launch<256, true, true, SCHED_KGROUP, EPI_F32_T, SPLIT_A, true>(
         "bwd_down_wgrad", ta, tb, tc, a, mt / 2, st, &tl);

@@ -123,13 +123,19 @@ def test_bitwise_deterministic(name):
                 assert np.array_equal(a, b)
 
 
-def test_bf16_output_flags_round_the_fp32_outputs():
+@pytest.mark.parametrize("name,single", [("wide", False), ("wide", True), ("d384", False),
+                                         ("ragged", False)])
+def test_bf16_output_flags_round_the_fp32_outputs(name, single):
     """With the bf16-output flags every output is the round-to-nearest-even
-    of the default fp32 output, bit for bit."""
-    shape = SMALL["wide"]
+    of the default fp32 output, bit for bit.  The weight gradients' bf16 TMA
+    stores: row-major and transposed (d % 256 == 0), row-major only (d384,
+    ragged), on CTA pairs and on single CTAs."""
+    shape = SMALL[name]
     inp = gen.make_inputs(shape, seed=1)
-    a = _gpu.run_gpu(shape, inp)
-    b = _gpu.run_gpu(shape, inp, flags=api.FLAG_BF16_ACT_OUT | api.FLAG_BF16_WGRAD_OUT)
+    extra = api.FLAG_SINGLE_CTA_GEMM if single else 0
+    a = _gpu.run_gpu(shape, inp, flags=extra)
+    b = _gpu.run_gpu(shape, inp,
+                     flags=api.FLAG_BF16_ACT_OUT | api.FLAG_BF16_WGRAD_OUT | extra)
     assert b["status"] == 0
     for n in ("y", "dx", "dw_router", "dw_gate_up", "dw_down"):
         assert a[n].dtype == torch.float32 and b[n].dtype == torch.bfloat16
