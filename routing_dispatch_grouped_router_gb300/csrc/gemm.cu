@@ -1670,7 +1670,9 @@ static cudaError_t wgrad(const Dims& D, const char* name, const void* A_rows, in
   a.ldo = N;
   a.out_group_stride = M * N;
   a.accumulate = accumulate ? 1 : 0;
-  a.evict_first = 1;  // weight gradients: the layer's output
+  // dW with the default L2 policy: evict-first measured 393 vs 383 us for the
+  // fine workload's gate/up weight gradient
+  a.evict_first = 0;
   const int mt = a.E * a.m_tiles * a.n_tiles;
   if (D.wgrad_bf16) {
     // bf16 dW: the fp32 accumulation rounded once, stored through TMA
@@ -1732,7 +1734,9 @@ cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* P_hi
   a.out = dw_down;
   a.ldo = D.d;  // rows of one expert's block in the [E*d, I] view
   a.accumulate = accumulate ? 1 : 0;
-  a.evict_first = 1;  // weight gradients: the layer's output
+  // dW with the default L2 policy: evict-first measured 393 vs 383 us for the
+  // fine workload's gate/up weight gradient
+  a.evict_first = 0;
   const int mt = a.E * a.m_tiles * a.n_tiles;
   if (D.wgrad_bf16) {
     if (D.pair && a.m_tiles % 2 == 0)
