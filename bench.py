@@ -154,9 +154,8 @@ def mover_bytes(shape: gen.Shape, micro_batches: int = 1) -> dict:
                      shape.I)
     np_ = 2 * I // (256 if I % 256 == 0 else 128)
     return {
-        # read each token row once (its other k-1 copies come from L2), write R
-        # bf16 rows, read the row indices
-        "gather_rows": T * d * 2 + R * d * 2 + R * 4,
+        # read each token row once, write its k bf16 rows, read the positions
+        "dispatch_rows": T * d * 2 + R * d * 2 + R * 4,
         # read k fp32 expert rows + weights per token, write the fp32 token row
         "combine": R * 4 * d + T * 4 * d + R * 8,
         # read k fp32 dX rows and the dp partials, write fp32 dx (router rows from L2)
@@ -169,7 +168,7 @@ def mover_bytes(shape: gen.Shape, micro_batches: int = 1) -> dict:
 def mover_write_bytes(shape: gen.Shape, micro_batches: int = 1) -> dict:
     """Bytes each data-movement launch writes (part of mover_bytes)."""
     R, d, T, E = shape.R // micro_batches, shape.d, shape.T // micro_batches, shape.E
-    return {"gather_rows": R * d * 2, "combine": T * d * 4, "reverse_dispatch": T * d * 4,
+    return {"dispatch_rows": R * d * 2, "combine": T * d * 4, "reverse_dispatch": T * d * 4,
             "router_wgrad": E * d * 4}
 
 
@@ -620,7 +619,7 @@ def main():
             movers_perf[n] = {"GB/s": gbs, "frac_hbm": gbs / peaks["hbm"]}
             if n in wbytes:
                 # against the copy bandwidth and the measured write bandwidth
-                # together: write-heavy movers (the gather) are bound by the latter
+                # together: write-heavy movers (the dispatch) are bound by the latter
                 roof_us = mover_roofline_us(b, wbytes[n], peaks["hbm"], write_gbs)
                 movers_perf[n]["frac_roofline"] = roof_us / avg_us
     movers_perf["write_bw_gbs"] = write_gbs

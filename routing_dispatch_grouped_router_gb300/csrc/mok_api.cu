@@ -402,7 +402,7 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
                          at<int32_t>(workspace, F.block_base), o, status, st));
     void* x_perm = at<char>(saved, L.x_perm + (i % D.ring) * L.ring_slot_bytes);
     void* gu = D.recompute_gu ? nullptr : at<char>(saved, L.gate_up + blk);
-    MOK_CUDA(launch_gather_rows(D, xi, o.ptok, o.padded_offsets, x_perm, status, st));
+    MOK_CUDA(launch_dispatch_rows(D, xi, o.ppos, o.ptok, o.padded_offsets, x_perm, status, st));
     if (D.mx) {
       // expert GEMMs on the block-scaled tensor cores: x rows to MXFP8, the
       // gate/up GEMM writes h as MXFP8 for the down projection
@@ -517,10 +517,10 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
     if (defer && !D.mx) {
       // this micro-batch's rows go to its own slot (the deferred wgrad reads them)
       x_perm = at<char>(workspace, B.x_def) + static_cast<size_t>(i) * rows * D.d * 2;
-      MOK_CUDA(launch_gather_rows(D, xi, ptok, poff, x_perm, status, st));
+      MOK_CUDA(launch_dispatch_rows(D, xi, ppos, ptok, poff, x_perm, status, st));
     } else if (i < D.nmb - D.ring) {
       // the slot now holds a later micro-batch: dispatch this one again
-      MOK_CUDA(launch_gather_rows(D, xi, ptok, poff, x_perm, status, st));
+      MOK_CUDA(launch_dispatch_rows(D, xi, ppos, ptok, poff, x_perm, status, st));
     }
     if (D.recompute_gu) {
       // the forward's gate/up GEMM again, g and u only (no h)
@@ -534,7 +534,7 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
       }
     }
     // reverse-combine: pull dy rows into expert order
-    MOK_CUDA(launch_gather_rows(D, dyi, ptok, poff, dy_perm_i, status, st));
+    MOK_CUDA(launch_dispatch_rows(D, dyi, ppos, ptok, poff, dy_perm_i, status, st));
     const void* dy_row_op = dy_perm_i;
     const void* dy_col_op = dy_perm_i;
     const void* x_col_op = x_perm;

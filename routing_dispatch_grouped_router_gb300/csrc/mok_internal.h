@@ -105,10 +105,12 @@ cudaError_t launch_plan(const Dims& D, const int32_t* topk_idx, const float* top
                         int32_t* block_counts, int32_t* block_base, const PlanOut& o, int* status,
                         cudaStream_t st);
 
-// dst[r] = src[ptok[r]] (or zeros where ptok[r] < 0), rows [0, padded_offsets[E]).
-cudaError_t launch_gather_rows(const Dims& D, const void* src, const int32_t* ptok,
-                               const int32_t* padded_offsets, void* dst, int* status,
-                               cudaStream_t st);
+// Rows [0, padded_offsets[E]) of dst: dst[ppos[t, s]] = src[t] for every
+// token t and slot s, zeros where ptok[r] < 0 (padding).  Each src row is
+// read once.
+cudaError_t launch_dispatch_rows(const Dims& D, const void* src, const int32_t* ppos,
+                                 const int32_t* ptok, const int32_t* padded_offsets, void* dst,
+                                 int* status, cudaStream_t st);
 
 // y_t = sum_s p[t,s] O[ppos[t,s]] (O fp32; y fp32 or bf16).
 cudaError_t launch_combine(const Dims& D, const float* O, const int32_t* ppos, const float* topk_w,

@@ -334,101 +334,121 @@ cudaError_t launch_plan(const Dims& D, const int32_t* topk_idx, const float* top
 
 // ------------------------------------------------------------- row gather --
 
-// Destination-driven ("pull") gather staged through TMA: padded row r <
-// padded_offsets[E] receives src[ptok[r]], or zeros for a padding row.  CTA b
-// (one warp) moves rows b, b + G, b + 2G, ... (G CTAs), so at any moment the
-// grid writes one compact window of consecutive rows.  Rows pass through a
-// ring of `nslot` row-sized shared-memory slots: a bulk copy global -> shared
-// completing on the slot's mbarrier, then a bulk store shared -> global.  A
-// slot is refilled kGatherLag rows after its store was issued, so up to
-// kGatherLag + 1 stores and nslot - kGatherLag - 1 loads are in flight.  The
-// row indices come through a 128-entry shared ring that the warp refills 32
-// at a time, each refill's loads issued 16 rows before they are written, so
-// the issuing lane never waits on an index load.  A padding row's slot is
-// zeroed by the warp and stored like any other, so every row commits exactly
-// one bulk group and the lag counts rows.  Token rows are read with an L2
-// evict-last policy (each is read k times) and the output rows are stored
-// evict-first (a stream larger than L2 that should not displace them).
-constexpr int kGatherLag = 2;
-constexpr int kGatherMaxSlots = 32;
-constexpr int kGatherIdx = 128;
+// Dispatch of token rows into the padded expert-major row space, staged
+// through TMA and driven by the token: padded row r < padded_offsets[E]
+// receives src[t] where r is one of t's k padded positions (ppos[t, s]), and
+// zeros if r is a padding row.  Each token row is read from HBM once (one bulk
+// copy global -> shared completing on its slot's mbarrier) and stored to its
+// k rows from the same slot (k bulk stores, one bulk group).  CTA b (one
+// warp) takes tokens b, b + G, b + 2G, ... (G CTAs) through a ring of `nslot`
+// row-sized slots; a slot is refilled kDispatchLag tokens after its stores
+// were issued.  The k positions of each token come through a 128-token shared
+// ring that the warp refills 32 tokens at a time (each lane loads one token's
+// positions), each refill's loads issued 16 tokens before they are written,
+// so the issuing lane never waits on an index load.  Afterwards the CTA
+// stores a zeroed slot to the padding rows among rows b, b + G, ...
+constexpr int kDispatchLag = 2;
+constexpr int kDispatchMaxSlots = 32;
+constexpr int kDispatchIdx = 128;
 
-__global__ void __launch_bounds__(32) gather_rows_kernel(const uint8_t* __restrict__ src,
-                                                         const int32_t* __restrict__ ptok,
-                                                         const int32_t* __restrict__ poff_end,
-                                                         int T, uint32_t row_bytes, int nslot,
-                                                         uint8_t* __restrict__ dst, int* status) {
+__global__ void __launch_bounds__(32) dispatch_rows_kernel(
+    const uint8_t* __restrict__ src, const int32_t* __restrict__ ppos, int k,
+    const int32_t* __restrict__ ptok, const int32_t* __restrict__ poff_end, int T,
+    uint32_t row_bytes, int nslot, uint8_t* __restrict__ dst, int* status) {
   extern __shared__ __align__(128) uint8_t gsm[];
-  __shared__ __align__(8) uint64_t full[kGatherMaxSlots];
-  __shared__ int s_tok[kGatherIdx];
+  __shared__ __align__(8) uint64_t full[kDispatchMaxSlots];
+  __shared__ int s_pos[kDispatchIdx][kMaxTopK];
   const int lane = threadIdx.x;
-  const long long P = *poff_end;  // padded rows in use
   const long long G = gridDim.x;
   const long long first = blockIdx.x;
-  const long long n = (P > first) ? (P - first + G - 1) / G : 0;  // rows of this CTA
-  if (n <= 0) return;  // the whole warp
+  const long long n = (T > first) ? (T - first + G - 1) / G : 0;  // tokens of this CTA
+  const int never = 0;
   if (lane == 0) {
     for (int s = 0; s < nslot; ++s) mbar_init(&full[s], 1);
     fence_barrier_init();
   }
-  // indices of this CTA's rows 0..95; rows 96..127 come with the first refill
-  for (int i = lane; i < kGatherIdx - 32; i += 32) s_tok[i] = i < n ? ptok[first + i * G] : -1;
+  // positions of this CTA's tokens 0..95; tokens 96..127 come with the first refill
+  for (int i = lane; i < kDispatchIdx - 32; i += 32)
+#pragma unroll
+    for (int p = 0; p < kMaxTopK; ++p)
+      s_pos[i][p] = (i < n && p < k) ? ppos[(first + i * G) * k + p] : -1;
   __syncwarp();
   const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
-  auto issue = [&](long long j) {  // lane 0: this CTA's row j into its slot
+  auto issue = [&](long long j) {  // lane 0: token j's row into its slot
     const int s = static_cast<int>(j % nslot);
-    const int t = s_tok[j % kGatherIdx];
-    if (t >= 0 && t < T) {
-      mbar_arrive_expect_tx(&full[s], row_bytes);
-      bulk_load_hint(gsm + static_cast<size_t>(s) * row_bytes,
-                     src + static_cast<long long>(t) * row_bytes, row_bytes, &full[s], keep);
-    } else {
-      mbar_arrive(&full[s]);  // padding: the warp zeroes the slot at store time
-    }
+    mbar_arrive_expect_tx(&full[s], row_bytes);
+    bulk_load_hint(gsm + static_cast<size_t>(s) * row_bytes,
+                   src + (first + j * G) * static_cast<long long>(row_bytes), row_bytes, &full[s],
+                   keep);
   };
   if (lane == 0) {
     const long long pro = n < nslot ? n : nslot;
     for (long long j = 0; j < pro; ++j) issue(j);
   }
-  const int never = 0;
-  int pend = -1;  // the index refill in flight
+  int pend[kMaxTopK];  // the position refill in flight (lane's token)
+#pragma unroll
+  for (int p = 0; p < kMaxTopK; ++p) pend[p] = -1;
   for (long long j = 0; j < n; ++j) {
     __syncwarp();
     if ((j & 31) == 0) {
-      const long long jj = j + (kGatherIdx - 32) + lane;
-      pend = jj < n ? ptok[first + jj * G] : -1;
+      const long long jj = j + (kDispatchIdx - 32) + lane;
+#pragma unroll
+      for (int p = 0; p < kMaxTopK; ++p)
+        pend[p] = (jj < n && p < k) ? ppos[(first + jj * G) * k + p] : -1;
     } else if ((j & 31) == 16) {
-      s_tok[(j - 16 + (kGatherIdx - 32) + lane) % kGatherIdx] = pend;
-    }
-    const int s = static_cast<int>(j % nslot);
-    uint8_t* slot = gsm + static_cast<size_t>(s) * row_bytes;
-    const int t = s_tok[j % kGatherIdx];
-    if (!(t >= 0 && t < T)) {
-      for (uint32_t i = lane * 16; i < row_bytes; i += 32 * 16)
-        *reinterpret_cast<uint4*>(slot + i) = make_uint4(0, 0, 0, 0);
-      fence_proxy_async_smem();
+      const int e = static_cast<int>((j - 16 + (kDispatchIdx - 32) + lane) % kDispatchIdx);
+#pragma unroll
+      for (int p = 0; p < kMaxTopK; ++p) s_pos[e][p] = pend[p];
     }
     __syncwarp();
     if (lane == 0) {
+      const int s = static_cast<int>(j % nslot);
       const uint32_t par = static_cast<uint32_t>((j / nslot) & 1);
       if (!mbar_wait(&full[s], par, &never)) set_status(status, MOK_ERR_DEVICE_TIMEOUT);
-      bulk_store_hint(dst + (first + j * G) * row_bytes, slot, row_bytes, stream);
-      bulk_commit();
-      // the store of row j - lag has read its slot: refill it with row j - lag + nslot
-      const long long r = j - kGatherLag + nslot;
-      if (j >= kGatherLag && r < n) {
-        bulk_wait_read<kGatherLag>();
-        issue(r);
+      const uint8_t* slot = gsm + static_cast<size_t>(s) * row_bytes;
+      for (int p = 0; p < k; ++p) {
+        const int r = s_pos[j % kDispatchIdx][p];
+        if (r >= 0) bulk_store_hint(dst + static_cast<long long>(r) * row_bytes, slot, row_bytes,
+                                    stream);
       }
+      bulk_commit();
+      // token j - lag's stores have read their slot: refill it with token j - lag + nslot
+      const long long jr = j - kDispatchLag + nslot;
+      if (j >= kDispatchLag && jr < n) {
+        bulk_wait_read<kDispatchLag>();
+        issue(jr);
+      }
+    }
+  }
+  // padding rows: a zeroed slot stored to every row r = first + i G with no token
+  if (lane == 0) bulk_wait_read<0>();  // every slot has been read out
+  __syncwarp();
+  for (uint32_t i = lane * 16; i < row_bytes; i += 32 * 16)
+    *reinterpret_cast<uint4*>(gsm + i) = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  __syncwarp();
+  const long long P = *poff_end;
+  const long long m = (P > first) ? (P - first + G - 1) / G : 0;
+  for (long long i0 = 0; i0 < m; i0 += 32) {
+    const long long i = i0 + lane;
+    const int t = i < m ? ptok[first + i * G] : 0;
+    const unsigned pad = __ballot_sync(0xffffffffu, i < m && !(t >= 0 && t < T));
+    if (lane == 0 && pad) {
+      for (int l = 0; l < 32; ++l)
+        if (pad & (1u << l))
+          bulk_store_hint(dst + (first + (i0 + l) * G) * static_cast<long long>(row_bytes), gsm,
+                          row_bytes, stream);
+      bulk_commit();
     }
   }
   if (lane == 0) bulk_wait_all<0>();
 }
 
-cudaError_t launch_gather_rows(const Dims& D, const void* src, const int32_t* ptok,
-                               const int32_t* padded_offsets, void* dst, int* status,
-                               cudaStream_t st) {
+cudaError_t launch_dispatch_rows(const Dims& D, const void* src, const int32_t* ppos,
+                                 const int32_t* ptok, const int32_t* padded_offsets, void* dst,
+                                 int* status, cudaStream_t st) {
   if (D.T == 0) return cudaSuccess;
+  if (D.k > kMaxTopK) return cudaErrorInvalidValue;
   const uint32_t row_bytes = static_cast<uint32_t>(D.d * 2);
   // about 200 KB of slots per SM, split over up to four CTAs of at least six
   // slots each (d <= 16384: one CTA of six 32 KB slots at the largest)
@@ -436,23 +456,22 @@ cudaError_t launch_gather_rows(const Dims& D, const void* src, const int32_t* pt
   int per_sm = static_cast<int>(kSmemPerSm / (6 * row_bytes));
   per_sm = per_sm > 4 ? 4 : (per_sm < 1 ? 1 : per_sm);
   int nslot = static_cast<int>((kSmemPerSm / per_sm) / row_bytes);
-  nslot = nslot > kGatherMaxSlots ? kGatherMaxSlots : nslot;
-  if (nslot < kGatherLag + 2) return cudaErrorInvalidValue;
+  nslot = nslot > kDispatchMaxSlots ? kDispatchMaxSlots : nslot;
+  if (nslot < kDispatchLag + 2) return cudaErrorInvalidValue;
   const int smem = nslot * static_cast<int>(row_bytes);
   static int attr = 0;
   if (smem > attr) {
-    cudaError_t e = cudaFuncSetAttribute(gather_rows_kernel,
+    cudaError_t e = cudaFuncSetAttribute(dispatch_rows_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr = smem;
   }
   long long grid = static_cast<long long>(num_sms_current_device()) * per_sm;
-  const long long rows_cap = D.rows_max;
-  if (grid > rows_cap) grid = rows_cap;
-  ProfScope prof("gather_rows", st);
-  gather_rows_kernel<<<static_cast<unsigned>(grid), 32, smem, st>>>(
-      static_cast<const uint8_t*>(src), ptok, padded_offsets + D.E, static_cast<int>(D.T),
-      row_bytes, nslot, static_cast<uint8_t*>(dst), status);
+  if (grid > D.T) grid = D.T;
+  ProfScope prof("dispatch_rows", st);
+  dispatch_rows_kernel<<<static_cast<unsigned>(grid), 32, smem, st>>>(
+      static_cast<const uint8_t*>(src), ppos, static_cast<int>(D.k), ptok, padded_offsets + D.E,
+      static_cast<int>(D.T), row_bytes, nslot, static_cast<uint8_t*>(dst), status);
   count_launch();
   return cudaGetLastError();
 }

@@ -28,7 +28,7 @@ def test_micro_batches_divide_the_work_of_a_launch():
         else:
             assert part[n] * nmb == pytest.approx(whole[n])
     mw, mp = bench.mover_bytes(s), bench.mover_bytes(s, nmb)
-    for n in ("gather_rows", "combine"):
+    for n in ("dispatch_rows", "combine"):
         assert mp[n] * nmb == pytest.approx(mw[n], rel=1e-9)
 
 
@@ -38,7 +38,7 @@ def test_mover_bytes_follow_the_fp32_row_layout():
     R, T, d = s.T * s.k, s.T, s.d
     assert m["combine"] == R * d * 4 + T * d * 4 + R * 8
     # unique bytes: x read once, R rows written
-    assert m["gather_rows"] == T * d * 2 + R * d * 2 + R * 4
+    assert m["dispatch_rows"] == T * d * 2 + R * d * 2 + R * 4
 
 
 def test_workload_options():
