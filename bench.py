@@ -160,8 +160,9 @@ def mover_bytes(shape: gen.Shape, micro_batches: int = 1) -> dict:
         "combine": R * 4 * d + T * 4 * d + R * 8,
         # read k fp32 dX rows and the dp partials, write fp32 dx (router rows from L2)
         "reverse_dispatch": R * 4 * d + T * 4 * d + R * (12 + 4 * np_),
-        # read the dispatched bf16 rows once, write dW_r
-        "router_wgrad": R * 2 * d + E * d * 4,
+        # read each token row once (x, through the row -> token map), the map and
+        # dl per row, write dW_r
+        "router_wgrad": T * d * 2 + R * 8 + E * d * 4,
     }
 
 

@@ -570,7 +570,7 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
     // reverse-dispatch + router backward
     MOK_CUDA(launch_reverse_dispatch(D, dx_perm, ppos, topk_idx, topk_w, dp_part, w_router, dxi,
                                      dl_row, dl_tok, st));
-    MOK_CUDA(launch_router_wgrad(D, x_perm, dl_row, poff, counts, dw_router, !first, st));
+    MOK_CUDA(launch_router_wgrad(D, xi, ptok, dl_row, poff, counts, dw_router, !first, st));
   }
   if (defer) {
     // the expert weight gradients over all micro-batches: K runs through

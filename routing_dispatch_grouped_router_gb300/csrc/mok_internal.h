@@ -123,11 +123,12 @@ cudaError_t launch_reverse_dispatch(const Dims& D, const float* dX_perm, const i
                                     const float* dp_part, const void* w_router, void* dx,
                                     float* dl_row, float* dl_tok, cudaStream_t st);
 
-// dW_r[e] (+)= sum over rows of e of dl_row[r] * X_perm[r] (fp32 or bf16 out;
-// accumulation fp32 only).
-cudaError_t launch_router_wgrad(const Dims& D, const void* X_perm, const float* dl_row,
-                                const int32_t* padded_offsets, const int32_t* counts,
-                                void* dw_router, bool accumulate, cudaStream_t st);
+// dW_r[e] (+)= sum over rows r of e of dl_row[r] * x[ptok[r]] (fp32 or bf16
+// out; accumulation fp32 only).
+cudaError_t launch_router_wgrad(const Dims& D, const void* x, const int32_t* ptok,
+                                const float* dl_row, const int32_t* padded_offsets,
+                                const int32_t* counts, void* dw_router, bool accumulate,
+                                cudaStream_t st);
 
 // Grouped GEMMs on tcgen05 (see gemm.cu).
 cudaError_t gemm_fwd_gate_up(const Dims& D, const void* X_perm, const void* w_gate_up,

@@ -648,7 +648,9 @@ cudaError_t launch_reverse_dispatch(const Dims& D, const float* dX_perm, const i
 
 // ------------------------------------------------------ router weight grad --
 
-// dW_r[e, :] = sum over the real rows r of expert e of dl_row[r] * X_perm[r, :].
+// dW_r[e, :] = sum over the real rows r of expert e of dl_row[r] * x[ptok[r], :]
+// (x[ptok[r]] is dispatched row r; reading it from x, which the cache holds,
+// instead of the R dispatched rows gives the same values in the same order).
 // CTA (e, 64-column block): 32 row lanes x 8 column threads (8 columns each);
 // row lane i takes rows i, i+32, ...; the 32 partials are then added in lane
 // order.  Fixed order throughout.
@@ -662,7 +664,8 @@ __device__ __forceinline__ void axpy8(float (&acc)[8], float w, uint4 v) {
 }
 
 template <bool BF16_OUT>
-__global__ void router_wgrad_kernel(const uint4* __restrict__ Xp, const float* __restrict__ dl_row,
+__global__ void router_wgrad_kernel(const uint4* __restrict__ X, const int32_t* __restrict__ ptok,
+                                    const float* __restrict__ dl_row,
                                     const int32_t* __restrict__ poff,
                                     const int32_t* __restrict__ counts, int dv, void* dw,
                                     int accumulate) {
@@ -678,10 +681,13 @@ __global__ void router_wgrad_kernel(const uint4* __restrict__ Xp, const float* _
     for (; i + 3 * kRwRowLanes < n; i += 4 * kRwRowLanes) {
       uint4 v[4];
       float w[4];
+      int t[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) t[u] = ptok[r0 + i + u * kRwRowLanes];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const long long r = r0 + i + u * kRwRowLanes;
-        v[u] = ld_global_nc_v4(Xp + r * dv + cv);
+        v[u] = ld_global_nc_v4(X + static_cast<long long>(t[u]) * dv + cv);
         w[u] = dl_row[r];
       }
 #pragma unroll
@@ -689,7 +695,7 @@ __global__ void router_wgrad_kernel(const uint4* __restrict__ Xp, const float* _
     }
     for (; i < n; i += kRwRowLanes) {
       const long long r = r0 + i;
-      axpy8(acc, dl_row[r], ld_global_nc_v4(Xp + r * dv + cv));
+      axpy8(acc, dl_row[r], ld_global_nc_v4(X + static_cast<long long>(ptok[r]) * dv + cv));
     }
   }
 #pragma unroll
@@ -718,19 +724,20 @@ __global__ void router_wgrad_kernel(const uint4* __restrict__ Xp, const float* _
   }
 }
 
-cudaError_t launch_router_wgrad(const Dims& D, const void* X_perm, const float* dl_row,
-                                const int32_t* padded_offsets, const int32_t* counts,
-                                void* dw_router, bool accumulate, cudaStream_t st) {
+cudaError_t launch_router_wgrad(const Dims& D, const void* x, const int32_t* ptok,
+                                const float* dl_row, const int32_t* padded_offsets,
+                                const int32_t* counts, void* dw_router, bool accumulate,
+                                cudaStream_t st) {
   if (accumulate && D.wgrad_bf16) return cudaErrorInvalidValue;
   const int dv = static_cast<int>(D.d / 8);
   dim3 grid(static_cast<unsigned>(D.E), static_cast<unsigned>((dv + 7) / 8));
   ProfScope prof("router_wgrad", st);
   if (D.wgrad_bf16)
     router_wgrad_kernel<true><<<grid, kRwRowLanes * 8, 0, st>>>(
-        static_cast<const uint4*>(X_perm), dl_row, padded_offsets, counts, dv, dw_router, 0);
+        static_cast<const uint4*>(x), ptok, dl_row, padded_offsets, counts, dv, dw_router, 0);
   else
     router_wgrad_kernel<false><<<grid, kRwRowLanes * 8, 0, st>>>(
-        static_cast<const uint4*>(X_perm), dl_row, padded_offsets, counts, dv, dw_router,
+        static_cast<const uint4*>(x), ptok, dl_row, padded_offsets, counts, dv, dw_router,
         accumulate ? 1 : 0);
   count_launch();
   return cudaGetLastError();
