@@ -931,6 +931,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before_sync();
   if (PAIR) cluster_sync(); else __syncthreads();
   tc_fence_after_sync();
+  // Everything above touches only shared memory, TMEM and the kernel's
+  // parameters, so as a programmatic dependent it overlaps the previous
+  // kernel's tail; from here on that kernel's results are visible.
+  grid_dep_wait();
+  grid_dep_launch();
   const uint32_t tmem_base = *tmem_slot;
   volatile int* vabort = abort_flag;
   const int total = PAIR ? total_pairs<SCHED>(args) : total_tiles<SCHED>(args);
@@ -1328,31 +1333,42 @@ static cudaError_t launch(const char* name, const CUtensorMap& ta, const CUtenso
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (max_units <= 0) return cudaSuccess;
-  if (!PAIR) {
-    int grid = num_sms_current_device();
-    if (max_units < grid) grid = max_units;
-    ProfScope prof(name, st);
-    kern<<<grid, kThreads, smem, st>>>(ta, tb, tc, tl ? *tl : ta, args, om_v);
-    count_launch();
-    return cudaGetLastError();
-  }
-  // clusters of two CTAs, as many as can be resident at once (one per SM pair)
+  // every GEMM launches as a programmatic dependent of the kernel before it:
+  // its prologue (barriers, TMEM, descriptors) runs in that kernel's tail and
+  // it waits for that kernel's results before its first global access
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (!PAIR) {
+    int grid = num_sms_current_device();
+    if (max_units < grid) grid = max_units;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    ProfScope prof(name, st);
+    e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tl ? *tl : ta, args, om_v);
+    count_launch();
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
+  // clusters of two CTAs, as many as can be resident at once (one per SM pair)
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.numAttrs = 2;
   cfg.gridDim = dim3(static_cast<unsigned>(num_sms_current_device() / 2 * 2), 1, 1);
   static int max_clusters = -1;  // per kernel instantiation and process (one device type)
   if (max_clusters < 0) {
+    cudaLaunchConfig_t q = cfg;  // the cluster shape alone
+    q.attrs = &attr[1];
+    q.numAttrs = 1;
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &q);
     if (e != cudaSuccess) return e;
     max_clusters = n;
   }

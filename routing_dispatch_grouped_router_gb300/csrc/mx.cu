@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(256) mx_rows_kernel(const uint4* __restrict__ 
                                                       uint8_t* __restrict__ codes,
                                                       uint8_t* __restrict__ scales,
                                                       long long nchunks, long long tiled_nkg) {
+  grid_dep_launch();  // a GEMM after this kernel may start its prologue
   const int lane = threadIdx.x & 31;
   const long long G = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i0 = static_cast<long long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
@@ -134,6 +135,7 @@ __global__ void __launch_bounds__(256, ROWS_OUT ? 3 : 4) mx_cols_kernel(const ui
                                                          uint8_t* __restrict__ scales,
                                                          uint4* __restrict__ rows_out,
                                                          long long row_blocks, long long cols) {
+  grid_dep_launch();  // a GEMM after this kernel may start its prologue
   __shared__ __align__(16) float s_part[8][256];
   __shared__ __align__(16) int s_exp[256];
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
@@ -224,6 +226,7 @@ __global__ void __launch_bounds__(256) mx_cols_t_kernel(const uint32_t* __restri
                                                         uint8_t* __restrict__ scales,
                                                         uint32_t row_blocks, uint32_t cols,
                                                         uint32_t group_rows) {
+  grid_dep_launch();  // a GEMM after this kernel may start its prologue
   const int lane = threadIdx.x & 31;
   const uint32_t cp = cols / 2;          // bf16 pairs per row
   const uint32_t groups_c = cols / 64;   // 64-column groups per row

@@ -76,6 +76,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
 
 // --------------------------------------------------------------------- TMA --
 
+// Programmatic dependent launch.  grid_dep_wait: the grids this one depends
+// on have completed and their memory is visible (returns at once in a grid not
+// launched as a programmatic dependent).  grid_dep_launch: the next grid on the
+// stream, if launched as a programmatic dependent, may start once every CTA of
+// this grid has executed it (or exited).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }

@@ -355,6 +355,7 @@ __global__ void __launch_bounds__(32) dispatch_rows_kernel(
     const uint8_t* __restrict__ src, const int32_t* __restrict__ ppos, int k,
     const int32_t* __restrict__ ptok, const int32_t* __restrict__ poff_end, int T,
     uint32_t row_bytes, int nslot, uint8_t* __restrict__ dst, int* status) {
+  grid_dep_launch();  // a GEMM after this kernel may start its prologue
   extern __shared__ __align__(128) uint8_t gsm[];
   __shared__ __align__(8) uint64_t full[kDispatchMaxSlots];
   __shared__ int s_pos[kDispatchIdx][kMaxTopK];
@@ -521,6 +522,7 @@ __device__ __forceinline__ void store4(void* out, long long row, int dq, int c,
 template <bool BF16_OUT>
 __global__ void combine_kernel(const float4* __restrict__ O, const int32_t* __restrict__ ppos,
                                const float* __restrict__ topk_w, int k, int dq, void* y) {
+  grid_dep_launch();  // a GEMM after this kernel may start its prologue
   __shared__ int s_row[kMaxTopK];
   __shared__ float s_w[kMaxTopK];
   const long long t = blockIdx.x;
@@ -577,6 +579,7 @@ __global__ void reverse_dispatch_kernel(const float4* __restrict__ dXp,
                                         const float* __restrict__ dp_part, int np,
                                         const uint2* __restrict__ Wr, int k, int dq, void* dx,
                                         float* __restrict__ dl_row, float* __restrict__ dl_tok) {
+  grid_dep_launch();  // a GEMM after this kernel may start its prologue
   __shared__ int s_row[kMaxTopK];
   __shared__ int s_e[kMaxTopK];
   __shared__ float s_dl[kMaxTopK];
@@ -669,6 +672,7 @@ __global__ void router_wgrad_kernel(const uint4* __restrict__ X, const int32_t* 
                                     const int32_t* __restrict__ poff,
                                     const int32_t* __restrict__ counts, int dv, void* dw,
                                     int accumulate) {
+  grid_dep_launch();  // a GEMM after this kernel may start its prologue
   __shared__ float part[kRwRowLanes][8][8];
   const int e = blockIdx.x;
   const int cv = blockIdx.y * 8 + (threadIdx.x & 7);  // column vector index
