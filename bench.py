@@ -10,7 +10,8 @@ bf16, seeded synthetic inputs.  The weights (0.8 GB) and activations read per
 step are larger than the 129 MB L2, so no flush is needed between steps.
 
 Printed (rank 0, one JSON line): tokens/s over all ranks, per-kernel times
-from CUDA events recorded around each kernel inside the timed region, the
+from CUDA events recorded around each kernel on one in four steps of the timed
+region, the
 dominant kernel's roofline, the end-to-end number through the C ABI with
 pinned-host inputs and outputs, the fp64 oracle's CPU throughput on a small
 sample, and the SM clocks sampled during the timed region.
@@ -37,6 +38,7 @@ from routing_dispatch_grouped_router_gb300 import inputs as gen  # noqa: E402
 
 METRIC = "MoE layer fwd+bwd tokens/s on 1 GB300; grouped-GEMM % of tensor-core peak"
 WORKLOAD = "fine"
+PROFILE_EVERY = 4  # per-kernel events on one timed step in this many
 
 # Algorithmic work per launch of each kernel (R = T*k routed rows).
 #   GEMMs: 2*M*N*K flops with M summed over the experts' real rows.
@@ -512,9 +514,12 @@ def main():
         bus = None
     sampler = ClockSampler(str(bus) if bus is not None else None)
 
-    # ---- timed region: K steps, per-kernel events recorded on the stream
+    # ---- timed region: K steps.  Per-kernel events are recorded on the stream
+    # in one step of every PROFILE_EVERY (steps 0, 4, 8, ...): each event is a
+    # stream operation between two kernels, and recording them on every step
+    # would slow the very region they measure.
     api.profile_reset()
-    api.profile_enable(True)
+    prof_steps = (args.steps + PROFILE_EVERY - 1) // PROFILE_EVERY
     sampler.start()
     time.sleep(0.3)
     if world > 1:
@@ -523,7 +528,8 @@ def main():
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    for _ in range(args.steps):
+    for i in range(args.steps):
+        api.profile_enable(i % PROFILE_EVERY == 0)
         step()
     ev1.record(stream)
     torch.cuda.synchronize()
@@ -557,7 +563,7 @@ def main():
     movers = mover_bytes(shape, int(layer.layout.mb_count))
     if WORKLOAD == "mxfp8":
         movers.update(mx_quant_bytes(shape, int(layer.layout.mb_count), int(layer.layout.rows_max),
-                                     kernels, args.steps))
+                                     kernels, prof_steps))
     total_k = sum(v[1] for v in kernels.values())
     ksum = {}
     for name, (n, ms) in kernels.items():
@@ -662,6 +668,8 @@ def main():
             "roofline": roof, "movers": movers_perf, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps, "launches_per_step": launches_per_step,
             "clocks": clocks, "kernels": ksum,
+            "kernel_timing": f"CUDA events around each kernel on {prof_steps} of the "
+                             f"{args.steps} timed steps (one in {PROFILE_EVERY})",
         }
         print(json.dumps(line), flush=True)
     if world > 1:
