@@ -116,12 +116,12 @@ def gemm_bytes(shape: gen.Shape, micro_batches: int = 1, mx: bool = False,
 # grouped GEMMs on the fine workload, from the ncu capture summarised in
 # profiles/grouped_gemms_fine.txt (kernels as of the commit named there).
 NCU_TRAFFIC_FINE = {
-    "fwd_gate_up_swiglu": 689.628672e6 + 330.329e6,
-    "fwd_down": 343.459584e6 + 253.869e6,
-    "bwd_down_dgrad_swiglu": 767.473920e6 + 401.570e6,
-    "bwd_down_wgrad": 300.251904e6 + 479.844e6,
-    "bwd_gate_up_dgrad": 689.074688e6 + 271.439e6,
-    "bwd_gate_up_wgrad": 449.986816e6 + 1013.372e6,
+    "fwd_gate_up_swiglu": 688.822784e6 + 329.280e6,
+    "fwd_down": 343.471360e6 + 254.084e6,
+    "bwd_down_dgrad_swiglu": 768.187648e6 + 401.218e6,
+    "bwd_down_wgrad": 300.070400e6 + 479.529e6,
+    "bwd_gate_up_dgrad": 690.012160e6 + 271.601e6,
+    "bwd_gate_up_wgrad": 449.964800e6 + 1014.369e6,
 }
 
 
