@@ -594,6 +594,7 @@ __global__ void reverse_dispatch_kernel(const float4* __restrict__ dXp,
       p = topk_w[t * k + s];
       if (row >= 0) {
         const float* q = dp_part + static_cast<long long>(row) * np;
+#pragma unroll 4
         for (int j = 0; j < np; ++j) dp += q[j];
       }
     }
@@ -615,15 +616,25 @@ __global__ void reverse_dispatch_kernel(const float4* __restrict__ dXp,
   }
   __syncthreads();
   for (int c = threadIdx.x; c < dq; c += blockDim.x) {
+    // the k rows' loads all in flight, then the sum in slot order
+    float4 xr[kMaxTopK];
+    uint2 wr[kMaxTopK];
+#pragma unroll
+    for (int s = 0; s < kMaxTopK; ++s) {
+      if (s < k && s_row[s] >= 0) {
+        xr[s] = ld_nc_f4(dXp + static_cast<long long>(s_row[s]) * dq + c);
+        asm volatile("ld.global.nc.v2.b32 {%0, %1}, [%2];"
+                     : "=r"(wr[s].x), "=r"(wr[s].y)
+                     : "l"(Wr + static_cast<long long>(s_e[s]) * dq + c));
+      }
+    }
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int s = 0; s < k; ++s) {
-      if (s_row[s] < 0) continue;
-      add4(acc, ld_nc_f4(dXp + static_cast<long long>(s_row[s]) * dq + c));
-      uint2 w;
-      asm volatile("ld.global.nc.v2.b32 {%0, %1}, [%2];"
-                   : "=r"(w.x), "=r"(w.y)
-                   : "l"(Wr + static_cast<long long>(s_e[s]) * dq + c));
-      axpy4(acc, s_dl[s], bf16x4_to_f4(w));
+#pragma unroll
+    for (int s = 0; s < kMaxTopK; ++s) {
+      if (s < k && s_row[s] >= 0) {
+        add4(acc, xr[s]);
+        axpy4(acc, s_dl[s], bf16x4_to_f4(wr[s]));
+      }
     }
     store4<BF16_OUT>(dx, t, dq, c, acc);
   }
