@@ -130,16 +130,18 @@ def mx_quant_bytes(shape: gen.Shape, nmb: int, rows_max: int, kernels: dict, ste
     call the weights (rows: E4M3 codes + scales for the forward; columns along
     the dgrads' K for the backward: W_down as bf16 values, W_gate_up as
     transposed E4M3 codes + scales), per micro-batch the dispatched x rows
-    (codes), dy (one column-kernel launch reads it once and writes bf16 values
-    in both block directions) and the x rows along the columns for the weight
-    gradients."""
+    (codes), dy (one column-kernel launch writes bf16 values in both block
+    directions) and the x rows along the columns for the weight gradients.
+    The activation launches read the token rows through the row -> token map:
+    each token row once, each dispatched row written."""
     E, d, I = shape.E, shape.d, shape.I
     w_gu, w_d = E * 2 * I * d, E * d * I       # weight elements
     w = w_gu + w_d
     act = rows_max * d                         # one micro-batch's dispatched rows
+    tok = shape.T // nmb * d                   # one micro-batch's token rows
     q8 = 2 + 1 + 1 / 32                        # bf16 in, E4M3 code + 1/32 scale out
-    rows_bytes = w * q8 + nmb * act * q8
-    cols_bytes = w_d * 4 + w_gu * q8 + nmb * act * (2 + 2 + 2) + nmb * act * 4
+    rows_bytes = w * q8 + nmb * (tok * 2 + act * (1 + 1 / 32))
+    cols_bytes = w_d * 4 + w_gu * q8 + nmb * (tok * 2 + act * 4) + nmb * (tok * 2 + act * 2)
     out = {}
     for name, total in (("mx_quant_rows", rows_bytes), ("mx_quant_cols", cols_bytes)):
         if name in kernels:

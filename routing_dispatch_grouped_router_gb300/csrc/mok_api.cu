@@ -402,11 +402,14 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
                          at<int32_t>(workspace, F.block_base), o, status, st));
     void* x_perm = at<char>(saved, L.x_perm + (i % D.ring) * L.ring_slot_bytes);
     void* gu = D.recompute_gu ? nullptr : at<char>(saved, L.gate_up + blk);
-    MOK_CUDA(launch_dispatch_rows(D, xi, o.ppos, o.ptok, o.padded_offsets, x_perm, status, st));
+    if (!D.mx)
+      MOK_CUDA(launch_dispatch_rows(D, xi, o.ppos, o.ptok, o.padded_offsets, x_perm, status, st));
     if (D.mx) {
-      // expert GEMMs on the block-scaled tensor cores: x rows to MXFP8, the
-      // gate/up GEMM writes h as MXFP8 for the down projection
-      MOK_CUDA(launch_mx_rows(x_perm, nullptr, D.rows_max, D.d, xq_c, xq_s, st, true));
+      // expert GEMMs on the block-scaled tensor cores: the dispatched x rows
+      // go to MXFP8 straight from the token rows (no bf16 copy), the gate/up
+      // GEMM writes h as MXFP8 for the down projection
+      MOK_CUDA(launch_mx_rows(xi, nullptr, D.rows_max, D.d, xq_c, xq_s, st, true, o.ptok,
+                              static_cast<int>(D.T)));
       MOK_CUDA(gemm_fwd_gate_up_mx(D, xq_c, xq_s, wgu_c, wgu_s, o.mtile_prefix, o.padded_offsets,
                                    gu, h_c, h_s, status, st));
       MOK_CUDA(gemm_fwd_down_mx(D, h_c, h_s, wd_c, wd_s, o.mtile_prefix, o.padded_offsets, O,
@@ -518,14 +521,16 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
       // this micro-batch's rows go to its own slot (the deferred wgrad reads them)
       x_perm = at<char>(workspace, B.x_def) + static_cast<size_t>(i) * rows * D.d * 2;
       MOK_CUDA(launch_dispatch_rows(D, xi, ppos, ptok, poff, x_perm, status, st));
-    } else if (i < D.nmb - D.ring) {
+    } else if (i < D.nmb - D.ring && !D.mx) {
       // the slot now holds a later micro-batch: dispatch this one again
+      // (MXFP8 reads the token rows through the row -> token map instead)
       MOK_CUDA(launch_dispatch_rows(D, xi, ppos, ptok, poff, x_perm, status, st));
     }
     if (D.recompute_gu) {
       // the forward's gate/up GEMM again, g and u only (no h)
       if (D.mx) {
-        MOK_CUDA(launch_mx_rows(x_perm, nullptr, D.rows_max, D.d, rxq_c, rxq_s, st, true));
+        MOK_CUDA(launch_mx_rows(xi, nullptr, D.rows_max, D.d, rxq_c, rxq_s, st, true, ptok,
+                                static_cast<int>(D.T)));
         MOK_CUDA(gemm_fwd_gate_up_mx(D, rxq_c, rxq_s, rwgu_c, rwgu_s, mtp, poff,
                                      const_cast<void*>(gu), nullptr, nullptr, status, st));
       } else {
@@ -533,8 +538,9 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
                                   nullptr, status, st));
       }
     }
-    // reverse-combine: pull dy rows into expert order
-    MOK_CUDA(launch_dispatch_rows(D, dyi, ppos, ptok, poff, dy_perm_i, status, st));
+    // reverse-combine: dy rows into expert order (MXFP8: the quantisers below
+    // read them through the row -> token map instead)
+    if (!D.mx) MOK_CUDA(launch_dispatch_rows(D, dyi, ppos, ptok, poff, dy_perm_i, status, st));
     const void* dy_row_op = dy_perm_i;
     const void* dy_col_op = dy_perm_i;
     const void* x_col_op = x_perm;
@@ -542,9 +548,11 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
       void* q1 = at<char>(workspace, B.dyq_row);
       void* q2 = slot(at<char>(workspace, B.dyq_col), i, rows * D.d * 2);
       void* q3 = slot(at<char>(workspace, B.xq_col), i, rows * D.d * 2);
-      // dy in both block directions from one read
-      MOK_CUDA(launch_mx_cols(dy_perm_i, q2, D.rows_max, D.d, nullptr, nullptr, st, q1));
-      MOK_CUDA(launch_mx_cols(x_perm, q3, D.rows_max, D.d, nullptr, nullptr, st));
+      // dy in both block directions from one read of its token rows
+      MOK_CUDA(launch_mx_cols(dyi, q2, D.rows_max, D.d, nullptr, nullptr, st, q1, ptok,
+                              static_cast<int>(D.T)));
+      MOK_CUDA(launch_mx_cols(xi, q3, D.rows_max, D.d, nullptr, nullptr, st, nullptr, ptok,
+                              static_cast<int>(D.T)));
       dy_row_op = q1;
       dy_col_op = q2;
       x_col_op = q3;

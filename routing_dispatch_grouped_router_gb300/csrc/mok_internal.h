@@ -194,8 +194,11 @@ cudaError_t gemm_dense_bf16(int64_t M, int64_t N, int64_t K, const void* A, bool
 // blocks of 32 rows; codes/scales may be null.
 // tiled: scales in the tiled layout of mx_tiled_off (rows, cols multiples of
 // 128), the layout of the expert GEMMs' MXFP8 operands; else row-major.
+// rowmap != NULL: output row r quantises input row rowmap[r] (zeros where that is
+// not in [0, T)), so the dispatched rows need not be materialised.
 cudaError_t launch_mx_rows(const void* in, void* out, long long rows, long long cols,
-                           uint8_t* codes, uint8_t* scales, cudaStream_t st, bool tiled = false);
+                           uint8_t* codes, uint8_t* scales, cudaStream_t st, bool tiled = false,
+                           const int32_t* rowmap = nullptr, int T = 0);
 // Column blocks of a weight [rows = E*group_rows, cols] written as the K-major
 // operand [E*cols, group_rows]: E4M3 codes and tiled scales (group_rows % 128,
 // cols % 128).
@@ -205,7 +208,7 @@ cudaError_t launch_mx_cols_t(const void* in, long long rows, long long cols, lon
 // the row-block dequantised values of the same input (cols % 32 == 0).
 cudaError_t launch_mx_cols(const void* in, void* out, long long rows, long long cols,
                            uint8_t* codes, uint8_t* scales, cudaStream_t st,
-                           void* rows_out = nullptr);
+                           void* rows_out = nullptr, const int32_t* rowmap = nullptr, int T = 0);
 
 // One CTA whose mbarrier wait can never complete: exercises the bounded wait.
 cudaError_t launch_bounded_wait_selftest(int* status, cudaStream_t st);

@@ -75,13 +75,22 @@ __device__ __forceinline__ void uniform_factors(int s, float (&down)[8], float (
 // multiple of 4, so a block's four lanes are all in range or all out.
 // tiled_nkg > 0: scales in the tiled layout of a matrix with tiled_nkg*128
 // columns (mx_tiled_off); 0: row-major [rows, cols/32].
+// Optional source-row map of the quantisers: output row r takes input row
+// map[r] when that is a row of the input (0 <= map[r] < T), zeros otherwise
+// (the layer's dispatched rows: output row = padded row, input = token rows).
+struct RowMap {
+  const int32_t* map;  // NULL: output row r is input row r
+  int T;
+};
+
 constexpr int kRowUnroll = 4;
 template <bool CODES, bool OUT>
 __global__ void __launch_bounds__(256) mx_rows_kernel(const uint4* __restrict__ in,
                                                       uint4* __restrict__ out,
                                                       uint8_t* __restrict__ codes,
                                                       uint8_t* __restrict__ scales,
-                                                      long long nchunks, long long tiled_nkg) {
+                                                      long long nchunks, long long tiled_nkg,
+                                                      RowMap rm, uint32_t c8) {
   grid_dep_launch();  // a GEMM after this kernel may start its prologue
   const int lane = threadIdx.x & 31;
   const long long G = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -91,7 +100,13 @@ __global__ void __launch_bounds__(256) mx_rows_kernel(const uint4* __restrict__ 
 #pragma unroll
     for (int u = 0; u < kRowUnroll; ++u) {
       const long long c = i0 + lane + u * G;
-      w[u] = c < nchunks ? ld_global_nc_v4(in + c) : make_uint4(0, 0, 0, 0);
+      long long src = c;
+      if (rm.map && c < nchunks) {  // chunk count below 2^32 (checked by the launcher)
+        const uint32_t row = static_cast<uint32_t>(c) / c8;
+        const int t = rm.map[row];
+        src = (t >= 0 && t < rm.T) ? static_cast<long long>(t) * c8 + (c - row * c8) : -1;
+      }
+      w[u] = (c < nchunks && src >= 0) ? ld_global_nc_v4(in + src) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < kRowUnroll; ++u) {
@@ -134,7 +149,8 @@ __global__ void __launch_bounds__(256, ROWS_OUT ? 3 : 4) mx_cols_kernel(const ui
                                                          uint8_t* __restrict__ codes,
                                                          uint8_t* __restrict__ scales,
                                                          uint4* __restrict__ rows_out,
-                                                         long long row_blocks, long long cols) {
+                                                         long long row_blocks, long long cols,
+                                                         RowMap rm) {
   grid_dep_launch();  // a GEMM after this kernel may start its prologue
   __shared__ __align__(16) float s_part[8][256];
   __shared__ __align__(16) int s_exp[256];
@@ -149,8 +165,14 @@ __global__ void __launch_bounds__(256, ROWS_OUT ? 3 : 4) mx_cols_kernel(const ui
     const bool ok = ch < c8;
     uint4 x[4];
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
-      x[r] = ok ? ld_global_nc_v4(in + (rb * 32 + w + 8 * r) * c8 + ch) : make_uint4(0, 0, 0, 0);
+    for (int r = 0; r < 4; ++r) {
+      long long src = rb * 32 + w + 8 * r;
+      if (rm.map) {
+        const int t = rm.map[src];
+        src = (t >= 0 && t < rm.T) ? t : -1;
+      }
+      x[r] = (ok && src >= 0) ? ld_global_nc_v4(in + src * c8 + ch) : make_uint4(0, 0, 0, 0);
+    }
     float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -284,31 +306,37 @@ static unsigned grid_for(long long n, int threads) {
 }
 
 cudaError_t launch_mx_rows(const void* in, void* out, long long rows, long long cols,
-                           uint8_t* codes, uint8_t* scales, cudaStream_t st, bool tiled) {
+                           uint8_t* codes, uint8_t* scales, cudaStream_t st, bool tiled,
+                           const int32_t* rowmap, int T) {
   if (cols % 32) return cudaErrorInvalidValue;
   if (tiled && (rows % 128 || cols % 128)) return cudaErrorInvalidValue;
   const long long nchunks = rows * (cols / 8);
   if (nchunks == 0) return cudaSuccess;
   if (nchunks / 4 >= (1LL << 32)) return cudaErrorInvalidValue;  // 32-bit block index
+  if (rowmap && nchunks >= (1LL << 32)) return cudaErrorInvalidValue;  // 32-bit row index
+  const RowMap rm{rowmap, T};
+  const uint32_t c8 = static_cast<uint32_t>(cols / 8);
   ProfScope prof("mx_quant_rows", st);
   const unsigned grid = grid_for((nchunks + kRowUnroll - 1) / kRowUnroll, 256);
   const uint4* i4 = static_cast<const uint4*>(in);
   uint4* o4 = static_cast<uint4*>(out);
   const long long nkg = tiled ? cols / 128 : 0;
   if (codes && out)
-    mx_rows_kernel<true, true><<<grid, 256, 0, st>>>(i4, o4, codes, scales, nchunks, nkg);
+    mx_rows_kernel<true, true><<<grid, 256, 0, st>>>(i4, o4, codes, scales, nchunks, nkg, rm, c8);
   else if (codes)
-    mx_rows_kernel<true, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, nchunks, nkg);
+    mx_rows_kernel<true, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, nchunks, nkg, rm, c8);
   else if (out)
-    mx_rows_kernel<false, true><<<grid, 256, 0, st>>>(i4, o4, codes, scales, nchunks, nkg);
+    mx_rows_kernel<false, true><<<grid, 256, 0, st>>>(i4, o4, codes, scales, nchunks, nkg, rm, c8);
   else
-    mx_rows_kernel<false, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, nchunks, nkg);
+    mx_rows_kernel<false, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, nchunks, nkg, rm, c8);
   count_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_mx_cols(const void* in, void* out, long long rows, long long cols,
-                           uint8_t* codes, uint8_t* scales, cudaStream_t st, void* rows_out) {
+                           uint8_t* codes, uint8_t* scales, cudaStream_t st, void* rows_out,
+                           const int32_t* rowmap, int T) {
+  const RowMap rm{rowmap, T};
   if (rows % 32 || cols % 8 || (rows_out && (cols % 32 || !out || codes)))
     return cudaErrorInvalidValue;
   const long long ntiles = (rows / 32) * ((cols + 255) / 256);
@@ -322,15 +350,15 @@ cudaError_t launch_mx_cols(const void* in, void* out, long long rows, long long 
   uint4* r4 = static_cast<uint4*>(rows_out);
   const long long rb = rows / 32;
   if (rows_out)  // the layer's dy: bf16 values in both directions
-    mx_cols_kernel<false, true, true><<<grid, 256, 0, st>>>(i4, o4, codes, scales, r4, rb, cols);
+    mx_cols_kernel<false, true, true><<<grid, 256, 0, st>>>(i4, o4, codes, scales, r4, rb, cols, rm);
   else if (codes && out)
-    mx_cols_kernel<true, true, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, r4, rb, cols);
+    mx_cols_kernel<true, true, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, r4, rb, cols, rm);
   else if (codes)
-    mx_cols_kernel<true, false, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, r4, rb, cols);
+    mx_cols_kernel<true, false, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, r4, rb, cols, rm);
   else if (out)
-    mx_cols_kernel<false, true, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, r4, rb, cols);
+    mx_cols_kernel<false, true, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, r4, rb, cols, rm);
   else
-    mx_cols_kernel<false, false, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, r4, rb, cols);
+    mx_cols_kernel<false, false, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, r4, rb, cols, rm);
   count_launch();
   return cudaGetLastError();
 }

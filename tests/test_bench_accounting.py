@@ -62,10 +62,12 @@ def test_mx_quantiser_bytes_average_over_launches():
     kernels = {"mx_quant_cols": (18 * 20, 1.0), "mx_quant_rows": (10 * 20, 1.0)}
     got = bench.mx_quant_bytes(s, nmb, rows_max, kernels, steps=20)
     w_gu, w_d = s.E * 2 * s.I * s.d, s.E * s.I * s.d
-    act = rows_max * s.d
+    act, tok = rows_max * s.d, s.T // nmb * s.d
     q8 = 3 + 1 / 32
-    assert got["mx_quant_cols"] * 18 == pytest.approx(4 * w_d + q8 * w_gu + nmb * act * (6 + 4))
-    assert got["mx_quant_rows"] * 10 == pytest.approx((w_gu + w_d + nmb * act) * q8)
+    assert got["mx_quant_cols"] * 18 == pytest.approx(
+        4 * w_d + q8 * w_gu + nmb * (2 * tok + 4 * act) + nmb * (2 * tok + 2 * act))
+    assert got["mx_quant_rows"] * 10 == pytest.approx(
+        (w_gu + w_d) * q8 + nmb * (2 * tok + act * (1 + 1 / 32)))
 
 
 def test_reference_arm_prints_one_json_line():
