@@ -1,4 +1,4 @@
-// Router top-k, dispatch plan, row gather (dispatch / reverse-combine),
+// Router top-k, dispatch plan, row dispatch (dispatch / reverse-combine),
 // combine, reverse-dispatch with the router backward, router weight grad.
 //
 // Sources (page title, section):
@@ -6,9 +6,11 @@
 //     network (router) picks the best few experts for every token.
 //   [dothoosh] "Cursor Mixture-of-Kittens cuts MoE training latency by 5.8x",
 //     "MoK technical details", bullet "Hybrid communication": forward =
-//     dispatch (pulled by the receiver) then combine; backward =
-//     reverse-combine (pulled) then reverse-dispatch; bullet "Ring buffer
-//     logic": no token is dropped and no buffer is sized by the CPU.
+//     dispatch then combine; backward = reverse-combine then
+//     reverse-dispatch (across GPUs the pages pull the dispatch; within one
+//     HBM the dispatch here is driven by the token so that each token row is
+//     read once); bullet "Ring buffer logic": no token is dropped and no
+//     buffer is sized by the CPU.
 //   [aikraft] "Cursor MoK: revolution in MoE model training on NVL72", §03:
 //     the CPU is kept off the critical path (no host synchronisation).
 //
@@ -332,7 +334,7 @@ cudaError_t launch_plan(const Dims& D, const int32_t* topk_idx, const float* top
   return cudaGetLastError();
 }
 
-// ------------------------------------------------------------- row gather --
+// ----------------------------------------------------------- row dispatch --
 
 // Dispatch of token rows into the padded expert-major row space, staged
 // through TMA and driven by the token: padded row r < padded_offsets[E]
