@@ -89,8 +89,7 @@ __global__ void __launch_bounds__(256) mx_rows_kernel(const uint4* __restrict__ 
                                                       uint4* __restrict__ out,
                                                       uint8_t* __restrict__ codes,
                                                       uint8_t* __restrict__ scales,
-                                                      long long nchunks, long long tiled_nkg,
-                                                      RowMap rm, uint32_t c8) {
+                                                      long long nchunks, long long tiled_nkg) {
   grid_dep_launch();  // a GEMM after this kernel may start its prologue
   const int lane = threadIdx.x & 31;
   const long long G = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -100,13 +99,7 @@ __global__ void __launch_bounds__(256) mx_rows_kernel(const uint4* __restrict__ 
 #pragma unroll
     for (int u = 0; u < kRowUnroll; ++u) {
       const long long c = i0 + lane + u * G;
-      long long src = c;
-      if (rm.map && c < nchunks) {  // chunk count below 2^32 (checked by the launcher)
-        const uint32_t row = static_cast<uint32_t>(c) / c8;
-        const int t = rm.map[row];
-        src = (t >= 0 && t < rm.T) ? static_cast<long long>(t) * c8 + (c - row * c8) : -1;
-      }
-      w[u] = (c < nchunks && src >= 0) ? ld_global_nc_v4(in + src) : make_uint4(0, 0, 0, 0);
+      w[u] = c < nchunks ? ld_global_nc_v4(in + c) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < kRowUnroll; ++u) {
@@ -131,6 +124,59 @@ __global__ void __launch_bounds__(256) mx_rows_kernel(const uint4* __restrict__ 
         const uint32_t bpr = static_cast<uint32_t>(tiled_nkg) * 4;  // blocks per row
         const long long off = tiled_nkg > 0 ? mx_tiled_off(b / bpr, b % bpr, tiled_nkg) : b;
         scales[off] = static_cast<uint8_t>(s + 127);
+      }
+    }
+  }
+}
+
+// Row blocks of rows taken through a row map (output row r quantises input row
+// map[r], zeros when that is not a row of the input): one warp per output
+// row, the map read once per row; the lanes walk the row in 16-byte chunks,
+// four lanes per 32-value block as in mx_rows_kernel.  c8 % 4 == 0.
+template <bool CODES, bool OUT>
+__global__ void __launch_bounds__(256) mx_rows_map_kernel(const uint4* __restrict__ in,
+                                                          uint4* __restrict__ out,
+                                                          uint8_t* __restrict__ codes,
+                                                          uint8_t* __restrict__ scales,
+                                                          long long rows, uint32_t c8,
+                                                          long long tiled_nkg, RowMap rm) {
+  grid_dep_launch();  // a GEMM after this kernel may start its prologue
+  const int lane = threadIdx.x & 31;
+  const long long nw = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
+  for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+       r < rows; r += nw) {
+    const int t = rm.map[r];
+    const bool src_ok = t >= 0 && t < rm.T;
+    const uint4* src = in + static_cast<long long>(src_ok ? t : 0) * c8;
+    for (uint32_t j0 = 0; j0 < c8; j0 += 32 * kRowUnroll) {  // the same trips for every lane
+      uint4 w[kRowUnroll];
+#pragma unroll
+      for (int u = 0; u < kRowUnroll; ++u) {
+        const uint32_t j = j0 + u * 32 + lane;
+        w[u] = (src_ok && j < c8) ? ld_global_nc_v4(src + j) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kRowUnroll; ++u) {
+        const uint32_t j = j0 + u * 32 + lane;
+        float v[8];
+        unpack8(w[u], v);
+        float m = amax8(v);
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        if (j >= c8) continue;
+        const int s = mx_shared_of(m);
+        float down[8], up[8];
+        uniform_factors(s, down, up);
+        uint2 q;
+        uint4 deq;
+        mx_quant8<CODES, OUT>(v, down, up, &q, &deq);
+        const long long c = r * c8 + j;  // output chunk
+        if (CODES) reinterpret_cast<uint2*>(codes)[c] = q;
+        if (OUT) out[c] = deq;
+        if (scales && (lane & 3) == 0) {
+          const long long off = tiled_nkg > 0 ? mx_tiled_off(r, j >> 2, tiled_nkg) : (c >> 2);
+          scales[off] = static_cast<uint8_t>(s + 127);
+        }
       }
     }
   }
@@ -313,22 +359,37 @@ cudaError_t launch_mx_rows(const void* in, void* out, long long rows, long long 
   const long long nchunks = rows * (cols / 8);
   if (nchunks == 0) return cudaSuccess;
   if (nchunks / 4 >= (1LL << 32)) return cudaErrorInvalidValue;  // 32-bit block index
-  if (rowmap && nchunks >= (1LL << 32)) return cudaErrorInvalidValue;  // 32-bit row index
   const RowMap rm{rowmap, T};
   const uint32_t c8 = static_cast<uint32_t>(cols / 8);
   ProfScope prof("mx_quant_rows", st);
-  const unsigned grid = grid_for((nchunks + kRowUnroll - 1) / kRowUnroll, 256);
   const uint4* i4 = static_cast<const uint4*>(in);
   uint4* o4 = static_cast<uint4*>(out);
   const long long nkg = tiled ? cols / 128 : 0;
+  if (rowmap) {  // one warp per output row
+    const long long cap = static_cast<long long>(num_sms_current_device()) * 8;
+    const long long need = (rows + 7) / 8;
+    const unsigned g = static_cast<unsigned>(need < cap ? need : cap);
+    if (codes && out)
+      mx_rows_map_kernel<true, true><<<g, 256, 0, st>>>(i4, o4, codes, scales, rows, c8, nkg, rm);
+    else if (codes)
+      mx_rows_map_kernel<true, false><<<g, 256, 0, st>>>(i4, o4, codes, scales, rows, c8, nkg, rm);
+    else if (out)
+      mx_rows_map_kernel<false, true><<<g, 256, 0, st>>>(i4, o4, codes, scales, rows, c8, nkg, rm);
+    else
+      mx_rows_map_kernel<false, false><<<g, 256, 0, st>>>(i4, o4, codes, scales, rows, c8, nkg,
+                                                          rm);
+    count_launch();
+    return cudaGetLastError();
+  }
+  const unsigned grid = grid_for((nchunks + kRowUnroll - 1) / kRowUnroll, 256);
   if (codes && out)
-    mx_rows_kernel<true, true><<<grid, 256, 0, st>>>(i4, o4, codes, scales, nchunks, nkg, rm, c8);
+    mx_rows_kernel<true, true><<<grid, 256, 0, st>>>(i4, o4, codes, scales, nchunks, nkg);
   else if (codes)
-    mx_rows_kernel<true, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, nchunks, nkg, rm, c8);
+    mx_rows_kernel<true, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, nchunks, nkg);
   else if (out)
-    mx_rows_kernel<false, true><<<grid, 256, 0, st>>>(i4, o4, codes, scales, nchunks, nkg, rm, c8);
+    mx_rows_kernel<false, true><<<grid, 256, 0, st>>>(i4, o4, codes, scales, nchunks, nkg);
   else
-    mx_rows_kernel<false, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, nchunks, nkg, rm, c8);
+    mx_rows_kernel<false, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, nchunks, nkg);
   count_launch();
   return cudaGetLastError();
 }
