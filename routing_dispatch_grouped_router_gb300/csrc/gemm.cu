@@ -418,26 +418,6 @@ __device__ __forceinline__ void store_hi_lo16(__nv_bfloat16* hi, __nv_bfloat16* 
   }
 }
 
-// Stores 32 values as bf16 hi = bf16(v) and lo = bf16(v - hi).
-__device__ __forceinline__ void store_hi_lo32(__nv_bfloat16* hi, __nv_bfloat16* lo,
-                                              const float (&v)[32]) {
-  uint4* ph = reinterpret_cast<uint4*>(hi);
-  uint4* pl = reinterpret_cast<uint4*>(lo);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float v0 = v[8 * q + 2 * j], v1 = v[8 * q + 2 * j + 1];
-      const float a0 = bf16_round(v0), a1 = bf16_round(v1);
-      h[j] = pack_bf16x2(a0, a1);
-      l[j] = pack_bf16x2(v0 - a0, v1 - a1);
-    }
-    ph[q] = make_uint4(h[0], h[1], h[2], h[3]);
-    pl[q] = make_uint4(l[0], l[1], l[2], l[3]);
-  }
-}
-
 // One warp writes its 32 rows x 32 fp32 columns to the 4 KB staging buffer in
 // the 128-byte swizzled layout (16-byte chunk j of row r at chunk j ^ (r%8)),
 // then lane 0 stores it with one TMA tensor store at (x, y).
