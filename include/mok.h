@@ -121,14 +121,16 @@ typedef struct mok_saved_layout {
   size_t padded_pos;      /* int32 [T,k] row of (t,s) in the padded row space */
   size_t padded_token;    /* int32 [rows_max] token of each padded row, -1 for padding */
   size_t row_weight;      /* fp32 [rows_max] routing weight of each padded row, 0 for padding */
-  size_t x_perm;          /* bf16 [rows_max, d] dispatched token rows */
+  size_t x_perm;          /* bf16 [rows_max, d] dispatched token rows; MOK_NOT_KEPT with
+                             MOK_MXFP8 (its quantisers read the token rows through
+                             padded_token instead) */
   size_t gate_up;         /* fp32 [rows_max, 2I] pre-activation gate (cols 0..I-1) and up (I..2I-1);
                              MOK_NOT_KEPT with MOK_FLAG_RECOMPUTE_GATE_UP */
   size_t rows_max;        /* number of padded rows the buffers hold: T*k + 127*min(E, T*k), rounded to 128 */
   size_t mb_count;        /* micro-batches (1 without micro-batching) */
   size_t mb_stride;       /* bytes between consecutive micro-batches' fields */
   size_t ring_slots;      /* slots of dispatched rows (1 without micro-batching) */
-  size_t ring_slot_bytes; /* bytes between ring slots */
+  size_t ring_slot_bytes; /* bytes between ring slots (0 with MOK_MXFP8) */
   size_t total;           /* size of `saved` in bytes */
 } mok_saved_layout;
 

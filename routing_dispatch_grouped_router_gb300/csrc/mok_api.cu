@@ -177,7 +177,9 @@ void saved_layout(const Dims& D, mok_saved_layout* L, size_t* mtile_prefix_off) 
   BlockL B;
   block_layout(D, &B);
   const size_t base = 256;
-  const size_t slot = static_cast<size_t>(D.rows_max) * D.d * 2;
+  // MXFP8 keeps no dispatched bf16 rows: its quantisers read the token rows
+  // through the row -> token map
+  const size_t slot = D.mx ? 0 : static_cast<size_t>(D.rows_max) * D.d * 2;
   const size_t slot_al = (slot + 255) & ~static_cast<size_t>(255);
   const size_t ring0 = base + B.total * D.nmb;
   L->status = 0;
@@ -193,7 +195,7 @@ void saved_layout(const Dims& D, mok_saved_layout* L, size_t* mtile_prefix_off) 
   L->padded_token = base + B.padded_token;
   L->row_weight = base + B.row_weight;
   L->gate_up = D.recompute_gu ? MOK_NOT_KEPT : base + B.gate_up;
-  L->x_perm = ring0;
+  L->x_perm = D.mx ? MOK_NOT_KEPT : ring0;
   L->rows_max = static_cast<size_t>(D.rows_max);
   L->mb_count = static_cast<size_t>(D.nmb);
   L->mb_stride = B.total;
@@ -400,7 +402,7 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
     o.row_w = at<float>(saved, L.row_weight + blk);
     MOK_CUDA(launch_plan(D, topk_idx, topk_w, at<int32_t>(workspace, F.block_counts),
                          at<int32_t>(workspace, F.block_base), o, status, st));
-    void* x_perm = at<char>(saved, L.x_perm + (i % D.ring) * L.ring_slot_bytes);
+    void* x_perm = D.mx ? nullptr : at<char>(saved, L.x_perm + (i % D.ring) * L.ring_slot_bytes);
     void* gu = D.recompute_gu ? nullptr : at<char>(saved, L.gate_up + blk);
     if (!D.mx)
       MOK_CUDA(launch_dispatch_rows(D, xi, o.ppos, o.ptok, o.padded_offsets, x_perm, status, st));
@@ -516,7 +518,9 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
     const int32_t* ptok = at<int32_t>(saved, L.padded_token + blk);
     const float* row_w = at<float>(saved, L.row_weight + blk);
     const void* gu = D.recompute_gu ? at<char>(workspace, B.gu) : at<char>(saved, L.gate_up + blk);
-    void* x_perm = const_cast<char*>(at<char>(saved, L.x_perm + (i % D.ring) * L.ring_slot_bytes));
+    void* x_perm = D.mx ? nullptr
+                        : const_cast<char*>(at<char>(saved, L.x_perm + (i % D.ring) *
+                                                                  L.ring_slot_bytes));
     if (defer && !D.mx) {
       // this micro-batch's rows go to its own slot (the deferred wgrad reads them)
       x_perm = at<char>(workspace, B.x_def) + static_cast<size_t>(i) * rows * D.d * 2;

@@ -77,6 +77,21 @@ def test_workspace_sizes_cover_the_layout(lib):
     _no_overlap(_regions(L, 256, 2, 8, 256, 128), L.total)
 
 
+def test_mxfp8_keeps_no_dispatched_rows(lib):
+    """MXFP8 quantises the dispatched x rows straight from the token rows, so
+    `saved` has no ring of bf16 rows: x_perm is not kept and the buffer is
+    that much smaller than the BF16 one."""
+    bf = _desc(T=1024, mb=256, ring=2)
+    mx = _desc(T=1024, mb=256, ring=2)
+    mx.dtype = 1
+    Lb, Lm = _lib.SavedLayout(), _lib.SavedLayout()
+    assert lib.mok_moe_saved_layout(ctypes.byref(bf), ctypes.byref(Lb)) == 0
+    assert lib.mok_moe_saved_layout(ctypes.byref(mx), ctypes.byref(Lm)) == 0
+    assert Lm.x_perm == (1 << 64) - 1 and Lm.ring_slot_bytes == 0  # MOK_NOT_KEPT
+    assert Lb.total - Lm.total == 2 * Lb.ring_slot_bytes
+    _no_overlap(_regions(Lm, 1024, 2, 8, 256, 128, mb=256)[:-1], Lm.total)
+
+
 def test_micro_batch_layout(lib):
     d = _desc(T=1024, mb=256, ring=2)
     L = _lib.SavedLayout()
