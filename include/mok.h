@@ -296,8 +296,11 @@ const char* mok_status_string(mok_status status);
 int32_t mok_last_launch_count(void);
 
 /* Per-kernel timing.  While enabled, the library brackets each kernel it
- * enqueues with a pair of CUDA events on the same stream (host-side cost
- * only; the kernels themselves are unchanged).  mok_profile_collect waits
+ * enqueues with a pair of CUDA events on the same stream.  The kernels are
+ * unchanged, but the events are stream operations between them: they keep a
+ * GEMM's programmatic dependent launch from overlapping the kernel before it,
+ * so a profiled step runs slightly slower than an unprofiled one.
+ * mok_profile_collect waits
  * for the recorded events, then writes up to `max` entries, one per kernel
  * name, with launch counts and summed durations since the last reset, and
  * stores the number of entries in *n.  Not thread-safe: enable it around a

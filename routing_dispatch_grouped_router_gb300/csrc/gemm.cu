@@ -35,6 +35,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "mok_internal.h"
@@ -1342,7 +1343,10 @@ static cudaError_t launch(const char* name, const CUtensorMap& ta, const CUtenso
   attr[1].val.clusterDim.z = 1;
   cfg.numAttrs = 2;
   cfg.gridDim = dim3(static_cast<unsigned>(num_sms_current_device() / 2 * 2), 1, 1);
-  static int max_clusters = -1;  // per kernel instantiation and process (one device type)
+  // per kernel instantiation and process (one device type); racing first
+  // launches compute the same value
+  static std::atomic<int> max_clusters_cache{-1};
+  int max_clusters = max_clusters_cache.load(std::memory_order_relaxed);
   if (max_clusters < 0) {
     cudaLaunchConfig_t q = cfg;  // the cluster shape alone
     q.attrs = &attr[1];
@@ -1351,6 +1355,7 @@ static cudaError_t launch(const char* name, const CUtensorMap& ta, const CUtenso
     e = cudaOccupancyMaxActiveClusters(&n, kern, &q);
     if (e != cudaSuccess) return e;
     max_clusters = n;
+    max_clusters_cache.store(n, std::memory_order_relaxed);
   }
   if (max_clusters < 1) return cudaErrorInvalidConfiguration;
   int clusters = max_clusters < max_units ? max_clusters : max_units;

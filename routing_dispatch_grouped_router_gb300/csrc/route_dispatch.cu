@@ -462,13 +462,10 @@ cudaError_t launch_dispatch_rows(const Dims& D, const void* src, const int32_t* 
   nslot = nslot > kDispatchMaxSlots ? kDispatchMaxSlots : nslot;
   if (nslot < kDispatchLag + 2) return cudaErrorInvalidValue;
   const int smem = nslot * static_cast<int>(row_bytes);
-  static int attr = 0;
-  if (smem > attr) {
-    cudaError_t e = cudaFuncSetAttribute(dispatch_rows_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr = smem;
-  }
+  // set on every launch: the attribute belongs to the current device
+  cudaError_t e = cudaFuncSetAttribute(dispatch_rows_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
   long long grid = static_cast<long long>(num_sms_current_device()) * per_sm;
   if (grid > D.T) grid = D.T;
   ProfScope prof("dispatch_rows", st);
