@@ -53,6 +53,9 @@ SMALL = {
     "one_token": gen.Shape(T=1, d=128, E=8, I=128, k=8),
     "many_experts": gen.Shape(T=64, d=128, E=128, I=128, k=8),
     "wide": gen.Shape(T=512, d=512, E=16, I=512, k=4),
+    # the widest rows the layer takes: 32 KB per token row, so the dispatch
+    # runs one CTA per SM with six row slots
+    "d16384": gen.Shape(T=64, d=16384, E=4, I=128, k=2),
 }
 
 
@@ -288,7 +291,7 @@ def test_layer_micro_batched_bf16(ring):
     _gpu.full_parity(shape, inp, gpu)
 
 
-@pytest.mark.parametrize("name", ["tiny", "wide", "k1_I384"])
+@pytest.mark.parametrize("name", ["tiny", "wide", "k1_I384", "d16384"])
 def test_layer_parity_mxfp8(name):
     shape = SMALL[name]
     inp = gen.make_inputs(shape, seed=0)
