@@ -164,10 +164,26 @@ def mover_bytes(shape: gen.Shape, micro_batches: int = 1) -> dict:
         "combine": R * 4 * d + T * 4 * d + R * 8,
         # read k fp32 dX rows and the dp partials, write fp32 dx (router rows from L2)
         "reverse_dispatch": R * 4 * d + T * 4 * d + R * (12 + 4 * np_),
-        # read each token row once (x, through the row -> token map), the map and
-        # dl per row, write dW_r
+        # read each token row once, the k (expert, dl) pairs per token, write dW_r
         "router_wgrad": T * d * 2 + R * 8 + E * d * 4,
     }
+
+
+# kernels whose time belongs to another one's step: the router-weight
+# gradient is a tensor-core GEMM over token chunks plus the in-order sum of
+# its chunks' partial products
+FOLDED = {"router_wgrad_reduce": "router_wgrad"}
+
+
+def fold_kernels(kernels: dict) -> dict:
+    """{name: (launches, ms)} with each FOLDED kernel's time added to the
+    kernel it completes; the launch count stays that kernel's own."""
+    out = {n: v for n, v in kernels.items() if n not in FOLDED}
+    for n, (_, ms) in kernels.items():
+        if n in FOLDED:
+            launches, total = out.get(FOLDED[n], (0, 0.0))
+            out[FOLDED[n]] = (launches, total + ms)
+    return out
 
 
 def mover_write_bytes(shape: gen.Shape, micro_batches: int = 1) -> dict:
@@ -185,22 +201,28 @@ def mover_roofline_us(total_bytes: float, write_bytes: float, copy_gbs: float,
     return max(total_bytes / copy_gbs, write_bytes / write_gbs) / 1e3
 
 
-def measure_write_gbs(torch) -> float:
-    """HBM write bandwidth on this GPU: a 1 GiB zero fill (library kernel),
-    best of 5 CUDA-event timings, after one warm-up."""
+def measure_write_gbs(torch, api) -> tuple:
+    """HBM write bandwidth on this GPU: 1 GiB set to zero by torch's fill
+    kernel and by the library's bulk-store fill (the store path of the row
+    dispatch), best of 5 CUDA-event timings each after one warm-up.  Returns
+    (the faster one's GB/s, {fill: GB/s})."""
     buf = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
-    buf.zero_()
-    best = None
-    for _ in range(5):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        buf.zero_()
-        b.record()
-        torch.cuda.synchronize()
-        ms = a.elapsed_time(b)
-        best = ms if best is None else min(best, ms)
+    fills = {"torch zero_": lambda: buf.zero_(), "bulk-store fill": lambda: api.fill_zero(buf)}
+    rates = {}
+    for name, fill in fills.items():
+        fill()
+        best = None
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fill()
+            b.record()
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+        rates[name] = (1 << 30) / (best / 1e3) / 1e9
     del buf
-    return (1 << 30) / (best / 1e3) / 1e9
+    return max(rates.values()), rates
 
 
 def load_peaks():
@@ -540,7 +562,7 @@ def main():
     clocks = sampler.stop()
     api.profile_enable(False)
     elapsed_ms = ev0.elapsed_time(ev1)
-    kernels = api.profile_collect()
+    kernels = fold_kernels(api.profile_collect())
     if layer.status() != 0:
         raise RuntimeError("device status set during the timed region")
     t_max = max_over_ranks(elapsed_ms, dist, "cuda") if world > 1 else elapsed_ms
@@ -548,7 +570,7 @@ def main():
 
     # ---- per-kernel summary and the dominant kernel's roofline
     peaks = load_peaks()
-    write_gbs = measure_write_gbs(torch)
+    write_gbs, write_rates = measure_write_gbs(torch, api)
     flops = gemm_flops(shape, int(layer.layout.mb_count))
     gbytes = gemm_bytes(shape, int(layer.layout.mb_count), mx=WORKLOAD == "mxfp8",
                         wgrad_elem_bytes=2 if args.bf16_wgrad else 4)
@@ -589,7 +611,8 @@ def main():
                 "traffic": NCU_TRAFFIC_FINE.get(dom) if WORKLOAD == "fine" else None,
                 "traffic_source": "profiles/grouped_gemms_fine.txt",
                 "peak_source": f"hbm_gbs of {peaks['source']}; write bandwidth measured here "
-                               "(1 GiB zero fill)",
+                               "(1 GiB zero fill: the faster of torch's and the bulk-store one)",
+                "write_bw_fills_gbs": write_rates,
                 "algorithmic_per_launch": tb,
                 "tensor": {"achieved_tflops": flops[dom] / avg_s / 1e12,
                            "peak_tflops": peaks["bf16_sustained"],
@@ -632,6 +655,7 @@ def main():
                 roof_us = mover_roofline_us(b, wbytes[n], peaks["hbm"], write_gbs)
                 movers_perf[n]["frac_roofline"] = roof_us / avg_us
     movers_perf["write_bw_gbs"] = write_gbs
+    movers_perf["write_bw_fills_gbs"] = write_rates
 
     # ---- end to end through the C ABI: every step's x, dy uploaded from
     # pinned host memory and its y, dx read back to pinned host memory.  The

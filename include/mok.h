@@ -282,6 +282,14 @@ mok_status mok_gemm_mxfp8(int64_t M, int64_t N, int64_t K, const uint8_t* A, con
  * mok_get_device_status. */
 mok_status mok_selftest_bounded_wait(void* workspace, size_t ws_bytes, void* stream);
 
+/* Diagnostic: sets `bytes` bytes at device address `dst` to zero with bulk
+ * asynchronous stores (cp.async.bulk) from a zeroed shared-memory chunk, the
+ * store path the row-dispatch kernel writes with; timed alone it measures the
+ * HBM write bandwidth that path reaches.  dst 16-byte aligned and bytes a
+ * multiple of 16, else MOK_ERR_INVALID_ARG; bytes = 0 enqueues nothing.
+ * Asynchronous on `stream`; the caller owns `dst`. */
+mok_status mok_fill_zero(void* dst, size_t bytes, void* stream);
+
 /* Waits for `stream`, then reads the device status word at the start of
  * `buf` (the `saved` buffer of forward/backward, or the workspace of the
  * other entry points) into *code (a mok_status; MOK_OK = no device error). */

@@ -55,6 +55,7 @@ _SIGS = {
     "mok_gemm_mxfp8": (c_int32, [c_int64, c_int64, c_int64, c_void_p, c_void_p, c_void_p,
                                  c_void_p, c_void_p, c_int32, c_void_p, c_size_t, c_void_p]),
     "mok_selftest_bounded_wait": (c_int32, [c_void_p, c_size_t, c_void_p]),
+    "mok_fill_zero": (c_int32, [c_void_p, c_size_t, c_void_p]),
     "mok_get_device_status": (c_int32, [c_void_p, c_void_p, ctypes.POINTER(c_int32)]),
     "mok_status_string": (ctypes.c_char_p, [c_int32]),
     "mok_last_launch_count": (c_int32, []),

@@ -136,6 +136,14 @@ def device_status(buf, stream=None) -> int:
     return code.value
 
 
+def fill_zero(buf, stream=None):
+    """Zeroes the contiguous device tensor `buf` with the library's bulk-store
+    fill (its byte size a multiple of 16, its address 16-byte aligned)."""
+    nbytes = buf.numel() * buf.element_size()
+    _lib.check(_lib.load().mok_fill_zero(_ptr(buf), nbytes, _stream(stream)), "mok_fill_zero")
+    return buf
+
+
 def last_launch_count() -> int:
     return int(_lib.load().mok_last_launch_count())
 

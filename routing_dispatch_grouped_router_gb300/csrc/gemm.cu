@@ -1762,6 +1762,37 @@ cudaError_t gemm_wgrad_gate_up(const Dims& D, const void* dGU_hi, const void* dG
                dw_gate_up, accumulate, status, st, sg);
 }
 
+cudaError_t gemm_router_wgrad(const Dims& D, const void* x, const void* dl_hi, const void* dl_lo,
+                              const int32_t* rw_off, float* part, int* status, cudaStream_t st) {
+  // partial s [E_pad, d] = (dl_hi + dl_lo)^T x over tokens rw_off[s] .. rw_off[s+1]
+  // (the K-grouped schedule with one group per token chunk); tokens >= T of the
+  // last chunk are zero-filled by the TMA on both operands
+  if (D.T == 0) return cudaSuccess;
+  const RwSplit rw = router_wgrad_split(D);
+  const int64_t M = router_e_pad(D);
+  const int bn = router_wgrad_bn(D);
+  CUtensorMap ta, tb, tc, tl;
+  if (!make_map(&ta, dl_hi, M, D.T, M, 64)) return cudaErrorInvalidValue;
+  if (!make_map(&tl, dl_lo, M, D.T, M, 64)) return cudaErrorInvalidValue;
+  if (!make_map(&tb, x, D.d, D.T, D.d, 64)) return cudaErrorInvalidValue;
+  if (!make_out_map(&tc, part, D.d, rw.ks * M)) return cudaErrorInvalidValue;
+  GemmArgs a = blank_args(status);
+  a.E = rw.ks;
+  a.m_tiles = (int)(M / 128);
+  a.n_tiles = (int)(D.d / bn);
+  a.m_rows = (int)M;
+  a.poff = rw_off;
+  a.out = part;
+  a.ldo = D.d;
+  a.out_group_stride = M * D.d;
+  const int mt = a.E * a.m_tiles * a.n_tiles;
+  if (bn == 256)
+    return launch<256, true, true, SCHED_KGROUP, EPI_F32, SPLIT_A>("router_wgrad", ta, tb, tc, a,
+                                                                   mt, st, &tl);
+  return launch<128, true, true, SCHED_KGROUP, EPI_F32, SPLIT_A>("router_wgrad", ta, tb, tc, a,
+                                                                 mt, st, &tl);
+}
+
 cudaError_t launch_router_logits(const Dims& D, const void* x, const void* w_router,
                                  float* logits, int* status, cudaStream_t st) {
   // logits [T, E] fp32 = x [T,d] * W_r[E,d]^T; rows >= T and columns >= E

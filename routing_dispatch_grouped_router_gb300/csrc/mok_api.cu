@@ -239,8 +239,14 @@ void bwd_layout(const Dims& D, BwdWs* W) {
   W->p_lo = b.take(ns * rows * D.I * 2);
   W->dp_part = b.take(rows * D.np * 4);
   W->dx_perm = b.take(rows * D.d * 4);  // fp32
-  W->dl_row = b.take(rows * 4);
-  W->dl_tok = b.take(static_cast<size_t>(D.T) * D.k * 4);
+  // router-weight gradient: dense dl as a bf16 hi/lo pair [T, E padded to
+  // 128], its K-chunk offsets, and the chunks' fp32 partial products
+  const size_t epad = static_cast<size_t>(router_e_pad(D));
+  const RwSplit rw = router_wgrad_split(D);
+  W->dl_hi = b.take(static_cast<size_t>(D.T) * epad * 2);
+  W->dl_lo = b.take(static_cast<size_t>(D.T) * epad * 2);
+  W->rw_off = b.take(static_cast<size_t>(rw.ks + 1) * 4);
+  W->rw_part = b.take(static_cast<size_t>(rw.ks) * epad * D.d * 4);
   const size_t wgu = static_cast<size_t>(D.E) * 2 * D.I * D.d * 2;
   const size_t wd = static_cast<size_t>(D.E) * D.d * D.I * 2;
   W->dyq_row = D.mx ? b.take(rows * D.d * 2) : 0;  // MXFP8 copies
@@ -463,8 +469,10 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
   void* p_lo = at<char>(workspace, B.p_lo);
   float* dp_part = at<float>(workspace, B.dp_part);
   float* dx_perm = at<float>(workspace, B.dx_perm);
-  float* dl_row = at<float>(workspace, B.dl_row);
-  float* dl_tok = at<float>(workspace, B.dl_tok);
+  void* dl_hi = at<char>(workspace, B.dl_hi);
+  void* dl_lo = at<char>(workspace, B.dl_lo);
+  int32_t* rw_off = at<int32_t>(workspace, B.rw_off);
+  float* rw_part = at<float>(workspace, B.rw_part);
   uint8_t* dgu_c = D.mx ? at<uint8_t>(workspace, B.dgu_codes) : nullptr;
   uint8_t* dgu_s = D.mx ? at<uint8_t>(workspace, B.dgu_scales) : nullptr;
   uint8_t* wgu_t_c = D.mx ? at<uint8_t>(workspace, B.wgu_t_codes) : nullptr;
@@ -581,8 +589,9 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
                                   status, st));
     // reverse-dispatch + router backward
     MOK_CUDA(launch_reverse_dispatch(D, dx_perm, ppos, topk_idx, topk_w, dp_part, w_router, dxi,
-                                     dl_row, dl_tok, st));
-    MOK_CUDA(launch_router_wgrad(D, xi, ptok, dl_row, poff, counts, dw_router, !first, st));
+                                     dl_hi, dl_lo, rw_off, st));
+    MOK_CUDA(gemm_router_wgrad(D, xi, dl_hi, dl_lo, rw_off, rw_part, status, st));
+    MOK_CUDA(launch_router_wgrad_reduce(D, rw_part, dw_router, !first, st));
   }
   if (defer) {
     // the expert weight gradients over all micro-batches: K runs through
@@ -723,6 +732,15 @@ mok_status mok_selftest_bounded_wait(void* workspace, size_t ws_bytes, void* str
   int* status = static_cast<int*>(workspace);
   MOK_CUDA(cudaMemsetAsync(status, 0, sizeof(int), st));
   MOK_CUDA(launch_bounded_wait_selftest(status, st));
+  return MOK_OK;
+}
+
+mok_status mok_fill_zero(void* dst, size_t bytes, void* stream) {
+  if (bytes == 0) return MOK_OK;
+  if (!dst || !aligned16(dst) || bytes % 16) return MOK_ERR_INVALID_ARG;
+  mok_status s = mok_check_device();
+  if (s != MOK_OK) return s;
+  MOK_CUDA(launch_fill_zero(dst, bytes, static_cast<cudaStream_t>(stream)));
   return MOK_OK;
 }
 

@@ -62,7 +62,8 @@ struct FwdWs {
   size_t total;
 };
 struct BwdWs {
-  size_t dy_perm, dgu_hi, dgu_lo, p_hi, p_lo, dp_part, dx_perm, dl_row, dl_tok, dyq_row, dyq_col,
+  size_t dy_perm, dgu_hi, dgu_lo, p_hi, p_lo, dp_part, dx_perm, dl_hi, dl_lo, rw_off, rw_part,
+      dyq_row, dyq_col,
       xq_col, dgu_codes, dgu_scales, wd_col, wgu_t_codes, wgu_t_scales, gu, xq_codes, xq_scales,
       wgu_codes, wgu_scales, x_def, total;
 };
@@ -117,18 +118,43 @@ cudaError_t launch_combine(const Dims& D, const float* O, const int32_t* ppos, c
                            void* y, cudaStream_t st);
 
 // dl (router logit grad) from dp partials; dx_t = sum_s dX[ppos] + dl W_r[e]
-// (dX fp32; dx fp32 or bf16).
+// (dX fp32; dx fp32 or bf16).  Also writes dl as the dense operand of the
+// router-weight gradient, dl[t, e] for e < router_e_pad(D) (zero where e is
+// not among t's experts) as a bf16 hi/lo pair, and that GEMM's K-chunk
+// offsets (router_wgrad_split(D).ks + 1 of them, one chunk apart).
 cudaError_t launch_reverse_dispatch(const Dims& D, const float* dX_perm, const int32_t* ppos,
                                     const int32_t* topk_idx, const float* topk_w,
                                     const float* dp_part, const void* w_router, void* dx,
-                                    float* dl_row, float* dl_tok, cudaStream_t st);
+                                    void* dl_hi, void* dl_lo, int32_t* rw_off, cudaStream_t st);
 
-// dW_r[e] (+)= sum over rows r of e of dl_row[r] * x[ptok[r]] (fp32 or bf16
-// out; accumulation fp32 only).
-cudaError_t launch_router_wgrad(const Dims& D, const void* x, const int32_t* ptok,
-                                const float* dl_row, const int32_t* padded_offsets,
-                                const int32_t* counts, void* dw_router, bool accumulate,
-                                cudaStream_t st);
+// The router-weight gradient dW_r = dl^T x runs as a tensor-core GEMM over
+// token chunks: M = the experts padded to 128 (rows of dl^T), N = d, K = the
+// tokens, split into ks chunks of kb 64-row blocks; chunk s writes its fp32
+// partial product to part + s * router_e_pad(D) * d, and a second kernel adds
+// the ks partials in order.  ks targets 152 CTAs (the SM count of a GB300)
+// whatever the device, so that the sums do not depend on it.
+inline int64_t router_e_pad(const Dims& D) { return (D.E + 127) / 128 * 128; }
+inline int router_wgrad_bn(const Dims& D) { return D.d % 256 == 0 ? 256 : 128; }
+struct RwSplit {
+  int ks;  // K chunks (>= 1)
+  int kb;  // 64-token blocks per chunk
+};
+inline RwSplit router_wgrad_split(const Dims& D) {
+  const int64_t tiles = router_e_pad(D) / 128 * (D.d / router_wgrad_bn(D));
+  const int64_t nkb = (D.T + 63) / 64 > 0 ? (D.T + 63) / 64 : 1;
+  int64_t ks = 152 / tiles;
+  if (ks < 1) ks = 1;
+  if (ks > nkb) ks = nkb;
+  const int64_t kb = (nkb + ks - 1) / ks;
+  ks = (nkb + kb - 1) / kb;
+  return {static_cast<int>(ks), static_cast<int>(kb)};
+}
+cudaError_t gemm_router_wgrad(const Dims& D, const void* x, const void* dl_hi, const void* dl_lo,
+                              const int32_t* rw_off, float* part, int* status, cudaStream_t st);
+// dW_r (+)= sum over s < ks of the partials, in order (fp32 or bf16 out;
+// accumulation fp32 only)
+cudaError_t launch_router_wgrad_reduce(const Dims& D, const float* part, void* dw_router,
+                                       bool accumulate, cudaStream_t st);
 
 // Grouped GEMMs on tcgen05 (see gemm.cu).
 cudaError_t gemm_fwd_gate_up(const Dims& D, const void* X_perm, const void* w_gate_up,
@@ -212,6 +238,8 @@ cudaError_t launch_mx_cols(const void* in, void* out, long long rows, long long 
 
 // One CTA whose mbarrier wait can never complete: exercises the bounded wait.
 cudaError_t launch_bounded_wait_selftest(int* status, cudaStream_t st);
+// zeroes `bytes` (a multiple of 16) at 16-byte aligned dst with bulk stores
+cudaError_t launch_fill_zero(void* dst, size_t bytes, cudaStream_t st);
 
 // launches counter (host side)
 void count_launch(int n = 1);

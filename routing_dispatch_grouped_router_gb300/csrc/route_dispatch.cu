@@ -577,19 +577,43 @@ __global__ void reverse_dispatch_kernel(const float4* __restrict__ dXp,
                                         const float* __restrict__ topk_w,
                                         const float* __restrict__ dp_part, int np,
                                         const uint2* __restrict__ Wr, int k, int dq, void* dx,
-                                        float* __restrict__ dl_row, float* __restrict__ dl_tok) {
+                                        __nv_bfloat16* __restrict__ dl_hi,
+                                        __nv_bfloat16* __restrict__ dl_lo, int e_pad,
+                                        int32_t* __restrict__ rw_off, int rw_chunks,
+                                        int rw_chunk_rows) {
   grid_dep_launch();  // a GEMM after this kernel may start its prologue
   __shared__ int s_row[kMaxTopK];
   __shared__ int s_e[kMaxTopK];
   __shared__ float s_dl[kMaxTopK];
   const long long t = blockIdx.x;
+  const int s = threadIdx.x;  // slot, for the first k threads
+  int row = -1;
+  if (s < k) {
+    row = ppos[t * k + s];
+    s_row[s] = row;
+    s_e[s] = topk_idx[t * k + s];
+  }
+  __syncthreads();
+  // the k rows' loads of one column all in flight, then the sum in slot order
+  float4 xr[kMaxTopK];
+  uint2 wr[kMaxTopK];
+  auto load_rows = [&](int c) {
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < k && s_row[j] >= 0) {
+        xr[j] = ld_nc_f4(dXp + static_cast<long long>(s_row[j]) * dq + c);
+        asm volatile("ld.global.nc.v2.b32 {%0, %1}, [%2];"
+                     : "=r"(wr[j].x), "=r"(wr[j].y)
+                     : "l"(Wr + static_cast<long long>(s_e[j]) * dq + c));
+      }
+    }
+  };
+  // the first column's loads go out before the routing-weight gradient is known
+  const int c0 = threadIdx.x;
+  if (c0 < dq) load_rows(c0);
   if (threadIdx.x < 32) {
-    const int s = threadIdx.x;
-    int row = -1, e = 0;
     float p = 0.f, dp = 0.f;
     if (s < k) {
-      row = ppos[t * k + s];
-      e = topk_idx[t * k + s];
       p = topk_w[t * k + s];
       if (row >= 0) {
         const float* q = dp_part + static_cast<long long>(row) * np;
@@ -597,42 +621,35 @@ __global__ void reverse_dispatch_kernel(const float4* __restrict__ dXp,
         for (int j = 0; j < np; ++j) dp += q[j];
       }
     }
-    // c = sum_i p_i dp_i, summed in slot order by every lane
-    float c = 0.f;
+    // sum_i p_i dp_i, summed in slot order by every lane
+    float pdp = 0.f;
     for (int i = 0; i < kMaxTopK; ++i) {
       const float pi = __shfl_sync(0xffffffffu, p, i);
       const float di = __shfl_sync(0xffffffffu, dp, i);
-      if (i < k) c = fmaf(pi, di, c);
+      if (i < k) pdp = fmaf(pi, di, pdp);
     }
-    if (s < k) {
-      const float dl = (row >= 0) ? p * (dp - c) : 0.f;
-      s_row[s] = row;
-      s_e[s] = e;
-      s_dl[s] = dl;
-      dl_tok[t * k + s] = dl;
-      if (row >= 0) dl_row[row] = dl;
-    }
+    if (s < k) s_dl[s] = (row >= 0) ? p * (dp - pdp) : 0.f;
   }
+  if (blockIdx.x == 0)
+    for (int j = threadIdx.x; j <= rw_chunks; j += blockDim.x) rw_off[j] = j * rw_chunk_rows;
   __syncthreads();
-  for (int c = threadIdx.x; c < dq; c += blockDim.x) {
-    // the k rows' loads all in flight, then the sum in slot order
-    float4 xr[kMaxTopK];
-    uint2 wr[kMaxTopK];
-#pragma unroll
-    for (int s = 0; s < kMaxTopK; ++s) {
-      if (s < k && s_row[s] >= 0) {
-        xr[s] = ld_nc_f4(dXp + static_cast<long long>(s_row[s]) * dq + c);
-        asm volatile("ld.global.nc.v2.b32 {%0, %1}, [%2];"
-                     : "=r"(wr[s].x), "=r"(wr[s].y)
-                     : "l"(Wr + static_cast<long long>(s_e[s]) * dq + c));
-      }
-    }
+  // dense dl row of the router-weight gradient, as a bf16 hi/lo pair
+  for (int j = threadIdx.x; j < e_pad; j += blockDim.x) {
+    float v = 0.f;
+    for (int i = 0; i < k; ++i)
+      if (s_e[i] == j) v = s_dl[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    dl_hi[t * e_pad + j] = hi;
+    dl_lo[t * e_pad + j] = __float2bfloat16_rn(v - __bfloat162float(hi));
+  }
+  for (int c = c0; c < dq; c += blockDim.x) {
+    if (c != c0) load_rows(c);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int s = 0; s < kMaxTopK; ++s) {
-      if (s < k && s_row[s] >= 0) {
-        add4(acc, xr[s]);
-        axpy4(acc, s_dl[s], bf16x4_to_f4(wr[s]));
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < k && s_row[j] >= 0) {
+        add4(acc, xr[j]);
+        axpy4(acc, s_dl[j], bf16x4_to_f4(wr[j]));
       }
     }
     store4<BF16_OUT>(dx, t, dq, c, acc);
@@ -642,117 +659,123 @@ __global__ void reverse_dispatch_kernel(const float4* __restrict__ dXp,
 cudaError_t launch_reverse_dispatch(const Dims& D, const float* dX_perm, const int32_t* ppos,
                                     const int32_t* topk_idx, const float* topk_w,
                                     const float* dp_part, const void* w_router, void* dx,
-                                    float* dl_row, float* dl_tok, cudaStream_t st) {
+                                    void* dl_hi, void* dl_lo, int32_t* rw_off, cudaStream_t st) {
   if (D.T == 0) return cudaSuccess;
   const int dq = static_cast<int>(D.d / 4);
   const int th = row_threads(dq);
+  const RwSplit rw = router_wgrad_split(D);
+  const int e_pad = static_cast<int>(router_e_pad(D));
+  auto* hi = static_cast<__nv_bfloat16*>(dl_hi);
+  auto* lo = static_cast<__nv_bfloat16*>(dl_lo);
   ProfScope prof("reverse_dispatch", st);
   if (D.act_bf16)
     reverse_dispatch_kernel<true><<<static_cast<unsigned>(D.T), th, 0, st>>>(
         reinterpret_cast<const float4*>(dX_perm), ppos, topk_idx, topk_w, dp_part, D.np,
-        static_cast<const uint2*>(w_router), D.k, dq, dx, dl_row, dl_tok);
+        static_cast<const uint2*>(w_router), D.k, dq, dx, hi, lo, e_pad, rw_off, rw.ks,
+        rw.kb * 64);
   else
     reverse_dispatch_kernel<false><<<static_cast<unsigned>(D.T), th, 0, st>>>(
         reinterpret_cast<const float4*>(dX_perm), ppos, topk_idx, topk_w, dp_part, D.np,
-        static_cast<const uint2*>(w_router), D.k, dq, dx, dl_row, dl_tok);
+        static_cast<const uint2*>(w_router), D.k, dq, dx, hi, lo, e_pad, rw_off, rw.ks,
+        rw.kb * 64);
   count_launch();
   return cudaGetLastError();
 }
 
 // ------------------------------------------------------ router weight grad --
 
-// dW_r[e, :] = sum over the real rows r of expert e of dl_row[r] * x[ptok[r], :]
-// (x[ptok[r]] is dispatched row r; reading it from x, which the cache holds,
-// instead of the R dispatched rows gives the same values in the same order).
-// CTA (e, 64-column block): 32 row lanes x 8 column threads (8 columns each);
-// row lane i takes rows i, i+32, ...; the 32 partials are then added in lane
-// order.  Fixed order throughout.
-constexpr int kRwRowLanes = 32;
-
-__device__ __forceinline__ void axpy8(float (&acc)[8], float w, uint4 v) {
-  acc[0] = fmaf(w, bf16lo(v.x), acc[0]); acc[1] = fmaf(w, bf16hi(v.x), acc[1]);
-  acc[2] = fmaf(w, bf16lo(v.y), acc[2]); acc[3] = fmaf(w, bf16hi(v.y), acc[3]);
-  acc[4] = fmaf(w, bf16lo(v.z), acc[4]); acc[5] = fmaf(w, bf16hi(v.z), acc[5]);
-  acc[6] = fmaf(w, bf16lo(v.w), acc[6]); acc[7] = fmaf(w, bf16hi(v.w), acc[7]);
-}
-
+// dW_r = the sum of the ks partial products of the router-weight gradient
+// GEMM, added in chunk order (then + the previous dW_r with accumulate); ks = 0
+// (no tokens) gives zeros.  The
+// partial of chunk s holds rows e < E of an [E padded to 128, d] block at
+// part + s * split4 float4s; thread i takes float4 i of dW_r [E, d].
 template <bool BF16_OUT>
-__global__ void router_wgrad_kernel(const uint4* __restrict__ X, const int32_t* __restrict__ ptok,
-                                    const float* __restrict__ dl_row,
-                                    const int32_t* __restrict__ poff,
-                                    const int32_t* __restrict__ counts, int dv, void* dw,
-                                    int accumulate) {
+__global__ void router_wgrad_reduce_kernel(const float4* __restrict__ part, int ks,
+                                           long long split4, long long n4, void* dw,
+                                           int accumulate) {
   grid_dep_launch();  // a GEMM after this kernel may start its prologue
-  __shared__ float part[kRwRowLanes][8][8];
-  const int e = blockIdx.x;
-  const int cv = blockIdx.y * 8 + (threadIdx.x & 7);  // column vector index
-  const int lane_r = threadIdx.x >> 3;
-  const int r0 = poff[e], n = counts[e];
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  if (cv < dv) {
-    // four rows' loads in flight at a time; the sum still runs row by row
-    int i = lane_r;
-    for (; i + 3 * kRwRowLanes < n; i += 4 * kRwRowLanes) {
-      uint4 v[4];
-      float w[4];
-      int t[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) t[u] = ptok[r0 + i + u * kRwRowLanes];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const long long r = r0 + i + u * kRwRowLanes;
-        v[u] = ld_global_nc_v4(X + static_cast<long long>(t[u]) * dv + cv);
-        w[u] = dl_row[r];
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) axpy8(acc, w[u], v[u]);
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    float4 acc = ks > 0 ? ld_nc_f4(part + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 1; s < ks; ++s) {
+      const float4 v = ld_nc_f4(part + s * split4 + i);
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
-    for (; i < n; i += kRwRowLanes) {
-      const long long r = r0 + i;
-      axpy8(acc, dl_row[r], ld_global_nc_v4(X + static_cast<long long>(ptok[r]) * dv + cv));
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) part[lane_r][threadIdx.x & 7][j] = acc[j];
-  __syncthreads();
-  if (threadIdx.x < 8 && cv < dv) {
-    float tot[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int l = 0; l < kRwRowLanes; ++l)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) tot[j] += part[l][threadIdx.x][j];
-    const long long o = static_cast<long long>(e) * dv + cv;
     if (BF16_OUT) {
-      reinterpret_cast<uint4*>(dw)[o] =
-          make_uint4(pack_bf16x2(tot[0], tot[1]), pack_bf16x2(tot[2], tot[3]),
-                     pack_bf16x2(tot[4], tot[5]), pack_bf16x2(tot[6], tot[7]));
+      reinterpret_cast<uint2*>(dw)[i] =
+          make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
     } else {
-      float4* q = reinterpret_cast<float4*>(dw) + 2 * o;
+      float4* q = reinterpret_cast<float4*>(dw) + i;
       if (accumulate) {
-        const float4 a0 = q[0], a1 = q[1];
-        tot[0] += a0.x; tot[1] += a0.y; tot[2] += a0.z; tot[3] += a0.w;
-        tot[4] += a1.x; tot[5] += a1.y; tot[6] += a1.z; tot[7] += a1.w;
+        const float4 a = *q;
+        acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
       }
-      q[0] = make_float4(tot[0], tot[1], tot[2], tot[3]);
-      q[1] = make_float4(tot[4], tot[5], tot[6], tot[7]);
+      *q = acc;
     }
   }
 }
 
-cudaError_t launch_router_wgrad(const Dims& D, const void* x, const int32_t* ptok,
-                                const float* dl_row, const int32_t* padded_offsets,
-                                const int32_t* counts, void* dw_router, bool accumulate,
-                                cudaStream_t st) {
+cudaError_t launch_router_wgrad_reduce(const Dims& D, const float* part, void* dw_router,
+                                       bool accumulate, cudaStream_t st) {
   if (accumulate && D.wgrad_bf16) return cudaErrorInvalidValue;
-  const int dv = static_cast<int>(D.d / 8);
-  dim3 grid(static_cast<unsigned>(D.E), static_cast<unsigned>((dv + 7) / 8));
-  ProfScope prof("router_wgrad", st);
+  // no tokens: no partials, dW_r = 0 (or unchanged with accumulate)
+  const int ks = D.T == 0 ? 0 : router_wgrad_split(D).ks;
+  const long long n4 = D.E * D.d / 4;
+  const long long split4 = router_e_pad(D) * D.d / 4;
+  long long blocks = (n4 + 255) / 256;
+  const long long cap = static_cast<long long>(num_sms_current_device()) * 8;
+  if (blocks > cap) blocks = cap;
+  const auto* p4 = reinterpret_cast<const float4*>(part);
+  ProfScope prof("router_wgrad_reduce", st);
   if (D.wgrad_bf16)
-    router_wgrad_kernel<true><<<grid, kRwRowLanes * 8, 0, st>>>(
-        static_cast<const uint4*>(x), ptok, dl_row, padded_offsets, counts, dv, dw_router, 0);
+    router_wgrad_reduce_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+        p4, ks, split4, n4, dw_router, 0);
   else
-    router_wgrad_kernel<false><<<grid, kRwRowLanes * 8, 0, st>>>(
-        static_cast<const uint4*>(x), ptok, dl_row, padded_offsets, counts, dv, dw_router,
-        accumulate ? 1 : 0);
+    router_wgrad_reduce_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+        p4, ks, split4, n4, dw_router, accumulate ? 1 : 0);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// -------------------------------------------------------------- zero fill --
+
+constexpr int kFillChunk = 16384;  // bytes per bulk store
+
+// Zeroes [dst, dst + bytes) with bulk asynchronous stores from a zeroed
+// shared-memory chunk, the store path of dispatch_rows_kernel: chunk c is
+// written by CTA c % gridDim.x, the ragged tail (a multiple of 16 bytes) by
+// the last CTA.  At most 9 stores per CTA are in flight.
+__global__ void __launch_bounds__(32) fill_zero_kernel(uint8_t* __restrict__ dst,
+                                                       unsigned long long bytes) {
+  extern __shared__ __align__(128) uint8_t s_zero[];
+  grid_dep_launch();
+  for (int i = threadIdx.x; i < kFillChunk / 16; i += 32)
+    reinterpret_cast<uint4*>(s_zero)[i] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (threadIdx.x != 0) return;
+  const unsigned long long n = bytes / kFillChunk;
+  for (unsigned long long c = blockIdx.x; c < n; c += gridDim.x) {
+    bulk_store(dst + c * kFillChunk, s_zero, kFillChunk);
+    bulk_commit();
+    bulk_wait_read<8>();
+  }
+  const uint32_t rem = static_cast<uint32_t>(bytes - n * kFillChunk);
+  if (rem != 0 && blockIdx.x == gridDim.x - 1) {
+    bulk_store(dst + n * kFillChunk, s_zero, rem);
+    bulk_commit();
+  }
+  bulk_wait_all<0>();
+}
+
+cudaError_t launch_fill_zero(void* dst, size_t bytes, cudaStream_t st) {
+  if (bytes == 0) return cudaSuccess;
+  const unsigned long long chunks = bytes / kFillChunk;
+  const unsigned long long cap = static_cast<unsigned long long>(num_sms_current_device()) * 8;
+  const unsigned grid = static_cast<unsigned>(chunks == 0 ? 1 : (chunks < cap ? chunks : cap));
+  ProfScope prof("fill_zero", st);
+  fill_zero_kernel<<<grid, 32, kFillChunk, st>>>(static_cast<uint8_t*>(dst),
+                                                  static_cast<unsigned long long>(bytes));
   count_launch();
   return cudaGetLastError();
 }

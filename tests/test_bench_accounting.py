@@ -54,6 +54,11 @@ def test_workload_options():
     assert bench.layer_options(FakeApi) == {}
 
 
+def test_router_wgrad_reduce_folds_into_the_router_gradient():
+    k = {"router_wgrad": (4, 1.0), "router_wgrad_reduce": (4, 0.25), "combine": (4, 0.5)}
+    assert bench.fold_kernels(k) == {"router_wgrad": (4, 1.25), "combine": (4, 0.5)}
+
+
 def test_mx_quantiser_bytes_average_over_launches():
     s = gen.workload_shape("mxfp8")
     nmb, rows_max = 8, 32640

@@ -225,6 +225,29 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     _gpu.full_parity(shape, inp, _gpu.run_gpu(shape, inp))
 
 
+@pytest.mark.parametrize("offset,nbytes", [(0, 0), (16, 48), (0, 16384), (32, 3 * 16384 + 4080),
+                                           (16, (64 << 20) + 16)])
+def test_fill_zero_writes_exactly_its_range(offset, nbytes):
+    """The bulk-store fill zeroes whole chunks, the ragged tail and nothing
+    outside [dst, dst + bytes)."""
+    buf = torch.full((offset + nbytes + 64,), 0xA5, dtype=torch.uint8, device="cuda")
+    api.fill_zero(buf[offset:offset + nbytes])
+    torch.cuda.synchronize()
+    h = buf.cpu().numpy()
+    assert not h[offset:offset + nbytes].any()
+    assert (h[:offset] == 0xA5).all() and (h[offset + nbytes:] == 0xA5).all()
+
+
+def test_fill_zero_rejects_unaligned_arguments():
+    from routing_dispatch_grouped_router_gb300 import _lib
+    import ctypes
+    lib = _lib.load()
+    buf = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert lib.mok_fill_zero(ctypes.c_void_p(buf.data_ptr() + 8), 64, st) != 0
+    assert lib.mok_fill_zero(ctypes.c_void_p(buf.data_ptr()), 40, st) != 0
+
+
 # ------------------------------------------------------------ stage APIs ---
 
 def test_route_stage_matches_oracle():
