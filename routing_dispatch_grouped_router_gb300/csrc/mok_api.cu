@@ -519,7 +519,6 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
     char* dxi = static_cast<char*>(dx) + static_cast<size_t>(i) * D.T * D.d * dx_esz;
     const int32_t* topk_idx = at<int32_t>(saved, L.topk_idx + blk);
     const float* topk_w = at<float>(saved, L.topk_w + blk);
-    const int32_t* counts = at<int32_t>(saved, L.counts + blk);
     const int32_t* poff = at<int32_t>(saved, L.padded_offsets + blk);
     const int32_t* mtp = at<int32_t>(saved, mt_off + blk);
     const int32_t* ppos = at<int32_t>(saved, L.padded_pos + blk);
