@@ -152,6 +152,15 @@ def test_null_pointers_rejected_before_any_device_call(lib):
     assert code == 2
 
 
+def test_fill_zero_checks_arguments_before_any_device_call(lib):
+    """The write-bandwidth probe wants a 16-byte aligned address and a size
+    that is a multiple of 16; a zero size enqueues nothing."""
+    assert lib.mok_fill_zero(None, 0, None) == 0
+    assert lib.mok_fill_zero(None, 64, None) == 1
+    assert lib.mok_fill_zero(ctypes.c_void_p(24), 64, None) == 1
+    assert lib.mok_fill_zero(ctypes.c_void_p(32), 40, None) == 1
+
+
 def test_status_strings(lib):
     for c in (0, 1, 2, 3, 4, 5, 16, 17, 18):
         assert lib.mok_status_string(c).decode()
