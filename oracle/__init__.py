@@ -5,7 +5,8 @@ baseline leg of ``bench.py`` are the only users.  The CUDA path never imports,
 links or calls anything here, and nothing here imports the CUDA package.
 """
 from .moe_ref import (  # noqa: F401
-    NEAR_TIE, widen, bf16_round, silu, silu_grad, router_logits, route_ref, dispatch_ref,
+    NEAR_TIE, widen, bf16_round, silu, silu_grad, router_logits, routing_weights, route_ref,
+    dispatch_ref,
     expert_ffn, moe_forward_ref, moe_backward_ref,
 )
 from .mx_ref import e4m3_round, mx_quantize, mx_fake  # noqa: F401

@@ -134,6 +134,19 @@ def router_logits(x, w_router, bias=None) -> np.ndarray:
     return l
 
 
+def routing_weights(logits, topk_idx) -> np.ndarray:
+    """Softmax over each token's chosen experts, in the given slot order:
+    p_s = exp(l_s - m) / sum_{j in S} exp(l_j - m), m = max over S (float64).
+    With a chosen set taken from elsewhere (the kernel's, where a near-tie
+    makes the set undecidable), this gives the weights the definition
+    assigns to that set."""
+    sel = np.take_along_axis(np.asarray(logits, dtype=np.float64),
+                             np.asarray(topk_idx, dtype=np.int64), axis=1)
+    m = sel.max(axis=1, keepdims=True)
+    ex = np.exp(sel - m)
+    return ex / ex.sum(axis=1, keepdims=True)
+
+
 def route_ref(x, w_router, bias, k: int):
     """Top-k routing.
 
@@ -155,10 +168,8 @@ def route_ref(x, w_router, bias, k: int):
     cols = np.broadcast_to(np.arange(E), (T, E))
     order = np.lexsort((cols, -l32), axis=-1)
     idx = order[:, :k].astype(np.int32)
+    w = routing_weights(logits, idx)
     sel = np.take_along_axis(logits, idx.astype(np.int64), axis=1)
-    m = sel.max(axis=1, keepdims=True)
-    ex = np.exp(sel - m)
-    w = ex / ex.sum(axis=1, keepdims=True)
     ranked = np.take_along_axis(logits, order, axis=1)
     if k < E:
         flagged = (ranked[:, k - 1] - ranked[:, k]) < NEAR_TIE
