@@ -4,10 +4,12 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mok|reference]
 
 A step is one forward + backward of the layer (router, dispatch, grouped
-SwiGLU GEMMs, combine, and the mirrored backward) over one batch of the
-fine-grained workload: T=4096 tokens, d=2048, E=64 experts, I=1024, top-8,
-bf16, seeded synthetic inputs.  The weights (0.8 GB) and activations read per
-step are larger than the 129 MB L2, so no flush is needed between steps.
+SwiGLU GEMMs, combine, and the mirrored backward) over one batch of the large
+fine-grained workload by default: T=8192 tokens, d=7168, E=384 experts,
+I=2048, top-8, bf16, seeded synthetic inputs (`--workload` selects the fine,
+imbalanced, MXFP8 or tiny one).  The weights (33.8 GB) and activations read
+per step are far larger than the 129 MB L2, so no flush is needed between
+steps.
 
 Printed (rank 0, one JSON line): tokens/s over all ranks, per-kernel times
 from CUDA events recorded around each kernel on one in four steps of the timed
@@ -37,7 +39,7 @@ sys.path.insert(0, ROOT)
 from routing_dispatch_grouped_router_gb300 import inputs as gen  # noqa: E402
 
 METRIC = "MoE layer fwd+bwd tokens/s on 1 GB300; grouped-GEMM % of tensor-core peak"
-WORKLOAD = "fine"
+WORKLOAD = "large"
 PROFILE_EVERY = 4  # per-kernel events on one timed step in this many
 
 # Algorithmic work per launch of each kernel (R = T*k routed rows).
@@ -113,8 +115,9 @@ def gemm_bytes(shape: gen.Shape, micro_batches: int = 1, mx: bool = False,
 
 
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# grouped GEMMs on the fine workload, from the ncu capture summarised in
-# profiles/grouped_gemms_fine.txt (kernels as of the commit named there).
+# grouped GEMMs, per workload, from the ncu captures summarised in profiles/
+# (kernels as of the commit each file names); a kernel changed since its
+# capture has no entry.
 NCU_TRAFFIC_FINE = {
     "fwd_gate_up_swiglu": 688.822784e6 + 329.280e6,
     "fwd_down": 343.471360e6 + 254.084e6,
@@ -123,6 +126,13 @@ NCU_TRAFFIC_FINE = {
     "bwd_gate_up_dgrad": 690.012160e6 + 271.601e6,
     "bwd_gate_up_wgrad": 449.964800e6 + 1014.369e6,
 }
+NCU_TRAFFIC = {"fine": (NCU_TRAFFIC_FINE, "profiles/grouped_gemms_fine.txt")}
+
+
+def ncu_traffic(workload: str, kernel: str):
+    """(bytes per launch or None, source file) of a kernel's committed capture."""
+    table, src = NCU_TRAFFIC.get(workload, ({}, None))
+    return table.get(kernel), src
 
 
 def mx_quant_bytes(shape: gen.Shape, nmb: int, rows_max: int, kernels: dict, steps: int) -> dict:
@@ -164,9 +174,29 @@ def mover_bytes(shape: gen.Shape, micro_batches: int = 1) -> dict:
         "combine": R * 4 * d + T * 4 * d + R * 8,
         # read k fp32 dX rows and the dp partials, write fp32 dx (router rows from L2)
         "reverse_dispatch": R * 4 * d + T * 4 * d + R * (12 + 4 * np_),
-        # read each token row once, the k (expert, dl) pairs per token, write dW_r
-        "router_wgrad": T * d * 2 + R * 8 + E * d * 4,
+        # algorithmic: read each token row once, write dW_r (fp32); the executed
+        # form moves more (router_wgrad_executed_bytes)
+        "router_wgrad": T * d * 2 + E * d * 4,
     }
+
+
+def router_wgrad_executed_bytes(shape: gen.Shape, micro_batches: int = 1) -> float:
+    """Bytes the router-weight gradient moves as executed: the tensor-core
+    GEMM reads x once and the dense dl operand as a bf16 hi/lo pair [T, E
+    padded to 128] and writes one fp32 partial [E padded, d] per token chunk;
+    the reduce reads the partials and writes dW_r (fp32).  The chunk count
+    follows the library's split: ks = 152 // (M tiles x N tiles) chunks of
+    whole 64-token blocks, at least 1 and at most the block count."""
+    T, d, E = shape.T // micro_batches, shape.d, shape.E
+    e_pad = -(-E // 128) * 128
+    bn = 256 if d % 256 == 0 else 128
+    tiles = (e_pad // 128) * (d // bn)
+    nkb = max(1, -(-T // 64))
+    ks = min(max(1, 152 // tiles), nkb)
+    kb = -(-nkb // ks)
+    ks = -(-nkb // kb)
+    part = ks * e_pad * d * 4
+    return T * d * 2 + 2 * T * e_pad * 2 + 2 * part + E * d * 4
 
 
 # kernels whose time belongs to another one's step: the router-weight
@@ -311,7 +341,15 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
-def cpu_baseline(inp: dict, shape: gen.Shape, budget_s: float = 12.0, tokens_per_sample: int = 32):
+# tokens per oracle slice: a slice touches up to k x tokens experts, and the
+# oracle widens each touched expert's weights to float64 (0.35 GB per expert on
+# the large workload), so slices are sized to a few seconds each
+SLICE_TOKENS = {"tiny": 32, "fine": 32, "imbalanced": 2, "mxfp8": 2, "large": 1, "large_slice": 1}
+
+
+def cpu_baseline(inp: dict, shape: gen.Shape, budget_s: float = 12.0,
+                 tokens_per_sample: int | None = None):
+    tokens_per_sample = tokens_per_sample or SLICE_TOKENS.get(WORKLOAD, 1)
     t0 = time.perf_counter()
     done = 0
     n = 0
@@ -476,8 +514,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bf16-wgrad", action="store_true",
                     help="return the weight gradients in bf16 (default fp32)")
-    ap.add_argument("--workload", default="fine", choices=sorted(gen.WORKLOADS),
-                    help="fine (default, the measured configuration) or another configuration")
+    ap.add_argument("--workload", default="large", choices=sorted(gen.WORKLOADS),
+                    help="large (default: the configuration the targets are stated on), "
+                         "fine, imbalanced, mxfp8 or tiny")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     global WORKLOAD
@@ -608,8 +647,8 @@ def main():
                 "unit": "GB/s", "frac": ach / peaks["hbm"],
                 "frac_roofline": gemm_roofline_us(dom)[1] / (avg_s * 1e6),
                 "written_per_launch": tw, "write_bw_gbs": write_gbs,
-                "traffic": NCU_TRAFFIC_FINE.get(dom) if WORKLOAD == "fine" else None,
-                "traffic_source": "profiles/grouped_gemms_fine.txt",
+                "traffic": ncu_traffic(WORKLOAD, dom)[0],
+                "traffic_source": ncu_traffic(WORKLOAD, dom)[1],
                 "peak_source": f"hbm_gbs of {peaks['source']}; write bandwidth measured here "
                                "(1 GiB zero fill: the faster of torch's and the bulk-store one)",
                 "write_bw_fills_gbs": write_rates,
@@ -625,8 +664,8 @@ def main():
         peak = peaks["bf16_sustained"] * (2.0 if fp8 else 1.0)
         roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak,
                 "unit": "TFLOP/s", "frac": ach / peak,
-                "traffic": NCU_TRAFFIC_FINE.get(dom) if WORKLOAD == "fine" else None,
-                "traffic_source": "profiles/grouped_gemms_fine.txt",
+                "traffic": ncu_traffic(WORKLOAD, dom)[0],
+                "traffic_source": ncu_traffic(WORKLOAD, dom)[1],
                 "peak_source": f"bf16_tflops_sustained of {peaks['source']}"
                                + (" x 2 (nominal fp8/bf16 ratio)" if fp8 else ""),
                 "algorithmic_per_launch": flops[dom]}
@@ -649,6 +688,10 @@ def main():
             avg_us = kernels[n][1] / kernels[n][0] * 1e3
             gbs = b / (avg_us / 1e6) / 1e9
             movers_perf[n] = {"GB/s": gbs, "frac_hbm": gbs / peaks["hbm"]}
+            if n == "router_wgrad":
+                ex = router_wgrad_executed_bytes(shape, int(layer.layout.mb_count))
+                movers_perf[n].update({"bytes_algorithmic": b, "bytes_executed": ex,
+                                       "GB/s_executed": ex / (avg_us / 1e6) / 1e9})
             if n in wbytes:
                 # against the copy bandwidth and the measured write bandwidth
                 # together: write-heavy movers (the dispatch) are bound by the latter

@@ -31,6 +31,10 @@ WORKLOADS = {
     "large":      dict(T=8192,  d=7168, E=384, I=2048, k=8),
     "imbalanced": dict(T=16384, d=4096, E=128, I=1536, k=8, zipf_s=1.1),
     "mxfp8":      dict(T=16384, d=4096, E=128, I=1536, k=8, mb_tokens=2048, ring_slots=2),
+    # the large workload's widths and rows per expert (T*k/E = 170.7) with 1/16
+    # of its experts and tokens: its kernels at a size a full profiler capture
+    # can replay (2 GB of weights); per-expert work scales by 16 to the large one
+    "large_slice": dict(T=512, d=7168, E=24, I=2048, k=8),
 }
 
 # Scale of the Zipf offsets for the imbalanced workload (seed 0), found by

@@ -44,14 +44,17 @@ def test_mover_bytes_follow_the_fp32_row_layout():
 def test_workload_options():
     class FakeApi:
         MXFP8 = 1
+    assert bench.WORKLOAD == "large"  # the default: the configuration the targets name
     bench.WORKLOAD = "mxfp8"
     try:
         opts = bench.layer_options(FakeApi)
         assert opts == dict(dtype=1, mb_tokens=2048, ring_slots=2)
         assert "MXFP8" in bench.workload_config(gen.workload_shape("mxfp8"))["workload"]
     finally:
-        bench.WORKLOAD = "fine"
+        bench.WORKLOAD = "large"
     assert bench.layer_options(FakeApi) == {}
+    assert bench.workload_config(gen.workload_shape("large"))["workload"].startswith(
+        "large: T=8192 d=7168 E=384 I=2048 top-8")
 
 
 def test_router_wgrad_reduce_folds_into_the_router_gradient():
@@ -127,3 +130,20 @@ def test_gemm_bytes_fine_weight_gradients_are_hbm_bound():
     assert eight["bwd_gate_up_wgrad"][0] == pytest.approx(one["bwd_gate_up_wgrad"][0])
     for n, (t, w) in b.items():
         assert 0 < w < t, n
+
+
+def test_router_wgrad_bytes_algorithmic_and_executed():
+    """Algorithmic: x read once, fp32 dW_r written.  Executed (fine: 16
+    chunks of 256 tokens, E padded to 128): plus the dl hi/lo operand and the
+    fp32 partials written and read back."""
+    s = gen.workload_shape("fine")
+    T, d, E = s.T, s.d, s.E
+    assert bench.mover_bytes(s)["router_wgrad"] == T * d * 2 + E * d * 4
+    part = 16 * 128 * d * 4
+    assert bench.router_wgrad_executed_bytes(s) == T * d * 2 + 2 * T * 128 * 2 + 2 * part + E * d * 4
+
+
+def test_ncu_traffic_is_per_workload():
+    t, src = bench.ncu_traffic("fine", "bwd_gate_up_wgrad")
+    assert t > 1e9 and src.startswith("profiles/")
+    assert bench.ncu_traffic("tiny", "bwd_gate_up_wgrad") == (None, None)
