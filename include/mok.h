@@ -84,6 +84,15 @@ typedef enum mok_dtype {
  * 128-row tiles instead.  Both engines accumulate every output element over
  * the same K sequence, so the results are bitwise the same. */
 #define MOK_FLAG_SINGLE_CTA_GEMM 0x10u
+/* Dispatch recompute ([dothoosh] "Ring buffer logic": the reverse ring walk
+ * keeps forward activation replay small): `saved` keeps no dispatched token
+ * rows (x_perm is MOK_NOT_KEPT, ring_slot_bytes 0); the forward dispatches
+ * into its workspace and the backward gathers x into expert order again with
+ * the same kernel, so every result is bitwise the same.  Saves
+ * rows_max*d*2 bytes of `saved` per ring slot for one more row dispatch in
+ * the backward.  MXFP8 keeps no dispatched rows anyway (the flag is accepted
+ * and changes nothing there). */
+#define MOK_FLAG_RECOMPUTE_DISPATCH 0x20u
 
 /* Offset value of a mok_saved_layout field the flags leave out of `saved`. */
 #define MOK_NOT_KEPT ((size_t)-1)
@@ -104,7 +113,9 @@ typedef struct mok_moe_desc {
 /* Byte offsets, inside the `saved` buffer, of the forward results that the
  * backward consumes.  Row-indexed arrays use the padded row space: expert e
  * owns rows [padded_offsets[e], padded_offsets[e+1]), each segment a multiple
- * of 128 rows, its first counts[e] rows real and the rest zero.
+ * of 128 rows, its first counts[e] rows real, the padding rows after them zero
+ * up to the next multiple of 64 rows (the weight gradients' K blocks read
+ * them), and the rest of the segment unspecified (read by nothing).
  * With micro-batching the per-token fields describe micro-batch 0 (T =
  * mb_tokens) and micro-batch i's are at + i * mb_stride; x_perm is ring slot
  * 0 and slot j is at + j * ring_slot_bytes (micro-batch i was dispatched to
@@ -119,18 +130,19 @@ typedef struct mok_saved_layout {
   size_t token_of_row;    /* int32 [T*k] inverse of pos */
   size_t padded_offsets;  /* int32 [E+1] */
   size_t padded_pos;      /* int32 [T,k] row of (t,s) in the padded row space */
-  size_t padded_token;    /* int32 [rows_max] token of each padded row, -1 for padding */
+  size_t padded_token;    /* int32 [rows_max] token of each padded row; padding rows -1
+                             up to the segment's next multiple of 64 rows, -2 after */
   size_t row_weight;      /* fp32 [rows_max] routing weight of each padded row, 0 for padding */
   size_t x_perm;          /* bf16 [rows_max, d] dispatched token rows; MOK_NOT_KEPT with
                              MOK_MXFP8 (its quantisers read the token rows through
-                             padded_token instead) */
+                             padded_token instead) and with MOK_FLAG_RECOMPUTE_DISPATCH */
   size_t gate_up;         /* fp32 [rows_max, 2I] pre-activation gate (cols 0..I-1) and up (I..2I-1);
                              MOK_NOT_KEPT with MOK_FLAG_RECOMPUTE_GATE_UP */
   size_t rows_max;        /* number of padded rows the buffers hold: T*k + 127*min(E, T*k), rounded to 128 */
   size_t mb_count;        /* micro-batches (1 without micro-batching) */
   size_t mb_stride;       /* bytes between consecutive micro-batches' fields */
   size_t ring_slots;      /* slots of dispatched rows (1 without micro-batching) */
-  size_t ring_slot_bytes; /* bytes between ring slots (0 with MOK_MXFP8) */
+  size_t ring_slot_bytes; /* bytes between ring slots (0 when x_perm is not kept) */
   size_t total;           /* size of `saved` in bytes */
 } mok_saved_layout;
 
@@ -223,10 +235,13 @@ mok_status mok_moe_dispatch_plan(const mok_moe_desc* desc, const int32_t* topk_i
  * 127*E) + 8*E*ceil(T/256) bytes -- are rejected with
  * MOK_ERR_SCRATCH_LIMIT before anything is enqueued.
  *   status: device int32 that receives the device-side error code (reset to
- *           MOK_OK by this call), or NULL to keep it inside the scratch.
- * The first call on a device resolves the array's device address there
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  All calls share the one array, whose contents
+ *           MOK_OK by this call), e.g. MOK_ERR_DEVICE_INDEX for an expert
+ *           index outside [0, E); or NULL, and then the code stays inside the
+ *           scratch where the caller cannot read it.
+ * Every call resolves the array's device address in the current context
+ * (cudaGetSymbolAddress, which allocates nothing).  The first call in a
+ * process also loads the library's device code, so make one call before any
+ * stream capture.  All calls share the one array, whose contents
  * are whatever the last call left: each call rewrites what it reads, and two
  * calls whose work overlaps on the GPU (different streams, or different host
  * threads on one device) race on it. */

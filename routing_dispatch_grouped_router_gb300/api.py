@@ -17,6 +17,7 @@ FLAG_BF16_WGRAD_OUT = 0x2  # weight gradients written as bf16 (default fp32)
 FLAG_ACCUMULATE_WGRAD = 0x4  # backward adds into the fp32 weight gradients
 FLAG_RECOMPUTE_GATE_UP = 0x8  # g, u not kept by the forward; the backward recomputes them
 FLAG_SINGLE_CTA_GEMM = 0x10  # one-CTA 128-row GEMM tiles instead of CTA pairs
+FLAG_RECOMPUTE_DISPATCH = 0x20  # dispatched x rows not kept; the backward gathers them again
 NOT_KEPT = (1 << 64) - 1  # saved-layout offset of a field the flags leave out
 
 

@@ -103,6 +103,12 @@ struct GemmArgs {
   int nseg;
   int poff_stride;
   int seg_rows;
+  // KGROUP: [E+1] real (unpadded) row offsets in the same layout as poff, or
+  // NULL.  Given, the K loop of expert e in a row space covers its real rows
+  // rounded up to a 64-row block instead of its 128-padded rows: the padding
+  // rows of every weight-gradient operand are zero, so the skipped products
+  // are exact zeros and the sums do not change.
+  const int* coff;
   int* status;
 };
 
@@ -216,14 +222,19 @@ __device__ __forceinline__ int total_tiles(const GemmArgs& a) {
   return a.m_tiles * a.n_tiles * (a.k_splits > 1 ? a.k_splits : 1);
 }
 
+// K blocks of expert e in row space s of a KGROUP launch: its real rows
+// rounded up to 64 when the real offsets are given, else its padded rows.
+__device__ __forceinline__ int seg_kb(const GemmArgs& a, int s, int e) {
+  const long long o = static_cast<long long>(s) * a.poff_stride;
+  if (a.coff) return (__ldg(a.coff + o + e + 1) - __ldg(a.coff + o + e) + 63) / 64;
+  return (__ldg(a.poff + o + e + 1) - __ldg(a.poff + o + e)) / 64;
+}
+
 // K blocks of expert e over all row spaces of a KGROUP launch.
 __device__ __forceinline__ int kgroup_kb(const GemmArgs& a, int e) {
   const int ns = a.nseg > 1 ? a.nseg : 1;
   int n = 0;
-  for (int s = 0; s < ns; ++s) {
-    const int* p = a.poff + static_cast<long long>(s) * a.poff_stride;
-    n += (__ldg(p + e + 1) - __ldg(p + e)) / 64;
-  }
+  for (int s = 0; s < ns; ++s) n += seg_kb(a, s, e);
   return n;
 }
 
@@ -232,9 +243,8 @@ struct SegWalk {
   int seg, first_kb, nkb, row;
   __device__ __forceinline__ void load(const GemmArgs& a, int e) {
     const int* p = a.poff + static_cast<long long>(seg) * a.poff_stride;
-    const int k0 = __ldg(p + e), k1 = __ldg(p + e + 1);
-    nkb = (k1 - k0) / 64;
-    row = seg * a.seg_rows + k0;
+    nkb = seg_kb(a, seg, e);
+    row = seg * a.seg_rows + __ldg(p + e);
   }
   __device__ __forceinline__ void init(const GemmArgs& a, int e) {
     seg = 0;
@@ -1662,6 +1672,7 @@ static cudaError_t wgrad(const Dims& D, const char* name, const void* A_rows, in
   a.nseg = sg.nseg;
   a.poff_stride = sg.poff_stride;
   a.seg_rows = (int)D.rows_max;
+  a.coff = sg.coff;
   a.E = (int)D.E;
   a.m_tiles = (int)(M / 128);
   a.n_tiles = (int)(N / bn);
@@ -1727,6 +1738,7 @@ cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* P_hi
   a.nseg = sg.nseg;
   a.poff_stride = sg.poff_stride;
   a.seg_rows = (int)D.rows_max;
+  a.coff = sg.coff;
   a.E = (int)D.E;
   a.m_tiles = (int)(D.I / 128);
   a.n_tiles = (int)(D.d / 256);

@@ -94,7 +94,8 @@ mok_status make_dims(const mok_moe_desc* desc, Dims* out) {
   if (d.dtype != MOK_BF16 && d.dtype != MOK_MXFP8) return MOK_ERR_UNSUPPORTED;
   if (d.mb_tokens < 0 || d.ring_slots < 0) return MOK_ERR_INVALID_ARG;
   if (d.flags & ~(MOK_FLAG_BF16_ACT_OUT | MOK_FLAG_BF16_WGRAD_OUT | MOK_FLAG_ACCUMULATE_WGRAD |
-                  MOK_FLAG_RECOMPUTE_GATE_UP | MOK_FLAG_SINGLE_CTA_GEMM))
+                  MOK_FLAG_RECOMPUTE_GATE_UP | MOK_FLAG_SINGLE_CTA_GEMM |
+                  MOK_FLAG_RECOMPUTE_DISPATCH))
     return MOK_ERR_UNSUPPORTED;
   if ((d.flags & MOK_FLAG_ACCUMULATE_WGRAD) && (d.flags & MOK_FLAG_BF16_WGRAD_OUT))
     return MOK_ERR_UNSUPPORTED;  // accumulation is fp32 only
@@ -134,6 +135,7 @@ mok_status make_dims(const mok_moe_desc* desc, Dims* out) {
   D.accumulate = (d.flags & MOK_FLAG_ACCUMULATE_WGRAD) != 0;
   D.recompute_gu = (d.flags & MOK_FLAG_RECOMPUTE_GATE_UP) != 0;
   D.pair = (d.flags & MOK_FLAG_SINGLE_CTA_GEMM) == 0;
+  D.recompute_dispatch = (d.flags & MOK_FLAG_RECOMPUTE_DISPATCH) != 0 && !D.mx;
   // every row index and element offset used in 32-bit arithmetic must fit
   if (D.rows_max * 2 * D.I >= (1LL << 40)) return MOK_ERR_UNSUPPORTED;
   if (D.rows_max >= (1LL << 31) / 2) return MOK_ERR_UNSUPPORTED;
@@ -177,9 +179,10 @@ void saved_layout(const Dims& D, mok_saved_layout* L, size_t* mtile_prefix_off) 
   BlockL B;
   block_layout(D, &B);
   const size_t base = 256;
-  // MXFP8 keeps no dispatched bf16 rows: its quantisers read the token rows
-  // through the row -> token map
-  const size_t slot = D.mx ? 0 : static_cast<size_t>(D.rows_max) * D.d * 2;
+  // MXFP8 keeps no dispatched bf16 rows (its quantisers read the token rows
+  // through the row -> token map), nor does the dispatch-recompute mode
+  const bool keep_rows = !D.mx && !D.recompute_dispatch;
+  const size_t slot = keep_rows ? static_cast<size_t>(D.rows_max) * D.d * 2 : 0;
   const size_t slot_al = (slot + 255) & ~static_cast<size_t>(255);
   const size_t ring0 = base + B.total * D.nmb;
   L->status = 0;
@@ -195,7 +198,7 @@ void saved_layout(const Dims& D, mok_saved_layout* L, size_t* mtile_prefix_off) 
   L->padded_token = base + B.padded_token;
   L->row_weight = base + B.row_weight;
   L->gate_up = D.recompute_gu ? MOK_NOT_KEPT : base + B.gate_up;
-  L->x_perm = D.mx ? MOK_NOT_KEPT : ring0;
+  L->x_perm = keep_rows ? ring0 : MOK_NOT_KEPT;
   L->rows_max = static_cast<size_t>(D.rows_max);
   L->mb_count = static_cast<size_t>(D.nmb);
   L->mb_stride = B.total;
@@ -207,9 +210,11 @@ void saved_layout(const Dims& D, mok_saved_layout* L, size_t* mtile_prefix_off) 
 void fwd_layout(const Dims& D, FwdWs* W) {
   Bump b;
   const size_t rows = static_cast<size_t>(D.rows_max);
+  W->front_sync = b.take(256);  // directly before the block counts (one memset)
   W->block_counts = b.take(static_cast<size_t>(D.nb) * D.E * 4);
   W->block_base = b.take(static_cast<size_t>(D.nb) * D.E * 4);
   W->h = D.mx ? 0 : b.take(rows * D.I * 2);  // bf16 h (MXFP8: codes below)
+  W->x_perm = D.recompute_dispatch ? b.take(rows * D.d * 2) : 0;
   W->o = b.take(rows * D.d * 4);  // fp32 expert outputs
   W->logits = b.take(static_cast<size_t>(D.T) * D.E * 4 * router_k_splits(D));
   const size_t wgu = static_cast<size_t>(D.E) * 2 * D.I * D.d;  // elements
@@ -254,6 +259,8 @@ void bwd_layout(const Dims& D, BwdWs* W) {
   W->xq_col = D.mx ? b.take(ns * rows * D.d * 2) : 0;
   // BF16 with micro-batches: each micro-batch's dispatched x rows
   W->x_def = (!D.mx && ns > 1) ? b.take(ns * rows * D.d * 2) : 0;
+  // without micro-batches and with the dispatch recompute: x rows again
+  W->x_rd = (D.recompute_dispatch && ns == 1) ? b.take(rows * D.d * 2) : 0;
   // MXFP8 operands of the gate/up dgrad: dG, dU codes and W_gate_up
   // transposed ([E*d, 2I] codes), both with tiled scales
   W->dgu_codes = D.mx ? b.take(rows * 2 * D.I) : 0;
@@ -395,7 +402,6 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
     int32_t* topk_idx = at<int32_t>(saved, L.topk_idx + blk);
     float* topk_w = at<float>(saved, L.topk_w + blk);
     MOK_CUDA(launch_router_logits(D, xi, w_router, logits, status, st));
-    MOK_CUDA(launch_router_topk(D, logits, router_bias, topk_idx, topk_w, status, st));
     PlanOut o;
     o.counts = at<int32_t>(saved, L.counts + blk);
     o.offsets = at<int32_t>(saved, L.offsets + blk);
@@ -406,9 +412,16 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
     o.ppos = at<int32_t>(saved, L.padded_pos + blk);
     o.ptok = at<int32_t>(saved, L.padded_token + blk);
     o.row_w = at<float>(saved, L.row_weight + blk);
-    MOK_CUDA(launch_plan(D, topk_idx, topk_w, at<int32_t>(workspace, F.block_counts),
-                         at<int32_t>(workspace, F.block_base), o, status, st));
-    void* x_perm = D.mx ? nullptr : at<char>(saved, L.x_perm + (i % D.ring) * L.ring_slot_bytes);
+    // top-k selection, histogram, scans and stable placement: one persistent
+    // kernel walking the front-end schedule table
+    MOK_CUDA(launch_route_plan(D, logits, router_bias, topk_idx, topk_w,
+                               at<int32_t>(workspace, F.block_counts),
+                               at<int32_t>(workspace, F.block_base),
+                               at<unsigned>(workspace, F.front_sync), o, status, st));
+    void* x_perm = D.mx                   ? nullptr
+                   : D.recompute_dispatch ? at<char>(workspace, F.x_perm)
+                                          : at<char>(saved, L.x_perm + (i % D.ring) *
+                                                                L.ring_slot_bytes);
     void* gu = D.recompute_gu ? nullptr : at<char>(saved, L.gate_up + blk);
     if (!D.mx)
       MOK_CUDA(launch_dispatch_rows(D, xi, o.ppos, o.ptok, o.padded_offsets, x_perm, status, st));
@@ -442,7 +455,9 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
   mok_status s = make_dims(desc, &D);
   if (s != MOK_OK) return s;
   const bool empty = D.T == 0;  // no token rows: dy, x and dx may be NULL
-  if ((!dy && !empty) || (!x && !empty && D.ring < D.nmb) || !w_router || !w_gate_up ||
+  // x is read by every backward with tokens (the router-weight gradient, and
+  // the row dispatch or MXFP8 quantisers of the weight gradients)
+  if ((!dy && !empty) || (!x && !empty) || !w_router || !w_gate_up ||
       !w_down || !saved || (!dx && !empty) || !dw_router || !dw_gate_up || !dw_down ||
       !workspace)
     return MOK_ERR_INVALID_ARG;
@@ -525,12 +540,17 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
     const int32_t* ptok = at<int32_t>(saved, L.padded_token + blk);
     const float* row_w = at<float>(saved, L.row_weight + blk);
     const void* gu = D.recompute_gu ? at<char>(workspace, B.gu) : at<char>(saved, L.gate_up + blk);
-    void* x_perm = D.mx ? nullptr
-                        : const_cast<char*>(at<char>(saved, L.x_perm + (i % D.ring) *
-                                                                  L.ring_slot_bytes));
+    void* x_perm = (D.mx || D.recompute_dispatch)
+                       ? nullptr
+                       : const_cast<char*>(at<char>(saved, L.x_perm + (i % D.ring) *
+                                                                 L.ring_slot_bytes));
     if (defer && !D.mx) {
       // this micro-batch's rows go to its own slot (the deferred wgrad reads them)
       x_perm = at<char>(workspace, B.x_def) + static_cast<size_t>(i) * rows * D.d * 2;
+      MOK_CUDA(launch_dispatch_rows(D, xi, ppos, ptok, poff, x_perm, status, st));
+    } else if (D.recompute_dispatch) {
+      // saved keeps no dispatched rows: gather x into expert order again
+      x_perm = at<char>(workspace, B.x_rd);
       MOK_CUDA(launch_dispatch_rows(D, xi, ppos, ptok, poff, x_perm, status, st));
     } else if (i < D.nmb - D.ring && !D.mx) {
       // the slot now holds a later micro-batch: dispatch this one again
@@ -573,9 +593,13 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
     MOK_CUDA(gemm_bwd_down_dgrad(D, dy_row_op, wd_op, mtp, poff, static_cast<const float*>(gu),
                                  row_w, dgu_hi_i, dgu_lo_i, p_hi_i, p_lo_i, dgu_c, dgu_s, dp_part,
                                  status, st));
+    // the weight gradients' K loops stop at each expert's real rows
+    WgradSegs one;
+    one.coff = at<int32_t>(saved, L.offsets + blk);
     // down-projection wgrad: dW_down_e (+)= dY_e^T (P_hi + P_lo)_e
     if (!defer)
-      MOK_CUDA(gemm_wgrad_down(D, dy_col_op, p_hi_i, p_lo_i, poff, dw_down, !first, status, st));
+      MOK_CUDA(gemm_wgrad_down(D, dy_col_op, p_hi_i, p_lo_i, poff, dw_down, !first, status, st,
+                               one));
     // gate/up dgrad: dX_perm = dGU W_gu (fp32 rows)
     if (D.mx)
       MOK_CUDA(gemm_bwd_gate_up_dgrad_mx(D, dgu_c, dgu_s, wgu_t_c, wgu_t_s, mtp, poff, dx_perm,
@@ -585,7 +609,7 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
     // gate/up wgrad: dW_gu_e (+)= (dGU_hi + dGU_lo)_e^T X_e
     if (!defer)
       MOK_CUDA(gemm_wgrad_gate_up(D, dgu_hi_i, dgu_lo_i, x_col_op, poff, dw_gate_up, !first,
-                                  status, st));
+                                  status, st, one));
     // reverse-dispatch + router backward
     MOK_CUDA(launch_reverse_dispatch(D, dx_perm, ppos, topk_idx, topk_w, dp_part, w_router, dxi,
                                      dl_hi, dl_lo, rw_off, st));
@@ -598,6 +622,7 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
     WgradSegs sg;
     sg.nseg = D.nmb;
     sg.poff_stride = static_cast<int>(L.mb_stride / 4);
+    sg.coff = at<int32_t>(saved, L.offsets);
     const int32_t* poff0 = at<int32_t>(saved, L.padded_offsets);
     const void* dy_col = D.mx ? at<char>(workspace, B.dyq_col) : dy_perm;
     const void* x_col = D.mx ? at<char>(workspace, B.xq_col) : at<char>(workspace, B.x_def);

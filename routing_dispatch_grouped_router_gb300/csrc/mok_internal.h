@@ -35,6 +35,8 @@ struct Dims {
   bool mx;           // MXFP8 expert GEMM operands
   bool accumulate;   // backward adds into the weight gradients
   bool recompute_gu; // g, u not kept: the backward recomputes them
+  bool recompute_dispatch;  // BF16: dispatched x rows not kept in saved;
+                            // the backward dispatches them again
   bool pair;         // grouped GEMMs with 256-row tiles on CTA pairs (2-SM MMA)
 };
 
@@ -56,7 +58,8 @@ struct BlockL {
       padded_pos, padded_token, row_weight, gate_up, total;
 };
 struct FwdWs {
-  size_t block_counts, block_base, h, o, logits;
+  size_t front_sync, block_counts, block_base, h, o, logits;
+  size_t x_perm;  // dispatched x rows when saved keeps none (recompute_dispatch)
   // MXFP8: E4M3 codes and E8M0 scale bytes of x rows, h, W_gate_up, W_down
   size_t xq_codes, xq_scales, h_codes, h_scales, wgu_codes, wgu_scales, wd_codes, wd_scales;
   size_t total;
@@ -65,7 +68,7 @@ struct BwdWs {
   size_t dy_perm, dgu_hi, dgu_lo, p_hi, p_lo, dp_part, dx_perm, dl_hi, dl_lo, rw_off, rw_part,
       dyq_row, dyq_col,
       xq_col, dgu_codes, dgu_scales, wd_col, wgu_t_codes, wgu_t_scales, gu, xq_codes, xq_scales,
-      wgu_codes, wgu_scales, x_def, total;
+      wgu_codes, wgu_scales, x_def, x_rd, total;
 };
 struct StageWs {
   size_t status, block_counts, block_base, padded_offsets, mtile_prefix, ppos, ptok, row_w,
@@ -105,6 +108,15 @@ struct PlanOut {
 cudaError_t launch_plan(const Dims& D, const int32_t* topk_idx, const float* topk_w,
                         int32_t* block_counts, int32_t* block_base, const PlanOut& o, int* status,
                         cudaStream_t st);
+// The router's top-k and the dispatch plan in one persistent cooperative
+// kernel driven by a schedule table (front.cu); bitwise the same results as
+// launch_router_topk followed by launch_plan.  sync: 256 bytes of scratch;
+// it and block_counts are zeroed by this call (one memset when block_counts
+// starts 256 bytes after sync).
+cudaError_t launch_route_plan(const Dims& D, const float* logits, const float* bias,
+                              int32_t* topk_idx, float* topk_w, int32_t* block_counts,
+                              int32_t* block_base, unsigned* sync, const PlanOut& o, int* status,
+                              cudaStream_t st);
 
 // Rows [0, padded_offsets[E]) of dst: dst[ppos[t, s]] = src[t] for every
 // token t and slot s, zeros where ptok[r] < 0 (padding).  Each src row is
@@ -190,10 +202,13 @@ cudaError_t gemm_bwd_gate_up_dgrad(const Dims& D, const void* dGU, const void* w
 // Weight-gradient GEMMs over nseg row spaces (the micro-batches of a call):
 // operands are [nseg * rows_max, cols] with row space s at rows s*rows_max;
 // row space s has its padded offsets at poff + s*poff_stride.  K runs through
-// the row spaces in order.
+// the row spaces in order.  coff: the real (unpadded) row offsets in the same
+// layout, or NULL; given, each expert's K loop stops after its real rows
+// (rounded up to 64) instead of running through its zero padding rows.
 struct WgradSegs {
   int nseg = 1;
   int poff_stride = 0;  // int32 elements between successive offset arrays
+  const int32_t* coff = nullptr;
 };
 cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* P_hi,
                             const void* P_lo, const int32_t* poff, void* dw_down,

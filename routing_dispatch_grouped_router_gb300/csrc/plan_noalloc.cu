@@ -8,8 +8,6 @@
 #include <cuda_runtime.h>
 #include <string.h>
 
-#include <mutex>
-
 #include "mok_internal.h"
 
 namespace mok {
@@ -21,20 +19,14 @@ constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
 // cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-static std::mutex g_noalloc_mu;
-static void* g_noalloc_ptr[64] = {nullptr};  // device address, per device ordinal
-
-// Resolves the array's device address on the current device (once per device).
+// The array's device address in the current device's context.  Resolved on
+// every call (cudaGetSymbolAddress allocates nothing): an address cached per
+// device would go stale if the caller's framework tore the context down and
+// built a new one.
 static mok_status noalloc_scratch(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOK_ERR_NO_DEVICE;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MOK_ERR_CUDA;
-    g_noalloc_ptr[dev] = p;
-  }
-  *out = g_noalloc_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MOK_ERR_CUDA;
+  *out = p;
   return MOK_OK;
 }
 

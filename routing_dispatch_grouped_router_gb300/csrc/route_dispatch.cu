@@ -21,16 +21,14 @@
 #include <cuda_runtime.h>
 
 #include "mok_internal.h"
+#include "plan.cuh"
 #include "ptx.cuh"
 
 namespace mok {
 
 // ------------------------------------------------------------------ router --
 
-// One warp per token: add the bias, pick the k largest logits (exact ties to
-// the lower expert index; NaN counts as -inf and is reported), softmax over
-// the chosen k.  Slots come out in descending logit order.
-// PER = logits per lane: ceil(E / 32) rounded up to a power of two.
+// One warp per token (the body is topk_token in plan.cuh).
 template <int PER>
 __global__ void router_topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
                                    int T, int E, int k, int nsplit,
@@ -39,71 +37,7 @@ __global__ void router_topk_kernel(const float* __restrict__ logits, const float
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= T) return;
-  float v[PER];
-  bool nan_seen = false;
-  const float* row = logits + static_cast<long long>(warp) * E;
-#pragma unroll
-  for (int j = 0; j < PER; ++j) {
-    const int e = j * 32 + lane;
-    float x = -INFINITY;
-    if (e < E) {
-      // the split-K partial logits, summed in split order
-      x = row[e];
-      for (int sp = 1; sp < nsplit; ++sp) x += row[static_cast<long long>(sp) * T * E + e];
-      if (bias) x += bias[e];
-      if (x != x) {
-        nan_seen = true;
-        x = -INFINITY;
-      }
-    }
-    v[j] = x;
-  }
-  if (__any_sync(0xffffffffu, nan_seen) && lane == 0) set_status(status, MOK_ERR_DEVICE_NONFINITE);
-  float sel_v[kMaxTopK];
-  int sel_e[kMaxTopK];
-  for (int s = 0; s < k; ++s) {
-    // best of this lane: experts are visited in increasing index order, so a
-    // strict '>' keeps the lower index on equal values
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      const int e = j * 32 + lane;
-      if (e < E && (v[j] > bv || (v[j] == bv && e < be))) {
-        bv = v[j];
-        be = e;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-      if (ov > bv || (ov == bv && oe < be)) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    sel_v[s] = bv;
-    sel_e[s] = be;
-    // remove the winner
-#pragma unroll
-    for (int j = 0; j < PER; ++j)
-      if (j * 32 + lane == be) v[j] = NAN;  // NaN never wins a comparison
-  }
-  if (lane == 0) {
-    const float m = sel_v[0];
-    float den = 0.f;
-    float ex[kMaxTopK];
-    for (int s = 0; s < k; ++s) {
-      ex[s] = (sel_v[s] == -INFINITY) ? (m == -INFINITY ? 1.f : 0.f) : expf(sel_v[s] - m);
-      den += ex[s];
-    }
-    const float inv = 1.0f / den;
-    for (int s = 0; s < k; ++s) {
-      topk_idx[static_cast<long long>(warp) * k + s] = sel_e[s];
-      topk_w[static_cast<long long>(warp) * k + s] = ex[s] * inv;
-    }
-  }
+  topk_token<PER>(logits, bias, T, E, k, nsplit, warp, lane, topk_idx, topk_w, nullptr, status);
 }
 
 cudaError_t launch_router_topk(const Dims& D, const float* logits, const float* bias,
@@ -131,24 +65,6 @@ cudaError_t launch_router_topk(const Dims& D, const float* logits, const float* 
 
 // ----------------------------------------------------------- dispatch plan --
 
-// A token's k experts, loaded once into registers, and the mask of its valid
-// slots: bit s is set when slot s names an expert in range that no earlier
-// slot of the token names (a router never repeats; a caller's table might).
-__device__ __forceinline__ uint32_t load_row(const int32_t* row, int k, int E,
-                                             int (&ids)[kMaxTopK]) {
-#pragma unroll
-  for (int s = 0; s < kMaxTopK; ++s) ids[s] = s < k ? row[s] : -1;
-  uint32_t valid = 0;
-#pragma unroll
-  for (int s = 0; s < kMaxTopK; ++s) {
-    bool ok = s < k && ids[s] >= 0 && ids[s] < E;
-#pragma unroll
-    for (int j = 0; j < s; ++j) ok = ok && ids[j] != ids[s];
-    valid |= ok ? (1u << s) : 0u;
-  }
-  return valid;
-}
-
 __global__ void plan_hist_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
                                  int32_t* __restrict__ block_counts, int* status) {
   __shared__ int cnt[kMaxExperts];
@@ -168,94 +84,18 @@ __global__ void plan_hist_kernel(const int32_t* __restrict__ topk_idx, int T, in
     block_counts[static_cast<long long>(blockIdx.x) * E + e] = cnt[e];
 }
 
-// One CTA: per-expert totals and per-(block, expert) bases, then the
-// exclusive scans (plain and padded to 128 rows), the 128-row tile prefix,
-// and the padding rows of every expert segment (token -1, weight 0).
+// One CTA (the body is plan_scan_body in plan.cuh).
 __global__ void plan_scan_kernel(const int32_t* __restrict__ block_counts, int nb, int E,
                                  int32_t* __restrict__ block_base, int32_t* __restrict__ counts,
                                  int32_t* __restrict__ offsets, int32_t* __restrict__ poff,
                                  int32_t* __restrict__ mtile_prefix, int32_t* __restrict__ ptok,
                                  float* __restrict__ row_w) {
-  __shared__ int s_cnt[kMaxExperts];
-  __shared__ int s_off[kMaxExperts + 1];
-  __shared__ int s_poff[kMaxExperts + 1];
-  __shared__ int s_pair[kMaxExperts + 1];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int b = 0; b < nb; ++b) {
-      block_base[static_cast<long long>(b) * E + e] = run;
-      run += block_counts[static_cast<long long>(b) * E + e];
-    }
-    s_cnt[e] = run;
-    counts[e] = run;
-  }
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    // warp scan: lane owns experts [lane*PER, lane*PER+PER)
-    const int lane = threadIdx.x;
-    constexpr int PER = kMaxExperts / 32;
-    // row tiles of an expert, and pairs of row tiles (an odd count rounds up)
-    auto tiles = [](int c) { return (c + kRowPad - 1) / kRowPad; };
-    int sum = 0, psum = 0, qsum = 0;
-    for (int j = 0; j < PER; ++j) {
-      const int e = lane * PER + j;
-      if (e < E) {
-        sum += s_cnt[e];
-        psum += tiles(s_cnt[e]) * kRowPad;
-        qsum += (tiles(s_cnt[e]) + 1) / 2;
-      }
-    }
-    int incl = sum, pincl = psum, qincl = qsum;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int a = __shfl_up_sync(0xffffffffu, incl, off);
-      const int b = __shfl_up_sync(0xffffffffu, pincl, off);
-      const int c = __shfl_up_sync(0xffffffffu, qincl, off);
-      if (lane >= off) {
-        incl += a;
-        pincl += b;
-        qincl += c;
-      }
-    }
-    int run = incl - sum, prun = pincl - psum, qrun = qincl - qsum;
-    for (int j = 0; j < PER; ++j) {
-      const int e = lane * PER + j;
-      if (e < E) {
-        s_off[e] = run;
-        s_poff[e] = prun;
-        s_pair[e] = qrun;
-        run += s_cnt[e];
-        prun += tiles(s_cnt[e]) * kRowPad;
-        qrun += (tiles(s_cnt[e]) + 1) / 2;
-      }
-    }
-    if (lane == 31) {
-      s_off[E] = run;
-      s_poff[E] = prun;
-      s_pair[E] = qrun;
-    }
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-    offsets[e] = s_off[e];
-    poff[e] = s_poff[e];
-    mtile_prefix[e] = s_poff[e] / kRowPad;
-    mtile_prefix[E + 1 + e] = s_pair[e];  // prefix of tile pairs
-  }
-  // padding rows of each expert segment
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  for (int e = warp; e < E; e += nw) {
-    const int a = s_poff[e] + s_cnt[e], b = s_poff[e + 1];
-    for (int r = a + lane; r < b; r += 32) {
-      ptok[r] = -1;
-      if (row_w) row_w[r] = 0.f;
-    }
-  }
+  plan_scan_body(block_counts, nb, E, block_base, counts, offsets, poff, mtile_prefix, ptok,
+                 row_w);
 }
 
-// Stable placement: the rank of token t among the tokens of its block routed
-// to the same expert is the number of set bits below t in that expert's
-// 256-bit membership mask.
+// One CTA of kPlanBlock threads per block of tokens (the body is
+// plan_place_body in plan.cuh).
 __global__ void plan_place_kernel(const int32_t* __restrict__ topk_idx,
                                   const float* __restrict__ topk_w, int T, int E, int k,
                                   const int32_t* __restrict__ block_base,
@@ -263,49 +103,8 @@ __global__ void plan_place_kernel(const int32_t* __restrict__ topk_idx,
                                   const int32_t* __restrict__ poff, int32_t* __restrict__ pos,
                                   int32_t* __restrict__ token_of_row, int32_t* __restrict__ ppos,
                                   int32_t* __restrict__ ptok, float* __restrict__ row_w) {
-  constexpr int W = kPlanBlock / 32;  // 8 mask words per expert
-  __shared__ uint32_t mask[kMaxExperts * W];
-  // per expert: first row of this block's tokens, plain and padded
-  __shared__ int s_row[kMaxExperts], s_prow[kMaxExperts];
-  for (int i = threadIdx.x; i < E * W; i += blockDim.x) mask[i] = 0u;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int b = block_base[static_cast<long long>(blockIdx.x) * E + e];
-    s_row[e] = offsets[e] + b;
-    s_prow[e] = poff[e] + b;
-  }
-  __syncthreads();
-  const int t = blockIdx.x * kPlanBlock + threadIdx.x;
-  const int word = threadIdx.x >> 5, bit = threadIdx.x & 31;
-  int ids[kMaxTopK];
-  uint32_t valid = 0;
-  if (t < T) {
-    valid = load_row(topk_idx + static_cast<long long>(t) * k, k, E, ids);
-#pragma unroll
-    for (int s = 0; s < kMaxTopK; ++s)
-      if (valid & (1u << s)) atomicOr(&mask[ids[s] * W + word], 1u << bit);
-  }
-  __syncthreads();
-  if (t >= T) return;
-#pragma unroll
-  for (int s = 0; s < kMaxTopK; ++s) {
-    if (s >= k) break;
-    const long long ts = static_cast<long long>(t) * k + s;
-    if (!(valid & (1u << s))) {
-      if (pos) pos[ts] = -1;
-      ppos[ts] = -1;
-      continue;
-    }
-    const int e = ids[s];
-    int rank = __popc(mask[e * W + word] & ((1u << bit) - 1u));
-    for (int w = 0; w < word; ++w) rank += __popc(mask[e * W + w]);
-    const int p = s_row[e] + rank;
-    const int pp = s_prow[e] + rank;
-    if (pos) pos[ts] = p;
-    if (token_of_row) token_of_row[p] = t;
-    ppos[ts] = pp;
-    ptok[pp] = t;
-    if (row_w) row_w[pp] = topk_w[ts];
-  }
+  plan_place_body(blockIdx.x, topk_idx, topk_w, T, E, k, block_base, offsets, poff, pos,
+                  token_of_row, ppos, ptok, row_w);
 }
 
 cudaError_t launch_plan(const Dims& D, const int32_t* topk_idx, const float* topk_w,
@@ -348,7 +147,9 @@ cudaError_t launch_plan(const Dims& D, const int32_t* topk_idx, const float* top
 // ring that the warp refills 32 tokens at a time (each lane loads one token's
 // positions), each refill's loads issued 16 tokens before they are written,
 // so the issuing lane never waits on an index load.  Afterwards the CTA
-// stores a zeroed slot to the padding rows among rows b, b + G, ...
+// stores a zeroed slot to the padding rows among rows b, b + G, ... that the
+// plan marks as read (token -1: up to each expert's next 64-row boundary);
+// rows marked -2 are left as they are.
 constexpr int kDispatchLag = 2;
 constexpr int kDispatchMaxSlots = 32;
 constexpr int kDispatchIdx = 128;
@@ -423,7 +224,8 @@ __global__ void __launch_bounds__(32) dispatch_rows_kernel(
       }
     }
   }
-  // padding rows: a zeroed slot stored to every row r = first + i G with no token
+  // padding rows that are read: a zeroed slot stored to every row
+  // r = first + i G marked -1
   if (lane == 0) bulk_wait_read<0>();  // every slot has been read out
   __syncwarp();
   for (uint32_t i = lane * 16; i < row_bytes; i += 32 * 16)
@@ -435,7 +237,7 @@ __global__ void __launch_bounds__(32) dispatch_rows_kernel(
   for (long long i0 = 0; i0 < m; i0 += 32) {
     const long long i = i0 + lane;
     const int t = i < m ? ptok[first + i * G] : 0;
-    const unsigned pad = __ballot_sync(0xffffffffu, i < m && !(t >= 0 && t < T));
+    const unsigned pad = __ballot_sync(0xffffffffu, i < m && t == -1);
     if (lane == 0 && pad) {
       for (int l = 0; l < 32; ++l)
         if (pad & (1u << l))

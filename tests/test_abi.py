@@ -126,6 +126,39 @@ def test_recompute_flag_drops_gate_up_from_saved(lib):
     assert sr == Lr.total and br - bb == per_mb  # one micro-batch of g, u in the scratch
 
 
+def test_recompute_dispatch_flag_drops_the_dispatched_rows_from_saved(lib):
+    """MOK_FLAG_RECOMPUTE_DISPATCH: no ring of dispatched x rows in `saved`;
+    one slot moves to the forward scratch and, without micro-batches, one to
+    the backward scratch (with them the backward already dispatches each
+    micro-batch into its own weight-gradient slot)."""
+    for mb, ring in ((0, 0), (256, 2)):
+        T = 1024
+        base, rec = _desc(T=T, mb=mb, ring=ring), _desc(T=T, mb=mb, ring=ring, flags=0x20)
+        Lb, Lr = _lib.SavedLayout(), _lib.SavedLayout()
+        assert lib.mok_moe_saved_layout(ctypes.byref(base), ctypes.byref(Lb)) == 0
+        assert lib.mok_moe_saved_layout(ctypes.byref(rec), ctypes.byref(Lr)) == 0
+        assert Lr.x_perm == (1 << 64) - 1 and Lr.ring_slot_bytes == 0
+        slot = Lb.rows_max * 128 * 2
+        assert Lb.total - Lr.total == Lb.ring_slots * slot
+        _, fb, _, bb = _sizes(lib, base)
+        _, fr, sr, br = _sizes(lib, rec)
+        assert sr == Lr.total and fr - fb == slot
+        assert br - bb == (slot if mb == 0 else 0)
+    # accepted with MXFP8, which keeps no dispatched rows anyway
+    mx, mxr = _desc(dtype=1), _desc(dtype=1, flags=0x20)
+    assert _sizes(lib, mx)[1:] == _sizes(lib, mxr)[1:]
+
+
+def test_backward_rejects_a_missing_x(lib):
+    """Every backward with tokens reads x (the router-weight gradient), so a
+    NULL x is rejected before any device call, whatever the ring."""
+    d = _desc(T=1024, mb=256)
+    p = ctypes.c_void_p(256)
+    code = lib.mok_moe_backward(ctypes.byref(d), p, None, p, None, p, p, p, 1 << 40, p, p, p,
+                                p, p, 1 << 40, None)
+    assert code == 1
+
+
 @pytest.mark.parametrize("kw,expect", [
     (dict(k=9, E=16), 2), (dict(k=3, E=2), 2), (dict(E=513), 2), (dict(d=96), 2),
     (dict(I=200), 2), (dict(dtype=2), 2), (dict(T=-1), 1), (dict(k=0), 1), (dict(d=0), 1),

@@ -1,8 +1,9 @@
 """Parity of the CUDA layer (through the C ABI) against the fp64 oracle, plus
-determinism and edge cases.  Bar: routing, counts, offsets and permutation
-bit-exact (near-ties flagged by the oracle excluded); outputs and gradients
-within max|diff| <= 2e-2 * rms(oracle) per tensor; repeated calls bitwise
-identical."""
+determinism and edge cases.  Bar: routing bit-exact where the oracle decides
+it; dispatch plan bit-exact and every output and gradient within
+max|diff| <= 2e-2 * rms(oracle) per tensor, with the oracle's routing taking
+the kernel's choice only on near-ties (tests/_gpu.py forced_routing);
+repeated calls bitwise identical."""
 import numpy as np
 import pytest
 import torch
@@ -56,6 +57,9 @@ SMALL = {
     # the widest rows the layer takes: 32 KB per token row, so the dispatch
     # runs one CTA per SM with six row slots
     "d16384": gen.Shape(T=64, d=16384, E=4, I=128, k=2),
+    # E > 128: the router-weight gradient GEMM has two 128-row M tiles (E padded
+    # to 256), several token chunks and a ragged last chunk
+    "e200": gen.Shape(T=300, d=256, E=200, I=128, k=2),
 }
 
 
@@ -106,6 +110,29 @@ def test_layer_parity_fine_full_size():
     gpu = _gpu.run_gpu(shape, inp)
     errs = _gpu.full_parity(shape, inp, gpu)
     print("fine errs", errs)
+
+
+def test_nan_token_reports_status_and_leaves_other_tokens_finite():
+    """A NaN in one token's hidden state makes its router logits NaN: the
+    router treats them as -inf (so the token takes experts 0..k-1 with equal
+    weights), reports MOK_ERR_DEVICE_NONFINITE, and every other token keeps
+    its routing and finite outputs."""
+    shape = SMALL["wide"]
+    inp = gen.make_inputs(shape, seed=3)
+    clean = _gpu.run_gpu(shape, inp)
+    assert clean["status"] == 0
+    x = inp["x"].copy()
+    x[5, 17] = 0x7FC0  # bf16 quiet NaN
+    bad = _gpu.run_gpu(shape, dict(inp, x=x))
+    assert bad["status"] == 16
+    assert list(bad["topk_idx"][5]) == list(range(shape.k))
+    np.testing.assert_allclose(bad["topk_w"][5], 1.0 / shape.k, rtol=1e-6)
+    others = np.arange(shape.T) != 5
+    assert np.array_equal(bad["topk_idx"][others], clean["topk_idx"][others])
+    for n in ("y", "dx"):
+        got = _gpu.host64(bad[n])[others]
+        assert np.isfinite(got).all(), n
+        assert _gpu.rel_err(got, _gpu.host64(clean[n])[others]) <= 1e-6, n
 
 
 @pytest.mark.parametrize("name", ["tiny", "fine"])
@@ -182,6 +209,34 @@ def test_recompute_gate_up_is_bitwise_identical(dtype, mb, ring):
                      ("y", "dx", "dw_router", "dw_gate_up", "dw_down")])
     for a, b in zip(*outs):
         assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("flags,mb,ring", [
+    (0x20, 0, 0),          # dispatch recompute, one pass
+    (0x20, 256, 1),        # micro-batches through a 1-slot ring
+    (0x20 | 0x8, 0, 0),    # with the gate/up recompute too
+])
+def test_recompute_dispatch_is_bitwise_identical(flags, mb, ring):
+    """The backward's second dispatch of x gives the rows the forward's gave,
+    so every output is bitwise the same as with the rows kept in `saved`."""
+    shape = gen.Shape(T=1024, d=256, E=8, I=256, k=2)
+    inp = gen.make_inputs(shape, seed=7)
+    outs = []
+    for f in (0, flags):
+        g = _gpu.run_gpu(shape, inp, flags=f, mb_tokens=mb, ring_slots=ring)
+        assert g["status"] == 0
+        assert (g["layer"].layout.x_perm == api.NOT_KEPT) == bool(f & api.FLAG_RECOMPUTE_DISPATCH)
+        outs.append([g[n].view(torch.int32).cpu().numpy() for n in
+                     ("y", "dx", "dw_router", "dw_gate_up", "dw_down")])
+    for n, a, b in zip(("y", "dx", "dw_router", "dw_gate_up", "dw_down"), *outs):
+        assert np.array_equal(a, b), n
+
+
+def test_recompute_dispatch_parity():
+    shape = SMALL["wide"]
+    inp = gen.make_inputs(shape, seed=4)
+    gpu = _gpu.run_gpu(shape, inp, flags=api.FLAG_RECOMPUTE_DISPATCH)
+    _gpu.full_parity(shape, inp, gpu)
 
 
 def test_recompute_gate_up_parity():
@@ -280,6 +335,40 @@ def test_dispatch_plan_stage_bit_exact(T, E, k):
     assert np.array_equal(offsets.cpu().numpy(), o)
     assert np.array_equal(pos.cpu().numpy(), p)
     assert np.array_equal(tok.cpu().numpy(), t)
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "one_token", "many_experts", "e200", "fine"])
+def test_fused_front_end_matches_the_stage_kernels(name):
+    """The forward runs the router's top-k and the dispatch plan as one
+    persistent kernel walking a schedule table; the stage entry points run
+    them as four kernels (top-k, histogram, scan, placement).  Same inputs,
+    bitwise the same routing weights and plan."""
+    shape = SMALL.get(name) or gen.workload_shape(name)
+    inp = gen.make_inputs(shape, seed=2)
+    layer = api.MoELayer(shape.T, shape.d, shape.E, shape.I, shape.k)
+    x, wr, wgu, wd = (_gpu.dev_bf16(inp[n]) for n in ("x", "w_router", "w_gate_up", "w_down"))
+    layer.forward(x, wr, None, wgu, wd)
+    assert layer.status() == 0
+    T, k, E = shape.T, shape.k, shape.E
+    desc = api.make_desc(T, shape.d, E, shape.I, k)
+    ws = torch.zeros(api.stage_workspace_size(desc), dtype=torch.uint8, device="cuda")
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    api.route(desc, x, wr, None, idx, w, ws)
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    pos = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    tok = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    api.dispatch_plan(desc, idx, counts, offsets, pos, tok, ws)
+    assert api.device_status(ws) == 0
+    fused = {n: layer.saved_tensor(n, dt, shp) for n, dt, shp in (
+        ("topk_idx", torch.int32, (T, k)), ("topk_w", torch.int32, (T, k)),
+        ("counts", torch.int32, (E,)), ("offsets", torch.int32, (E + 1,)),
+        ("pos", torch.int32, (T, k)), ("token_of_row", torch.int32, (T * k,)))}
+    stages = dict(topk_idx=idx, topk_w=w.view(torch.int32), counts=counts, offsets=offsets,
+                  pos=pos, token_of_row=tok)
+    for n in stages:
+        assert torch.equal(fused[n], stages[n]), n
 
 
 def test_dispatch_plan_flags_bad_indices():

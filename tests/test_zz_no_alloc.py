@@ -63,6 +63,23 @@ def test_noalloc_plan_matches_workspace_plan_twice_in_a_row():
             assert np.array_equal(a, b)
 
 
+def test_noalloc_plan_reports_a_bad_index_in_the_callers_status():
+    """An expert index outside [0, E) is skipped on the device and reported as
+    MOK_ERR_DEVICE_INDEX (17) in the caller's status word, as the workspace
+    plan reports it in its workspace; both plans agree on every output."""
+    lib = _lib.load()
+    T, E, k = 200, 9, 3
+    rng = np.random.default_rng(12)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    idx[17, 2] = E
+    st_ref, ref = _plan(lib, idx, E, k, noalloc=False)
+    st_new, new = _plan(lib, idx, E, k, noalloc=True)
+    assert st_ref == 17 and st_new == 17
+    for a, b in zip(ref, new):
+        assert np.array_equal(a, b)
+    assert new[2][17, 2] == -1
+
+
 def test_noalloc_plan_rejects_problems_beyond_its_scratch():
     lib = _lib.load()
     desc = api.make_desc(200000, 128, 64, 128, 8)
