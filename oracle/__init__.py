@@ -10,3 +10,4 @@ from .moe_ref import (  # noqa: F401
     expert_ffn, moe_forward_ref, moe_backward_ref,
 )
 from .mx_ref import e4m3_round, mx_quantize, mx_fake  # noqa: F401
+from .nvfp4_ref import e2m1_round, nvfp4_quantize, nvfp4_fake  # noqa: F401
