@@ -265,6 +265,39 @@ mok_status mok_moe_dispatch_plan_noalloc(const mok_moe_desc* desc, const int32_t
 mok_status mok_mx_quantize(const void* in, int64_t rows, int64_t cols, int along_rows, void* out,
                            uint8_t* codes, uint8_t* scales, void* stream);
 
+/* NVFP4 ([dothoosh] "Background: solving the MoE bottleneck": Cursor's earlier
+ * expert GEMMs ran in MXFP8 and NVFP4; the format is NVIDIA's, the order of
+ * its fp32 operations this library's): E2M1 elements, one E4M3 scale per 16
+ * consecutive values along K, one fp32 scale per tensor.
+ *   g   = amax / 2688 (= 6 * 448), 1 for an all-zero tensor
+ *   s_b = RNE_E4M3(amax_b / (6 g))      (6 g rounded to fp32 first; <= 448)
+ *   q   = RNE_E2M1(v / (s_b g))         (s_b g rounded first; +-6 saturated;
+ *                                        0 where s_b = 0)
+ * Finite inputs only (a NaN is ignored by the tensor amax).
+ *
+ * mok_nvfp4_tensor_scale: g of the n bf16 values at `in` (n % 8 == 0, `in`
+ * 16-byte aligned), written to the device fp32 *g (used as scratch first). */
+mok_status mok_nvfp4_tensor_scale(const void* in, int64_t n, float* g, void* stream);
+
+/* NVFP4 codes and block scales of bf16 [rows, cols] row-major (blocks of 16
+ * along a row, cols % 16 == 0) with the tensor scale at device *g:
+ * codes uint8 [rows, cols/2] (value 2i in the low nibble of byte i, 2i+1 in
+ * the high one; 8-byte aligned), scales uint8 [rows, cols/16] E4M3 bytes. */
+mok_status mok_nvfp4_quantize(const void* in, int64_t rows, int64_t cols, const float* g,
+                              uint8_t* codes, uint8_t* scales, void* stream);
+
+/* Dense NVFP4 GEMM on the block-scaled FP4 tensor cores
+ * (tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X), a diagnostic of
+ * the scale placement:  C[M,N] fp32 = gA gB sum_k qA[m,k] sA[m,k/16] qB[n,k]
+ * sB[n,k/16], with A [M, K/2] and B [N, K/2] codes, A_scales [M, K/16] and
+ * B_scales [N, K/16] bytes (as mok_nvfp4_quantize writes them) and the tensor
+ * scales at device A_g, B_g.  M, N multiples of 128, K of 256.  workspace: at
+ * least 256 bytes (its first int32 is the device status word). */
+mok_status mok_gemm_nvfp4(int64_t M, int64_t N, int64_t K, const uint8_t* A,
+                          const uint8_t* A_scales, const float* A_g, const uint8_t* B,
+                          const uint8_t* B_scales, const float* B_g, float* C, void* workspace,
+                          size_t ws_bytes, void* stream);
+
 /* Dense GEMM through the layer's tcgen05 engine, C[M,N] = A B in bf16 with
  * fp32 accumulation and bf16 output (a diagnostic of the grouped engine):
  *   a_mn_major = 0: A stored [M,K];  1: A stored [K,M]

@@ -54,6 +54,12 @@ _SIGS = {
                                 c_void_p, c_void_p, c_size_t, c_void_p]),
     "mok_gemm_mxfp8": (c_int32, [c_int64, c_int64, c_int64, c_void_p, c_void_p, c_void_p,
                                  c_void_p, c_void_p, c_int32, c_void_p, c_size_t, c_void_p]),
+    "mok_nvfp4_tensor_scale": (c_int32, [c_void_p, c_int64, c_void_p, c_void_p]),
+    "mok_nvfp4_quantize": (c_int32, [c_void_p, c_int64, c_int64, c_void_p, c_void_p, c_void_p,
+                                     c_void_p]),
+    "mok_gemm_nvfp4": (c_int32, [c_int64, c_int64, c_int64, c_void_p, c_void_p, c_void_p,
+                                 c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                                 c_void_p]),
     "mok_selftest_bounded_wait": (c_int32, [c_void_p, c_size_t, c_void_p]),
     "mok_fill_zero": (c_int32, [c_void_p, c_size_t, c_void_p]),
     "mok_get_device_status": (c_int32, [c_void_p, c_void_p, ctypes.POINTER(c_int32)]),

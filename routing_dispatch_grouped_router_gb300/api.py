@@ -128,6 +128,40 @@ def mx_quantize(x, along_rows: bool, out=None, codes=None, scales=None, stream=N
     return out
 
 
+def nvfp4_tensor_scale(x, g=None, stream=None):
+    """NVFP4 tensor scale of a bf16 tensor into the device fp32 `g` (see
+    mok_nvfp4_tensor_scale)."""
+    g = torch.empty(1, dtype=torch.float32, device=x.device) if g is None else g
+    _lib.check(_lib.load().mok_nvfp4_tensor_scale(_ptr(x), x.numel(), _ptr(g), _stream(stream)),
+               "mok_nvfp4_tensor_scale")
+    return g
+
+
+def nvfp4_quantize(x, g, codes=None, scales=None, stream=None):
+    """NVFP4 codes [rows, cols/2] and E4M3 block scales [rows, cols/16] of a
+    2-D bf16 tensor with tensor scale g (see mok_nvfp4_quantize)."""
+    rows, cols = x.shape
+    codes = torch.empty(rows, cols // 2, dtype=torch.uint8, device=x.device) if codes is None \
+        else codes
+    scales = torch.empty(rows, cols // 16, dtype=torch.uint8, device=x.device) if scales is None \
+        else scales
+    _lib.check(_lib.load().mok_nvfp4_quantize(_ptr(x), rows, cols, _ptr(g), _ptr(codes),
+                                              _ptr(scales), _stream(stream)),
+               "mok_nvfp4_quantize")
+    return codes, scales
+
+
+def gemm_nvfp4(A, sa, ga, B, sb, gb, C, workspace, stream=None):
+    """C[M,N] fp32 = ga gb dequant(A) dequant(B)^T for NVFP4 codes A [M,K/2],
+    B [N,K/2], E4M3 block scales sa [M,K/16], sb [N,K/16] and device tensor
+    scales ga, gb (see mok_gemm_nvfp4)."""
+    M, N = C.shape
+    K = 2 * A.shape[1]
+    _lib.check(_lib.load().mok_gemm_nvfp4(M, N, K, _ptr(A), _ptr(sa), _ptr(ga), _ptr(B),
+                                          _ptr(sb), _ptr(gb), _ptr(C), _ptr(workspace),
+                                          workspace.numel(), _stream(stream)), "mok_gemm_nvfp4")
+
+
 def device_status(buf, stream=None) -> int:
     """Synchronises the stream and returns the device status word of `buf`."""
     lib = _lib.load()

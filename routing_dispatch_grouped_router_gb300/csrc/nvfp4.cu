@@ -1,0 +1,379 @@
+// NVFP4: E2M1 elements, one E4M3 scale per 16 consecutive values along K, and
+// one fp32 scale per tensor -- the quantiser and a dense GEMM on the
+// block-scaled FP4 tensor cores (tcgen05.mma.kind::mxf4nvf4.block_scale,
+// scale_vec::4X).
+//
+// Source: [dothoosh] "Cursor Mixture-of-Kittens cuts MoE training latency by
+// 5.8x", section "Background: solving the MoE bottleneck": Cursor's earlier
+// training kernels ran the expert GEMMs in MXFP8 and NVFP4.  The pages do not
+// define the format; NVIDIA's published NVFP4 is taken, with one fixed order
+// of fp32 operations:
+//   tensor scale   g   = amax / 2688 (6 * 448), or 1 for an all-zero tensor
+//   block scale    s_b = RNE_E4M3(amax_b / (6 g))      (6 g rounded first)
+//   element        q   = RNE_E2M1(v / (s_b g))         (s_b g rounded first;
+//                        0 where s_b = 0), saturating at +-6
+//   value          q * s_b * g.
+//
+// The GEMM computes C[M,N] = alpha * sum_k qA[m,k] sA[m,k/16] qB[n,k] sB[n,k/16]
+// with alpha = gA * gB: the tensor cores apply the block scales, the epilogue
+// the tensor scales.  One CTA per 128 x 128 tile of C:
+//   warp 0      producer: TMA loads of the A and B code tiles (128 rows x 128
+//               bytes = 256 values, 128-byte swizzle) and the gather of their
+//               scale bytes: per 64-value MMA step j one 512-byte block, row r
+//               at byte 16*(r%32) + 4*(r/32) + i for its 16-value block i;
+//   warp 1      MMA: per stage, tcgen05.cp of the eight scale blocks to TMEM
+//               (32x128b, replicated to the four lane quarters) and four
+//               tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (K = 64
+//               each, four scales per row);
+//   warps 2..5  epilogue: TMEM -> registers -> alpha * acc -> fp32 C.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "mok_internal.h"
+#include "mx.cuh"
+#include "ptx.cuh"
+
+namespace mok {
+namespace {
+
+// ------------------------------------------------------------- quantiser --
+
+// amax of the tensor as the bits of a non-negative float (the integer order of
+// such bits is their value order, so atomicMax takes the maximum whatever the
+// order of the updates).
+__global__ void nv_amax_kernel(const uint4* __restrict__ in, long long nchunks,
+                               unsigned* __restrict__ amax_bits) {
+  float m = 0.f;
+  const long long G = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < nchunks;
+       i += G) {
+    const uint4 w = in[i];
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      m = fmaxf(m, fabsf(bf16lo(u[j])));
+      m = fmaxf(m, fabsf(bf16hi(u[j])));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if ((threadIdx.x & 31) == 0) atomicMax(amax_bits, __float_as_uint(m));
+}
+
+// *g (holding the amax bits) <- the tensor scale
+__global__ void nv_scale_kernel(float* g) {
+  const float amax = __uint_as_float(*reinterpret_cast<unsigned*>(g));
+  *g = amax > 0.f ? amax / 2688.0f : 1.0f;
+}
+
+__device__ __forceinline__ uint8_t cvt_e2m1x2(float hi, float lo) {
+  uint16_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
+      : "=h"(r)
+      : "f"(hi), "f"(lo));
+  return static_cast<uint8_t>(r);
+}
+
+// One thread per block of 16 values along a row: 8 code bytes (value 2i in
+// the low nibble of byte i, 2i+1 in the high one) and one E4M3 scale byte.
+__global__ void nv_quant_kernel(const uint4* __restrict__ in, long long nblk,
+                                const float* __restrict__ g_ptr, uint8_t* __restrict__ codes,
+                                uint8_t* __restrict__ scales) {
+  const float g = *g_ptr;
+  const float six_g = 6.0f * g;
+  const long long G = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long b = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; b < nblk;
+       b += G) {
+    const uint4 w0 = in[2 * b], w1 = in[2 * b + 1];
+    const uint32_t u[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    float v[16];
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[2 * j] = bf16lo(u[j]);
+      v[2 * j + 1] = bf16hi(u[j]);
+      amax = fmaxf(amax, fmaxf(fabsf(v[2 * j]), fabsf(v[2 * j + 1])));
+    }
+    const float x = amax / six_g;
+    const uint8_t sb = static_cast<uint8_t>(cvt_e4m3x2(0.f, x) & 0xFFu);
+    float sb_hi, sb_f;
+    e4m3x2_to_f32(sb, &sb_hi, &sb_f);
+    const float denom = sb_f * g;
+    uint32_t c[2] = {0u, 0u};
+    if (sb != 0) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t byte = cvt_e2m1x2(v[2 * j + 1] / denom, v[2 * j] / denom);
+        c[j >> 2] |= byte << (8 * (j & 3));
+      }
+    }
+    *reinterpret_cast<uint2*>(codes + 8 * b) = make_uint2(c[0], c[1]);
+    scales[b] = sb;
+  }
+}
+
+// ---------------------------------------------------------------- GEMM ----
+
+constexpr int kNvStages = 4;
+constexpr int kNvTile = 128;                  // M = N = 128
+constexpr int kNvBK = 128;                    // code bytes per row per stage (256 values)
+constexpr int kNvCodeBytes = kNvTile * kNvBK;  // 16 KB per operand tile
+constexpr int kNvSfBlock = 512;               // 128 rows x 4 scale bytes (one MMA step)
+constexpr int kNvSfBytes = 4 * kNvSfBlock;    // four MMA steps per stage
+constexpr int kNvStageBytes = 2 * kNvCodeBytes + 2 * kNvSfBytes;  // 36 KB
+constexpr int kNvThreads = 192;
+// TMEM: accumulator columns [0,128); stage s keeps A scales at 128 + 32s
+// (four columns per MMA step) and B scales at 144 + 32s
+constexpr uint32_t kNvTmemCols = 256;
+constexpr int kNvSmem = 1024 + kNvStages * kNvStageBytes + 256;
+
+// Instruction descriptor of kind::mxf4nvf4 with block scaling: E2M1 A and B
+// (packed, K-major), UE4M3 scales (scale_vec::4X: the four bytes of a TMEM
+// word are the row's four 16-value blocks of the step; scale ids 0).
+__device__ __forceinline__ uint32_t idesc_nvf4(int M, int N) {
+  return (1u << 7)                                  // A format: E2M1
+         | (1u << 10)                               // B format: E2M1
+         | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+         | (0u << 23)                               // scale type: UE4M3
+         | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+      " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kNvThreads, 1)
+    nv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const uint8_t* __restrict__ sa, const uint8_t* __restrict__ sb,
+                   const float* __restrict__ ga, const float* __restrict__ gb, float* C, int N,
+                   int K, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kNvStages * kNvStageBytes);
+  uint64_t* empty = full + kNvStages;
+  uint64_t* tfull = empty + kNvStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tile = blockIdx.x, m_tile = blockIdx.y;
+  const int nkb = K / (2 * kNvBK);  // 256 values per stage
+  const long long ks = K / 16;      // scale bytes per row
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kNvStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kNvTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  volatile int* vabort = abort_flag;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer --
+    bool ok = true;
+    for (int kb = 0; kb < nkb && ok; ++kb) {
+      const int s = kb % kNvStages;
+      const uint32_t par = static_cast<uint32_t>((kb / kNvStages) & 1);
+      if (!mbar_wait(&empty[s], par ^ 1u, vabort)) {
+        ok = false;
+        break;
+      }
+      uint8_t* st = smem + s * kNvStageBytes;
+      // scale bytes of this stage: 16 per row, 4 per MMA step
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        gather_sf(st + 2 * kNvCodeBytes + j * kNvSfBlock, sa, ks, (long long)m_tile * kNvTile,
+                  (long long)kb * 16 + 4 * j, lane);
+        gather_sf(st + 2 * kNvCodeBytes + kNvSfBytes + j * kNvSfBlock, sb, ks,
+                  (long long)n_tile * kNvTile, (long long)kb * 16 + 4 * j, lane);
+      }
+      fence_proxy_async_smem();  // the scale copies read these bytes through the async proxy
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full[s], 2 * kNvCodeBytes);
+        tma_load_2d(st, &tmA, &full[s], kb * kNvBK, m_tile * kNvTile);
+        tma_load_2d(st + kNvCodeBytes, &tmB, &full[s], kb * kNvBK, n_tile * kNvTile);
+      }
+    }
+    if (!ok && lane == 0) {
+      *vabort = 1;
+      set_status(status, MOK_ERR_DEVICE_TIMEOUT);
+      spin_ns(1000000ull);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // --------------------------------------------------------------- MMA --
+      bool ok = true;
+      for (int kb = 0; kb < nkb && ok; ++kb) {
+        const int s = kb % kNvStages;
+        const uint32_t par = static_cast<uint32_t>((kb / kNvStages) & 1);
+        if (!mbar_wait(&full[s], par, vabort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t a_base = smem_addr(smem + s * kNvStageBytes);
+        const uint32_t b_base = a_base + kNvCodeBytes;
+        const uint32_t sfa_col = tmem_base + 128u + 32u * s;
+        const uint32_t sfb_col = sfa_col + 16u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          tmem_cp_sf(sfa_col + 4u * j, smem_desc_sf(a_base + 2 * kNvCodeBytes + j * kNvSfBlock));
+          tmem_cp_sf(sfb_col + 4u * j,
+                     smem_desc_sf(a_base + 2 * kNvCodeBytes + kNvSfBytes + j * kNvSfBlock));
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          // 64 values = 32 bytes per step inside the 128-byte swizzled rows
+          const uint64_t ad = smem_desc_sw128(a_base + j * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(b_base + j * 32, 16, 1024);
+          mma_nvf4(tmem_base, ad, bd, idesc_nvf4(kNvTile, kNvTile), sfa_col + 4u * j,
+                   sfb_col + 4u * j, (kb | j) != 0 ? 1u : 0u);
+        }
+        mma_commit(&empty[s]);
+      }
+      if (ok) {
+        mma_commit(tfull);
+      } else {
+        *vabort = 1;
+        set_status(status, MOK_ERR_DEVICE_TIMEOUT);
+        mma_commit(tfull);  // lets the epilogue leave; its results are void
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue --
+    const int q = warp & 3;  // TMEM lane quarter of this warp
+    const int zero = 0;
+    if (!mbar_wait(tfull, 0, &zero)) set_status(status, MOK_ERR_DEVICE_TIMEOUT);
+    tc_fence_after_sync();
+    const float alpha = *ga * *gb;
+    const long long row = (long long)m_tile * kNvTile + q * 32 + lane;
+    float* out = C + row * N + (long long)n_tile * kNvTile;
+#pragma unroll 1
+    for (int c = 0; c < kNvTile; c += 16) {
+      uint32_t r[16];
+      tmem_ld16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + c, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 16; j += 4)
+        *reinterpret_cast<float4*>(out + c + j) =
+            make_float4(alpha * __uint_as_float(r[j]), alpha * __uint_as_float(r[j + 1]),
+                        alpha * __uint_as_float(r[j + 2]), alpha * __uint_as_float(r[j + 3]));
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kNvTmemCols);
+  }
+}
+
+}  // namespace
+}  // namespace mok
+
+using namespace mok;
+
+extern "C" mok_status mok_nvfp4_tensor_scale(const void* in, int64_t n, float* g, void* stream) {
+  if (n < 0) return MOK_ERR_INVALID_ARG;
+  if (!g || (n > 0 && !in)) return MOK_ERR_INVALID_ARG;
+  if (n % 8 != 0 || (reinterpret_cast<uintptr_t>(in) & 15u) ||
+      (reinterpret_cast<uintptr_t>(g) & 3u))
+    return MOK_ERR_INVALID_ARG;
+  mok_status s = mok_check_device();
+  if (s != MOK_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(g, 0, sizeof(float), st) != cudaSuccess) return MOK_ERR_CUDA;
+  const long long nchunks = n / 8;
+  if (nchunks > 0) {
+    long long grid = (nchunks + 255) / 256;
+    const long long cap = static_cast<long long>(num_sms_current_device()) * 8;
+    if (grid > cap) grid = cap;
+    ProfScope prof("nvfp4_amax", st);
+    nv_amax_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(
+        static_cast<const uint4*>(in), nchunks, reinterpret_cast<unsigned*>(g));
+    count_launch();
+  }
+  nv_scale_kernel<<<1, 1, 0, st>>>(g);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? MOK_OK : MOK_ERR_CUDA;
+}
+
+extern "C" mok_status mok_nvfp4_quantize(const void* in, int64_t rows, int64_t cols,
+                                         const float* g, uint8_t* codes, uint8_t* scales,
+                                         void* stream) {
+  if (rows < 0 || cols <= 0 || cols % 16 != 0) return MOK_ERR_INVALID_ARG;
+  if (rows > 0 && (!in || !g || !codes || !scales)) return MOK_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(in) & 15u) || (reinterpret_cast<uintptr_t>(codes) & 7u) ||
+      (reinterpret_cast<uintptr_t>(g) & 3u))
+    return MOK_ERR_INVALID_ARG;
+  mok_status s = mok_check_device();
+  if (s != MOK_OK) return s;
+  const long long nblk = rows * cols / 16;
+  if (nblk == 0) return MOK_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  long long grid = (nblk + 255) / 256;
+  const long long cap = static_cast<long long>(num_sms_current_device()) * 16;
+  if (grid > cap) grid = cap;
+  ProfScope prof("nvfp4_quantize", st);
+  nv_quant_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(static_cast<const uint4*>(in),
+                                                               nblk, g, codes, scales);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? MOK_OK : MOK_ERR_CUDA;
+}
+
+extern "C" mok_status mok_gemm_nvfp4(int64_t M, int64_t N, int64_t K, const uint8_t* A,
+                                     const uint8_t* A_scales, const float* A_g, const uint8_t* B,
+                                     const uint8_t* B_scales, const float* B_g, float* C,
+                                     void* workspace, size_t ws_bytes, void* stream) {
+  if (!A || !A_scales || !A_g || !B || !B_scales || !B_g || !C || !workspace)
+    return MOK_ERR_INVALID_ARG;
+  if (ws_bytes < 256) return MOK_ERR_WORKSPACE;
+  if (M <= 0 || N <= 0 || K <= 0 || M % kNvTile || N % kNvTile || K % 256)
+    return MOK_ERR_UNSUPPORTED;
+  if (M > (1 << 24) || N > (1 << 24) || K > (1 << 20)) return MOK_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(A) & 15u) || (reinterpret_cast<uintptr_t>(B) & 15u) ||
+      (reinterpret_cast<uintptr_t>(A_scales) & 3u) || (reinterpret_cast<uintptr_t>(B_scales) & 3u) ||
+      (reinterpret_cast<uintptr_t>(C) & 15u))
+    return MOK_ERR_INVALID_ARG;
+  mok_status s = mok_check_device();
+  if (s != MOK_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* status = static_cast<int*>(workspace);
+  if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return MOK_ERR_CUDA;
+  CUtensorMap ta, tb;
+  const auto u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  // codes: [rows, K/2] bytes, 128-byte boxes of 128 rows
+  if (!make_tensor_map_2d(&ta, u8, 1, A, K / 2, M, K / 2, kNvBK, kNvTile, sw) ||
+      !make_tensor_map_2d(&tb, u8, 1, B, K / 2, N, K / 2, kNvBK, kNvTile, sw))
+    return MOK_ERR_INVALID_ARG;
+  if (cudaFuncSetAttribute(nv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kNvSmem) != cudaSuccess)
+    return MOK_ERR_CUDA;
+  dim3 grid(static_cast<unsigned>(N / kNvTile), static_cast<unsigned>(M / kNvTile));
+  ProfScope prof("gemm_nvfp4", st);
+  nv_gemm_kernel<<<grid, kNvThreads, kNvSmem, st>>>(ta, tb, A_scales, B_scales, A_g, B_g, C,
+                                                    static_cast<int>(N), static_cast<int>(K),
+                                                    status);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? MOK_OK : MOK_ERR_CUDA;
+}
