@@ -133,19 +133,19 @@ constexpr int kStagingBytes = 4096;  // per epilogue warp: 32 rows x 128 bytes
 // six bf16 output blocks of a chunk (6 x 1 KB).
 constexpr int kGuStageBytes = 8192;
 constexpr int kSwigluBwdStaging = kGuStageBytes + 6 * 1024;
-// Double-buffered store staging (a block is written while the previous
-// block's store still reads shared memory) is implemented but off: it costs
-// the 256-wide pair kernels their sixth operand stage, and measured slower
-// (fwd_gate_up 245 -> 260 us, fwd_down 132 -> 151 us on the fine workload).
-template <int EPI, int SPLIT, int SCHED>
-constexpr bool dbuf_store() {
-  return false;
-}
-template <int EPI, int SPLIT, int SCHED>
+// Double-buffered store staging (DB: a block is written while the previous
+// block's store still reads shared memory), chosen per launch for the fp32
+// weight gradients (K-grouped, plain and transposed stores) whose tiles run
+// few K blocks (short_k_wgrad): there the epilogue's store chain, not the
+// MMAs, sets the pace (large workload: 29.7 -> 29.0 ms per step), while with
+// long K loops the operand stage it costs matters more (fine workload: the
+// gate/up weight gradient 366 -> 419 us with it).  Off for the M-grouped
+// GEMMs: it costs the 256-wide pair kernels their sixth operand stage, and
+// measured slower there (fwd_gate_up 245 -> 260 us, fwd_down 132 -> 151 us on
+// the fine workload).
+template <int EPI, int SPLIT, int SCHED, bool DB>
 constexpr int staging_bytes() {
-  return EPI == EPI_SWIGLU_BWD ? kSwigluBwdStaging
-                               : (dbuf_store<EPI, SPLIT, SCHED>() ? 2 * kStagingBytes
-                                                                  : kStagingBytes);
+  return EPI == EPI_SWIGLU_BWD ? kSwigluBwdStaging : (DB ? 2 * kStagingBytes : kStagingBytes);
 }
 
 template <int BN, int SPLIT = SPLIT_NONE, bool PAIR = false, int STG = kStagingBytes>
@@ -477,10 +477,18 @@ __device__ __forceinline__ void stage_and_store_f32(uint8_t* base, uint32_t& n,
 // lane i holds row i of the accumulator block (v[j] = column j), and the
 // staging buffer receives column j of the block as its row j, so the TMA store
 // at (x, y) writes element (i, j) to output row y + j, column x + i.
-__device__ __forceinline__ void stage_and_store_f32_t(uint8_t* buf, const CUtensorMap* tmC,
+// DBUF: `base` holds two buffers used alternately (as stage_and_store_f32).
+template <bool DBUF = false>
+__device__ __forceinline__ void stage_and_store_f32_t(uint8_t* base, uint32_t& n,
+                                                      const CUtensorMap* tmC,
                                                       const float (&v)[32], int lane, int x,
                                                       int y, bool add, bool evict_first) {
-  if (lane == 0) bulk_wait_read<0>();
+  uint8_t* buf = DBUF ? base + (n & 1u) * kStagingBytes : base;
+  ++n;
+  if (lane == 0) {  // the store that last used this buffer has read it
+    if (DBUF) bulk_wait_read<1>();
+    else bulk_wait_read<0>();
+  }
   __syncwarp();
   const int chunk = lane >> 2, word = (lane & 3) * 4;
 #pragma unroll
@@ -587,7 +595,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
         stage_and_store_bf16_t(stage_buf, tmC, v, lane, x, tl.e * a.ldo + col0 + c,
                                a.evict_first != 0);
       else
-        stage_and_store_f32_t(stage_buf, tmC, v, lane, x, tl.e * a.ldo + col0 + c,
+        stage_and_store_f32_t<DBUF>(stage_buf, nst, tmC, v, lane, x, tl.e * a.ldo + col0 + c,
                               a.accumulate != 0, a.evict_first != 0);
     }
   } else if (EPI == EPI_BF16 || EPI == EPI_F32) {
@@ -840,13 +848,15 @@ __device__ __forceinline__ uint32_t swiglu_bwd_tma(const GemmArgs& a, const Tile
 
 // ------------------------------------------------------------------- kernel --
 
-template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, int SPLIT, bool PAIR>
+template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, int SPLIT, bool PAIR, bool DB>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmL,
                 const __grid_constant__ GemmArgs args, const __grid_constant__ OutMaps om) {
-  using C = Cfg<BN, SPLIT, PAIR, staging_bytes<EPI, SPLIT, SCHED>()>;
-  constexpr bool kDbuf = dbuf_store<EPI, SPLIT, SCHED>();
+  using C = Cfg<BN, SPLIT, PAIR, staging_bytes<EPI, SPLIT, SCHED, DB>()>;
+  constexpr bool kDbuf = DB;
+  static_assert(!DB || ((EPI == EPI_F32 || EPI == EPI_F32_T) && SCHED == SCHED_KGROUP),
+                "double-buffered staging: the fp32 weight-gradient epilogues");
   static_assert(!PAIR || (SCHED != SCHED_DENSE && SPLIT != SPLIT_B && BN == 256), "pair");
   static_assert(SPLIT != SPLIT_MX ||
                     (!A_MN && !B_MN && BN == (PAIR ? 256 : 128) && SCHED == SCHED_MGROUP),
@@ -1311,7 +1321,7 @@ static bool make_out_map_bf16_t(CUtensorMap* m, const void* base, uint64_t cols,
 // max_units: an upper bound on the tiles (PAIR: tile pairs) of the launch;
 // the kernel reads the exact count on the device.
 template <int BN, bool A_MN, bool B_MN, int SCHED, int EPI, int SPLIT = SPLIT_NONE,
-          bool PAIR = false>
+          bool PAIR = false, bool DB = false>
 static cudaError_t launch(const char* name, const CUtensorMap& ta, const CUtensorMap& tb,
                           const CUtensorMap& tc, const GemmArgs& args, int max_units,
                           cudaStream_t st, const CUtensorMap* tl = nullptr,
@@ -1319,8 +1329,8 @@ static cudaError_t launch(const char* name, const CUtensorMap& ta, const CUtenso
   OutMaps om_v;
   if (om) om_v = *om;
   else memset(&om_v, 0, sizeof(om_v));
-  auto kern = gemm_kernel<BN, A_MN, B_MN, SCHED, EPI, SPLIT, PAIR>;
-  constexpr int smem = Cfg<BN, SPLIT, PAIR, staging_bytes<EPI, SPLIT, SCHED>()>::SMEM_BYTES;
+  auto kern = gemm_kernel<BN, A_MN, B_MN, SCHED, EPI, SPLIT, PAIR, DB>;
+  constexpr int smem = Cfg<BN, SPLIT, PAIR, staging_bytes<EPI, SPLIT, SCHED, DB>()>::SMEM_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (max_units <= 0) return cudaSuccess;
@@ -1649,6 +1659,14 @@ cudaError_t gemm_bwd_gate_up_dgrad(const Dims& D, const void* dGU, const void* w
                                                          st);
 }
 
+// Double-buffered store staging for a weight gradient whose experts average at
+// most 384 real rows over the launch's row spaces (six 64-row K blocks per
+// output tile): a function of the shape only.
+static bool short_k_wgrad(const Dims& D, int nseg) {
+  const int64_t rows = D.R * (nseg > 1 ? nseg : 1);
+  return rows <= 384 * D.E;
+}
+
 // K-grouped weight gradient C_e [M, N] = A_e^T B_e over the expert's padded
 // rows, A_e = rows of `A_rows` (inner dim M), B_e = rows of `B_rows` (inner
 // dim N).  One of the two operands comes as a hi/lo pair (`lo_is_a` selects
@@ -1703,15 +1721,31 @@ static cudaError_t wgrad(const Dims& D, const char* name, const void* A_rows, in
                                                                         st, &tl);
   }
   if (!make_out_map(&tc, out, N, D.E * M)) return cudaErrorInvalidValue;
-  if (!lo_is_a)
+  const bool db = short_k_wgrad(D, sg.nseg);
+  if (!lo_is_a) {
+    if (db)
+      return launch<128, true, true, SCHED_KGROUP, EPI_F32, SPLIT_B, false, true>(
+          name, ta, tb, tc, a, mt, st, &tl);
     return launch<128, true, true, SCHED_KGROUP, EPI_F32, SPLIT_B>(name, ta, tb, tc, a, mt, st,
                                                                    &tl);
-  if (bn == 256 && D.pair && a.m_tiles % 2 == 0)
+  }
+  if (bn == 256 && D.pair && a.m_tiles % 2 == 0) {
+    if (db)
+      return launch<256, true, true, SCHED_KGROUP, EPI_F32, SPLIT_A, true, true>(
+          name, ta, tb, tc, a, mt / 2, st, &tl);
     return launch<256, true, true, SCHED_KGROUP, EPI_F32, SPLIT_A, true>(name, ta, tb, tc, a,
                                                                          mt / 2, st, &tl);
-  if (bn == 256)
+  }
+  if (bn == 256) {
+    if (db)
+      return launch<256, true, true, SCHED_KGROUP, EPI_F32, SPLIT_A, false, true>(
+          name, ta, tb, tc, a, mt, st, &tl);
     return launch<256, true, true, SCHED_KGROUP, EPI_F32, SPLIT_A>(name, ta, tb, tc, a, mt, st,
                                                                    &tl);
+  }
+  if (db)
+    return launch<128, true, true, SCHED_KGROUP, EPI_F32, SPLIT_A, false, true>(
+        name, ta, tb, tc, a, mt, st, &tl);
   return launch<128, true, true, SCHED_KGROUP, EPI_F32, SPLIT_A>(name, ta, tb, tc, a, mt, st, &tl);
 }
 
@@ -1758,9 +1792,17 @@ cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* P_hi
     return launch<256, true, true, SCHED_KGROUP, EPI_BF16_T, SPLIT_A>("bwd_down_wgrad", ta, tb,
                                                                       tc, a, mt, st, &tl);
   }
-  if (D.pair && a.m_tiles % 2 == 0)
+  const bool db = short_k_wgrad(D, sg.nseg);
+  if (D.pair && a.m_tiles % 2 == 0) {
+    if (db)
+      return launch<256, true, true, SCHED_KGROUP, EPI_F32_T, SPLIT_A, true, true>(
+          "bwd_down_wgrad", ta, tb, tc, a, mt / 2, st, &tl);
     return launch<256, true, true, SCHED_KGROUP, EPI_F32_T, SPLIT_A, true>(
         "bwd_down_wgrad", ta, tb, tc, a, mt / 2, st, &tl);
+  }
+  if (db)
+    return launch<256, true, true, SCHED_KGROUP, EPI_F32_T, SPLIT_A, false, true>(
+        "bwd_down_wgrad", ta, tb, tc, a, mt, st, &tl);
   return launch<256, true, true, SCHED_KGROUP, EPI_F32_T, SPLIT_A>("bwd_down_wgrad", ta, tb, tc,
                                                                    a, mt, st, &tl);
 }

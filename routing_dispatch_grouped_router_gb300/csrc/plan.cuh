@@ -52,9 +52,13 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ logits,
     v[j] = x;
   }
   if (__any_sync(0xffffffffu, nan_seen) && lane == 0) set_status(status, MOK_ERR_DEVICE_NONFINITE);
+  // slot loops unrolled over kMaxTopK (guarded by k) so that the selected
+  // values and experts stay in registers
   float sel_v[kMaxTopK];
   int sel_e[kMaxTopK];
-  for (int s = 0; s < k; ++s) {
+#pragma unroll
+  for (int s = 0; s < kMaxTopK; ++s) {
+    if (s >= k) break;
     // best of this lane: experts are visited in increasing index order, so a
     // strict '>' keeps the lower index on equal values
     float bv = -INFINITY;
@@ -87,18 +91,26 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ logits,
     const float m = sel_v[0];
     float den = 0.f;
     float ex[kMaxTopK];
-    for (int s = 0; s < k; ++s) {
+#pragma unroll
+    for (int s = 0; s < kMaxTopK; ++s) {
+      if (s >= k) break;
       ex[s] = (sel_v[s] == -INFINITY) ? (m == -INFINITY ? 1.f : 0.f) : expf(sel_v[s] - m);
       den += ex[s];
     }
     const float inv = 1.0f / den;
-    for (int s = 0; s < k; ++s) {
+#pragma unroll
+    for (int s = 0; s < kMaxTopK; ++s) {
+      if (s >= k) break;
       topk_idx[static_cast<long long>(token) * k + s] = sel_e[s];
       topk_w[static_cast<long long>(token) * k + s] = ex[s] * inv;
     }
     if (block_counts) {
       int32_t* bc = block_counts + static_cast<long long>(token / kPlanBlock) * E;
-      for (int s = 0; s < k; ++s) atomicAdd(bc + sel_e[s], 1);
+#pragma unroll
+      for (int s = 0; s < kMaxTopK; ++s) {
+        if (s >= k) break;
+        atomicAdd(bc + sel_e[s], 1);
+      }
     }
   }
 }
@@ -142,10 +154,18 @@ __device__ __forceinline__ void plan_scan_body(const int32_t* __restrict__ block
   __shared__ int s_poff[kMaxExperts + 1];
   __shared__ int s_pair[kMaxExperts + 1];
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    // eight blocks' counts in flight at a time, then their running sum
     int run = 0;
-    for (int b = 0; b < nb; ++b) {
-      block_base[static_cast<long long>(b) * E + e] = run;
-      run += block_counts[static_cast<long long>(b) * E + e];
+    for (int b0 = 0; b0 < nb; b0 += 8) {
+      int c[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        c[j] = b0 + j < nb ? block_counts[static_cast<long long>(b0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (b0 + j < nb) block_base[static_cast<long long>(b0 + j) * E + e] = run;
+        run += c[j];
+      }
     }
     s_cnt[e] = run;
     counts[e] = run;
