@@ -45,6 +45,10 @@ quantised GEMMs the identity <dy, O> = <dy W_down, h> no longer holds exactly;
 the router-weight gradient is taken the way the pages fuse it into the SwiGLU
 backward ([dothoosh] "Precision and scheduling"): dp = <dA, h> with dA the
 (quantised) down-projection dgrad of the row and h unquantised.
+``precision="nvfp4"`` quantises the forward GEMMs' operands to NVFP4 (see
+_nvfp4_experts and nvfp4_ref.py: per-tensor fp32 scales, E4M3 scales per 16
+values along K); the backward is the float64 one on the forward's g, u, h,
+with the router-weight gradient in the same fused form dp = <dy W_down, h>.
 dy is itself a bf16 input,
 so the down dgrad dH = p * (dy W_down) needs no rounded operand.  The expert
 output O, y, dp, the router gradient, dx and the weight gradients are not
@@ -65,6 +69,7 @@ from __future__ import annotations
 import numpy as np
 
 from .mx_ref import mx_fake
+from .nvfp4_ref import nvfp4_fake
 
 NEAR_TIE = 1e-5
 
@@ -102,7 +107,7 @@ def _identity(a):
 
 
 def _rounder(precision: str):
-    if precision in ("fp64", "mxfp8"):
+    if precision in ("fp64", "mxfp8", "nvfp4"):
         return _identity
     if precision == "bf16":
         return bf16_round
@@ -243,6 +248,37 @@ def _mx_rows(a):
     return mx_fake(a, 0)[:n]
 
 
+def _nvfp4_experts(X, w_gate_up, w_down, offsets, tok, R):
+    """The experts' GEMMs on NVFP4 operands (nvfp4_ref): every operand is
+    quantised along its GEMM's reduction dimension, with its tensor scale
+    taken over the whole tensor -- x over all tokens, W_gate_up over all
+    experts' stacked [E*2I, d] rows, W_down over all [E*d, I] rows, and h over
+    all routed rows.  h = silu(g) u is materialised in bf16 before its
+    quantisation (the layer stores it so between the two GEMMs).  Returns
+    (G, U, H, O) in expert order; H is silu(G) U before any rounding."""
+    Wgu = widen(w_gate_up)
+    Wd = widen(w_down)
+    E, I2, d = Wgu.shape
+    I = I2 // 2
+    Xq = nvfp4_fake(X, -1)
+    Wgu_q = nvfp4_fake(Wgu.reshape(E * I2, d), -1).reshape(E, I2, d)
+    Wd_q = nvfp4_fake(Wd.reshape(E * d, I), -1).reshape(E, d, I)
+    G = np.zeros((R, I)); U = np.zeros((R, I)); H = np.zeros((R, I)); O = np.zeros((R, d))
+    for e in range(E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if a == b:
+            continue
+        G[a:b] = Xq[tok[a:b]] @ Wgu_q[e, :I].T
+        U[a:b] = Xq[tok[a:b]] @ Wgu_q[e, I:].T
+        H[a:b] = silu(G[a:b]) * U[a:b]
+    Hq = nvfp4_fake(bf16_round(H), -1) if R else H
+    for e in range(E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if a < b:
+            O[a:b] = Hq[a:b] @ Wd_q[e].T
+    return G, U, H, O
+
+
 def moe_forward_ref(x, w_router, bias, w_gate_up, w_down, k: int, routing=None,
                     keep=False, precision="fp64"):
     """y_t = sum_s p[t,s] * FFN_{e[t,s]}(x_t), summed in slot order.
@@ -266,9 +302,11 @@ def moe_forward_ref(x, w_router, bias, w_gate_up, w_down, k: int, routing=None,
     I = np.asarray(w_gate_up).shape[1] // 2
     O = np.zeros((R, d))
     G = np.zeros((R, I)); U = np.zeros((R, I)); H = np.zeros((R, I))
+    if precision == "nvfp4":
+        G, U, H, O = _nvfp4_experts(X, w_gate_up, w_down, offsets, tok, R)
     for e in range(E):
         a, b = int(offsets[e]), int(offsets[e + 1])
-        if a == b:
+        if a == b or precision == "nvfp4":
             continue
         G[a:b], U[a:b], H[a:b], O[a:b] = expert_ffn(X[tok[a:b]], w_gate_up[e], w_down[e], rnd,
                                                      mx=(precision == "mxfp8"))
@@ -323,7 +361,7 @@ def moe_backward_ref(x, w_router, bias, w_gate_up, w_down, k: int, dy,
     for s in range(k):
         row_p[pos[:, s]] = p[:, s]
     dO = row_p[:, None] * dY[row_t]
-    if precision == "mxfp8":
+    if precision in ("mxfp8", "nvfp4"):
         dp_rows = np.zeros(R)
     else:
         dp = np.einsum("tsd,td->ts", O[pos], dY)
@@ -355,6 +393,10 @@ def moe_backward_ref(x, w_router, bias, w_gate_up, w_down, k: int, dy,
                 dw_down[e][...] = _mx_rows(dYe).T @ (row_p[a:b, None] * H[a:b])
                 dw_gate_up[e][...] = dGU.T @ _mx_rows(Xe)
             continue
+        if precision == "nvfp4":
+            # router-weight gradient in the fused form, <dA, h> with dA the
+            # (unquantised) down dgrad: the forward's O is quantised
+            dp_rows[a:b] = ((dYe @ Wd) * H[a:b]).sum(axis=1)
         dH = dO[a:b] @ Wd                       # [rows, I]
         dG = rnd(dH * U[a:b] * silu_grad(G[a:b]))
         dU = rnd(dH * silu(G[a:b]))
@@ -365,7 +407,7 @@ def moe_backward_ref(x, w_router, bias, w_gate_up, w_down, k: int, dy,
             dw_gate_up[e][:I] = dG.T @ Xe
             dw_gate_up[e][I:] = dU.T @ Xe
 
-    if precision == "mxfp8":
+    if precision in ("mxfp8", "nvfp4"):
         dp = dp_rows[pos]
 
     # reverse-dispatch: sum each token's k rows in slot order

@@ -11,7 +11,12 @@ values, float32 scale per tensor).
     magnitude on the code 6, and every element within half a grid step (in
     units of the block's scale) of its value;
   * all-zero blocks and tensors stay zero; quantising along axis 0 is
-    quantising the transpose along axis 1.
+    quantising the transpose along axis 1;
+  * the layer's NVFP4 mode: with quantisation switched off it is the fp64
+    mode; W_down scaled by 2^3 scales y by 2^3 (the tensor scale absorbs it);
+    and the axis of each forward operand (x and W_gate_up along d, W_down and
+    h along I) by power-of-two scale covariance of rows below each tensor's
+    maximum; planted wrong axes fail these pins.
 """
 import numpy as np
 import pytest
@@ -124,3 +129,163 @@ def test_nvfp4_scales_are_e4m3_values():
     _, _, sb, _ = nvfp4_ref.nvfp4_quantize(rng.standard_normal((8, 64)), axis=1)
     assert np.array_equal(mx_ref.e4m3_round(sb), sb)
     assert (sb >= 0).all() and (sb <= 448).all()
+
+
+# ----------------------------------------------------------------------------
+# the layer's NVFP4 mode (moe_forward_ref(precision="nvfp4")): forward GEMM
+# operands quantised along their reduction dimension with whole-tensor scales;
+# h in bf16 before its quantisation; float64 backward with dp = <dy W_down, h>
+# ----------------------------------------------------------------------------
+
+import oracle  # noqa: E402
+from oracle import moe_ref  # noqa: E402
+
+D, I_ = 64, 96
+
+
+def _case(seed, T=64, E=2, gate_positive=False):
+    """Top-1 routing forced to T // E tokens per expert; the largest value of
+    x sits in token 0, of W_gate_up in row 0 and of W_down in row 0 of expert
+    0, so scaling other rows down by a power of two leaves every tensor scale
+    as it is."""
+    rng = np.random.default_rng(seed)
+    x = rng.uniform(1, 2, (T, D)) if gate_positive else rng.standard_normal((T, D))
+    wgu = rng.standard_normal((E, 2 * I_, D)) / np.sqrt(D)
+    if gate_positive:
+        wgu[:, :I_] = rng.uniform(1, 2, (E, I_, D))
+    wd = rng.standard_normal((E, D, I_)) / np.sqrt(I_)
+    x[0, 0] = 3 * np.abs(x).max()
+    wgu[0, 0, 0] = 3 * np.abs(wgu).max()
+    wd[0, 0, 0] = 3 * np.abs(wd).max()
+    idx = rng.permutation(np.repeat(np.arange(E), T // E)).astype(np.int32)[:, None]
+    return dict(x=x, w_router=rng.standard_normal((E, D)), w_gate_up=wgu, w_down=wd,
+                dy=rng.standard_normal((T, D)), routing=(idx, np.ones((T, 1))))
+
+
+def _fwd(c, precision="nvfp4"):
+    return oracle.moe_forward_ref(c["x"], c["w_router"], None, c["w_gate_up"], c["w_down"], 1,
+                                  routing=c["routing"], keep=True, precision=precision)
+
+
+def _scaled(before, after, mask, f, what):
+    want = np.where(mask, before * f, before)
+    np.testing.assert_allclose(after, want, rtol=1e-12,
+                               atol=1e-12 * float(np.sqrt(np.mean(want ** 2))), err_msg=what)
+
+
+def test_nvfp4_layer_without_quantisation_is_fp64(monkeypatch):
+    c = _case(30)
+    y64, f64 = _fwd(c, "fp64")
+    g64 = oracle.moe_backward_ref(c["x"], c["w_router"], None, c["w_gate_up"], c["w_down"], 1,
+                                  c["dy"], fwd=f64)
+    monkeypatch.setattr(moe_ref, "nvfp4_fake", lambda a, axis=-1: np.asarray(a, np.float64))
+    monkeypatch.setattr(moe_ref, "bf16_round", lambda a: np.asarray(a, np.float64))
+    yn, fn = _fwd(c)
+    gn = oracle.moe_backward_ref(c["x"], c["w_router"], None, c["w_gate_up"], c["w_down"], 1,
+                                 c["dy"], fwd=fn)
+    np.testing.assert_allclose(yn, y64, rtol=1e-12, atol=1e-12)
+    for n in ("dx", "dw_router", "dw_gate_up", "dw_down", "dp"):
+        np.testing.assert_allclose(gn[n], g64[n], rtol=1e-10, atol=1e-10, err_msg=n)
+
+
+def test_nvfp4_layer_is_fp64_plus_fp4_noise():
+    c = _case(31)
+    y64, _ = _fwd(c, "fp64")
+    yn, _ = _fwd(c)
+    rel = np.sqrt(np.mean((yn - y64) ** 2) / np.mean(y64 ** 2))
+    assert 1e-2 < rel < 0.5, rel
+
+
+def _pin_w_down_global_scale():
+    """W_down -> 2^3 W_down: its tensor scale absorbs the factor, so y -> 2^3 y."""
+    c = _case(32)
+    y0, _ = _fwd(c)
+    y1, _ = _fwd(dict(c, w_down=c["w_down"] * 8.0))
+    _scaled(y0, y1, True, 8.0, "y")
+
+
+def _pin_x_rows():
+    """Tokens (not token 0) -> 2^-2: x is quantised along d, so their g, u rows
+    scale by 2^-2."""
+    c = _case(33)
+    _, f0 = _fwd(c)
+    sel = (np.arange(64) % 3 == 1)
+    _, f1 = _fwd(dict(c, x=np.where(sel[:, None], c["x"] / 4, c["x"])))
+    rows = np.zeros(f0["G"].shape[0], dtype=bool)
+    rows[f0["pos"][sel, 0]] = True
+    _scaled(f0["G"], f1["G"], rows[:, None], 0.25, "G")
+    _scaled(f0["U"], f1["U"], rows[:, None], 0.25, "U")
+
+
+def _pin_w_gate_up_rows():
+    """W_gate_up rows (not row 0) -> 2^-1: quantised along d, so the matching
+    columns of g (or u) scale by 2^-1."""
+    c = _case(34)
+    _, f0 = _fwd(c)
+    n = np.zeros(2 * I_, dtype=bool)
+    n[[5, 40, I_ + 3, I_ + 77]] = True
+    w = c["w_gate_up"].copy()
+    w[:, n] /= 2
+    _, f1 = _fwd(dict(c, w_gate_up=w))
+    _scaled(f0["G"], f1["G"], n[None, :I_], 0.5, "G")
+    _scaled(f0["U"], f1["U"], n[None, I_:], 0.5, "U")
+
+
+def _pin_w_down_rows():
+    """W_down rows j (not 0) -> 2^-1: quantised along I, so y[:, j] scales."""
+    c = _case(35)
+    y0, _ = _fwd(c)
+    j = np.zeros(D, dtype=bool)
+    j[[3, 17, 50]] = True
+    w = c["w_down"].copy()
+    w[:, j] /= 2
+    y1, _ = _fwd(dict(c, w_down=w))
+    _scaled(y0, y1, j[None, :], 0.5, "y")
+
+
+def _pin_h_rows():
+    """Gate-positive regime (h = g u exactly): tokens (not token 0) -> 2^-1
+    scale their h rows by 2^-2; h is quantised along I, so their y rows scale
+    by 2^-2."""
+    c = _case(36, gate_positive=True)
+    y0, f0 = _fwd(c)
+    assert f0["G"].min() >= 64
+    sel = (np.arange(64) % 4 == 2)
+    y1, _ = _fwd(dict(c, x=np.where(sel[:, None], c["x"] / 2, c["x"])))
+    _scaled(y0, y1, sel[:, None], 0.25, "y")
+
+
+NV_PINS = {"w_down_global_scale": _pin_w_down_global_scale, "x_rows": _pin_x_rows,
+           "w_gate_up_rows": _pin_w_gate_up_rows, "w_down_rows": _pin_w_down_rows,
+           "h_rows": _pin_h_rows}
+
+
+@pytest.mark.parametrize("name", sorted(NV_PINS))
+def test_nvfp4_layer_quantisation_axes(name):
+    NV_PINS[name]()
+
+
+def _plant(monkeypatch, shape_tail, rows):
+    """nvfp4_fake along the rows instead of the columns for arrays whose
+    trailing dimension is shape_tail (and row count `rows`, if given)."""
+    real = nvfp4_ref.nvfp4_fake
+
+    def fake(a, axis=-1):
+        a = np.asarray(a)
+        if a.shape[-1] == shape_tail and (rows is None or a.shape[0] == rows) \
+                and axis % a.ndim == a.ndim - 1:
+            axis = 0
+        return real(a, axis)
+    monkeypatch.setattr(moe_ref, "nvfp4_fake", fake)
+
+
+@pytest.mark.parametrize("tail,rows,pin", [
+    (D, 64, "x_rows"),                   # x along the tokens
+    (D, 2 * 2 * I_, "w_gate_up_rows"),   # W_gate_up along 2I
+    (I_, 2 * D, "w_down_rows"),          # W_down along d
+    (I_, 64, "h_rows"),                  # h along the tokens
+])
+def test_planted_nvfp4_axis_is_caught(monkeypatch, tail, rows, pin):
+    _plant(monkeypatch, tail, rows)
+    with pytest.raises(AssertionError):
+        NV_PINS[pin]()
