@@ -60,8 +60,16 @@ typedef enum mok_status {
 
 typedef enum mok_dtype {
   MOK_BF16 = 0,  /* bf16 operands, fp32 accumulation, bf16 I/O */
-  MOK_MXFP8 = 1  /* expert GEMMs on MXFP8 operands: E4M3 with one E8M0 scale per 32
+  MOK_MXFP8 = 1, /* expert GEMMs on MXFP8 operands: E4M3 with one E8M0 scale per 32
                     values along K, fp32 accumulation (see mok_moe_forward) */
+  MOK_NVFP4 = 2  /* forward expert GEMMs on NVFP4 operands (see mok_nvfp4_quantize):
+                    x, W_gate_up along d and h, W_down along I, each with its
+                    tensor scale over the whole tensor; h rounded to bf16 before
+                    its quantisation; the backward as in MOK_BF16, with
+                    dp = <dy W_down, h>.  d and I multiples of 256; CTA-pair
+                    GEMMs only (MOK_FLAG_SINGLE_CTA_GEMM and
+                    MOK_FLAG_RECOMPUTE_GATE_UP unsupported); no dispatched rows
+                    are kept in saved */
 } mok_dtype;
 
 /* Output dtypes.  By default y, dx and the three weight gradients are fp32

@@ -11,7 +11,7 @@ import torch
 
 from . import _lib
 
-BF16, MXFP8 = 0, 1
+BF16, MXFP8, NVFP4 = 0, 1, 2
 FLAG_BF16_ACT_OUT = 0x1    # y and dx written as bf16 (default fp32)
 FLAG_BF16_WGRAD_OUT = 0x2  # weight gradients written as bf16 (default fp32)
 FLAG_ACCUMULATE_WGRAD = 0x4  # backward adds into the fp32 weight gradients

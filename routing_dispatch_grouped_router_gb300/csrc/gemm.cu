@@ -60,7 +60,13 @@ enum Epi : int {
 // SPLIT_MX: not a split but the MXFP8 operand mode: A and B are E4M3 codes
 // (K-major, 128 K values per stage) with one E8M0 scale byte per 32 K values,
 // multiplied by tcgen05.mma.kind::mxf8f6f4.block_scale (single CTA, BN=128).
-enum Split : int { SPLIT_NONE = 0, SPLIT_A = 1, SPLIT_B = 2, SPLIT_MX = 3 };
+// SPLIT_NV: the NVFP4 operand mode (CTA pairs only): A and B are packed E2M1
+// codes (K-major, 256 K values = 128 bytes per stage) with one E4M3 scale per
+// 16 K values, multiplied by tcgen05.mma.kind::mxf4nvf4.block_scale
+// (scale_vec::4X); the tensor scales of A and B multiply the accumulator in
+// the epilogue.
+enum Split : int { SPLIT_NONE = 0, SPLIT_A = 1, SPLIT_B = 2, SPLIT_MX = 3, SPLIT_NV = 4 };
+constexpr bool block_scaled(int split) { return split == SPLIT_MX || split == SPLIT_NV; }
 
 struct GemmArgs {
   int E;             // groups (experts); 1 for dense
@@ -85,7 +91,9 @@ struct GemmArgs {
   int mx;                   // SwiGLU epilogues: quantise the derived GEMM operands to MXFP8
   const uint8_t* sa;        // SPLIT_MX: A scale bytes, tiled layout (mx_tiled_off)
   const uint8_t* sb;        // SPLIT_MX: B scale bytes, tiled layout
-  int ks;                   // SPLIT_MX: K / 32 (scale bytes per row)
+  int ks;                   // SPLIT_MX: K / 32 (scale bytes per row); SPLIT_NV: K / 64
+  const float* ga;          // SPLIT_NV: device tensor scale of A
+  const float* gb;          // SPLIT_NV: device tensor scale of B
   uint8_t* h_codes;         // SWIGLU_FWD with SPLIT_MX: h as E4M3 codes [rows, I] (NULL: none)
   uint8_t* h_scales;        // ... and its E8M0 bytes (tiled layout, mx_tiled_off)
   int accumulate;           // fp32 TMA-store epilogue: add into C instead of overwriting
@@ -161,18 +169,23 @@ struct Cfg {
   // 512-byte scale blocks of the stage (A's 128 rows, B's 128 rows)
   static constexpr int SF_OFF = A_TILES * A_BYTES + B_TILES * B_BYTES;
   // (CTA pairs: the CTA's 128 A rows, and all 256 B rows of the pair's tile)
-  static constexpr int SF_BYTES = SPLIT != SPLIT_MX ? 0 : (PAIR ? 1536 : 1024);
+  // SPLIT_NV (pairs): four 512-byte blocks per 128 rows (one per K = 64 MMA):
+  // 2 KB for the CTA's A rows, 4 KB for the 256 B rows
+  static constexpr int SF_BYTES =
+      SPLIT == SPLIT_MX ? (PAIR ? 1536 : 1024) : (SPLIT == SPLIT_NV ? 6144 : 0);
   static constexpr int STAGE_BYTES =
-      SPLIT == SPLIT_MX ? (SF_OFF + SF_BYTES + 1023) / 1024 * 1024 : SF_OFF;
-  // accumulators; MXFP8 pairs keep one (256 columns) so that the stages'
-  // scale columns fit beside it (12 per stage: 4 for A, 8 for B)
-  static constexpr int NACC = (SPLIT == SPLIT_MX && PAIR) ? 1 : 2;
-  static constexpr int SF_COLS = SPLIT != SPLIT_MX ? 0 : (PAIR ? 12 : 8);
+      block_scaled(SPLIT) ? (SF_OFF + SF_BYTES + 1023) / 1024 * 1024 : SF_OFF;
+  // accumulators; block-scaled pairs keep one (256 columns) so that the
+  // stages' scale columns fit beside it (MXFP8: 12 per stage, 4 for A and 8
+  // for B; NVFP4: 48, 16 for A and 32 for B)
+  static constexpr int NACC = (block_scaled(SPLIT) && PAIR) ? 1 : 2;
+  static constexpr int SF_COLS =
+      SPLIT == SPLIT_MX ? (PAIR ? 12 : 8) : (SPLIT == SPLIT_NV ? 48 : 0);
   static constexpr int BAR_BYTES = 512;
   static constexpr int STAGE_ROOM = 232448 - 1024 - BAR_BYTES - kEpiWarps * STG;
   static constexpr int STAGES = (STAGE_ROOM / STAGE_BYTES) < 6 ? (STAGE_ROOM / STAGE_BYTES) : 6;
   // SPLIT_MX: after the accumulators, 8 columns of scales per stage
-  static constexpr int TMEM_COLS = SPLIT == SPLIT_MX ? 512 : 2 * BN;
+  static constexpr int TMEM_COLS = block_scaled(SPLIT) ? 512 : 2 * BN;
   static constexpr int STAGING_OFF = STAGES * STAGE_BYTES;
   static constexpr int STAGING_PER_WARP = STG;
   static constexpr int BAR_OFF = STAGING_OFF + kEpiWarps * STG;
@@ -193,6 +206,10 @@ static_assert(Cfg<256, SPLIT_NONE, false, kSwigluBwdStaging>::STAGES >= 2 &&
 static_assert(Cfg<128, SPLIT_MX>::STAGES == 5 && Cfg<128, SPLIT_MX>::STAGE_BYTES % 1024 == 0 &&
                   2 * 128 + 8 * Cfg<128, SPLIT_MX>::STAGES <= 512,
               "MXFP8 stages");
+static_assert(Cfg<256, SPLIT_NV, true>::STAGES == 5 &&
+                  Cfg<256, SPLIT_NV, true>::STAGE_BYTES % 1024 == 0 &&
+                  256 + 48 * Cfg<256, SPLIT_NV, true>::STAGES <= 512,
+              "NVFP4 pair stages");
 static_assert(Cfg<256, SPLIT_MX, true>::STAGES == 5 &&
                   Cfg<256, SPLIT_MX, true>::STAGE_BYTES % 1024 == 0 &&
                   256 + 12 * Cfg<256, SPLIT_MX, true>::STAGES <= 512,
@@ -545,6 +562,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
   constexpr int HALF_COLS = BN / 2;
   const int row_in_tile = q * 32 + lane;
   const bool zero_k = (tl.num_kb == 0);
+  // NVFP4: the product of the operands' tensor scales (the block scales were
+  // applied by the tensor cores)
+  const float alpha = SPLIT == SPLIT_NV ? __ldg(a.ga) * __ldg(a.gb) : 1.0f;
   if ((EPI == EPI_F32 || EPI == EPI_BF16_TMA) && SCHED != SCHED_DENSE) {
     // fp32 (or bf16) C through TMA stores; C viewed as 2-D [rows, N]
     const int y = (SCHED == SCHED_KGROUP ? tl.e * a.m_rows : 0) + tl.row0 + q * 32;
@@ -569,6 +589,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
         float v[32];
         if (!zero_k) {
           tmem_ld32(taddr + half * HALF_COLS + c, v);
+          if (SPLIT == SPLIT_NV) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] *= alpha;
+          }
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = 0.f;
@@ -673,6 +697,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
       float g[32], u[32];
       tmem_ld32(taddr + half * 64 + c, g);
       tmem_ld32(taddr + 128 + half * 64 + c, u);
+      if (SPLIT == SPLIT_NV) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          g[j] *= alpha;
+          u[j] *= alpha;
+        }
+      }
       if (SPLIT == SPLIT_MX ? a.h_codes != nullptr : a.out2 != nullptr) {
         float hv[32];
 #pragma unroll
@@ -861,7 +892,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(SPLIT != SPLIT_MX ||
                     (!A_MN && !B_MN && BN == (PAIR ? 256 : 128) && SCHED == SCHED_MGROUP),
                 "MXFP8 operands: K-major, 128-wide tiles (256 on CTA pairs)");
-  constexpr int KX = SPLIT == SPLIT_MX ? 128 : 64;  // K values per stage
+  static_assert(SPLIT != SPLIT_NV || (PAIR && BN == 256 && !A_MN && !B_MN &&
+                                      SCHED == SCHED_MGROUP &&
+                                      (EPI == EPI_SWIGLU_FWD || EPI == EPI_F32)),
+                "NVFP4 operands: K-major, M-grouped, CTA pairs");
+  // TMA x coordinate per stage: K values (bf16), code bytes (MXFP8, NVFP4)
+  constexpr int KX = block_scaled(SPLIT) ? 128 : 64;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -908,7 +944,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (kTmaStore) tma_prefetch_desc(&tmC);
-    if (SPLIT == SPLIT_MX && PAIR) {
+    if (block_scaled(SPLIT) && PAIR) {
       tma_prefetch_desc(&om.sfa);
       tma_prefetch_desc(&om.sfb);
     }
@@ -1019,7 +1055,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else if (leader) {
             if (lane == 0)
               mbar_arrive_expect_tx(&full[stage],
-                                    2 * (C::SF_OFF + (SPLIT == SPLIT_MX ? C::SF_BYTES : 0)));
+                                    2 * (C::SF_OFF + (block_scaled(SPLIT) ? C::SF_BYTES : 0)));
           }
           if (PAIR && SPLIT == SPLIT_MX) {
             // scale blocks by TMA: this CTA's A rows, and all BN rows of B
@@ -1031,6 +1067,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  ? tl.e * args.b_group_rows + tl.n_tile * 128 + (blk ? args.I : 0)
                                  : tl.e * args.b_group_rows + tl.n_tile * BN + blk * 128;
               load(sA + C::SF_OFF + 512 + blk * 512, &om.sfb, 0, 2 * ((g0 >> 7) * nkg + kg));
+            }
+          }
+          if (PAIR && SPLIT == SPLIT_NV) {
+            // the stage's four scale blocks per 128 rows (2 KB, one TMA copy
+            // each): this CTA's A rows, and both 128-row halves of B
+            const int nkb = args.ks, k4 = 4 * (tl.kb0 + kb);
+            load(sA + C::SF_OFF, &om.sfa, 0, 2 * ((tl.row0 >> 7) * nkb + k4));
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk) {
+              const int g0 = EPI == EPI_SWIGLU_FWD
+                                 ? tl.e * args.b_group_rows + tl.n_tile * 128 + (blk ? args.I : 0)
+                                 : tl.e * args.b_group_rows + tl.n_tile * BN + blk * 128;
+              load(sA + C::SF_OFF + 2048 + blk * 2048, &om.sfb, 0, 2 * ((g0 >> 7) * nkb + k4));
             }
           }
           // A tile: 128 rows (M) x 64 (K)  (+ its lo tile with SPLIT_A)
@@ -1133,7 +1182,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after_sync();
           const uint32_t a_base = smem_addr(tiles + stage * C::STAGE_BYTES);
           const uint32_t b_base = a_base + C::B_OFF;
-          if constexpr (SPLIT == SPLIT_MX) {
+          if constexpr (SPLIT == SPLIT_NV) {
+            // per K = 64 MMA j: the A scale block to 4 columns, the two B
+            // half blocks to 8 (rows 0..127, then 128..255), each CTA's
+            // blocks to its own TMEM; then the block-scaled FP4 MMA
+            const uint32_t sfa = tmem_base + C::NACC * BN + C::SF_COLS * stage;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              tmem_cp_sf_pair(sfa + 4u * j, smem_desc_sf(a_base + C::SF_OFF + 512 * j));
+              tmem_cp_sf_pair(sfa + 16u + 8u * j,
+                              smem_desc_sf(a_base + C::SF_OFF + 2048 + 512 * j));
+              tmem_cp_sf_pair(sfa + 20u + 8u * j,
+                              smem_desc_sf(a_base + C::SF_OFF + 4096 + 512 * j));
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint64_t ad = smem_desc_sw128(a_base + j * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(b_base + j * 32, 16, 1024);
+              mma_nvf4_pair(d_tmem, ad, bd, idesc_nvf4(256, BN), sfa + 4u * j,
+                            sfa + 16u + 8u * j, (kb | j) != 0 ? 1u : 0u);
+            }
+          } else if constexpr (SPLIT == SPLIT_MX) {
             // scales to TMEM (SF_COLS columns per stage after the
             // accumulators), then four K=32 block-scaled MMAs, scale byte j
             // each; CTA pairs copy each CTA's blocks to its own TMEM
@@ -1536,6 +1605,90 @@ cudaError_t gemm_fwd_down_mx(const Dims& D, const uint8_t* h_codes, const uint8_
                              int* status, cudaStream_t st) {
   return grouped_mx_f32("fwd_down", D, D.I, h_codes, h_scales, wd_codes, wd_scales, mtile_prefix,
                         poff, O, status, st);
+}
+
+// NVFP4 scales in the tiled layout (one 512-byte block per 128 rows x 64 K
+// values, the four blocks of a 256-value stage consecutive) as a TMA map of
+// 256-byte rows: one stage's blocks of a 128-row tile are a 2 KB box.
+static bool make_nv_sf_map(CUtensorMap* m, const uint8_t* scales, int64_t rows, int64_t K) {
+  const uint64_t blocks = static_cast<uint64_t>(rows / 128) * static_cast<uint64_t>(K / 64);
+  return make_map_t(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, scales, 256, 2 * blocks, 256, 256, 8,
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// NVFP4 operands (packed E2M1 codes [rows, K/2] K-major, tiled E4M3 scales,
+// device tensor scales): the gate/up GEMM with fp32 g, u to GU and bf16 h to
+// H, on CTA pairs (256 rows x 128 FFN columns of gate and of up per tile).
+cudaError_t gemm_fwd_gate_up_nv(const Dims& D, const uint8_t* x_codes, const uint8_t* x_scales,
+                                const float* x_g, const uint8_t* wgu_codes,
+                                const uint8_t* wgu_scales, const float* wgu_g,
+                                const int32_t* mtile_prefix, const int32_t* poff, void* GU,
+                                void* H, int* status, cudaStream_t st) {
+  const auto u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  if (D.d % 256 || D.I % 128 || !GU || !H) return cudaErrorInvalidValue;
+  CUtensorMap ta, tb, tc;
+  if (!make_map_t(&ta, u8, 1, x_codes, D.d / 2, D.rows_max, D.d / 2, 128, 128, sw) ||
+      !make_map_t(&tb, u8, 1, wgu_codes, D.d / 2, D.E * 2 * D.I, D.d / 2, 128, 128, sw) ||
+      !make_out_map(&tc, GU, 2 * D.I, D.rows_max))
+    return cudaErrorInvalidValue;
+  GemmArgs a = blank_args(status);
+  a.store_c = 1;
+  a.evict_first = 1;
+  a.E = (int)D.E;
+  a.n_tiles = (int)(D.I / 128);
+  a.num_kb = (int)(D.d / 256);
+  a.b_group_rows = (int)(2 * D.I);
+  a.I = (int)D.I;
+  a.mtile_prefix = mtile_prefix;
+  a.poff = poff;
+  a.out = GU;
+  a.out2 = H;
+  a.ks = (int)(D.d / 64);
+  a.ga = x_g;
+  a.gb = wgu_g;
+  OutMaps om;
+  memset(&om, 0, sizeof(om));
+  if (!make_nv_sf_map(&om.sfa, x_scales, D.rows_max, D.d) ||
+      !make_nv_sf_map(&om.sfb, wgu_scales, D.E * 2 * D.I, D.d))
+    return cudaErrorInvalidValue;
+  return launch<256, false, false, SCHED_MGROUP, EPI_SWIGLU_FWD, SPLIT_NV, true>(
+      "fwd_gate_up_swiglu", ta, tb, tc, a, max_mpairs(D) * a.n_tiles, st, nullptr, &om);
+}
+
+// NVFP4 operands: the down projection O[rows_max, d] (fp32) = h W_down_e^T per
+// expert segment, on CTA pairs (256 x 256 tiles).
+cudaError_t gemm_fwd_down_nv(const Dims& D, const uint8_t* h_codes, const uint8_t* h_scales,
+                             const float* h_g, const uint8_t* wd_codes, const uint8_t* wd_scales,
+                             const float* wd_g, const int32_t* mtile_prefix, const int32_t* poff,
+                             void* O, int* status, cudaStream_t st) {
+  const auto u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  if (D.d % 256 || D.I % 256) return cudaErrorInvalidValue;
+  CUtensorMap ta, tb, tc;
+  if (!make_map_t(&ta, u8, 1, h_codes, D.I / 2, D.rows_max, D.I / 2, 128, 128, sw) ||
+      !make_map_t(&tb, u8, 1, wd_codes, D.I / 2, D.E * D.d, D.I / 2, 128, 128, sw) ||
+      !make_out_map(&tc, O, D.d, D.rows_max))
+    return cudaErrorInvalidValue;
+  GemmArgs a = blank_args(status);
+  a.E = (int)D.E;
+  a.n_tiles = (int)(D.d / 256);
+  a.num_kb = (int)(D.I / 256);
+  a.b_group_rows = (int)D.d;
+  a.mtile_prefix = mtile_prefix;
+  a.poff = poff;
+  a.out = O;
+  a.ldo = D.d;
+  a.ks = (int)(D.I / 64);
+  a.ga = h_g;
+  a.gb = wd_g;
+  OutMaps om;
+  memset(&om, 0, sizeof(om));
+  if (!make_nv_sf_map(&om.sfa, h_scales, D.rows_max, D.I) ||
+      !make_nv_sf_map(&om.sfb, wd_scales, D.E * D.d, D.I))
+    return cudaErrorInvalidValue;
+  return launch<256, false, false, SCHED_MGROUP, EPI_F32, SPLIT_NV, true>(
+      "fwd_down", ta, tb, tc, a, max_mpairs(D) * a.n_tiles, st, nullptr, &om);
 }
 
 cudaError_t gemm_bwd_gate_up_dgrad_mx(const Dims& D, const uint8_t* dgu_codes,

@@ -91,7 +91,12 @@ mok_status make_dims(const mok_moe_desc* desc, Dims* out) {
   if (!desc || !out) return MOK_ERR_INVALID_ARG;
   const mok_moe_desc& d = *desc;
   if (d.T < 0 || d.d <= 0 || d.E <= 0 || d.I <= 0 || d.k <= 0) return MOK_ERR_INVALID_ARG;
-  if (d.dtype != MOK_BF16 && d.dtype != MOK_MXFP8) return MOK_ERR_UNSUPPORTED;
+  if (d.dtype != MOK_BF16 && d.dtype != MOK_MXFP8 && d.dtype != MOK_NVFP4)
+    return MOK_ERR_UNSUPPORTED;
+  if (d.dtype == MOK_NVFP4 &&
+      ((d.flags & (MOK_FLAG_SINGLE_CTA_GEMM | MOK_FLAG_RECOMPUTE_GATE_UP)) || d.d % 256 ||
+       d.I % 256))
+    return MOK_ERR_UNSUPPORTED;
   if (d.mb_tokens < 0 || d.ring_slots < 0) return MOK_ERR_INVALID_ARG;
   if (d.flags & ~(MOK_FLAG_BF16_ACT_OUT | MOK_FLAG_BF16_WGRAD_OUT | MOK_FLAG_ACCUMULATE_WGRAD |
                   MOK_FLAG_RECOMPUTE_GATE_UP | MOK_FLAG_SINGLE_CTA_GEMM |
@@ -135,7 +140,10 @@ mok_status make_dims(const mok_moe_desc* desc, Dims* out) {
   D.accumulate = (d.flags & MOK_FLAG_ACCUMULATE_WGRAD) != 0;
   D.recompute_gu = (d.flags & MOK_FLAG_RECOMPUTE_GATE_UP) != 0;
   D.pair = (d.flags & MOK_FLAG_SINGLE_CTA_GEMM) == 0;
-  D.recompute_dispatch = (d.flags & MOK_FLAG_RECOMPUTE_DISPATCH) != 0 && !D.mx;
+  D.nv = d.dtype == MOK_NVFP4;
+  // NVFP4 quantises the token rows through the row map and keeps no
+  // dispatched rows; its BF16 backward gathers them again
+  D.recompute_dispatch = ((d.flags & MOK_FLAG_RECOMPUTE_DISPATCH) != 0 && !D.mx) || D.nv;
   // every row index and element offset used in 32-bit arithmetic must fit
   if (D.rows_max * 2 * D.I >= (1LL << 40)) return MOK_ERR_UNSUPPORTED;
   if (D.rows_max >= (1LL << 31) / 2) return MOK_ERR_UNSUPPORTED;
@@ -214,7 +222,7 @@ void fwd_layout(const Dims& D, FwdWs* W) {
   W->block_counts = b.take(static_cast<size_t>(D.nb) * D.E * 4);
   W->block_base = b.take(static_cast<size_t>(D.nb) * D.E * 4);
   W->h = D.mx ? 0 : b.take(rows * D.I * 2);  // bf16 h (MXFP8: codes below)
-  W->x_perm = D.recompute_dispatch ? b.take(rows * D.d * 2) : 0;
+  W->x_perm = (D.recompute_dispatch && !D.nv) ? b.take(rows * D.d * 2) : 0;
   W->o = b.take(rows * D.d * 4);  // fp32 expert outputs
   W->logits = b.take(static_cast<size_t>(D.T) * D.E * 4 * router_k_splits(D));
   const size_t wgu = static_cast<size_t>(D.E) * 2 * D.I * D.d;  // elements
@@ -227,6 +235,15 @@ void fwd_layout(const Dims& D, FwdWs* W) {
   mx(rows * D.I, &W->h_codes, &W->h_scales);
   mx(wgu, &W->wgu_codes, &W->wgu_scales);
   mx(wd, &W->wd_codes, &W->wd_scales);
+  auto nv = [&](size_t elems, size_t* codes, size_t* scales) {
+    *codes = D.nv ? b.take(elems / 2) : 0;
+    *scales = D.nv ? b.take(elems / 16) : 0;
+  };
+  nv(rows * D.d, &W->nxq_codes, &W->nxq_scales);
+  nv(rows * D.I, &W->nh_codes, &W->nh_scales);
+  nv(wgu, &W->nwgu_codes, &W->nwgu_scales);
+  nv(wd, &W->nwd_codes, &W->nwd_scales);
+  W->nv_g = D.nv ? b.take(256) : 0;
   W->total = b.o;
 }
 
@@ -390,6 +407,24 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
     MOK_CUDA(launch_mx_rows(w_gate_up, nullptr, D.E * 2 * D.I, D.d, wgu_c, wgu_s, st, true));
     MOK_CUDA(launch_mx_rows(w_down, nullptr, D.E * D.d, D.I, wd_c, wd_s, st, true));
   }
+  // NVFP4: tensor scales [x, h, W_gate_up, W_down]; the weights once per call
+  float* nvg = D.nv ? at<float>(workspace, F.nv_g) : nullptr;
+  uint8_t* nxq_c = at<uint8_t>(workspace, F.nxq_codes);
+  uint8_t* nxq_s = at<uint8_t>(workspace, F.nxq_scales);
+  uint8_t* nh_c = at<uint8_t>(workspace, F.nh_codes);
+  uint8_t* nh_s = at<uint8_t>(workspace, F.nh_scales);
+  uint8_t* nwgu_c = at<uint8_t>(workspace, F.nwgu_codes);
+  uint8_t* nwgu_s = at<uint8_t>(workspace, F.nwgu_scales);
+  uint8_t* nwd_c = at<uint8_t>(workspace, F.nwd_codes);
+  uint8_t* nwd_s = at<uint8_t>(workspace, F.nwd_scales);
+  if (D.nv) {
+    MOK_CUDA(launch_nv_tensor_scale(w_gate_up, D.E * 2 * D.I * D.d, nvg + 2, st));
+    MOK_CUDA(launch_nv_quant_tiled(w_gate_up, D.E * 2 * D.I, D.d, nvg + 2, nwgu_c, nwgu_s,
+                                   nullptr, 0, st));
+    MOK_CUDA(launch_nv_tensor_scale(w_down, D.E * D.d * D.I, nvg + 3, st));
+    MOK_CUDA(launch_nv_quant_tiled(w_down, D.E * D.d, D.I, nvg + 3, nwd_c, nwd_s, nullptr, 0,
+                                   st));
+  }
   const size_t y_esz = D.act_bf16 ? 2 : 4;
   float* logits = at<float>(workspace, F.logits);
   void* h = D.mx ? nullptr : at<char>(workspace, F.h);
@@ -423,9 +458,23 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
                                           : at<char>(saved, L.x_perm + (i % D.ring) *
                                                                 L.ring_slot_bytes);
     void* gu = D.recompute_gu ? nullptr : at<char>(saved, L.gate_up + blk);
-    if (!D.mx)
+    if (!D.mx && !D.nv)
       MOK_CUDA(launch_dispatch_rows(D, xi, o.ppos, o.ptok, o.padded_offsets, x_perm, status, st));
-    if (D.mx) {
+    if (D.nv) {
+      // expert GEMMs on the block-scaled FP4 tensor cores: the x rows go to
+      // NVFP4 straight from the token rows; h is written in bf16, then gets
+      // its tensor scale (over the plan's rows) and its codes
+      MOK_CUDA(launch_nv_tensor_scale(xi, D.T * D.d, nvg + 0, st));
+      MOK_CUDA(launch_nv_quant_tiled(xi, D.rows_max, D.d, nvg + 0, nxq_c, nxq_s, o.ptok,
+                                     static_cast<int>(D.T), st));
+      MOK_CUDA(gemm_fwd_gate_up_nv(D, nxq_c, nxq_s, nvg + 0, nwgu_c, nwgu_s, nvg + 2,
+                                   o.mtile_prefix, o.padded_offsets, gu, h, status, st));
+      MOK_CUDA(launch_nv_tensor_scale(h, D.rows_max * D.I, nvg + 1, st,
+                                      o.padded_offsets + D.E, D.I));
+      MOK_CUDA(launch_nv_quant_tiled(h, D.rows_max, D.I, nvg + 1, nh_c, nh_s, nullptr, 0, st));
+      MOK_CUDA(gemm_fwd_down_nv(D, nh_c, nh_s, nvg + 1, nwd_c, nwd_s, nvg + 3, o.mtile_prefix,
+                                o.padded_offsets, O, status, st));
+    } else if (D.mx) {
       // expert GEMMs on the block-scaled tensor cores: the dispatched x rows
       // go to MXFP8 straight from the token rows (no bf16 copy), the gate/up
       // GEMM writes h as MXFP8 for the down projection

@@ -35,6 +35,7 @@ struct Dims {
   bool mx;           // MXFP8 expert GEMM operands
   bool accumulate;   // backward adds into the weight gradients
   bool recompute_gu; // g, u not kept: the backward recomputes them
+  bool nv;           // NVFP4 forward expert GEMMs (backward on the BF16 path)
   bool recompute_dispatch;  // BF16: dispatched x rows not kept in saved;
                             // the backward dispatches them again
   bool pair;         // grouped GEMMs with 256-row tiles on CTA pairs (2-SM MMA)
@@ -60,6 +61,10 @@ struct BlockL {
 struct FwdWs {
   size_t front_sync, block_counts, block_base, h, o, logits;
   size_t x_perm;  // dispatched x rows when saved keeps none (recompute_dispatch)
+  // NVFP4: codes and tiled scales of the x rows, h, W_gate_up, W_down, and
+  // the four fp32 tensor scales (x, h, W_gate_up, W_down)
+  size_t nxq_codes, nxq_scales, nh_codes, nh_scales, nwgu_codes, nwgu_scales, nwd_codes,
+      nwd_scales, nv_g;
   // MXFP8: E4M3 codes and E8M0 scale bytes of x rows, h, W_gate_up, W_down
   size_t xq_codes, xq_scales, h_codes, h_scales, wgu_codes, wgu_scales, wd_codes, wd_scales;
   size_t total;
@@ -177,6 +182,17 @@ cudaError_t gemm_fwd_gate_up_mx(const Dims& D, const uint8_t* x_codes, const uin
                                 const int32_t* mtile_prefix, const int32_t* poff, void* GU,
                                 uint8_t* h_codes, uint8_t* h_scales, int* status,
                                 cudaStream_t st);
+// NVFP4 forward GEMMs on CTA pairs (gemm.cu): packed E2M1 codes [rows, K/2],
+// tiled E4M3 scales (launch_nv_quant_tiled), device tensor scales.
+cudaError_t gemm_fwd_gate_up_nv(const Dims& D, const uint8_t* x_codes, const uint8_t* x_scales,
+                                const float* x_g, const uint8_t* wgu_codes,
+                                const uint8_t* wgu_scales, const float* wgu_g,
+                                const int32_t* mtile_prefix, const int32_t* poff, void* GU,
+                                void* H, int* status, cudaStream_t st);
+cudaError_t gemm_fwd_down_nv(const Dims& D, const uint8_t* h_codes, const uint8_t* h_scales,
+                             const float* h_g, const uint8_t* wd_codes, const uint8_t* wd_scales,
+                             const float* wd_g, const int32_t* mtile_prefix, const int32_t* poff,
+                             void* O, int* status, cudaStream_t st);
 cudaError_t gemm_fwd_down_mx(const Dims& D, const uint8_t* h_codes, const uint8_t* h_scales,
                              const uint8_t* wd_codes, const uint8_t* wd_scales,
                              const int32_t* mtile_prefix, const int32_t* poff, void* O,
@@ -250,6 +266,18 @@ cudaError_t launch_mx_cols_t(const void* in, long long rows, long long cols, lon
 cudaError_t launch_mx_cols(const void* in, void* out, long long rows, long long cols,
                            uint8_t* codes, uint8_t* scales, cudaStream_t st,
                            void* rows_out = nullptr, const int32_t* rowmap = nullptr, int T = 0);
+
+// NVFP4 (nvfp4.cu): the tensor scale of n bf16 values into the device *g
+// (which the call also uses as scratch), and codes [rows, cols/2] with E4M3
+// block scales in the tiled layout (one 512-byte block per 128 rows x 64
+// values, consecutive along K) of bf16 [rows, cols] or, with `map`, of the
+// rows map[r] of a [T, cols] input (zeros where map[r] is not in [0, T)).
+// rows_dev (or NULL): only the first *rows_dev rows of row_elems values count.
+cudaError_t launch_nv_tensor_scale(const void* in, long long n, float* g, cudaStream_t st,
+                                   const int32_t* rows_dev = nullptr, long long row_elems = 0);
+cudaError_t launch_nv_quant_tiled(const void* in, long long rows, long long cols, const float* g,
+                                  uint8_t* codes, uint8_t* scales, const int32_t* map, int T,
+                                  cudaStream_t st);
 
 // One CTA whose mbarrier wait can never complete: exercises the bounded wait.
 cudaError_t launch_bounded_wait_selftest(int* status, cudaStream_t st);

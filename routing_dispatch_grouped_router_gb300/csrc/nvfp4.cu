@@ -38,11 +38,32 @@ namespace {
 
 // ------------------------------------------------------------- quantiser --
 
+}  // namespace
+
+// Byte of the scale of row r, 16-value block c16, in the tiled layout of a
+// matrix with 64 * nkb columns: one 512-byte block per 128 rows x 64 values,
+// the blocks of a 128-row tile consecutive along K, and inside a block row r
+// at byte 16 * (r % 32) + 4 * ((r / 32) % 4) + c16 % 4 -- the arrangement
+// the 32x128b scale copy to TMEM takes, so a CTA loads a stage's blocks with
+// one TMA copy.
+static __host__ __device__ inline long long nv_tiled_off(long long r, long long c16,
+                                                        long long nkb) {
+  return ((r >> 7) * nkb + (c16 >> 2)) * 512 + 16 * (r & 31) + 4 * ((r >> 5) & 3) + (c16 & 3);
+}
+
+namespace {
+
 // amax of the tensor as the bits of a non-negative float (the integer order of
 // such bits is their value order, so atomicMax takes the maximum whatever the
 // order of the updates).
 __global__ void nv_amax_kernel(const uint4* __restrict__ in, long long nchunks,
-                               unsigned* __restrict__ amax_bits) {
+                               unsigned* __restrict__ amax_bits,
+                               const int32_t* __restrict__ rows_dev, long long row_chunks) {
+  // rows_dev (or NULL): only the first *rows_dev rows of row_chunks chunks
+  if (rows_dev) {
+    const long long lim = static_cast<long long>(*rows_dev) * row_chunks;
+    nchunks = lim < nchunks ? lim : nchunks;
+  }
   float m = 0.f;
   const long long G = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < nchunks;
@@ -76,15 +97,33 @@ __device__ __forceinline__ uint8_t cvt_e2m1x2(float hi, float lo) {
 
 // One thread per block of 16 values along a row: 8 code bytes (value 2i in
 // the low nibble of byte i, 2i+1 in the high one) and one E4M3 scale byte.
-__global__ void nv_quant_kernel(const uint4* __restrict__ in, long long nblk,
+// tiled_nkb > 0: the scale bytes go to the tiled layout of a matrix with
+// 64 * tiled_nkb columns (nv_tiled_off); 0: row-major [rows, cols/16].
+// map (or NULL): output row r takes input row map[r] when that is a row of
+// the input (0 <= map[r] < T), zeros otherwise (codes 0, scale 0).
+__global__ void nv_quant_kernel(const uint4* __restrict__ in, long long nblk, int blk_per_row,
                                 const float* __restrict__ g_ptr, uint8_t* __restrict__ codes,
-                                uint8_t* __restrict__ scales) {
+                                uint8_t* __restrict__ scales, long long tiled_nkb,
+                                const int32_t* __restrict__ map, int T) {
   const float g = *g_ptr;
   const float six_g = 6.0f * g;
   const long long G = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long b = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; b < nblk;
        b += G) {
-    const uint4 w0 = in[2 * b], w1 = in[2 * b + 1];
+    const long long r = b / blk_per_row;
+    const int c16 = static_cast<int>(b - r * blk_per_row);
+    long long src = b;
+    bool zero = false;
+    if (map) {
+      const int t = map[r];
+      zero = !(t >= 0 && t < T);
+      src = static_cast<long long>(zero ? 0 : t) * blk_per_row + c16;
+    }
+    uint4 w0 = make_uint4(0u, 0u, 0u, 0u), w1 = w0;
+    if (!zero) {
+      w0 = in[2 * src];
+      w1 = in[2 * src + 1];
+    }
     const uint32_t u[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
     float v[16];
     float amax = 0.f;
@@ -108,7 +147,7 @@ __global__ void nv_quant_kernel(const uint4* __restrict__ in, long long nblk,
       }
     }
     *reinterpret_cast<uint2*>(codes + 8 * b) = make_uint2(c[0], c[1]);
-    scales[b] = sb;
+    scales[tiled_nkb > 0 ? nv_tiled_off(r, c16, tiled_nkb) : b] = sb;
   }
 }
 
@@ -126,28 +165,6 @@ constexpr int kNvThreads = 192;
 // (four columns per MMA step) and B scales at 144 + 32s
 constexpr uint32_t kNvTmemCols = 256;
 constexpr int kNvSmem = 1024 + kNvStages * kNvStageBytes + 256;
-
-// Instruction descriptor of kind::mxf4nvf4 with block scaling: E2M1 A and B
-// (packed, K-major), UE4M3 scales (scale_vec::4X: the four bytes of a TMEM
-// word are the row's four 16-value blocks of the step; scale ids 0).
-__device__ __forceinline__ uint32_t idesc_nvf4(int M, int N) {
-  return (1u << 7)                                  // A format: E2M1
-         | (1u << 10)                               // B format: E2M1
-         | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
-         | (0u << 23)                               // scale type: UE4M3
-         | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
-}
-
-__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
-      " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-      : "memory");
-}
 
 __global__ void __launch_bounds__(kNvThreads, 1)
     nv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -288,6 +305,43 @@ __global__ void __launch_bounds__(kNvThreads, 1)
 }
 
 }  // namespace
+
+cudaError_t launch_nv_tensor_scale(const void* in, long long n, float* g, cudaStream_t st,
+                                   const int32_t* rows_dev, long long row_elems) {
+  cudaError_t e = cudaMemsetAsync(g, 0, sizeof(float), st);
+  if (e != cudaSuccess) return e;
+  const long long nchunks = n / 8;
+  if (nchunks > 0) {
+    long long grid = (nchunks + 255) / 256;
+    const long long cap = static_cast<long long>(num_sms_current_device()) * 8;
+    if (grid > cap) grid = cap;
+    ProfScope prof("nvfp4_amax", st);
+    nv_amax_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(
+        static_cast<const uint4*>(in), nchunks, reinterpret_cast<unsigned*>(g), rows_dev,
+        row_elems / 8);
+    count_launch();
+  }
+  nv_scale_kernel<<<1, 1, 0, st>>>(g);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nv_quant_tiled(const void* in, long long rows, long long cols, const float* g,
+                                  uint8_t* codes, uint8_t* scales, const int32_t* map, int T,
+                                  cudaStream_t st) {
+  const long long nblk = rows * cols / 16;
+  if (nblk == 0) return cudaSuccess;
+  long long grid = (nblk + 255) / 256;
+  const long long cap = static_cast<long long>(num_sms_current_device()) * 16;
+  if (grid > cap) grid = cap;
+  ProfScope prof("nvfp4_quantize", st);
+  nv_quant_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(
+      static_cast<const uint4*>(in), nblk, static_cast<int>(cols / 16), g, codes, scales,
+      cols / 64, map, T);
+  count_launch();
+  return cudaGetLastError();
+}
+
 }  // namespace mok
 
 using namespace mok;
@@ -309,7 +363,7 @@ extern "C" mok_status mok_nvfp4_tensor_scale(const void* in, int64_t n, float* g
     if (grid > cap) grid = cap;
     ProfScope prof("nvfp4_amax", st);
     nv_amax_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(
-        static_cast<const uint4*>(in), nchunks, reinterpret_cast<unsigned*>(g));
+        static_cast<const uint4*>(in), nchunks, reinterpret_cast<unsigned*>(g), nullptr, 0);
     count_launch();
   }
   nv_scale_kernel<<<1, 1, 0, st>>>(g);
@@ -334,8 +388,9 @@ extern "C" mok_status mok_nvfp4_quantize(const void* in, int64_t rows, int64_t c
   const long long cap = static_cast<long long>(num_sms_current_device()) * 16;
   if (grid > cap) grid = cap;
   ProfScope prof("nvfp4_quantize", st);
-  nv_quant_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(static_cast<const uint4*>(in),
-                                                               nblk, g, codes, scales);
+  nv_quant_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(
+      static_cast<const uint4*>(in), nblk, static_cast<int>(cols / 16), g, codes, scales, 0,
+      nullptr, 0);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? MOK_OK : MOK_ERR_CUDA;
 }

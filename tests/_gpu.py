@@ -200,14 +200,20 @@ def full_parity(shape: gen.Shape, inp: dict, gpu: dict, tol=BF16_TOL, precision=
                                     precision=precision)
     g = oracle.moe_backward_ref(inp["x"], *args, inp["dy"], fwd=fwd)
     if nmb > 1:
-        parts = []
+        parts, ys = [], []
         for i in range(nmb):
             sl = slice(i * mb, (i + 1) * mb)
-            _, fi = oracle.moe_forward_ref(inp["x"][sl], *args, routing=(gidx[sl], pf[sl]),
-                                           keep=True, precision=precision)
+            yi, fi = oracle.moe_forward_ref(inp["x"][sl], *args, routing=(gidx[sl], pf[sl]),
+                                            keep=True, precision=precision)
+            ys.append(yi)
             parts.append(oracle.moe_backward_ref(inp["x"][sl], *args, inp["dy"][sl], fwd=fi))
         for n in ("dw_router", "dw_gate_up", "dw_down"):
             g[n] = sum(q[n] for q in parts)
+        if precision == "nvfp4":
+            # NVFP4 tensor scales are taken per micro-batch (its x, its h), so
+            # y and dx are those of each micro-batch's own forward
+            y = np.concatenate(ys)
+            g["dx"] = np.concatenate([q["dx"] for q in parts])
     errs = {}
     errs["y"] = rel_err(host64(gpu["y"]), y)
     errs["dx"] = rel_err(host64(gpu["dx"]), g["dx"])

@@ -123,3 +123,59 @@ def test_nvfp4_gemm_matches_dequantised_product(M, N, K):
     scale = np.abs(out["a"][3]) @ np.abs(out["b"][3]).T
     # fp32 accumulation and the fp32 product of the two tensor scales
     assert np.all(np.abs(got - ref) <= 4e-6 * scale + 1e-30)
+
+
+# ------------------------------------------------------------ the layer ---
+
+NV_TOL = 6e-2  # as for MXFP8: E2M1 flips where the kernel's fp32 h and the
+               # oracle's fp64 h fall on two sides of a rounding boundary
+
+NV_SHAPES = {
+    "small": gen.Shape(T=256, d=256, E=8, I=256, k=2),
+    "ragged": gen.Shape(T=300, d=256, E=5, I=256, k=2),
+    "wide": gen.Shape(T=512, d=512, E=16, I=512, k=4),
+    "many_experts": gen.Shape(T=200, d=256, E=64, I=256, k=8),
+}
+
+
+@pytest.mark.parametrize("name", list(NV_SHAPES))
+def test_layer_parity_nvfp4(name):
+    """Forward expert GEMMs on NVFP4 operands, every output against the
+    oracle's NVFP4 mode (the same quantisation of x, the weights and h; the
+    float64 backward on the forward's g, u)."""
+    shape = NV_SHAPES[name]
+    inp = gen.make_inputs(shape, seed=0)
+    gpu = _gpu.run_gpu(shape, inp, dtype=api.NVFP4)
+    assert gpu["layer"].layout.x_perm == api.NOT_KEPT
+    errs = _gpu.full_parity(shape, inp, gpu, tol=NV_TOL, precision="nvfp4")
+    print(name, errs)
+
+
+def test_layer_nvfp4_micro_batched_and_deterministic():
+    shape = gen.Shape(T=1024, d=256, E=8, I=256, k=2)
+    inp = gen.make_inputs(shape, seed=3)
+    outs = []
+    for _ in range(3):
+        g = _gpu.run_gpu(shape, inp, dtype=api.NVFP4, mb_tokens=256, ring_slots=2)
+        assert g["status"] == 0 and g["nmb"] == 4
+        outs.append([g[n].view(torch.int32).cpu().numpy() for n in
+                     ("y", "dx", "dw_router", "dw_gate_up", "dw_down")])
+    for a, b in zip(outs[0], outs[1]):
+        assert np.array_equal(a, b)
+    for a, b in zip(outs[0], outs[2]):
+        assert np.array_equal(a, b)
+    print(_gpu.full_parity(shape, inp, g, tol=NV_TOL, precision="nvfp4"))
+
+
+def test_layer_nvfp4_rejects_what_it_does_not_support():
+    from routing_dispatch_grouped_router_gb300 import _lib
+    import ctypes
+    lib = _lib.load()
+    f, s, b = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    for kw in (dict(d=128), dict(I=128), dict(flags=api.FLAG_SINGLE_CTA_GEMM),
+               dict(flags=api.FLAG_RECOMPUTE_GATE_UP)):
+        args = dict(T=64, d=256, E=4, I=256, k=2, dtype=api.NVFP4)
+        args.update(kw)
+        desc = api.make_desc(**args)
+        assert lib.mok_moe_workspace_size(ctypes.byref(desc), ctypes.byref(f), ctypes.byref(s),
+                                          ctypes.byref(b)) == 2
