@@ -49,6 +49,19 @@ PROFILE_EVERY = 4  # per-kernel events on one timed step in this many
 
 # GEMMs that run on the block-scaled FP8 tensor cores in the MXFP8 workload
 MX_GEMMS = ("fwd_gate_up_swiglu", "fwd_down", "bwd_gate_up_dgrad")
+# ... and on the block-scaled FP4 tensor cores in the NVFP4 workload
+NV_GEMMS = ("fwd_gate_up_swiglu", "fwd_down")
+
+
+def peak_ratio(workload: str, gemm: str) -> float:
+    """A GEMM's tensor peak relative to the measured bf16 one: the nominal
+    dense ratios of GB300 (fp8 4.5 / bf16 2.25 PFLOP/s = 2, fp4 13.5 / 2.25 = 6)
+    for the GEMMs that run on those operands."""
+    if workload == "mxfp8" and gemm in MX_GEMMS:
+        return 2.0
+    if workload == "nvfp4" and gemm in NV_GEMMS:
+        return 6.0
+    return 1.0
 
 
 # Weight-gradient GEMMs: with micro-batches the layer defers them and launches
@@ -77,7 +90,7 @@ def gemm_flops(shape: gen.Shape, micro_batches: int = 1) -> dict:
 
 
 def gemm_bytes(shape: gen.Shape, micro_batches: int = 1, mx: bool = False,
-               wgrad_elem_bytes: int = 4) -> dict:
+               wgrad_elem_bytes: int = 4, nv: bool = False) -> dict:
     """Algorithmic HBM bytes of one launch of each grouped GEMM in the layer's
     layout, as (total, written): every operand read once, every output written
     once.  Forward: bf16 rows, weights, fp32 g/u and O, bf16 h.  Backward:
@@ -85,15 +98,20 @@ def gemm_bytes(shape: gen.Shape, micro_batches: int = 1, mx: bool = False,
     pairs; the dgrads write fp32 rows; the weight gradients read their hi/lo
     operand and write dW (fp32 by default).  MXFP8: E4M3 codes (+1/32 scale
     byte) for the block-scaled GEMMs' operands.  A deferred weight gradient
-    reads every micro-batch's operands and writes dW once."""
+    reads every micro-batch's operands and writes dW once.  NVFP4: the
+    forward GEMMs read E2M1 codes (half a byte, +1/16 scale byte per value)."""
     R, d, I, E = shape.R // micro_batches, shape.d, shape.I, shape.E
     wgu, wd = E * 2 * I * d, E * d * I
     q8 = 1 + 1 / 32
+    q4 = 0.5 + 1 / 16
     a_gu, w_gu = (R * d * q8, wgu * q8) if mx else (R * d * 2, wgu * 2)
+    if nv:
+        a_gu, w_gu = R * d * q4, wgu * q4
     h_out = R * I * q8 if mx else R * I * 2
     f = {
         "fwd_gate_up_swiglu": (a_gu + w_gu + R * 2 * I * 4 + h_out, R * 2 * I * 4 + h_out),
-        "fwd_down": ((R * I * q8 + wd * q8) if mx else (R * I * 2 + wd * 2)) + R * d * 4,
+        "fwd_down": ((R * I * q8 + wd * q8) if mx else
+                     ((R * I * q4 + wd * q4) if nv else (R * I * 2 + wd * 2))) + R * d * 4,
         "bwd_down_dgrad_swiglu": R * d * 2 + wd * 2 + R * 2 * I * 4 + R * 2 * I * 4 + R * I * 4
                                  + (R * 2 * I * q8 if mx else 0),
         "bwd_gate_up_dgrad": ((R * 2 * I * q8 + wgu * q8) if mx else (R * 2 * I * 2 + wgu * 2))
@@ -344,7 +362,8 @@ def cpu_cores() -> int:
 # tokens per oracle slice: a slice touches up to k x tokens experts, and the
 # oracle widens each touched expert's weights to float64 (0.35 GB per expert on
 # the large workload), so slices are sized to a few seconds each
-SLICE_TOKENS = {"tiny": 32, "fine": 32, "imbalanced": 2, "mxfp8": 2, "large": 1, "large_slice": 1}
+SLICE_TOKENS = {"tiny": 32, "fine": 32, "imbalanced": 2, "mxfp8": 2, "nvfp4": 2, "large": 1,
+                "large_slice": 1}
 
 
 def cpu_baseline(inp: dict, shape: gen.Shape, budget_s: float = 12.0,
@@ -399,6 +418,9 @@ def workload_config(shape: gen.Shape) -> dict:
     if WORKLOAD == "mxfp8":
         prec = (f"MXFP8 operands, {shape.T // w['mb_tokens']} micro-batches of {w['mb_tokens']} "
                 f"tokens through a {w['ring_slots']}-slot ring")
+    if w.get("nvfp4"):
+        prec = ("NVFP4 forward GEMM operands (E2M1, E4M3 per 16, fp32 per tensor), "
+                "BF16 backward")
     if w.get("zipf_s"):
         prec += f", Zipf({w['zipf_s']}) router bias"
     wbytes = shape.E * 3 * shape.I * shape.d * 2
@@ -419,7 +441,10 @@ def layer_options(api, bf16_wgrad: bool = False) -> dict:
         if bf16_wgrad:
             raise SystemExit("--bf16-wgrad: the micro-batched workload accumulates dW in fp32")
         return dict(dtype=api.MXFP8, mb_tokens=w["mb_tokens"], ring_slots=w["ring_slots"])
-    return dict(flags=api.FLAG_BF16_WGRAD_OUT) if bf16_wgrad else {}
+    opts = dict(flags=api.FLAG_BF16_WGRAD_OUT) if bf16_wgrad else {}
+    if w.get("nvfp4"):
+        opts["dtype"] = api.NVFP4
+    return opts
 
 
 # ------------------------------------------------------------- multi-rank --
@@ -516,7 +541,7 @@ def main():
                     help="return the weight gradients in bf16 (default fp32)")
     ap.add_argument("--workload", default="large", choices=sorted(gen.WORKLOADS),
                     help="large (default: the configuration the targets are stated on), "
-                         "fine, imbalanced, mxfp8 or tiny")
+                         "fine, imbalanced, mxfp8, nvfp4 or tiny")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     global WORKLOAD
@@ -612,13 +637,13 @@ def main():
     write_gbs, write_rates = measure_write_gbs(torch, api)
     flops = gemm_flops(shape, int(layer.layout.mb_count))
     gbytes = gemm_bytes(shape, int(layer.layout.mb_count), mx=WORKLOAD == "mxfp8",
-                        wgrad_elem_bytes=2 if args.bf16_wgrad else 4)
+                        wgrad_elem_bytes=2 if args.bf16_wgrad else 4,
+                        nv=WORKLOAD == "nvfp4")
 
     def gemm_roofline_us(n):
         """(bound, shortest time in us) of GEMM n: tensor time at the measured
         (FP8: x2) peak against HBM time at the copy and write bandwidths."""
-        fp8 = WORKLOAD == "mxfp8" and n in MX_GEMMS
-        t_tc = flops[n] / (peaks["bf16_sustained"] * (2.0 if fp8 else 1.0) * 1e12) * 1e6
+        t_tc = flops[n] / (peaks["bf16_sustained"] * peak_ratio(WORKLOAD, n) * 1e12) * 1e6
         if n not in gbytes:
             return "tensor", t_tc
         t_mem = mover_roofline_us(gbytes[n][0], gbytes[n][1], peaks["hbm"], write_gbs)
@@ -658,16 +683,17 @@ def main():
                            "frac": flops[dom] / avg_s / 1e12 / peaks["bf16_sustained"]}}
     elif dom in flops:
         ach = flops[dom] / avg_s / 1e12
-        # the MXFP8 workload's block-scaled GEMMs run on the FP8 tensor rate: their
-        # peak is the measured bf16 one times the nominal fp8/bf16 ratio (2)
-        fp8 = WORKLOAD == "mxfp8" and dom in MX_GEMMS
-        peak = peaks["bf16_sustained"] * (2.0 if fp8 else 1.0)
+        # block-scaled GEMMs run on the FP8 / FP4 tensor rates: their peak is the
+        # measured bf16 one times the nominal ratio (peak_ratio)
+        ratio = peak_ratio(WORKLOAD, dom)
+        peak = peaks["bf16_sustained"] * ratio
         roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak,
                 "unit": "TFLOP/s", "frac": ach / peak,
                 "traffic": ncu_traffic(WORKLOAD, dom)[0],
                 "traffic_source": ncu_traffic(WORKLOAD, dom)[1],
                 "peak_source": f"bf16_tflops_sustained of {peaks['source']}"
-                               + (" x 2 (nominal fp8/bf16 ratio)" if fp8 else ""),
+                               + (f" x {ratio:g} (nominal low-precision/bf16 ratio)"
+                                  if ratio != 1.0 else ""),
                 "algorithmic_per_launch": flops[dom]}
     else:
         ach = movers.get(dom, 0) / avg_s / 1e9
@@ -723,11 +749,13 @@ def main():
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if WORKLOAD != "mxfp8" else "mxfp8",
-            "dtype_detail": None if WORKLOAD != "mxfp8" else (
-                "E4M3 + E8M0 per 32: block-scaled FP8 MMAs for the forward GEMMs and the "
-                "gate/up dgrad; bf16 MMAs on MX-valued operands for the down dgrad; "
-                "weight gradients on bf16 hi/lo operands"),
+            "dtype": {"mxfp8": "mxfp8", "nvfp4": "nvfp4"}.get(WORKLOAD, "bf16"),
+            "dtype_detail": {
+                "mxfp8": "E4M3 + E8M0 per 32: block-scaled FP8 MMAs for the forward GEMMs and "
+                         "the gate/up dgrad; bf16 MMAs on MX-valued operands for the down "
+                         "dgrad; weight gradients on bf16 hi/lo operands",
+                "nvfp4": "E2M1 + E4M3 per 16 + fp32 per tensor: block-scaled FP4 MMAs for "
+                         "the forward GEMMs; the backward on the BF16 engine"}.get(WORKLOAD),
             "data": "synthetic",
             "config": dict(workload_config(shape),
                            weight_grad_out="bf16" if args.bf16_wgrad else "fp32"),

@@ -35,6 +35,9 @@ WORKLOADS = {
     # of its experts and tokens: its kernels at a size a full profiler capture
     # can replay (2 GB of weights); per-expert work scales by 16 to the large one
     "large_slice": dict(T=512, d=7168, E=24, I=2048, k=8),
+    # the imbalanced workload's shape without its router bias, with the forward
+    # expert GEMMs on NVFP4 operands
+    "nvfp4":      dict(T=16384, d=4096, E=128, I=1536, k=8, nvfp4=True),
 }
 
 # Scale of the Zipf offsets for the imbalanced workload (seed 0), found by

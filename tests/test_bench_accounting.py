@@ -147,3 +147,19 @@ def test_ncu_traffic_is_per_workload():
     t, src = bench.ncu_traffic("fine", "bwd_gate_up_wgrad")
     assert t > 1e9 and src.startswith("profiles/")
     assert bench.ncu_traffic("tiny", "bwd_gate_up_wgrad") == (None, None)
+
+
+def test_low_precision_peaks_and_bytes():
+    """FP8 GEMMs against 2x and FP4 GEMMs against 6x the measured bf16 peak
+    (GB300's nominal dense ratios); NVFP4 forward operands are half a byte
+    plus a sixteenth of a scale byte per value."""
+    assert bench.peak_ratio("mxfp8", "fwd_down") == 2.0
+    assert bench.peak_ratio("nvfp4", "fwd_down") == 6.0
+    assert bench.peak_ratio("nvfp4", "bwd_gate_up_dgrad") == 1.0
+    assert bench.peak_ratio("large", "fwd_down") == 1.0
+    s = gen.workload_shape("nvfp4")
+    R, d, I, E = s.R, s.d, s.I, s.E
+    nv, bf = bench.gemm_bytes(s, nv=True), bench.gemm_bytes(s)
+    q4 = 0.5 + 1 / 16
+    assert nv["fwd_down"][0] == R * I * q4 + E * d * I * q4 + R * d * 4
+    assert nv["bwd_gate_up_dgrad"] == bf["bwd_gate_up_dgrad"]
