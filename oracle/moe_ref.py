@@ -45,10 +45,11 @@ quantised GEMMs the identity <dy, O> = <dy W_down, h> no longer holds exactly;
 the router-weight gradient is taken the way the pages fuse it into the SwiGLU
 backward ([dothoosh] "Precision and scheduling"): dp = <dA, h> with dA the
 (quantised) down-projection dgrad of the row and h unquantised.
-``precision="nvfp4"`` quantises the forward GEMMs' operands to NVFP4 (see
-_nvfp4_experts and nvfp4_ref.py: per-tensor fp32 scales, E4M3 scales per 16
-values along K); the backward is the float64 one on the forward's g, u, h,
-with the router-weight gradient in the same fused form dp = <dy W_down, h>.
+``precision="nvfp4"`` quantises the forward GEMMs' operands and those of the
+gate/up dgrad to NVFP4 (see _nvfp4_experts, _nvfp4_gate_up_dgrad and
+nvfp4_ref.py: per-tensor fp32 scales, E4M3 scales per 16 values along K); the
+rest of the backward is the float64 one on the forward's g, u, h, with the
+router-weight gradient in the same fused form dp = <dy W_down, h>.
 dy is itself a bf16 input,
 so the down dgrad dH = p * (dy W_down) needs no rounded operand.  The expert
 output O, y, dp, the router gradient, dx and the weight gradients are not
@@ -279,6 +280,24 @@ def _nvfp4_experts(X, w_gate_up, w_down, offsets, tok, R):
     return G, U, H, O
 
 
+def _nvfp4_gate_up_dgrad(dGU, w_gate_up, offsets):
+    """The gate/up dgrad dX = [dG dU] W_gate_up on NVFP4 operands: [dG dU]
+    (as bf16, the layer's stored form) along 2I with its tensor scale over all
+    routed rows, W_gate_up along 2I with its tensor scale over all experts
+    (the same scale as in the forward: the same tensor)."""
+    Wgu = widen(w_gate_up)
+    E, I2, d = Wgu.shape
+    dGU_q = nvfp4_fake(bf16_round(dGU), -1)
+    # each expert's [2I, d] weights as d rows of 2I values, quantised along 2I
+    Wt_q = nvfp4_fake(Wgu.transpose(0, 2, 1).reshape(E * d, I2), -1).reshape(E, d, I2)
+    dX = np.zeros((dGU.shape[0], d))
+    for e in range(E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if a < b:
+            dX[a:b] = dGU_q[a:b] @ Wt_q[e].T
+    return dX
+
+
 def moe_forward_ref(x, w_router, bias, w_gate_up, w_down, k: int, routing=None,
                     keep=False, precision="fp64"):
     """y_t = sum_s p[t,s] * FFN_{e[t,s]}(x_t), summed in slot order.
@@ -367,6 +386,7 @@ def moe_backward_ref(x, w_router, bias, w_gate_up, w_down, k: int, dy,
         dp = np.einsum("tsd,td->ts", O[pos], dY)
 
     dX_rows = np.zeros((R, d))
+    dGU_all = np.zeros((R, 2 * I)) if precision == "nvfp4" else None
     if grad_experts is None:
         dw_gate_up = np.zeros((E, 2 * I, d))
         dw_down = np.zeros((E, d, I))
@@ -400,13 +420,20 @@ def moe_backward_ref(x, w_router, bias, w_gate_up, w_down, k: int, dy,
         dH = dO[a:b] @ Wd                       # [rows, I]
         dG = rnd(dH * U[a:b] * silu_grad(G[a:b]))
         dU = rnd(dH * silu(G[a:b]))
-        dX_rows[a:b] = dG @ Wgu[:I] + dU @ Wgu[I:]
+        if precision == "nvfp4":
+            # the gate/up dgrad runs after every expert's dG/dU exists (its
+            # operand's tensor scale covers all rows): kept for below
+            dGU_all[a:b] = np.concatenate([dG, dU], axis=1)
+        else:
+            dX_rows[a:b] = dG @ Wgu[:I] + dU @ Wgu[I:]
         if grad_experts is None or e in dw_down:
             # sum_r p_r dy_r h_r^T, with p applied on the h side
             dw_down[e][...] = dYe.T @ rnd(row_p[a:b, None] * H[a:b])
             dw_gate_up[e][:I] = dG.T @ Xe
             dw_gate_up[e][I:] = dU.T @ Xe
 
+    if precision == "nvfp4" and R:
+        dX_rows = _nvfp4_gate_up_dgrad(dGU_all, w_gate_up, offsets)
     if precision in ("mxfp8", "nvfp4"):
         dp = dp_rows[pos]
 

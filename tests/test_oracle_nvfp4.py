@@ -16,7 +16,8 @@ values, float32 scale per tensor).
     mode; W_down scaled by 2^3 scales y by 2^3 (the tensor scale absorbs it);
     and the axis of each forward operand (x and W_gate_up along d, W_down and
     h along I) by power-of-two scale covariance of rows below each tensor's
-    maximum; planted wrong axes fail these pins.
+    maximum, and of the gate/up dgrad's operands (dG/dU and W_gate_up along
+    2I); planted wrong axes fail these pins.
 """
 import numpy as np
 import pytest
@@ -255,9 +256,43 @@ def _pin_h_rows():
     _scaled(y0, y1, sel[:, None], 0.25, "y")
 
 
+def _bwd(c, f):
+    return oracle.moe_backward_ref(c["x"], c["w_router"], None, c["w_gate_up"], c["w_down"], 1,
+                                   c["dy"], fwd=f)
+
+
+def _pin_w_gate_up_columns_backward():
+    """W_gate_up column j (not 0) -> 2^-1 in the backward only (forward
+    intermediates kept): the gate/up dgrad quantises W_gate_up along 2I, so
+    feature j of dx scales by 2^-1."""
+    c = _case(37)
+    _, f = _fwd(c)
+    g0 = _bwd(c, f)
+    j = np.zeros(D, dtype=bool)
+    j[[2, 33, 61]] = True
+    w = c["w_gate_up"].copy()
+    w[:, :, j] /= 2
+    g1 = _bwd(dict(c, w_gate_up=w), f)
+    _scaled(g0["dx"], g1["dx"], j[None, :], 0.5, "dx")
+
+
+def _pin_dgu_rows_backward():
+    """dy rows (not token 0, whose huge dy holds the tensor maximum of dG/dU)
+    -> 2^-1: dG/dU rows scale by 2^-1 and are quantised along 2I, so those
+    tokens' dx rows scale by 2^-1."""
+    c = _case(38)
+    c["dy"][0] *= 64
+    _, f = _fwd(c)
+    g0 = _bwd(c, f)
+    sel = (np.arange(64) % 5 == 3)
+    g1 = _bwd(dict(c, dy=np.where(sel[:, None], c["dy"] / 2, c["dy"])), f)
+    _scaled(g0["dx"], g1["dx"], sel[:, None], 0.5, "dx")
+
+
 NV_PINS = {"w_down_global_scale": _pin_w_down_global_scale, "x_rows": _pin_x_rows,
            "w_gate_up_rows": _pin_w_gate_up_rows, "w_down_rows": _pin_w_down_rows,
-           "h_rows": _pin_h_rows}
+           "h_rows": _pin_h_rows, "w_gate_up_columns_backward": _pin_w_gate_up_columns_backward,
+           "dgu_rows_backward": _pin_dgu_rows_backward}
 
 
 @pytest.mark.parametrize("name", sorted(NV_PINS))
@@ -284,6 +319,8 @@ def _plant(monkeypatch, shape_tail, rows):
     (D, 2 * 2 * I_, "w_gate_up_rows"),   # W_gate_up along 2I
     (I_, 2 * D, "w_down_rows"),          # W_down along d
     (I_, 64, "h_rows"),                  # h along the tokens
+    (2 * I_, 2 * D, "w_gate_up_columns_backward"),  # W_gate_up (transposed) along d
+    (2 * I_, 64, "dgu_rows_backward"),              # dG/dU along the tokens
 ])
 def test_planted_nvfp4_axis_is_caught(monkeypatch, tail, rows, pin):
     _plant(monkeypatch, tail, rows)
