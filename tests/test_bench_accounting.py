@@ -149,6 +149,19 @@ def test_ncu_traffic_is_per_workload():
     assert bench.ncu_traffic("tiny", "bwd_gate_up_wgrad") == (None, None)
 
 
+def test_large_traffic_scales_the_slice_capture_to_the_algorithmic_bytes():
+    """The large workload's traffic comes from a capture of its slice scaled by
+    the expert ratio; the slice must keep the large workload's per-expert
+    shape, and the scaled weight-gradient traffic sits at its algorithmic
+    bytes (dW written once, its operands read once)."""
+    big, sl = gen.workload_shape("large"), gen.workload_shape("large_slice")
+    assert (big.d, big.I, big.k) == (sl.d, sl.I, sl.k)
+    assert big.E == 16 * sl.E and big.T == 16 * sl.T
+    t, src = bench.ncu_traffic("large", "bwd_gate_up_wgrad")
+    alg = bench.gemm_bytes(big)["bwd_gate_up_wgrad"][0]
+    assert 0.95 < t / alg < 1.05 and "large_slice" in src
+
+
 def test_low_precision_peaks_and_bytes():
     """FP8 GEMMs against 2x and FP4 GEMMs against 6x the measured bf16 peak
     (GB300's nominal dense ratios); NVFP4 forward operands are half a byte
