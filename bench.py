@@ -50,7 +50,7 @@ PROFILE_EVERY = 4  # per-kernel events on one timed step in this many
 # GEMMs that run on the block-scaled FP8 tensor cores in the MXFP8 workload
 MX_GEMMS = ("fwd_gate_up_swiglu", "fwd_down", "bwd_gate_up_dgrad")
 # ... and on the block-scaled FP4 tensor cores in the NVFP4 workload
-NV_GEMMS = ("fwd_gate_up_swiglu", "fwd_down")
+NV_GEMMS = ("fwd_gate_up_swiglu", "fwd_down", "bwd_gate_up_dgrad")
 
 
 def peak_ratio(workload: str, gemm: str) -> float:
@@ -99,7 +99,8 @@ def gemm_bytes(shape: gen.Shape, micro_batches: int = 1, mx: bool = False,
     operand and write dW (fp32 by default).  MXFP8: E4M3 codes (+1/32 scale
     byte) for the block-scaled GEMMs' operands.  A deferred weight gradient
     reads every micro-batch's operands and writes dW once.  NVFP4: the
-    forward GEMMs read E2M1 codes (half a byte, +1/16 scale byte per value)."""
+    forward GEMMs and the gate/up dgrad read E2M1 codes (half a byte, +1/16
+    scale byte per value)."""
     R, d, I, E = shape.R // micro_batches, shape.d, shape.I, shape.E
     wgu, wd = E * 2 * I * d, E * d * I
     q8 = 1 + 1 / 32
@@ -114,7 +115,8 @@ def gemm_bytes(shape: gen.Shape, micro_batches: int = 1, mx: bool = False,
                      ((R * I * q4 + wd * q4) if nv else (R * I * 2 + wd * 2))) + R * d * 4,
         "bwd_down_dgrad_swiglu": R * d * 2 + wd * 2 + R * 2 * I * 4 + R * 2 * I * 4 + R * I * 4
                                  + (R * 2 * I * q8 if mx else 0),
-        "bwd_gate_up_dgrad": ((R * 2 * I * q8 + wgu * q8) if mx else (R * 2 * I * 2 + wgu * 2))
+        "bwd_gate_up_dgrad": ((R * 2 * I * q8 + wgu * q8) if mx else
+                              ((R * 2 * I * q4 + wgu * q4) if nv else (R * 2 * I * 2 + wgu * 2)))
                              + R * d * 4,
     }
     w = {
@@ -431,8 +433,8 @@ def workload_config(shape: gen.Shape) -> dict:
         prec = (f"MXFP8 operands, {shape.T // w['mb_tokens']} micro-batches of {w['mb_tokens']} "
                 f"tokens through a {w['ring_slots']}-slot ring")
     if w.get("nvfp4"):
-        prec = ("NVFP4 forward GEMM operands (E2M1, E4M3 per 16, fp32 per tensor), "
-                "BF16 backward")
+        prec = ("NVFP4 operands (E2M1, E4M3 per 16, fp32 per tensor) for the forward GEMMs "
+                "and the gate/up dgrad")
     if w.get("zipf_s"):
         prec += f", Zipf({w['zipf_s']}) router bias"
     wbytes = shape.E * 3 * shape.I * shape.d * 2
@@ -767,7 +769,8 @@ def main():
                          "the gate/up dgrad; bf16 MMAs on MX-valued operands for the down "
                          "dgrad; weight gradients on bf16 hi/lo operands",
                 "nvfp4": "E2M1 + E4M3 per 16 + fp32 per tensor: block-scaled FP4 MMAs for "
-                         "the forward GEMMs; the backward on the BF16 engine"}.get(WORKLOAD),
+                         "the forward GEMMs and the gate/up dgrad; the down dgrad and the "
+                         "weight gradients on the BF16 engine"}.get(WORKLOAD),
             "data": "synthetic",
             "config": dict(workload_config(shape),
                            weight_grad_out="bf16" if args.bf16_wgrad else "fp32"),

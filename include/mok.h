@@ -62,12 +62,15 @@ typedef enum mok_dtype {
   MOK_BF16 = 0,  /* bf16 operands, fp32 accumulation, bf16 I/O */
   MOK_MXFP8 = 1, /* expert GEMMs on MXFP8 operands: E4M3 with one E8M0 scale per 32
                     values along K, fp32 accumulation (see mok_moe_forward) */
-  MOK_NVFP4 = 2  /* forward expert GEMMs on NVFP4 operands (see mok_nvfp4_quantize):
-                    x, W_gate_up along d and h, W_down along I, each with its
-                    tensor scale over the whole tensor; h rounded to bf16 before
-                    its quantisation; the backward as in MOK_BF16, with
-                    dp = <dy W_down, h>.  d and I multiples of 256; CTA-pair
-                    GEMMs only (MOK_FLAG_SINGLE_CTA_GEMM and
+  MOK_NVFP4 = 2  /* expert GEMMs on NVFP4 operands (see mok_nvfp4_quantize),
+                    each with its tensor scale over the whole tensor.  Forward:
+                    x, W_gate_up along d and h, W_down along I; h rounded to
+                    bf16 before its quantisation.  Backward: the gate/up dgrad
+                    on dG/dU (bf16, along 2I, tensor scale over the
+                    micro-batch's routed rows) and W_gate_up along 2I; the
+                    down-projection dgrad and the weight gradients as in
+                    MOK_BF16, with dp = <dy W_down, h>.  d and I multiples of
+                    256; CTA-pair GEMMs only (MOK_FLAG_SINGLE_CTA_GEMM and
                     MOK_FLAG_RECOMPUTE_GATE_UP unsupported); no dispatched rows
                     are kept in saved */
 } mok_dtype;
@@ -146,6 +149,9 @@ typedef struct mok_saved_layout {
                              padded_token instead) and with MOK_FLAG_RECOMPUTE_DISPATCH */
   size_t gate_up;         /* fp32 [rows_max, 2I] pre-activation gate (cols 0..I-1) and up (I..2I-1);
                              MOK_NOT_KEPT with MOK_FLAG_RECOMPUTE_GATE_UP */
+  size_t nv_weight_scales; /* MOK_NVFP4: fp32 [2] tensor scales of W_gate_up and W_down (the
+                             backward reuses W_gate_up's, so the weights must not change
+                             between the two calls); MOK_NOT_KEPT otherwise */
   size_t rows_max;        /* number of padded rows the buffers hold: T*k + 127*min(E, T*k), rounded to 128 */
   size_t mb_count;        /* micro-batches (1 without micro-batching) */
   size_t mb_stride;       /* bytes between consecutive micro-batches' fields */
@@ -293,6 +299,16 @@ mok_status mok_nvfp4_tensor_scale(const void* in, int64_t n, float* g, void* str
  * the high one; 8-byte aligned), scales uint8 [rows, cols/16] E4M3 bytes. */
 mok_status mok_nvfp4_quantize(const void* in, int64_t rows, int64_t cols, const float* g,
                               uint8_t* codes, uint8_t* scales, void* stream);
+
+/* NVFP4 of the columns of ng stacked bf16 matrices [K, C] (row-major, K
+ * along the rows; blocks of 16 along K) with the tensor scale at device *g:
+ * out row i*C + c holds column c of matrix i.  codes uint8 [ng*C, K/2] (low
+ * nibble first), scales uint8 [ng*C, K/16] E4M3 bytes.  K % 64 == 0,
+ * C % 128 == 0; in and codes 16-byte aligned.  The layer uses it for
+ * W_gate_up along 2I, the gate/up dgrad's reduction dimension. */
+mok_status mok_nvfp4_quantize_cols(const void* in, int64_t ng, int64_t K, int64_t C,
+                                   const float* g, uint8_t* codes, uint8_t* scales,
+                                   void* stream);
 
 /* Dense NVFP4 GEMM on the block-scaled FP4 tensor cores
  * (tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X), a diagnostic of

@@ -23,7 +23,7 @@ class SavedLayout(ctypes.Structure):
     _fields_ = [(n, c_size_t) for n in (
         "status", "topk_idx", "topk_w", "counts", "offsets", "pos", "token_of_row",
         "padded_offsets", "padded_pos", "padded_token", "row_weight", "x_perm", "gate_up",
-        "rows_max", "mb_count", "mb_stride", "ring_slots", "ring_slot_bytes", "total")]
+        "nv_weight_scales", "rows_max", "mb_count", "mb_stride", "ring_slots", "ring_slot_bytes", "total")]
 
 
 class KernelTime(ctypes.Structure):
@@ -57,6 +57,8 @@ _SIGS = {
     "mok_nvfp4_tensor_scale": (c_int32, [c_void_p, c_int64, c_void_p, c_void_p]),
     "mok_nvfp4_quantize": (c_int32, [c_void_p, c_int64, c_int64, c_void_p, c_void_p, c_void_p,
                                      c_void_p]),
+    "mok_nvfp4_quantize_cols": (c_int32, [c_void_p, c_int64, c_int64, c_int64, c_void_p,
+                                          c_void_p, c_void_p, c_void_p]),
     "mok_gemm_nvfp4": (c_int32, [c_int64, c_int64, c_int64, c_void_p, c_void_p, c_void_p,
                                  c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
                                  c_void_p]),

@@ -151,6 +151,22 @@ def nvfp4_quantize(x, g, codes=None, scales=None, stream=None):
     return codes, scales
 
 
+def nvfp4_quantize_cols(x, g, codes=None, scales=None, stream=None):
+    """NVFP4 of the columns of a bf16 [ng, K, C] (or [K, C]) tensor, blocks of
+    16 along K: codes [ng*C, K/2] and E4M3 scales [ng*C, K/16] (see
+    mok_nvfp4_quantize_cols)."""
+    x3 = x if x.dim() == 3 else x.unsqueeze(0)
+    ng, K, C = x3.shape
+    codes = torch.empty(ng * C, K // 2, dtype=torch.uint8, device=x.device) if codes is None \
+        else codes
+    scales = torch.empty(ng * C, K // 16, dtype=torch.uint8, device=x.device) if scales is None \
+        else scales
+    _lib.check(_lib.load().mok_nvfp4_quantize_cols(_ptr(x3), ng, K, C, _ptr(g), _ptr(codes),
+                                                   _ptr(scales), _stream(stream)),
+               "mok_nvfp4_quantize_cols")
+    return codes, scales
+
+
 def gemm_nvfp4(A, sa, ga, B, sb, gb, C, workspace, stream=None):
     """C[M,N] fp32 = ga gb dequant(A) dequant(B)^T for NVFP4 codes A [M,K/2],
     B [N,K/2], E4M3 block scales sa [M,K/16], sb [N,K/16] and device tensor

@@ -1656,39 +1656,62 @@ cudaError_t gemm_fwd_gate_up_nv(const Dims& D, const uint8_t* x_codes, const uin
       "fwd_gate_up_swiglu", ta, tb, tc, a, max_mpairs(D) * a.n_tiles, st, nullptr, &om);
 }
 
-// NVFP4 operands: the down projection O[rows_max, d] (fp32) = h W_down_e^T per
-// expert segment, on CTA pairs (256 x 256 tiles).
-cudaError_t gemm_fwd_down_nv(const Dims& D, const uint8_t* h_codes, const uint8_t* h_scales,
-                             const float* h_g, const uint8_t* wd_codes, const uint8_t* wd_scales,
-                             const float* wd_g, const int32_t* mtile_prefix, const int32_t* poff,
-                             void* O, int* status, cudaStream_t st) {
+// An M-grouped GEMM on NVFP4 operands with fp32 rows out, on CTA pairs
+// (256 x 256 tiles): O[rows_max, d] = A[rows_max, K] B_e[d, K]^T per expert
+// segment, A and B packed E2M1 codes [.., K/2] with tiled scales.  The down
+// projection (K = I) and the gate/up dgrad (K = 2I, B = W_gate_up transposed).
+static cudaError_t grouped_nv_f32(const char* name, const Dims& D, int64_t K,
+                                  const uint8_t* a_codes, const uint8_t* a_scales,
+                                  const float* a_g, const uint8_t* b_codes,
+                                  const uint8_t* b_scales, const float* b_g,
+                                  const int32_t* mtile_prefix, const int32_t* poff, void* O,
+                                  int* status, cudaStream_t st) {
   const auto u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
-  if (D.d % 256 || D.I % 256) return cudaErrorInvalidValue;
+  if (D.d % 256 || K % 256) return cudaErrorInvalidValue;
   CUtensorMap ta, tb, tc;
-  if (!make_map_t(&ta, u8, 1, h_codes, D.I / 2, D.rows_max, D.I / 2, 128, 128, sw) ||
-      !make_map_t(&tb, u8, 1, wd_codes, D.I / 2, D.E * D.d, D.I / 2, 128, 128, sw) ||
+  if (!make_map_t(&ta, u8, 1, a_codes, K / 2, D.rows_max, K / 2, 128, 128, sw) ||
+      !make_map_t(&tb, u8, 1, b_codes, K / 2, D.E * D.d, K / 2, 128, 128, sw) ||
       !make_out_map(&tc, O, D.d, D.rows_max))
     return cudaErrorInvalidValue;
   GemmArgs a = blank_args(status);
   a.E = (int)D.E;
   a.n_tiles = (int)(D.d / 256);
-  a.num_kb = (int)(D.I / 256);
+  a.num_kb = (int)(K / 256);
   a.b_group_rows = (int)D.d;
   a.mtile_prefix = mtile_prefix;
   a.poff = poff;
   a.out = O;
   a.ldo = D.d;
-  a.ks = (int)(D.I / 64);
-  a.ga = h_g;
-  a.gb = wd_g;
+  a.ks = (int)(K / 64);
+  a.ga = a_g;
+  a.gb = b_g;
   OutMaps om;
   memset(&om, 0, sizeof(om));
-  if (!make_nv_sf_map(&om.sfa, h_scales, D.rows_max, D.I) ||
-      !make_nv_sf_map(&om.sfb, wd_scales, D.E * D.d, D.I))
+  if (!make_nv_sf_map(&om.sfa, a_scales, D.rows_max, K) ||
+      !make_nv_sf_map(&om.sfb, b_scales, D.E * D.d, K))
     return cudaErrorInvalidValue;
   return launch<256, false, false, SCHED_MGROUP, EPI_F32, SPLIT_NV, true>(
-      "fwd_down", ta, tb, tc, a, max_mpairs(D) * a.n_tiles, st, nullptr, &om);
+      name, ta, tb, tc, a, max_mpairs(D) * a.n_tiles, st, nullptr, &om);
+}
+
+cudaError_t gemm_fwd_down_nv(const Dims& D, const uint8_t* h_codes, const uint8_t* h_scales,
+                             const float* h_g, const uint8_t* wd_codes, const uint8_t* wd_scales,
+                             const float* wd_g, const int32_t* mtile_prefix, const int32_t* poff,
+                             void* O, int* status, cudaStream_t st) {
+  return grouped_nv_f32("fwd_down", D, D.I, h_codes, h_scales, h_g, wd_codes, wd_scales, wd_g,
+                        mtile_prefix, poff, O, status, st);
+}
+
+cudaError_t gemm_bwd_gate_up_dgrad_nv(const Dims& D, const uint8_t* dgu_codes,
+                                      const uint8_t* dgu_scales, const float* dgu_g,
+                                      const uint8_t* wgu_t_codes, const uint8_t* wgu_t_scales,
+                                      const float* wgu_g, const int32_t* mtile_prefix,
+                                      const int32_t* poff, void* dX_perm, int* status,
+                                      cudaStream_t st) {
+  return grouped_nv_f32("bwd_gate_up_dgrad", D, 2 * D.I, dgu_codes, dgu_scales, dgu_g,
+                        wgu_t_codes, wgu_t_scales, wgu_g, mtile_prefix, poff, dX_perm, status,
+                        st);
 }
 
 cudaError_t gemm_bwd_gate_up_dgrad_mx(const Dims& D, const uint8_t* dgu_codes,

@@ -206,6 +206,7 @@ void saved_layout(const Dims& D, mok_saved_layout* L, size_t* mtile_prefix_off) 
   L->padded_token = base + B.padded_token;
   L->row_weight = base + B.row_weight;
   L->gate_up = D.recompute_gu ? MOK_NOT_KEPT : base + B.gate_up;
+  L->nv_weight_scales = D.nv ? 16 : MOK_NOT_KEPT;  // inside the status block
   L->x_perm = keep_rows ? ring0 : MOK_NOT_KEPT;
   L->rows_max = static_cast<size_t>(D.rows_max);
   L->mb_count = static_cast<size_t>(D.nmb);
@@ -278,13 +279,16 @@ void bwd_layout(const Dims& D, BwdWs* W) {
   W->x_def = (!D.mx && ns > 1) ? b.take(ns * rows * D.d * 2) : 0;
   // without micro-batches and with the dispatch recompute: x rows again
   W->x_rd = (D.recompute_dispatch && ns == 1) ? b.take(rows * D.d * 2) : 0;
-  // MXFP8 operands of the gate/up dgrad: dG, dU codes and W_gate_up
-  // transposed ([E*d, 2I] codes), both with tiled scales
-  W->dgu_codes = D.mx ? b.take(rows * 2 * D.I) : 0;
-  W->dgu_scales = D.mx ? b.take(rows * 2 * D.I / 32) : 0;
+  // block-scaled operands of the gate/up dgrad: dG, dU codes and W_gate_up
+  // transposed ([E*d, 2I] values), both with tiled scales -- MXFP8 one byte
+  // and a scale per 32 values, NVFP4 half a byte and a scale per 16
+  const size_t dgu_n = rows * 2 * D.I, wgu_n = wgu / 2;
+  W->dgu_codes = D.mx ? b.take(dgu_n) : D.nv ? b.take(dgu_n / 2) : 0;
+  W->dgu_scales = D.mx ? b.take(dgu_n / 32) : D.nv ? b.take(dgu_n / 16) : 0;
   W->wd_col = D.mx ? b.take(wd) : 0;
-  W->wgu_t_codes = D.mx ? b.take(wgu / 2) : 0;
-  W->wgu_t_scales = D.mx ? b.take(wgu / 64) : 0;
+  W->wgu_t_codes = D.mx ? b.take(wgu_n) : D.nv ? b.take(wgu_n / 2) : 0;
+  W->wgu_t_scales = D.mx ? b.take(wgu_n / 32) : D.nv ? b.take(wgu_n / 16) : 0;
+  W->nv_g = D.nv ? b.take(256) : 0;  // NVFP4: dG/dU's tensor scale
   // recompute of g, u: their fp32 rows, and the forward's MXFP8 operands
   W->gu = D.recompute_gu ? b.take(rows * 2 * D.I * 4) : 0;
   const bool rmx = D.recompute_gu && D.mx;  // MXFP8 operands of the recomputed gate/up GEMM
@@ -407,8 +411,10 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
     MOK_CUDA(launch_mx_rows(w_gate_up, nullptr, D.E * 2 * D.I, D.d, wgu_c, wgu_s, st, true));
     MOK_CUDA(launch_mx_rows(w_down, nullptr, D.E * D.d, D.I, wd_c, wd_s, st, true));
   }
-  // NVFP4: tensor scales [x, h, W_gate_up, W_down]; the weights once per call
+  // NVFP4: tensor scales [x, h] in the workspace; the weights', once per
+  // call, in `saved` [W_gate_up, W_down] (the backward reuses W_gate_up's)
   float* nvg = D.nv ? at<float>(workspace, F.nv_g) : nullptr;
+  float* nvw = D.nv ? at<float>(saved, L.nv_weight_scales) : nullptr;
   uint8_t* nxq_c = at<uint8_t>(workspace, F.nxq_codes);
   uint8_t* nxq_s = at<uint8_t>(workspace, F.nxq_scales);
   uint8_t* nh_c = at<uint8_t>(workspace, F.nh_codes);
@@ -418,11 +424,11 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
   uint8_t* nwd_c = at<uint8_t>(workspace, F.nwd_codes);
   uint8_t* nwd_s = at<uint8_t>(workspace, F.nwd_scales);
   if (D.nv) {
-    MOK_CUDA(launch_nv_tensor_scale(w_gate_up, D.E * 2 * D.I * D.d, nvg + 2, st));
-    MOK_CUDA(launch_nv_quant_tiled(w_gate_up, D.E * 2 * D.I, D.d, nvg + 2, nwgu_c, nwgu_s,
+    MOK_CUDA(launch_nv_tensor_scale(w_gate_up, D.E * 2 * D.I * D.d, nvw + 0, st));
+    MOK_CUDA(launch_nv_quant_tiled(w_gate_up, D.E * 2 * D.I, D.d, nvw + 0, nwgu_c, nwgu_s,
                                    nullptr, 0, st));
-    MOK_CUDA(launch_nv_tensor_scale(w_down, D.E * D.d * D.I, nvg + 3, st));
-    MOK_CUDA(launch_nv_quant_tiled(w_down, D.E * D.d, D.I, nvg + 3, nwd_c, nwd_s, nullptr, 0,
+    MOK_CUDA(launch_nv_tensor_scale(w_down, D.E * D.d * D.I, nvw + 1, st));
+    MOK_CUDA(launch_nv_quant_tiled(w_down, D.E * D.d, D.I, nvw + 1, nwd_c, nwd_s, nullptr, 0,
                                    st));
   }
   const size_t y_esz = D.act_bf16 ? 2 : 4;
@@ -467,12 +473,12 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
       MOK_CUDA(launch_nv_tensor_scale(xi, D.T * D.d, nvg + 0, st));
       MOK_CUDA(launch_nv_quant_tiled(xi, D.rows_max, D.d, nvg + 0, nxq_c, nxq_s, o.ptok,
                                      static_cast<int>(D.T), st));
-      MOK_CUDA(gemm_fwd_gate_up_nv(D, nxq_c, nxq_s, nvg + 0, nwgu_c, nwgu_s, nvg + 2,
+      MOK_CUDA(gemm_fwd_gate_up_nv(D, nxq_c, nxq_s, nvg + 0, nwgu_c, nwgu_s, nvw + 0,
                                    o.mtile_prefix, o.padded_offsets, gu, h, status, st));
       MOK_CUDA(launch_nv_tensor_scale(h, D.rows_max * D.I, nvg + 1, st,
                                       o.padded_offsets + D.E, D.I));
       MOK_CUDA(launch_nv_quant_tiled(h, D.rows_max, D.I, nvg + 1, nh_c, nh_s, nullptr, 0, st));
-      MOK_CUDA(gemm_fwd_down_nv(D, nh_c, nh_s, nvg + 1, nwd_c, nwd_s, nvg + 3, o.mtile_prefix,
+      MOK_CUDA(gemm_fwd_down_nv(D, nh_c, nh_s, nvg + 1, nwd_c, nwd_s, nvw + 1, o.mtile_prefix,
                                 o.padded_offsets, O, status, st));
     } else if (D.mx) {
       // expert GEMMs on the block-scaled tensor cores: the dispatched x rows
@@ -537,10 +543,14 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
   void* dl_lo = at<char>(workspace, B.dl_lo);
   int32_t* rw_off = at<int32_t>(workspace, B.rw_off);
   float* rw_part = at<float>(workspace, B.rw_part);
-  uint8_t* dgu_c = D.mx ? at<uint8_t>(workspace, B.dgu_codes) : nullptr;
-  uint8_t* dgu_s = D.mx ? at<uint8_t>(workspace, B.dgu_scales) : nullptr;
-  uint8_t* wgu_t_c = D.mx ? at<uint8_t>(workspace, B.wgu_t_codes) : nullptr;
-  uint8_t* wgu_t_s = D.mx ? at<uint8_t>(workspace, B.wgu_t_scales) : nullptr;
+  const bool bs = D.mx || D.nv;  // block-scaled gate/up dgrad
+  uint8_t* dgu_c = bs ? at<uint8_t>(workspace, B.dgu_codes) : nullptr;
+  uint8_t* dgu_s = bs ? at<uint8_t>(workspace, B.dgu_scales) : nullptr;
+  uint8_t* wgu_t_c = bs ? at<uint8_t>(workspace, B.wgu_t_codes) : nullptr;
+  uint8_t* wgu_t_s = bs ? at<uint8_t>(workspace, B.wgu_t_scales) : nullptr;
+  // NVFP4: dG/dU's tensor scale (per micro-batch) and W_gate_up's (the forward's)
+  float* nv_dgu_g = D.nv ? at<float>(workspace, B.nv_g) : nullptr;
+  const float* nv_wgu_g = D.nv ? at<float>(saved, L.nv_weight_scales) : nullptr;
   const void* wd_op = w_down;
   // MXFP8 operands of the recomputed gate/up GEMM (the forward's kernel)
   uint8_t* rwgu_c = at<uint8_t>(workspace, B.wgu_codes);
@@ -558,6 +568,8 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
     MOK_CUDA(launch_mx_cols_t(w_gate_up, D.E * 2 * D.I, D.d, 2 * D.I, wgu_t_c, wgu_t_s, st));
     wd_op = wd_q;
   }
+  if (D.nv)  // W_gate_up along 2I: codes [E*d, I] with tiled scales
+    MOK_CUDA(launch_nv_quant_t(w_gate_up, D.E, 2 * D.I, D.d, nv_wgu_g, wgu_t_c, wgu_t_s, st));
   const size_t dx_esz = D.act_bf16 ? 2 : 4;
   // micro-batches in reverse, so the last ring slots are still resident.
   // With several micro-batches the expert weight gradients are deferred: each
@@ -640,8 +652,9 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
     // down-projection dgrad + SwiGLU backward + router-weight partials;
     // dG, dU and P = p h leave as bf16 hi/lo pairs (and dG, dU as MXFP8)
     MOK_CUDA(gemm_bwd_down_dgrad(D, dy_row_op, wd_op, mtp, poff, static_cast<const float*>(gu),
-                                 row_w, dgu_hi_i, dgu_lo_i, p_hi_i, p_lo_i, dgu_c, dgu_s, dp_part,
-                                 status, st));
+                                 row_w, dgu_hi_i, dgu_lo_i, p_hi_i, p_lo_i,
+                                 D.mx ? dgu_c : nullptr, D.mx ? dgu_s : nullptr, dp_part, status,
+                                 st));
     // the weight gradients' K loops stop at each expert's real rows
     WgradSegs one;
     one.coff = at<int32_t>(saved, L.offsets + blk);
@@ -650,10 +663,19 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
       MOK_CUDA(gemm_wgrad_down(D, dy_col_op, p_hi_i, p_lo_i, poff, dw_down, !first, status, st,
                                one));
     // gate/up dgrad: dX_perm = dGU W_gu (fp32 rows)
-    if (D.mx)
+    if (D.mx) {
       MOK_CUDA(gemm_bwd_gate_up_dgrad_mx(D, dgu_c, dgu_s, wgu_t_c, wgu_t_s, mtp, poff, dx_perm,
                                          status, st));
-    else
+    } else if (D.nv) {
+      // dG/dU (bf16, the hi half) to NVFP4 along 2I: the tensor scale over
+      // the routed rows (padding rows, whose values nothing reads, skipped)
+      MOK_CUDA(launch_nv_tensor_scale(dgu_hi_i, D.rows_max * 2 * D.I, nv_dgu_g, st, poff + D.E,
+                                      2 * D.I, ptok));
+      MOK_CUDA(launch_nv_quant_tiled(dgu_hi_i, D.rows_max, 2 * D.I, nv_dgu_g, dgu_c, dgu_s,
+                                     nullptr, 0, st));
+      MOK_CUDA(gemm_bwd_gate_up_dgrad_nv(D, dgu_c, dgu_s, nv_dgu_g, wgu_t_c, wgu_t_s, nv_wgu_g,
+                                         mtp, poff, dx_perm, status, st));
+    } else
       MOK_CUDA(gemm_bwd_gate_up_dgrad(D, dgu_hi_i, w_gate_up, mtp, poff, dx_perm, status, st));
     // gate/up wgrad: dW_gu_e (+)= (dGU_hi + dGU_lo)_e^T X_e
     if (!defer)

@@ -73,7 +73,7 @@ struct BwdWs {
   size_t dy_perm, dgu_hi, dgu_lo, p_hi, p_lo, dp_part, dx_perm, dl_hi, dl_lo, rw_off, rw_part,
       dyq_row, dyq_col,
       xq_col, dgu_codes, dgu_scales, wd_col, wgu_t_codes, wgu_t_scales, gu, xq_codes, xq_scales,
-      wgu_codes, wgu_scales, x_def, x_rd, total;
+      wgu_codes, wgu_scales, x_def, x_rd, nv_g, total;
 };
 struct StageWs {
   size_t status, block_counts, block_base, padded_offsets, mtile_prefix, ppos, ptok, row_w,
@@ -193,6 +193,14 @@ cudaError_t gemm_fwd_down_nv(const Dims& D, const uint8_t* h_codes, const uint8_
                              const float* h_g, const uint8_t* wd_codes, const uint8_t* wd_scales,
                              const float* wd_g, const int32_t* mtile_prefix, const int32_t* poff,
                              void* O, int* status, cudaStream_t st);
+// the gate/up dgrad dX_perm = [dG dU] W_gate_up on NVFP4 operands: dG/dU
+// codes [rows_max, I] (2I values) and W_gate_up transposed [E*d, I] codes
+cudaError_t gemm_bwd_gate_up_dgrad_nv(const Dims& D, const uint8_t* dgu_codes,
+                                      const uint8_t* dgu_scales, const float* dgu_g,
+                                      const uint8_t* wgu_t_codes, const uint8_t* wgu_t_scales,
+                                      const float* wgu_g, const int32_t* mtile_prefix,
+                                      const int32_t* poff, void* dX_perm, int* status,
+                                      cudaStream_t st);
 cudaError_t gemm_fwd_down_mx(const Dims& D, const uint8_t* h_codes, const uint8_t* h_scales,
                              const uint8_t* wd_codes, const uint8_t* wd_scales,
                              const int32_t* mtile_prefix, const int32_t* poff, void* O,
@@ -272,9 +280,16 @@ cudaError_t launch_mx_cols(const void* in, void* out, long long rows, long long 
 // block scales in the tiled layout (one 512-byte block per 128 rows x 64
 // values, consecutive along K) of bf16 [rows, cols] or, with `map`, of the
 // rows map[r] of a [T, cols] input (zeros where map[r] is not in [0, T)).
-// rows_dev (or NULL): only the first *rows_dev rows of row_elems values count.
+// rows_dev (or NULL): only the first *rows_dev rows of row_elems values count;
+// rowmap (or NULL): rows r with rowmap[r] < 0 do not count.
 cudaError_t launch_nv_tensor_scale(const void* in, long long n, float* g, cudaStream_t st,
-                                   const int32_t* rows_dev = nullptr, long long row_elems = 0);
+                                   const int32_t* rows_dev = nullptr, long long row_elems = 0,
+                                   const int32_t* rowmap = nullptr);
+// The transposed form of ng stacked bf16 [K, C] matrices: codes [ng*C, K/2]
+// and tiled scales, blocks of 16 along K (K a multiple of 64, C of 128).
+cudaError_t launch_nv_quant_t(const void* in, long long ng, long long K, long long C,
+                              const float* g, uint8_t* codes, uint8_t* scales, cudaStream_t st,
+                              bool tiled = true);
 cudaError_t launch_nv_quant_tiled(const void* in, long long rows, long long cols, const float* g,
                                   uint8_t* codes, uint8_t* scales, const int32_t* map, int T,
                                   cudaStream_t st);

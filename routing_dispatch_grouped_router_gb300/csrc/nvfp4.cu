@@ -58,8 +58,10 @@ namespace {
 // order of the updates).
 __global__ void nv_amax_kernel(const uint4* __restrict__ in, long long nchunks,
                                unsigned* __restrict__ amax_bits,
-                               const int32_t* __restrict__ rows_dev, long long row_chunks) {
-  // rows_dev (or NULL): only the first *rows_dev rows of row_chunks chunks
+                               const int32_t* __restrict__ rows_dev, long long row_chunks,
+                               const int32_t* __restrict__ rowmap) {
+  // rows_dev (or NULL): only the first *rows_dev rows of row_chunks chunks;
+  // rowmap (or NULL): rows r with rowmap[r] < 0 (padding) do not count
   if (rows_dev) {
     const long long lim = static_cast<long long>(*rows_dev) * row_chunks;
     nchunks = lim < nchunks ? lim : nchunks;
@@ -68,6 +70,7 @@ __global__ void nv_amax_kernel(const uint4* __restrict__ in, long long nchunks,
   const long long G = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < nchunks;
        i += G) {
+    if (rowmap && rowmap[i / row_chunks] < 0) continue;
     const uint4 w = in[i];
     const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -149,6 +152,59 @@ __global__ void nv_quant_kernel(const uint4* __restrict__ in, long long nblk, in
     *reinterpret_cast<uint2*>(codes + 8 * b) = make_uint2(c[0], c[1]);
     scales[tiled_nkb > 0 ? nv_tiled_off(r, c16, tiled_nkb) : b] = sb;
   }
+}
+
+// Transposed NVFP4 of `ng` stacked bf16 matrices [K, C] (K along the rows):
+// out row g*C + c holds column c of matrix g as K values, quantised in blocks
+// of 16 along K -- codes [ng*C, K/2], scales in the tiled layout (K/64 blocks
+// per 128 rows) or row-major [ng*C, K/16].  One CTA per 64 x 64 tile: the tile is read row by row into
+// shared memory, then thread t quantises column t/4's 16 values 16*(t%4).. .
+__global__ void __launch_bounds__(256)
+    nv_quant_t_kernel(const uint16_t* __restrict__ in, int K, int C,
+                      const float* __restrict__ g_ptr, uint8_t* __restrict__ codes,
+                      uint8_t* __restrict__ scales, bool tiled) {
+  // row stride 65: the four 16-row bands a warp reads fall in different banks
+  __shared__ uint16_t tile[64][65];
+  const int kt = blockIdx.x, ct = blockIdx.y, grp = blockIdx.z;
+  const uint16_t* src = in + (static_cast<long long>(grp) * K + kt * 64) * C + ct * 64;
+  for (int i = threadIdx.x; i < 64 * 8; i += 256) {
+    const int r = i >> 3, c8 = i & 7;
+    const uint4 w = *reinterpret_cast<const uint4*>(src + static_cast<long long>(r) * C + 8 * c8);
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      tile[r][8 * c8 + 2 * j] = static_cast<uint16_t>(u[j] & 0xFFFFu);
+      tile[r][8 * c8 + 2 * j + 1] = static_cast<uint16_t>(u[j] >> 16);
+    }
+  }
+  __syncthreads();
+  const float g = *g_ptr;
+  const float six_g = 6.0f * g;
+  const int n = threadIdx.x >> 2, b = threadIdx.x & 3;
+  float v[16];
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    v[j] = __uint_as_float(static_cast<uint32_t>(tile[16 * b + j][n]) << 16);
+    amax = fmaxf(amax, fabsf(v[j]));
+  }
+  const float x = amax / six_g;
+  const uint8_t sb = static_cast<uint8_t>(cvt_e4m3x2(0.f, x) & 0xFFu);
+  float sb_hi, sb_f;
+  e4m3x2_to_f32(sb, &sb_hi, &sb_f);
+  const float denom = sb_f * g;
+  uint32_t c[2] = {0u, 0u};
+  if (sb != 0) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t byte = cvt_e2m1x2(v[2 * j + 1] / denom, v[2 * j] / denom);
+      c[j >> 2] |= byte << (8 * (j & 3));
+    }
+  }
+  const long long row = static_cast<long long>(grp) * C + ct * 64 + n;
+  const long long k16 = kt * 4 + b;
+  *reinterpret_cast<uint2*>(codes + row * (K / 2) + k16 * 8) = make_uint2(c[0], c[1]);
+  scales[tiled ? nv_tiled_off(row, k16, K / 64) : row * (K / 16) + k16] = sb;
 }
 
 // ---------------------------------------------------------------- GEMM ----
@@ -307,7 +363,9 @@ __global__ void __launch_bounds__(kNvThreads, 1)
 }  // namespace
 
 cudaError_t launch_nv_tensor_scale(const void* in, long long n, float* g, cudaStream_t st,
-                                   const int32_t* rows_dev, long long row_elems) {
+                                   const int32_t* rows_dev, long long row_elems,
+                                   const int32_t* rowmap) {
+  if ((rows_dev || rowmap) && row_elems < 8) return cudaErrorInvalidValue;
   cudaError_t e = cudaMemsetAsync(g, 0, sizeof(float), st);
   if (e != cudaSuccess) return e;
   const long long nchunks = n / 8;
@@ -318,10 +376,26 @@ cudaError_t launch_nv_tensor_scale(const void* in, long long n, float* g, cudaSt
     ProfScope prof("nvfp4_amax", st);
     nv_amax_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(
         static_cast<const uint4*>(in), nchunks, reinterpret_cast<unsigned*>(g), rows_dev,
-        row_elems / 8);
+        (rows_dev || rowmap) ? row_elems / 8 : 1, rowmap);
     count_launch();
   }
   nv_scale_kernel<<<1, 1, 0, st>>>(g);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nv_quant_t(const void* in, long long ng, long long K, long long C,
+                              const float* g, uint8_t* codes, uint8_t* scales, cudaStream_t st,
+                              bool tiled) {
+  // whole 128-row blocks of the tiled scale layout; 16-byte aligned rows
+  if (K % 64 || C % 128 || ng <= 0) return cudaErrorInvalidValue;
+  if (reinterpret_cast<uintptr_t>(in) % 16 || reinterpret_cast<uintptr_t>(codes) % 16)
+    return cudaErrorInvalidValue;
+  ProfScope prof("nvfp4_quantize_t", st);
+  dim3 grid(static_cast<unsigned>(K / 64), static_cast<unsigned>(C / 64),
+            static_cast<unsigned>(ng));
+  nv_quant_t_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(in), static_cast<int>(K),
+                                          static_cast<int>(C), g, codes, scales, tiled);
   count_launch();
   return cudaGetLastError();
 }
@@ -363,7 +437,8 @@ extern "C" mok_status mok_nvfp4_tensor_scale(const void* in, int64_t n, float* g
     if (grid > cap) grid = cap;
     ProfScope prof("nvfp4_amax", st);
     nv_amax_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(
-        static_cast<const uint4*>(in), nchunks, reinterpret_cast<unsigned*>(g), nullptr, 0);
+        static_cast<const uint4*>(in), nchunks, reinterpret_cast<unsigned*>(g), nullptr, 1,
+        nullptr);
     count_launch();
   }
   nv_scale_kernel<<<1, 1, 0, st>>>(g);
@@ -393,6 +468,23 @@ extern "C" mok_status mok_nvfp4_quantize(const void* in, int64_t rows, int64_t c
       nullptr, 0);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? MOK_OK : MOK_ERR_CUDA;
+}
+
+extern "C" mok_status mok_nvfp4_quantize_cols(const void* in, int64_t ng, int64_t K, int64_t C,
+                                              const float* g, uint8_t* codes, uint8_t* scales,
+                                              void* stream) {
+  if (ng < 0 || K <= 0 || C <= 0 || K % 64 || C % 128) return MOK_ERR_INVALID_ARG;
+  if (ng > 0 && (!in || !g || !codes || !scales)) return MOK_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(in) & 15u) || (reinterpret_cast<uintptr_t>(codes) & 15u) ||
+      (reinterpret_cast<uintptr_t>(g) & 3u) || K / 64 > 65535 || C / 64 > 65535 || ng > 65535)
+    return MOK_ERR_INVALID_ARG;
+  mok_status s = mok_check_device();
+  if (s != MOK_OK) return s;
+  if (ng == 0) return MOK_OK;
+  return launch_nv_quant_t(in, ng, K, C, g, codes, scales, static_cast<cudaStream_t>(stream),
+                           false) == cudaSuccess
+             ? MOK_OK
+             : MOK_ERR_CUDA;
 }
 
 extern "C" mok_status mok_gemm_nvfp4(int64_t M, int64_t N, int64_t K, const uint8_t* A,

@@ -92,6 +92,21 @@ def test_mxfp8_keeps_no_dispatched_rows(lib):
     _no_overlap(_regions(Lm, 1024, 2, 8, 256, 128, mb=256)[:-1], Lm.total)
 
 
+def test_nvfp4_weight_scales_sit_in_the_status_block(lib):
+    """NVFP4 keeps the weights' two fp32 tensor scales for the backward inside
+    the 256-byte status block (after the status word); the other dtypes keep
+    none."""
+    bf = _desc(T=1024, mb=256, ring=2)
+    nv = _desc(T=1024, mb=256, ring=2)
+    nv.dtype, nv.d, nv.I = 2, 256, 256
+    Lb, Ln = _lib.SavedLayout(), _lib.SavedLayout()
+    assert lib.mok_moe_saved_layout(ctypes.byref(bf), ctypes.byref(Lb)) == 0
+    assert lib.mok_moe_saved_layout(ctypes.byref(nv), ctypes.byref(Ln)) == 0
+    assert Lb.nv_weight_scales == (1 << 64) - 1
+    assert Ln.status + 4 <= Ln.nv_weight_scales and Ln.nv_weight_scales + 8 <= Ln.topk_idx
+    assert Ln.nv_weight_scales % 4 == 0 and Ln.topk_idx == 256
+
+
 def test_micro_batch_layout(lib):
     d = _desc(T=1024, mb=256, ring=2)
     L = _lib.SavedLayout()

@@ -164,15 +164,18 @@ def test_large_traffic_scales_the_slice_capture_to_the_algorithmic_bytes():
 
 def test_low_precision_peaks_and_bytes():
     """FP8 GEMMs against 2x and FP4 GEMMs against 6x the measured bf16 peak
-    (GB300's nominal dense ratios); NVFP4 forward operands are half a byte
-    plus a sixteenth of a scale byte per value."""
+    (GB300's nominal dense ratios); NVFP4 operands (the forward GEMMs' and
+    the gate/up dgrad's) are half a byte plus a sixteenth of a scale byte per
+    value."""
     assert bench.peak_ratio("mxfp8", "fwd_down") == 2.0
     assert bench.peak_ratio("nvfp4", "fwd_down") == 6.0
-    assert bench.peak_ratio("nvfp4", "bwd_gate_up_dgrad") == 1.0
+    assert bench.peak_ratio("nvfp4", "bwd_gate_up_dgrad") == 6.0
+    assert bench.peak_ratio("nvfp4", "bwd_down_dgrad_swiglu") == 1.0
     assert bench.peak_ratio("large", "fwd_down") == 1.0
     s = gen.workload_shape("nvfp4")
     R, d, I, E = s.R, s.d, s.I, s.E
     nv, bf = bench.gemm_bytes(s, nv=True), bench.gemm_bytes(s)
     q4 = 0.5 + 1 / 16
     assert nv["fwd_down"][0] == R * I * q4 + E * d * I * q4 + R * d * 4
-    assert nv["bwd_gate_up_dgrad"] == bf["bwd_gate_up_dgrad"]
+    assert nv["bwd_gate_up_dgrad"][0] == R * 2 * I * q4 + E * 2 * I * d * q4 + R * d * 4
+    assert nv["bwd_down_dgrad_swiglu"] == bf["bwd_down_dgrad_swiglu"]

@@ -61,6 +61,29 @@ def test_nvfp4_quantize_bit_exact(shape):
     assert (scales.cpu().numpy()[7, 0] == 0) and (codes.cpu().numpy()[7, :8] == 0).all()
 
 
+@pytest.mark.parametrize("ng,K,C", [(1, 64, 128), (3, 192, 256)])
+def test_nvfp4_quantize_cols_bit_exact(ng, K, C):
+    """The column quantiser (blocks of 16 down each column of each stacked
+    matrix) against the oracle's quantiser along K, bit for bit."""
+    rng = np.random.default_rng(ng * K + C)
+    a = rng.standard_normal((ng, K, C)).astype(np.float32) * np.exp(
+        rng.uniform(-10, 10, (ng, 1, C)).astype(np.float32))
+    a[0, 16:32, 5] = 0.0                    # an all-zero block
+    a[-1, :16, 7] *= 1e-20                  # a block whose scale underflows to 0
+    bits = gen.f32_to_bf16_bits(a)
+    x = _gpu.dev_bf16(bits)
+    g = api.nvfp4_tensor_scale(x)
+    codes, scales = api.nvfp4_quantize_cols(x, g)
+    vals = gen.bf16_bits_to_f32(bits).astype(np.float64)
+    _, q, sb, gr = nvfp4_ref.nvfp4_quantize(vals, 1)     # along K, one tensor scale
+    assert np.float32(g.item()) == np.float32(gr)
+    got_q = _decode_e2m1(codes.cpu().numpy()).reshape(ng, C, K)
+    got_s = _decode_e4m3(scales.cpu().numpy()).reshape(ng, C, K // 16)
+    assert np.array_equal(got_s, sb)
+    assert np.array_equal(got_q, q.transpose(0, 2, 1))
+    assert got_s[0, 5, 1] == 0 and got_s[-1, 7, 0] == 0
+
+
 def _gemm(ca, sa, ga, cb, sb, gb):
     dev = [torch.from_numpy(np.ascontiguousarray(v)).cuda() for v in (ca, sa, cb, sb)]
     gad = torch.tensor([ga], dtype=torch.float32, device="cuda")
