@@ -8,14 +8,16 @@ Source: [dothoosh] "Cursor Mixture-of-Kittens cuts MoE training latency by
 training kernels ran the expert GEMMs in MXFP8 and NVFP4.  The pages do not
 define NVFP4, so NVIDIA's published format is taken (a reading, listed in the
 design notes), with one fixed order of operations, all in float32 (the
-kernel's precision, so that both sides take every rounding decision alike):
+kernel's precision, so that both sides take every rounding decision alike);
+the block and element steps multiply by rounded reciprocals:
   * tensor scale   g   = amax(|a|) / 2688          (2688 = 6 * 448: the
                    largest E2M1 magnitude times the largest E4M3 one);
                    g = 1 for an all-zero tensor;
-  * block scale    s_b = RNE_E4M3(amax_b / (6 g))  (6 g rounded first;
-                   saturating at 448; a positive E4M3 value or 0);
-  * element        q   = RNE_E2M1(v / (s_b g))     (s_b g rounded first;
-                   saturating at +-6; 0 where s_b = 0);
+  * block scale    s_b = RNE_E4M3(amax_b * r6)     with r6 = RN(1 / RN(6 g));
+                   saturating at 448; a positive E4M3 value or 0;
+  * element        q   = RNE_E2M1(v * r_b)         with r_b = RN(1 / RN(s_b g))
+                   (the largest finite float32 where that overflows);
+                   saturating at +-6; 0 where s_b = 0;
   * value          q * s_b * g.
 E2M1: sign, two exponent bits (bias 1), one mantissa bit; magnitudes 0, 0.5,
 1, 1.5, 2, 3, 4, 6; ties go to the even code (mantissa bit 0).
@@ -66,11 +68,14 @@ def nvfp4_quantize(a, axis: int = -1):
     blocks = xf.reshape(xf.shape[:-1] + (n // BLOCK, BLOCK))
     amax_b = np.abs(blocks).max(axis=-1)
     six_g = np.float32(np.float32(6.0) * g)
-    sb = e4m3_round((amax_b / six_g).astype(np.float32).astype(np.float64))
+    r6 = np.float32(np.float32(1.0) / six_g)
+    sb = e4m3_round((amax_b * r6).astype(np.float32).astype(np.float64))
     sb = np.minimum(sb, E4M3_MAX)
     denom = (_f32(sb) * g).astype(np.float32)                    # s_b g, rounded
-    with np.errstate(divide="ignore", invalid="ignore"):
-        ratio = (blocks / denom[..., None]).astype(np.float32).astype(np.float64)
+    with np.errstate(divide="ignore", over="ignore"):
+        rb = (np.float32(1.0) / denom).astype(np.float32)        # inf where s_b = 0
+        rb = np.minimum(rb, np.finfo(np.float32).max)
+        ratio = (blocks * rb[..., None]).astype(np.float32).astype(np.float64)
     q = np.where(sb[..., None] > 0, e2m1_round(ratio), 0.0)
     deq = q * sb[..., None] * np.float64(g)
     out = np.moveaxis(deq.reshape(x.shape), -1, axis)
