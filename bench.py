@@ -40,6 +40,14 @@ from routing_dispatch_grouped_router_gb300 import inputs as gen  # noqa: E402
 
 METRIC = "MoE layer fwd+bwd tokens/s on 1 GB300; grouped-GEMM % of tensor-core peak"
 WORKLOAD = "large"
+# operand precision of the expert GEMMs: the workload's own, or --precision
+PRECISION = "bf16"
+
+
+def workload_precision(name: str) -> str:
+    """The precision a workload is defined with: mxfp8, nvfp4 or bf16."""
+    w = gen.WORKLOADS[name]
+    return "mxfp8" if name == "mxfp8" else ("nvfp4" if w.get("nvfp4") else "bf16")
 PROFILE_EVERY = 4  # per-kernel events on one timed step in this many
 
 # Algorithmic work per launch of each kernel (R = T*k routed rows).
@@ -53,13 +61,13 @@ MX_GEMMS = ("fwd_gate_up_swiglu", "fwd_down", "bwd_gate_up_dgrad")
 NV_GEMMS = ("fwd_gate_up_swiglu", "fwd_down", "bwd_gate_up_dgrad")
 
 
-def peak_ratio(workload: str, gemm: str) -> float:
+def peak_ratio(precision: str, gemm: str) -> float:
     """A GEMM's tensor peak relative to the measured bf16 one: the nominal
     dense ratios of GB300 (fp8 4.5 / bf16 2.25 PFLOP/s = 2, fp4 13.5 / 2.25 = 6)
     for the GEMMs that run on those operands."""
-    if workload == "mxfp8" and gemm in MX_GEMMS:
+    if precision == "mxfp8" and gemm in MX_GEMMS:
         return 2.0
-    if workload == "nvfp4" and gemm in NV_GEMMS:
+    if precision == "nvfp4" and gemm in NV_GEMMS:
         return 6.0
     return 1.0
 
@@ -377,7 +385,7 @@ def cpu_cores() -> int:
 # oracle widens each touched expert's weights to float64 (0.35 GB per expert on
 # the large workload), so slices are sized to a few seconds each
 SLICE_TOKENS = {"tiny": 32, "fine": 32, "imbalanced": 2, "mxfp8": 2, "nvfp4": 2, "large": 1,
-                "large_slice": 1}
+                "large_slice": 1, "nvfp4_slice": 2}
 
 
 def cpu_baseline(inp: dict, shape: gen.Shape, budget_s: float = 12.0,
@@ -428,13 +436,16 @@ def run_reference(args, shape: gen.Shape, rank: int):
 
 def workload_config(shape: gen.Shape) -> dict:
     w = gen.WORKLOADS[WORKLOAD]
-    prec = "bf16"
-    if WORKLOAD == "mxfp8":
-        prec = (f"MXFP8 operands, {shape.T // w['mb_tokens']} micro-batches of {w['mb_tokens']} "
-                f"tokens through a {w['ring_slots']}-slot ring")
-    if w.get("nvfp4"):
-        prec = ("NVFP4 operands (E2M1, E4M3 per 16, fp32 per tensor) for the forward GEMMs "
-                "and the gate/up dgrad")
+    prec = {"bf16": "bf16",
+            "mxfp8": "MXFP8 operands (E4M3, E8M0 per 32) for the forward GEMMs and the gate/up "
+                     "dgrad",
+            "nvfp4": "NVFP4 operands (E2M1, E4M3 per 16, fp32 per tensor) for the forward "
+                     "GEMMs and the gate/up dgrad"}[PRECISION]
+    if PRECISION != workload_precision(WORKLOAD):
+        prec += f" (the {WORKLOAD} workload run at this precision)"
+    if w.get("mb_tokens"):
+        prec += (f", {shape.T // w['mb_tokens']} micro-batches of {w['mb_tokens']} tokens "
+                 f"through a {w['ring_slots']}-slot ring")
     if w.get("zipf_s"):
         prec += f", Zipf({w['zipf_s']}) router bias"
     wbytes = shape.E * 3 * shape.I * shape.d * 2
@@ -451,13 +462,15 @@ def layer_options(api, bf16_wgrad: bool = False) -> dict:
     """MoELayer keyword arguments of the selected workload (bf16_wgrad: weight
     gradients returned in bf16, rounded once from the fp32 accumulation)."""
     w = gen.WORKLOADS[WORKLOAD]
-    if WORKLOAD == "mxfp8":
+    opts = {}
+    if w.get("mb_tokens"):
         if bf16_wgrad:
-            raise SystemExit("--bf16-wgrad: the micro-batched workload accumulates dW in fp32")
-        return dict(dtype=api.MXFP8, mb_tokens=w["mb_tokens"], ring_slots=w["ring_slots"])
-    opts = dict(flags=api.FLAG_BF16_WGRAD_OUT) if bf16_wgrad else {}
-    if w.get("nvfp4"):
-        opts["dtype"] = api.NVFP4
+            raise SystemExit("--bf16-wgrad: a micro-batched workload accumulates dW in fp32")
+        opts.update(mb_tokens=w["mb_tokens"], ring_slots=w["ring_slots"])
+    elif bf16_wgrad:
+        opts["flags"] = api.FLAG_BF16_WGRAD_OUT
+    if PRECISION != "bf16":
+        opts["dtype"] = {"mxfp8": api.MXFP8, "nvfp4": api.NVFP4}[PRECISION]
     return opts
 
 
@@ -556,10 +569,13 @@ def main():
     ap.add_argument("--workload", default="large", choices=sorted(gen.WORKLOADS),
                     help="large (default: the configuration the targets are stated on), "
                          "fine, imbalanced, mxfp8, nvfp4 or tiny")
+    ap.add_argument("--precision", default=None, choices=["bf16", "mxfp8", "nvfp4"],
+                    help="expert-GEMM operands (default: the workload's own)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
-    global WORKLOAD
+    global WORKLOAD, PRECISION
     WORKLOAD = args.workload
+    PRECISION = args.precision or workload_precision(WORKLOAD)
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -650,20 +666,20 @@ def main():
     peaks = load_peaks()
     write_gbs, write_rates = measure_write_gbs(torch, api)
     flops = gemm_flops(shape, int(layer.layout.mb_count))
-    gbytes = gemm_bytes(shape, int(layer.layout.mb_count), mx=WORKLOAD == "mxfp8",
+    gbytes = gemm_bytes(shape, int(layer.layout.mb_count), mx=PRECISION == "mxfp8",
                         wgrad_elem_bytes=2 if args.bf16_wgrad else 4,
-                        nv=WORKLOAD == "nvfp4")
+                        nv=PRECISION == "nvfp4")
 
     def gemm_roofline_us(n):
         """(bound, shortest time in us) of GEMM n: tensor time at the measured
         (FP8: x2) peak against HBM time at the copy and write bandwidths."""
-        t_tc = flops[n] / (peaks["bf16_sustained"] * peak_ratio(WORKLOAD, n) * 1e12) * 1e6
+        t_tc = flops[n] / (peaks["bf16_sustained"] * peak_ratio(PRECISION, n) * 1e12) * 1e6
         if n not in gbytes:
             return "tensor", t_tc
         t_mem = mover_roofline_us(gbytes[n][0], gbytes[n][1], peaks["hbm"], write_gbs)
         return ("hbm", t_mem) if t_mem > t_tc else ("tensor", t_tc)
     movers = mover_bytes(shape, int(layer.layout.mb_count))
-    if WORKLOAD == "mxfp8":
+    if PRECISION == "mxfp8":
         movers.update(mx_quant_bytes(shape, int(layer.layout.mb_count), int(layer.layout.rows_max),
                                      kernels, prof_steps))
     total_k = sum(v[1] for v in kernels.values())
@@ -686,8 +702,8 @@ def main():
                 "unit": "GB/s", "frac": ach / peaks["hbm"],
                 "frac_roofline": gemm_roofline_us(dom)[1] / (avg_s * 1e6),
                 "written_per_launch": tw, "write_bw_gbs": write_gbs,
-                "traffic": ncu_traffic(WORKLOAD, dom)[0],
-                "traffic_source": ncu_traffic(WORKLOAD, dom)[1],
+                "traffic": ncu_traffic(WORKLOAD if PRECISION == workload_precision(WORKLOAD) else "", dom)[0],
+                "traffic_source": ncu_traffic(WORKLOAD if PRECISION == workload_precision(WORKLOAD) else "", dom)[1],
                 "peak_source": f"hbm_gbs of {peaks['source']}; write bandwidth measured here "
                                "(1 GiB zero fill: the faster of torch's and the bulk-store one)",
                 "write_bw_fills_gbs": write_rates,
@@ -699,12 +715,12 @@ def main():
         ach = flops[dom] / avg_s / 1e12
         # block-scaled GEMMs run on the FP8 / FP4 tensor rates: their peak is the
         # measured bf16 one times the nominal ratio (peak_ratio)
-        ratio = peak_ratio(WORKLOAD, dom)
+        ratio = peak_ratio(PRECISION, dom)
         peak = peaks["bf16_sustained"] * ratio
         roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak,
                 "unit": "TFLOP/s", "frac": ach / peak,
-                "traffic": ncu_traffic(WORKLOAD, dom)[0],
-                "traffic_source": ncu_traffic(WORKLOAD, dom)[1],
+                "traffic": ncu_traffic(WORKLOAD if PRECISION == workload_precision(WORKLOAD) else "", dom)[0],
+                "traffic_source": ncu_traffic(WORKLOAD if PRECISION == workload_precision(WORKLOAD) else "", dom)[1],
                 "peak_source": f"bf16_tflops_sustained of {peaks['source']}"
                                + (f" x {ratio:g} (nominal low-precision/bf16 ratio)"
                                   if ratio != 1.0 else ""),
@@ -763,14 +779,14 @@ def main():
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": {"mxfp8": "mxfp8", "nvfp4": "nvfp4"}.get(WORKLOAD, "bf16"),
+            "dtype": PRECISION,
             "dtype_detail": {
                 "mxfp8": "E4M3 + E8M0 per 32: block-scaled FP8 MMAs for the forward GEMMs and "
                          "the gate/up dgrad; bf16 MMAs on MX-valued operands for the down "
                          "dgrad; weight gradients on bf16 hi/lo operands",
                 "nvfp4": "E2M1 + E4M3 per 16 + fp32 per tensor: block-scaled FP4 MMAs for "
                          "the forward GEMMs and the gate/up dgrad; the down dgrad and the "
-                         "weight gradients on the BF16 engine"}.get(WORKLOAD),
+                         "weight gradients on the BF16 engine"}.get(PRECISION),
             "data": "synthetic",
             "config": dict(workload_config(shape),
                            weight_grad_out="bf16" if args.bf16_wgrad else "fp32"),

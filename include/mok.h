@@ -152,6 +152,14 @@ typedef struct mok_saved_layout {
   size_t nv_weight_scales; /* MOK_NVFP4: fp32 [2] tensor scales of W_gate_up and W_down (the
                              backward reuses W_gate_up's, so the weights must not change
                              between the two calls); MOK_NOT_KEPT otherwise */
+  size_t w_gate_up_t;     /* W_gate_up along 2I, the gate/up dgrad's operand, written by the
+                             forward (column c of expert e's [2I, d] matrix as row e*d + c):
+                             MOK_NVFP4: E2M1 codes [E*d, I], then E*2I*d/16 E4M3 scale bytes;
+                             MOK_MXFP8: E4M3 codes [E*d, 2I], then E*2I*d/32 E8M0 bytes; the
+                             scales in the GEMM's tiled layout.  MOK_NOT_KEPT for MOK_BF16 */
+  size_t w_down_col;      /* MOK_MXFP8: W_down fake-quantised along d (blocks of 32 rows of
+                             each expert's [d, I] matrix), bf16 [E*d, I], the down dgrad's
+                             operand, written by the forward; MOK_NOT_KEPT otherwise */
   size_t rows_max;        /* number of padded rows the buffers hold: T*k + 127*min(E, T*k), rounded to 128 */
   size_t mb_count;        /* micro-batches (1 without micro-batching) */
   size_t mb_stride;       /* bytes between consecutive micro-batches' fields */
@@ -284,9 +292,10 @@ mok_status mok_mx_quantize(const void* in, int64_t rows, int64_t cols, int along
  * its fp32 operations this library's): E2M1 elements, one E4M3 scale per 16
  * consecutive values along K, one fp32 scale per tensor.
  *   g   = amax / 2688 (= 6 * 448), 1 for an all-zero tensor
- *   s_b = RNE_E4M3(amax_b / (6 g))      (6 g rounded to fp32 first; <= 448)
- *   q   = RNE_E2M1(v / (s_b g))         (s_b g rounded first; +-6 saturated;
- *                                        0 where s_b = 0)
+ *   s_b = RNE_E4M3(amax_b * RN(1 / RN(6 g)))          (<= 448)
+ *   q   = RNE_E2M1(v * RN(1 / RN(s_b g)))             (+-6 saturated; the
+ *         reciprocal capped at the largest finite float; 0 where s_b = 0)
+ * (RN: one fp32 rounding to nearest even.)
  * Finite inputs only (a NaN is ignored by the tensor amax).
  *
  * mok_nvfp4_tensor_scale: g of the n bf16 values at `in` (n % 8 == 0, `in`

@@ -23,7 +23,7 @@ class SavedLayout(ctypes.Structure):
     _fields_ = [(n, c_size_t) for n in (
         "status", "topk_idx", "topk_w", "counts", "offsets", "pos", "token_of_row",
         "padded_offsets", "padded_pos", "padded_token", "row_weight", "x_perm", "gate_up",
-        "nv_weight_scales", "rows_max", "mb_count", "mb_stride", "ring_slots", "ring_slot_bytes", "total")]
+        "nv_weight_scales", "w_gate_up_t", "w_down_col", "rows_max", "mb_count", "mb_stride", "ring_slots", "ring_slot_bytes", "total")]
 
 
 class KernelTime(ctypes.Structure):

@@ -214,6 +214,22 @@ void saved_layout(const Dims& D, mok_saved_layout* L, size_t* mtile_prefix_off) 
   L->ring_slots = static_cast<size_t>(D.ring);
   L->ring_slot_bytes = slot_al;
   L->total = ring0 + slot_al * D.ring;
+  // block-scaled weights in the backward's orientations, written by the
+  // forward from the same reads as its own codes: W_gate_up along 2I (the
+  // gate/up dgrad's operand: codes, then tiled scales) and, for MXFP8,
+  // W_down along d (the down dgrad's bf16 operand on MX values)
+  auto al = [](size_t v) { return (v + 255) & ~static_cast<size_t>(255); };
+  const size_t n = static_cast<size_t>(D.E) * 2 * D.I * D.d;
+  L->w_gate_up_t = MOK_NOT_KEPT;
+  L->w_down_col = MOK_NOT_KEPT;
+  if (D.nv || D.mx) {
+    L->w_gate_up_t = L->total;
+    L->total += al(D.nv ? n / 2 + n / 16 : n + n / 32);
+  }
+  if (D.mx) {
+    L->w_down_col = L->total;
+    L->total += al(static_cast<size_t>(D.E) * D.d * D.I * 2);
+  }
 }
 
 void fwd_layout(const Dims& D, FwdWs* W) {
@@ -271,7 +287,6 @@ void bwd_layout(const Dims& D, BwdWs* W) {
   W->rw_off = b.take(static_cast<size_t>(rw.ks + 1) * 4);
   W->rw_part = b.take(static_cast<size_t>(rw.ks) * epad * D.d * 4);
   const size_t wgu = static_cast<size_t>(D.E) * 2 * D.I * D.d * 2;
-  const size_t wd = static_cast<size_t>(D.E) * D.d * D.I * 2;
   W->dyq_row = D.mx ? b.take(rows * D.d * 2) : 0;  // MXFP8 copies
   W->dyq_col = D.mx ? b.take(ns * rows * D.d * 2) : 0;
   W->xq_col = D.mx ? b.take(ns * rows * D.d * 2) : 0;
@@ -279,15 +294,12 @@ void bwd_layout(const Dims& D, BwdWs* W) {
   W->x_def = (!D.mx && ns > 1) ? b.take(ns * rows * D.d * 2) : 0;
   // without micro-batches and with the dispatch recompute: x rows again
   W->x_rd = (D.recompute_dispatch && ns == 1) ? b.take(rows * D.d * 2) : 0;
-  // block-scaled operands of the gate/up dgrad: dG, dU codes and W_gate_up
-  // transposed ([E*d, 2I] values), both with tiled scales -- MXFP8 one byte
-  // and a scale per 32 values, NVFP4 half a byte and a scale per 16
-  const size_t dgu_n = rows * 2 * D.I, wgu_n = wgu / 2;
+  // block-scaled dG, dU (the gate/up dgrad's A operand; its B, W_gate_up
+  // along 2I, is in saved): codes with tiled scales -- MXFP8 one byte and a
+  // scale per 32 values, NVFP4 half a byte and a scale per 16
+  const size_t dgu_n = rows * 2 * D.I;
   W->dgu_codes = D.mx ? b.take(dgu_n) : D.nv ? b.take(dgu_n / 2) : 0;
   W->dgu_scales = D.mx ? b.take(dgu_n / 32) : D.nv ? b.take(dgu_n / 16) : 0;
-  W->wd_col = D.mx ? b.take(wd) : 0;
-  W->wgu_t_codes = D.mx ? b.take(wgu_n) : D.nv ? b.take(wgu_n / 2) : 0;
-  W->wgu_t_scales = D.mx ? b.take(wgu_n / 32) : D.nv ? b.take(wgu_n / 16) : 0;
   W->nv_g = D.nv ? b.take(256) : 0;  // NVFP4: dG/dU's tensor scale
   // recompute of g, u: their fp32 rows, and the forward's MXFP8 operands
   W->gu = D.recompute_gu ? b.take(rows * 2 * D.I * 4) : 0;
@@ -408,8 +420,13 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
   uint8_t* h_c = at<uint8_t>(workspace, F.h_codes);
   uint8_t* h_s = at<uint8_t>(workspace, F.h_scales);
   if (D.mx) {
-    MOK_CUDA(launch_mx_rows(w_gate_up, nullptr, D.E * 2 * D.I, D.d, wgu_c, wgu_s, st, true));
-    MOK_CUDA(launch_mx_rows(w_down, nullptr, D.E * D.d, D.I, wd_c, wd_s, st, true));
+    // each weight read once for both orientations: the backward's forms go
+    // to saved (W_gate_up along 2I as codes, W_down along d as bf16 values)
+    uint8_t* wt = at<uint8_t>(saved, L.w_gate_up_t);
+    MOK_CUDA(launch_mx_quant_2d(w_gate_up, D.E, 2 * D.I, D.d, wgu_c, wgu_s, wt,
+                                wt + D.E * 2 * D.I * D.d, nullptr, st));
+    MOK_CUDA(launch_mx_quant_2d(w_down, D.E, D.d, D.I, wd_c, wd_s, nullptr, nullptr,
+                                at<char>(saved, L.w_down_col), st));
   }
   // NVFP4: tensor scales [x, h] in the workspace; the weights', once per
   // call, in `saved` [W_gate_up, W_down] (the backward reuses W_gate_up's)
@@ -425,8 +442,11 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
   uint8_t* nwd_s = at<uint8_t>(workspace, F.nwd_scales);
   if (D.nv) {
     MOK_CUDA(launch_nv_tensor_scale(w_gate_up, D.E * 2 * D.I * D.d, nvw + 0, st));
-    MOK_CUDA(launch_nv_quant_tiled(w_gate_up, D.E * 2 * D.I, D.d, nvw + 0, nwgu_c, nwgu_s,
-                                   nullptr, 0, st));
+    // W_gate_up in both orientations: along d for this GEMM, along 2I (into
+    // saved) for the backward's gate/up dgrad
+    uint8_t* wt = at<uint8_t>(saved, L.w_gate_up_t);
+    MOK_CUDA(launch_nv_quant_2d(w_gate_up, D.E, 2 * D.I, D.d, nvw + 0, nwgu_c, nwgu_s, wt,
+                                wt + D.E * 2 * D.I * D.d / 2, st));
     MOK_CUDA(launch_nv_tensor_scale(w_down, D.E * D.d * D.I, nvw + 1, st));
     MOK_CUDA(launch_nv_quant_tiled(w_down, D.E * D.d, D.I, nvw + 1, nwd_c, nwd_s, nullptr, 0,
                                    st));
@@ -546,8 +566,12 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
   const bool bs = D.mx || D.nv;  // block-scaled gate/up dgrad
   uint8_t* dgu_c = bs ? at<uint8_t>(workspace, B.dgu_codes) : nullptr;
   uint8_t* dgu_s = bs ? at<uint8_t>(workspace, B.dgu_scales) : nullptr;
-  uint8_t* wgu_t_c = bs ? at<uint8_t>(workspace, B.wgu_t_codes) : nullptr;
-  uint8_t* wgu_t_s = bs ? at<uint8_t>(workspace, B.wgu_t_scales) : nullptr;
+  // (NVFP4: the forward left W_gate_up along 2I in saved)
+  // (the forward left W_gate_up along 2I in saved: codes, then scales)
+  const uint8_t* wgu_t_c = bs ? at<uint8_t>(saved, L.w_gate_up_t) : nullptr;
+  const uint8_t* wgu_t_s = D.mx   ? wgu_t_c + D.E * 2 * D.I * D.d
+                           : D.nv ? wgu_t_c + D.E * 2 * D.I * D.d / 2
+                                  : nullptr;
   // NVFP4: dG/dU's tensor scale (per micro-batch) and W_gate_up's (the forward's)
   float* nv_dgu_g = D.nv ? at<float>(workspace, B.nv_g) : nullptr;
   const float* nv_wgu_g = D.nv ? at<float>(saved, L.nv_weight_scales) : nullptr;
@@ -559,17 +583,8 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
   uint8_t* rxq_s = at<uint8_t>(workspace, B.xq_scales);
   if (D.mx && D.recompute_gu)
     MOK_CUDA(launch_mx_rows(w_gate_up, nullptr, D.E * 2 * D.I, D.d, rwgu_c, rwgu_s, st, true));
-  if (D.mx) {
-    // weights quantised once per call along the dgrads' reduction dims:
-    // W_down along d (bf16 values, blocks of 32 rows), W_gate_up along 2I
-    // (E4M3 codes written K-major for the block-scaled gate/up dgrad)
-    void* wd_q = at<char>(workspace, B.wd_col);
-    MOK_CUDA(launch_mx_cols(w_down, wd_q, D.E * D.d, D.I, nullptr, nullptr, st));
-    MOK_CUDA(launch_mx_cols_t(w_gate_up, D.E * 2 * D.I, D.d, 2 * D.I, wgu_t_c, wgu_t_s, st));
-    wd_op = wd_q;
-  }
-  if (D.nv)  // W_gate_up along 2I: codes [E*d, I] with tiled scales
-    MOK_CUDA(launch_nv_quant_t(w_gate_up, D.E, 2 * D.I, D.d, nv_wgu_g, wgu_t_c, wgu_t_s, st));
+  // MXFP8: W_down along d (bf16 values, blocks of 32 rows), from the forward
+  if (D.mx) wd_op = at<char>(saved, L.w_down_col);
   const size_t dx_esz = D.act_bf16 ? 2 : 4;
   // micro-batches in reverse, so the last ring slots are still resident.
   // With several micro-batches the expert weight gradients are deferred: each

@@ -72,7 +72,7 @@ struct FwdWs {
 struct BwdWs {
   size_t dy_perm, dgu_hi, dgu_lo, p_hi, p_lo, dp_part, dx_perm, dl_hi, dl_lo, rw_off, rw_part,
       dyq_row, dyq_col,
-      xq_col, dgu_codes, dgu_scales, wd_col, wgu_t_codes, wgu_t_scales, gu, xq_codes, xq_scales,
+      xq_col, dgu_codes, dgu_scales, gu, xq_codes, xq_scales,
       wgu_codes, wgu_scales, x_def, x_rd, nv_g, total;
 };
 struct StageWs {
@@ -269,6 +269,13 @@ cudaError_t launch_mx_rows(const void* in, void* out, long long rows, long long 
 // cols % 128).
 cudaError_t launch_mx_cols_t(const void* in, long long rows, long long cols, long long group_rows,
                              uint8_t* codes, uint8_t* scales, cudaStream_t st);
+// A weight [ng*K, C] in both block directions from one read: rows (blocks of
+// 32 along C) as codes [ng*K, C] with tiled scales, and columns (blocks of 32
+// along K) as codes [ng*C, K] with tiled scales (ccodes) or as bf16 values in
+// the input's layout (cvals; exactly one of the two).  K, C multiples of 128.
+cudaError_t launch_mx_quant_2d(const void* in, long long ng, long long K, long long C,
+                               uint8_t* rcodes, uint8_t* rscales, uint8_t* ccodes,
+                               uint8_t* cscales, void* cvals, cudaStream_t st);
 // Column blocks (rows % 32 == 0, cols % 8 == 0); rows_out != NULL also writes
 // the row-block dequantised values of the same input (cols % 32 == 0).
 cudaError_t launch_mx_cols(const void* in, void* out, long long rows, long long cols,
@@ -285,11 +292,14 @@ cudaError_t launch_mx_cols(const void* in, void* out, long long rows, long long 
 cudaError_t launch_nv_tensor_scale(const void* in, long long n, float* g, cudaStream_t st,
                                    const int32_t* rows_dev = nullptr, long long row_elems = 0,
                                    const int32_t* rowmap = nullptr);
-// The transposed form of ng stacked bf16 [K, C] matrices: codes [ng*C, K/2]
-// and tiled scales, blocks of 16 along K (K a multiple of 64, C of 128).
-cudaError_t launch_nv_quant_t(const void* in, long long ng, long long K, long long C,
-                              const float* g, uint8_t* codes, uint8_t* scales, cudaStream_t st,
-                              bool tiled = true);
+// NVFP4 of ng stacked bf16 [K, C] matrices in both orientations from one
+// read: rows (blocks along C: codes [ng*K, C/2], tiled scales) and columns
+// (blocks along K: codes [ng*C, K/2], scales tiled or row-major); NULL codes
+// skip an orientation.  K and C multiples of 128.
+cudaError_t launch_nv_quant_2d(const void* in, long long ng, long long K, long long C,
+                               const float* g, uint8_t* rcodes, uint8_t* rscales,
+                               uint8_t* ccodes, uint8_t* cscales, cudaStream_t st,
+                               bool ctiled = true);
 cudaError_t launch_nv_quant_tiled(const void* in, long long rows, long long cols, const float* g,
                                   uint8_t* codes, uint8_t* scales, const int32_t* map, int T,
                                   cudaStream_t st);

@@ -12,6 +12,7 @@
 #include "mok_internal.h"
 #include "mx.cuh"
 #include "ptx.cuh"
+#include "quant_tile.cuh"
 
 namespace mok {
 
@@ -344,6 +345,95 @@ __global__ void __launch_bounds__(256) mx_cols_t_kernel(const uint32_t* __restri
   }
 }
 
+// A weight [ng*K, C] (ng stacked [K, C] matrices) in both block directions
+// from one read: the rows (blocks of 32 along C) as E4M3 codes [ng*K, C] with
+// tiled scales (C/128 K groups), and the columns (blocks of 32 along K)
+// either as codes written transposed, [ng*C, K] (row g*C + c holds column c
+// of matrix g) with tiled scales (K/128 K groups), or as dequantised bf16
+// values in the input's layout.  Persistent CTAs walk the 128 x 128 tiles
+// (quant_tile.cuh); for each direction thread t takes line t % 128 and its
+// two blocks 2 (t / 128), +1: 64 contiguous code bytes and two adjacent scale
+// bytes.  The column values go back into the staged tile and leave in
+// coalesced 16-byte rows.
+__device__ __forceinline__ void mx_store32(uint8_t* p, const uint32_t (&a)[8]) {
+  uint4* q = reinterpret_cast<uint4*>(p);
+  q[0] = make_uint4(a[0], a[1], a[2], a[3]);
+  q[1] = make_uint4(a[4], a[5], a[6], a[7]);
+}
+
+__global__ void __launch_bounds__(256)
+    mx_quant_2d_kernel(const uint16_t* __restrict__ in, int K, int C, int ng,
+                       uint8_t* __restrict__ rcodes, uint8_t* __restrict__ rscales,
+                       uint8_t* __restrict__ ccodes, uint8_t* __restrict__ cscales,
+                       uint16_t* __restrict__ cvals) {
+  extern __shared__ __align__(16) uint16_t qt_smem[];
+  const int line = threadIdx.x & 127, pair = threadIdx.x >> 7;
+  qt_walk(in, K, C, ng, qt_smem, [&](uint16_t* tile, const QtTile& q) {
+    const long long row0 = static_cast<long long>(q.grp) * K + q.kt * 128;
+    {
+      // row `line`, values 64 pair .. 64 pair + 63: two blocks along C
+      const long long row = row0 + line;
+      uint32_t sc = 0u;
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        float v[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float u[8];
+          unpack8(*reinterpret_cast<const uint4*>(tile + line * kQtPitch + 64 * pair + 32 * b +
+                                                  8 * c),
+                  u);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[8 * c + j] = u[j];
+        }
+        uint32_t cw[8];
+        sc |= mx_encode32(v, cw) << (8 * b);
+        mx_store32(rcodes + row * C + q.ct * 128 + 64 * pair + 32 * b, cw);
+      }
+      *reinterpret_cast<uint16_t*>(rscales + mx_tiled_off(row, q.ct * 4 + 2 * pair, C / 128)) =
+          static_cast<uint16_t>(sc);
+    }
+    if (cvals) __syncthreads();  // the tile is rewritten below
+    {
+      // column `line`, values 64 pair .. 64 pair + 63 along K: two blocks
+      const long long orow = static_cast<long long>(q.grp) * C + q.ct * 128 + line;
+      uint32_t sc = 0u;
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        uint16_t* col = tile + (64 * pair + 32 * b) * kQtPitch + line;
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          v[j] = __uint_as_float(static_cast<uint32_t>(col[j * kQtPitch]) << 16);
+        if (ccodes) {
+          uint32_t cw[8];
+          sc |= mx_encode32(v, cw) << (8 * b);
+          mx_store32(ccodes + orow * K + q.kt * 128 + 64 * pair + 32 * b, cw);
+        } else {
+          mx_fake32(v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)  // rounded to bf16 as mx_quant8 does
+            col[j * kQtPitch] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
+        }
+      }
+      if (ccodes)
+        *reinterpret_cast<uint16_t*>(cscales +
+                                     mx_tiled_off(orow, q.kt * 4 + 2 * pair, K / 128)) =
+            static_cast<uint16_t>(sc);
+    }
+    if (cvals) {
+      __syncthreads();
+      uint16_t* dst = cvals + row0 * C + q.ct * 128;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = threadIdx.x + 256 * j, r = i >> 4, c8 = i & 15;
+        *reinterpret_cast<uint4*>(dst + static_cast<long long>(r) * C + 8 * c8) =
+            *reinterpret_cast<const uint4*>(tile + r * kQtPitch + 8 * c8);
+      }
+    }
+  });
+}
+
 static unsigned grid_for(long long n, int threads) {
   long long g = (n + threads - 1) / threads;
   const long long cap = static_cast<long long>(num_sms_current_device()) * 8;
@@ -439,6 +529,32 @@ cudaError_t launch_mx_cols_t(const void* in, long long rows, long long cols, lon
   mx_cols_t_kernel<<<static_cast<unsigned>(blocks < cap ? blocks : cap), 256, 0, st>>>(
       static_cast<const uint32_t*>(in), codes, scales, static_cast<uint32_t>(rows / 32),
       static_cast<uint32_t>(cols), static_cast<uint32_t>(group_rows));
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_quant_2d(const void* in, long long ng, long long K, long long C,
+                               uint8_t* rcodes, uint8_t* rscales, uint8_t* ccodes,
+                               uint8_t* cscales, void* cvals, cudaStream_t st) {
+  if (K % 128 || C % 128 || ng <= 0 || K / 128 > 65535 || C / 128 > 65535 || ng > 65535)
+    return cudaErrorInvalidValue;
+  if (!rcodes || !rscales || (!ccodes == !cvals) || (ccodes && !cscales))
+    return cudaErrorInvalidValue;
+  if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(rcodes) |
+       reinterpret_cast<uintptr_t>(ccodes) | reinterpret_cast<uintptr_t>(cvals)) & 15u ||
+      (reinterpret_cast<uintptr_t>(rscales) | reinterpret_cast<uintptr_t>(cscales)) & 1u)
+    return cudaErrorInvalidValue;
+  ProfScope prof("mx_quant_2d", st);
+  const cudaError_t e = cudaFuncSetAttribute(  // the two staging buffers
+      mx_quant_2d_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQtSmemBytes);
+  if (e != cudaSuccess) return e;
+  const long long ntiles = ng * (K / 128) * (C / 128);
+  if (ntiles >= (1LL << 31)) return cudaErrorInvalidValue;
+  const long long cap = static_cast<long long>(num_sms_current_device()) * 3;
+  mx_quant_2d_kernel<<<static_cast<unsigned>(ntiles < cap ? ntiles : cap), 256, kQtSmemBytes,
+                       st>>>(static_cast<const uint16_t*>(in), static_cast<int>(K),
+                             static_cast<int>(C), static_cast<int>(ng), rcodes, rscales, ccodes,
+                             cscales, static_cast<uint16_t*>(cvals));
   count_launch();
   return cudaGetLastError();
 }

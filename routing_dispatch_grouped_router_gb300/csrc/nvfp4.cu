@@ -9,10 +9,13 @@
 // define the format; NVIDIA's published NVFP4 is taken, with one fixed order
 // of fp32 operations:
 //   tensor scale   g   = amax / 2688 (6 * 448), or 1 for an all-zero tensor
-//   block scale    s_b = RNE_E4M3(amax_b / (6 g))      (6 g rounded first)
-//   element        q   = RNE_E2M1(v / (s_b g))         (s_b g rounded first;
-//                        0 where s_b = 0), saturating at +-6
+//   block scale    s_b = RNE_E4M3(amax_b * RN(1 / RN(6 g)))
+//   element        q   = RNE_E2M1(v * RN(1 / RN(s_b g)))   (the reciprocal
+//                        capped at the largest finite float; 0 where s_b = 0),
+//                        saturating at +-6
 //   value          q * s_b * g.
+// (Products with rounded reciprocals rather than quotients: one multiply per
+// element, which keeps the quantisers off the ALU limit.)
 //
 // The GEMM computes C[M,N] = alpha * sum_k qA[m,k] sA[m,k/16] qB[n,k] sB[n,k/16]
 // with alpha = gA * gB: the tensor cores apply the block scales, the epilogue
@@ -32,6 +35,7 @@
 #include "mok_internal.h"
 #include "mx.cuh"
 #include "ptx.cuh"
+#include "quant_tile.cuh"
 
 namespace mok {
 namespace {
@@ -98,6 +102,29 @@ __device__ __forceinline__ uint8_t cvt_e2m1x2(float hi, float lo) {
   return static_cast<uint8_t>(r);
 }
 
+// One NVFP4 block of 16 values: its E4M3 scale byte (returned) and its eight
+// code bytes (value 2i in the low nibble of byte i) in c.  r6 = RN(1 / RN(6 g)):
+//   s_b = RNE_E4M3(amax_b * r6),  q = RNE_E2M1(v * r_b),  r_b = RN(1 / RN(s_b g))
+// (r_b capped at the largest finite float, so that v = 0 gives 0).
+__device__ __forceinline__ uint8_t nv_block(const float (&v)[16], float g, float r6,
+                                            uint32_t (&c)[2]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  const uint8_t sb = static_cast<uint8_t>(cvt_e4m3x2(0.f, amax * r6) & 0xFFu);
+  float sb_hi, sb_f;
+  e4m3x2_to_f32(sb, &sb_hi, &sb_f);
+  c[0] = c[1] = 0u;
+  if (sb != 0) {
+    const float rb = fminf(__frcp_rn(sb_f * g), 3.402823466e38f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      c[j >> 2] |= static_cast<uint32_t>(cvt_e2m1x2(v[2 * j + 1] * rb, v[2 * j] * rb))
+                   << (8 * (j & 3));
+  }
+  return sb;
+}
+
 // One thread per block of 16 values along a row: 8 code bytes (value 2i in
 // the low nibble of byte i, 2i+1 in the high one) and one E4M3 scale byte.
 // tiled_nkb > 0: the scale bytes go to the tiled layout of a matrix with
@@ -109,12 +136,15 @@ __global__ void nv_quant_kernel(const uint4* __restrict__ in, long long nblk, in
                                 uint8_t* __restrict__ scales, long long tiled_nkb,
                                 const int32_t* __restrict__ map, int T) {
   const float g = *g_ptr;
-  const float six_g = 6.0f * g;
+  const float r6 = __frcp_rn(6.0f * g);
   const long long G = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long b = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; b < nblk;
-       b += G) {
-    const long long r = b / blk_per_row;
-    const int c16 = static_cast<int>(b - r * blk_per_row);
+  long long b = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  // row and block-in-row of b, stepped by G (one division per thread)
+  long long r = b / blk_per_row;
+  int c16 = static_cast<int>(b - r * blk_per_row);
+  const long long dr = G / blk_per_row;
+  const int dc = static_cast<int>(G - dr * blk_per_row);
+  for (; b < nblk; b += G) {
     long long src = b;
     bool zero = false;
     if (map) {
@@ -129,82 +159,95 @@ __global__ void nv_quant_kernel(const uint4* __restrict__ in, long long nblk, in
     }
     const uint32_t u[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
     float v[16];
-    float amax = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       v[2 * j] = bf16lo(u[j]);
       v[2 * j + 1] = bf16hi(u[j]);
-      amax = fmaxf(amax, fmaxf(fabsf(v[2 * j]), fabsf(v[2 * j + 1])));
     }
-    const float x = amax / six_g;
-    const uint8_t sb = static_cast<uint8_t>(cvt_e4m3x2(0.f, x) & 0xFFu);
-    float sb_hi, sb_f;
-    e4m3x2_to_f32(sb, &sb_hi, &sb_f);
-    const float denom = sb_f * g;
-    uint32_t c[2] = {0u, 0u};
-    if (sb != 0) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t byte = cvt_e2m1x2(v[2 * j + 1] / denom, v[2 * j] / denom);
-        c[j >> 2] |= byte << (8 * (j & 3));
-      }
-    }
+    uint32_t c[2];
+    const uint8_t sb = nv_block(v, g, r6, c);
     *reinterpret_cast<uint2*>(codes + 8 * b) = make_uint2(c[0], c[1]);
     scales[tiled_nkb > 0 ? nv_tiled_off(r, c16, tiled_nkb) : b] = sb;
+    r += dr;
+    c16 += dc;
+    if (c16 >= blk_per_row) {
+      c16 -= blk_per_row;
+      ++r;
+    }
   }
 }
 
-// Transposed NVFP4 of `ng` stacked bf16 matrices [K, C] (K along the rows):
-// out row g*C + c holds column c of matrix g as K values, quantised in blocks
-// of 16 along K -- codes [ng*C, K/2], scales in the tiled layout (K/64 blocks
-// per 128 rows) or row-major [ng*C, K/16].  One CTA per 64 x 64 tile: the tile is read row by row into
-// shared memory, then thread t quantises column t/4's 16 values 16*(t%4).. .
+// NVFP4 of `ng` stacked bf16 matrices [K, C] (row-major) in both
+// orientations from one read: the rows (blocks of 16 along C; codes
+// [ng*K, C/2], scales tiled with C/64 blocks per 128 rows) and the columns
+// (blocks of 16 along K; out row g*C + c holds column c of matrix g: codes
+// [ng*C, K/2], scales tiled with K/64 blocks per 128 rows, or row-major
+// [ng*C, K/16]).  Either output may be skipped (NULL codes).  Persistent CTAs
+// walk the 128 x 128 tiles (quant_tile.cuh); for each orientation thread t
+// takes line t % 128 and its blocks 4 (t / 128) .. +3, so it writes 32
+// contiguous code bytes and 4 contiguous scale bytes.
 __global__ void __launch_bounds__(256)
-    nv_quant_t_kernel(const uint16_t* __restrict__ in, int K, int C,
-                      const float* __restrict__ g_ptr, uint8_t* __restrict__ codes,
-                      uint8_t* __restrict__ scales, bool tiled) {
-  // row stride 65: the four 16-row bands a warp reads fall in different banks
-  __shared__ uint16_t tile[64][65];
-  const int kt = blockIdx.x, ct = blockIdx.y, grp = blockIdx.z;
-  const uint16_t* src = in + (static_cast<long long>(grp) * K + kt * 64) * C + ct * 64;
-  for (int i = threadIdx.x; i < 64 * 8; i += 256) {
-    const int r = i >> 3, c8 = i & 7;
-    const uint4 w = *reinterpret_cast<const uint4*>(src + static_cast<long long>(r) * C + 8 * c8);
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      tile[r][8 * c8 + 2 * j] = static_cast<uint16_t>(u[j] & 0xFFFFu);
-      tile[r][8 * c8 + 2 * j + 1] = static_cast<uint16_t>(u[j] >> 16);
-    }
-  }
-  __syncthreads();
+    nv_quant_2d_kernel(const uint16_t* __restrict__ in, int K, int C, int ng,
+                       const float* __restrict__ g_ptr, uint8_t* __restrict__ rcodes,
+                       uint8_t* __restrict__ rscales, uint8_t* __restrict__ ccodes,
+                       uint8_t* __restrict__ cscales, bool ctiled) {
+  extern __shared__ __align__(16) uint16_t qt_smem[];
   const float g = *g_ptr;
-  const float six_g = 6.0f * g;
-  const int n = threadIdx.x >> 2, b = threadIdx.x & 3;
-  float v[16];
-  float amax = 0.f;
+  const float r6 = __frcp_rn(6.0f * g);
+  const int line = threadIdx.x & 127, quad = threadIdx.x >> 7;
+  qt_walk(in, K, C, ng, qt_smem, [&](uint16_t* tile, const QtTile& q) {
+    if (rcodes) {
+      // row `line` of the tile, values 64 quad .. 64 quad + 63 (blocks 4 quad ..)
+      const long long row = static_cast<long long>(q.grp) * K + q.kt * 128 + line;
+      uint4* cp = reinterpret_cast<uint4*>(rcodes + row * (C / 2) + q.ct * 64 + 32 * quad);
+      uint32_t sw = 0u, cw[8];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    v[j] = __uint_as_float(static_cast<uint32_t>(tile[16 * b + j][n]) << 16);
-    amax = fmaxf(amax, fabsf(v[j]));
-  }
-  const float x = amax / six_g;
-  const uint8_t sb = static_cast<uint8_t>(cvt_e4m3x2(0.f, x) & 0xFFu);
-  float sb_hi, sb_f;
-  e4m3x2_to_f32(sb, &sb_hi, &sb_f);
-  const float denom = sb_f * g;
-  uint32_t c[2] = {0u, 0u};
-  if (sb != 0) {
+      for (int blk = 0; blk < 4; ++blk) {
+        const uint16_t* src = tile + line * kQtPitch + 64 * quad + 16 * blk;
+        const uint4 a = *reinterpret_cast<const uint4*>(src);
+        const uint4 b = *reinterpret_cast<const uint4*>(src + 8);
+        const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        float v[16];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t byte = cvt_e2m1x2(v[2 * j + 1] / denom, v[2 * j] / denom);
-      c[j >> 2] |= byte << (8 * (j & 3));
+        for (int j = 0; j < 8; ++j) {
+          v[2 * j] = bf16lo(u[j]);
+          v[2 * j + 1] = bf16hi(u[j]);
+        }
+        uint32_t c[2];
+        sw |= static_cast<uint32_t>(nv_block(v, g, r6, c)) << (8 * blk);
+        cw[2 * blk] = c[0];
+        cw[2 * blk + 1] = c[1];
+      }
+      // one 32-byte run: both halves of a sector from the same thread
+      cp[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      cp[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+      *reinterpret_cast<uint32_t*>(rscales + nv_tiled_off(row, q.ct * 8 + 4 * quad, C / 64)) =
+          sw;
     }
-  }
-  const long long row = static_cast<long long>(grp) * C + ct * 64 + n;
-  const long long k16 = kt * 4 + b;
-  *reinterpret_cast<uint2*>(codes + row * (K / 2) + k16 * 8) = make_uint2(c[0], c[1]);
-  scales[tiled ? nv_tiled_off(row, k16, K / 64) : row * (K / 16) + k16] = sb;
+    if (ccodes) {
+      // column `line` of the tile, values 64 quad .. 64 quad + 63 along K
+      const long long row = static_cast<long long>(q.grp) * C + q.ct * 128 + line;
+      const long long k16 = q.kt * 8 + 4 * quad;
+      uint4* cp = reinterpret_cast<uint4*>(ccodes + row * (K / 2) + k16 * 8);
+      uint32_t sw = 0u, cw[8];
+#pragma unroll
+      for (int blk = 0; blk < 4; ++blk) {
+        const uint16_t* col = tile + (64 * quad + 16 * blk) * kQtPitch + line;
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          v[j] = __uint_as_float(static_cast<uint32_t>(col[j * kQtPitch]) << 16);
+        uint32_t c[2];
+        sw |= static_cast<uint32_t>(nv_block(v, g, r6, c)) << (8 * blk);
+        cw[2 * blk] = c[0];
+        cw[2 * blk + 1] = c[1];
+      }
+      cp[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      cp[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+      *reinterpret_cast<uint32_t*>(cscales + (ctiled ? nv_tiled_off(row, k16, K / 64)
+                                                     : row * (K / 16) + k16)) = sw;
+    }
+  });
 }
 
 // ---------------------------------------------------------------- GEMM ----
@@ -384,18 +427,29 @@ cudaError_t launch_nv_tensor_scale(const void* in, long long n, float* g, cudaSt
   return cudaGetLastError();
 }
 
-cudaError_t launch_nv_quant_t(const void* in, long long ng, long long K, long long C,
-                              const float* g, uint8_t* codes, uint8_t* scales, cudaStream_t st,
-                              bool tiled) {
-  // whole 128-row blocks of the tiled scale layout; 16-byte aligned rows
-  if (K % 64 || C % 128 || ng <= 0) return cudaErrorInvalidValue;
-  if (reinterpret_cast<uintptr_t>(in) % 16 || reinterpret_cast<uintptr_t>(codes) % 16)
+cudaError_t launch_nv_quant_2d(const void* in, long long ng, long long K, long long C,
+                               const float* g, uint8_t* rcodes, uint8_t* rscales,
+                               uint8_t* ccodes, uint8_t* cscales, cudaStream_t st, bool ctiled) {
+  // whole 128 x 128 tiles (whole 128-row blocks of both tiled layouts)
+  if (K % 128 || C % 128 || ng <= 0 || K / 128 > 65535 || C / 128 > 65535 || ng > 65535)
     return cudaErrorInvalidValue;
-  ProfScope prof("nvfp4_quantize_t", st);
-  dim3 grid(static_cast<unsigned>(K / 64), static_cast<unsigned>(C / 64),
-            static_cast<unsigned>(ng));
-  nv_quant_t_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(in), static_cast<int>(K),
-                                          static_cast<int>(C), g, codes, scales, tiled);
+  if ((rcodes && !rscales) || (ccodes && !cscales) || (!rcodes && !ccodes))
+    return cudaErrorInvalidValue;
+  if (reinterpret_cast<uintptr_t>(in) % 16 || reinterpret_cast<uintptr_t>(rcodes) % 16 ||
+      reinterpret_cast<uintptr_t>(ccodes) % 16 || reinterpret_cast<uintptr_t>(rscales) % 4 ||
+      reinterpret_cast<uintptr_t>(cscales) % 4)
+    return cudaErrorInvalidValue;
+  ProfScope prof(rcodes && ccodes ? "nvfp4_quantize_2d" : "nvfp4_quantize_cols", st);
+  const cudaError_t e = cudaFuncSetAttribute(  // the two staging buffers
+      nv_quant_2d_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQtSmemBytes);
+  if (e != cudaSuccess) return e;
+  const long long ntiles = ng * (K / 128) * (C / 128);
+  if (ntiles >= (1LL << 31)) return cudaErrorInvalidValue;
+  const long long cap = static_cast<long long>(num_sms_current_device()) * 3;
+  nv_quant_2d_kernel<<<static_cast<unsigned>(ntiles < cap ? ntiles : cap), 256, kQtSmemBytes,
+                       st>>>(static_cast<const uint16_t*>(in), static_cast<int>(K),
+                             static_cast<int>(C), static_cast<int>(ng), g, rcodes, rscales,
+                             ccodes, cscales, ctiled);
   count_launch();
   return cudaGetLastError();
 }
@@ -473,16 +527,17 @@ extern "C" mok_status mok_nvfp4_quantize(const void* in, int64_t rows, int64_t c
 extern "C" mok_status mok_nvfp4_quantize_cols(const void* in, int64_t ng, int64_t K, int64_t C,
                                               const float* g, uint8_t* codes, uint8_t* scales,
                                               void* stream) {
-  if (ng < 0 || K <= 0 || C <= 0 || K % 64 || C % 128) return MOK_ERR_INVALID_ARG;
+  if (ng < 0 || K <= 0 || C <= 0 || K % 128 || C % 128) return MOK_ERR_INVALID_ARG;
   if (ng > 0 && (!in || !g || !codes || !scales)) return MOK_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(in) & 15u) || (reinterpret_cast<uintptr_t>(codes) & 15u) ||
-      (reinterpret_cast<uintptr_t>(g) & 3u) || K / 64 > 65535 || C / 64 > 65535 || ng > 65535)
+      (reinterpret_cast<uintptr_t>(scales) & 3u) || (reinterpret_cast<uintptr_t>(g) & 3u) ||
+      K / 128 > 65535 || C / 128 > 65535 || ng > 65535)
     return MOK_ERR_INVALID_ARG;
   mok_status s = mok_check_device();
   if (s != MOK_OK) return s;
   if (ng == 0) return MOK_OK;
-  return launch_nv_quant_t(in, ng, K, C, g, codes, scales, static_cast<cudaStream_t>(stream),
-                           false) == cudaSuccess
+  return launch_nv_quant_2d(in, ng, K, C, g, nullptr, nullptr, codes, scales,
+                            static_cast<cudaStream_t>(stream), false) == cudaSuccess
              ? MOK_OK
              : MOK_ERR_CUDA;
 }

@@ -38,6 +38,10 @@ WORKLOADS = {
     # the imbalanced workload's shape without its router bias, with the forward
     # expert GEMMs on NVFP4 operands
     "nvfp4":      dict(T=16384, d=4096, E=128, I=1536, k=8, nvfp4=True),
+    # the nvfp4 workload's widths and rows per expert with 1/8 of its experts
+    # and tokens (0.6 GB of weights): its kernels at a size a full profiler
+    # capture can replay
+    "nvfp4_slice": dict(T=2048, d=4096, E=16, I=1536, k=8, nvfp4=True),
 }
 
 # Scale of the Zipf offsets for the imbalanced workload (seed 0), found by

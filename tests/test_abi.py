@@ -79,8 +79,9 @@ def test_workspace_sizes_cover_the_layout(lib):
 
 def test_mxfp8_keeps_no_dispatched_rows(lib):
     """MXFP8 quantises the dispatched x rows straight from the token rows, so
-    `saved` has no ring of bf16 rows: x_perm is not kept and the buffer is
-    that much smaller than the BF16 one."""
+    `saved` has no ring of bf16 rows: x_perm is not kept.  It keeps the
+    weights in the backward's orientations instead (W_gate_up along 2I as
+    codes and scales, W_down along d as bf16 values)."""
     bf = _desc(T=1024, mb=256, ring=2)
     mx = _desc(T=1024, mb=256, ring=2)
     mx.dtype = 1
@@ -88,21 +89,31 @@ def test_mxfp8_keeps_no_dispatched_rows(lib):
     assert lib.mok_moe_saved_layout(ctypes.byref(bf), ctypes.byref(Lb)) == 0
     assert lib.mok_moe_saved_layout(ctypes.byref(mx), ctypes.byref(Lm)) == 0
     assert Lm.x_perm == (1 << 64) - 1 and Lm.ring_slot_bytes == 0  # MOK_NOT_KEPT
-    assert Lb.total - Lm.total == 2 * Lb.ring_slot_bytes
+    # ... and keeps the weights' backward forms instead (after everything else)
+    n = mx.E * 2 * mx.I * mx.d
+    wt = (n + n // 32 + 255) // 256 * 256
+    wd = (mx.E * mx.d * mx.I * 2 + 255) // 256 * 256
+    assert Lm.w_gate_up_t + wt == Lm.w_down_col and Lm.w_down_col + wd == Lm.total
+    assert Lb.total - (Lm.total - wt - wd) == 2 * Lb.ring_slot_bytes
+    assert Lb.w_gate_up_t == Lb.w_down_col == (1 << 64) - 1
     _no_overlap(_regions(Lm, 1024, 2, 8, 256, 128, mb=256)[:-1], Lm.total)
 
 
 def test_nvfp4_weight_scales_sit_in_the_status_block(lib):
     """NVFP4 keeps the weights' two fp32 tensor scales for the backward inside
-    the 256-byte status block (after the status word); the other dtypes keep
-    none."""
+    the 256-byte status block (after the status word), and W_gate_up along 2I
+    after everything else; the other dtypes keep neither."""
     bf = _desc(T=1024, mb=256, ring=2)
     nv = _desc(T=1024, mb=256, ring=2)
     nv.dtype, nv.d, nv.I = 2, 256, 256
     Lb, Ln = _lib.SavedLayout(), _lib.SavedLayout()
     assert lib.mok_moe_saved_layout(ctypes.byref(bf), ctypes.byref(Lb)) == 0
     assert lib.mok_moe_saved_layout(ctypes.byref(nv), ctypes.byref(Ln)) == 0
-    assert Lb.nv_weight_scales == (1 << 64) - 1
+    assert Lb.nv_weight_scales == (1 << 64) - 1 and Lb.w_gate_up_t == (1 << 64) - 1
+    # W_gate_up along 2I after everything else: codes and scales of E*2I*d values
+    n = nv.E * 2 * nv.I * nv.d
+    assert Ln.w_gate_up_t % 256 == 0 and Ln.w_gate_up_t + n // 2 + n // 16 <= Ln.total
+    assert Ln.w_gate_up_t >= 256 + Ln.mb_count * Ln.mb_stride  # after the micro-batch blocks
     assert Ln.status + 4 <= Ln.nv_weight_scales and Ln.nv_weight_scales + 8 <= Ln.topk_idx
     assert Ln.nv_weight_scales % 4 == 0 and Ln.topk_idx == 256
 

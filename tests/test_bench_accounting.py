@@ -44,17 +44,30 @@ def test_mover_bytes_follow_the_fp32_row_layout():
 def test_workload_options():
     class FakeApi:
         MXFP8 = 1
+        NVFP4 = 2
+        FLAG_BF16_WGRAD_OUT = 2
     assert bench.WORKLOAD == "large"  # the default: the configuration the targets name
-    bench.WORKLOAD = "mxfp8"
-    try:
-        opts = bench.layer_options(FakeApi)
-        assert opts == dict(dtype=1, mb_tokens=2048, ring_slots=2)
-        assert "MXFP8" in bench.workload_config(gen.workload_shape("mxfp8"))["workload"]
-    finally:
-        bench.WORKLOAD = "large"
-    assert bench.layer_options(FakeApi) == {}
-    assert bench.workload_config(gen.workload_shape("large"))["workload"].startswith(
-        "large: T=8192 d=7168 E=384 I=2048 top-8")
+    assert bench.PRECISION == "bf16"
+
+    def opts(workload, precision=None):
+        bench.WORKLOAD = workload
+        bench.PRECISION = precision or bench.workload_precision(workload)
+        try:
+            return (bench.layer_options(FakeApi),
+                    bench.workload_config(gen.workload_shape(workload))["workload"])
+        finally:
+            bench.WORKLOAD, bench.PRECISION = "large", "bf16"
+    o, cfg = opts("mxfp8")
+    assert o == dict(dtype=1, mb_tokens=2048, ring_slots=2) and "MXFP8" in cfg
+    # the same micro-batched ring at another precision
+    o, cfg = opts("mxfp8", "bf16")
+    assert o == dict(mb_tokens=2048, ring_slots=2)
+    assert "8 micro-batches of 2048 tokens" in cfg and "at this precision" in cfg
+    o, cfg = opts("nvfp4")
+    assert o == dict(dtype=2) and "NVFP4" in cfg
+    o, cfg = opts("large")
+    assert o == {} and cfg.startswith("large: T=8192 d=7168 E=384 I=2048 top-8")
+    assert bench.workload_precision("imbalanced") == "bf16"
 
 
 def test_router_wgrad_reduce_folds_into_the_router_gradient():
