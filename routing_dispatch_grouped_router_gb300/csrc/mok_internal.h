@@ -214,7 +214,7 @@ cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* 
                                 void* P_lo, uint8_t* dgu_codes, uint8_t* dgu_scales,
                                 float* dp_part, int* status, cudaStream_t st);
 // MXFP8: dX_perm = dGU W_gate_up per expert on the block-scaled tensor cores,
-// dGU as the codes B2 writes, W_gate_up as launch_mx_cols_t writes it.
+// dGU as the codes B2 writes, W_gate_up as launch_mx_quant_2d writes it (along 2I).
 cudaError_t gemm_bwd_gate_up_dgrad_mx(const Dims& D, const uint8_t* dgu_codes,
                                       const uint8_t* dgu_scales, const uint8_t* wgu_t_codes,
                                       const uint8_t* wgu_t_scales, const int32_t* mtile_prefix,
@@ -264,11 +264,7 @@ cudaError_t gemm_dense_bf16(int64_t M, int64_t N, int64_t K, const void* A, bool
 cudaError_t launch_mx_rows(const void* in, void* out, long long rows, long long cols,
                            uint8_t* codes, uint8_t* scales, cudaStream_t st, bool tiled = false,
                            const int32_t* rowmap = nullptr, int T = 0);
-// Column blocks of a weight [rows = E*group_rows, cols] written as the K-major
-// operand [E*cols, group_rows]: E4M3 codes and tiled scales (group_rows % 128,
-// cols % 128).
-cudaError_t launch_mx_cols_t(const void* in, long long rows, long long cols, long long group_rows,
-                             uint8_t* codes, uint8_t* scales, cudaStream_t st);
+
 // A weight [ng*K, C] in both block directions from one read: rows (blocks of
 // 32 along C) as codes [ng*K, C] with tiled scales, and columns (blocks of 32
 // along K) as codes [ng*C, K] with tiled scales (ccodes) or as bf16 values in

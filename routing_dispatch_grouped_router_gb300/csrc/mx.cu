@@ -283,68 +283,6 @@ __global__ void __launch_bounds__(256, ROWS_OUT ? 3 : 4) mx_cols_kernel(const ui
   }
 }
 
-// Column blocks written transposed, for a weight stored [E*G rows, C cols]
-// (G rows per expert) that an MMA needs K-major along G: the E4M3 codes go to
-// [E*C rows, G cols] (row e*C + c holds expert e's column c) with the scales
-// in the tiled layout of that matrix (mx_tiled_off, G/128 K groups).  One warp
-// per 32-row block and 64 columns: lane l holds columns 2l, 2l+1 of the 32
-// rows (bf16 pairs, 128 contiguous bytes per warp and row), so each lane has
-// two whole blocks and writes each block's 32 codes as one 32-byte run.
-__global__ void __launch_bounds__(256) mx_cols_t_kernel(const uint32_t* __restrict__ in,
-                                                        uint8_t* __restrict__ codes,
-                                                        uint8_t* __restrict__ scales,
-                                                        uint32_t row_blocks, uint32_t cols,
-                                                        uint32_t group_rows) {
-  grid_dep_launch();  // a GEMM after this kernel may start its prologue
-  const int lane = threadIdx.x & 31;
-  const uint32_t cp = cols / 2;          // bf16 pairs per row
-  const uint32_t groups_c = cols / 64;   // 64-column groups per row
-  const uint32_t kb = group_rows / 32;   // 32-row blocks per expert
-  const uint32_t n_kg = group_rows / 128;
-  const uint32_t nwork = row_blocks * groups_c;
-  const uint32_t nwarps = gridDim.x * (blockDim.x / 32);
-  for (uint32_t wi = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; wi < nwork;
-       wi += nwarps) {
-    const uint32_t rb = wi / groups_c, cg = wi - rb * groups_c;
-    const uint32_t e = rb / kb, j = rb - e * kb;
-    const uint32_t c2 = cg * 32 + lane;
-    uint32_t x[32];
-#pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      const uint32_t* p = in + (static_cast<long long>(rb) * 32 + r) * cp + c2;
-      asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(x[r]) : "l"(p));
-    }
-    float m0 = 0.f, m1 = 0.f;
-#pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      m0 = fmaxf(m0, fabsf(bf16lo(x[r])));
-      m1 = fmaxf(m1, fabsf(bf16hi(x[r])));
-    }
-    const int s0 = mx_shared_of(m0), s1 = mx_shared_of(m1);
-    const float d0 = exp2i(-s0), d1 = exp2i(-s1);
-    uint32_t w0[8], w1[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      // cvt packs its first operand into the upper byte: rows 4i..4i+3 in order
-      const uint32_t a01 = cvt_e4m3x2(bf16lo(x[4 * i + 1]) * d0, bf16lo(x[4 * i]) * d0);
-      const uint32_t a23 = cvt_e4m3x2(bf16lo(x[4 * i + 3]) * d0, bf16lo(x[4 * i + 2]) * d0);
-      const uint32_t b01 = cvt_e4m3x2(bf16hi(x[4 * i + 1]) * d1, bf16hi(x[4 * i]) * d1);
-      const uint32_t b23 = cvt_e4m3x2(bf16hi(x[4 * i + 3]) * d1, bf16hi(x[4 * i + 2]) * d1);
-      w0[i] = a01 | (a23 << 16);
-      w1[i] = b01 | (b23 << 16);
-    }
-    const long long orow = static_cast<long long>(e) * cols + 2 * c2;  // column 2*c2's row
-    uint4* o0 = reinterpret_cast<uint4*>(codes + orow * group_rows + j * 32);
-    uint4* o1 = reinterpret_cast<uint4*>(codes + (orow + 1) * group_rows + j * 32);
-    o0[0] = make_uint4(w0[0], w0[1], w0[2], w0[3]);
-    o0[1] = make_uint4(w0[4], w0[5], w0[6], w0[7]);
-    o1[0] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-    o1[1] = make_uint4(w1[4], w1[5], w1[6], w1[7]);
-    scales[mx_tiled_off(orow, j, n_kg)] = static_cast<uint8_t>(s0 + 127);
-    scales[mx_tiled_off(orow + 1, j, n_kg)] = static_cast<uint8_t>(s1 + 127);
-  }
-}
-
 // A weight [ng*K, C] (ng stacked [K, C] matrices) in both block directions
 // from one read: the rows (blocks of 32 along C) as E4M3 codes [ng*K, C] with
 // tiled scales (C/128 K groups), and the columns (blocks of 32 along K)
@@ -510,25 +448,6 @@ cudaError_t launch_mx_cols(const void* in, void* out, long long rows, long long 
     mx_cols_kernel<false, true, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, r4, rb, cols, rm);
   else
     mx_cols_kernel<false, false, false><<<grid, 256, 0, st>>>(i4, o4, codes, scales, r4, rb, cols, rm);
-  count_launch();
-  return cudaGetLastError();
-}
-
-cudaError_t launch_mx_cols_t(const void* in, long long rows, long long cols, long long group_rows,
-                             uint8_t* codes, uint8_t* scales, cudaStream_t st) {
-  if (group_rows <= 0 || group_rows % 128 || rows % group_rows || cols % 128 || !codes ||
-      !scales)
-    return cudaErrorInvalidValue;
-  const long long nwork = (rows / 32) * (cols / 64);
-  if (nwork == 0) return cudaSuccess;
-  if (nwork >= (1LL << 31) || cols >= (1LL << 31) || group_rows >= (1LL << 31))
-    return cudaErrorInvalidValue;
-  ProfScope prof("mx_quant_cols", st);
-  const long long blocks = (nwork + 7) / 8;  // 8 warps per CTA
-  const long long cap = static_cast<long long>(num_sms_current_device()) * 8;
-  mx_cols_t_kernel<<<static_cast<unsigned>(blocks < cap ? blocks : cap), 256, 0, st>>>(
-      static_cast<const uint32_t*>(in), codes, scales, static_cast<uint32_t>(rows / 32),
-      static_cast<uint32_t>(cols), static_cast<uint32_t>(group_rows));
   count_launch();
   return cudaGetLastError();
 }
