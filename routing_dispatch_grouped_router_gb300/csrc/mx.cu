@@ -289,84 +289,122 @@ __global__ void __launch_bounds__(256, ROWS_OUT ? 3 : 4) mx_cols_kernel(const ui
 // either as codes written transposed, [ng*C, K] (row g*C + c holds column c
 // of matrix g) with tiled scales (K/128 K groups), or as dequantised bf16
 // values in the input's layout.  Persistent CTAs walk the 128 x 128 tiles
-// (quant_tile.cuh); for each direction thread t takes line t % 128 and its
-// two blocks 2 (t / 128), +1: 64 contiguous code bytes and two adjacent scale
-// bytes.  The column values go back into the staged tile and leave in
-// coalesced 16-byte rows.
-__device__ __forceinline__ void mx_store32(uint8_t* p, const uint32_t (&a)[8]) {
-  uint4* q = reinterpret_cast<uint4*>(p);
-  q[0] = make_uint4(a[0], a[1], a[2], a[3]);
-  q[1] = make_uint4(a[4], a[5], a[6], a[7]);
+// (quant_tile.cuh).  Warps 0-3 take the rows, one row per thread (128
+// contiguous code bytes); warps 4-7 the columns, a pair of adjacent columns
+// and half of the tile's K per thread, read as 4-byte pairs (one 128-byte run
+// per warp and row).  Column codes leave as 64-byte runs per column, column
+// values as 4-byte pairs (again one 128-byte run per warp and row).
+
+// MX encoding (mx_encode32's rule) of the 32 values held in the low (HI =
+// false) or high halves of 32 packed bf16 pairs.
+template <bool HI>
+__device__ __forceinline__ uint32_t mx_encode_half32(const uint32_t (&x)[32], uint32_t (&w)[8]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(HI ? bf16hi(x[j]) : bf16lo(x[j])));
+  const int sh = mx_shared_of(amax);
+  const float down = exp2i(-sh);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    // cvt packs its first operand into the upper byte
+    const uint32_t p01 = cvt_e4m3x2((HI ? bf16hi(x[4 * i + 1]) : bf16lo(x[4 * i + 1])) * down,
+                                    (HI ? bf16hi(x[4 * i]) : bf16lo(x[4 * i])) * down);
+    const uint32_t p23 = cvt_e4m3x2((HI ? bf16hi(x[4 * i + 3]) : bf16lo(x[4 * i + 3])) * down,
+                                    (HI ? bf16hi(x[4 * i + 2]) : bf16lo(x[4 * i + 2])) * down);
+    w[i] = p01 | (p23 << 16);
+  }
+  return static_cast<uint32_t>(sh + 127);
 }
 
-__global__ void __launch_bounds__(256)
+// MX fake quantisation (mx_fake32's rule, rounded to bf16 as mx_quant8 does)
+// of the 32 values in one half of 32 packed bf16 pairs, in place.
+template <bool HI>
+__device__ __forceinline__ void mx_fake_half32(uint32_t (&x)[32]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(HI ? bf16hi(x[j]) : bf16lo(x[j])));
+  const int sh = mx_shared_of(amax);
+  const float down = exp2i(-sh), up = exp2i(sh);
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    const uint16_t qv = cvt_e4m3x2((HI ? bf16hi(x[j + 1]) : bf16lo(x[j + 1])) * down,
+                                   (HI ? bf16hi(x[j]) : bf16lo(x[j])) * down);
+    float fh, fl;
+    e4m3x2_to_f32(qv, &fh, &fl);
+    const uint32_t b0 = __bfloat16_as_ushort(__float2bfloat16_rn(fl * up));
+    const uint32_t b1 = __bfloat16_as_ushort(__float2bfloat16_rn(fh * up));
+    x[j] = HI ? ((x[j] & 0xFFFFu) | (b0 << 16)) : ((x[j] & 0xFFFF0000u) | b0);
+    x[j + 1] = HI ? ((x[j + 1] & 0xFFFFu) | (b1 << 16)) : ((x[j + 1] & 0xFFFF0000u) | b1);
+  }
+}
+
+__global__ void __launch_bounds__(256, 3)
     mx_quant_2d_kernel(const uint16_t* __restrict__ in, int K, int C, int ng,
                        uint8_t* __restrict__ rcodes, uint8_t* __restrict__ rscales,
                        uint8_t* __restrict__ ccodes, uint8_t* __restrict__ cscales,
                        uint16_t* __restrict__ cvals) {
   extern __shared__ __align__(16) uint16_t qt_smem[];
-  const int line = threadIdx.x & 127, pair = threadIdx.x >> 7;
+  const int t = threadIdx.x;
   qt_walk(in, K, C, ng, qt_smem, [&](uint16_t* tile, const QtTile& q) {
     const long long row0 = static_cast<long long>(q.grp) * K + q.kt * 128;
-    {
-      // row `line`, values 64 pair .. 64 pair + 63: two blocks along C
-      const long long row = row0 + line;
+    if (t < 128) {
+      // row t: four blocks along C
+      const long long row = row0 + t;
+      uint4* cp = reinterpret_cast<uint4*>(rcodes + row * C + q.ct * 128);
       uint32_t sc = 0u;
 #pragma unroll
-      for (int b = 0; b < 2; ++b) {
+      for (int b = 0; b < 4; ++b) {
         float v[32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float u[8];
-          unpack8(*reinterpret_cast<const uint4*>(tile + line * kQtPitch + 64 * pair + 32 * b +
-                                                  8 * c),
-                  u);
+          unpack8(*reinterpret_cast<const uint4*>(tile + t * kQtPitch + 32 * b + 8 * c), u);
 #pragma unroll
           for (int j = 0; j < 8; ++j) v[8 * c + j] = u[j];
         }
         uint32_t cw[8];
         sc |= mx_encode32(v, cw) << (8 * b);
-        mx_store32(rcodes + row * C + q.ct * 128 + 64 * pair + 32 * b, cw);
+        cp[2 * b] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        cp[2 * b + 1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
       }
-      *reinterpret_cast<uint16_t*>(rscales + mx_tiled_off(row, q.ct * 4 + 2 * pair, C / 128)) =
-          static_cast<uint16_t>(sc);
-    }
-    if (cvals) __syncthreads();  // the tile is rewritten below
-    {
-      // column `line`, values 64 pair .. 64 pair + 63 along K: two blocks
-      const long long orow = static_cast<long long>(q.grp) * C + q.ct * 128 + line;
-      uint32_t sc = 0u;
+      *reinterpret_cast<uint32_t*>(rscales + mx_tiled_off(row, q.ct * 4, C / 128)) = sc;
+    } else {
+      // columns 2p, 2p+1, K rows 64 h .. 64 h + 63: two blocks each
+      const int p = t & 63, h = (t - 128) >> 6;
+      const long long orow = static_cast<long long>(q.grp) * C + q.ct * 128 + 2 * p;
+      uint32_t s0 = 0u, s1 = 0u;
 #pragma unroll
       for (int b = 0; b < 2; ++b) {
-        uint16_t* col = tile + (64 * pair + 32 * b) * kQtPitch + line;
-        float v[32];
+        const int k0 = 64 * h + 32 * b;
+        uint32_t x[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          v[j] = __uint_as_float(static_cast<uint32_t>(col[j * kQtPitch]) << 16);
+          x[j] = *reinterpret_cast<const uint32_t*>(tile + (k0 + j) * kQtPitch + 2 * p);
         if (ccodes) {
           uint32_t cw[8];
-          sc |= mx_encode32(v, cw) << (8 * b);
-          mx_store32(ccodes + orow * K + q.kt * 128 + 64 * pair + 32 * b, cw);
+          s0 |= mx_encode_half32<false>(x, cw) << (8 * b);
+          uint4* c0 = reinterpret_cast<uint4*>(ccodes + orow * K + q.kt * 128 + k0);
+          c0[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+          c0[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+          s1 |= mx_encode_half32<true>(x, cw) << (8 * b);
+          uint4* c1 = reinterpret_cast<uint4*>(ccodes + (orow + 1) * K + q.kt * 128 + k0);
+          c1[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+          c1[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
         } else {
-          mx_fake32(v);
+          mx_fake_half32<false>(x);
+          mx_fake_half32<true>(x);
+          uint16_t* dst = cvals + (row0 + k0) * C + q.ct * 128 + 2 * p;
 #pragma unroll
-          for (int j = 0; j < 32; ++j)  // rounded to bf16 as mx_quant8 does
-            col[j * kQtPitch] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
+          for (int j = 0; j < 32; ++j)
+            *reinterpret_cast<uint32_t*>(dst + static_cast<long long>(j) * C) = x[j];
         }
       }
-      if (ccodes)
+      if (ccodes) {
+        *reinterpret_cast<uint16_t*>(cscales + mx_tiled_off(orow, q.kt * 4 + 2 * h, K / 128)) =
+            static_cast<uint16_t>(s0);
         *reinterpret_cast<uint16_t*>(cscales +
-                                     mx_tiled_off(orow, q.kt * 4 + 2 * pair, K / 128)) =
-            static_cast<uint16_t>(sc);
-    }
-    if (cvals) {
-      __syncthreads();
-      uint16_t* dst = cvals + row0 * C + q.ct * 128;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = threadIdx.x + 256 * j, r = i >> 4, c8 = i & 15;
-        *reinterpret_cast<uint4*>(dst + static_cast<long long>(r) * C + 8 * c8) =
-            *reinterpret_cast<const uint4*>(tile + r * kQtPitch + 8 * c8);
+                                     mx_tiled_off(orow + 1, q.kt * 4 + 2 * h, K / 128)) =
+            static_cast<uint16_t>(s1);
       }
     }
   });

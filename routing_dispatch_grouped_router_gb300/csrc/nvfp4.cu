@@ -183,10 +183,11 @@ __global__ void nv_quant_kernel(const uint4* __restrict__ in, long long nblk, in
 // (blocks of 16 along K; out row g*C + c holds column c of matrix g: codes
 // [ng*C, K/2], scales tiled with K/64 blocks per 128 rows, or row-major
 // [ng*C, K/16]).  Either output may be skipped (NULL codes).  Persistent CTAs
-// walk the 128 x 128 tiles (quant_tile.cuh); for each orientation thread t
-// takes line t % 128 and its blocks 4 (t / 128) .. +3, so it writes 32
-// contiguous code bytes and 4 contiguous scale bytes.
-__global__ void __launch_bounds__(256)
+// walk the 128 x 128 tiles (quant_tile.cuh).  Warps 0-3 take the rows, one
+// row per thread (64 contiguous code bytes); warps 4-7 the columns, a pair of
+// adjacent columns and half of the tile's K per thread, read as 4-byte pairs
+// (one 128-byte run per warp and row), so each column gets a 32-byte code run.
+__global__ void __launch_bounds__(256, 3)
     nv_quant_2d_kernel(const uint16_t* __restrict__ in, int K, int C, int ng,
                        const float* __restrict__ g_ptr, uint8_t* __restrict__ rcodes,
                        uint8_t* __restrict__ rscales, uint8_t* __restrict__ ccodes,
@@ -194,58 +195,73 @@ __global__ void __launch_bounds__(256)
   extern __shared__ __align__(16) uint16_t qt_smem[];
   const float g = *g_ptr;
   const float r6 = __frcp_rn(6.0f * g);
-  const int line = threadIdx.x & 127, quad = threadIdx.x >> 7;
+  const int t = threadIdx.x;
   qt_walk(in, K, C, ng, qt_smem, [&](uint16_t* tile, const QtTile& q) {
-    if (rcodes) {
-      // row `line` of the tile, values 64 quad .. 64 quad + 63 (blocks 4 quad ..)
-      const long long row = static_cast<long long>(q.grp) * K + q.kt * 128 + line;
-      uint4* cp = reinterpret_cast<uint4*>(rcodes + row * (C / 2) + q.ct * 64 + 32 * quad);
-      uint32_t sw = 0u, cw[8];
+    if (t < 128) {
+      if (!rcodes) return;
+      // row t of the tile: eight blocks along C
+      const long long row = static_cast<long long>(q.grp) * K + q.kt * 128 + t;
+      uint4* cp = reinterpret_cast<uint4*>(rcodes + row * (C / 2) + q.ct * 64);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t sw = 0u, cw[8];
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk) {
+          const uint16_t* src = tile + t * kQtPitch + 64 * half + 16 * blk;
+          const uint4 a = *reinterpret_cast<const uint4*>(src);
+          const uint4 b = *reinterpret_cast<const uint4*>(src + 8);
+          const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            v[2 * j] = bf16lo(u[j]);
+            v[2 * j + 1] = bf16hi(u[j]);
+          }
+          uint32_t c[2];
+          sw |= static_cast<uint32_t>(nv_block(v, g, r6, c)) << (8 * blk);
+          cw[2 * blk] = c[0];
+          cw[2 * blk + 1] = c[1];
+        }
+        cp[2 * half] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        cp[2 * half + 1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+        *reinterpret_cast<uint32_t*>(
+            rscales + nv_tiled_off(row, q.ct * 8 + 4 * half, C / 64)) = sw;
+      }
+    } else {
+      if (!ccodes) return;
+      // columns 2p, 2p+1 of the tile, K rows 64 h .. 64 h + 63: four blocks each
+      const int p = t & 63, h = (t - 128) >> 6;
+      uint32_t sw0 = 0u, sw1 = 0u, cw0[8], cw1[8];
 #pragma unroll
       for (int blk = 0; blk < 4; ++blk) {
-        const uint16_t* src = tile + line * kQtPitch + 64 * quad + 16 * blk;
-        const uint4 a = *reinterpret_cast<const uint4*>(src);
-        const uint4 b = *reinterpret_cast<const uint4*>(src + 8);
-        const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        float v[16];
+        const uint16_t* src = tile + (64 * h + 16 * blk) * kQtPitch + 2 * p;
+        float v0[16], v1[16];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          v[2 * j] = bf16lo(u[j]);
-          v[2 * j + 1] = bf16hi(u[j]);
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(src + j * kQtPitch);
+          v0[j] = bf16lo(w);
+          v1[j] = bf16hi(w);
         }
         uint32_t c[2];
-        sw |= static_cast<uint32_t>(nv_block(v, g, r6, c)) << (8 * blk);
-        cw[2 * blk] = c[0];
-        cw[2 * blk + 1] = c[1];
+        sw0 |= static_cast<uint32_t>(nv_block(v0, g, r6, c)) << (8 * blk);
+        cw0[2 * blk] = c[0];
+        cw0[2 * blk + 1] = c[1];
+        sw1 |= static_cast<uint32_t>(nv_block(v1, g, r6, c)) << (8 * blk);
+        cw1[2 * blk] = c[0];
+        cw1[2 * blk + 1] = c[1];
       }
-      // one 32-byte run: both halves of a sector from the same thread
-      cp[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-      cp[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-      *reinterpret_cast<uint32_t*>(rscales + nv_tiled_off(row, q.ct * 8 + 4 * quad, C / 64)) =
-          sw;
-    }
-    if (ccodes) {
-      // column `line` of the tile, values 64 quad .. 64 quad + 63 along K
-      const long long row = static_cast<long long>(q.grp) * C + q.ct * 128 + line;
-      const long long k16 = q.kt * 8 + 4 * quad;
-      uint4* cp = reinterpret_cast<uint4*>(ccodes + row * (K / 2) + k16 * 8);
-      uint32_t sw = 0u, cw[8];
-#pragma unroll
-      for (int blk = 0; blk < 4; ++blk) {
-        const uint16_t* col = tile + (64 * quad + 16 * blk) * kQtPitch + line;
-        float v[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          v[j] = __uint_as_float(static_cast<uint32_t>(col[j * kQtPitch]) << 16);
-        uint32_t c[2];
-        sw |= static_cast<uint32_t>(nv_block(v, g, r6, c)) << (8 * blk);
-        cw[2 * blk] = c[0];
-        cw[2 * blk + 1] = c[1];
-      }
-      cp[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-      cp[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+      const long long row = static_cast<long long>(q.grp) * C + q.ct * 128 + 2 * p;
+      const long long k16 = q.kt * 8 + 4 * h;
+      uint4* c0 = reinterpret_cast<uint4*>(ccodes + row * (K / 2) + k16 * 8);
+      uint4* c1 = reinterpret_cast<uint4*>(ccodes + (row + 1) * (K / 2) + k16 * 8);
+      c0[0] = make_uint4(cw0[0], cw0[1], cw0[2], cw0[3]);
+      c0[1] = make_uint4(cw0[4], cw0[5], cw0[6], cw0[7]);
+      c1[0] = make_uint4(cw1[0], cw1[1], cw1[2], cw1[3]);
+      c1[1] = make_uint4(cw1[4], cw1[5], cw1[6], cw1[7]);
       *reinterpret_cast<uint32_t*>(cscales + (ctiled ? nv_tiled_off(row, k16, K / 64)
-                                                     : row * (K / 16) + k16)) = sw;
+                                                     : row * (K / 16) + k16)) = sw0;
+      *reinterpret_cast<uint32_t*>(cscales + (ctiled ? nv_tiled_off(row + 1, k16, K / 64)
+                                                     : (row + 1) * (K / 16) + k16)) = sw1;
     }
   });
 }
