@@ -103,6 +103,23 @@ def test_layer_zero_tokens():
     assert (dwgu == 0).all() and (dwd == 0).all() and (dwr == 0).all()
 
 
+@pytest.mark.parametrize("dtype", [api.MXFP8, api.NVFP4])
+def test_layer_zero_tokens_block_scaled(dtype):
+    """No tokens in the block-scaled modes: the weights are still quantised
+    (and their backward forms written), every GEMM has no rows, and the
+    weight gradients come out zero."""
+    layer = api.MoELayer(0, 256, 4, 256, 2, dtype=dtype)
+    wr = torch.zeros(4, 256, dtype=torch.bfloat16, device="cuda")
+    wgu = torch.ones(4, 512, 256, dtype=torch.bfloat16, device="cuda")
+    wd = torch.ones(4, 256, 256, dtype=torch.bfloat16, device="cuda")
+    x = torch.empty(0, 256, dtype=torch.bfloat16, device="cuda")
+    y = layer.forward(x, wr, None, wgu, wd)
+    dx, dwr, dwgu, dwd = layer.backward(x, x, wr, None, wgu, wd)
+    assert layer.status() == 0
+    assert y.numel() == 0 and dx.numel() == 0
+    assert (dwgu == 0).all() and (dwd == 0).all() and (dwr == 0).all()
+
+
 def test_layer_parity_fine_full_size():
     """The fine-grained workload at its full size, every element."""
     shape = gen.workload_shape("fine")

@@ -202,3 +202,30 @@ def test_layer_nvfp4_rejects_what_it_does_not_support():
         desc = api.make_desc(**args)
         assert lib.mok_moe_workspace_size(ctypes.byref(desc), ctypes.byref(f), ctypes.byref(s),
                                           ctypes.byref(b)) == 2
+
+
+@pytest.mark.parametrize("dtype", [api.MXFP8, api.NVFP4])
+def test_block_scaled_accumulate_and_bf16_outputs(dtype):
+    """The output flags in the block-scaled modes: accumulating weight
+    gradients over two calls gives exactly twice one call (the forward writes
+    the same quantised weights again), and bf16 activations are the fp32 ones
+    rounded once."""
+    shape = NV_SHAPES["wide"]
+    inp = gen.make_inputs(shape, seed=9)
+    one = _gpu.run_gpu(shape, inp, dtype=dtype)
+    x, wr, wgu, wd, dy = (_gpu.dev_bf16(inp[n]) for n in ("x", "w_router", "w_gate_up", "w_down",
+                                                          "dy"))
+    layer = api.MoELayer(shape.T, shape.d, shape.E, shape.I, shape.k, dtype=dtype,
+                         flags=api.FLAG_ACCUMULATE_WGRAD)
+    dws = [torch.zeros(t.shape, dtype=torch.float32, device="cuda") for t in (wr, wgu, wd)]
+    for _ in range(2):
+        layer.forward(x, wr, None, wgu, wd)
+        layer.backward(dy, x, wr, None, wgu, wd, dw_router=dws[0], dw_gate_up=dws[1],
+                       dw_down=dws[2])
+    assert layer.status() == 0
+    for got, ref in zip(dws, (one["dw_router"], one["dw_gate_up"], one["dw_down"])):
+        assert torch.equal(got, 2 * ref)
+    bf = _gpu.run_gpu(shape, inp, dtype=dtype, flags=api.FLAG_BF16_ACT_OUT)
+    assert bf["status"] == 0
+    for n in ("y", "dx"):
+        assert torch.equal(bf[n], one[n].to(torch.bfloat16))
