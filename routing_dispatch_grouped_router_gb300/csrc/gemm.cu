@@ -734,6 +734,99 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
   }
 }
 
+// ------------------------------- block-scaled pairs: accumulator in registers --
+// The block-scaled pair GEMMs keep one accumulator (their scale columns fill
+// the rest of TMEM), so the MMAs of the next tile wait for this tile's
+// epilogue.  These epilogues first copy the warp's 128 accumulator columns
+// into registers; the caller then frees the accumulator, and the stores run
+// while the next tile's MMAs do.
+
+// The warp's 128 columns: EPI_F32, columns half*128 .. +127; SwiGLU forward,
+// gate columns half*64 .. +63 then up columns 128 + half*64 .. +63.
+template <int EPI>
+__device__ __forceinline__ void acc_to_regs(uint32_t taddr, int half, float (&acc)[128]) {
+  uint32_t r[8][16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t col = EPI == EPI_SWIGLU_FWD
+                             ? (j < 4 ? half * 64 + 16 * j : 128 + half * 64 + 16 * (j - 4))
+                             : half * 128 + 16 * j;
+    tmem_ld16(taddr + col, r[j]);
+  }
+  tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[16 * j + i] = __uint_as_float(r[j][i]);
+}
+
+template <int EPI, int SPLIT, bool DBUF>
+__device__ __forceinline__ void epilogue_regs(const GemmArgs& a, const Tile& tl,
+                                              float (&acc)[128], int q, int lane, int half,
+                                              uint8_t* stage_buf, uint32_t& nst,
+                                              const CUtensorMap* tmC) {
+  // NVFP4: the product of the operands' tensor scales (the block scales were
+  // applied by the tensor cores)
+  const float alpha = SPLIT == SPLIT_NV ? __ldg(a.ga) * __ldg(a.gb) : 1.0f;
+  if (SPLIT == SPLIT_NV) {
+#pragma unroll
+    for (int j = 0; j < 128; ++j) acc[j] *= alpha;
+  }
+  const int y = tl.row0 + q * 32;
+  if constexpr (EPI == EPI_F32) {
+    const int col0 = tl.n_tile * 256 + half * 128;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float v[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = acc[32 * c + j];
+      stage_and_store_f32<DBUF>(stage_buf, nst, tmC, v, lane, col0 + 32 * c, y,
+                                a.accumulate != 0, a.evict_first != 0);
+    }
+  } else {
+    // gate acc[0..63], up acc[64..127] for FFN columns n0 .. n0+63
+    const long long r = tl.row0 + q * 32 + lane;
+    const int I = a.I;
+    const int n0 = tl.n_tile * 128 + half * 64;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      float g[32], u[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        g[j] = acc[32 * c + j];
+        u[j] = acc[64 + 32 * c + j];
+      }
+      // g and u leave first; h then takes g's registers
+      if (a.store_c) {
+        stage_and_store_f32<DBUF>(stage_buf, nst, tmC, g, lane, n0 + 32 * c, y, false,
+                                  a.evict_first != 0);
+        stage_and_store_f32<DBUF>(stage_buf, nst, tmC, u, lane, I + n0 + 32 * c, y, false,
+                                  a.evict_first != 0);
+      }
+      if (SPLIT == SPLIT_MX ? a.h_codes != nullptr : a.out2 != nullptr) {
+        float (&hv)[32] = g;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          float sg;
+          hv[j] = silu_f(g[j], &sg) * u[j];
+        }
+        if (SPLIT == SPLIT_MX) {
+          uint32_t w[8];
+          const uint32_t sbyte = mx_encode32(hv, w);
+          uint4* cp = reinterpret_cast<uint4*>(a.h_codes + r * I + n0 + 32 * c);
+          cp[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          cp[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          a.h_scales[mx_tiled_off(r, (n0 + 32 * c) / 32, I / 128)] =
+              static_cast<uint8_t>(sbyte);
+        } else {
+          store_bf16x32(static_cast<__nv_bfloat16*>(a.out2) + r * (long long)I + n0 + 32 * c,
+                        hv);
+        }
+      }
+    }
+  }
+}
+
 // ------------------------------------------ SwiGLU backward, TMA operands --
 // g, u of one chunk: 32 rows (this warp's lane quarter) x 16 fp32 columns of
 // each, TMA-loaded into a 4 KB staging buffer (g at +0, u at +2048, 64-byte
@@ -1268,6 +1361,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // SwiGLU backward: g, u come by TMA (tmC maps them); `gu_chunks` counts
     // the chunks this warp has requested
     constexpr bool kGuTma = EPI == EPI_SWIGLU_BWD;
+    // block-scaled pairs (one accumulator): free it before the stores
+    constexpr bool kEarlyRelease = PAIR && block_scaled(SPLIT) && C::NACC == 1 &&
+                                   SCHED == SCHED_MGROUP && BN == 256 &&
+                                   (EPI == EPI_F32 || EPI == EPI_SWIGLU_FWD);
     uint64_t* wbar = gu_bar + 2 * (warp - 2);
     uint32_t gu_chunks = 0;
     uint32_t nst = 0;  // TMA-store blocks issued by this warp
@@ -1288,6 +1385,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      if constexpr (kEarlyRelease) {
+        // the accumulator to registers, freed at once; the stores follow
+        float accr[128];
+        if (valid) acc_to_regs<EPI>(taddr, half, accr);
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * acc);
+        if (valid)
+          epilogue_regs<EPI, SPLIT, kDbuf>(args, tl, accr, q, lane, half, stage_buf, nst, &tmC);
+        continue;
+      }
       if constexpr (kGuTma) {
         if (valid)
           gu_chunks = swiglu_bwd_tma<BN>(args, tl, taddr, q, lane, half, stage_buf, wbar,
