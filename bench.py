@@ -176,24 +176,49 @@ def ncu_traffic(workload: str, kernel: str):
 
 
 def mx_quant_bytes(shape: gen.Shape, nmb: int, rows_max: int, kernels: dict, steps: int) -> dict:
-    """Average bytes per launch of the MXFP8 quantisers in one step: once per
-    call the weights (rows: E4M3 codes + scales for the forward; columns along
-    the dgrads' K for the backward: W_down as bf16 values, W_gate_up as
-    transposed E4M3 codes + scales), per micro-batch the dispatched x rows
-    (codes), dy (one column-kernel launch writes bf16 values in both block
-    directions) and the x rows along the columns for the weight gradients.
-    The activation launches read the token rows through the row -> token map:
-    each token row once, each dispatched row written."""
+    """Average bytes per launch of the MXFP8 quantisers in one step.  Once per
+    call, one launch per weight reads it and writes both orientations: W_gate_up
+    as E4M3 codes + scales along d (the forward) and along 2I (the gate/up
+    dgrad), W_down as codes + scales along I and as bf16 MX values along d (the
+    down dgrad).  Per micro-batch: the dispatched x rows as codes (row
+    launch), dy in both block directions as bf16 values and x along the rows
+    as bf16 values (two column launches).  The activation launches read the
+    token rows through the row -> token map: each token row once, each
+    dispatched row written."""
     E, d, I = shape.E, shape.d, shape.I
     w_gu, w_d = E * 2 * I * d, E * d * I       # weight elements
-    w = w_gu + w_d
     act = rows_max * d                         # one micro-batch's dispatched rows
     tok = shape.T // nmb * d                   # one micro-batch's token rows
-    q8 = 2 + 1 + 1 / 32                        # bf16 in, E4M3 code + 1/32 scale out
-    rows_bytes = w * q8 + nmb * (tok * 2 + act * (1 + 1 / 32))
-    cols_bytes = w_d * 4 + w_gu * q8 + nmb * (tok * 2 + act * 4) + nmb * (tok * 2 + act * 2)
+    c8 = 1 + 1 / 32                            # E4M3 code + 1/32 scale byte
+    two_d = w_gu * (2 + 2 * c8) + w_d * (2 + c8 + 2)
+    rows_bytes = nmb * (tok * 2 + act * c8)
+    cols_bytes = nmb * (tok * 2 + act * 4) + nmb * (tok * 2 + act * 2)
     out = {}
-    for name, total in (("mx_quant_rows", rows_bytes), ("mx_quant_cols", cols_bytes)):
+    for name, total in (("mx_quant_2d", two_d), ("mx_quant_rows", rows_bytes),
+                        ("mx_quant_cols", cols_bytes)):
+        if name in kernels:
+            n, _ = kernels[name]
+            out[name] = total / (n / steps)
+    return out
+
+
+def nv_quant_bytes(shape: gen.Shape, rows_max: int, kernels: dict, steps: int) -> dict:
+    """Average bytes per launch of the NVFP4 quantisers in one step (one call,
+    no micro-batches).  W_gate_up: one launch reads it and writes E2M1 codes
+    + E4M3 scales along d and along 2I.  Row launches: W_down, x (token rows
+    through the row map, each read once), h and dG/dU (all padded rows).
+    Tensor scales: one read of W_gate_up, W_down and x, and of h and dG/dU over
+    the routed rows."""
+    E, d, I, R = shape.E, shape.d, shape.I, shape.R
+    w_gu, w_d = E * 2 * I * d, E * d * I
+    c4 = 0.5 + 1 / 16                          # E2M1 code + 1/16 scale byte
+    two_d = w_gu * (2 + 2 * c4)
+    rows = (w_d * (2 + c4) + (shape.T * d * 2 + rows_max * d * c4)
+            + rows_max * I * (2 + c4) + rows_max * 2 * I * (2 + c4))
+    amax = 2 * (w_gu + w_d + shape.T * d + R * I + R * 2 * I)
+    out = {}
+    for name, total in (("nvfp4_quantize_2d", two_d), ("nvfp4_quantize", rows),
+                        ("nvfp4_amax", amax)):
         if name in kernels:
             n, _ = kernels[name]
             out[name] = total / (n / steps)
@@ -682,6 +707,8 @@ def main():
     if PRECISION == "mxfp8":
         movers.update(mx_quant_bytes(shape, int(layer.layout.mb_count), int(layer.layout.rows_max),
                                      kernels, prof_steps))
+    if PRECISION == "nvfp4":
+        movers.update(nv_quant_bytes(shape, int(layer.layout.rows_max), kernels, prof_steps))
     total_k = sum(v[1] for v in kernels.values())
     ksum = {}
     for name, (n, ms) in kernels.items():
