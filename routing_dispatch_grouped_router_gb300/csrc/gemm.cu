@@ -141,6 +141,13 @@ constexpr int kStagingBytes = 4096;  // per epilogue warp: 32 rows x 128 bytes
 // six bf16 output blocks of a chunk (6 x 1 KB).
 constexpr int kGuStageBytes = 8192;
 constexpr int kSwigluBwdStaging = kGuStageBytes + 6 * 1024;
+// The SwiGLU backward with its outputs stored straight from registers (DB on
+// EPI_SWIGLU_BWD): no output staging, so two more operand stages.  Faster
+// where the K loop (d) is long and the weights stream: large workload,
+// d = 7168, 3117 -> 2977 us; slower where the epilogue dominates: fine,
+// d = 2048, 257 -> 327 us (16-byte stores, half a sector per lane and store).
+constexpr int kSwigluBwdStagingDirect = kGuStageBytes;
+constexpr int kSwigluBwdDirectMinD = 6144;
 // Double-buffered store staging (DB: a block is written while the previous
 // block's store still reads shared memory), chosen per launch for the fp32
 // weight gradients (K-grouped, plain and transposed stores) whose tiles run
@@ -153,7 +160,8 @@ constexpr int kSwigluBwdStaging = kGuStageBytes + 6 * 1024;
 // the fine workload).
 template <int EPI, int SPLIT, int SCHED, bool DB>
 constexpr int staging_bytes() {
-  return EPI == EPI_SWIGLU_BWD ? kSwigluBwdStaging : (DB ? 2 * kStagingBytes : kStagingBytes);
+  return EPI == EPI_SWIGLU_BWD ? (DB ? kSwigluBwdStagingDirect : kSwigluBwdStaging)
+                               : (DB ? 2 * kStagingBytes : kStagingBytes);
 }
 
 template <int BN, int SPLIT = SPLIT_NONE, bool PAIR = false, int STG = kStagingBytes>
@@ -200,7 +208,8 @@ static_assert(Cfg<256, SPLIT_NONE, true>::SMEM_BYTES <= 232448 &&
 static_assert(Cfg<256, SPLIT_A, true>::SMEM_BYTES <= 232448 &&
                   Cfg<256, SPLIT_A, true>::STAGES >= 4, "smem");
 static_assert(Cfg<256, SPLIT_NONE, true, kSwigluBwdStaging>::SMEM_BYTES <= 232448 &&
-                  Cfg<256, SPLIT_NONE, true, kSwigluBwdStaging>::STAGES == 3, "smem");
+                  Cfg<256, SPLIT_NONE, true, kSwigluBwdStaging>::STAGES == 3 &&
+                  Cfg<256, SPLIT_NONE, true, kSwigluBwdStagingDirect>::STAGES == 5, "smem");
 static_assert(Cfg<256, SPLIT_NONE, false, kSwigluBwdStaging>::STAGES >= 2 &&
                   Cfg<128, SPLIT_NONE, false, kSwigluBwdStaging>::STAGES >= 3, "smem");
 static_assert(Cfg<128, SPLIT_MX>::STAGES == 5 && Cfg<128, SPLIT_MX>::STAGE_BYTES % 1024 == 0 &&
@@ -856,7 +865,7 @@ __device__ __forceinline__ void gu_issue(const GemmArgs& a, const Tile& tl, int 
 // quantised to MXFP8 (the gate/up dgrad's A operand): a block is 32
 // consecutive columns of a row, so each odd chunk encodes itself together
 // with the even chunk before it (n0 is a multiple of 32).
-template <int BN>
+template <int BN, bool DIRECT>
 __device__ __forceinline__ uint32_t swiglu_bwd_tma(const GemmArgs& a, const Tile& tl,
                                                    uint32_t taddr, int q, int lane, int half,
                                                    uint8_t* stage_buf, uint64_t* wbar,
@@ -944,6 +953,18 @@ __device__ __forceinline__ uint32_t swiglu_bwd_tma(const GemmArgs& a, const Tile
         a.dgu_scales[mx_tiled_off(r, (I + col) / 32, 2 * I / 128)] = static_cast<uint8_t>(sbyte);
       }
     }
+    if constexpr (DIRECT) {
+      // the row's 16 columns of the six outputs from registers: 32
+      // contiguous bytes per output and lane
+      const long long o2 = r * (2LL * I) + n0 + c, o1 = r * static_cast<long long>(I) + n0 + c;
+      __nv_bfloat16* gh = static_cast<__nv_bfloat16*>(a.out);
+      __nv_bfloat16* gl = static_cast<__nv_bfloat16*>(a.out3);
+      store_hi_lo16(gh + o2, gl + o2, t);
+      store_hi_lo16(gh + o2 + I, gl + o2 + I, dA);
+      store_hi_lo16(static_cast<__nv_bfloat16*>(a.out2) + o1,
+                    static_cast<__nv_bfloat16*>(a.out4) + o1, u);
+      continue;
+    }
     if (lane == 0) bulk_wait_read<0>();  // the previous chunk's stores have read staging
     __syncwarp();
     uint8_t* row = ostage + lane * 32;
@@ -979,8 +1000,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ GemmArgs args, const __grid_constant__ OutMaps om) {
   using C = Cfg<BN, SPLIT, PAIR, staging_bytes<EPI, SPLIT, SCHED, DB>()>;
   constexpr bool kDbuf = DB;
-  static_assert(!DB || ((EPI == EPI_F32 || EPI == EPI_F32_T) && SCHED == SCHED_KGROUP),
-                "double-buffered staging: the fp32 weight-gradient epilogues");
+  static_assert(!DB || ((EPI == EPI_F32 || EPI == EPI_F32_T) && SCHED == SCHED_KGROUP) ||
+                    (EPI == EPI_SWIGLU_BWD && PAIR),
+                "DB: double-buffered staging of the fp32 weight gradients, or the SwiGLU "
+                "backward's stores from registers");
   static_assert(!PAIR || (SCHED != SCHED_DENSE && SPLIT != SPLIT_B && BN == 256), "pair");
   static_assert(SPLIT != SPLIT_MX ||
                     (!A_MN && !B_MN && BN == (PAIR ? 256 : 128) && SCHED == SCHED_MGROUP),
@@ -1398,7 +1421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if constexpr (kGuTma) {
         if (valid)
-          gu_chunks = swiglu_bwd_tma<BN>(args, tl, taddr, q, lane, half, stage_buf, wbar,
+          gu_chunks = swiglu_bwd_tma<BN, kDbuf>(args, tl, taddr, q, lane, half, stage_buf, wbar,
                                          gu_chunks, &tmC, &om, vabort);
       } else if (valid) {
         epilogue_tile<BN, SCHED, EPI, kDbuf, SPLIT>(args, tl, taddr, q, lane, half, stage_buf,
@@ -1904,6 +1927,9 @@ cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* 
   a.dp_part = dp_part;
   a.np = D.np;
   const int mt = max_mtiles(D) * a.n_tiles;
+  if (bn == 256 && D.pair && D.d >= kSwigluBwdDirectMinD)  // long K: operand stages first
+    return launch<256, false, true, SCHED_MGROUP, EPI_SWIGLU_BWD, SPLIT_NONE, true, true>(
+        "bwd_down_dgrad_swiglu", ta, tb, tg, a, max_mpairs(D) * a.n_tiles, st, nullptr, &om);
   if (bn == 256 && D.pair)
     return launch<256, false, true, SCHED_MGROUP, EPI_SWIGLU_BWD, SPLIT_NONE, true>(
         "bwd_down_dgrad_swiglu", ta, tb, tg, a, max_mpairs(D) * a.n_tiles, st, nullptr, &om);

@@ -60,6 +60,9 @@ SMALL = {
     # E > 128: the router-weight gradient GEMM has two 128-row M tiles (E padded
     # to 256), several token chunks and a ragged last chunk
     "e200": gen.Shape(T=300, d=256, E=200, I=128, k=2),
+    # d >= 6144 with 256-wide down-dgrad tiles: the SwiGLU backward stores
+    # from registers (long K loop, five operand stages)
+    "d7168": gen.Shape(T=256, d=7168, E=4, I=512, k=2),
 }
 
 
