@@ -156,13 +156,13 @@ NCU_TRAFFIC_FINE = {
 }
 # The large workload's GEMMs from a capture of its slice (1/16 of its experts and
 # tokens, the same widths and rows per expert): per-expert work, so 16x the bytes.
-# (The down dgrad has changed since that capture and has no entry.)
 NCU_TRAFFIC_LARGE = {k: 16 * v for k, v in {
-    "fwd_gate_up_swiglu": 1.511236e9 + 0.102995e9,
-    "fwd_down": 0.733158e9 + 0.150349e9,
-    "bwd_down_wgrad": 0.104096e9 + 1.347123e9,
-    "bwd_gate_up_dgrad": 1.474296e9 + 0.163004e9,
-    "bwd_gate_up_wgrad": 0.141870e9 + 2.757503e9,
+    "fwd_gate_up_swiglu": 1.511167e9 + 0.103032e9,
+    "fwd_down": 0.732591e9 + 0.149962e9,
+    "bwd_down_dgrad_swiglu": 0.948928e9 + 0.124636e9,
+    "bwd_down_wgrad": 0.103904e9 + 1.347200e9,
+    "bwd_gate_up_dgrad": 1.474263e9 + 0.162597e9,
+    "bwd_gate_up_wgrad": 0.141883e9 + 2.756988e9,
 }.items()}
 NCU_TRAFFIC = {"fine": (NCU_TRAFFIC_FINE, "profiles/grouped_gemms_fine.txt"),
                "large": (NCU_TRAFFIC_LARGE,
