@@ -147,12 +147,12 @@ def gemm_bytes(shape: gen.Shape, micro_batches: int = 1, mx: bool = False,
 # (kernels as of the commit each file names); a kernel changed since its
 # capture has no entry.
 NCU_TRAFFIC_FINE = {
-    "fwd_gate_up_swiglu": 688.822784e6 + 329.280e6,
-    "fwd_down": 343.471360e6 + 254.084e6,
-    "bwd_down_dgrad_swiglu": 768.187648e6 + 401.218e6,
-    "bwd_down_wgrad": 300.070400e6 + 479.529e6,
-    "bwd_gate_up_dgrad": 690.012160e6 + 271.601e6,
-    "bwd_gate_up_wgrad": 449.964800e6 + 1014.369e6,
+    "fwd_gate_up_swiglu": 687.948544e6 + 329.665e6,
+    "fwd_down": 343.4496e6 + 254.065e6,
+    "bwd_down_dgrad_swiglu": 768.087808e6 + 401.775e6,
+    "bwd_down_wgrad": 284.920576e6 + 479.158e6,
+    "bwd_gate_up_dgrad": 688.581888e6 + 271.775e6,
+    "bwd_gate_up_wgrad": 427.131136e6 + 1013.622e6,
 }
 # The large workload's GEMMs from a capture of its slice (1/16 of its experts and
 # tokens, the same widths and rows per expert): per-expert work, so 16x the bytes.
