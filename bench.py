@@ -581,6 +581,32 @@ def e2e_pipelined(layer, inp, x, dy, wr, bias, wgu, wd, dwr, dwgu, dwd, stream, 
     torch.cuda.synchronize()
     return e0.elapsed_time(e1)
 
+def graph_steps(torch, step, steps: int, stream, world: int, dist) -> float:
+    """Milliseconds for `steps` replays of one step captured in a CUDA graph
+    (the same kernels, without per-launch host work or launch gaps)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()
+    stream.wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -797,6 +823,15 @@ def main():
            "h2d_bytes_per_step": 2 * xh_bytes, "d2h_bytes_per_step": 2 * x.numel() * 4,
            "steps": args.e2e_steps}
 
+    # ---- the same step replayed from a CUDA graph (after the timed region)
+    g_ms = graph_steps(torch, step, args.steps, stream, world, dist)
+    if world > 1:
+        g_ms = max_over_ranks(g_ms, dist, "cuda")
+    if layer.status() != 0:
+        raise RuntimeError("device status set during the graph replays")
+    graph_line = {"ms_per_step": g_ms / args.steps, "steps": args.steps,
+                  "value": job_throughput(world, shape.T, args.steps, g_ms), "unit": "tokens/s"}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(inp, shape)
@@ -821,6 +856,7 @@ def main():
             "grouped_gemm_frac_of_peak": gg_tflops / peaks["bf16_sustained"],
             "all_gemm_tflops": gemm_fl / (gemm_ms / 1e3) / 1e12 if gemm_ms else 0.0,
             "roofline": roof, "movers": movers_perf, "cpu_baseline": cpu, "e2e": e2e,
+            "graph": graph_line,
             "gpu_launches": launches_per_step * args.steps, "launches_per_step": launches_per_step,
             "clocks": clocks, "kernels": ksum,
             "kernel_timing": f"CUDA events around each kernel on {prof_steps} of the "

@@ -489,3 +489,40 @@ def test_mx_quantize_bit_exact(along_rows, shape):
     mag = np.where(e > 0, 2.0 ** (e - 7) * (1 + m / 8), 2.0 ** -6 * (m / 8))
     sh = np.repeat(shared, 32, axis=0) if along_rows else np.repeat(shared, 32, axis=1)
     np.testing.assert_array_equal(np.where(s == 1, -mag, mag) * 2.0 ** sh, ref)
+
+
+@pytest.mark.parametrize("dtype", [api.BF16, api.MXFP8, api.NVFP4])
+def test_layer_step_replays_in_a_cuda_graph(dtype):
+    """Forward + backward enqueue only stream-ordered work (no allocation, no
+    host read-back), so a whole step can be captured in a CUDA graph; replays
+    give the eager results bit for bit."""
+    shape = SMALL["wide"]
+    inp = gen.make_inputs(shape, seed=4)
+    eager = _gpu.run_gpu(shape, inp, dtype=dtype)
+    assert eager["status"] == 0
+    layer = api.MoELayer(shape.T, shape.d, shape.E, shape.I, shape.k, dtype=dtype)
+    x, wr, wgu, wd, dy = (_gpu.dev_bf16(inp[n]) for n in ("x", "w_router", "w_gate_up", "w_down",
+                                                          "dy"))
+    f32 = dict(dtype=torch.float32, device="cuda")
+    y, dx = torch.empty(x.shape, **f32), torch.empty(x.shape, **f32)
+    dws = [torch.empty(t.shape, **f32) for t in (wr, wgu, wd)]
+
+    def step():
+        layer.forward(x, wr, None, wgu, wd, y=y)
+        layer.backward(dy, x, wr, None, wgu, wd, dx=dx, dw_router=dws[0], dw_gate_up=dws[1],
+                       dw_down=dws[2])
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()  # first calls outside the capture (kernel attributes, descriptors)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for t in [y, dx] + dws:
+        t.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    for got, n in zip([y, dx] + dws, ("y", "dx", "dw_router", "dw_gate_up", "dw_down")):
+        assert torch.equal(got, eager[n]), n
