@@ -76,7 +76,7 @@ struct GemmArgs {
   int b_group_rows;  // MGROUP: rows of B per expert in its 2-D view
   int m_rows;        // KGROUP: rows of C per group (C viewed as [E*m_rows, N])
   int I;             // SwiGLU epilogues: FFN width
-  int m_valid, n_valid;  // DENSE: valid rows / columns of C
+  int m_valid, n_valid;  // valid rows / columns of C (DENSE; M- and K-grouped: 0 = all)
   const int* mtile_prefix;  // MGROUP: [E+1] prefix of 128-row tiles per expert, then
                             // [E+1] prefix of tile pairs (an odd count rounded up)
   const int* poff;          // MGROUP/KGROUP: [E+1] padded row offsets
@@ -578,10 +578,16 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
     // fp32 (or bf16) C through TMA stores; C viewed as 2-D [rows, N]
     const int y = (SCHED == SCHED_KGROUP ? tl.e * a.m_rows : 0) + tl.row0 + q * 32;
     const int col0 = tl.n_tile * BN + half * HALF_COLS;
+    // a ragged last tile (M or N a multiple of 32, not of the tile): this
+    // warp's 32 rows and each 32-column chunk lie wholly inside or outside C,
+    // and what lies outside belongs to the next expert's block or past C, so
+    // it is not stored
+    if (a.m_valid > 0 && tl.row0 + q * 32 >= a.m_valid) return;
     if constexpr (EPI == EPI_BF16_TMA) {
       // 64 columns per store: 128-byte rows
 #pragma unroll 1
       for (int c = 0; c < HALF_COLS; c += 64) {
+        if (a.n_valid > 0 && col0 + c >= a.n_valid) break;  // (a partial box is clipped)
         float v0[32], v1[32];
         if (!zero_k) {
           tmem_ld32(taddr + half * HALF_COLS + c, v0);
@@ -595,6 +601,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
     } else {
 #pragma unroll 1
       for (int c = 0; c < HALF_COLS; c += 32) {
+        if (a.n_valid > 0 && col0 + c >= a.n_valid) break;
         float v[32];
         if (!zero_k) {
           tmem_ld32(taddr + half * HALF_COLS + c, v);
@@ -1617,7 +1624,7 @@ cudaError_t gemm_fwd_gate_up(const Dims& D, const void* X_perm, const void* w_ga
   a.evict_first = 1;  // g, u are read again only by the backward
   a.E = (int)D.E;
   a.n_tiles = (int)(D.I / 128);
-  a.num_kb = (int)(D.d / 64);
+  a.num_kb = (int)((D.d + 63) / 64);  // a ragged last K block reads zeros
   a.b_group_rows = (int)(2 * D.I);
   a.I = (int)D.I;
   a.mtile_prefix = mtile_prefix;
@@ -1866,7 +1873,8 @@ cudaError_t gemm_fwd_down(const Dims& D, const void* H, const void* w_down,
   if (!make_out_map(&tc, O, D.d, D.rows_max)) return cudaErrorInvalidValue;
   GemmArgs a = blank_args(status);
   a.E = (int)D.E;
-  a.n_tiles = (int)(D.d / bn);
+  a.n_tiles = (int)((D.d + bn - 1) / bn);
+  a.n_valid = (int)D.d;
   a.num_kb = (int)(D.I / 64);
   a.b_group_rows = (int)D.d;
   a.mtile_prefix = mtile_prefix;
@@ -1909,7 +1917,7 @@ cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* 
   GemmArgs a = blank_args(status);
   a.E = (int)D.E;
   a.n_tiles = (int)(D.I / bn);
-  a.num_kb = (int)(D.d / 64);
+  a.num_kb = (int)((D.d + 63) / 64);  // dY reads zeros past d
   a.b_group_rows = (int)D.d;
   a.I = (int)D.I;
   a.mtile_prefix = mtile_prefix;
@@ -1951,7 +1959,8 @@ cudaError_t gemm_bwd_gate_up_dgrad(const Dims& D, const void* dGU, const void* w
   if (!make_out_map(&tc, dX_perm, D.d, D.rows_max)) return cudaErrorInvalidValue;
   GemmArgs a = blank_args(status);
   a.E = (int)D.E;
-  a.n_tiles = (int)(D.d / bn);
+  a.n_tiles = (int)((D.d + bn - 1) / bn);
+  a.n_valid = (int)D.d;
   a.num_kb = (int)(2 * D.I / 64);
   a.b_group_rows = (int)(2 * D.I);
   a.mtile_prefix = mtile_prefix;
@@ -2002,8 +2011,10 @@ static cudaError_t wgrad(const Dims& D, const char* name, const void* A_rows, in
   a.seg_rows = (int)D.rows_max;
   a.coff = sg.coff;
   a.E = (int)D.E;
-  a.m_tiles = (int)(M / 128);
-  a.n_tiles = (int)(N / bn);
+  a.m_tiles = (int)((M + 127) / 128);
+  a.n_tiles = (int)((N + bn - 1) / bn);
+  a.m_valid = (int)M;
+  a.n_valid = (int)N;
   a.m_rows = (int)M;
   a.poff = poff;
   a.out = out;
@@ -2143,7 +2154,8 @@ cudaError_t gemm_router_wgrad(const Dims& D, const void* x, const void* dl_hi, c
   GemmArgs a = blank_args(status);
   a.E = rw.ks;
   a.m_tiles = (int)(M / 128);
-  a.n_tiles = (int)(D.d / bn);
+  a.n_tiles = (int)((D.d + bn - 1) / bn);
+  a.n_valid = (int)D.d;
   a.m_rows = (int)M;
   a.poff = rw_off;
   a.out = part;
@@ -2170,7 +2182,7 @@ cudaError_t launch_router_logits(const Dims& D, const void* x, const void* w_rou
   a.E = 1;
   a.m_tiles = (int)((D.T + 127) / 128);
   a.n_tiles = (int)((D.E + bn - 1) / bn);
-  a.num_kb = (int)(D.d / 64);
+  a.num_kb = (int)((D.d + 63) / 64);
   a.m_valid = (int)D.T;
   a.n_valid = (int)D.E;
   a.out = logits;

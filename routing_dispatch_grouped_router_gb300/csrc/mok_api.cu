@@ -105,7 +105,11 @@ mok_status make_dims(const mok_moe_desc* desc, Dims* out) {
   if ((d.flags & MOK_FLAG_ACCUMULATE_WGRAD) && (d.flags & MOK_FLAG_BF16_WGRAD_OUT))
     return MOK_ERR_UNSUPPORTED;  // accumulation is fp32 only
   if (d.E > kMaxExperts || d.k > kMaxTopK || d.k > d.E) return MOK_ERR_UNSUPPORTED;
-  if (d.d % 128 != 0 || d.I % 128 != 0) return MOK_ERR_UNSUPPORTED;
+  // d: a multiple of 32 from 128 on (ragged GEMM tiles: zero-filled loads, unstored
+  // columns); I: a multiple of 128 (gate and up columns share a B tile); MXFP8
+  // operands: d a multiple of 128 as well
+  if (d.d % 32 != 0 || d.d < 128 || d.I % 128 != 0) return MOK_ERR_UNSUPPORTED;
+  if (d.dtype == MOK_MXFP8 && d.d % 128 != 0) return MOK_ERR_UNSUPPORTED;
   if (d.d > 16384 || d.I > 16384) return MOK_ERR_UNSUPPORTED;
   if (d.T * d.k >= (1LL << 31) / 2) return MOK_ERR_UNSUPPORTED;
   Dims D;

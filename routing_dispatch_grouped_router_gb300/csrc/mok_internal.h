@@ -47,7 +47,7 @@ struct Dims {
 inline int router_k_splits(const Dims& D) {
   const int64_t bn = D.E > 128 ? 256 : 128;
   const int64_t tiles = ((D.T + 127) / 128) * ((D.E + bn - 1) / bn);
-  const int64_t nkb = D.d / 64;
+  const int64_t nkb = (D.d + 63) / 64;
   int s = 1;
   while (s < 8 && tiles * s * 2 <= 128 && nkb % (s * 2) == 0) s *= 2;
   return s;
@@ -157,7 +157,8 @@ struct RwSplit {
   int kb;  // 64-token blocks per chunk
 };
 inline RwSplit router_wgrad_split(const Dims& D) {
-  const int64_t tiles = router_e_pad(D) / 128 * (D.d / router_wgrad_bn(D));
+  const int64_t bn = router_wgrad_bn(D);
+  const int64_t tiles = router_e_pad(D) / 128 * ((D.d + bn - 1) / bn);
   const int64_t nkb = (D.T + 63) / 64 > 0 ? (D.T + 63) / 64 : 1;
   int64_t ks = 152 / tiles;
   if (ks < 1) ks = 1;

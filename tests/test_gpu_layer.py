@@ -63,6 +63,10 @@ SMALL = {
     # d >= 6144 with 256-wide down-dgrad tiles: the SwiGLU backward stores
     # from registers (long K loop, five operand stages)
     "d7168": gen.Shape(T=256, d=7168, E=4, I=512, k=2),
+    # d a multiple of 32 but not of 128: ragged K blocks (zero-filled) and
+    # ragged N and M tiles (unstored chunks) wherever d is a GEMM dimension
+    "d160": gen.Shape(T=300, d=160, E=5, I=128, k=2),
+    "d2880": gen.Shape(T=128, d=2880, E=4, I=256, k=2),
 }
 
 
