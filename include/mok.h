@@ -30,10 +30,9 @@
  *
  * Shape requirements (MOK_ERR_UNSUPPORTED otherwise)
  *   1 <= k <= min(E, 8);  1 <= E <= 512;  0 <= T;  T*k < 2^31;
- *   d a multiple of 32, 128 <= d <= 16384 (a d that is not a multiple of the
- *   GEMM tiles gives ragged tiles: zero-filled loads, unstored columns);
- *   I a multiple of 128, I <= 16384 (gate and up columns share a GEMM tile);
- *   MOK_MXFP8: d a multiple of 128; MOK_NVFP4: d and I multiples of 256;
+ *   d and I multiples of 32, 128 <= d, I <= 16384 (widths that are not
+ *   multiples of the GEMM tiles give ragged tiles: zero-filled loads, unstored
+ *   columns); MOK_MXFP8: d and I multiples of 128; MOK_NVFP4: of 256;
  *   micro-batching: T a multiple of mb_tokens, 0 <= ring_slots <= T/mb_tokens,
  *   fp32 weight-gradient outputs (they accumulate over micro-batches).
  */

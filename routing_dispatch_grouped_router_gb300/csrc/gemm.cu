@@ -621,6 +621,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
     // C^T through TMA: accumulator rows are output columns; C viewed as
     // [E * N, M] with group e's block at rows e*N
     const int x = tl.row0 + q * 32;
+    if (a.m_valid > 0 && x >= a.m_valid) return;  // a ragged M tile (M a multiple of 32)
     const int col0 = tl.n_tile * BN + half * HALF_COLS;
 #pragma unroll 1
     for (int c = 0; c < HALF_COLS; c += 32) {
@@ -710,6 +711,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
     __nv_bfloat16* h = static_cast<__nv_bfloat16*>(a.out2) + r * (long long)I;
 #pragma unroll 1
     for (int c = 0; c < 64; c += 32) {
+      if (n0 + c >= I) break;  // a ragged last tile (I a multiple of 32)
       float g[32], u[32];
       tmem_ld32(taddr + half * 64 + c, g);
       tmem_ld32(taddr + 128 + half * 64 + c, u);
@@ -908,6 +910,9 @@ __device__ __forceinline__ uint32_t swiglu_bwd_tma(const GemmArgs& a, const Tile
       g[4 * j] = a4.x; g[4 * j + 1] = a4.y; g[4 * j + 2] = a4.z; g[4 * j + 3] = a4.w;
       u[4 * j] = b4.x; u[4 * j + 1] = b4.y; u[4 * j + 2] = b4.z; u[4 * j + 3] = b4.w;
     }
+    // a ragged last tile (I a multiple of 32): columns past I have no outputs
+    // and add nothing to dp (their g, u were still staged, and are dropped)
+    if (n0 + c >= I) continue;
     {
       uint32_t r0[16];
       tmem_ld16(taddr + half * HALF_COLS + c, r0);
@@ -1623,7 +1628,7 @@ cudaError_t gemm_fwd_gate_up(const Dims& D, const void* X_perm, const void* w_ga
   a.store_c = GU ? 1 : 0;
   a.evict_first = 1;  // g, u are read again only by the backward
   a.E = (int)D.E;
-  a.n_tiles = (int)(D.I / 128);
+  a.n_tiles = (int)((D.I + 127) / 128);  // a ragged last tile: FFN columns past I unstored
   a.num_kb = (int)((D.d + 63) / 64);  // a ragged last K block reads zeros
   a.b_group_rows = (int)(2 * D.I);
   a.I = (int)D.I;
@@ -1875,7 +1880,7 @@ cudaError_t gemm_fwd_down(const Dims& D, const void* H, const void* w_down,
   a.E = (int)D.E;
   a.n_tiles = (int)((D.d + bn - 1) / bn);
   a.n_valid = (int)D.d;
-  a.num_kb = (int)(D.I / 64);
+  a.num_kb = (int)((D.I + 63) / 64);
   a.b_group_rows = (int)D.d;
   a.mtile_prefix = mtile_prefix;
   a.poff = poff;
@@ -1916,7 +1921,7 @@ cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* 
   if (!make_map(&tb, w_down, D.I, D.E * D.d, D.I, 64)) return cudaErrorInvalidValue;
   GemmArgs a = blank_args(status);
   a.E = (int)D.E;
-  a.n_tiles = (int)(D.I / bn);
+  a.n_tiles = (int)((D.I + bn - 1) / bn);  // columns past I: no outputs, no dp
   a.num_kb = (int)((D.d + 63) / 64);  // dY reads zeros past d
   a.b_group_rows = (int)D.d;
   a.I = (int)D.I;
@@ -1961,7 +1966,7 @@ cudaError_t gemm_bwd_gate_up_dgrad(const Dims& D, const void* dGU, const void* w
   a.E = (int)D.E;
   a.n_tiles = (int)((D.d + bn - 1) / bn);
   a.n_valid = (int)D.d;
-  a.num_kb = (int)(2 * D.I / 64);
+  a.num_kb = (int)((2 * D.I + 63) / 64);
   a.b_group_rows = (int)(2 * D.I);
   a.mtile_prefix = mtile_prefix;
   a.poff = poff;
@@ -2095,7 +2100,8 @@ cudaError_t gemm_wgrad_down(const Dims& D, const void* dY_perm, const void* P_hi
   a.seg_rows = (int)D.rows_max;
   a.coff = sg.coff;
   a.E = (int)D.E;
-  a.m_tiles = (int)(D.I / 128);
+  a.m_tiles = (int)((D.I + 127) / 128);
+  a.m_valid = (int)D.I;
   a.n_tiles = (int)(D.d / 256);
   a.m_rows = (int)D.I;
   a.poff = poff;

@@ -105,11 +105,10 @@ mok_status make_dims(const mok_moe_desc* desc, Dims* out) {
   if ((d.flags & MOK_FLAG_ACCUMULATE_WGRAD) && (d.flags & MOK_FLAG_BF16_WGRAD_OUT))
     return MOK_ERR_UNSUPPORTED;  // accumulation is fp32 only
   if (d.E > kMaxExperts || d.k > kMaxTopK || d.k > d.E) return MOK_ERR_UNSUPPORTED;
-  // d: a multiple of 32 from 128 on (ragged GEMM tiles: zero-filled loads, unstored
-  // columns); I: a multiple of 128 (gate and up columns share a B tile); MXFP8
-  // operands: d a multiple of 128 as well
-  if (d.d % 32 != 0 || d.d < 128 || d.I % 128 != 0) return MOK_ERR_UNSUPPORTED;
-  if (d.dtype == MOK_MXFP8 && d.d % 128 != 0) return MOK_ERR_UNSUPPORTED;
+  // d and I: multiples of 32 from 128 on (ragged GEMM tiles: zero-filled loads,
+  // unstored columns); MXFP8 operands: multiples of 128 (its code tiles)
+  if (d.d % 32 != 0 || d.d < 128 || d.I % 32 != 0 || d.I < 128) return MOK_ERR_UNSUPPORTED;
+  if (d.dtype == MOK_MXFP8 && (d.d % 128 != 0 || d.I % 128 != 0)) return MOK_ERR_UNSUPPORTED;
   if (d.d > 16384 || d.I > 16384) return MOK_ERR_UNSUPPORTED;
   if (d.T * d.k >= (1LL << 31) / 2) return MOK_ERR_UNSUPPORTED;
   Dims D;
@@ -137,7 +136,7 @@ mok_status make_dims(const mok_moe_desc* desc, Dims* out) {
   D.rows_max = (D.R + (kRowPad - 1) * segs + kRowPad - 1) / kRowPad * kRowPad;
   D.nb = (D.T + kPlanBlock - 1) / kPlanBlock;
   D.bn_dgrad = (D.I % 256 == 0) ? 256 : 128;
-  D.np = static_cast<int>(D.I / D.bn_dgrad) * 2;
+  D.np = static_cast<int>((D.I + D.bn_dgrad - 1) / D.bn_dgrad) * 2;
   D.act_bf16 = (d.flags & MOK_FLAG_BF16_ACT_OUT) != 0;
   D.wgrad_bf16 = (d.flags & MOK_FLAG_BF16_WGRAD_OUT) != 0;
   D.mx = d.dtype == MOK_MXFP8;

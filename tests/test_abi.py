@@ -226,10 +226,12 @@ def test_status_strings(lib):
     assert lib.mok_status_string(999) == b"unknown status"
 
 
-def test_hidden_width_multiple_of_32(lib):
-    """d may be any multiple of 32 from 128 on in BF16 (ragged GEMM tiles);
-    MXFP8 keeps d a multiple of 128, NVFP4 of 256; I stays a multiple of 128."""
+def test_widths_multiples_of_32(lib):
+    """d and I may be any multiples of 32 from 128 on in BF16 (ragged GEMM
+    tiles); MXFP8 keeps them multiples of 128, NVFP4 of 256."""
     ok = lambda **kw: _sizes(lib, _desc(**kw))[0]
     assert ok(d=160) == 0 and ok(d=2880) == 0 and ok(d=7168) == 0
-    assert ok(d=96) == 2 and ok(d=200) == 2 and ok(I=160) == 2
-    assert ok(d=2880, dtype=1) == 2 and ok(d=2944, dtype=2, I=256) == 2
+    assert ok(I=160) == 0 and ok(I=2880) == 0 and ok(d=2880, I=2880) == 0
+    assert ok(d=96) == 2 and ok(d=200) == 2 and ok(I=96) == 2 and ok(I=200) == 2
+    assert ok(d=2880, dtype=1) == 2 and ok(I=160, dtype=1) == 2
+    assert ok(d=2944, dtype=2, I=256) == 2 and ok(d=256, dtype=2, I=384) == 2

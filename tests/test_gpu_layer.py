@@ -67,6 +67,13 @@ SMALL = {
     # ragged N and M tiles (unstored chunks) wherever d is a GEMM dimension
     "d160": gen.Shape(T=300, d=160, E=5, I=128, k=2),
     "d2880": gen.Shape(T=128, d=2880, E=4, I=256, k=2),
+    # I a multiple of 32 but not of 128: a ragged last gate/up tile (FFN
+    # columns past I unstored), ragged down-dgrad tiles (no outputs, no dp),
+    # ragged K blocks in the down projection and the gate/up dgrad, ragged M
+    # tiles in the weight gradients
+    "i160": gen.Shape(T=200, d=256, E=4, I=160, k=2),
+    "d160_i224": gen.Shape(T=150, d=160, E=6, I=224, k=3),
+    "d2880_i2880": gen.Shape(T=64, d=2880, E=4, I=2880, k=2),
 }
 
 
