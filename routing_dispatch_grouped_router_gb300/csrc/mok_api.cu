@@ -10,6 +10,7 @@
 //   [aikraft] "Cursor MoK: revolution in MoE model training on NVL72", §03:
 //     no CPU-GPU synchronisation on the critical path.  Every buffer and grid
 //     here is sized from (T, k, E, d, I) bounds; no count is read back.
+#include <nvtx3/nvToolsExt.h>
 #include <cuda_runtime.h>
 #include <string.h>
 
@@ -47,7 +48,12 @@ static cudaEvent_t pool_event() {
   return g_pool[g_pool_used++];
 }
 
+// Every kernel launch is also an NVTX range (domain-less, named as the kernel
+// step), and each forward / backward call one around them, so a system
+// profiler's timeline shows the layer's steps; without a tool attached the
+// NVTX calls return at once.
 void prof_begin(const char* name, cudaStream_t st) {
+  nvtxRangePushA(name);
   if (!g_prof) return;
   ProfRec r{name, pool_event(), pool_event()};
   if (!r.a || !r.b) return;
@@ -56,9 +62,16 @@ void prof_begin(const char* name, cudaStream_t st) {
 }
 
 void prof_end(cudaStream_t st) {
+  nvtxRangePop();
   if (!g_prof || g_recs.empty()) return;
   cudaEventRecord(g_recs.back().b, st);
 }
+
+// An NVTX range for the span of a scope (one forward or backward call).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 int num_sms_current_device() {
   static int cache[64] = {0};
@@ -388,6 +401,7 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
                            const float* router_bias, const void* w_gate_up, const void* w_down,
                            void* y, void* saved, size_t saved_bytes, void* workspace,
                            size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("mok_moe_forward");
   Dims D;
   mok_status s = make_dims(desc, &D);
   if (s != MOK_OK) return s;
@@ -528,6 +542,7 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
                             const void* w_gate_up, const void* w_down, const void* saved,
                             size_t saved_bytes, void* dx, void* dw_router, void* dw_gate_up,
                             void* dw_down, void* workspace, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("mok_moe_backward");
   (void)router_bias;
   Dims D;
   mok_status s = make_dims(desc, &D);
