@@ -537,3 +537,29 @@ def test_layer_step_replays_in_a_cuda_graph(dtype):
     assert layer.status() == 0
     for got, n in zip([y, dx] + dws, ("y", "dx", "dw_router", "dw_gate_up", "dw_down")):
         assert torch.equal(got, eager[n]), n
+
+
+def test_expert_relabelling_equivariance_fine():
+    """Relabelling the experts (their router rows, bias entries and weights
+    permuted together) leaves y and dx bitwise unchanged and permutes the
+    weight gradients, bit for bit: each expert's GEMMs see the same rows in the
+    same order wherever the expert sits, and the combine and the reverse
+    dispatch add the slots in logit order, not expert order."""
+    shape = gen.workload_shape("fine")
+    inp = gen.make_inputs(shape, seed=8)
+    perm = np.random.default_rng(8).permutation(shape.E)
+    relabelled = dict(inp)
+    for n in ("w_router", "w_gate_up", "w_down"):
+        relabelled[n] = np.ascontiguousarray(inp[n][perm])
+    if inp.get("bias") is not None:
+        relabelled["bias"] = np.ascontiguousarray(inp["bias"][perm])
+    a = _gpu.run_gpu(shape, inp)
+    b = _gpu.run_gpu(shape, relabelled)
+    assert a["status"] == 0 and b["status"] == 0
+    # expert i of the second run is expert perm[i] of the first
+    assert np.array_equal(perm[b["topk_idx"]], a["topk_idx"])
+    for n in ("y", "dx"):
+        assert torch.equal(b[n].view(torch.int32), a[n].view(torch.int32)), n
+    p = torch.from_numpy(perm).cuda()
+    for n in ("dw_router", "dw_gate_up", "dw_down"):
+        assert torch.equal(b[n].view(torch.int32), a[n][p].view(torch.int32)), n
