@@ -563,3 +563,18 @@ def test_expert_relabelling_equivariance_fine():
     p = torch.from_numpy(perm).cuda()
     for n in ("dw_router", "dw_gate_up", "dw_down"):
         assert torch.equal(b[n].view(torch.int32), a[n][p].view(torch.int32)), n
+
+
+@pytest.mark.parametrize("mode", ["single_cta", "micro_batched", "recompute"])
+def test_ragged_widths_in_every_layer_mode(mode):
+    """Ragged d and I (multiples of 32, not of the tiles) through the other
+    kernel paths: single-CTA tiles, micro-batches with deferred weight
+    gradients over a two-slot ring, and the recompute flags."""
+    shape = gen.Shape(T=150, d=160, E=6, I=224, k=3)
+    inp = gen.make_inputs(shape, seed=12)
+    kw = {"single_cta": dict(flags=api.FLAG_SINGLE_CTA_GEMM),
+          "micro_batched": dict(mb_tokens=50, ring_slots=2),
+          "recompute": dict(flags=api.FLAG_RECOMPUTE_GATE_UP | api.FLAG_RECOMPUTE_DISPATCH)}[mode]
+    gpu = _gpu.run_gpu(shape, inp, **kw)
+    assert gpu["status"] == 0
+    _gpu.full_parity(shape, inp, gpu)
