@@ -137,16 +137,22 @@ constexpr int kStagingBytes = 4096;  // per epilogue warp: 32 rows x 128 bytes
 // tcgen05.mma.cta_group::2; each CTA stages its own 128 rows of A and BN/2
 // rows of B, and holds its 128 x BN accumulator in its own TMEM.
 // Staging bytes per epilogue warp: 4 KB (TMA-store blocks); the SwiGLU
-// backward double-buffers its fp32 g, u operands (2 x 4 KB) and stages the
-// six bf16 output blocks of a chunk (6 x 1 KB).
-constexpr int kGuStageBytes = 8192;
-constexpr int kSwigluBwdStaging = kGuStageBytes + 6 * 1024;
+// backward stages its fp32 g, u operands in one 4 KB buffer (the next chunk's
+// copies go out as soon as the warp holds the current one in registers) and
+// the six bf16 output blocks of a chunk (6 x 1 KB).  One g, u buffer instead
+// of two gives the pair kernel a fourth operand stage (imbalanced workload:
+// 1922 -> 1679 us; fine 255 -> 252 us).
+constexpr int kGuBufBytes = 4096;
+constexpr int kSwigluBwdStaging = kGuBufBytes + 6 * 1024;
 // The SwiGLU backward with its outputs stored straight from registers (DB on
 // EPI_SWIGLU_BWD): no output staging, so two more operand stages.  Faster
 // where the K loop (d) is long and the weights stream: large workload,
 // d = 7168, 3117 -> 2977 us; slower where the epilogue dominates: fine,
 // d = 2048, 257 -> 327 us (16-byte stores, half a sector per lane and store).
-constexpr int kSwigluBwdStagingDirect = kGuStageBytes;
+// This form keeps two g, u buffers (chunk n + 1's copies in flight while
+// chunk n waits): with one, and a sixth operand stage, it measured slower
+// (2977 -> 3211 us).
+constexpr int kSwigluBwdStagingDirect = 2 * kGuBufBytes;
 constexpr int kSwigluBwdDirectMinD = 6144;
 // Double-buffered store staging (DB: a block is written while the previous
 // block's store still reads shared memory), chosen per launch for the fp32
@@ -208,7 +214,7 @@ static_assert(Cfg<256, SPLIT_NONE, true>::SMEM_BYTES <= 232448 &&
 static_assert(Cfg<256, SPLIT_A, true>::SMEM_BYTES <= 232448 &&
                   Cfg<256, SPLIT_A, true>::STAGES >= 4, "smem");
 static_assert(Cfg<256, SPLIT_NONE, true, kSwigluBwdStaging>::SMEM_BYTES <= 232448 &&
-                  Cfg<256, SPLIT_NONE, true, kSwigluBwdStaging>::STAGES == 3 &&
+                  Cfg<256, SPLIT_NONE, true, kSwigluBwdStaging>::STAGES == 4 &&
                   Cfg<256, SPLIT_NONE, true, kSwigluBwdStagingDirect>::STAGES == 5, "smem");
 static_assert(Cfg<256, SPLIT_NONE, false, kSwigluBwdStaging>::STAGES >= 2 &&
                   Cfg<128, SPLIT_NONE, false, kSwigluBwdStaging>::STAGES >= 3, "smem");
@@ -847,11 +853,12 @@ __device__ __forceinline__ void epilogue_regs(const GemmArgs& a, const Tile& tl,
 
 // ------------------------------------------ SwiGLU backward, TMA operands --
 // g, u of one chunk: 32 rows (this warp's lane quarter) x 16 fp32 columns of
-// each, TMA-loaded into a 4 KB staging buffer (g at +0, u at +2048, 64-byte
-// swizzle: 16-byte chunk j of row r at chunk j ^ ((r >> 1) & 3)).  The
-// warp's chunks are numbered from the kernel start; chunk n uses buffer n & 1
-// and completes phase n >> 1 of that buffer's barrier.
-template <int BN>
+// each, TMA-loaded into one of the warp's NBUF 4 KB staging buffers (g at +0,
+// u at +2048, 64-byte swizzle: 16-byte chunk j of row r at chunk
+// j ^ ((r >> 1) & 3)).  The warp's chunks are numbered from the kernel
+// start; chunk n uses buffer n % NBUF and completes phase n / NBUF of that
+// buffer's barrier.
+template <int BN, int NBUF>
 __device__ __forceinline__ void gu_issue(const GemmArgs& a, const Tile& tl, int q, int lane,
                                          int half, int c, uint8_t* stage_buf, uint64_t* wbar,
                                          uint32_t count, const CUtensorMap* tmG) {
@@ -859,18 +866,21 @@ __device__ __forceinline__ void gu_issue(const GemmArgs& a, const Tile& tl, int 
   fence_proxy_async_smem();
   __syncwarp();
   if (lane != 0) return;
-  const int b = count & 1;
-  uint8_t* buf = stage_buf + b * 4096;
+  const int b = NBUF == 2 ? static_cast<int>(count & 1u) : 0;
+  uint8_t* buf = stage_buf + b * kGuBufBytes;
   const int x = tl.n_tile * BN + half * (BN / 2) + c;
   const int y = tl.row0 + q * 32;
-  mbar_arrive_expect_tx(&wbar[b], 4096);
+  mbar_arrive_expect_tx(&wbar[b], kGuBufBytes);
   tma_load_2d(buf, tmG, &wbar[b], x, y);
   tma_load_2d(buf + 2048, tmG, &wbar[b], a.I + x, y);
 }
 
 // The SwiGLU backward epilogue of one tile with g, u staged by TMA, chunk 0
 // already requested; the next chunk's copies are in flight while this one is
-// computed.  Returns the updated chunk count.  With a.mx, dG and dU are also
+// computed (with one buffer they are issued once every lane holds the current
+// chunk's g, u in registers; with two, before waiting for it).  DIRECT stores
+// the outputs from registers and keeps two buffers.  Returns the updated
+// chunk count.  With a.mx, dG and dU are also
 // quantised to MXFP8 (the gate/up dgrad's A operand): a block is 32
 // consecutive columns of a row, so each odd chunk encodes itself together
 // with the even chunk before it (n0 is a multiple of 32).
@@ -885,23 +895,25 @@ __device__ __forceinline__ uint32_t swiglu_bwd_tma(const GemmArgs& a, const Tile
   const int I = a.I;
   const int n0 = tl.n_tile * BN + half * HALF_COLS;
   const int y = tl.row0 + q * 32;
+  constexpr int NBUF = DIRECT ? 2 : 1;
   // output blocks of a chunk, 32 rows x 32 bytes each: dG hi, dG lo, dU hi,
   // dU lo, P hi, P lo
-  uint8_t* ostage = stage_buf + kGuStageBytes;
+  uint8_t* ostage = stage_buf + NBUF * kGuBufBytes;
   const float p = a.row_w[r];
   float dp = 0.f;
   const int sw = (lane >> 1) & 3;
   float t_prev[16], dA_prev[16];  // mx: the even chunk's dG, dU
 #pragma unroll 1
   for (int c = 0; c < HALF_COLS; c += 16, ++count) {
-    if (c + 16 < HALF_COLS)
-      gu_issue<BN>(a, tl, q, lane, half, c + 16, stage_buf, wbar, count + 1, tmG);
-    const int b = count & 1;
-    if (!mbar_wait(&wbar[b], (count >> 1) & 1u, vabort)) {
+    if (NBUF == 2 && c + 16 < HALF_COLS)
+      gu_issue<BN, NBUF>(a, tl, q, lane, half, c + 16, stage_buf, wbar, count + 1, tmG);
+    const int b = NBUF == 2 ? static_cast<int>(count & 1u) : 0;
+    const uint32_t par = NBUF == 2 ? ((count >> 1) & 1u) : (count & 1u);
+    if (!mbar_wait(&wbar[b], par, vabort)) {
       *vabort = 1;
       set_status(a.status, MOK_ERR_DEVICE_TIMEOUT);
     }
-    const uint8_t* buf = stage_buf + b * 4096 + lane * 64;
+    const uint8_t* buf = stage_buf + b * kGuBufBytes + lane * 64;
     float g[16], u[16], dA[16], t[16];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -910,6 +922,10 @@ __device__ __forceinline__ uint32_t swiglu_bwd_tma(const GemmArgs& a, const Tile
       g[4 * j] = a4.x; g[4 * j + 1] = a4.y; g[4 * j + 2] = a4.z; g[4 * j + 3] = a4.w;
       u[4 * j] = b4.x; u[4 * j + 1] = b4.y; u[4 * j + 2] = b4.z; u[4 * j + 3] = b4.w;
     }
+    // one buffer: it is free again, so the next chunk's copies go out
+    // (gu_issue orders every lane's reads above before them)
+    if (NBUF == 1 && c + 16 < HALF_COLS)
+      gu_issue<BN, NBUF>(a, tl, q, lane, half, c + 16, stage_buf, wbar, count + 1, tmG);
     // a ragged last tile (I a multiple of 32): columns past I have no outputs
     // and add nothing to dp (their g, u were still staged, and are dropped)
     if (n0 + c >= I) continue;
@@ -1411,7 +1427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t acc_par = static_cast<uint32_t>(C::NACC == 2 ? ((it >> 1) & 1) : (it & 1));
       // the tile's first g, u chunk does not depend on the accumulator
       if (kGuTma && valid)
-        gu_issue<BN>(args, tl, q, lane, half, 0, stage_buf, wbar, gu_chunks, &tmC);
+        gu_issue<BN, kDbuf ? 2 : 1>(args, tl, q, lane, half, 0, stage_buf, wbar, gu_chunks,
+                                    &tmC);
       if (!wait(&tfull[acc], acc_par)) {
         *vabort = 1;
         set_status(args.status, MOK_ERR_DEVICE_TIMEOUT);
