@@ -57,35 +57,74 @@ static __host__ __device__ inline long long nv_tiled_off(long long r, long long 
 
 namespace {
 
-// amax of the tensor as the bits of a non-negative float (the integer order of
-// such bits is their value order, so atomicMax takes the maximum whatever the
-// order of the updates).
-__global__ void nv_amax_kernel(const uint4* __restrict__ in, long long nchunks,
-                               unsigned* __restrict__ amax_bits,
-                               const int32_t* __restrict__ rows_dev, long long row_chunks,
-                               const int32_t* __restrict__ rowmap) {
-  // rows_dev (or NULL): only the first *rows_dev rows of row_chunks chunks;
-  // rowmap (or NULL): rows r with rowmap[r] < 0 (padding) do not count
-  if (rows_dev) {
-    const long long lim = static_cast<long long>(*rows_dev) * row_chunks;
-    nchunks = lim < nchunks ? lim : nchunks;
-  }
+// Largest |value| of eight bf16 values (one 16-byte chunk).
+__device__ __forceinline__ float amax8(const uint4& w) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
   float m = 0.f;
-  const long long G = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < nchunks;
-       i += G) {
-    if (rowmap && rowmap[i / row_chunks] < 0) continue;
-    const uint4 w = in[i];
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      m = fmaxf(m, fabsf(bf16lo(u[j])));
-      m = fmaxf(m, fabsf(bf16hi(u[j])));
-    }
+  for (int j = 0; j < 4; ++j) {
+    m = fmaxf(m, fabsf(bf16lo(u[j])));
+    m = fmaxf(m, fabsf(bf16hi(u[j])));
   }
+  return m;
+}
+
+// The warp's amax into *amax_bits as the bits of a non-negative float (the
+// integer order of such bits is their value order, so atomicMax takes the
+// maximum whatever the order of the updates).
+__device__ __forceinline__ void amax_publish(float m, unsigned* amax_bits) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
   if ((threadIdx.x & 31) == 0) atomicMax(amax_bits, __float_as_uint(m));
+}
+
+// Plain tensor of nchunks 16-byte chunks (8 bf16 values each), grid-strided
+// with four independent loads in flight per thread.
+__global__ void nv_amax_kernel(const uint4* __restrict__ in, long long nchunks,
+                               unsigned* __restrict__ amax_bits) {
+  float m = 0.f;
+  const long long G = static_cast<long long>(gridDim.x) * blockDim.x;
+  long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + 3 * G < nchunks; i += 4 * G) {
+    uint4 w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w[j] = __ldg(in + i + j * G);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m = fmaxf(m, amax8(w[j]));
+  }
+  for (; i < nchunks; i += G) m = fmaxf(m, amax8(__ldg(in + i)));
+  amax_publish(m, amax_bits);
+}
+
+// A [nrows, row_chunks] tensor, one warp per row (the lanes split the row's
+// chunks, four loads in flight each): rows_dev (or NULL) limits it to the
+// first *rows_dev rows, and rows r with rowmap[r] < 0 (padding) do not count.
+__global__ void nv_amax_rows_kernel(const uint4* __restrict__ in, long long nrows,
+                                    int row_chunks, unsigned* __restrict__ amax_bits,
+                                    const int32_t* __restrict__ rows_dev,
+                                    const int32_t* __restrict__ rowmap) {
+  if (rows_dev) {
+    const long long lim = *rows_dev;
+    nrows = lim < nrows ? lim : nrows;
+  }
+  const int lane = threadIdx.x & 31;
+  const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  float m = 0.f;
+  for (long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+       r < nrows; r += nw) {
+    if (rowmap && rowmap[r] < 0) continue;  // the same row for the whole warp
+    const uint4* p = in + r * row_chunks;
+    int c = lane;
+    for (; c + 96 < row_chunks; c += 128) {
+      uint4 w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[j] = __ldg(p + c + 32 * j);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) m = fmaxf(m, amax8(w[j]));
+    }
+    for (; c < row_chunks; c += 32) m = fmaxf(m, amax8(__ldg(p + c)));
+  }
+  amax_publish(m, amax_bits);
 }
 
 // *g (holding the amax bits) <- the tensor scale
@@ -429,13 +468,24 @@ cudaError_t launch_nv_tensor_scale(const void* in, long long n, float* g, cudaSt
   if (e != cudaSuccess) return e;
   const long long nchunks = n / 8;
   if (nchunks > 0) {
-    long long grid = (nchunks + 255) / 256;
     const long long cap = static_cast<long long>(num_sms_current_device()) * 8;
-    if (grid > cap) grid = cap;
     ProfScope prof("nvfp4_amax", st);
-    nv_amax_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(
-        static_cast<const uint4*>(in), nchunks, reinterpret_cast<unsigned*>(g), rows_dev,
-        (rows_dev || rowmap) ? row_elems / 8 : 1, rowmap);
+    if (rows_dev || rowmap) {
+      // whole rows of row_elems values (a multiple of 8)
+      const long long row_chunks = row_elems / 8, nrows = nchunks / row_chunks;
+      if (row_elems % 8 || row_chunks > (1 << 30)) return cudaErrorInvalidValue;
+      long long grid = (nrows + 7) / 8;  // eight warps per CTA, one row each
+      if (grid > cap) grid = cap;
+      if (grid < 1) grid = 1;
+      nv_amax_rows_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(
+          static_cast<const uint4*>(in), nrows, static_cast<int>(row_chunks),
+          reinterpret_cast<unsigned*>(g), rows_dev, rowmap);
+    } else {
+      long long grid = (nchunks + 255) / 256;
+      if (grid > cap) grid = cap;
+      nv_amax_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(
+          static_cast<const uint4*>(in), nchunks, reinterpret_cast<unsigned*>(g));
+    }
     count_launch();
   }
   nv_scale_kernel<<<1, 1, 0, st>>>(g);
@@ -507,8 +557,7 @@ extern "C" mok_status mok_nvfp4_tensor_scale(const void* in, int64_t n, float* g
     if (grid > cap) grid = cap;
     ProfScope prof("nvfp4_amax", st);
     nv_amax_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(
-        static_cast<const uint4*>(in), nchunks, reinterpret_cast<unsigned*>(g), nullptr, 1,
-        nullptr);
+        static_cast<const uint4*>(in), nchunks, reinterpret_cast<unsigned*>(g));
     count_launch();
   }
   nv_scale_kernel<<<1, 1, 0, st>>>(g);
