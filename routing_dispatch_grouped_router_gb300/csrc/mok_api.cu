@@ -522,7 +522,7 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
       // go to MXFP8 straight from the token rows (no bf16 copy), the gate/up
       // GEMM writes h as MXFP8 for the down projection
       MOK_CUDA(launch_mx_rows(xi, nullptr, D.rows_max, D.d, xq_c, xq_s, st, true, o.ptok,
-                              static_cast<int>(D.T)));
+                              static_cast<int>(D.T), o.padded_offsets + D.E));
       MOK_CUDA(gemm_fwd_gate_up_mx(D, xq_c, xq_s, wgu_c, wgu_s, o.mtile_prefix, o.padded_offsets,
                                    gu, h_c, h_s, status, st));
       MOK_CUDA(gemm_fwd_down_mx(D, h_c, h_s, wd_c, wd_s, o.mtile_prefix, o.padded_offsets, O,
@@ -655,7 +655,7 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
       // the forward's gate/up GEMM again, g and u only (no h)
       if (D.mx) {
         MOK_CUDA(launch_mx_rows(xi, nullptr, D.rows_max, D.d, rxq_c, rxq_s, st, true, ptok,
-                                static_cast<int>(D.T)));
+                                static_cast<int>(D.T), poff + D.E));
         MOK_CUDA(gemm_fwd_gate_up_mx(D, rxq_c, rxq_s, rwgu_c, rwgu_s, mtp, poff,
                                      const_cast<void*>(gu), nullptr, nullptr, status, st));
       } else {
@@ -673,11 +673,12 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
       void* q1 = at<char>(workspace, B.dyq_row);
       void* q2 = slot(at<char>(workspace, B.dyq_col), i, rows * D.d * 2);
       void* q3 = slot(at<char>(workspace, B.xq_col), i, rows * D.d * 2);
-      // dy in both block directions from one read of its token rows
+      // dy in both block directions from one read of its token rows; rows
+      // past the plan's padded total are read by no GEMM and left unwritten
       MOK_CUDA(launch_mx_cols(dyi, q2, D.rows_max, D.d, nullptr, nullptr, st, q1, ptok,
-                              static_cast<int>(D.T)));
+                              static_cast<int>(D.T), poff + D.E));
       MOK_CUDA(launch_mx_cols(xi, q3, D.rows_max, D.d, nullptr, nullptr, st, nullptr, ptok,
-                              static_cast<int>(D.T)));
+                              static_cast<int>(D.T), poff + D.E));
       dy_row_op = q1;
       dy_col_op = q2;
       x_col_op = q3;

@@ -262,9 +262,12 @@ cudaError_t gemm_dense_bf16(int64_t M, int64_t N, int64_t K, const void* A, bool
 // 128), the layout of the expert GEMMs' MXFP8 operands; else row-major.
 // rowmap != NULL: output row r quantises input row rowmap[r] (zeros where that is
 // not in [0, T)), so the dispatched rows need not be materialised.
+// rows_dev (or NULL; row-map form only): the device count of leading rows
+// that anything reads; later rows are left unwritten.
 cudaError_t launch_mx_rows(const void* in, void* out, long long rows, long long cols,
                            uint8_t* codes, uint8_t* scales, cudaStream_t st, bool tiled = false,
-                           const int32_t* rowmap = nullptr, int T = 0);
+                           const int32_t* rowmap = nullptr, int T = 0,
+                           const int32_t* rows_dev = nullptr);
 
 // A weight [ng*K, C] in both block directions from one read: rows (blocks of
 // 32 along C) as codes [ng*K, C] with tiled scales, and columns (blocks of 32
@@ -275,9 +278,11 @@ cudaError_t launch_mx_quant_2d(const void* in, long long ng, long long K, long l
                                uint8_t* cscales, void* cvals, cudaStream_t st);
 // Column blocks (rows % 32 == 0, cols % 8 == 0); rows_out != NULL also writes
 // the row-block dequantised values of the same input (cols % 32 == 0).
+// rows_dev (or NULL): as launch_mx_rows' (whole 32-row blocks).
 cudaError_t launch_mx_cols(const void* in, void* out, long long rows, long long cols,
                            uint8_t* codes, uint8_t* scales, cudaStream_t st,
-                           void* rows_out = nullptr, const int32_t* rowmap = nullptr, int T = 0);
+                           void* rows_out = nullptr, const int32_t* rowmap = nullptr, int T = 0,
+                           const int32_t* rows_dev = nullptr);
 
 // NVFP4 (nvfp4.cu): the tensor scale of n bf16 values into the device *g
 // (which the call also uses as scratch), and codes [rows, cols/2] with E4M3

@@ -82,6 +82,9 @@ __device__ __forceinline__ void uniform_factors(int s, float (&down)[8], float (
 struct RowMap {
   const int32_t* map;  // NULL: output row r is input row r
   int T;
+  // NULL, or the number of leading output rows anything reads (the plan's
+  // padded row total, on the device): rows past it are left unwritten
+  const int32_t* nrows;
 };
 
 constexpr int kRowUnroll = 4;
@@ -132,8 +135,11 @@ __global__ void __launch_bounds__(256) mx_rows_kernel(const uint4* __restrict__ 
 
 // Row blocks of rows taken through a row map (output row r quantises input row
 // map[r], zeros when that is not a row of the input): one warp per output
-// row, the map read once per row; the lanes walk the row in 16-byte chunks,
-// four lanes per 32-value block as in mx_rows_kernel.  c8 % 4 == 0.
+// row, the map read once per row (the warp's next row's entry is read while
+// this row is processed); the lanes walk the row in 16-byte chunks, kMapUnroll
+// in flight per lane, four lanes per 32-value block as in mx_rows_kernel.
+// c8 % 4 == 0.
+constexpr int kMapUnroll = 8;
 template <bool CODES, bool OUT>
 __global__ void __launch_bounds__(256) mx_rows_map_kernel(const uint4* __restrict__ in,
                                                           uint4* __restrict__ out,
@@ -142,22 +148,28 @@ __global__ void __launch_bounds__(256) mx_rows_map_kernel(const uint4* __restric
                                                           long long rows, uint32_t c8,
                                                           long long tiled_nkg, RowMap rm) {
   grid_dep_launch();  // a GEMM after this kernel may start its prologue
+  if (rm.nrows) {
+    const long long lim = *rm.nrows;
+    rows = lim < rows ? lim : rows;
+  }
   const int lane = threadIdx.x & 31;
   const long long nw = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
-  for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
-       r < rows; r += nw) {
-    const int t = rm.map[r];
+  long long r = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+  int t_next = r < rows ? rm.map[r] : -1;
+  for (; r < rows; r += nw) {
+    const int t = t_next;
+    if (r + nw < rows) t_next = rm.map[r + nw];
     const bool src_ok = t >= 0 && t < rm.T;
     const uint4* src = in + static_cast<long long>(src_ok ? t : 0) * c8;
-    for (uint32_t j0 = 0; j0 < c8; j0 += 32 * kRowUnroll) {  // the same trips for every lane
-      uint4 w[kRowUnroll];
+    for (uint32_t j0 = 0; j0 < c8; j0 += 32 * kMapUnroll) {  // the same trips for every lane
+      uint4 w[kMapUnroll];
 #pragma unroll
-      for (int u = 0; u < kRowUnroll; ++u) {
+      for (int u = 0; u < kMapUnroll; ++u) {
         const uint32_t j = j0 + u * 32 + lane;
         w[u] = (src_ok && j < c8) ? ld_global_nc_v4(src + j) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int u = 0; u < kRowUnroll; ++u) {
+      for (int u = 0; u < kMapUnroll; ++u) {
         const uint32_t j = j0 + u * 32 + lane;
         float v[8];
         unpack8(w[u], v);
@@ -203,14 +215,18 @@ __global__ void __launch_bounds__(256, ROWS_OUT ? 3 : 4) mx_cols_kernel(const ui
   __shared__ __align__(16) int s_exp[256];
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   const long long c8 = cols / 8;  // 16-byte chunks per row
+  if (rm.nrows) {
+    const long long lim = (static_cast<long long>(*rm.nrows) + 31) / 32;
+    row_blocks = lim < row_blocks ? lim : row_blocks;
+  }
   // tile counts below 2^31 (checked by the launcher): 32-bit division
   const uint32_t tiles_c = static_cast<uint32_t>((cols + 255) / 256);
   const uint32_t ntiles = static_cast<uint32_t>(row_blocks) * tiles_c;
-  for (uint32_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+  // this thread's four chunks of tile t (zeros outside the input)
+  auto load_tile = [&](uint32_t t, uint4 (&x)[4]) {
     const long long rb = t / tiles_c, tc = t - static_cast<uint32_t>(rb) * tiles_c;
-    const long long ch = tc * 32 + l;  // this lane's chunk of each row
+    const long long ch = tc * 32 + l;
     const bool ok = ch < c8;
-    uint4 x[4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       long long src = rb * 32 + w + 8 * r;
@@ -220,6 +236,19 @@ __global__ void __launch_bounds__(256, ROWS_OUT ? 3 : 4) mx_cols_kernel(const ui
       }
       x[r] = (ok && src >= 0) ? ld_global_nc_v4(in + src * c8 + ch) : make_uint4(0, 0, 0, 0);
     }
+  };
+  // the next trip's loads (and their row-map reads) are in flight while this
+  // trip is reduced and quantised
+  uint4 xn[4];
+  if (blockIdx.x < ntiles) load_tile(blockIdx.x, xn);
+  for (uint32_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const long long rb = t / tiles_c, tc = t - static_cast<uint32_t>(rb) * tiles_c;
+    const long long ch = tc * 32 + l;  // this lane's chunk of each row
+    const bool ok = ch < c8;
+    uint4 x[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) x[r] = xn[r];
+    if (t + gridDim.x < ntiles) load_tile(t + gridDim.x, xn);
     float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -419,13 +448,14 @@ static unsigned grid_for(long long n, int threads) {
 
 cudaError_t launch_mx_rows(const void* in, void* out, long long rows, long long cols,
                            uint8_t* codes, uint8_t* scales, cudaStream_t st, bool tiled,
-                           const int32_t* rowmap, int T) {
+                           const int32_t* rowmap, int T, const int32_t* rows_dev) {
   if (cols % 32) return cudaErrorInvalidValue;
   if (tiled && (rows % 128 || cols % 128)) return cudaErrorInvalidValue;
   const long long nchunks = rows * (cols / 8);
   if (nchunks == 0) return cudaSuccess;
   if (nchunks / 4 >= (1LL << 32)) return cudaErrorInvalidValue;  // 32-bit block index
-  const RowMap rm{rowmap, T};
+  if (rows_dev && !rowmap) return cudaErrorInvalidValue;  // (the row-map kernel honours it)
+  const RowMap rm{rowmap, T, rows_dev};
   const uint32_t c8 = static_cast<uint32_t>(cols / 8);
   ProfScope prof("mx_quant_rows", st);
   const uint4* i4 = static_cast<const uint4*>(in);
@@ -462,8 +492,8 @@ cudaError_t launch_mx_rows(const void* in, void* out, long long rows, long long 
 
 cudaError_t launch_mx_cols(const void* in, void* out, long long rows, long long cols,
                            uint8_t* codes, uint8_t* scales, cudaStream_t st, void* rows_out,
-                           const int32_t* rowmap, int T) {
-  const RowMap rm{rowmap, T};
+                           const int32_t* rowmap, int T, const int32_t* rows_dev) {
+  const RowMap rm{rowmap, T, rows_dev};
   if (rows % 32 || cols % 8 || (rows_out && (cols % 32 || !out || codes)))
     return cudaErrorInvalidValue;
   const long long ntiles = (rows / 32) * ((cols + 255) / 256);
