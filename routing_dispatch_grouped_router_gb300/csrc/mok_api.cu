@@ -509,12 +509,13 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
       // its tensor scale (over the plan's rows) and its codes
       MOK_CUDA(launch_nv_tensor_scale(xi, D.T * D.d, nvg + 0, st));
       MOK_CUDA(launch_nv_quant_tiled(xi, D.rows_max, D.d, nvg + 0, nxq_c, nxq_s, o.ptok,
-                                     static_cast<int>(D.T), st));
+                                     static_cast<int>(D.T), st, o.padded_offsets + D.E));
       MOK_CUDA(gemm_fwd_gate_up_nv(D, nxq_c, nxq_s, nvg + 0, nwgu_c, nwgu_s, nvw + 0,
                                    o.mtile_prefix, o.padded_offsets, gu, h, status, st));
       MOK_CUDA(launch_nv_tensor_scale(h, D.rows_max * D.I, nvg + 1, st,
                                       o.padded_offsets + D.E, D.I));
-      MOK_CUDA(launch_nv_quant_tiled(h, D.rows_max, D.I, nvg + 1, nh_c, nh_s, nullptr, 0, st));
+      MOK_CUDA(launch_nv_quant_tiled(h, D.rows_max, D.I, nvg + 1, nh_c, nh_s, nullptr, 0, st,
+                                     o.padded_offsets + D.E));
       MOK_CUDA(gemm_fwd_down_nv(D, nh_c, nh_s, nvg + 1, nwd_c, nwd_s, nvw + 1, o.mtile_prefix,
                                 o.padded_offsets, O, status, st));
     } else if (D.mx) {
@@ -706,7 +707,7 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
       MOK_CUDA(launch_nv_tensor_scale(dgu_hi_i, D.rows_max * 2 * D.I, nv_dgu_g, st, poff + D.E,
                                       2 * D.I, ptok));
       MOK_CUDA(launch_nv_quant_tiled(dgu_hi_i, D.rows_max, 2 * D.I, nv_dgu_g, dgu_c, dgu_s,
-                                     nullptr, 0, st));
+                                     nullptr, 0, st, poff + D.E));
       MOK_CUDA(gemm_bwd_gate_up_dgrad_nv(D, dgu_c, dgu_s, nv_dgu_g, wgu_t_c, wgu_t_s, nv_wgu_g,
                                          mtp, poff, dx_perm, status, st));
     } else

@@ -302,9 +302,11 @@ cudaError_t launch_nv_quant_2d(const void* in, long long ng, long long K, long l
                                const float* g, uint8_t* rcodes, uint8_t* rscales,
                                uint8_t* ccodes, uint8_t* cscales, cudaStream_t st,
                                bool ctiled = true);
+// rows_dev (or NULL): the device count of leading rows that anything reads;
+// later rows are left unwritten.
 cudaError_t launch_nv_quant_tiled(const void* in, long long rows, long long cols, const float* g,
                                   uint8_t* codes, uint8_t* scales, const int32_t* map, int T,
-                                  cudaStream_t st);
+                                  cudaStream_t st, const int32_t* rows_dev = nullptr);
 
 // One CTA whose mbarrier wait can never complete: exercises the bounded wait.
 cudaError_t launch_bounded_wait_selftest(int* status, cudaStream_t st);

@@ -170,10 +170,16 @@ __device__ __forceinline__ uint8_t nv_block(const float (&v)[16], float g, float
 // 64 * tiled_nkb columns (nv_tiled_off); 0: row-major [rows, cols/16].
 // map (or NULL): output row r takes input row map[r] when that is a row of
 // the input (0 <= map[r] < T), zeros otherwise (codes 0, scale 0).
+// rows_dev (or NULL): only the first *rows_dev rows (the rows anything reads).
 __global__ void nv_quant_kernel(const uint4* __restrict__ in, long long nblk, int blk_per_row,
                                 const float* __restrict__ g_ptr, uint8_t* __restrict__ codes,
                                 uint8_t* __restrict__ scales, long long tiled_nkb,
-                                const int32_t* __restrict__ map, int T) {
+                                const int32_t* __restrict__ map, int T,
+                                const int32_t* __restrict__ rows_dev) {
+  if (rows_dev) {
+    const long long lim = static_cast<long long>(*rows_dev) * blk_per_row;
+    nblk = lim < nblk ? lim : nblk;
+  }
   const float g = *g_ptr;
   const float r6 = __frcp_rn(6.0f * g);
   const long long G = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -522,7 +528,7 @@ cudaError_t launch_nv_quant_2d(const void* in, long long ng, long long K, long l
 
 cudaError_t launch_nv_quant_tiled(const void* in, long long rows, long long cols, const float* g,
                                   uint8_t* codes, uint8_t* scales, const int32_t* map, int T,
-                                  cudaStream_t st) {
+                                  cudaStream_t st, const int32_t* rows_dev) {
   const long long nblk = rows * cols / 16;
   if (nblk == 0) return cudaSuccess;
   long long grid = (nblk + 255) / 256;
@@ -531,7 +537,7 @@ cudaError_t launch_nv_quant_tiled(const void* in, long long rows, long long cols
   ProfScope prof("nvfp4_quantize", st);
   nv_quant_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(
       static_cast<const uint4*>(in), nblk, static_cast<int>(cols / 16), g, codes, scales,
-      cols / 64, map, T);
+      cols / 64, map, T, rows_dev);
   count_launch();
   return cudaGetLastError();
 }
@@ -584,7 +590,7 @@ extern "C" mok_status mok_nvfp4_quantize(const void* in, int64_t rows, int64_t c
   ProfScope prof("nvfp4_quantize", st);
   nv_quant_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(
       static_cast<const uint4*>(in), nblk, static_cast<int>(cols / 16), g, codes, scales, 0,
-      nullptr, 0);
+      nullptr, 0, nullptr);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? MOK_OK : MOK_ERR_CUDA;
 }
