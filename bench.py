@@ -147,12 +147,12 @@ def gemm_bytes(shape: gen.Shape, micro_batches: int = 1, mx: bool = False,
 # (kernels as of the commit each file names); a kernel changed since its
 # capture has no entry.
 NCU_TRAFFIC_FINE = {
-    "fwd_gate_up_swiglu": 687.948544e6 + 329.665e6,
-    "fwd_down": 343.4496e6 + 254.065e6,
-    "bwd_down_dgrad_swiglu": 768.087808e6 + 401.775e6,
-    "bwd_down_wgrad": 284.920576e6 + 479.158e6,
-    "bwd_gate_up_dgrad": 688.581888e6 + 271.775e6,
-    "bwd_gate_up_wgrad": 427.131136e6 + 1013.622e6,
+    "fwd_gate_up_swiglu": 692.171008e6 + 331.434e6,
+    "fwd_down": 343.480064e6 + 254.962e6,
+    "bwd_down_dgrad_swiglu": 793.161984e6 + 407.398e6,
+    "bwd_down_wgrad": 284.956928e6 + 479.619e6,
+    "bwd_gate_up_dgrad": 691.839488e6 + 272.103e6,
+    "bwd_gate_up_wgrad": 427.144704e6 + 1013.483e6,
 }
 # The large workload's GEMMs from a capture of its slice (1/16 of its experts and
 # tokens, the same widths and rows per expert): per-expert work, so 16x the bytes.
