@@ -175,7 +175,7 @@ def ncu_traffic(workload: str, kernel: str):
     return table.get(kernel), src
 
 
-def mx_quant_bytes(shape: gen.Shape, nmb: int, rows_max: int, kernels: dict, steps: int) -> dict:
+def mx_quant_bytes(shape: gen.Shape, nmb: int, kernels: dict, steps: int) -> dict:
     """Average bytes per launch of the MXFP8 quantisers in one step.  Once per
     call, one launch per weight reads it and writes both orientations: W_gate_up
     as E4M3 codes + scales along d (the forward) and along 2I (the gate/up
@@ -184,10 +184,11 @@ def mx_quant_bytes(shape: gen.Shape, nmb: int, rows_max: int, kernels: dict, ste
     launch), dy in both block directions as bf16 values and x along the rows
     as bf16 values (two column launches).  The activation launches read the
     token rows through the row -> token map: each token row once, each
-    dispatched row written."""
+    routed row written (algorithmic bytes: the padding rows the kernels also
+    write, up to the plan's padded total, are not counted)."""
     E, d, I = shape.E, shape.d, shape.I
     w_gu, w_d = E * 2 * I * d, E * d * I       # weight elements
-    act = rows_max * d                         # one micro-batch's dispatched rows
+    act = shape.T // nmb * shape.k * d         # one micro-batch's routed rows
     tok = shape.T // nmb * d                   # one micro-batch's token rows
     c8 = 1 + 1 / 32                            # E4M3 code + 1/32 scale byte
     two_d = w_gu * (2 + 2 * c8) + w_d * (2 + c8 + 2)
@@ -202,19 +203,20 @@ def mx_quant_bytes(shape: gen.Shape, nmb: int, rows_max: int, kernels: dict, ste
     return out
 
 
-def nv_quant_bytes(shape: gen.Shape, rows_max: int, kernels: dict, steps: int) -> dict:
+def nv_quant_bytes(shape: gen.Shape, kernels: dict, steps: int) -> dict:
     """Average bytes per launch of the NVFP4 quantisers in one step (one call,
     no micro-batches).  W_gate_up: one launch reads it and writes E2M1 codes
     + E4M3 scales along d and along 2I.  Row launches: W_down, x (token rows
-    through the row map, each read once), h and dG/dU (all padded rows).
-    Tensor scales: one read of W_gate_up, W_down and x, and of h and dG/dU over
-    the routed rows."""
+    through the row map, each read once), h and dG/dU, over the routed rows
+    (algorithmic bytes: the padding rows up to the plan's padded total are
+    not counted).  Tensor scales: one read of W_gate_up, W_down and x, and of
+    h and dG/dU over the routed rows."""
     E, d, I, R = shape.E, shape.d, shape.I, shape.R
     w_gu, w_d = E * 2 * I * d, E * d * I
     c4 = 0.5 + 1 / 16                          # E2M1 code + 1/16 scale byte
     two_d = w_gu * (2 + 2 * c4)
-    rows = (w_d * (2 + c4) + (shape.T * d * 2 + rows_max * d * c4)
-            + rows_max * I * (2 + c4) + rows_max * 2 * I * (2 + c4))
+    rows = (w_d * (2 + c4) + (shape.T * d * 2 + R * d * c4)
+            + R * I * (2 + c4) + R * 2 * I * (2 + c4))
     amax = 2 * (w_gu + w_d + shape.T * d + R * I + R * 2 * I)
     out = {}
     for name, total in (("nvfp4_quantize_2d", two_d), ("nvfp4_quantize", rows),
@@ -744,10 +746,9 @@ def main():
         return ("hbm", t_mem) if t_mem > t_tc else ("tensor", t_tc)
     movers = mover_bytes(shape, int(layer.layout.mb_count))
     if PRECISION == "mxfp8":
-        movers.update(mx_quant_bytes(shape, int(layer.layout.mb_count), int(layer.layout.rows_max),
-                                     kernels, prof_steps))
+        movers.update(mx_quant_bytes(shape, int(layer.layout.mb_count), kernels, prof_steps))
     if PRECISION == "nvfp4":
-        movers.update(nv_quant_bytes(shape, int(layer.layout.rows_max), kernels, prof_steps))
+        movers.update(nv_quant_bytes(shape, kernels, prof_steps))
     total_k = sum(v[1] for v in kernels.values())
     ksum = {}
     for name, (n, ms) in kernels.items():

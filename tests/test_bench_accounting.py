@@ -77,14 +77,16 @@ def test_router_wgrad_reduce_folds_into_the_router_gradient():
 
 def test_mx_quantiser_bytes_average_over_launches():
     s = gen.workload_shape("mxfp8")
-    nmb, rows_max = 8, 32640
+    nmb = 8
     # per step: one two-orientation launch per weight; per micro-batch the x
-    # rows (codes), and column launches for dy (both directions) and for x
+    # rows (codes), and column launches for dy (both directions) and for x;
+    # the activation bytes count the routed rows (2048 tokens x top-8 per
+    # micro-batch), not the padding rows
     kernels = {"mx_quant_2d": (2 * 20, 1.0), "mx_quant_cols": (16 * 20, 1.0),
                "mx_quant_rows": (8 * 20, 1.0)}
-    got = bench.mx_quant_bytes(s, nmb, rows_max, kernels, steps=20)
+    got = bench.mx_quant_bytes(s, nmb, kernels, steps=20)
     w_gu, w_d = s.E * 2 * s.I * s.d, s.E * s.I * s.d
-    act, tok = rows_max * s.d, s.T // nmb * s.d
+    act, tok = 2048 * 8 * s.d, s.T // nmb * s.d
     c8 = 1 + 1 / 32
     assert got["mx_quant_2d"] * 2 == pytest.approx(
         2 * w_gu + 2 * c8 * w_gu + 2 * w_d + c8 * w_d + 2 * w_d)
@@ -95,15 +97,16 @@ def test_mx_quantiser_bytes_average_over_launches():
 
 def test_nv_quantiser_bytes_average_over_launches():
     s = gen.workload_shape("nvfp4")
-    rows_max = 150016
     kernels = {"nvfp4_quantize_2d": (20, 1.0), "nvfp4_quantize": (80, 1.0),
                "nvfp4_amax": (100, 1.0)}
-    got = bench.nv_quant_bytes(s, rows_max, kernels, steps=20)
+    got = bench.nv_quant_bytes(s, kernels, steps=20)
     w_gu, w_d = s.E * 2 * s.I * s.d, s.E * s.I * s.d
     c4 = 0.5 + 1 / 16
     assert got["nvfp4_quantize_2d"] == pytest.approx(w_gu * 2 + 2 * c4 * w_gu)
-    # codes are a quarter of the bf16 bytes plus a 16th for the scales
-    assert got["nvfp4_quantize"] * 4 > (w_d + s.T * s.d) * 2
+    # four row launches: W_down, then x, h and dG/dU over the routed rows
+    assert got["nvfp4_quantize"] * 4 == pytest.approx(
+        w_d * (2 + c4) + s.T * s.d * 2 + s.R * s.d * c4 + s.R * s.I * (2 + c4)
+        + s.R * 2 * s.I * (2 + c4))
     assert got["nvfp4_amax"] * 5 == pytest.approx(
         2 * (w_gu + w_d + s.T * s.d + s.R * s.I + s.R * 2 * s.I))
 
