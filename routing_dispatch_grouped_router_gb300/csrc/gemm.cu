@@ -116,6 +116,10 @@ struct GemmArgs {
   // rounded up to a 64-row block instead of its 128-padded rows: the padding
   // rows of every weight-gradient operand are zero, so the skipped products
   // are exact zeros and the sums do not change.
+  // MGROUP: the same offsets, or NULL.  Given, the rows of expert e past its
+  // real rows rounded up to 64 (the plan's token -2 rows, which only whole-
+  // tile GEMMs read, for output rows nothing reads) get no epilogue: no
+  // operand loads, no stores, whole 32-row quarters.
   const int* coff;
   int* status;
 };
@@ -1425,8 +1429,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Tile tl = tile_at(t, &valid);
       const int acc = C::NACC == 2 ? (it & 1) : 0;
       const uint32_t acc_par = static_cast<uint32_t>(C::NACC == 2 ? ((it >> 1) & 1) : (it & 1));
+      // this warp's 32 rows: none of them read by anything (args.coff)
+      bool unread = false;
+      if (SCHED == SCHED_MGROUP && args.coff != nullptr && valid) {
+        const int used = (__ldg(args.coff + tl.e + 1) - __ldg(args.coff + tl.e) + 63) / 64 * 64;
+        unread = tl.row0 + q * 32 - __ldg(args.poff + tl.e) >= used;
+      }
+      const bool work = valid && !unread;
       // the tile's first g, u chunk does not depend on the accumulator
-      if (kGuTma && valid)
+      if (kGuTma && work)
         gu_issue<BN, kDbuf ? 2 : 1>(args, tl, q, lane, half, 0, stage_buf, wbar, gu_chunks,
                                     &tmC);
       if (!wait(&tfull[acc], acc_par)) {
@@ -1440,19 +1451,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (kEarlyRelease) {
         // the accumulator to registers, freed at once; the stores follow
         float accr[128];
-        if (valid) acc_to_regs<EPI>(taddr, half, accr);
+        if (work) acc_to_regs<EPI>(taddr, half, accr);
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * acc);
-        if (valid)
+        if (work)
           epilogue_regs<EPI, SPLIT, kDbuf>(args, tl, accr, q, lane, half, stage_buf, nst, &tmC);
         continue;
       }
       if constexpr (kGuTma) {
-        if (valid)
+        if (work)
           gu_chunks = swiglu_bwd_tma<BN, kDbuf>(args, tl, taddr, q, lane, half, stage_buf, wbar,
                                          gu_chunks, &tmC, &om, vabort);
-      } else if (valid) {
+      } else if (work) {
         epilogue_tile<BN, SCHED, EPI, kDbuf, SPLIT>(args, tl, taddr, q, lane, half, stage_buf,
                                                     nst, &tmC);
       }
@@ -1651,6 +1662,7 @@ cudaError_t gemm_fwd_gate_up(const Dims& D, const void* X_perm, const void* w_ga
   a.I = (int)D.I;
   a.mtile_prefix = mtile_prefix;
   a.poff = poff;
+  a.coff = D.coff;  // unread padding rows: no epilogue
   a.out = GU;
   a.out2 = H;
   a.mx = D.mx ? 1 : 0;
@@ -1697,6 +1709,7 @@ cudaError_t gemm_fwd_gate_up_mx(const Dims& D, const uint8_t* x_codes, const uin
   a.I = (int)D.I;
   a.mtile_prefix = mtile_prefix;
   a.poff = poff;
+  a.coff = D.coff;  // unread padding rows: no epilogue
   a.out = GU;
   a.sa = x_scales;
   a.sb = wgu_scales;
@@ -1740,6 +1753,7 @@ static cudaError_t grouped_mx_f32(const char* name, const Dims& D, int64_t K,
   a.b_group_rows = (int)D.d;
   a.mtile_prefix = mtile_prefix;
   a.poff = poff;
+  a.coff = D.coff;  // unread padding rows: no epilogue
   a.out = O;  // fp32 [rows_max, d]
   a.ldo = D.d;
   a.sa = a_scales;
@@ -1802,6 +1816,7 @@ cudaError_t gemm_fwd_gate_up_nv(const Dims& D, const uint8_t* x_codes, const uin
   a.I = (int)D.I;
   a.mtile_prefix = mtile_prefix;
   a.poff = poff;
+  a.coff = D.coff;  // unread padding rows: no epilogue
   a.out = GU;
   a.out2 = H;
   a.ks = (int)(D.d / 64);
@@ -1841,6 +1856,7 @@ static cudaError_t grouped_nv_f32(const char* name, const Dims& D, int64_t K,
   a.b_group_rows = (int)D.d;
   a.mtile_prefix = mtile_prefix;
   a.poff = poff;
+  a.coff = D.coff;  // unread padding rows: no epilogue
   a.out = O;
   a.ldo = D.d;
   a.ks = (int)(K / 64);
@@ -1901,6 +1917,7 @@ cudaError_t gemm_fwd_down(const Dims& D, const void* H, const void* w_down,
   a.b_group_rows = (int)D.d;
   a.mtile_prefix = mtile_prefix;
   a.poff = poff;
+  a.coff = D.coff;  // unread padding rows: no epilogue
   a.out = O;  // fp32 [rows_max, d]
   a.ldo = D.d;
   const int mt = max_mtiles(D) * a.n_tiles;
@@ -1944,6 +1961,7 @@ cudaError_t gemm_bwd_down_dgrad(const Dims& D, const void* dY_perm, const void* 
   a.I = (int)D.I;
   a.mtile_prefix = mtile_prefix;
   a.poff = poff;
+  a.coff = D.coff;  // unread padding rows: no epilogue
   a.out = dGU_hi;
   a.out2 = P_hi;
   a.out3 = dGU_lo;
@@ -1987,6 +2005,7 @@ cudaError_t gemm_bwd_gate_up_dgrad(const Dims& D, const void* dGU, const void* w
   a.b_group_rows = (int)(2 * D.I);
   a.mtile_prefix = mtile_prefix;
   a.poff = poff;
+  a.coff = D.coff;  // unread padding rows: no epilogue
   a.out = dX_perm;  // fp32 [rows_max, d]
   a.ldo = D.d;
   const int mt = max_mtiles(D) * a.n_tiles;

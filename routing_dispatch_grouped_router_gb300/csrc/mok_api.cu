@@ -490,6 +490,7 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
     o.ppos = at<int32_t>(saved, L.padded_pos + blk);
     o.ptok = at<int32_t>(saved, L.padded_token + blk);
     o.row_w = at<float>(saved, L.row_weight + blk);
+    D.coff = o.offsets;  // this micro-batch's grouped GEMMs skip its unread rows
     // top-k selection, histogram, scans and stable placement: one persistent
     // kernel walking the front-end schedule table
     MOK_CUDA(launch_route_plan(D, logits, router_bias, topk_idx, topk_w,
@@ -512,8 +513,9 @@ mok_status mok_moe_forward(const mok_moe_desc* desc, const void* x, const void* 
                                      static_cast<int>(D.T), st, o.padded_offsets + D.E));
       MOK_CUDA(gemm_fwd_gate_up_nv(D, nxq_c, nxq_s, nvg + 0, nwgu_c, nwgu_s, nvw + 0,
                                    o.mtile_prefix, o.padded_offsets, gu, h, status, st));
+      // (over the routed rows: the padding rows nothing reads hold no h)
       MOK_CUDA(launch_nv_tensor_scale(h, D.rows_max * D.I, nvg + 1, st,
-                                      o.padded_offsets + D.E, D.I));
+                                      o.padded_offsets + D.E, D.I, o.ptok));
       MOK_CUDA(launch_nv_quant_tiled(h, D.rows_max, D.I, nvg + 1, nh_c, nh_s, nullptr, 0, st,
                                      o.padded_offsets + D.E));
       MOK_CUDA(gemm_fwd_down_nv(D, nh_c, nh_s, nvg + 1, nwd_c, nwd_s, nvw + 1, o.mtile_prefix,
@@ -634,6 +636,7 @@ mok_status mok_moe_backward(const mok_moe_desc* desc, const void* dy, const void
     const int32_t* ppos = at<int32_t>(saved, L.padded_pos + blk);
     const int32_t* ptok = at<int32_t>(saved, L.padded_token + blk);
     const float* row_w = at<float>(saved, L.row_weight + blk);
+    D.coff = at<int32_t>(saved, L.offsets + blk);  // grouped GEMMs: unread rows skipped
     const void* gu = D.recompute_gu ? at<char>(workspace, B.gu) : at<char>(saved, L.gate_up + blk);
     void* x_perm = (D.mx || D.recompute_dispatch)
                        ? nullptr

@@ -39,6 +39,11 @@ struct Dims {
   bool recompute_dispatch;  // BF16: dispatched x rows not kept in saved;
                             // the backward dispatches them again
   bool pair;         // grouped GEMMs with 256-row tiles on CTA pairs (2-SM MMA)
+  // Set by the layer before the M-grouped GEMMs of a micro-batch (NULL
+  // otherwise): its plan's [E+1] real row offsets.  Rows of expert e from its
+  // real rows rounded up to 64 to its 128-padded end are read by nothing, so
+  // those GEMMs skip their epilogue there (whole 32-row quarters).
+  const int32_t* coff = nullptr;
 };
 
 // Split-K factor of the router logit GEMM: the largest power of two (up to
