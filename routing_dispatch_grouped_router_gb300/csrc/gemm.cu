@@ -131,6 +131,9 @@ struct GemmArgs {
 struct OutMaps {
   CUtensorMap dgu_hi, dgu_lo, p_hi, p_lo;
   CUtensorMap sfa, sfb;
+  // SwiGLU forward with bf16 h: h [rows, I], 32 x 32 blocks of 64-byte rows
+  // (64-byte swizzle); a zeroed map (no h, or h as MXFP8 codes) is unused
+  CUtensorMap h;
 };
 
 constexpr int kThreads = 320;
@@ -574,10 +577,37 @@ __device__ __forceinline__ void stage_and_store_bf16_t(uint8_t* buf, const CUten
   if (lane == 0) tma_out_2d(tmC, buf, x, y, false, evict_first);
 }
 
+// A warp's 32 rows x 32 values rounded to bf16 (nearest even), lane i
+// holding row i: staging row i is 64 bytes in the 64-byte-swizzled layout
+// (16-byte chunk j of row r at chunk j ^ ((r >> 1) & 3)), stored with one TMA
+// store at (x, y): whole 32-byte sectors instead of one lane's 16-byte
+// pieces of 32 rows per store instruction.
+__device__ __forceinline__ void stage_and_store_bf16_rows32(uint8_t* buf, const CUtensorMap* tm,
+                                                            const float (&v)[32], int lane,
+                                                            int x, int y) {
+  if (lane == 0) bulk_wait_read<0>();  // earlier stores have read the staging
+  __syncwarp();
+  uint8_t* row = buf + lane * 64;
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint4*>(row + ((j ^ sw) << 4)) =
+        make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                   pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                   pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tm, buf, x, y);
+    bulk_commit();
+  }
+}
+
 template <int BN, int SCHED, int EPI, bool DBUF, int SPLIT>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl, uint32_t taddr,
                                               int q, int lane, int half, uint8_t* stage_buf,
-                                              uint32_t& nst, const CUtensorMap* tmC) {
+                                              uint32_t& nst, const CUtensorMap* tmC,
+                                              const CUtensorMap* tmH) {
   constexpr int HALF_COLS = BN / 2;
   const int row_in_tile = q * 32 + lane;
   const bool zero_k = (tl.num_kb == 0);
@@ -718,7 +748,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
     const int I = a.I;
     const int n0 = tl.n_tile * 128 + half * 64;
     const int y = tl.row0 + q * 32;
-    __nv_bfloat16* h = static_cast<__nv_bfloat16*>(a.out2) + r * (long long)I;
 #pragma unroll 1
     for (int c = 0; c < 64; c += 32) {
       if (n0 + c >= I) break;  // a ragged last tile (I a multiple of 32)
@@ -749,7 +778,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& a, const Tile& tl,
           a.h_scales[mx_tiled_off(r, (n0 + c) / 32, I / 128)] = static_cast<uint8_t>(sbyte);
         } else {
           if (a.mx) mx_fake32(hv);  // one MX block: 32 consecutive columns of a row
-          store_bf16x32(h + n0 + c, hv);
+          stage_and_store_bf16_rows32(stage_buf, tmH, hv, lane, n0 + c, y);
         }
       }
       if (a.store_c) {
@@ -792,7 +821,7 @@ template <int EPI, int SPLIT, bool DBUF>
 __device__ __forceinline__ void epilogue_regs(const GemmArgs& a, const Tile& tl,
                                               float (&acc)[128], int q, int lane, int half,
                                               uint8_t* stage_buf, uint32_t& nst,
-                                              const CUtensorMap* tmC) {
+                                              const CUtensorMap* tmC, const CUtensorMap* tmH) {
   // NVFP4: the product of the operands' tensor scales (the block scales were
   // applied by the tensor cores)
   const float alpha = SPLIT == SPLIT_NV ? __ldg(a.ga) * __ldg(a.gb) : 1.0f;
@@ -847,8 +876,7 @@ __device__ __forceinline__ void epilogue_regs(const GemmArgs& a, const Tile& tl,
           a.h_scales[mx_tiled_off(r, (n0 + 32 * c) / 32, I / 128)] =
               static_cast<uint8_t>(sbyte);
         } else {
-          store_bf16x32(static_cast<__nv_bfloat16*>(a.out2) + r * (long long)I + n0 + 32 * c,
-                        hv);
+          stage_and_store_bf16_rows32(stage_buf, tmH, hv, lane, n0 + 32 * c, y);
         }
       }
     }
@@ -1096,6 +1124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&om.sfa);
       tma_prefetch_desc(&om.sfb);
     }
+    if (EPI == EPI_SWIGLU_FWD && SPLIT != SPLIT_MX) tma_prefetch_desc(&om.h);
     if (EPI == EPI_SWIGLU_BWD) {
       tma_prefetch_desc(&om.dgu_hi);
       tma_prefetch_desc(&om.dgu_lo);
@@ -1456,7 +1485,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * acc);
         if (work)
-          epilogue_regs<EPI, SPLIT, kDbuf>(args, tl, accr, q, lane, half, stage_buf, nst, &tmC);
+          epilogue_regs<EPI, SPLIT, kDbuf>(args, tl, accr, q, lane, half, stage_buf, nst, &tmC,
+                                           &om.h);
         continue;
       }
       if constexpr (kGuTma) {
@@ -1465,7 +1495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          gu_chunks, &tmC, &om, vabort);
       } else if (work) {
         epilogue_tile<BN, SCHED, EPI, kDbuf, SPLIT>(args, tl, taddr, q, lane, half, stage_buf,
-                                                    nst, &tmC);
+                                                    nst, &tmC, &om.h);
       }
       tc_fence_before_sync();
       __syncwarp();
@@ -1552,7 +1582,8 @@ static bool make_out_map(CUtensorMap* m, const void* base, uint64_t cols, uint64
 static bool make_out_map_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
   return make_map_t(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, cols, rows, cols, 64, 32);
 }
-// bf16 C^T: 32 x 32 blocks (64-byte rows, 64-byte swizzle)
+// bf16 [rows, cols] stored in 32 x 32 blocks (64-byte rows, 64-byte swizzle):
+// C^T blocks of the transposed weight gradients, and h
 static bool make_out_map_bf16_t(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
   return make_map_t(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, cols, rows, cols, 32, 32,
                     CU_TENSOR_MAP_SWIZZLE_64B);
@@ -1666,11 +1697,14 @@ cudaError_t gemm_fwd_gate_up(const Dims& D, const void* X_perm, const void* w_ga
   a.out = GU;
   a.out2 = H;
   a.mx = D.mx ? 1 : 0;
+  OutMaps om;  // h through TMA stores of 32 x 32 blocks
+  memset(&om, 0, sizeof(om));
+  if (H && !make_out_map_bf16_t(&om.h, H, D.I, D.rows_max)) return cudaErrorInvalidValue;
   if (D.pair)
     return launch<256, false, false, SCHED_MGROUP, EPI_SWIGLU_FWD, SPLIT_NONE, true>(
-        "fwd_gate_up_swiglu", ta, tb, tc, a, max_mpairs(D) * a.n_tiles, st);
+        "fwd_gate_up_swiglu", ta, tb, tc, a, max_mpairs(D) * a.n_tiles, st, nullptr, &om);
   return launch<256, false, false, SCHED_MGROUP, EPI_SWIGLU_FWD>(
-      "fwd_gate_up_swiglu", ta, tb, tc, a, max_mtiles(D) * a.n_tiles, st);
+      "fwd_gate_up_swiglu", ta, tb, tc, a, max_mtiles(D) * a.n_tiles, st, nullptr, &om);
 }
 
 // The tiled scales of a [rows, K] MXFP8 operand as a TMA map: 512-byte blocks
@@ -1825,7 +1859,8 @@ cudaError_t gemm_fwd_gate_up_nv(const Dims& D, const uint8_t* x_codes, const uin
   OutMaps om;
   memset(&om, 0, sizeof(om));
   if (!make_nv_sf_map(&om.sfa, x_scales, D.rows_max, D.d) ||
-      !make_nv_sf_map(&om.sfb, wgu_scales, D.E * 2 * D.I, D.d))
+      !make_nv_sf_map(&om.sfb, wgu_scales, D.E * 2 * D.I, D.d) ||
+      !make_out_map_bf16_t(&om.h, H, D.I, D.rows_max))
     return cudaErrorInvalidValue;
   return launch<256, false, false, SCHED_MGROUP, EPI_SWIGLU_FWD, SPLIT_NV, true>(
       "fwd_gate_up_swiglu", ta, tb, tc, a, max_mpairs(D) * a.n_tiles, st, nullptr, &om);
