@@ -147,22 +147,22 @@ def gemm_bytes(shape: gen.Shape, micro_batches: int = 1, mx: bool = False,
 # (kernels as of the commit each file names); a kernel changed since its
 # capture has no entry.
 NCU_TRAFFIC_FINE = {
-    "fwd_gate_up_swiglu": 693.654784e6 + 313.342e6,
-    "fwd_down": 343.464192e6 + 241.090e6,
-    "bwd_down_dgrad_swiglu": 782.689280e6 + 384.740e6,
-    "bwd_down_wgrad": 285.004032e6 + 479.528e6,
-    "bwd_gate_up_dgrad": 692.472832e6 + 257.977e6,
-    "bwd_gate_up_wgrad": 427.247872e6 + 1013.580e6,
+    "fwd_gate_up_swiglu": 689.183232e6 + 312.882e6,
+    "fwd_down": 343.459072e6 + 240.195e6,
+    "bwd_down_dgrad_swiglu": 781.232640e6 + 383.957e6,
+    "bwd_down_wgrad": 284.840960e6 + 479.524e6,
+    "bwd_gate_up_dgrad": 688.372224e6 + 257.197e6,
+    "bwd_gate_up_wgrad": 427.129344e6 + 1013.322e6,
 }
 # The large workload's GEMMs from a capture of its slice (1/16 of its experts and
 # tokens, the same widths and rows per expert): per-expert work, so 16x the bytes.
 NCU_TRAFFIC_LARGE = {k: 16 * v for k, v in {
-    "fwd_gate_up_swiglu": 1.510968e9 + 0.078380e9,
-    "fwd_down": 0.732572e9 + 0.112679e9,
-    "bwd_down_dgrad_swiglu": 0.908462e9 + 0.092356e9,
-    "bwd_down_wgrad": 0.103906e9 + 1.347370e9,
-    "bwd_gate_up_dgrad": 1.474297e9 + 0.122984e9,
-    "bwd_gate_up_wgrad": 0.141863e9 + 2.757091e9,
+    "fwd_gate_up_swiglu": 1.511265e9 + 0.078212e9,
+    "fwd_down": 0.733215e9 + 0.112134e9,
+    "bwd_down_dgrad_swiglu": 0.908464e9 + 0.092401e9,
+    "bwd_down_wgrad": 0.103909e9 + 1.347131e9,
+    "bwd_gate_up_dgrad": 1.474287e9 + 0.122661e9,
+    "bwd_gate_up_wgrad": 0.142005e9 + 2.757084e9,
 }.items()}
 NCU_TRAFFIC = {"fine": (NCU_TRAFFIC_FINE, "profiles/grouped_gemms_fine.txt"),
                "large": (NCU_TRAFFIC_LARGE,
