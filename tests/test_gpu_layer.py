@@ -578,3 +578,39 @@ def test_ragged_widths_in_every_layer_mode(mode):
     gpu = _gpu.run_gpu(shape, inp, **kw)
     assert gpu["status"] == 0
     _gpu.full_parity(shape, inp, gpu)
+
+
+# ------------------------------------------- padding rows that nothing reads ---
+
+@pytest.mark.parametrize("T,mb,ring", [(480, 0, 0), (640, 160, 1)])
+def test_unread_padding_rows_reach_no_output(T, mb, ring):
+    """Rows of an expert's segment past its real rows rounded up to 64 (the
+    plan's token -2 rows) are read only by whole-tile GEMMs, for output rows
+    that nothing reads: the dispatch leaves them unwritten and the grouped
+    GEMMs skip their epilogue there.  With the dispatched x rows and the saved
+    fp32 g, u filled with NaN before the call instead of zeros, every output is
+    bitwise the same.  (About 160 and 53 rows per expert: 64 such rows each.)"""
+    shape = gen.Shape(T=T, d=256, E=6, I=256, k=2)
+    inp = gen.make_inputs(shape, seed=7)
+    outs = []
+    for poison in (False, True):
+        layer = api.MoELayer(shape.T, shape.d, shape.E, shape.I, shape.k, mb_tokens=mb,
+                             ring_slots=ring)
+        L = layer.layout
+        nmb = int(L.mb_count)
+        if poison:
+            # only float row arrays: NaN bytes (0xFF) in bf16 and fp32
+            rows = int(L.rows_max)
+            for s in range(max(int(L.ring_slots), 1)):
+                off = int(L.x_perm) + s * int(L.ring_slot_bytes)
+                layer.saved[off:off + rows * shape.d * 2].fill_(0xFF)
+            for i in range(nmb):
+                off = int(L.gate_up) + i * int(L.mb_stride)
+                layer.saved[off:off + rows * 2 * shape.I * 4].fill_(0xFF)
+        gpu = _gpu.run_gpu(shape, inp, layer=layer)
+        assert gpu["status"] == 0
+        counts = np.concatenate(gpu["mb_counts"])
+        assert ((counts % 128 >= 1) & (counts % 128 <= 64)).any()  # such rows exist
+        outs.append([gpu[n].clone() for n in ("y", "dx", "dw_router", "dw_gate_up", "dw_down")])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
