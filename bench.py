@@ -72,6 +72,18 @@ def peak_ratio(precision: str, gemm: str) -> float:
     return 1.0
 
 
+def gemm_peak_fraction(flops: dict, kernels: dict, names, bf16_tflops: float,
+                       precision: str) -> float:
+    """Fraction of the tensor peak the GEMMs `names` reach together: the time
+    their algorithmic FLOPs take at each one's own operands' peak (FP8 and FP4
+    GEMMs at the nominal 2x and 6x of the bf16 one) over their measured time.
+    `kernels[name]` = (launches, total ms), `flops[name]` = FLOP per launch."""
+    ms = sum(kernels[n][1] for n in names)
+    at_peak = sum(flops[n] * kernels[n][0] / (bf16_tflops * 1e12 * peak_ratio(precision, n))
+                  for n in names) * 1e3
+    return at_peak / ms if ms else 0.0
+
+
 # Weight-gradient GEMMs: with micro-batches the layer defers them and launches
 # each once per step over every micro-batch's rows
 DEFERRED_WGRADS = ("bwd_down_wgrad", "bwd_gate_up_wgrad")
@@ -804,12 +816,7 @@ def main():
     gg_ms = sum(kernels[n][1] for n in gg)
     gg_fl = sum(flops[n] * kernels[n][0] for n in gg)
     gg_tflops = gg_fl / (gg_ms / 1e3) / 1e12 if gg_ms else 0.0
-    # fraction of the tensor peak: each GEMM's FLOPs at its own operands' peak
-    # (FP8 and FP4 GEMMs at the nominal 2x and 6x of the measured bf16 one),
-    # over the GEMMs' measured time
-    gg_peak_ms = sum(flops[n] * kernels[n][0] / (peaks["bf16_sustained"] * 1e12
-                                                 * peak_ratio(PRECISION, n)) * 1e3 for n in gg)
-    gg_frac = gg_peak_ms / gg_ms if gg_ms else 0.0
+    gg_frac = gemm_peak_fraction(flops, kernels, gg, peaks["bf16_sustained"], PRECISION)
     movers_perf = {}
     wbytes = mover_write_bytes(shape, int(layer.layout.mb_count))
     for n, b in movers.items():

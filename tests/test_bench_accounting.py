@@ -212,3 +212,16 @@ def test_low_precision_peaks_and_bytes():
     assert nv["fwd_down"][0] == R * I * q4 + E * d * I * q4 + R * d * 4
     assert nv["bwd_gate_up_dgrad"][0] == R * 2 * I * q4 + E * 2 * I * d * q4 + R * d * 4
     assert nv["bwd_down_dgrad_swiglu"] == bf["bwd_down_dgrad_swiglu"]
+
+
+def test_gemm_peak_fraction_takes_each_gemm_at_its_own_peak():
+    # two GEMMs of 1 TFLOP each, one launch, 1 ms each, bf16 peak 1000 TFLOP/s
+    flops = {"fwd_gate_up_swiglu": 1e12, "bwd_gate_up_wgrad": 1e12}
+    kernels = {"fwd_gate_up_swiglu": (1, 1.0), "bwd_gate_up_wgrad": (1, 1.0)}
+    names = list(flops)
+    # bf16: both at the bf16 peak -> 1 ms each at peak, 2 ms measured
+    assert bench.gemm_peak_fraction(flops, kernels, names, 1000.0, "bf16") == pytest.approx(1.0)
+    # NVFP4: the forward GEMM's peak is 6x, so its FLOPs take 1/6 ms at peak
+    got = bench.gemm_peak_fraction(flops, kernels, names, 1000.0, "nvfp4")
+    assert got == pytest.approx((1 / 6 + 1) / 2)
+    assert bench.gemm_peak_fraction(flops, {n: (1, 0.0) for n in names}, [], 1000.0, "bf16") == 0.0
