@@ -170,7 +170,8 @@ constexpr int kSwigluBwdDirectMinD = 6144;
 // gate/up weight gradient 366 -> 419 us with it).  Off for the M-grouped
 // GEMMs: it costs the 256-wide pair kernels their sixth operand stage, and
 // measured slower there (fwd_gate_up 245 -> 260 us, fwd_down 132 -> 151 us on
-// the fine workload).
+// the fine workload), as it did for the block-scaled pairs' register epilogues
+// (their fifth stage: NVFP4 fwd_down 713 -> 805 us).
 template <int EPI, int SPLIT, int SCHED, bool DB>
 constexpr int staging_bytes() {
   return EPI == EPI_SWIGLU_BWD ? (DB ? kSwigluBwdStagingDirect : kSwigluBwdStaging)
